@@ -1,0 +1,181 @@
+"""CPU oracle of the verification sampler -- TEST INFRASTRUCTURE ONLY.
+
+Python marshalling for ``sv_oracle.c`` (a plain single-threaded C restatement of the
+verification step; see its header for the pages it follows and the readings it takes).
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import this package. The library's product path never uses it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sv_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsvoracle.so")
+_lib = None
+
+RACE_NONE, RACE_RESIDUAL, RACE_EXCLUDE, RACE_BONUS, RACE_FALLBACK = range(5)
+EBATCH = 1
+
+# Strict IEEE binary32: no contraction of a*b+c into fma (only the explicit fmaf calls
+# fuse), no fast-math reassociation.
+CFLAGS = ["-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile sv_oracle.c into libsvoracle.so next to it (atomic replace)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    try:
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True, capture_output=True,
+                       text=True)
+        os.replace(tmp, _LIB_PATH)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        L = ctypes.CDLL(build())
+        vp, u32, u64, i32, f32 = (ctypes.c_void_p, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int,
+                                  ctypes.c_float)
+        L.spec_verify_ref_philox.argtypes = [vp, vp, vp]
+        L.spec_verify_ref_philox.restype = None
+        L.spec_verify_ref_uniform.argtypes = [u64, u32, u32, u32, u32, i32]
+        L.spec_verify_ref_uniform.restype = f32
+        L.spec_verify_ref_uniform_from_word.argtypes = [u32]
+        L.spec_verify_ref_uniform_from_word.restype = f32
+        L.spec_verify_ref_exp.argtypes = [f32]
+        L.spec_verify_ref_exp.restype = f32
+        L.spec_verify_ref_log.argtypes = [f32]
+        L.spec_verify_ref_log.restype = f32
+        L.spec_verify_ref_run.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32,
+                                          vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.spec_verify_ref_run.restype = i32
+        L.spec_verify_ref_residual_row.argtypes = [vp, i32, i32, f32, vp, vp, vp, vp, vp]
+        L.spec_verify_ref_residual_row.restype = None
+        for f in ("spec_verify_ref_exp_n", "spec_verify_ref_log_n"):
+            getattr(L, f).argtypes = [vp, vp, ctypes.c_int64]
+            getattr(L, f).restype = None
+        L.spec_verify_ref_race_uniforms.argtypes = [u64, u32, u32, i32, vp]
+        L.spec_verify_ref_race_uniforms.restype = None
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def philox(ctr, key) -> np.ndarray:
+    c = np.ascontiguousarray(ctr, dtype=np.uint32)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().spec_verify_ref_philox(_p(c), _p(k), _p(out))
+    return out
+
+
+def uniform(seed: int, c0: int, c1: int, c2: int, c3: int, word: int) -> float:
+    return lib().spec_verify_ref_uniform(seed, c0, c1, c2, c3, word)
+
+
+def uniform_from_word(w: int) -> float:
+    return lib().spec_verify_ref_uniform_from_word(w)
+
+
+def exp32(x: float) -> float:
+    return lib().spec_verify_ref_exp(x)
+
+
+def log32(x: float) -> float:
+    return lib().spec_verify_ref_log(x)
+
+
+def exp32_n(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib().spec_verify_ref_exp_n(_p(x), _p(out), x.size)
+    return out
+
+
+def log32_n(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(x)
+    lib().spec_verify_ref_log_n(_p(x), _p(out), x.size)
+    return out
+
+
+def race_uniforms(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
+    out = np.empty(n, dtype=np.float32)
+    lib().spec_verify_ref_race_uniforms(seed, j, ireq, n, _p(out))
+    return out
+
+
+def residual_row(logits_row: np.ndarray, bf16: bool, invT: float, q: np.ndarray):
+    """t_v = exp(x_v - m), rr_v = fma(-S, q_v, t_v), m, S for one row, as the race uses them."""
+    V = logits_row.shape[-1]
+    row = np.ascontiguousarray(logits_row)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    t = np.empty(V, dtype=np.float32)
+    rr = np.empty(V, dtype=np.float32)
+    m = ctypes.c_float()
+    S = ctypes.c_float()
+    lib().spec_verify_ref_residual_row(_p(row), int(bf16), V, invT, _p(q), _p(t), _p(rr),
+                                       ctypes.byref(m), ctypes.byref(S))
+    return t, rr, m.value, S.value
+
+
+def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_override=None,
+        seed: int | None = None) -> dict:
+    """Run the oracle on a ``workloads.Batch`` (or any object with the same fields).
+
+    Returns sampled, num_sampled, num_rejected, the per-row stats (row_max, row_sumexp,
+    row_argmax), the per-position acceptance margins, the per-request race gap and kind,
+    j* per request and the status code.
+    """
+    cu = np.ascontiguousarray(batch.cu_num_draft, dtype=np.int32)
+    n = cu.shape[0] - 1
+    nd = int(cu[-1])
+    R = nd + n
+    kmax = batch.max_spec_len if max_spec_len is None else max_spec_len
+    V = int(batch.vocab_size)
+    logits = np.ascontiguousarray(batch.logits)
+    bf16 = batch.logits_dtype == "bf16"
+    ids = np.ascontiguousarray(batch.draft_ids, dtype=np.int32)
+    q = None if batch.draft_probs is None else np.ascontiguousarray(batch.draft_probs, dtype=np.float32)
+    T = np.ascontiguousarray(batch.temperature, dtype=np.float32)
+    g = np.ascontiguousarray(batch.is_greedy, dtype=np.uint8)
+    out = dict(
+        sampled=np.empty((n, kmax + 1), dtype=np.int32),
+        num_sampled=np.empty(n, dtype=np.int32),
+        num_rejected=np.empty(n, dtype=np.int32),
+        row_max=np.empty(R, dtype=np.float32),
+        row_sumexp=np.empty(R, dtype=np.float32),
+        row_argmax=np.empty(R, dtype=np.int32),
+        accept_margin=np.empty(max(nd, 1), dtype=np.float64),
+        race_gap=np.empty(max(n, 1), dtype=np.float64),
+        race_kind=np.empty(max(n, 1), dtype=np.int32),
+        jstar=np.empty(max(n, 1), dtype=np.int32),
+    )
+    uo = None if u_override is None else np.ascontiguousarray(u_override, dtype=np.float32)
+    s = batch.seed if seed is None else seed
+    rc = lib().spec_verify_ref_run(
+        _p(logits), int(bf16), V, _p(ids), _p(q), _p(cu), _p(T), _p(g), s, req_index_base, n, nd,
+        kmax, _p(out["sampled"]), _p(out["num_sampled"]), _p(out["num_rejected"]), _p(out["row_max"]),
+        _p(out["row_sumexp"]), _p(out["row_argmax"]), _p(out["accept_margin"]), _p(out["race_gap"]),
+        _p(out["race_kind"]), _p(out["jstar"]), _p(uo))
+    out["accept_margin"] = out["accept_margin"][:nd]
+    for k in ("race_gap", "race_kind", "jstar"):
+        out[k] = out[k][:n]
+    out["status"] = rc
+    return out

@@ -1,0 +1,451 @@
+/*
+ * ORACLE FOR THE SPECULATIVE-DECODING VERIFICATION SAMPLER -- TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, single-threaded CPU restatement of what the verification step computes,
+ * written from the pages' description. Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg use it; the library's product path never links, loads or calls it, and
+ * it shares no code with the CUDA implementation.
+ *
+ * Pages cited (title, section):
+ *   [MTP-eagle]     "【vllm】DeepSeekMTP、eagle" (benyoew.github.io): the sample() call tree,
+ *                   _rejection_sample_kernel, get_num_sampled_and_rejected.
+ *   [spec-notes]    "vLLM 投机解码（Eagle / MTP）实现与运行流程" (llx-08 notes): residual
+ *                   distribution Q&A, bonus token and NO_DRAFT_PROBS Q&A, 4-token examples,
+ *                   section 8 (rejection sampling) 8.2 / 8.3, section 9.2.
+ *   [spec-in-vllm]  "speculative decoding in vLLM" (jiangwei.me): section 7.0 (5-token
+ *                   example), 7.0.1 (greedy), 7.0.2 (bonus), 7.3 (Gumbel argmax), 7.4 (kernels).
+ *   [mini-sglang]   "mini-sglang" (blog.thunguo.space): "how tokens are sampled" (greedy rule).
+ *
+ * Readings where the pages leave a step open (each one is also listed in the design doc):
+ *   - p = softmax(logits / T) with x_v = logit_v * (1/T) in binary32; T <= 0 (or a set greedy
+ *     flag) means greedy verification.
+ *   - Acceptance test p(d)/q(d) >= u with u in (0,1); q(d) = 1 without draft probabilities.
+ *   - Every random draw is keyed: Philox4x32-10, key = seed, counter = (v>>2, j, request, tag),
+ *     word v&3; tag 0 = acceptance uniform (v = 0), tag 1 = race exponentials.
+ *   - Sampling from a distribution proportional to w_v is the exponential race
+ *     argmax_v (log w_v - log E_v), E_v = -log U_v, lowest index on equal keys.
+ *   - The residual weight is rr_v = fma(-S, q_v, t_v) with t_v = exp(x_v - m), i.e.
+ *     S * (p_v - q_v) rounded once; the constant log S is left out of the keys.
+ *   - exp and log inside every decision are the binary32 functions below (Cody-Waite
+ *     reduction + Taylor polynomial; reduction to [sqrt(1/2), sqrt(2)) + atanh series), so
+ *     that any implementation that follows the same steps gets the same bits.
+ *   - S, the sum of exponentials, is accumulated in double in index order.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define REF_TAG_ACCEPT 0u
+#define REF_TAG_RACE 1u
+
+/* ------------------------------------------------------------------------------------ */
+/* Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+ * SC'11. Each round multiplies counter words 0 and 2 by the round multipliers, and the
+ * key is bumped by the Weyl constants (golden ratio, sqrt(3)-1) between rounds.         */
+/* ------------------------------------------------------------------------------------ */
+void spec_verify_ref_philox(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    const uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t p0 = (uint64_t)M0 * c0;
+        uint64_t p1 = (uint64_t)M1 * c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n1 = lo1;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        uint32_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+        k0 += W0;
+        k1 += W1;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Uniform in (0,1): the top 23 bits of a Philox word w, centred in their cell,
+ * U = (floor(w / 2^9) + 1/2) / 2^23. Every step is exact in binary32, U is never 0 or 1. */
+float spec_verify_ref_uniform_from_word(uint32_t w)
+{
+    return ((float)(w >> 9) + 0.5f) * 0x1p-23f;
+}
+
+float spec_verify_ref_uniform(uint64_t seed, uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                              int word)
+{
+    uint32_t ctr[4] = {c0, c1, c2, c3};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    spec_verify_ref_philox(ctr, key, out);
+    return spec_verify_ref_uniform_from_word(out[word & 3]);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* binary32 exp and log used inside every decision.                                      */
+/* ------------------------------------------------------------------------------------ */
+static inline float bits_f(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+static inline uint32_t f_bits(float f) { uint32_t b; memcpy(&b, &f, 4); return b; }
+
+#define REF_LOG2E 0x1.715476p+0f   /* log2(e) rounded to binary32 */
+#define REF_LN2_HI 0x1.62e430p-1f  /* ln 2 rounded to binary32 */
+#define REF_LN2_LO -0x1.05c610p-29f /* ln 2 - REF_LN2_HI, rounded to binary32 */
+
+/* exp(d) for d <= 88, defined as 0 below -87 (where exp(d) < 1.7e-38).
+ * Cody & Waite (1980) reduction d = k ln2 + r, |r| <= ln2/2, with k = round(d log2 e) taken
+ * by adding 1.5*2^23 in one fused multiply-add; exp(r) by its Taylor polynomial of degree 7
+ * (truncation error < 6e-9 relative) in Horner form; the result is exp(r) * 2^k. */
+float spec_verify_ref_exp(float d)
+{
+    if (!(d >= -87.0f)) return d != d ? d : 0.0f;
+    if (d > 88.0f) return INFINITY;
+    const float shifter = 0x1.8p+23f;
+    float kf = fmaf(d, REF_LOG2E, shifter) - shifter;
+    float r = fmaf(-kf, REF_LN2_HI, d);
+    r = fmaf(-kf, REF_LN2_LO, r);
+    float p = 0x1.a01a02p-13f;            /* 1/7! */
+    p = fmaf(p, r, 0x1.6c16c2p-10f);      /* 1/6! */
+    p = fmaf(p, r, 0x1.111112p-7f);       /* 1/5! */
+    p = fmaf(p, r, 0x1.555556p-5f);       /* 1/4! */
+    p = fmaf(p, r, 0x1.555556p-3f);       /* 1/3! */
+    p = fmaf(p, r, 0.5f);                 /* 1/2! */
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    int k = (int)kf;
+    return p * bits_f((uint32_t)(k + 127) << 23);
+}
+
+/* log(x) for finite x > 0 (0 -> -inf, negative or NaN -> NaN, +inf -> +inf).
+ * x = 2^k f with f in [sqrt(1/2), sqrt(2)); ln f = 2 atanh(s), s = (f-1)/(f+1), |s| < 0.172,
+ * summed as 2s + s z (2/3 + z (2/5 + z (2/7 + z 2/9))), z = s^2 (truncation < 1e-9
+ * relative); ln x = k ln2 + ln f. Subnormal x is scaled by 2^23 first. */
+float spec_verify_ref_log(float x)
+{
+    if (x != x || x < 0.0f) return NAN;
+    if (x == 0.0f) return -INFINITY;
+    if (x == INFINITY) return INFINITY;
+    int k = 0;
+    uint32_t b = f_bits(x);
+    if (b < 0x00800000u) {
+        b = f_bits(x * 0x1p+23f);
+        k = -23;
+    }
+    k += (int)(b >> 23) - 127;
+    uint32_t fb = (b & 0x007FFFFFu) | 0x3F800000u;
+    if (fb > 0x3FB504F3u) { /* f > sqrt(2): halve it */
+        fb -= 0x00800000u;
+        k += 1;
+    }
+    float f = bits_f(fb);
+    float g = f - 1.0f;
+    float s = g / (g + 2.0f);
+    float z = s * s;
+    float P = fmaf(z, 0x1.c71c72p-3f, 0x1.24924ap-2f); /* 2/9, 2/7 */
+    P = fmaf(z, P, 0x1.99999ap-2f);                    /* 2/5 */
+    P = fmaf(z, P, 0x1.555556p-1f);                    /* 2/3 */
+    float R = z * P;
+    float lnf = fmaf(s, R, s + s);
+    float kf = (float)k;
+    return fmaf(kf, REF_LN2_HI, fmaf(kf, REF_LN2_LO, lnf));
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* The verification step.                                                                */
+/* ------------------------------------------------------------------------------------ */
+enum { REF_OK = 0, REF_EINVAL = -1, REF_EBATCH = 1 };
+enum { REF_RACE_NONE = 0, REF_RACE_RESIDUAL = 1, REF_RACE_EXCLUDE = 2, REF_RACE_BONUS = 3,
+       REF_RACE_FALLBACK = 4 };
+
+static inline float logit_at(const void *logits, int bf16, size_t idx)
+{
+    if (bf16) return bits_f((uint32_t)((const uint16_t *)logits)[idx] << 16);
+    return ((const float *)logits)[idx];
+}
+
+typedef struct {
+    float m;      /* max_v x_v */
+    double S;     /* sum_v exp(x_v - m), accumulated in double in index order */
+    float S_f;    /* S rounded to binary32: the value the decisions use */
+    int32_t amax; /* argmax of the raw logits, lowest index on ties */
+} row_stats_t;
+
+/* Softmax statistics of one row: [spec-in-vllm] 7.4 (block stats: max, argmax, sum of exp,
+ * for a log-sum-exp) and [spec-notes] 8.2 (target probs = softmax of the processed logits). */
+static row_stats_t row_stats(const void *logits, int bf16, size_t row, int V, float invT)
+{
+    const size_t base = row * (size_t)V;
+    row_stats_t st;
+    st.m = -INFINITY;
+    st.amax = 0;
+    float best_raw = logit_at(logits, bf16, base);
+    for (int v = 0; v < V; ++v) {
+        float l = logit_at(logits, bf16, base + (size_t)v);
+        float x = l * invT;
+        if (x > st.m) st.m = x;
+        if (l > best_raw) {
+            best_raw = l;
+            st.amax = v;
+        }
+    }
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) {
+        float x = logit_at(logits, bf16, base + (size_t)v) * invT;
+        S += (double)spec_verify_ref_exp(x - st.m);
+    }
+    st.S = S;
+    st.S_f = (float)S;
+    return st;
+}
+
+typedef struct {
+    int32_t idx;   /* winner, or -1 when no candidate */
+    float key;     /* winner's key */
+    double gap;    /* winner's key minus the runner-up's (+inf with fewer than two) */
+    int64_t ncand; /* number of candidates */
+} race_t;
+
+/* Offer candidate v (offered in increasing v): the larger key wins, and an equal key at a
+ * higher index loses to the earlier one, so the winner is the lowest index among the largest
+ * keys. `second` tracks the runner-up key for the decision margin. */
+static inline void race_offer(race_t *r, float key, int32_t v, float *second)
+{
+    r->ncand++;
+    if (r->idx < 0) {
+        r->key = key;
+        r->idx = v;
+    } else if (key > r->key) {
+        *second = r->key;
+        r->key = key;
+        r->idx = v;
+    } else if (key > *second) {
+        *second = key;
+    }
+}
+
+/* Exponential race over one row at position j of request ireq, [spec-notes] NO_DRAFT_PROBS
+ * answer (argmax(prob / q) with q ~ Exp(1) needs no normalisation) and [spec-in-vllm] 7.3
+ * (Gumbel argmax). Keys are taken in log form: key_v = log w_v - log E_v.
+ *   q == NULL : w_v proportional to p_v; key_v = x_v - log E_v; token `exclude` is left out
+ *               (the rejected draft token when there are no draft probabilities).
+ *   q != NULL : residual weights rr_v = fma(-S, q_v, t_v) = S (p_v - q_v) rounded once,
+ *               candidates rr_v > 0 ([spec-notes] residual distribution max(0, p - q)).  */
+static race_t race_row(const void *logits, int bf16, size_t row, int V, float invT, float m,
+                       float S_f, const float *q, int32_t exclude, uint64_t seed, uint32_t j,
+                       uint32_t ireq)
+{
+    race_t r = {-1, -INFINITY, INFINITY, 0};
+    float second = -INFINITY;
+    const size_t base = row * (size_t)V;
+    for (int v = 0; v < V; ++v) {
+        if (v == exclude) continue;
+        float x = logit_at(logits, bf16, base + (size_t)v) * invT;
+        float logw;
+        if (q) {
+            float t = spec_verify_ref_exp(x - m);
+            float rr = fmaf(-S_f, q[v], t);
+            if (!(rr > 0.0f)) continue;
+            logw = spec_verify_ref_log(rr);
+        } else {
+            logw = x;
+        }
+        float U = spec_verify_ref_uniform(seed, (uint32_t)v >> 2, j, ireq, REF_TAG_RACE, v & 3);
+        float E = -spec_verify_ref_log(U);
+        float key = logw - spec_verify_ref_log(E);
+        race_offer(&r, key, v, &second);
+    }
+    if (r.idx >= 0 && r.ncand >= 2) r.gap = (double)r.key - (double)second;
+    return r;
+}
+
+/*
+ * Verify one batch. Layout ([MTP-eagle] sample(): num_draft + 1 logit rows per request):
+ *   logits       [num_draft_tokens + num_reqs, V], row of (request i, position j) is
+ *                cu_num_draft[i] + i + j, j = K_i is the bonus row; bf16 bits or binary32.
+ *   draft_ids    [num_draft_tokens], draft j of request i at cu_num_draft[i] + j.
+ *   draft_probs  [num_draft_tokens, V] binary32 or NULL (no draft probabilities).
+ *   temperature, is_greedy [num_reqs].
+ * Outputs: sampled [num_reqs, max_spec_len + 1] (-1 padded), num_sampled, num_rejected.
+ * Optional diagnostics (NULL to skip): row_max, row_sumexp (binary32 S), row_argmax per row;
+ * accept_margin per draft position (|u - p/q| in double; +inf for greedy or invalid ids;
+ * NaN where not evaluated); race_gap, race_kind, jstar per request.
+ * u_override (test hook, NULL normally): acceptance uniforms per draft position.
+ * Returns 0; REF_EBATCH when cu_num_draft is inconsistent (then every request emits
+ * num_sampled = num_rejected = 0 and a row of -1); REF_EINVAL for bad arguments.
+ */
+int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
+                        const int32_t *draft_ids, const float *draft_probs,
+                        const int32_t *cu_num_draft, const float *temperature,
+                        const uint8_t *is_greedy, uint64_t seed, uint32_t req_index_base,
+                        int num_reqs, int num_draft_tokens, int max_spec_len, int32_t *sampled,
+                        int32_t *num_sampled, int32_t *num_rejected, float *row_max,
+                        float *row_sumexp, int32_t *row_argmax, double *accept_margin,
+                        double *race_gap, int32_t *race_kind, int32_t *jstar_out,
+                        const float *u_override)
+{
+    if (num_reqs < 0 || num_draft_tokens < 0 || max_spec_len < 0 || vocab_size <= 0) return REF_EINVAL;
+    const int V = vocab_size;
+    const int stride = max_spec_len + 1;
+    int bad = cu_num_draft[0] != 0 || cu_num_draft[num_reqs] != num_draft_tokens;
+    for (int i = 0; i < num_reqs && !bad; ++i) {
+        int K = cu_num_draft[i + 1] - cu_num_draft[i];
+        bad = K < 0 || K > max_spec_len;
+    }
+    if (accept_margin)
+        for (int k = 0; k < num_draft_tokens; ++k) accept_margin[k] = NAN;
+    if (bad) {
+        for (int i = 0; i < num_reqs; ++i) {
+            for (int s = 0; s < stride; ++s) sampled[(size_t)i * stride + s] = -1;
+            num_sampled[i] = 0;
+            num_rejected[i] = 0;
+            if (race_gap) race_gap[i] = INFINITY;
+            if (race_kind) race_kind[i] = REF_RACE_NONE;
+            if (jstar_out) jstar_out[i] = -1;
+        }
+        return REF_EBATCH;
+    }
+
+    for (int i = 0; i < num_reqs; ++i) {
+        const int q0 = cu_num_draft[i];
+        const int K = cu_num_draft[i + 1] - q0;
+        const size_t row0 = (size_t)q0 + (size_t)i;
+        const uint32_t ireq = req_index_base + (uint32_t)i;
+        const float T = temperature[i];
+        /* greedy: flag set, or temperature 0 ([spec-in-vllm] 7.0.1; [mini-sglang] T <= 0) */
+        const int greedy = is_greedy[i] != 0 || !(T > 0.0f);
+        const float invT = greedy ? 1.0f : 1.0f / T;
+
+        /* stats of every row (rows after a rejection are reported too, for inspection) */
+        row_stats_t st[K + 1];
+        for (int j = 0; j <= K; ++j) {
+            st[j] = row_stats(logits, logits_bf16, row0 + (size_t)j, V, invT);
+            if (row_max) row_max[row0 + j] = st[j].m;
+            if (row_sumexp) row_sumexp[row0 + j] = st[j].S_f;
+            if (row_argmax) row_argmax[row0 + j] = st[j].amax;
+        }
+
+        /* [MTP-eagle] _rejection_sample_kernel: walk the draft positions, stop at the
+         * first rejection; [spec-notes] 8.3 greedy and stochastic rules. */
+        int jstar = K;
+        for (int j = 0; j < K; ++j) {
+            const int32_t d = draft_ids[q0 + j];
+            int acc;
+            double margin;
+            if (greedy) {
+                acc = d == st[j].amax;
+                margin = INFINITY;
+            } else if (d < 0 || d >= V) {
+                acc = 0; /* [spec-notes] accept only when draft_token_id < vocab_size */
+                margin = INFINITY;
+            } else {
+                const float x_d = logit_at(logits, logits_bf16, (row0 + j) * (size_t)V + d) * invT;
+                const float t_d = spec_verify_ref_exp(x_d - st[j].m);
+                const float p_d = t_d / st[j].S_f;
+                const float q_d = draft_probs ? draft_probs[(size_t)(q0 + j) * V + d] : 1.0f;
+                const float u = u_override
+                                    ? u_override[q0 + j]
+                                    : spec_verify_ref_uniform(seed, 0u, (uint32_t)j, ireq,
+                                                              REF_TAG_ACCEPT, 0);
+                /* [spec-notes] answer code: draft_prob > 0 and target_prob / draft_prob >= uniform */
+                acc = q_d > 0.0f && p_d / q_d >= u;
+                margin = q_d > 0.0f ? fabs((double)u - (double)t_d / st[j].S / (double)q_d)
+                                    : INFINITY;
+            }
+            if (accept_margin) accept_margin[q0 + j] = margin;
+            if (!acc) {
+                jstar = j;
+                break;
+            }
+        }
+
+        int32_t token;
+        int kind = REF_RACE_NONE;
+        double gap = INFINITY;
+        if (greedy) {
+            /* [spec-notes] 8.3 greedy: output the target argmax at the mismatch; the bonus is
+             * the argmax of the bonus row. */
+            token = st[jstar].amax;
+        } else if (jstar == K) {
+            /* [spec-notes] bonus token: sampled from p at the position after the last draft;
+             * K = 0 is the plain Gumbel-max sample of a non-speculative request. */
+            race_t r = race_row(logits, logits_bf16, row0 + K, V, invT, st[K].m, st[K].S_f, NULL,
+                                -1, seed, (uint32_t)K, ireq);
+            token = r.idx;
+            gap = r.gap;
+            kind = REF_RACE_BONUS;
+        } else if (draft_probs) {
+            const float *q = draft_probs + (size_t)(q0 + jstar) * V;
+            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
+                                st[jstar].S_f, q, -1, seed, (uint32_t)jstar, ireq);
+            kind = REF_RACE_RESIDUAL;
+            if (r.idx < 0) {
+                /* nothing left of max(0, p - q) after rounding: sample from p itself so that
+                 * the emitted token is still a target-side draw */
+                r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
+                             st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                kind = REF_RACE_FALLBACK;
+            }
+            token = r.idx;
+            gap = r.gap;
+        } else {
+            /* [spec-notes] NO_DRAFT_PROBS: q is a point mass on d, so the residual is p with d
+             * removed; an out-of-range d removes nothing. */
+            const int32_t d = draft_ids[q0 + jstar];
+            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
+                                st[jstar].S_f, NULL, d, seed, (uint32_t)jstar, ireq);
+            if (r.idx < 0) /* V == 1 and d == 0: nothing else to draw */
+                r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
+                             st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+            token = r.idx;
+            gap = r.gap;
+            kind = REF_RACE_EXCLUDE;
+        }
+
+        /* [MTP-eagle] sampled[num_reqs, num_spec_steps + 1], num_sampled; [spec-notes] 9.2
+         * num_rejected = num_draft - num_accepted */
+        int32_t *out = sampled + (size_t)i * stride;
+        for (int j = 0; j < jstar; ++j) out[j] = draft_ids[q0 + j];
+        out[jstar] = token;
+        for (int s = jstar + 1; s < stride; ++s) out[s] = -1;
+        num_sampled[i] = jstar + 1;
+        num_rejected[i] = K - jstar;
+        if (race_gap) race_gap[i] = gap;
+        if (race_kind) race_kind[i] = kind;
+        if (jstar_out) jstar_out[i] = jstar;
+    }
+    return REF_OK;
+}
+
+/* Residual weights of one row as the race uses them (for identity checks):
+ * t_v = exp(x_v - m), rr_v = fma(-S, q_v, t_v); also returns m and S (binary32). */
+void spec_verify_ref_residual_row(const void *logits_row, int logits_bf16, int vocab_size,
+                                  float invT, const float *q, float *t_out, float *rr_out,
+                                  float *m_out, float *S_out)
+{
+    row_stats_t st = row_stats(logits_row, logits_bf16, 0, vocab_size, invT);
+    for (int v = 0; v < vocab_size; ++v) {
+        float x = logit_at(logits_row, logits_bf16, (size_t)v) * invT;
+        t_out[v] = spec_verify_ref_exp(x - st.m);
+        if (rr_out) rr_out[v] = fmaf(-st.S_f, q[v], t_out[v]);
+    }
+    *m_out = st.m;
+    *S_out = st.S_f;
+}
+
+/* Element-wise exp / log over arrays (for the accuracy checks of the two functions). */
+void spec_verify_ref_exp_n(const float *in, float *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = spec_verify_ref_exp(in[k]);
+}
+
+void spec_verify_ref_log_n(const float *in, float *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = spec_verify_ref_log(in[k]);
+}
+
+/* Uniforms of the race for positions v in [0, n) of (request ireq, position j). */
+void spec_verify_ref_race_uniforms(uint64_t seed, uint32_t j, uint32_t ireq, int32_t n, float *out)
+{
+    for (int32_t v = 0; v < n; ++v)
+        out[v] = spec_verify_ref_uniform(seed, (uint32_t)v >> 2, j, ireq, REF_TAG_RACE, v & 3);
+}
