@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 speculative-decoding verification sampler.
+
+One step = one call of the verification step (all three kernels) on one batch of the
+bandwidth workload: 256 requests x (K=5 draft positions + 1 bonus) = 1536 logit rows of a
+151936-token vocabulary in bf16, fp32 draft distributions for the 1280 draft positions
+(1245 MB of inputs, larger than the 129 MB L2, so no flush is needed between steps).
+
+Prints one JSON line (rank 0). Metric: verified draft positions per second, whole job.
+  python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload 0..4]
+Under torchrun (N > 1) every rank verifies its own batch (weak scaling, no collective on the
+data path); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft positions/sec"
+UNIT = "positions/s"
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stats_kernel_workload3.md")
+KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_rejection_gb300", "csrc",
+                             "spec_verify.cu")
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--profile-steps", type=int, default=500)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU work of the oracle baseline sample (seconds)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_config(b):
+    return {
+        "workload": f"{b.num_reqs} requests, K={b.max_spec_len} draft tokens + 1 bonus each, "
+                    f"V={b.vocab_size}, {b.logits_dtype} logits ({b.meta.get('workload', '')})",
+        "num_reqs": b.num_reqs,
+        "draft_positions": b.num_draft_tokens,
+        "logit_rows": b.num_rows,
+        "vocab": b.vocab_size,
+        "logits_dtype": b.logits_dtype,
+        "draft_probs": "fp32" if b.draft_probs is not None else "none",
+        "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)) / 1e6, 2),
+    }
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+class ClockSampler:
+    def __init__(self, gpu_index: str):
+        self.samples = []  # (t, sm, max, power, reasons_active dict)
+        self.proc = None
+        self.err = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", gpu_index], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError as e:
+            self.err = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            try:
+                pw = float(parts[3])
+            except ValueError:
+                pw = None
+            act = {r: parts[5 + k].lower().startswith("active") for k, r in enumerate(REASONS)}
+            self.samples.append((time.perf_counter(), sm, mx, pw, act))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": f"nvidia-smi unavailable: {self.err}"}
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        note = "samples inside the timed region"
+        if not win:  # timed region shorter than the sampling period: nearest samples
+            win = sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]
+            note = "timed region shorter than the 50 ms sampling period: nearest samples"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        sm = sorted(s[1] for s in win)
+        reasons = sorted({r for s in win for r, a in s[4].items() if a})
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(s[2] for s in win), "reasons": reasons,
+                "samples": len(win), "power_w_max": max((s[3] or 0) for s in win), "note": note}
+
+
+def gpu_index_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------------------------
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the stats kernel from the committed ncu summary, if the kernel
+    source has not changed since it was taken (source hash recorded in the summary)."""
+    import hashlib
+    try:
+        with open(PROFILE_SUMMARY, encoding="utf-8") as f:
+            text = f.read()
+        with open(KERNEL_SOURCE, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None, "no ncu summary"
+    fields = dict(l.split(":", 1) for l in text.splitlines() if l.startswith(("traffic_bytes_per_launch:", "kernel_source_sha256_16:")))
+    if fields.get("kernel_source_sha256_16", "").strip() != digest:
+        return None, "kernel changed since the ncu capture"
+    try:
+        return int(fields["traffic_bytes_per_launch"].strip()), "ncu dram__bytes_read.sum + dram__bytes_write.sum"
+    except (KeyError, ValueError):
+        return None, "no traffic line"
+
+
+# ---------------------------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------------------------
+def time_oracle(workload_index: int, seconds: float):
+    """Time the oracle (as it stands, single-threaded) on the first requests of the workload,
+    enough of them for about `seconds` of CPU work. Returns (positions/s, description)."""
+    import oracle
+    import workloads
+
+    one = workloads.workload(workload_index, num_reqs=2)
+    t = time.perf_counter()
+    oracle.run(one)
+    per_req = max((time.perf_counter() - t) / one.num_reqs, 1e-4)
+    n = max(2, int(seconds / per_req))
+    b = workloads.workload(workload_index, num_reqs=n)
+    t = time.perf_counter()
+    oracle.run(b)
+    dt = time.perf_counter() - t
+    desc = (f"oracle (single thread) on the first {b.num_reqs} requests of the workload "
+            f"({b.num_draft_tokens} draft positions, {b.num_rows} rows), {dt:.1f} s")
+    return b.num_draft_tokens / dt, desc, b.num_rows / dt
+
+
+# ---------------------------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    """The reference arm: the oracle as it stands, on this machine's host cores."""
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+
+    full = workloads.workload(args.workload, num_reqs=2)
+    t = time.perf_counter()
+    oracle.run(full)
+    per_req = max((time.perf_counter() - t) / 2, 1e-4)
+    budget = 150.0
+    n = int(max(1, min(256, budget / max(1, args.steps + args.warmup) / per_req)))
+    sample = workloads.workload(args.workload, num_reqs=n)
+    for _ in range(args.warmup):
+        oracle.run(sample)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.run(sample)
+    dt = time.perf_counter() - t0
+    value = sample.num_draft_tokens * args.steps / dt
+    cfg = workload_config(workloads.workload(args.workload))
+    cfg["reference_sample_requests_per_step"] = n
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step: the oracle on the first {n} requests of workload "
+                                   f"{args.workload} ({sample.num_draft_tokens} draft positions)"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_rejection_gb300 as sv
+    import workloads
+
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    if rank == 0:
+        sv.build()
+    if dist:
+        dist.barrier()
+    sv.lib()
+
+    b = workloads.workload(args.workload)
+    dev = torch.device("cuda", local)
+    logits_np = b.logits.view(np.int16) if b.logits.dtype == np.uint16 else b.logits
+    d_logits = torch.from_numpy(logits_np).to(dev)
+    d_q = torch.from_numpy(b.draft_probs).to(dev) if b.draft_probs is not None else None
+    d_ids = torch.from_numpy(b.draft_ids).to(dev)
+    d_cu = torch.from_numpy(b.cu_num_draft).to(dev)
+    d_T = torch.from_numpy(b.temperature).to(dev)
+    d_g = torch.from_numpy(b.is_greedy).to(dev)
+    n, nd, kmax, V = b.num_reqs, b.num_draft_tokens, b.max_spec_len, b.vocab_size
+    ctx = sv.SpecVerify(n, kmax, V, b.logits_dtype, b.draft_probs is not None, device=local)
+    outs = (torch.empty((n, kmax + 1), dtype=torch.int32, device=dev),
+            torch.empty(n, dtype=torch.int32, device=dev),
+            torch.empty(n, dtype=torch.int32, device=dev))
+    base = rank * n  # every rank draws its own numbers
+
+    def step():
+        ctx.run(d_logits, d_ids, d_q, d_cu, d_T, d_g, b.seed, req_index_base=base,
+                max_spec_len=kmax, out=outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_index_for(local)) if rank == 0 else None
+    if sampler:
+        time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    start.record()
+    for _ in range(args.steps):
+        step()
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    if sampler:
+        time.sleep(0.1)
+        sampler.stop()
+    ms_per_step = elapsed_ms / args.steps
+    value = world * nd / (ms_per_step / 1e3)
+    mean_sampled = float(outs[1].float().mean().item())
+
+    # per-kernel durations: CUDA events between the kernels, on the launching stream
+    ctx.set_profiling(True)
+    prof_steps = max(1, min(args.profile_steps, args.steps))
+    for _ in range(prof_steps):
+        step()
+    torch.cuda.synchronize()
+    kms, calls = ctx.get_profile()
+    ctx.set_profiling(False)
+    kavg = {k: v / max(calls, 1) for k, v in kms.items()}
+
+    # end to end through the host-buffer entry point: H2D of the inputs, verify, D2H of results
+    e2e = None
+    if not args.no_e2e:
+        ctx.reserve_host_io()
+        h_logits = torch.from_numpy(logits_np).pin_memory()
+        h_q = torch.from_numpy(b.draft_probs).pin_memory() if b.draft_probs is not None else None
+        h_ids = torch.from_numpy(b.draft_ids).pin_memory()
+        h_cu = torch.from_numpy(b.cu_num_draft).pin_memory()
+        h_T = torch.from_numpy(b.temperature).pin_memory()
+        h_g = torch.from_numpy(b.is_greedy).pin_memory()
+        h_out = (torch.empty((n, kmax + 1), dtype=torch.int32).pin_memory(),
+                 torch.empty(n, dtype=torch.int32).pin_memory(),
+                 torch.empty(n, dtype=torch.int32).pin_memory())
+
+        def e2e_step():
+            ctx.run_host(h_logits, h_ids, h_q, h_cu, h_T, h_g, b.seed, *h_out,
+                         req_index_base=base, max_spec_len=kmax)
+
+        for _ in range(2):
+            e2e_step()
+        ke = max(1, args.e2e_steps)
+        if dist:
+            dist.barrier()
+        te = time.perf_counter()
+        for _ in range(ke):
+            e2e_step()
+        te = time.perf_counter() - te
+        if dist:
+            t = torch.tensor([te], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            te = float(t.item())
+        h2d = (h_logits.numel() * h_logits.element_size()
+               + (h_q.numel() * 4 if h_q is not None else 0)
+               + nd * 4 + (n + 1) * 4 + n * 4 + n)
+        d2h = sum(t.numel() * 4 for t in h_out)
+        e2e = {"value": world * nd * ke / te, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": ke, "ms_per_step": te / ke * 1e3,
+               "timing": "host wall clock around run_host (copies + kernels + stream sync)"}
+        if not np.array_equal(h_out[0].numpy(), outs[0].cpu().numpy()):
+            raise RuntimeError("host-buffer path disagrees with the device path")
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak_gbs()
+    stats_bytes = b.num_rows * V * b.elem_bytes   # every logit read once: R x V x element size
+    achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
+    traffic, traffic_src = recorded_traffic()
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        v, desc, _ = time_oracle(args.workload, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+    clocks = sampler.summary(t0, t1) if sampler else None
+    cfg = workload_config(b)
+    cfg.update({"l2": "inputs larger than L2 (no flush between steps)", "parallelism":
+                f"replicas x{world}" if world > 1 else "single GPU",
+                "req_index_base": "rank * num_reqs"})
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
+        "e2e": e2e, "gpu_launches": sv.spec_verify_launches_per_run() * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "sv_stats_kernel (row statistics, reads every logit once)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "traffic_source": traffic_src,
+                     "algorithmic_bytes_per_launch": stats_bytes},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "kernel_ms": {**kavg, "profiled_calls": calls},
+        "rows_per_s": world * b.num_rows / (ms_per_step / 1e3),
+        "full_bytes_gbs": world * b.bytes_full() / (ms_per_step / 1e3) / 1e9,
+        "mean_num_sampled": mean_sampled,
+    }
+    print(json.dumps(line), flush=True)
+    ctx.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,178 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 speculative-decoding verification sampler.
+ *
+ * One call verifies a batch of requests: for each request i with K_i draft tokens it takes
+ * the target model's logits at the K_i draft positions and at one bonus position, computes
+ * p = softmax(logits / T), accepts draft d at position j when u < min(1, p(d) / q(d)), stops at
+ * the first rejection and emits there a token drawn from the residual max(0, p - q) (or from p
+ * with d removed when no draft distribution is given), or appends a bonus token drawn from p
+ * when every draft is accepted. Greedy requests accept iff d is the target argmax.
+ *
+ * Pages (title, section) the operation is defined by:
+ *   [MTP-eagle]    "【vllm】DeepSeekMTP、eagle": sample() call tree -- logits at num_draft + 1
+ *                  positions per request, Gumbel-max sampler, _rejection_sample_kernel (one
+ *                  program per request, stop at the first mismatch, bonus when all match),
+ *                  outputs sampled[num_reqs, num_spec_steps + 1], num_sampled, num_rejected.
+ *   [spec-notes]   "vLLM 投机解码（Eagle / MTP）实现与运行流程": residual distribution Q&A
+ *                  (min(1, p/q), max(0, p - q) normalised), bonus token and NO_DRAFT_PROBS
+ *                  Q&A (accept test code, masked target probs, argmax(prob / Exp(1))),
+ *                  section 8.2 (rejection_sample(draft_token_ids, num_draft_tokens,
+ *                  draft_probs, target_probs, bonus_token_ids)), 8.3 (greedy / stochastic
+ *                  rules), 9.2 (num_rejected = num_draft - num_accepted).
+ *   [spec-in-vllm] "speculative decoding in vLLM": 7.0 acceptance u < p/q and residual,
+ *                  7.0.1 greedy, 7.0.2 bonus, 7.3 Gumbel argmax, 7.4 stats / reject /
+ *                  resample / insert kernels.
+ *   [mini-sglang]  "mini-sglang", "how tokens are sampled": temperature <= 0 means greedy.
+ *
+ * Conventions fixed by this library where the pages leave them open:
+ *   - Rows: the logits of (request i, position j), j = 0..K_i (j = K_i is the bonus
+ *     position), are row cu_num_draft[i] + i + j of a row-major [num_draft_tokens + num_reqs, V]
+ *     array; draft j of request i is draft_ids[cu_num_draft[i] + j] and its distribution is row
+ *     cu_num_draft[i] + j of draft_probs [num_draft_tokens, V].
+ *   - x_v = logit_v * (1 / T) in binary32; a request is greedy if is_greedy[i] != 0 or
+ *     !(T > 0). Greedy argmax is over the raw logits, lowest index on ties.
+ *   - Random draws are keyed, so results are reproducible and independent of launch shape:
+ *     Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed), hi32(seed)), counter =
+ *     (v >> 2, j, req_index_base + i, tag), word v & 3, uniform U = ((w >> 9) + 1/2) / 2^23.
+ *     tag 0 (v = 0): acceptance uniform u; tag 1: race exponentials E_v = -log U_v.
+ *   - A draw from weights w_v is the exponential race argmax_v (log w_v - log E_v), lowest
+ *     index on equal keys. Residual weights are rr_v = fma(-S, q_v, exp(x_v - m)) (S times
+ *     p_v - q_v, rounded once), candidates rr_v > 0; if none is left after rounding, the token
+ *     is drawn from p. Without draft probabilities the rejected draft token is removed.
+ *   - Acceptance: 0 <= d < V and q(d) > 0 and p(d) / q(d) >= u (binary32), q(d) = 1 without
+ *     draft probabilities. An out-of-range draft id is rejected, not an error.
+ *   - exp / log inside these decisions are fixed binary32 functions (Cody-Waite reduction
+ *     with a degree-7 Taylor polynomial; atanh series on [sqrt(1/2), sqrt(2))), so decisions
+ *     are reproducible bit for bit on any implementation that follows them.
+ *   - sampled[i, :] holds the accepted drafts, then the recovered or bonus token, then -1.
+ *     num_sampled[i] = accepted + 1, num_rejected[i] = K_i - accepted.
+ *
+ * Error behaviour: every entry point returns a status code (SV_OK or a negative SV_E*) and
+ * never aborts the process. Problems visible on the host (NULL pointers, sizes beyond the
+ * capacity given at init, dtype mismatch) are returned before anything is launched. Problems
+ * in device data (cu_num_draft not starting at 0, decreasing, a K_i above
+ * max_spec_len_this_batch, or a total different from num_draft_tokens) make every request of
+ * that call emit num_sampled = num_rejected = 0 and a row of -1, and set SV_ERR_BATCH in the
+ * context's error word (read with spec_verify_last_error).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define SV_OK 0
+#define SV_EINVAL (-1)    /* NULL or misaligned pointer, negative size, bad argument */
+#define SV_ECAPACITY (-2) /* a size above the capacity given to spec_verify_init */
+#define SV_EDTYPE (-3)    /* logits dtype not SV_F32 / SV_BF16 */
+#define SV_ECUDA (-4)     /* a CUDA runtime call failed */
+#define SV_EDEVICE (-5)   /* no usable device, or not an sm_103 device */
+
+/* logits element types */
+#define SV_F32 0  /* IEEE binary32 */
+#define SV_BF16 1 /* bfloat16 (upper half of a binary32) */
+
+/* bits of the device error word */
+#define SV_ERR_BATCH 1u /* inconsistent cu_num_draft / draft lengths in some call */
+
+typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
+
+/*
+ * Create a context on `device` (a CUDA ordinal) for batches of at most max_num_reqs requests,
+ * at most max_spec_len draft tokens each, vocabulary size vocab_size and logits of type
+ * logits_dtype (SV_F32 / SV_BF16). has_draft_probs = 0 promises that draft_probs is always
+ * NULL (only the host-buffer entry point sizes anything by it).
+ * The context owns its device scratch (per-row statistics, per-split partials, counters),
+ * allocated here once; spec_verify_run allocates nothing. Free with spec_verify_free.
+ * Returns SV_OK and *out, or an error with *out = NULL.
+ */
+int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, int vocab_size,
+                     int logits_dtype, int has_draft_probs, int device);
+
+/*
+ * Verify one batch, asynchronously on `cuda_stream` (a cudaStream_t; NULL = legacy default
+ * stream). All pointers are device pointers owned by the caller and must stay valid until the
+ * stream reaches the end of this call; logits and draft_probs must be 16-byte aligned.
+ *   logits        [num_draft_tokens + num_reqs, vocab_size] of the context's dtype (layout above)
+ *   draft_ids     [num_draft_tokens] int32
+ *   draft_probs   [num_draft_tokens, vocab_size] binary32 distributions, or NULL (draft ids only)
+ *   cu_num_draft  [num_reqs + 1] int32 prefix sums of the draft lengths, cu_num_draft[0] = 0
+ *   temperature   [num_reqs] binary32;  is_greedy [num_reqs] uint8
+ *   seed, req_index_base: RNG key and the request index of the first request (so a batch split
+ *                 across calls or devices draws the same numbers as the whole batch)
+ *   max_spec_len_this_batch: row length - 1 of `sampled`; every K_i must be <= it
+ *   sampled       [num_reqs, max_spec_len_this_batch + 1] int32 (out)
+ *   num_sampled, num_rejected  [num_reqs] int32 (out)
+ *   opt_row_max, opt_row_sumexp [num_draft_tokens + num_reqs] binary32, opt_row_argmax int32:
+ *                 optional (NULL to skip) per-row m = max_v x_v, S = sum_v exp(x_v - m) and the
+ *                 raw-logit argmax, for every row including rows after a rejection (greedy rows
+ *                 use T = 1 for m and S).
+ * The call performs no allocation and no host synchronisation and may be captured in a CUDA
+ * graph. Calls on one context must not overlap on the device (they share its scratch).
+ */
+int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
+                    const float *draft_probs, const int32_t *cu_num_draft,
+                    const float *temperature, const uint8_t *is_greedy, uint64_t seed,
+                    uint32_t req_index_base, int num_reqs, int num_draft_tokens,
+                    int max_spec_len_this_batch, int32_t *sampled, int32_t *num_sampled,
+                    int32_t *num_rejected, float *opt_row_max, float *opt_row_sumexp,
+                    int32_t *opt_row_argmax, void *cuda_stream);
+
+/*
+ * Allocate device staging buffers sized for the context's capacity (logits, draft_probs if
+ * has_draft_probs, and the small per-request arrays) so that spec_verify_run_host can be used.
+ */
+int spec_verify_reserve_host_io(spec_verify_ctx *ctx);
+
+/*
+ * Same as spec_verify_run but every pointer is a HOST pointer (page-locked memory gives
+ * asynchronous copies; pageable memory works too). The inputs are copied to the context's
+ * staging buffers, the batch is verified, and sampled / num_sampled / num_rejected are copied
+ * back; the call returns after the stream has finished (the outputs are ready). Requires
+ * spec_verify_reserve_host_io.
+ */
+int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
+                         const float *draft_probs, const int32_t *cu_num_draft,
+                         const float *temperature, const uint8_t *is_greedy, uint64_t seed,
+                         uint32_t req_index_base, int num_reqs, int num_draft_tokens,
+                         int max_spec_len_this_batch, int32_t *sampled, int32_t *num_sampled,
+                         int32_t *num_rejected, void *cuda_stream);
+
+/*
+ * Read and clear the context's device error word (SV_ERR_* bits) into *err_word. Waits for
+ * the device (synchronises the context's device).
+ */
+int spec_verify_last_error(spec_verify_ctx *ctx, uint32_t *err_word);
+
+/*
+ * Kernel timing. With enable != 0, each later spec_verify_run records CUDA events around its
+ * kernels on the call's stream. spec_verify_get_profile waits for the recorded work and
+ * returns, per kernel (0 = plan, 1 = row statistics, 2 = race and emit), the summed
+ * milliseconds in ms[3] and the number of timed calls in *calls, then resets the sums.
+ */
+int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable);
+int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[3], int64_t *calls);
+
+/* Launch-shape knobs (elements per CTA of the statistics and race kernels; 0 keeps the
+ * current value). Values are rounded up to a multiple of 8 and clamped to the context's
+ * scratch capacity. Results do not depend on them. */
+int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk, int race_chunk);
+
+/* Number of kernel launches one spec_verify_run makes for a non-empty batch. */
+int spec_verify_launches_per_run(void);
+
+/* Release the context and its device memory. NULL is a no-op. */
+void spec_verify_free(spec_verify_ctx *ctx);
+
+/* Static description of a status code. */
+const char *spec_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

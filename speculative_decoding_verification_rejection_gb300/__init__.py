@@ -1,0 +1,316 @@
+"""GB300-native speculative-decoding verification sampler.
+
+Python binding of the C ABI in ``include/spec_verify.h`` (``libspecverify.so``, built in-tree
+for sm_103a by :func:`build`). This module only marshals arguments: every step of the
+verification runs in the library's CUDA kernels. PyTorch tensors are accepted for device
+memory and streams; raw integer pointers work as well.
+
+The same names as the C ABI are exported (``spec_verify_init``, ``spec_verify_run``, ...),
+plus :class:`SpecVerify`, a small owner of a context.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_INCLUDE = os.path.join(_ROOT, "include")
+_HEADER = os.path.join(_INCLUDE, "spec_verify.h")
+_SOURCES = [os.path.join(_PKG, "csrc", "spec_verify.cu"), os.path.join(_PKG, "csrc", "sv_device.cuh")]
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
+              "-shared", "-Xcompiler", "-fPIC", "-I" + _INCLUDE]
+
+SV_OK, SV_EINVAL, SV_ECAPACITY, SV_EDTYPE, SV_ECUDA, SV_EDEVICE = 0, -1, -2, -3, -4, -5
+SV_F32, SV_BF16 = 0, 1
+SV_ERR_BATCH = 1
+KERNELS = ("plan", "stats", "race")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        msg = _status_string(status)
+        super().__init__(f"{what}: {msg} ({status})")
+        self.status = status
+
+
+def _nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), "/usr/local/cuda/bin/nvcc", "nvcc"):
+        if cand and (os.path.sep not in cand or os.path.exists(cand)):
+            return cand
+    return "nvcc"
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    return any(os.path.getmtime(s) > t for s in _SOURCES + [_HEADER])
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libspecverify.so for sm_103a next to this file (atomic replace)."""
+    if not force and not _stale():
+        return LIB_PATH
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_PKG)
+    os.close(fd)
+    cmd = [_nvcc(), *NVCC_FLAGS, "-o", tmp, _SOURCES[0]]
+    try:
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stderr[-4000:])
+        if verbose:
+            print(r.stderr)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        if os.path.exists(tmp):
+            os.unlink(tmp)
+    return LIB_PATH
+
+
+def declared_symbols() -> list[str]:
+    """Names of the functions include/spec_verify.h declares."""
+    with open(_HEADER, encoding="utf-8") as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(spec_verify_\w+)\s*\(", text, re.M)))
+
+
+def lib():
+    """The loaded C library (ctypes), built first if missing. Raises if it cannot be built or
+    loaded: there is no fallback implementation."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if _stale():
+        try:
+            build()
+        except (OSError, RuntimeError) as e:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError("libspecverify.so is missing and could not be built: " + str(e))
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, u32, u64, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64
+    L.spec_verify_init.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32]
+    L.spec_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp,
+                                  vp, vp, vp, vp]
+    L.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp,
+                                       vp, vp]
+    L.spec_verify_reserve_host_io.argtypes = [vp]
+    L.spec_verify_last_error.argtypes = [vp, ctypes.POINTER(u32)]
+    L.spec_verify_set_profiling.argtypes = [vp, i32]
+    L.spec_verify_get_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
+    L.spec_verify_set_chunks.argtypes = [vp, i32, i32]
+    L.spec_verify_launches_per_run.argtypes = []
+    L.spec_verify_free.argtypes = [vp]
+    L.spec_verify_free.restype = None
+    L.spec_verify_status_string.argtypes = [i32]
+    L.spec_verify_status_string.restype = ctypes.c_char_p
+    for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_host",
+              "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
+              "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
+        getattr(L, f).restype = i32
+    _lib = L
+    return L
+
+
+def _status_string(status: int) -> str:
+    try:
+        return lib().spec_verify_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - only for messages
+        return "status"
+
+
+def _check(status: int, what: str) -> None:
+    if status != SV_OK:
+        raise SpecVerifyError(status, what)
+
+
+def _ptr(x):
+    """Device or host address of a tensor / array / int (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if not x.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ---- thin wrappers with the C names --------------------------------------------------------
+
+def spec_verify_init(max_num_reqs: int, max_spec_len: int, vocab_size: int, logits_dtype: int,
+                     has_draft_probs: int, device: int) -> int:
+    ctx = ctypes.c_void_p()
+    _check(lib().spec_verify_init(ctypes.byref(ctx), max_num_reqs, max_spec_len, vocab_size,
+                                  logits_dtype, has_draft_probs, device), "spec_verify_init")
+    return ctx.value
+
+
+def spec_verify_run(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy,
+                    seed, req_index_base, num_reqs, num_draft_tokens, max_spec_len_this_batch,
+                    sampled, num_sampled, num_rejected, opt_row_max=None, opt_row_sumexp=None,
+                    opt_row_argmax=None, cuda_stream=None) -> None:
+    _check(lib().spec_verify_run(ctx, _ptr(logits), _ptr(draft_ids), _ptr(draft_probs),
+                                 _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy), seed,
+                                 req_index_base, num_reqs, num_draft_tokens,
+                                 max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled),
+                                 _ptr(num_rejected), _ptr(opt_row_max), _ptr(opt_row_sumexp),
+                                 _ptr(opt_row_argmax), _stream_handle(cuda_stream)),
+           "spec_verify_run")
+
+
+def spec_verify_run_host(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
+                         is_greedy, seed, req_index_base, num_reqs, num_draft_tokens,
+                         max_spec_len_this_batch, sampled, num_sampled, num_rejected,
+                         cuda_stream=None) -> None:
+    _check(lib().spec_verify_run_host(ctx, _ptr(logits), _ptr(draft_ids), _ptr(draft_probs),
+                                      _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy), seed,
+                                      req_index_base, num_reqs, num_draft_tokens,
+                                      max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled),
+                                      _ptr(num_rejected), _stream_handle(cuda_stream)),
+           "spec_verify_run_host")
+
+
+def spec_verify_reserve_host_io(ctx) -> None:
+    _check(lib().spec_verify_reserve_host_io(ctx), "spec_verify_reserve_host_io")
+
+
+def spec_verify_last_error(ctx) -> int:
+    w = ctypes.c_uint32()
+    _check(lib().spec_verify_last_error(ctx, ctypes.byref(w)), "spec_verify_last_error")
+    return w.value
+
+
+def spec_verify_set_profiling(ctx, enable: bool) -> None:
+    _check(lib().spec_verify_set_profiling(ctx, int(enable)), "spec_verify_set_profiling")
+
+
+def spec_verify_get_profile(ctx):
+    ms = (ctypes.c_double * 3)()
+    calls = ctypes.c_int64()
+    _check(lib().spec_verify_get_profile(ctx, ms, ctypes.byref(calls)), "spec_verify_get_profile")
+    return dict(zip(KERNELS, list(ms))), calls.value
+
+
+def spec_verify_set_chunks(ctx, stats_chunk: int = 0, race_chunk: int = 0) -> None:
+    _check(lib().spec_verify_set_chunks(ctx, stats_chunk, race_chunk), "spec_verify_set_chunks")
+
+
+def spec_verify_launches_per_run() -> int:
+    return lib().spec_verify_launches_per_run()
+
+
+def spec_verify_free(ctx) -> None:
+    if ctx:
+        lib().spec_verify_free(ctx)
+
+
+def spec_verify_status_string(status: int) -> str:
+    return _status_string(status)
+
+
+# ---- convenience owner ---------------------------------------------------------------------
+
+def _dtype_code(logits_dtype) -> int:
+    s = str(logits_dtype).lower()
+    if "bf16" in s or "bfloat16" in s:
+        return SV_BF16
+    if "f32" in s or "float32" in s or s in ("float", "torch.float"):
+        return SV_F32
+    raise ValueError(f"unsupported logits dtype {logits_dtype}")
+
+
+class SpecVerify:
+    """Owns one context. Tensors passed to :meth:`run` must live on the context's device."""
+
+    def __init__(self, max_num_reqs: int, max_spec_len: int, vocab_size: int, logits_dtype="bf16",
+                 has_draft_probs: bool = True, device: int = 0):
+        self.max_num_reqs, self.max_spec_len, self.vocab_size = max_num_reqs, max_spec_len, vocab_size
+        self.dtype_code = _dtype_code(logits_dtype)
+        self.device = device
+        self.ctx = spec_verify_init(max_num_reqs, max_spec_len, vocab_size, self.dtype_code,
+                                    int(has_draft_probs), device)
+
+    def run(self, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy, seed: int,
+            *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
+            row_stats: bool = False, stream=None):
+        """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
+        and, with row_stats=True, also (row_max, row_sumexp, row_argmax)."""
+        import torch
+        num_reqs = cu_num_draft.numel() - 1
+        nd = draft_ids.numel()
+        kmax = self.max_spec_len if max_spec_len is None else max_spec_len
+        if logits.dim() != 2 or logits.shape[0] != nd + num_reqs or logits.shape[1] != self.vocab_size:
+            raise ValueError("logits must be [num_draft_tokens + num_reqs, vocab_size]")
+        dev = logits.device
+        if out is None:
+            out = (torch.empty((num_reqs, kmax + 1), dtype=torch.int32, device=dev),
+                   torch.empty(num_reqs, dtype=torch.int32, device=dev),
+                   torch.empty(num_reqs, dtype=torch.int32, device=dev))
+        stats = (None, None, None)
+        if row_stats:
+            R = nd + num_reqs
+            stats = (torch.empty(R, dtype=torch.float32, device=dev),
+                     torch.empty(R, dtype=torch.float32, device=dev),
+                     torch.empty(R, dtype=torch.int32, device=dev))
+        spec_verify_run(self.ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
+                        is_greedy, seed, req_index_base, num_reqs, nd, kmax, *out, *stats,
+                        cuda_stream=stream)
+        return (*out, *stats) if row_stats else out
+
+    def reserve_host_io(self) -> None:
+        spec_verify_reserve_host_io(self.ctx)
+
+    def run_host(self, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy,
+                 seed: int, sampled, num_sampled, num_rejected, *, req_index_base: int = 0,
+                 max_spec_len: int | None = None, stream=None) -> None:
+        """Verify a batch held in host memory (numpy arrays or CPU tensors; pinned memory
+        gives asynchronous copies); outputs are written to the host arrays given."""
+        num_reqs = len(cu_num_draft) - 1
+        nd = len(draft_ids)
+        kmax = self.max_spec_len if max_spec_len is None else max_spec_len
+        spec_verify_run_host(self.ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
+                             is_greedy, seed, req_index_base, num_reqs, nd, kmax, sampled,
+                             num_sampled, num_rejected, cuda_stream=stream)
+
+    def last_error(self) -> int:
+        return spec_verify_last_error(self.ctx)
+
+    def set_profiling(self, enable: bool) -> None:
+        spec_verify_set_profiling(self.ctx, enable)
+
+    def get_profile(self):
+        return spec_verify_get_profile(self.ctx)
+
+    def set_chunks(self, stats_chunk: int = 0, race_chunk: int = 0) -> None:
+        spec_verify_set_chunks(self.ctx, stats_chunk, race_chunk)
+
+    def close(self) -> None:
+        if self.ctx:
+            spec_verify_free(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass

@@ -1,0 +1,123 @@
+// Device-side random numbers and binary32 elementary functions of the verification sampler.
+//
+// Every decision of the sampler (acceptance test, race keys) is defined with these functions,
+// so they use only correctly rounded binary32 operations written as explicit intrinsics
+// (__fmaf_rn, __fmul_rn, __fadd_rn, __fsub_rn, __fdiv_rn): the compiler may not contract or
+// reorder them, and the result is fixed bit for bit by the algorithm below.
+#pragma once
+
+#include <cstdint>
+
+namespace sv {
+
+// ---------------------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
+// SC'11): ten rounds; a round multiplies counter words 0 and 2 by the two round multipliers,
+// mixes the high halves with the other counter words and the key, and the key is advanced by
+// the two Weyl increments (golden ratio and sqrt(3) - 1 in 32-bit fixed point).
+// ---------------------------------------------------------------------------------------
+struct Philox4 {
+    uint32_t x, y, z, w;
+};
+
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1)
+{
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t lo0 = 0xD2511F53u * c0;
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+        const uint32_t lo1 = 0xCD9E8D57u * c2;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+        c0 = hi1 ^ c1 ^ k0;
+        c1 = lo1;
+        c2 = hi0 ^ c3 ^ k1;
+        c3 = lo0;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return Philox4{c0, c1, c2, c3};
+}
+
+// U in (0,1) from a 32-bit word: (floor(w / 2^9) + 1/2) * 2^-23, exact in binary32.
+__device__ __forceinline__ float uniform_from_word(uint32_t w)
+{
+    return __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+}
+
+constexpr uint32_t kTagAccept = 0u;
+constexpr uint32_t kTagRace = 1u;
+
+// Largest value of -log(E) with E = -log(U), U <= 1 - 2^-24 (about 16.6355), padded.
+constexpr float kGumbelMax = 16.7f;
+
+// ---------------------------------------------------------------------------------------
+// binary32 exp: Cody & Waite (1980) reduction d = k ln2 + r with k = round(d log2 e) taken by
+// adding 1.5 * 2^23 in one fused multiply-add, r reduced with a two-part ln 2, exp(r) by its
+// degree-7 Taylor polynomial in Horner form, result exp(r) * 2^k. Defined as 0 below -87.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float exp_f32(float d)
+{
+    if (!(d >= -87.0f)) return d != d ? d : 0.0f;
+    if (d > 88.0f) return __int_as_float(0x7F800000);
+    const float shifter = 0x1.8p+23f;
+    const float kf = __fsub_rn(__fmaf_rn(d, 0x1.715476p+0f, shifter), shifter);
+    float r = __fmaf_rn(-kf, 0x1.62e430p-1f, d);     // ln 2 rounded to binary32
+    r = __fmaf_rn(-kf, -0x1.05c610p-29f, r);          // the remainder of ln 2
+    float p = 0x1.a01a02p-13f;                         // 1/7!
+    p = __fmaf_rn(p, r, 0x1.6c16c2p-10f);              // 1/6!
+    p = __fmaf_rn(p, r, 0x1.111112p-7f);               // 1/5!
+    p = __fmaf_rn(p, r, 0x1.555556p-5f);               // 1/4!
+    p = __fmaf_rn(p, r, 0x1.555556p-3f);               // 1/3!
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    const int k = __float2int_rn(kf);
+    return __fmul_rn(p, __int_as_float((k + 127) << 23));
+}
+
+// ---------------------------------------------------------------------------------------
+// binary32 log for x > 0: x = 2^k f with f in [sqrt(1/2), sqrt(2)), ln f = 2 atanh(s),
+// s = (f - 1) / (f + 1), summed as 2s + s z (2/3 + z (2/5 + z (2/7 + z 2/9))), z = s^2;
+// ln x = k ln 2 + ln f with a two-part ln 2. Subnormals are scaled by 2^23 first.
+// 0 -> -inf, negative or NaN -> NaN, +inf -> +inf.
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ float log_f32(float x)
+{
+    if (x != x || x < 0.0f) return __int_as_float(0x7FC00000);
+    if (x == 0.0f) return __int_as_float(0xFF800000);
+    if (x == __int_as_float(0x7F800000)) return x;
+    int k = 0;
+    uint32_t b = __float_as_uint(x);
+    if (b < 0x00800000u) {
+        b = __float_as_uint(__fmul_rn(x, 0x1p+23f));
+        k = -23;
+    }
+    k += static_cast<int>(b >> 23) - 127;
+    uint32_t fb = (b & 0x007FFFFFu) | 0x3F800000u;
+    if (fb > 0x3FB504F3u) {  // f > sqrt(2): halve it
+        fb -= 0x00800000u;
+        k += 1;
+    }
+    const float f = __uint_as_float(fb);
+    const float g = __fsub_rn(f, 1.0f);
+    const float s = __fdiv_rn(g, __fadd_rn(g, 2.0f));
+    const float z = __fmul_rn(s, s);
+    float P = __fmaf_rn(z, 0x1.c71c72p-3f, 0x1.24924ap-2f);  // 2/9, 2/7
+    P = __fmaf_rn(z, P, 0x1.99999ap-2f);                      // 2/5
+    P = __fmaf_rn(z, P, 0x1.555556p-1f);                      // 2/3
+    const float R = __fmul_rn(z, P);
+    const float lnf = __fmaf_rn(s, R, __fadd_rn(s, s));
+    const float kf = __int2float_rn(k);
+    return __fmaf_rn(kf, 0x1.62e430p-1f, __fmaf_rn(kf, -0x1.05c610p-29f, lnf));
+}
+
+// Fast 2^x (MUFU), for sums and for conservative screening only -- never for a decision.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+}  // namespace sv

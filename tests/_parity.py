@@ -1,0 +1,105 @@
+"""GPU-vs-oracle comparison used by the -m gpu tests and the smoke check.
+
+Token ids and accept lengths must match bit for bit. The only exception is a request whose
+outputs differ after a decision the oracle calls too close to call: an acceptance test with
+|u - p/q| < 1e-6 at a position both sides evaluated, or a residual race whose two best keys
+are closer than 1e-6 (the residual depends on the row's sum of exponentials S, which the two
+sides accumulate in different orders). Such a request is a counted tie and the rest of it is
+not compared. The row statistics must match: m and the argmax exactly, S to 1e-5 relative.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+TIE_MARGIN = 1e-6
+S_RTOL = 1e-5
+RACE_RESIDUAL = 1
+
+
+def to_device(batch, device="cuda:0"):
+    import torch
+
+    logits = np.ascontiguousarray(batch.logits)
+    lt = torch.from_numpy(logits.view(np.int16) if logits.dtype == np.uint16 else logits).to(device)
+    q = None
+    if batch.draft_probs is not None:
+        q = torch.from_numpy(np.ascontiguousarray(batch.draft_probs, np.float32)).to(device)
+    return dict(
+        logits=lt,
+        draft_ids=torch.from_numpy(np.ascontiguousarray(batch.draft_ids, np.int32)).to(device),
+        draft_probs=q,
+        cu_num_draft=torch.from_numpy(np.ascontiguousarray(batch.cu_num_draft, np.int32)).to(device),
+        temperature=torch.from_numpy(np.ascontiguousarray(batch.temperature, np.float32)).to(device),
+        is_greedy=torch.from_numpy(np.ascontiguousarray(batch.is_greedy, np.uint8)).to(device),
+    )
+
+
+def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, chunks=None,
+            device="cuda:0"):
+    """Run the library on a workloads.Batch; returns numpy outputs incl. row stats."""
+    import torch
+
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    kmax = batch.max_spec_len if max_spec_len is None else max_spec_len
+    own = ctx is None
+    if own:
+        ctx = sv.SpecVerify(max(batch.num_reqs, 1), max(kmax, 0), batch.vocab_size,
+                            batch.logits_dtype, batch.draft_probs is not None,
+                            device=torch.device(device).index or 0)
+    if chunks:
+        ctx.set_chunks(*chunks)
+    d = to_device(batch, device)
+    outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
+                   d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,
+                   req_index_base=req_index_base, max_spec_len=kmax, row_stats=True)
+    torch.cuda.synchronize()
+    names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
+    res = {k: v.cpu().numpy() for k, v in zip(names, outs)}
+    res["error_word"] = ctx.last_error()
+    if own:
+        ctx.close()
+    return res
+
+
+def compare(batch, gpu: dict, ref: dict) -> dict:
+    """Compare GPU outputs with the oracle's. Returns counts; raises AssertionError with the
+    first real mismatches."""
+    cu = batch.cu_num_draft
+    n = batch.num_reqs
+    ties, bad = [], []
+    for i in range(n):
+        if (gpu["num_sampled"][i] == ref["num_sampled"][i]
+                and gpu["num_rejected"][i] == ref["num_rejected"][i]
+                and np.array_equal(gpu["sampled"][i], ref["sampled"][i])):
+            continue
+        js_ref = int(ref["jstar"][i])
+        js_gpu = int(gpu["num_sampled"][i]) - 1
+        upto = min(js_ref, js_gpu)
+        m = ref["accept_margin"][cu[i]:cu[i] + max(upto, -1) + 1]
+        m = m[~np.isnan(m)]
+        closest = float(m.min()) if m.size else np.inf
+        if js_ref == js_gpu and ref["race_kind"][i] == RACE_RESIDUAL:
+            closest = min(closest, float(ref["race_gap"][i]))
+        (ties if closest < TIE_MARGIN else bad).append((i, closest))
+    R = batch.num_rows
+    stats_ok = dict(
+        row_max=bool(np.array_equal(gpu["row_max"][:R], ref["row_max"][:R])),
+        row_argmax=bool(np.array_equal(gpu["row_argmax"][:R], ref["row_argmax"][:R])),
+    )
+    rel = np.abs(gpu["row_sumexp"][:R].astype(np.float64) - ref["row_sumexp"][:R]) / \
+        np.maximum(np.abs(ref["row_sumexp"][:R].astype(np.float64)), 1e-30)
+    stats_ok["row_sumexp"] = bool(np.all(rel <= S_RTOL))
+    out = dict(requests=n, positions=int(cu[-1]), ties=len(ties), mismatches=bad,
+               max_sumexp_rel=float(rel.max()) if R else 0.0, **stats_ok)
+    return out
+
+
+def assert_parity(batch, gpu: dict, ref: dict) -> dict:
+    r = compare(batch, gpu, ref)
+    assert not r["mismatches"], f"{len(r['mismatches'])} requests differ: {r['mismatches'][:5]}"
+    assert r["row_max"], "row max differs"
+    assert r["row_argmax"], "row argmax differs"
+    assert r["row_sumexp"], f"row sum of exponentials off by {r['max_sumexp_rel']:.3g} relative"
+    assert r["ties"] <= 1e-5 * max(r["positions"], 1), f"{r['ties']} counted ties"
+    return r
