@@ -165,6 +165,36 @@ int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk, int race_chunk
 /* Number of kernel launches one spec_verify_run makes for a non-empty batch. */
 int spec_verify_launches_per_run(void);
 
+/*
+ * Verification without any allocation, for callers that cannot allocate device memory: code
+ * that runs inside another framework's memory pool or a plugin's execute call, where
+ * cudaMalloc is forbidden or would synchronise the device at a bad moment, or processes whose
+ * device memory is fully reserved up front. This entry point has no counterpart on the pages:
+ * it is the same verification as spec_verify_run (same arguments, same results, the logits
+ * type and vocabulary size given directly instead of through a context), but its scratch
+ * space is a fixed static array inside the library (about 2.6 MB on every device that loads
+ * it, held until the process exits).
+ *   Limits: vocab_size <= SV_NOALLOC_MAX_VOCAB, num_reqs <= SV_NOALLOC_MAX_REQS, and
+ *   num_draft_tokens + num_reqs <= SV_NOALLOC_MAX_ROWS; larger batches return SV_ECAPACITY.
+ * It runs on the current device. Its first call on a device looks up the array's device
+ * address (once per device); make that first call before any stream capture. All calls on a
+ * device share the array, so calls that overlap on the GPU (different streams, or different
+ * host threads) race with each other and must be serialised by the caller. The device error
+ * word of spec_verify_last_error is not available here: an inconsistent cu_num_draft shows
+ * as num_sampled = num_rejected = 0 and a row of -1 for every request.
+ */
+#define SV_NOALLOC_MAX_REQS 1024
+#define SV_NOALLOC_MAX_ROWS 8192
+#define SV_NOALLOC_MAX_VOCAB 262144
+int spec_verify_run_noalloc(const void *logits, int logits_dtype, int vocab_size,
+                            const int32_t *draft_ids, const float *draft_probs,
+                            const int32_t *cu_num_draft, const float *temperature,
+                            const uint8_t *is_greedy, uint64_t seed, uint32_t req_index_base,
+                            int num_reqs, int num_draft_tokens, int max_spec_len_this_batch,
+                            int32_t *sampled, int32_t *num_sampled, int32_t *num_rejected,
+                            float *opt_row_max, float *opt_row_sumexp, int32_t *opt_row_argmax,
+                            void *cuda_stream);
+
 /* Release the context and its device memory. NULL is a no-op. */
 void spec_verify_free(spec_verify_ctx *ctx);
 

@@ -101,6 +101,8 @@ def lib():
                                   vp, vp, vp, vp]
     L.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp,
                                        vp, vp]
+    L.spec_verify_run_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32,
+                                          i32, vp, vp, vp, vp, vp, vp, vp]
     L.spec_verify_reserve_host_io.argtypes = [vp]
     L.spec_verify_last_error.argtypes = [vp, ctypes.POINTER(u32)]
     L.spec_verify_set_profiling.argtypes = [vp, i32]
@@ -111,7 +113,7 @@ def lib():
     L.spec_verify_free.restype = None
     L.spec_verify_status_string.argtypes = [i32]
     L.spec_verify_status_string.restype = ctypes.c_char_p
-    for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_host",
+    for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_host", "spec_verify_run_noalloc",
               "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
               "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
         getattr(L, f).restype = i32
@@ -188,6 +190,26 @@ def spec_verify_run_host(ctx, logits, draft_ids, draft_probs, cu_num_draft, temp
                                       max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled),
                                       _ptr(num_rejected), _stream_handle(cuda_stream)),
            "spec_verify_run_host")
+
+
+def spec_verify_run_noalloc(logits, logits_dtype, vocab_size, draft_ids, draft_probs,
+                            cu_num_draft, temperature, is_greedy, seed, req_index_base, num_reqs,
+                            num_draft_tokens, max_spec_len_this_batch, sampled, num_sampled,
+                            num_rejected, opt_row_max=None, opt_row_sumexp=None,
+                            opt_row_argmax=None, cuda_stream=None) -> None:
+    """Verification that allocates nothing (scratch in a static device array of the library,
+    limits SV_NOALLOC_MAX_*), for callers that cannot allocate device memory. Runs on the
+    current device; overlapping calls on one device race and must be serialised."""
+    _check(lib().spec_verify_run_noalloc(_ptr(logits), _dtype_code(logits_dtype)
+                                         if isinstance(logits_dtype, str) else logits_dtype,
+                                         vocab_size, _ptr(draft_ids), _ptr(draft_probs),
+                                         _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy),
+                                         seed, req_index_base, num_reqs, num_draft_tokens,
+                                         max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled),
+                                         _ptr(num_rejected), _ptr(opt_row_max),
+                                         _ptr(opt_row_sumexp), _ptr(opt_row_argmax),
+                                         _stream_handle(cuda_stream)),
+           "spec_verify_run_noalloc")
 
 
 def spec_verify_reserve_host_io(ctx) -> None:

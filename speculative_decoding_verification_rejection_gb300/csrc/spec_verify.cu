@@ -1059,3 +1059,125 @@ const char *spec_verify_status_string(int status)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// Entry point that allocates nothing: the scratch lives in a fixed-size static device array.
+// ---------------------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+
+constexpr int kNoAllocMaxReqs = SV_NOALLOC_MAX_REQS;
+constexpr int kNoAllocMaxRows = SV_NOALLOC_MAX_ROWS;
+constexpr int kNoAllocMaxVocab = SV_NOALLOC_MAX_VOCAB;
+constexpr int kNoAllocSplits1 = (kNoAllocMaxVocab + kDefaultStatsChunk - 1) / kDefaultStatsChunk;
+constexpr int kNoAllocSplits2 = (kNoAllocMaxVocab + kDefaultRaceChunk - 1) / kDefaultRaceChunk;
+
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+constexpr size_t kOffRowInfo = 0;
+constexpr size_t kOffRowStat = kOffRowInfo + align256(sizeof(RowInfo) * kNoAllocMaxRows);
+constexpr size_t kOffStatPart = kOffRowStat + align256(sizeof(RowStat) * kNoAllocMaxRows);
+constexpr size_t kOffCounters =
+    kOffStatPart + align256(sizeof(StatPart) * size_t(kNoAllocMaxRows) * kNoAllocSplits1);
+constexpr size_t kOffFlags =
+    kOffCounters + align256(sizeof(unsigned) * size_t(kNoAllocMaxRows + kNoAllocMaxReqs));
+constexpr size_t kOffReqInfo = kOffFlags + align256(2 * sizeof(unsigned));
+constexpr size_t kOffRacePart = kOffReqInfo + align256(sizeof(ReqInfo) * kNoAllocMaxReqs);
+constexpr size_t kNoAllocBytes =
+    kOffRacePart + align256(sizeof(RacePart) * size_t(kNoAllocMaxReqs) * kNoAllocSplits2);
+
+// One copy per device that loads this library, kept until the process exits. Every call of
+// spec_verify_run_noalloc on a device shares it.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void *g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Device address of the static scratch on the current device, looked up once per device
+// (the host-side name of the array is not a device address).
+int noalloc_base(int dev, void **out)
+{
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_base[dev]) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr) {
+            cudaGetLastError();
+            return SV_ECUDA;
+        }
+        g_noalloc_base[dev] = p;
+    }
+    *out = g_noalloc_base[dev];
+    return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int vocab_size,
+                                       const int32_t *draft_ids, const float *draft_probs,
+                                       const int32_t *cu_num_draft, const float *temperature,
+                                       const uint8_t *is_greedy, uint64_t seed,
+                                       uint32_t req_index_base, int num_reqs, int num_draft_tokens,
+                                       int max_spec_len_this_batch, int32_t *sampled,
+                                       int32_t *num_sampled, int32_t *num_rejected,
+                                       float *opt_row_max, float *opt_row_sumexp,
+                                       int32_t *opt_row_argmax, void *cuda_stream)
+{
+    if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
+    if (vocab_size <= 0 || num_reqs < 0 || num_draft_tokens < 0 || max_spec_len_this_batch < 0)
+        return SV_EINVAL;
+    if (vocab_size > kNoAllocMaxVocab || num_reqs > kNoAllocMaxReqs ||
+        static_cast<long long>(num_draft_tokens) + num_reqs > kNoAllocMaxRows ||
+        static_cast<long long>(num_draft_tokens) >
+            static_cast<long long>(num_reqs) * max_spec_len_this_batch)
+        return SV_ECAPACITY;
+    if (num_reqs == 0) return SV_OK;
+    if (!logits || !cu_num_draft || !temperature || !is_greedy || !sampled || !num_sampled ||
+        !num_rejected || (num_draft_tokens > 0 && !draft_ids))
+        return SV_EINVAL;
+    if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(draft_probs) % 16 != 0)
+        return SV_EINVAL;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return SV_EDEVICE;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3)
+        return SV_EDEVICE;
+    void *base = nullptr;
+    const int rc = noalloc_base(dev, &base);
+    if (rc != SV_OK) return rc;
+    auto *bytes = static_cast<unsigned char *>(base);
+
+    // A context on the host stack whose scratch pointers are carved from the static array.
+    spec_verify_ctx view;
+    view.device = dev;
+    view.max_num_reqs = kNoAllocMaxReqs;
+    view.max_spec_len = max_spec_len_this_batch;
+    view.V = vocab_size;
+    view.dtype = logits_dtype;
+    view.has_q = draft_probs != nullptr;
+    view.max_rows = kNoAllocMaxRows;
+    view.max_splits = kNoAllocSplits2;
+    view.rowinfo = reinterpret_cast<RowInfo *>(bytes + kOffRowInfo);
+    view.rowstat = reinterpret_cast<RowStat *>(bytes + kOffRowStat);
+    view.statpart = reinterpret_cast<StatPart *>(bytes + kOffStatPart);
+    view.counters = reinterpret_cast<unsigned *>(bytes + kOffCounters);
+    view.flags = reinterpret_cast<unsigned *>(bytes + kOffFlags);
+    view.reqinfo = reinterpret_cast<ReqInfo *>(bytes + kOffReqInfo);
+    view.racepart = reinterpret_cast<RacePart *>(bytes + kOffRacePart);
+    auto stream = static_cast<cudaStream_t>(cuda_stream);
+    if (logits_dtype == SV_BF16)
+        return launch_all<uint16_t>(&view, static_cast<const uint16_t *>(logits), draft_ids,
+                                    draft_probs, cu_num_draft, temperature, is_greedy, seed,
+                                    req_index_base, num_reqs, num_draft_tokens,
+                                    max_spec_len_this_batch, sampled, num_sampled, num_rejected,
+                                    opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
+    return launch_all<float>(&view, static_cast<const float *>(logits), draft_ids, draft_probs,
+                             cu_num_draft, temperature, is_greedy, seed, req_index_base, num_reqs,
+                             num_draft_tokens, max_spec_len_this_batch, sampled, num_sampled,
+                             num_rejected, opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
+}
