@@ -42,6 +42,8 @@ def parse_args():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", type=int, default=3)
+    p.add_argument("--num-reqs", type=int, default=None,
+                   help="only the first N requests of the workload (bounded cases for profiling)")
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--profile-steps", type=int, default=500)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -249,7 +251,7 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     sv.lib()
 
-    b = workloads.workload(args.workload)
+    b = workloads.workload(args.workload, num_reqs=args.num_reqs)
     dev = torch.device("cuda", local)
     logits_np = b.logits.view(np.int16) if b.logits.dtype == np.uint16 else b.logits
     d_logits = torch.from_numpy(logits_np).to(dev)

@@ -77,7 +77,9 @@ extern "C" {
 #define SV_BF16 1 /* bfloat16 (upper half of a binary32) */
 
 /* bits of the device error word */
-#define SV_ERR_BATCH 1u /* inconsistent cu_num_draft / draft lengths in some call */
+#define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
+#define SV_ERR_TIMEOUT 2u /* a kernel gave up waiting for its own staged copies (2 s bound); the
+                             outputs of that call are not valid */
 
 typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
 
@@ -151,15 +153,16 @@ int spec_verify_last_error(spec_verify_ctx *ctx, uint32_t *err_word);
 /*
  * Kernel timing. With enable != 0, each later spec_verify_run records CUDA events around its
  * kernels on the call's stream. spec_verify_get_profile waits for the recorded work and
- * returns, per kernel (0 = plan, 1 = row statistics, 2 = race and emit), the summed
- * milliseconds in ms[3] and the number of timed calls in *calls, then resets the sums.
+ * returns, per kernel (0 = plan, 1 = row statistics, 2 = row finalisation, 3 = race and emit),
+ * the summed milliseconds in ms[4] and the number of timed calls in *calls, then resets the sums.
  */
 int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable);
-int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[3], int64_t *calls);
+int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[4], int64_t *calls);
 
-/* Launch-shape knobs (elements per CTA of the statistics and race kernels; 0 keeps the
- * current value). Values are rounded up to a multiple of 8 and clamped to the context's
- * scratch capacity. Results do not depend on them. */
+/* Launch-shape knobs: elements per CTA of the statistics and race kernels (0 keeps the
+ * current value; -1 restores the default, automatic: the flattened logits, or the raced rows,
+ * split evenly over a grid sized in whole waves of CTAs). Values are rounded up to a multiple
+ * of 8 and kept at or above 2048. Results do not depend on them. */
 int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk, int race_chunk);
 
 /* Number of kernel launches one spec_verify_run makes for a non-empty batch. */
@@ -172,7 +175,7 @@ int spec_verify_launches_per_run(void);
  * device memory is fully reserved up front. This entry point has no counterpart on the pages:
  * it is the same verification as spec_verify_run (same arguments, same results, the logits
  * type and vocabulary size given directly instead of through a context), but its scratch
- * space is a fixed static array inside the library (about 2.6 MB on every device that loads
+ * space is a fixed static array inside the library (about 2.8 MB on every device that loads
  * it, held until the process exits).
  *   Limits: vocab_size <= SV_NOALLOC_MAX_VOCAB, num_reqs <= SV_NOALLOC_MAX_REQS, and
  *   num_draft_tokens + num_reqs <= SV_NOALLOC_MAX_ROWS; larger batches return SV_ECAPACITY.

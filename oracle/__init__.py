@@ -67,8 +67,8 @@ def lib():
         for f in ("spec_verify_ref_exp_n", "spec_verify_ref_log_n"):
             getattr(L, f).argtypes = [vp, vp, ctypes.c_int64]
             getattr(L, f).restype = None
-        L.spec_verify_ref_race_uniforms.argtypes = [u64, u32, u32, i32, vp]
-        L.spec_verify_ref_race_uniforms.restype = None
+        L.spec_verify_ref_race_clocks.argtypes = [u64, u32, u32, i32, vp]
+        L.spec_verify_ref_race_clocks.restype = None
         _lib = L
     return _lib
 
@@ -115,9 +115,10 @@ def log32_n(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def race_uniforms(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
+def race_clocks(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
+    """Race clocks E_v (binary32) of tokens 0..n-1 of (request ireq, position j)."""
     out = np.empty(n, dtype=np.float32)
-    lib().spec_verify_ref_race_uniforms(seed, j, ireq, n, _p(out))
+    lib().spec_verify_ref_race_clocks(seed, j, ireq, n, _p(out))
     return out
 
 

@@ -20,10 +20,15 @@
  *   - p = softmax(logits / T) with x_v = logit_v * (1/T) in binary32; T <= 0 (or a set greedy
  *     flag) means greedy verification.
  *   - Acceptance test p(d)/q(d) >= u with u in (0,1); q(d) = 1 without draft probabilities.
- *   - Every random draw is keyed: Philox4x32-10, key = seed, counter = (v>>2, j, request, tag),
- *     word v&3; tag 0 = acceptance uniform (v = 0), tag 1 = race exponentials.
+ *   - Every random draw is keyed: Philox4x32-10, key = seed, counter words (c0, j, request,
+ *     c3). The acceptance uniform of position j is word 0 of counter (0, j, request, 0).
  *   - Sampling from a distribution proportional to w_v is the exponential race
- *     argmax_v (log w_v - log E_v), E_v = -log U_v, lowest index on equal keys.
+ *     argmax_v (log w_v - log E_v) over i.i.d. Exp(1) clocks E_v, lowest index on equal keys.
+ *     The clocks come in blocks of 16 tokens (block g = v >> 4, slot s = v & 15): counter
+ *     (g, j, request, 8) gives W (word 0) and the slot a = word 1 & 15 holding the block's
+ *     smallest clock E_min = -log(W) / 16; the other slots' clocks are E_min + (-log U_s), U_s
+ *     word s & 3 of counter (g, j, request, 9 + s / 4). By the memoryless property of the
+ *     exponential these 16 clocks are i.i.d. Exp(1).
  *   - The residual weight is rr_v = fma(-S, q_v, t_v) with t_v = exp(x_v - m), i.e.
  *     S * (p_v - q_v) rounded once; the constant log S is left out of the keys.
  *   - exp and log inside every decision are the binary32 functions below (Cody-Waite
@@ -35,8 +40,8 @@
 #include <stdint.h>
 #include <string.h>
 
-#define REF_TAG_ACCEPT 0u
-#define REF_TAG_RACE 1u
+#define REF_TAG_ACCEPT 0u  /* counter word 3 of the acceptance uniform */
+#define REF_CLOCK_HEAD 8u  /* counter word 3 of a block's head call; its slot calls use 9..12 */
 
 /* ------------------------------------------------------------------------------------ */
 /* Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
@@ -150,6 +155,26 @@ float spec_verify_ref_log(float x)
     return fmaf(kf, REF_LN2_HI, fmaf(kf, REF_LN2_LO, lnf));
 }
 
+/* Race clock of token v at position j of request ireq (see the header): i.i.d. Exp(1). */
+float spec_verify_ref_race_clock(uint64_t seed, uint32_t j, uint32_t ireq, int32_t v)
+{
+    const uint32_t g = (uint32_t)v >> 4;
+    const uint32_t slot = (uint32_t)v & 15u;
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t ctr[4] = {g, j, ireq, REF_CLOCK_HEAD};
+    uint32_t head[4];
+    spec_verify_ref_philox(ctr, key, head);
+    const float W = spec_verify_ref_uniform_from_word(head[0]);
+    const uint32_t a = head[1] & 15u;
+    const float emin = -spec_verify_ref_log(W) * 0.0625f; /* E_W / 16, exact scaling */
+    if (slot == a) return emin;
+    ctr[3] = REF_CLOCK_HEAD + 1u + slot / 4u;
+    uint32_t words[4];
+    spec_verify_ref_philox(ctr, key, words);
+    const float U = spec_verify_ref_uniform_from_word(words[slot & 3u]);
+    return emin + (-spec_verify_ref_log(U));
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* The verification step.                                                                */
 /* ------------------------------------------------------------------------------------ */
@@ -225,7 +250,8 @@ static inline void race_offer(race_t *r, float key, int32_t v, float *second)
 
 /* Exponential race over one row at position j of request ireq, [spec-notes] NO_DRAFT_PROBS
  * answer (argmax(prob / q) with q ~ Exp(1) needs no normalisation) and [spec-in-vllm] 7.3
- * (Gumbel argmax). Keys are taken in log form: key_v = log w_v - log E_v.
+ * (Gumbel argmax). Keys are taken in log form: key_v = log w_v - log E_v, E_v the token's race
+ * clock.
  *   q == NULL : w_v proportional to p_v; key_v = x_v - log E_v; token `exclude` is left out
  *               (the rejected draft token when there are no draft probabilities).
  *   q != NULL : residual weights rr_v = fma(-S, q_v, t_v) = S (p_v - q_v) rounded once,
@@ -249,8 +275,7 @@ static race_t race_row(const void *logits, int bf16, size_t row, int V, float in
         } else {
             logw = x;
         }
-        float U = spec_verify_ref_uniform(seed, (uint32_t)v >> 2, j, ireq, REF_TAG_RACE, v & 3);
-        float E = -spec_verify_ref_log(U);
+        float E = spec_verify_ref_race_clock(seed, j, ireq, v);
         float key = logw - spec_verify_ref_log(E);
         race_offer(&r, key, v, &second);
     }
@@ -443,9 +468,8 @@ void spec_verify_ref_log_n(const float *in, float *out, int64_t n)
     for (int64_t k = 0; k < n; ++k) out[k] = spec_verify_ref_log(in[k]);
 }
 
-/* Uniforms of the race for positions v in [0, n) of (request ireq, position j). */
-void spec_verify_ref_race_uniforms(uint64_t seed, uint32_t j, uint32_t ireq, int32_t n, float *out)
+/* Race clocks of tokens v in [0, n) of (request ireq, position j). */
+void spec_verify_ref_race_clocks(uint64_t seed, uint32_t j, uint32_t ireq, int32_t n, float *out)
 {
-    for (int32_t v = 0; v < n; ++v)
-        out[v] = spec_verify_ref_uniform(seed, (uint32_t)v >> 2, j, ireq, REF_TAG_RACE, v & 3);
+    for (int32_t v = 0; v < n; ++v) out[v] = spec_verify_ref_race_clock(seed, j, ireq, v);
 }

@@ -29,7 +29,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 SV_OK, SV_EINVAL, SV_ECAPACITY, SV_EDTYPE, SV_ECUDA, SV_EDEVICE = 0, -1, -2, -3, -4, -5
 SV_F32, SV_BF16 = 0, 1
 SV_ERR_BATCH = 1
-KERNELS = ("plan", "stats", "race")
+KERNELS = ("plan", "stats", "finalize", "race")
 
 _lib = None
 
@@ -227,7 +227,7 @@ def spec_verify_set_profiling(ctx, enable: bool) -> None:
 
 
 def spec_verify_get_profile(ctx):
-    ms = (ctypes.c_double * 3)()
+    ms = (ctypes.c_double * len(KERNELS))()
     calls = ctypes.c_int64()
     _check(lib().spec_verify_get_profile(ctx, ms, ctypes.byref(calls)), "spec_verify_get_profile")
     return dict(zip(KERNELS, list(ms))), calls.value

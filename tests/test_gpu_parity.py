@@ -51,6 +51,8 @@ CUSTOM = [
     (6, 65536, [2, 5, 3, 0, 1, 4, 2, 3], "f32", "indep"),
     (7, 7, [3, 1, 0, 2], "f32", "noisy"),                  # tiny vocabulary
     (8, 129, [8, 0, 1], "bf16", "indep"),
+    (9, 4004, [2, 4, 0, 3, 1], "bf16", "noisy"),          # V % 8 == 4: bf16 rows 8-byte aligned
+    (10, 2052, [5, 5, 5, 5, 5, 5, 5, 5], "f32", "noisy"),  # rows a little above the minimum chunk
 ]
 
 

@@ -126,7 +126,7 @@ def test_sharding_by_requests_with_index_base_reproduces_the_batch():
 
 
 def test_race_winner_brute_force():
-    """Recompute every race key in float64 from the uniforms of (request, position) and compare
+    """Recompute every race key in float64 from the race clocks of (request, position) and compare
     the winner. Races run at positions 0..2 of the second request of a batch, with a request
     index base, so the counter's position and request words are both exercised."""
     rng = np.random.default_rng(17)
@@ -156,8 +156,8 @@ def test_race_winner_brute_force():
         invT = np.float32(1.0) / np.float32(T)
         row = cu[1] + 1 + js
         x = (logits[row] * invT).astype(np.float64)
-        U = oracle.race_uniforms(seed, js, base + 1, V).astype(np.float64)
-        g = -np.log(-np.log(U))
+        clocks = oracle.race_clocks(seed, js, base + 1, V).astype(np.float64)
+        g = -np.log(clocks)
         if mode == 1:
             p = np.exp(x - x.max()) / np.exp(x - x.max()).sum()
             w = np.maximum(p - q[cu[1] + js].astype(np.float64), 0)

@@ -85,16 +85,28 @@ def test_philox_matches_triton_library(tmp_path):
         np.testing.assert_array_equal(got, want, err_msg=f"seed {s:#x}")
 
 
-def test_race_counter_layout_matches_triton(tmp_path):
-    """The race's uniforms for (request i, position j, token v) come from counter
-    (v >> 2, j, i, tag 1), word v & 3, key = seed."""
-    seed, j, i, n = 0xDEADBEEF12345, 3, 17, 64
-    ctr = np.array([[c, j, i, 1] for c in range(n // 4)], dtype=np.uint32)
+def _u(w):
+    return ((np.asarray(w, np.uint64) >> 9).astype(np.float64) + 0.5) * 2.0**-23
+
+
+def test_race_clock_layout_matches_triton(tmp_path):
+    """The race clock of token v (block g = v >> 4, slot s = v & 15) at (request i, position j):
+    counter (g, j, i, 8) gives W (word 0) and the argmin slot a (word 1 & 15); E_min = -ln(W)/16;
+    slot s != a adds -ln U_s, U_s word s & 3 of counter (g, j, i, 9 + s // 4)."""
+    seed, j, i, nblk = 0xDEADBEEF12345, 3, 17, 12
+    ctr = np.array([[g, j, i, 8 + k] for g in range(nblk) for k in range(5)], dtype=np.uint32)
     pad = np.zeros((64 - ctr.shape[0], 4), dtype=np.uint32)
-    words = _triton_philox([(seed, np.vstack([ctr, pad]))], tmp_path)[0][: n // 4].reshape(-1)
-    want = ((words >> 9).astype(np.float32) + np.float32(0.5)) * np.float32(2.0**-23)
-    got = oracle.race_uniforms(seed, j, i, n)
-    np.testing.assert_array_equal(got, want)
+    words = _triton_philox([(seed, np.vstack([ctr, pad]))], tmp_path)[0][: ctr.shape[0]]
+    want = np.empty(16 * nblk)
+    for g in range(nblk):
+        head = words[5 * g]
+        emin = -np.log(_u(head[0])) / 16.0
+        a = int(head[1]) & 15
+        for s_ in range(16):
+            v = 16 * g + s_
+            want[v] = emin if s_ == a else emin - np.log(_u(words[5 * g + 1 + s_ // 4][s_ % 4]))
+    got = oracle.race_clocks(seed, j, i, 16 * nblk).astype(np.float64)
+    np.testing.assert_allclose(got, want, rtol=2e-6)
 
 
 def test_uniform_map_extremes_and_exactness():
@@ -110,10 +122,28 @@ def test_uniform_map_extremes_and_exactness():
 
 
 def test_uniforms_are_uniform_and_uncorrelated():
-    u = oracle.race_uniforms(99, 0, 0, 400_000).astype(np.float64)
-    counts, _ = np.histogram(u, bins=200, range=(0, 1))
+    u = np.array([oracle.uniform(99, c, 0, 0, 0, w) for c in range(25_000) for w in range(4)])
+    counts, _ = np.histogram(u, bins=100, range=(0, 1))
     assert stats.chisquare(counts).pvalue > 1e-3
-    assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.01          # neighbours (same Philox call)
-    a = oracle.race_uniforms(99, 0, 1, 100_000).astype(np.float64)  # another request
-    assert abs(np.corrcoef(u[:100_000], a)[0, 1]) < 0.02
     assert stats.kstest(u, "uniform").pvalue > 1e-3
+    assert abs(np.corrcoef(u[:-1], u[1:])[0, 1]) < 0.02        # words of one call and neighbours
+    v = np.array([oracle.uniform(99, c, 0, 1, 0, 0) for c in range(25_000)])  # another request
+    assert abs(np.corrcoef(u[::4], v)[0, 1]) < 0.03
+
+
+def test_race_clocks_are_iid_exponential():
+    """The block construction (minimum of 16 and memoryless excesses) must give i.i.d. Exp(1)
+    clocks: the marginal of every slot, the argmin slot uniform, no correlation in a block."""
+    n = 16 * 40_000
+    e = oracle.race_clocks(2024, 1, 5, n).astype(np.float64)
+    assert stats.kstest(e, "expon").pvalue > 1e-3
+    blocks = e.reshape(-1, 16)
+    for s_ in (0, 5, 15):
+        assert stats.kstest(blocks[:, s_], "expon").pvalue > 1e-3
+    argmin = np.bincount(blocks.argmin(axis=1), minlength=16)
+    assert stats.chisquare(argmin).pvalue > 1e-3
+    assert stats.kstest(blocks.min(axis=1) * 16, "expon").pvalue > 1e-3   # min of 16 ~ Exp(16)
+    c = np.corrcoef(blocks[:, 2], blocks[:, 9])[0, 1]
+    assert abs(c) < 0.02
+    other = oracle.race_clocks(2024, 2, 5, 16 * 5000).astype(np.float64)  # another position
+    assert abs(np.corrcoef(e[: other.size], other)[0, 1]) < 0.03
