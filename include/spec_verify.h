@@ -33,12 +33,18 @@
  *     !(T > 0). Greedy argmax is over the raw logits, lowest index on ties.
  *   - Random draws are keyed, so results are reproducible and independent of launch shape:
  *     Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed), hi32(seed)), counter =
- *     (v >> 2, j, req_index_base + i, tag), word v & 3, uniform U = ((w >> 9) + 1/2) / 2^23.
- *     tag 0 (v = 0): acceptance uniform u; tag 1: race exponentials E_v = -log U_v.
- *   - A draw from weights w_v is the exponential race argmax_v (log w_v - log E_v), lowest
- *     index on equal keys. Residual weights are rr_v = fma(-S, q_v, exp(x_v - m)) (S times
- *     p_v - q_v, rounded once), candidates rr_v > 0; if none is left after rounding, the token
- *     is drawn from p. Without draft probabilities the rejected draft token is removed.
+ *     (c0, j, req_index_base + i, tag), uniform U = ((w >> 9) + 1/2) / 2^23 of a 32-bit word w.
+ *     The acceptance uniform u of position j is word 0 of counter (0, j, i', 0).
+ *   - A draw from weights w_v is the exponential race argmax_v (log w_v - log E_v) over i.i.d.
+ *     Exp(1) clocks E_v, lowest index on equal keys. The clocks come in groups of 64 tokens
+ *     (g = v >> 6, slot s = v & 63): counter (g, j, i', 8) gives W (word 0) and the slot
+ *     a = word 1 & 63 that holds the group's smallest clock E_g = -log(W) / 64; slot s != a has
+ *     clock E_g + (-log U_s), U_s word s & 3 of counter (g, j, i', 9 + s / 4). (By the
+ *     memoryless property these are i.i.d. Exp(1); E_g bounds every key of the group, which
+ *     lets the race skip whole groups.) Keys over p are x_v - log E_v. Residual weights are
+ *     rr_v = fma(-S, q_v, exp(x_v - m)) (S times p_v - q_v, rounded once), candidates rr_v > 0,
+ *     keys log rr_v - log E_v; if no candidate is left after rounding, the token is drawn from
+ *     p. Without draft probabilities the rejected draft token is removed.
  *   - Acceptance: 0 <= d < V and q(d) > 0 and p(d) / q(d) >= u (binary32), q(d) = 1 without
  *     draft probabilities. An out-of-range draft id is rejected, not an error.
  *   - exp / log inside these decisions are fixed binary32 functions (Cody-Waite reduction
@@ -78,8 +84,6 @@ extern "C" {
 
 /* bits of the device error word */
 #define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
-#define SV_ERR_TIMEOUT 2u /* a kernel gave up waiting for its own staged copies (2 s bound); the
-                             outputs of that call are not valid */
 
 typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
 
@@ -88,8 +92,10 @@ typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
  * at most max_spec_len draft tokens each, vocabulary size vocab_size and logits of type
  * logits_dtype (SV_F32 / SV_BF16). has_draft_probs = 0 promises that draft_probs is always
  * NULL (only the host-buffer entry point sizes anything by it).
- * The context owns its device scratch (per-row statistics, per-split partials, counters),
+ * The context owns its device scratch (the per-segment partial statistics and an error word),
  * allocated here once; spec_verify_run allocates nothing. Free with spec_verify_free.
+ * Returns SV_ECAPACITY when the race's per-group bounds of one row (about 12 bytes per 64
+ * tokens) do not fit in one CTA's shared memory (vocab_size above about a million).
  * Returns SV_OK and *out, or an error with *out = NULL.
  */
 int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, int vocab_size,
@@ -112,7 +118,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
  *   opt_row_max, opt_row_sumexp [num_draft_tokens + num_reqs] binary32, opt_row_argmax int32:
  *                 optional (NULL to skip) per-row m = max_v x_v, S = sum_v exp(x_v - m) and the
  *                 raw-logit argmax, for every row including rows after a rejection (greedy rows
- *                 use T = 1 for m and S).
+ *                 use T = 1 for m and S); not written when the batch is inconsistent.
  * The call performs no allocation and no host synchronisation and may be captured in a CUDA
  * graph. Calls on one context must not overlap on the device (they share its scratch).
  */
@@ -153,17 +159,18 @@ int spec_verify_last_error(spec_verify_ctx *ctx, uint32_t *err_word);
 /*
  * Kernel timing. With enable != 0, each later spec_verify_run records CUDA events around its
  * kernels on the call's stream. spec_verify_get_profile waits for the recorded work and
- * returns, per kernel (0 = plan, 1 = row statistics, 2 = row finalisation, 3 = race and emit),
- * the summed milliseconds in ms[4] and the number of timed calls in *calls, then resets the sums.
+ * returns, per kernel (0 = row statistics, 1 = verify: acceptance, race and emit), the summed
+ * milliseconds in ms[0..1] (ms holds spec_verify_launches_per_run() entries) and the number of
+ * timed calls in *calls, then resets the sums.
  */
 int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable);
-int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[4], int64_t *calls);
+int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls);
 
-/* Launch-shape knobs: elements per CTA of the statistics and race kernels (0 keeps the
- * current value; -1 restores the default, automatic: the flattened logits, or the raced rows,
- * split evenly over a grid sized in whole waves of CTAs). Values are rounded up to a multiple
- * of 8 and kept at or above 2048. Results do not depend on them. */
-int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk, int race_chunk);
+/* Launch-shape knob: elements per CTA of the statistics kernel (0 keeps the current value; -1
+ * restores the default, automatic: the flattened logits split evenly over a grid sized in whole
+ * waves of CTAs). Values are rounded up to a multiple of 8 and kept at or above 2048. Results do
+ * not depend on it (S, a sum, up to rounding). */
+int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk);
 
 /* Number of kernel launches one spec_verify_run makes for a non-empty batch. */
 int spec_verify_launches_per_run(void);
@@ -175,7 +182,7 @@ int spec_verify_launches_per_run(void);
  * device memory is fully reserved up front. This entry point has no counterpart on the pages:
  * it is the same verification as spec_verify_run (same arguments, same results, the logits
  * type and vocabulary size given directly instead of through a context), but its scratch
- * space is a fixed static array inside the library (about 2.8 MB on every device that loads
+ * space is a fixed static array inside the library (about 2.2 MB on every device that loads
  * it, held until the process exits).
  *   Limits: vocab_size <= SV_NOALLOC_MAX_VOCAB, num_reqs <= SV_NOALLOC_MAX_REQS, and
  *   num_draft_tokens + num_reqs <= SV_NOALLOC_MAX_ROWS; larger batches return SV_ECAPACITY.

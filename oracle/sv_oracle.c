@@ -24,11 +24,11 @@
  *     c3). The acceptance uniform of position j is word 0 of counter (0, j, request, 0).
  *   - Sampling from a distribution proportional to w_v is the exponential race
  *     argmax_v (log w_v - log E_v) over i.i.d. Exp(1) clocks E_v, lowest index on equal keys.
- *     The clocks come in blocks of 16 tokens (block g = v >> 4, slot s = v & 15): counter
- *     (g, j, request, 8) gives W (word 0) and the slot a = word 1 & 15 holding the block's
- *     smallest clock E_min = -log(W) / 16; the other slots' clocks are E_min + (-log U_s), U_s
+ *     The clocks come in groups of 64 tokens (group g = v >> 6, slot s = v & 63): counter
+ *     (g, j, request, 8) gives W (word 0) and the slot a = word 1 & 63 holding the group's
+ *     smallest clock E_min = -log(W) / 64; the other slots' clocks are E_min + (-log U_s), U_s
  *     word s & 3 of counter (g, j, request, 9 + s / 4). By the memoryless property of the
- *     exponential these 16 clocks are i.i.d. Exp(1).
+ *     exponential these 64 clocks are i.i.d. Exp(1).
  *   - The residual weight is rr_v = fma(-S, q_v, t_v) with t_v = exp(x_v - m), i.e.
  *     S * (p_v - q_v) rounded once; the constant log S is left out of the keys.
  *   - exp and log inside every decision are the binary32 functions below (Cody-Waite
@@ -41,7 +41,7 @@
 #include <string.h>
 
 #define REF_TAG_ACCEPT 0u  /* counter word 3 of the acceptance uniform */
-#define REF_CLOCK_HEAD 8u  /* counter word 3 of a block's head call; its slot calls use 9..12 */
+#define REF_CLOCK_HEAD 8u  /* counter word 3 of a group's head call; its slot calls use 9..24 */
 
 /* ------------------------------------------------------------------------------------ */
 /* Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
@@ -158,15 +158,15 @@ float spec_verify_ref_log(float x)
 /* Race clock of token v at position j of request ireq (see the header): i.i.d. Exp(1). */
 float spec_verify_ref_race_clock(uint64_t seed, uint32_t j, uint32_t ireq, int32_t v)
 {
-    const uint32_t g = (uint32_t)v >> 4;
-    const uint32_t slot = (uint32_t)v & 15u;
+    const uint32_t g = (uint32_t)v >> 6;
+    const uint32_t slot = (uint32_t)v & 63u;
     uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
     uint32_t ctr[4] = {g, j, ireq, REF_CLOCK_HEAD};
     uint32_t head[4];
     spec_verify_ref_philox(ctr, key, head);
     const float W = spec_verify_ref_uniform_from_word(head[0]);
-    const uint32_t a = head[1] & 15u;
-    const float emin = -spec_verify_ref_log(W) * 0.0625f; /* E_W / 16, exact scaling */
+    const uint32_t a = head[1] & 63u;
+    const float emin = -spec_verify_ref_log(W) * 0.015625f; /* E_W / 64, exact scaling */
     if (slot == a) return emin;
     ctr[3] = REF_CLOCK_HEAD + 1u + slot / 4u;
     uint32_t words[4];

@@ -29,7 +29,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 SV_OK, SV_EINVAL, SV_ECAPACITY, SV_EDTYPE, SV_ECUDA, SV_EDEVICE = 0, -1, -2, -3, -4, -5
 SV_F32, SV_BF16 = 0, 1
 SV_ERR_BATCH = 1
-KERNELS = ("plan", "stats", "finalize", "race")
+KERNELS = ("stats", "verify")
 
 _lib = None
 
@@ -107,7 +107,7 @@ def lib():
     L.spec_verify_last_error.argtypes = [vp, ctypes.POINTER(u32)]
     L.spec_verify_set_profiling.argtypes = [vp, i32]
     L.spec_verify_get_profile.argtypes = [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(i64)]
-    L.spec_verify_set_chunks.argtypes = [vp, i32, i32]
+    L.spec_verify_set_chunks.argtypes = [vp, i32]
     L.spec_verify_launches_per_run.argtypes = []
     L.spec_verify_free.argtypes = [vp]
     L.spec_verify_free.restype = None
@@ -233,8 +233,8 @@ def spec_verify_get_profile(ctx):
     return dict(zip(KERNELS, list(ms))), calls.value
 
 
-def spec_verify_set_chunks(ctx, stats_chunk: int = 0, race_chunk: int = 0) -> None:
-    _check(lib().spec_verify_set_chunks(ctx, stats_chunk, race_chunk), "spec_verify_set_chunks")
+def spec_verify_set_chunks(ctx, stats_chunk: int = 0) -> None:
+    _check(lib().spec_verify_set_chunks(ctx, stats_chunk), "spec_verify_set_chunks")
 
 
 def spec_verify_launches_per_run() -> int:
@@ -323,8 +323,8 @@ class SpecVerify:
     def get_profile(self):
         return spec_verify_get_profile(self.ctx)
 
-    def set_chunks(self, stats_chunk: int = 0, race_chunk: int = 0) -> None:
-        spec_verify_set_chunks(self.ctx, stats_chunk, race_chunk)
+    def set_chunks(self, stats_chunk: int = 0) -> None:
+        spec_verify_set_chunks(self.ctx, stats_chunk)
 
     def close(self) -> None:
         if self.ctx:

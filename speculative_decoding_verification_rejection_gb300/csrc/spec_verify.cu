@@ -1,26 +1,31 @@
 // GB300 (sm_103a) implementation of the speculative-decoding verification sampler behind the
 // C ABI declared in include/spec_verify.h.
 //
-// One call = four kernels on the caller's stream, no allocation, no host synchronisation:
-//   1. plan  (1 CTA)    validate cu_num_draft, map every logit row to (request, j), list the
-//                       sampling (non-greedy) requests, clear the cross-CTA counters.
-//   2. stats (4 waves)  stream every logit once, the flattened [rows x V] array split evenly
-//                       over the CTAs, one partial (max, sum of exp, argmax) per row segment
-//                       ([spec-in-vllm] 7.4 block stats).
-//   3. finalize (warp per row) combine a row's partials: m = max x, S = sum exp(x - m), raw
-//                       argmax; run the row's acceptance test ([spec-notes] 8.3 and the
-//                       NO_DRAFT_PROBS answer code); the warp that completes a request's last row
-//                       finds the first rejection j* ([MTP-eagle] _rejection_sample_kernel),
-//                       emits greedy requests outright and records for sampling requests which
-//                       row to race.
-//   4. race  (2 waves)  the raced rows -- one per sampling request -- concatenated and split
-//                       evenly over the CTAs: the exponential race over the residual
-//                       max(0, p - q), over p without the rejected draft, or over p for the bonus
-//                       / non-speculative draw ([spec-notes] residual and NO_DRAFT_PROBS answers,
-//                       [spec-in-vllm] 7.3); the CTA that completes a request's race emits
-//                       sampled / num_sampled / num_rejected.
-// Only the emitted row of a request is raced: a residual that is never emitted cannot change
-// any output, so its logits and q row are never read twice.
+// One call = two kernels on the caller's stream, no allocation, no host synchronisation:
+//   1. stats  (whole waves)      stream every logit once, the flattened [rows x V] array split
+//                                evenly over the CTAs; each CTA looks its rows' requests up in
+//                                cu_num_draft (for the temperature) and writes one partial
+//                                (max, sum of exp, argmax) per row segment ([spec-in-vllm] 7.4
+//                                block stats).
+//   2. verify (CTA per request)  validate cu_num_draft; combine each row's partials into
+//                                m = max x, S = sum exp(x - m) and the raw argmax; test every
+//                                draft ([spec-notes] 8.3 and the NO_DRAFT_PROBS answer code);
+//                                find the first rejection j* ([MTP-eagle]
+//                                _rejection_sample_kernel); emit the argmax there for a greedy
+//                                request, or draw the token at j* for a sampling request by the
+//                                exponential race over the residual max(0, p - q), over p without
+//                                the rejected draft, or over p for the bonus draw ([spec-notes]
+//                                residual and NO_DRAFT_PROBS answers, [spec-in-vllm] 7.3).
+//
+// The race is a best-first search, not a scan. A row's race clocks come in groups of 64 tokens
+// whose head Philox call gives the group's smallest clock E_g, so no key in group g exceeds
+// max_{v in g} x_v - log E_g (a race over p; the residual weight is at most exp(x - m), so its
+// keys are at most that minus m). The verify CTA takes the largest logit of every 64-element
+// line of the raced row, bounds every group with one Philox call, evaluates first the groups
+// with the best bounds and then only the groups whose bound still reaches the best key found --
+// a few dozen of the V / 64 groups on typical rows. Only exact keys decide, so the winner is the
+// argmax over all tokens, as a full scan would find it; only the raced row's logits and the q
+// entries of evaluated groups are read.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -36,56 +41,20 @@
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kPlanThreads = 1024;
-constexpr int kMinChunk = 2048;     // smallest elements per CTA (bounds the partial buffers)
-constexpr int kStatsWaves = 4;      // automatic statistics grid: this many full waves of CTAs
-constexpr int kRaceWaves = 2;       // automatic race grid
-constexpr int kFixedChunk = 16384;  // chunk of the static-scratch entry point (both kernels)
+constexpr int kThreads = 256;       // both kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kMinChunk = 2048;     // smallest elements per statistics CTA (bounds the partials)
+constexpr int kStatsWaves = 2;      // automatic statistics grid: this many full waves of CTAs
+constexpr int kFixedChunk = 16384;  // statistics chunk of the static-scratch entry point
+constexpr int kGroup = 64;          // tokens per race-clock group = elements per line
 constexpr float kLog2e = 0x1.715476p+0f;
 constexpr float kInf = __builtin_huge_valf();
-
-enum : int32_t { kFlagGreedy = 1, kFlagBonus = 2, kFlagKShift = 8 };  // flags = g | b | K << 8
-
-struct __align__(16) RowInfo {
-    int32_t req;    // request index within the call
-    int32_t j;      // position, K = bonus
-    int32_t flags;  // kFlagGreedy | kFlagBonus | K << kFlagKShift
-    float invT;     // 1 / T (1 for greedy rows)
-};
-
-struct __align__(16) RowStat {
-    float m;          // max_v x_v
-    float S;          // sum_v exp(x_v - m)
-    int32_t amax;     // raw-logit argmax, lowest index
-    int32_t acc;      // acceptance of the row's draft (bonus rows: 1)
-    uint32_t seed_p;  // race key of the argmax token in a race over p (encoded), for screening
-    uint32_t seed_r;  // its key in the residual race (encoded; none on bonus rows or if rr <= 0)
-    uint32_t pad[2];
-};
-
-struct __align__(16) ReqState {  // what the race of a sampling request needs
-    int32_t jstar;   // first rejected position (K if every draft was accepted)
-    int32_t K;
-    int32_t q0;      // cu_num_draft[i]
-    int32_t row;     // the raced logit row
-    float m, S, invT;
-    uint32_t seed;   // screening seed of the race (encoded key)
-    uint32_t seed_p; // seed of a race over p on the same row (the empty-residual fallback)
-    int32_t excl;    // token removed from the race (the rejected draft without q), else -1
-    int32_t pad[2];
-};
 
 struct __align__(16) StatPart {
     float L;       // max raw logit of the segment
     float s;       // sum of 2^((l - L) c) over the segment
     int32_t idx;   // lowest index of L
     int32_t pad;
-};
-
-struct __align__(8) RacePart {
-    float key;
-    int32_t idx;   // -1: no candidate
 };
 
 // ---------------------------------------------------------------------------------------
@@ -110,7 +79,9 @@ __device__ __forceinline__ uint4 ldg_v4(const void *p)
 // ---------------------------------------------------------------------------------------
 // race keys
 // ---------------------------------------------------------------------------------------
-// Keys as order-preserving unsigned integers, so that atomicMax can share a threshold.
+// Keys as order-preserving unsigned integers. A candidate is packed as (key, ~v) into 64 bits,
+// so that the largest packed value is the largest key with the lowest index among equal keys;
+// 0 means no candidate (every finite or infinite key encodes above 0).
 __device__ __forceinline__ unsigned key_enc(float f)
 {
     const unsigned b = __float_as_uint(f);
@@ -120,50 +91,27 @@ __device__ __forceinline__ float key_dec(unsigned e)
 {
     return __uint_as_float((e & 0x80000000u) ? (e & 0x7FFFFFFFu) : ~e);
 }
-constexpr unsigned kKeyNone = 0x007FFFFFu;  // key_enc(-inf): no threshold yet
-
-// Full key of a token (the definition, bit for bit): over p, x - log E; over the residual,
-// log(fma(-S, q, exp(x - m))) - log E; E the token's race clock. Returns false if the token is
-// not a candidate (residual weight <= 0).
-template <bool kResidual>
-__device__ __forceinline__ bool race_key(float x, float qv, float E, float m, float S, float &key)
+__device__ __forceinline__ unsigned long long pack_key(float key, int v)
 {
-    if constexpr (kResidual) {
-        const float t = sv::exp_f32(__fsub_rn(x, m));
-        const float rr = __fmaf_rn(-S, qv, t);
-        if (!(rr > 0.0f)) return false;
-        key = __fsub_rn(sv::log_f32(rr), sv::log_f32(E));
-    } else {
-        key = __fsub_rn(x, sv::log_f32(E));
-    }
-    return true;
+    return (static_cast<unsigned long long>(key_enc(key)) << 32) |
+           static_cast<unsigned>(~static_cast<unsigned>(v));
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long p)
+{
+    const unsigned hi = static_cast<unsigned>(p >> 32);
+    const unsigned mh = __reduce_max_sync(0xFFFFFFFFu, hi);
+    const unsigned ml = __reduce_max_sync(0xFFFFFFFFu, hi == mh ? static_cast<unsigned>(p) : 0u);
+    return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
-__device__ __forceinline__ uint32_t pick_word(const sv::Philox4 &r, int k)
-{
-    return (k & 2) ? ((k & 1) ? r.w : r.z) : ((k & 1) ? r.y : r.x);
-}
+// Upper bound of a key computed as b with binary32 exp / log: covers the functions' few-ulp
+// errors and their possible non-monotonicity at that level, with a wide margin.
+__device__ __forceinline__ float key_bound(float b) { return b + (1e-3f + 1e-5f * fabsf(b)); }
 
-// Race clock of slot s of a block from its head words (W word, slot a) and the slot call's word
-// (unused for s == a): E_min = -log(W) / 16, plus -log(U_s) for s != a.
-__device__ __forceinline__ float race_clock(uint32_t w_head, int a, int s, uint32_t w_slot)
+// Group g's smallest clock: E_g = -log(W) / 64 from word 0 of its head call (exact scaling).
+__device__ __forceinline__ float group_emin(const sv::Philox4 &h)
 {
-    const float emin = __fmul_rn(-sv::log_f32(sv::uniform_from_word(w_head)), 0.0625f);
-    if (s == a) return emin;
-    return __fadd_rn(emin, -sv::log_f32(sv::uniform_from_word(w_slot)));
-}
-
-// Clock of token v at position j of request ireq (two Philox calls; used off the hot path).
-__device__ __forceinline__ float token_clock(int v, uint32_t j, uint32_t ireq, uint64_t seed)
-{
-    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-    const uint32_t g = static_cast<uint32_t>(v) >> 4;
-    const int s = v & 15;
-    const sv::Philox4 h = sv::philox4x32_10(g, j, ireq, sv::kClockHead, k0, k1);
-    const int a = static_cast<int>(h.y & 15u);
-    uint32_t w = 0u;
-    if (s != a) w = pick_word(sv::philox4x32_10(g, j, ireq, sv::kClockHead + 1u + (s >> 2), k0, k1), s & 3);
-    return race_clock(h.x, a, s, w);
+    return __fmul_rn(-sv::log_f32(sv::uniform_from_word(h.x)), 0x1p-6f);
 }
 
 __device__ __forceinline__ void emit_row(int i, int jstar, int K, int q0, int token,
@@ -182,86 +130,37 @@ __device__ __forceinline__ void emit_row(int i, int jstar, int K, int q0, int to
 }
 
 // ---------------------------------------------------------------------------------------
-// 1. plan
+// requests
 // ---------------------------------------------------------------------------------------
-// Scratch words per request: rows-done counter, race counter, race threshold, sampling list.
-struct ReqWords {
-    unsigned *rows_done, *race_counter, *race_thr;
-    int *rand_req, *n_rand;
-};
-
-__global__ void __launch_bounds__(kPlanThreads)
-sv_plan_kernel(const int32_t *__restrict__ cu, const float *__restrict__ temperature,
-               const uint8_t *__restrict__ is_greedy, int num_reqs, int num_draft_tokens,
-               int kmax, RowInfo *__restrict__ rowinfo, ReqWords rw,
-               int32_t *__restrict__ sampled, int stride,
-               int32_t *__restrict__ num_sampled, int32_t *__restrict__ num_rejected,
-               unsigned *__restrict__ flags)
+// Request of logit row r: the largest i in [0, n) with cu[i] + i <= r (request i owns rows
+// cu[i] + i .. cu[i + 1] + i). A 32-way search by one full warp; the result stays in [0, n)
+// whatever cu holds.
+__device__ __forceinline__ int row_request(const int32_t *__restrict__ cu, int n, int r, int lane)
 {
-    __shared__ int bad;
-    __shared__ int warp_count[kPlanThreads / 32];
-    __shared__ int s_base;
-    if (threadIdx.x == 0) {
-        bad = (cu[0] != 0) || (cu[num_reqs] != num_draft_tokens);
-        s_base = 0;
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int step = (hi - lo + 31) >> 5;
+        const int p = lo + lane * step;
+        const bool ok = lane == 0 || (p < hi && __ldg(cu + p) + p <= r);
+        const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
+        lo += (31 - __clz(b)) * step;
+        hi = min(hi, lo + step);
     }
-    __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int i0 = 0; i0 < num_reqs; i0 += blockDim.x) {
-        const int i = i0 + threadIdx.x;
-        bool sampling = false;
-        if (i < num_reqs) {
-            rw.rows_done[i] = 0u;
-            rw.race_counter[i] = 0u;
-            rw.race_thr[i] = kKeyNone;
-            const int lo = cu[i], hi = cu[i + 1];
-            const int K = hi - lo;
-            if (K < 0 || K > kmax || lo < 0 || hi > num_draft_tokens) {
-                bad = 1;
-            } else {
-                const float T = temperature[i];
-                const bool greedy = is_greedy[i] != 0 || !(T > 0.0f);
-                const float invT = greedy ? 1.0f : __frcp_rn(T);
-                const int32_t f = (greedy ? kFlagGreedy : 0) | (K << kFlagKShift);
-                for (int j = 0; j <= K; ++j)
-                    rowinfo[lo + i + j] = RowInfo{i, j, f | (j == K ? kFlagBonus : 0), invT};
-                sampling = !greedy;
-            }
-        }
-        // list the sampling requests in index order (ballot within warps, scan across warps)
-        const unsigned m = __ballot_sync(0xFFFFFFFFu, sampling);
-        if (lane == 0) warp_count[warp] = __popc(m);
-        __syncthreads();
-        if (warp == 0) {
-            const int c = warp_count[lane];
-            int x = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-                if (lane >= o) x += y;
-            }
-            warp_count[lane] = x - c;  // exclusive prefix
-        }
-        __syncthreads();
-        if (sampling)
-            rw.rand_req[s_base + warp_count[warp] + __popc(m & ((1u << lane) - 1u))] = i;
-        __syncthreads();
-        if (threadIdx.x == blockDim.x - 1)
-            s_base += warp_count[warp] + __popc(m);
-        __syncthreads();
-    }
-    if (threadIdx.x == 0) {
-        *rw.n_rand = bad ? 0 : s_base;
-        flags[0] = bad ? 1u : 0u;
-        if (bad) atomicOr(&flags[1], SV_ERR_BATCH);
-    }
-    if (bad)  // an inconsistent batch emits nothing for any request
-        for (int i = threadIdx.x; i < num_reqs; i += blockDim.x)
-            emit_row(i, -1, 0, 0, -1, nullptr, sampled, stride, num_sampled, num_rejected, 0, 1);
+    return lo;
+}
+
+// 1 / T of request i, or 1 for a greedy request (flag set, or !(T > 0)).
+__device__ __forceinline__ float request_invT(const float *__restrict__ temperature,
+                                              const uint8_t *__restrict__ is_greedy, int i,
+                                              bool &greedy)
+{
+    const float T = __ldg(temperature + i);
+    greedy = __ldg(is_greedy + i) != 0 || !(T > 0.0f);
+    return greedy ? 1.0f : __frcp_rn(T);
 }
 
 // ---------------------------------------------------------------------------------------
-// 2. row statistics, acceptance test, request completion
+// 1. row statistics
 // ---------------------------------------------------------------------------------------
 struct OnlineMax {
     float L = -kInf;   // running max of raw logits
@@ -303,24 +202,14 @@ __device__ __forceinline__ void unpack(const uint4 &w, float (&l)[16 / sizeof(T)
 }
 
 // Fold a batch of NV 16-byte vectors (vectors u0, u0 + kThreads, ...; element indices increase
-// with the vector) without branches: the batch max first, then one rescale of the running sum,
-// then the sum of 2^((l - L) c). Only the batch that first reached the max is recorded; its
-// lowest index is recovered at the end of the segment.
+// with the vector; nv of them valid) whose largest element is mx, without branches: one rescale
+// of the running sum, then the sum of 2^((l - L) c). Only the batch that first reached the max is
+// recorded; its lowest index is recovered at the end of the segment.
 template <typename T, int NV>
-__device__ __forceinline__ void fold_batch(OnlineMax &st, const uint4 (&w)[NV], int nv, int u0,
-                                           float c)
+__device__ __forceinline__ void fold_sum(OnlineMax &st, const uint4 (&w)[NV], int nv, int u0,
+                                         float c, float mx)
 {
     constexpr int kVec = 16 / sizeof(T);
-    float mx = -kInf;
-#pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        if (k < nv) {
-            float l[kVec];
-            unpack<T>(w[k], l);
-#pragma unroll
-            for (int h = 0; h < kVec; ++h) mx = fmaxf(mx, l[h]);
-        }
-    }
     const bool up = mx > st.L;
     st.s *= sv::ex2_approx(up ? (st.L - mx) * c : 0.0f);  // L = -inf: 2^-inf = 0 (s was 0)
     st.best_u = up ? u0 : st.best_u;
@@ -341,6 +230,57 @@ __device__ __forceinline__ void fold_batch(OnlineMax &st, const uint4 (&w)[NV], 
     st.s += s0 + s1;
 }
 
+// Largest element of a 16-byte vector in a form that combines cheaply (bf16: two halves packed
+// in a word, max.bf16x2; fp32: a float), and the largest over the lanes that share a 64-element
+// line (8 consecutive lanes for bf16, 16 for fp32, aligned to that in the warp; every lane of the
+// warp must take part).
+template <typename T> struct VecMax;
+template <> struct VecMax<uint16_t> {
+    using P = uint32_t;
+    static constexpr int kLanes = 8;
+    static __device__ __forceinline__ P max2(P a, P b)
+    {
+        P d;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    static __device__ __forceinline__ P of(const uint4 &w) { return max2(max2(w.x, w.y), max2(w.z, w.w)); }
+    static __device__ __forceinline__ P none() { return 0xFF80FF80u; }
+    static __device__ __forceinline__ float value(P m)
+    {
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+    }
+    static __device__ __forceinline__ P line(P m)
+    {
+#pragma unroll
+        for (int o = 1; o < kLanes; o <<= 1) m = max2(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        return m;
+    }
+    static __device__ __forceinline__ uint16_t store(P m)  // a bf16 value: exact
+    {
+        return static_cast<uint16_t>(__float_as_uint(value(m)) >> 16);
+    }
+};
+template <> struct VecMax<float> {
+    using P = float;
+    static constexpr int kLanes = 16;
+    static __device__ __forceinline__ P max2(P a, P b) { return fmaxf(a, b); }
+    static __device__ __forceinline__ P of(const uint4 &w)
+    {
+        return fmaxf(fmaxf(__uint_as_float(w.x), __uint_as_float(w.y)),
+                     fmaxf(__uint_as_float(w.z), __uint_as_float(w.w)));
+    }
+    static __device__ __forceinline__ P none() { return -kInf; }
+    static __device__ __forceinline__ float value(P m) { return m; }
+    static __device__ __forceinline__ P line(P m)
+    {
+#pragma unroll
+        for (int o = 1; o < kLanes; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        return m;
+    }
+    static __device__ __forceinline__ float store(P m) { return m; }
+};
+
 __device__ __forceinline__ void combine_stat(float &L, float &s, int &idx, float L2, float s2,
                                              int i2, float c)
 {
@@ -356,8 +296,8 @@ __device__ __forceinline__ void combine_stat(float &L, float &s, int &idx, float
 // Warp then block reduction of (L, s, idx); result valid in thread 0.
 __device__ __forceinline__ void block_reduce_stat(float &L, float &s, int &idx, float c)
 {
-    __shared__ float sh_L[kThreads / 32], sh_s[kThreads / 32];
-    __shared__ int sh_i[kThreads / 32];
+    __shared__ float sh_L[kWarps], sh_s[kWarps];
+    __shared__ int sh_i[kWarps];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
@@ -374,9 +314,9 @@ __device__ __forceinline__ void block_reduce_stat(float &L, float &s, int &idx, 
     }
     __syncthreads();
     if (warp == 0) {
-        L = lane < kThreads / 32 ? sh_L[lane] : -kInf;
-        s = lane < kThreads / 32 ? sh_s[lane] : 0.0f;
-        idx = lane < kThreads / 32 ? sh_i[lane] : INT_MAX;
+        L = lane < kWarps ? sh_L[lane] : -kInf;
+        s = lane < kWarps ? sh_s[lane] : 0.0f;
+        idx = lane < kWarps ? sh_i[lane] : INT_MAX;
 #pragma unroll
         for (int o = 4; o > 0; o >>= 1) {
             const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
@@ -387,147 +327,80 @@ __device__ __forceinline__ void block_reduce_stat(float &L, float &s, int &idx, 
     }
 }
 
-// Acceptance test of the row's draft ([spec-notes] answer code: draft_prob > 0 and
-// target_prob / draft_prob >= uniform; greedy: d == argmax, [spec-notes] 8.3). One thread.
-template <typename T>
-__device__ __forceinline__ int accept_test(const T *rp, int V, const RowInfo &ri, int row, float m,
-                                           float S, int amax, const int32_t *__restrict__ draft_ids,
-                                           const float *__restrict__ q, uint64_t seed,
-                                           uint32_t req_base)
-{
-    if (ri.flags & kFlagBonus) return 1;
-    const int qrow = row - ri.req;  // cu_num_draft[i] + j
-    const int d = draft_ids[qrow];
-    if (ri.flags & kFlagGreedy) return d == amax;
-    if (d < 0 || d >= V) return 0;
-    const float x_d = __fmul_rn(Elem<T>::at(rp, d), ri.invT);
-    const float t_d = sv::exp_f32(__fsub_rn(x_d, m));
-    const float p_d = __fdiv_rn(t_d, S);
-    const float q_d = q ? __ldg(q + static_cast<size_t>(qrow) * V + d) : 1.0f;
-    const sv::Philox4 r = sv::philox4x32_10(0u, static_cast<uint32_t>(ri.j),
-                                            req_base + static_cast<uint32_t>(ri.req),
-                                            sv::kTagAccept, static_cast<uint32_t>(seed),
-                                            static_cast<uint32_t>(seed >> 32));
-    const float u = sv::uniform_from_word(r.x);
-    return (q_d > 0.0f) && (__fdiv_rn(p_d, q_d) >= u);
-}
-
-struct StatsOut {  // what the statistics kernel writes besides per-row partials
-    RowStat *rowstat;
-    ReqState *reqstate;
-    unsigned *rows_done;
-    int32_t *sampled, *num_sampled, *num_rejected;
-    int stride;
-    float *opt_max, *opt_sum;
-    int32_t *opt_amax;
+struct RequestTable {
+    const int32_t *cu;
+    const float *temperature;
+    const uint8_t *is_greedy;
+    int n;
 };
 
-// The request's last row has been finalised (one thread): find j*, emit a greedy request, or
-// record the race of a sampling request.
-__device__ __noinline__ void complete_request(int i, int row0, int K, bool greedy, float invT,
-                                              const int32_t *__restrict__ draft_ids, bool has_q,
-                                              const StatsOut &o)
-{
-    const int q0 = row0 - i;
-    int js = K;
-    for (int jj = 0; jj < K; ++jj)
-        if (__ldcg(&o.rowstat[row0 + jj].acc) == 0) {
-            js = jj;
-            break;
-        }
-    const RowStat *rs = &o.rowstat[row0 + js];
-    const int amax = __ldcg(&rs->amax);
-    if (greedy) {  // [spec-notes] 8.3: the target argmax at the mismatch, or of the bonus row
-        emit_row(i, js, K, q0, amax, draft_ids, o.sampled, o.stride, o.num_sampled,
-                 o.num_rejected, 0, 1);
-        return;
-    }
-    const bool residual = js < K && has_q;
-    const int excl = (js < K && !has_q) ? draft_ids[q0 + js] : -1;
-    const uint32_t seed_p = __ldcg(&rs->seed_p);
-    const uint32_t seed = residual ? __ldcg(&rs->seed_r) : (amax == excl ? kKeyNone : seed_p);
-    o.reqstate[i] = ReqState{js, K, q0, row0 + js, __ldcg(&rs->m), __ldcg(&rs->S), invT, seed,
-                             seed_p, excl, {0, 0}};
-}
-
-// Finalise row `row` from its combined statistics (one thread): m, S, the argmax, the acceptance
-// of the row's draft and the race's screening seeds (the argmax token's keys); the finaliser of
-// a request's last row completes the request.
-template <typename T>
-__device__ __forceinline__ void finalize_row(const T *rp, int V, int row, const RowInfo &ri,
-                                             float L, float s, int idx,
-                                             const int32_t *__restrict__ draft_ids,
-                                             const float *__restrict__ q, uint64_t seed,
-                                             uint32_t req_base, const StatsOut &o)
-{
-    const float m = __fmul_rn(L, ri.invT);  // = max_v fl(l_v / T): rounding is monotone
-    const int amax = idx == INT_MAX ? 0 : idx;
-    const int acc = accept_test<T>(rp, V, ri, row, m, s, amax, draft_ids, q, seed, req_base);
-    uint32_t seed_p = kKeyNone, seed_r = kKeyNone;
-    if (!(ri.flags & kFlagGreedy)) {
-        const float x = __fmul_rn(Elem<T>::at(rp, amax), ri.invT);
-        const float E = token_clock(amax, static_cast<uint32_t>(ri.j),
-                                    req_base + static_cast<uint32_t>(ri.req), seed);
-        float key;
-        if (race_key<false>(x, 0.0f, E, m, s, key)) seed_p = key_enc(key);
-        if (q && !(ri.flags & kFlagBonus)) {
-            const float qv = __ldg(q + static_cast<size_t>(row - ri.req) * V + amax);
-            if (race_key<true>(x, qv, E, m, s, key)) seed_r = key_enc(key);
-        }
-    }
-    o.rowstat[row] = RowStat{m, s, amax, acc, seed_p, seed_r, {0u, 0u}};
-    if (o.opt_max) o.opt_max[row] = m;
-    if (o.opt_sum) o.opt_sum[row] = s;
-    if (o.opt_amax) o.opt_amax[row] = amax;
-
-    const int K = ri.flags >> kFlagKShift;
-    __threadfence();
-    if (atomicAdd(&o.rows_done[ri.req], 1u) == static_cast<unsigned>(K)) {
-        __threadfence();
-        o.rows_done[ri.req] = 0u;
-        complete_request(ri.req, row - ri.j, K, (ri.flags & kFlagGreedy) != 0, ri.invT, draft_ids,
-                         q != nullptr, o);
-    }
-}
-
-// Segment [b, e) of row `row`, by the whole CTA: stream the logits in batches of four 16-byte
-// loads per thread (the row's parameters arrive while the first batch is in flight), reduce,
-// and publish the segment's partial statistics.
+// Segment [b, e) of row `row`, by the whole CTA: the elements before the first 64-element line
+// boundary one by one, then whole 16-byte vectors in batches of four loads per thread (the row's
+// request is looked up while the first batch is in flight), then the last few elements one by
+// one; reduce and publish the segment's partial statistics. With `lines`, the largest logit of
+// every line that the vectors cover completely is stored at lines[line] (line = (base_off +
+// flattened element) / 64).
 template <typename T>
 __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int V, int row, int b,
-                                              int e, int seg, int maxseg,
-                                              const RowInfo *__restrict__ rowinfo,
-                                              StatPart *__restrict__ part)
+                                              int e, int seg, int maxseg, int base_off,
+                                              const RequestTable &rq, StatPart *__restrict__ part,
+                                              T *__restrict__ lines)
 {
-    const T *rp = logits + static_cast<size_t>(row) * static_cast<size_t>(V);
+    __shared__ float s_c;
+    const long long rbase = static_cast<long long>(row) * V;
+    const T *rp = logits + rbase;
     constexpr int kVec = 16 / sizeof(T);
+    constexpr int kVPL = VecMax<T>::kLanes;  // vectors per line
     constexpr int kU = 4;
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(rp + b);
-    const int head = static_cast<int>(((16u - (addr & 15u)) & 15u) / sizeof(T));
-    const int a0 = min(e, b + head);
+    const long long pos_b = base_off + rbase + b;  // line coordinate of element b
+    const int head = static_cast<int>((kGroup - (pos_b & (kGroup - 1))) & (kGroup - 1));
+    const int a0 = min(e, b + head);  // on a line boundary (hence on a 16-byte boundary)
     const int nvec = (e - a0) / kVec;
     const int a1 = a0 + nvec * kVec;
     const char *vbase = reinterpret_cast<const char *>(rp + a0);
+    const long long line0 = (pos_b + (a0 - b)) >> 6;  // line of vector 0 when a0 < e
+    const int lane = threadIdx.x & 31;
 
+    // the warp's vectors of a batch start at ub: the loop runs the same iterations in every lane
+    int ub = static_cast<int>(threadIdx.x) & ~31;
     uint4 w[kU];
-    int u0 = static_cast<int>(threadIdx.x);
 #pragma unroll
     for (int k = 0; k < kU; ++k) {
-        const int u = u0 + k * kThreads;
+        const int u = ub + lane + k * kThreads;
         w[k] = u < nvec ? ldg_v4(vbase + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
     }
-    const RowInfo ri = rowinfo[row];
-    const float c = ri.invT * kLog2e;
+    if (threadIdx.x < 32) {
+        const int i = row_request(rq.cu, rq.n, row, lane);
+        if (threadIdx.x == 0) {
+            bool greedy;
+            s_c = request_invT(rq.temperature, rq.is_greedy, i, greedy) * kLog2e;
+        }
+    }
+    __syncthreads();
+    const float c = s_c;
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
-    while (u0 < nvec) {
-        const int nv = min(kU, (nvec - u0 + kThreads - 1) / kThreads);
-        fold_batch<T, kU>(st, w, nv, u0, c);
-        u0 += kThreads * kU;
+    while (ub < nvec) {
+        const int u0 = ub + lane;
+        const int nv = min(kU, (nvec - u0 + kThreads - 1) / kThreads);  // <= 0: nothing to fold
+        typename VecMax<T>::P bm = VecMax<T>::none();
 #pragma unroll
         for (int k = 0; k < kU; ++k) {
-            const int u = u0 + k * kThreads;
+            const typename VecMax<T>::P pm = VecMax<T>::of(w[k]);
+            if (k < nv) bm = VecMax<T>::max2(bm, pm);
+            if (lines) {
+                const int u = u0 + k * kThreads;
+                const typename VecMax<T>::P lm = VecMax<T>::line(pm);
+                if ((lane & (kVPL - 1)) == 0 && u + kVPL - 1 < nvec)
+                    lines[line0 + u / kVPL] = VecMax<T>::store(lm);
+            }
+        }
+        fold_sum<T, kU>(st, w, nv, u0, c, VecMax<T>::value(bm));
+        ub += kThreads * kU;
+#pragma unroll
+        for (int k = 0; k < kU; ++k) {
+            const int u = ub + lane + k * kThreads;
             w[k] = u < nvec ? ldg_v4(vbase + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
         }
     }
@@ -552,17 +425,16 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
 }
 
 // Row statistics over the flattened [rows x V] logits, split evenly: CTA k streams elements
-// [k * chunk, (k + 1) * chunk), which covers one or more row segments, and writes one partial per
+// [k * chunk - base_off, (k + 1) * chunk - base_off) (chunk a multiple of 64, so that CTAs meet
+// on line boundaries), which covers one or more row segments, and writes one partial per
 // segment. Pure streaming: no atomics, nothing waits on another CTA.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 6)
+__global__ void __launch_bounds__(kThreads, 5)
 sv_stats_kernel(const T *__restrict__ logits, int V, long long total, long long chunk, int maxseg,
-                const RowInfo *__restrict__ rowinfo, StatPart *__restrict__ part,
-                const unsigned *__restrict__ flags)
+                int base_off, RequestTable rq, StatPart *__restrict__ part, T *__restrict__ lines)
 {
-    if (flags[0]) return;
-    const long long start = static_cast<long long>(blockIdx.x) * chunk;
-    const long long stop = min(total, start + chunk);
+    const long long start = max(0LL, static_cast<long long>(blockIdx.x) * chunk - base_off);
+    const long long stop = min(total, static_cast<long long>(blockIdx.x + 1) * chunk - base_off);
     if (start >= stop) return;
     const int r_first = static_cast<int>(start / V);
     const int r_last = static_cast<int>((stop - 1) / V);
@@ -570,773 +442,578 @@ sv_stats_kernel(const T *__restrict__ logits, int V, long long total, long long 
         const long long rbase = static_cast<long long>(row) * V;
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
-        const int fk = static_cast<int>(rbase / chunk);
-        stats_segment<T>(logits, V, row, b, e, static_cast<int>(blockIdx.x) - fk, maxseg, rowinfo,
-                         part);
+        const int fk = static_cast<int>((base_off + rbase) / chunk);
+        stats_segment<T>(logits, V, row, b, e, static_cast<int>(blockIdx.x) - fk, maxseg, base_off,
+                         rq, part, lines);
     }
 }
 
-// One warp per row: combine the row's segment partials in segment order (deterministic) and
-// finalise it (acceptance test, race seeds, request completion).
-template <typename T>
-__global__ void __launch_bounds__(kThreads)
-sv_finalize_kernel(const T *__restrict__ logits, int V, int rows, long long chunk, int maxseg,
-                   const RowInfo *__restrict__ rowinfo, const StatPart *__restrict__ part,
-                   const int32_t *__restrict__ draft_ids, const float *__restrict__ q,
-                   uint64_t seed, uint32_t req_base, StatsOut o, const unsigned *__restrict__ flags)
-{
-    if (flags[0]) return;
-    const int row = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    if (row >= rows) return;
-    const int lane = threadIdx.x & 31;
-    const RowInfo ri = rowinfo[row];
-    const float c = ri.invT * kLog2e;
-    const long long rbase = static_cast<long long>(row) * V;
-    const int nseg = static_cast<int>((rbase + V - 1) / chunk) - static_cast<int>(rbase / chunk) + 1;
-    float L = -kInf, s = 0.0f;
-    int idx = INT_MAX;
-    for (int k = lane; k < nseg; k += 32) {
-        const float4 raw = __ldg(reinterpret_cast<const float4 *>(part) +
-                                 static_cast<size_t>(row) * maxseg + k);
-        combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
-    }
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-        const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o2);
-        const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o2);
-        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o2);
-        combine_stat(L, s, idx, L2, s2, i2, c);
-    }
-    if (lane == 0)
-        finalize_row<T>(logits + rbase, V, row, ri, L, s, idx, draft_ids, q, seed, req_base, o);
-}
-
 // ---------------------------------------------------------------------------------------
-// Bulk-copy (TMA) staging: cp.async.bulk global -> shared, completion on an mbarrier. Every
-// wait is bounded by the global timer.
+// 2. verify: acceptance, first rejection, race search, emit
 // ---------------------------------------------------------------------------------------
-constexpr unsigned long long kWaitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ uint32_t smem_addr(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_fence_init()
-{
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_expect(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
-                 "r"(bytes) : "memory");
-}
-// Copy [src, src + bytes) to dst (both 16-byte aligned, bytes a multiple of 16), completing
-// `bytes` of the transaction the barrier expects.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ unsigned long long global_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-                 "selp.u32 %0, 1, 0, p;\n\t}"
-                 : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
-    return ok != 0;
-}
-// Wait for the phase with parity `parity`; false after `limit_ns` (never expected: the caller
-// records an error and stops using the buffers).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, unsigned long long limit_ns)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (global_ns() - t0 > limit_ns) return false;
-    return true;
-}
-
-// ---------------------------------------------------------------------------------------
-// 3. race + emit
-// ---------------------------------------------------------------------------------------
-// Screening. A thread skips a token only when its key is certainly below `ks`, a key that some
-// candidate of the same race has already reached (so ks never exceeds the winner's key, and the
-// winner -- or an equal key at a lower index -- is never skipped). ks is shared by the warp
-// (redux), the CTA (shared memory) and all CTAs of the request (a global word).
-struct RaceState {
-    float kb = -kInf;        // this thread's best key
-    int ib = -1;             // its index (-1: none yet)
-    unsigned ks_enc = kKeyNone;
-    float pre_x;             // p-race: skip a group whose max x is below this
-    float kbl;               // p-race: (ks - delta) * log2 e
-    float pre_rr;            // residual: skip a group whose rr upper bounds are all below this
-    float ekb;               // residual: >= exp(delta - ks)
+struct VerifyParams {
+    RequestTable rq;
+    const int32_t *draft_ids;
+    const float *q;
+    const StatPart *part;
+    uint64_t seed;
+    uint32_t req_base;
+    int nd, kmax, V, maxseg, base_off;
+    long long chunk;
+    int32_t *sampled, *num_sampled, *num_rejected;
+    float *opt_max, *opt_sum;
+    int32_t *opt_amax;
+    unsigned *flags;
 };
 
-constexpr float kSafe = 1.0f + 0x1p-10f;  // covers MUFU and argument rounding errors
-
-// Screening constants from ks. With delta = 1e-3 + 1e-5 |ks| (far above the few-ulp error of
-// the binary32 key), a token whose key is certainly below ks - delta is skipped:
-//   - with no randomness: key <= log w - log(clock) < log w + kClockLogMax;
-//   - with its block's head: every clock of the block is >= E_min = -log(W)/16 >= (1 - W)/16,
-//     so key < ks - delta once (1 - W)/16 > w exp(delta - ks);
-//   - with its own slot word: clock >= (1 - W)/16 + (1 - U) (the slot a: (1 - W)/16).
-__device__ __forceinline__ void refresh(RaceState &st)
+// Acceptance test of draft j ([spec-notes] answer code: draft_prob > 0 and
+// target_prob / draft_prob >= uniform; greedy: d == argmax, [spec-notes] 8.3). One thread.
+template <typename T>
+__device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, int j, int qrow,
+                                             float invT, float m, float S, int amax,
+                                             const int32_t *__restrict__ draft_ids,
+                                             const float *__restrict__ q, uint64_t seed,
+                                             uint32_t ireq)
 {
-    if (st.ks_enc == kKeyNone) {
-        st.pre_x = -kInf;
-        st.kbl = -kInf;
-        st.pre_rr = -kInf;
-        st.ekb = kInf;
-        return;
-    }
-    const float ks = key_dec(st.ks_enc);
-    const float delta = 1e-3f + 1e-5f * fabsf(ks);
-    st.pre_x = ks - (sv::kClockLogMax + delta);
-    st.kbl = (ks - delta) * kLog2e;
-    st.pre_rr = sv::ex2_approx((ks - sv::kClockLogMax - delta) * kLog2e) * (1.0f - 0x1p-9f);
-    st.ekb = sv::ex2_approx((delta - ks) * kLog2e) * kSafe;
+    const int d = __ldg(draft_ids + qrow);
+    if (greedy) return d == amax;
+    if (d < 0 || d >= V) return false;
+    const float x_d = __fmul_rn(Elem<T>::at(rp, d), invT);
+    const float t_d = sv::exp_f32(__fsub_rn(x_d, m));
+    const float p_d = __fdiv_rn(t_d, S);
+    const float q_d = q ? __ldg(q + static_cast<size_t>(qrow) * V + d) : 1.0f;
+    const sv::Philox4 r = sv::philox4x32_10(0u, static_cast<uint32_t>(j), ireq, sv::kTagAccept,
+                                            static_cast<uint32_t>(seed),
+                                            static_cast<uint32_t>(seed >> 32));
+    const float u = sv::uniform_from_word(r.x);
+    return (q_d > 0.0f) && (__fdiv_rn(p_d, q_d) >= u);
 }
 
-__device__ __forceinline__ void raise_threshold(RaceState &st, unsigned enc)
+// Where a row's elements fall on the 64-element lines of the flattened logits. Flattened
+// element e sits on line (base_off + e) / 64, base_off = (address of the array mod 64 elements)
+// / element size: a line is 64 elements starting on a 64-element boundary of memory.
+struct RowLines {
+    long long P0;  // base_off + first flattened element of the row
+    long long L0;  // line of the row's first element
+    int nl;        // lines the row touches
+    int kf, kl;    // first and last line (relative to L0) that lies entirely inside the row
+    // line (relative to L0) that holds token v
+    __device__ __forceinline__ int of(int v) const { return static_cast<int>(((P0 + v) >> 6) - L0); }
+};
+
+__device__ __forceinline__ RowLines row_lines(long long row, int V, int base_off)
 {
-    if (enc > st.ks_enc) {
-        st.ks_enc = enc;
-        refresh(st);
-    }
+    RowLines rl;
+    rl.P0 = base_off + row * V;
+    rl.L0 = rl.P0 >> 6;
+    rl.nl = static_cast<int>(((rl.P0 + V - 1) >> 6) - rl.L0) + 1;
+    rl.kf = (rl.P0 & (kGroup - 1)) ? 1 : 0;
+    rl.kl = ((rl.P0 + V) & (kGroup - 1)) ? rl.nl - 2 : rl.nl - 1;
+    return rl;
 }
 
-__device__ __forceinline__ bool race_better(float ka, int ia, float kb, int ib)
+// lm[k] = largest raw logit of the row on line L0 + k (the row's own elements only). The lines
+// inside the row come from `lines` (written by the statistics kernel) or, without it, from
+// coalesced 16-byte loads of the row; a partial first / last line is read by warp 0 / 1.
+template <typename T>
+__device__ void row_line_max(const T *__restrict__ rp, int V, const RowLines &rl,
+                             const T *__restrict__ lines, float *__restrict__ lm)
 {
-    // is (ka, ia) better than (kb, ib)? larger key, then lower index; -1 = no candidate
-    if (ia < 0) return false;
-    if (ib < 0) return true;
-    return ka > kb || (ka == kb && ia < ib);
-}
-
-// The full key out of line (rarely reached). NaN = not a candidate.
-template <bool kResidual>
-__device__ __noinline__ float race_key_slow(float x, float qv, uint32_t w_head, int a, int s,
-                                            uint32_t w_slot, float m, float S)
-{
-    float key;
-    const float E = race_clock(w_head, a, s, w_slot);
-    return race_key<kResidual>(x, qv, E, m, S, key) ? key : __int_as_float(0x7FC00000);
-}
-
-// Offer token v (slot s of its block) whose clock is at least clock_lb; the full key is computed
-// only if the screen cannot rule the token out. Returns true if the thread's threshold rose.
-template <bool kResidual>
-__device__ __forceinline__ bool race_offer(RaceState &st, unsigned *s_thr, int v, float x,
-                                           float qv, float clock_lb, uint32_t w_head, int a,
-                                           int s, uint32_t w_slot, float m, float S, float rr_up)
-{
-    if constexpr (kResidual) {
-        if (!(rr_up > 0.0f)) return false;
-        if (clock_lb > rr_up * st.ekb) return false;
+    constexpr int kVPL = VecMax<T>::kLanes;  // vectors per line
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lines) {
+        for (int k = rl.kf + static_cast<int>(threadIdx.x); k <= rl.kl; k += kThreads)
+            lm[k] = Elem<T>::at(lines, static_cast<size_t>(rl.L0 + k));
     } else {
-        if (clock_lb > sv::ex2_approx(fmaf(x, kLog2e, -st.kbl)) * kSafe) return false;
+        const int nvec = max(0, rl.kl - rl.kf + 1) * kVPL;
+        // line L0 + kf starts at token (L0 + kf) * 64 - P0 of the row, on a 16-byte boundary
+        const char *lbase = reinterpret_cast<const char *>(rp + ((rl.L0 + rl.kf) * kGroup - rl.P0));
+        for (int base = 0; base < nvec; base += 4 * kThreads) {
+            uint4 w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int u = base + static_cast<int>(threadIdx.x) + k * kThreads;
+                w[k] = u < nvec ? ldg_v4(lbase + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float mx = VecMax<T>::value(VecMax<T>::line(VecMax<T>::of(w[k])));
+                const int u = base + static_cast<int>(threadIdx.x) + k * kThreads;
+                if ((lane & (kVPL - 1)) == 0 && u < nvec) lm[rl.kf + u / kVPL] = mx;
+            }
+        }
     }
-    const float key = race_key_slow<kResidual>(x, qv, w_head, a, s, w_slot, m, S);
-    if (key != key) return false;
-    if (st.ib < 0 || key > st.kb) {
-        st.kb = key;
-        st.ib = v;
+    // partial lines: the first (if the row does not start a line) and the last (if the row does
+    // not end one and it is another line)
+    int k = -1;
+    if (warp == 0 && rl.kf == 1) k = 0;
+    if (warp == 1 && rl.kl == rl.nl - 2 && (rl.nl > 1 || rl.kf == 0)) k = rl.nl - 1;
+    if (k >= 0) {
+        const long long p = (rl.L0 + k) * kGroup;  // first line coordinate of the line
+        float mx = -kInf;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long v = p + h * 32 + lane - rl.P0;  // token of the row
+            if (v >= 0 && v < V) mx = fmaxf(mx, Elem<T>::at(rp, static_cast<size_t>(v)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (lane == 0) lm[k] = mx;
     }
-    const unsigned enc = key_enc(key);
-    if (enc > st.ks_enc) {
-        raise_threshold(st, enc);
-        atomicMax(s_thr, enc);
-        return true;
-    }
-    return false;
 }
 
-__device__ __forceinline__ unsigned ld_relaxed(const unsigned *p)
+// The raced row as the search sees it.
+template <typename T>
+struct RaceRow {
+    const T *rp;        // logits row
+    const float *qrow;  // draft distribution row (residual race) or nullptr
+    int V, G;           // vocabulary, groups
+    int excl;           // token left out (rejected draft without q), or -1
+    float m, S, invT;
+    uint32_t j, ireq, k0, k1;  // Philox counter words 1, 2 and key
+};
+
+// Shared memory of the search (one CTA).
+constexpr int kBins = 32;  // candidate bins of the best-first order
+
+struct SearchSmem {
+    unsigned long long *buf;  // [sp] candidate entries (key bound, group); shares space with lm
+    unsigned long long *tmp;  // [sp] the entries in bin order
+    int *bin_n;               // [kBins + 1] entries per bin, then bin starts
+    unsigned *bin_max;        // [kBins] largest key bound (encoded) of each bin
+    unsigned *range;          // [2] largest and smallest key bound (encoded) of the list
+    float *lm;                // [G + 2] line maxima of the row, until the bounds are taken
+    float *pb;                // [G] p-race bound per group (NaN once evaluated)
+    float *eg;                // [G] smallest clock E_g of the group
+    uint8_t *ag;              // [G] slot that holds it
+    unsigned long long *best; // best candidate so far, packed (key, ~v); 0 = none
+    int *cnt;
+};
+
+// Dynamic shared memory layout of a verify CTA (bytes): the candidate buffer (a power of two
+// >= G entries of 8 bytes, also holding the G + 2 line maxima), the binned copy of it, m / S /
+// argmax of the request's rows (kmax + 1 each), pb, eg, ag.
+struct VerifyLayout {
+    size_t tmp, rows, pb, eg, ag, total;
+};
+__host__ __device__ inline int search_capacity(int G)
 {
-    unsigned v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
+    int sp = 1;
+    while (sp < G) sp <<= 1;
+    return sp;
+}
+__host__ __device__ inline VerifyLayout verify_layout(int V, int kmax)
+{
+    const size_t G = static_cast<size_t>((V + kGroup - 1) / kGroup);
+    const size_t sp = static_cast<size_t>(search_capacity(static_cast<int>(G)));
+    VerifyLayout l;
+    const size_t buf = 8 * sp > 4 * (G + 2) ? 8 * sp : 4 * (G + 2);
+    l.tmp = (buf + 15) / 16 * 16;
+    l.rows = l.tmp + 8 * sp;
+    l.pb = l.rows + 12 * (static_cast<size_t>(kmax) + 1);
+    l.eg = l.pb + 4 * G;
+    l.ag = l.eg + 4 * G;
+    l.total = l.ag + G;
+    return l;
 }
 
-// One step of the race for this lane's 4 consecutive tokens v0..v0+3 (raw logit words lc, q words
-// qc). The 4 lanes of a quad cover one 16-token clock block. Per block: the bound without
-// randomness; then the quad's first lane draws the block head and the block is ruled out if even
-// its smallest clock cannot beat ks; only then does each lane draw its own slots' words. Must be
-// called by all 32 lanes of the warp (shuffles); lanes past the end pass v0 >= e. Returns true
-// if this lane raised its threshold with a key of its own.
-template <typename T, bool kResidual>
-__device__ __forceinline__ bool race_step(RaceState &st, unsigned *s_thr,
-                                          const uint32_t (&lc)[sizeof(T)], const uint32_t (&qc)[4],
-                                          int v0, int e, float invT, float m, float S, int exclude,
-                                          uint32_t j, uint32_t ireq, uint32_t k0, uint32_t k1)
+// pb[g] = bound of group g in a race over p, fl(x_max - log E_g) with x_max = fl(line max * invT);
+// eg[g] = E_g, ag[g] = a from the group's head call. Returns the thread's best (pb, g) packed, 0 if
+// it has no group.
+template <typename T>
+__device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &rl,
+                                           const SearchSmem &sm)
+{
+    constexpr int kStep = 4;  // independent groups per thread and step (Philox chains overlap)
+    unsigned long long best = 0;
+    for (int g0 = threadIdx.x; g0 < r.G; g0 += kStep * kThreads) {
+        float lmax[kStep];
+        sv::Philox4 h[kStep];
+#pragma unroll
+        for (int k = 0; k < kStep; ++k) {
+            const int g = min(g0 + k * kThreads, r.G - 1);
+            const int v0 = g * kGroup, v1 = min(v0 + kGroup, r.V) - 1;
+            lmax[k] = fmaxf(sm.lm[rl.of(v0)], sm.lm[rl.of(v1)]);
+            h[k] = sv::philox4x32_10(static_cast<uint32_t>(g), r.j, r.ireq, sv::kClockHead, r.k0, r.k1);
+        }
+#pragma unroll
+        for (int k = 0; k < kStep; ++k) {
+            const int g = g0 + k * kThreads;
+            if (g < r.G) {
+                const float E = group_emin(h[k]);
+                const float b = __fsub_rn(__fmul_rn(lmax[k], r.invT), sv::log_f32(E));
+                sm.pb[g] = b;
+                sm.eg[g] = E;
+                sm.ag[g] = static_cast<uint8_t>(h[k].y & 63u);
+                best = max(best, pack_key(b, g));
+            }
+        }
+    }
+    return best;
+}
+
+__device__ __forceinline__ unsigned long long ld_best(const unsigned long long *s_best)
+{
+    // one 64-bit shared load, broadcast from lane 0 so that the warp takes one decision
+    const unsigned long long v = *reinterpret_cast<const volatile unsigned long long *>(s_best);
+    return __shfl_sync(0xFFFFFFFFu, v, 0);
+}
+
+// Exact keys of up to B groups by one warp (two adjacent tokens per lane and group; gs[k] < 0:
+// no group), merged into *sm.best. All loads are issued before the first group is evaluated.
+// Slot s = v & 63 of group g: its clock is E_g for the head's slot a, else fl(E_g + (-log U_s)),
+// U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4).
+template <typename T, bool kRes, int B>
+__device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm)
 {
     const int lane = threadIdx.x & 31;
-    const int quarter = lane & 3;  // this lane's slots in the block: 4 * quarter .. 4 * quarter + 3
-    float x[4], wv[4];  // x = logit / T; wv: the weight proxy the screens compare
+    float l[B][2], qv[B][2];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        float l;
-        if constexpr (sizeof(T) == 2)
-            l = (k & 1) ? __uint_as_float(lc[k >> 1] & 0xFFFF0000u) : __uint_as_float(lc[k >> 1] << 16);
-        else
-            l = __uint_as_float(lc[k]);
-        x[k] = __fmul_rn(l, invT);
-        if constexpr (kResidual) {  // upper bound of rr = fma(-S, q, exp(x - m))
-            const float t_up = sv::ex2_approx((x[k] - m) * kLog2e) * kSafe;
-            wv[k] = v0 + k < e ? fmaf(-S, __uint_as_float(qc[k]), t_up) : -kInf;
+    for (int k = 0; k < B; ++k) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int v = gs[k] * kGroup + 2 * lane + h;
+            const bool in = gs[k] >= 0 && v < r.V;
+            l[k][h] = in ? Elem<T>::at(r.rp, v) : -kInf;
+            qv[k][h] = 0.0f;
+            if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < B; ++k) {
+        const int g = gs[k];
+        if (g < 0) continue;
+        const float E = sm.eg[g];
+        const int a = sm.ag[g];
+        const int v0 = g * kGroup + 2 * lane, v1 = v0 + 1;
+        const bool in0 = v0 < r.V, in1 = v1 < r.V;
+        const float x0 = __fmul_rn(l[k][0], r.invT), x1 = __fmul_rn(l[k][1], r.invT);
+        float w0 = 0.0f, w1 = 0.0f;
+        bool c0, c1;
+        if constexpr (kRes) {
+            w0 = __fmaf_rn(-r.S, qv[k][0], sv::exp_f32(__fsub_rn(x0, r.m)));
+            w1 = __fmaf_rn(-r.S, qv[k][1], sv::exp_f32(__fsub_rn(x1, r.m)));
+            c0 = in0 && w0 > 0.0f;
+            c1 = in1 && w1 > 0.0f;
+            // the group's largest residual weight bounds its keys more tightly than its line max
+            const float wm = __uint_as_float(__reduce_max_sync(
+                0xFFFFFFFFu, __float_as_uint(fmaxf(c0 ? w0 : 0.0f, c1 ? w1 : 0.0f))));
+            if (!(wm > 0.0f)) continue;
+            const unsigned long long cur = ld_best(sm.best);
+            if (cur != 0 && key_enc(key_bound(__fsub_rn(sv::log_f32(wm), sv::log_f32(E)))) <
+                                static_cast<unsigned>(cur >> 32))
+                continue;
         } else {
-            wv[k] = v0 + k < e ? x[k] : -kInf;
+            c0 = in0 && v0 != r.excl;
+            c1 = in1 && v1 != r.excl;
         }
-    }
-    float mx = fmaxf(fmaxf(wv[0], wv[1]), fmaxf(wv[2], wv[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));  // the block's largest weight
-    bool go;
-    if (kResidual) go = (mx > 0.0f) && !(mx < st.pre_rr);
-    else go = (mx > -kInf) && !(mx < st.pre_x);
-    const uint32_t g = static_cast<uint32_t>(v0 - 4 * quarter) >> 4;
-    uint32_t hw0 = 0u, hw1 = 0u;  // block head, drawn by the quad's first lane
-    if (go && quarter == 0) {
-        const sv::Philox4 h = sv::philox4x32_10(g, j, ireq, sv::kClockHead, k0, k1);
-        hw0 = h.x;
-        hw1 = h.y;
-    }
-    hw0 = __shfl_sync(0xFFFFFFFFu, hw0, lane & ~3);
-    hw1 = __shfl_sync(0xFFFFFFFFu, hw1, lane & ~3);
-    const float emin_lb = (1.0f - sv::uniform_from_word(hw0)) * 0.0625f;  // exact
-    if (go) {
-        const float cmax = kResidual ? mx * st.ekb
-                                     : sv::ex2_approx(fmaf(mx, kLog2e, -st.kbl)) * kSafe;
-        go = !(emin_lb > cmax);
-    }
-    bool raised = false;
-    if (go) {
-        const int a = static_cast<int>(hw1 & 15u);
-        const sv::Philox4 r = sv::philox4x32_10(g, j, ireq, sv::kClockHead + 1u + quarter, k0, k1);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int v = v0 + k;
-            if (v >= e || v == exclude) continue;
-            const int s = 4 * quarter + k;
-            const uint32_t ws = pick_word(r, k);
-            const float lb = s == a ? emin_lb : emin_lb + (1.0f - sv::uniform_from_word(ws));
-            raised |= race_offer<kResidual>(st, s_thr, v, x[k], __uint_as_float(qc[k]), lb, hw0,
-                                            a, s, ws, m, S, wv[k]);
-        }
-    }
-    return raised;
-}
-
-// Bring in the thresholds others have reached: the CTA's shared word every step, the request's
-// global word every 4th step, read one exchange ahead (a stale value is a lower key and only
-// screens less). After the step the warp shares its best threshold with one redux.
-__device__ __forceinline__ void pull_threshold(RaceState &st, unsigned *s_thr, unsigned *g_thr,
-                                               int step, unsigned &g_seen)
-{
-    raise_threshold(st, *reinterpret_cast<volatile unsigned *>(s_thr));
-    if (g_thr && (step & 3) == 0) {
-        if (g_seen > st.ks_enc) {
-            raise_threshold(st, g_seen);
-            atomicMax(s_thr, g_seen);
-        }
-        g_seen = ld_relaxed(g_thr);
-    }
-}
-
-__device__ __forceinline__ void push_threshold(RaceState &st, unsigned *g_thr, bool raised)
-{
-    if (raised && g_thr) atomicMax(g_thr, st.ks_enc);  // publish to the other CTAs
-    raise_threshold(st, __reduce_max_sync(0xFFFFFFFFu, st.ks_enc));  // share in the warp
-}
-
-template <typename T, bool kResidual>
-__device__ __forceinline__ void load_quad(uint32_t (&l)[sizeof(T)], uint32_t (&qq)[4],
-                                          const T *__restrict__ rp, const float *__restrict__ qrow,
-                                          int v0, int e, bool aligned)
-{
-    if (aligned && v0 + 4 <= e) {
-        if constexpr (sizeof(T) == 2) {
-            const uint2 w = __ldg(reinterpret_cast<const uint2 *>(rp + v0));
-            l[0] = w.x;
-            l[1] = w.y;
+        const sv::Philox4 sl = sv::philox4x32_10(
+            static_cast<uint32_t>(g), r.j, r.ireq, sv::kClockHead + 1u + static_cast<uint32_t>(lane >> 1),
+            r.k0, r.k1);
+        const int s0 = 2 * lane, s1 = s0 + 1;  // slot words s & 3: 0 / 2 and 1 / 3
+        const uint32_t ws0 = (lane & 1) ? sl.z : sl.x;
+        const uint32_t ws1 = (lane & 1) ? sl.w : sl.y;
+        const float E0 = s0 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws0)));
+        const float E1 = s1 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws1)));
+        float k0, k1;
+        if constexpr (kRes) {
+            k0 = __fsub_rn(sv::log_f32(w0), sv::log_f32(E0));
+            k1 = __fsub_rn(sv::log_f32(w1), sv::log_f32(E1));
         } else {
-            const uint4 w = ldg_v4(rp + v0);
-            l[0] = w.x; l[1] = w.y; l[2] = w.z; l[3] = w.w;
+            k0 = __fsub_rn(x0, sv::log_f32(E0));
+            k1 = __fsub_rn(x1, sv::log_f32(E1));
         }
-        if constexpr (kResidual) {
-            const uint4 w = ldg_v4(qrow + v0);
-            qq[0] = w.x; qq[1] = w.y; qq[2] = w.z; qq[3] = w.w;
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const bool in = v0 + k < e;
-            if constexpr (sizeof(T) == 2) {
-                const uint32_t h = in ? static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t *>(rp) + v0 + k)) : 0xFF80u;
-                if (k & 1) l[k >> 1] |= h << 16;
-                else l[k >> 1] = h;
-            } else {
-                l[k] = in ? __float_as_uint(__ldg(reinterpret_cast<const float *>(rp) + v0 + k)) : 0xFF800000u;
-            }
-            if constexpr (kResidual) qq[k] = in ? __float_as_uint(__ldg(qrow + v0 + k)) : 0u;
-        }
+        unsigned long long p = 0;
+        if (c0) p = pack_key(k0, v0);
+        if (c1) p = max(p, pack_key(k1, v1));
+        p = warp_max_u64(p);
+        if (lane == 0 && p != 0) atomicMax(sm.best, p);
     }
 }
 
-// Race over [b, e) of one row (b a multiple of 16) reading the logits (and q) directly from global
-// memory, each thread with its next 4 tokens' loads in flight.
-template <typename T, bool kResidual>
-__device__ __forceinline__ void race_span(RaceState &st, unsigned *s_thr, unsigned *g_thr,
-                                          const T *__restrict__ rp,
-                                          const float *__restrict__ qrow, int b, int e,
-                                          float invT, float m, float S, int exclude, uint32_t j,
-                                          uint32_t ireq, uint32_t k0, uint32_t k1, bool aligned)
+// Order the entries buf[0, cnt) roughly best first into tmp, by the whole CTA: kBins bins of
+// equal width in key bound, from the largest bound down to 40 below it (lower bounds share the
+// last bin), bin 0 first, any order inside a bin. The bin of an entry goes to bits 24..31 of its
+// low word (groups are < 2^24); bin_max[b] is the largest bound in bin b.
+__device__ void bin_order(const SearchSmem &sm, int cnt)
 {
-    constexpr int kStride = 4 * kThreads;
-    uint32_t lc[sizeof(T)], ln[sizeof(T)], qc[4] = {0u, 0u, 0u, 0u}, qn[4] = {0u, 0u, 0u, 0u};
-    unsigned g_seen = kKeyNone;
-    const int warp_first = b + 4 * static_cast<int>(threadIdx.x & ~31u);
-    int v0 = b + 4 * static_cast<int>(threadIdx.x);
-    if (v0 < e) load_quad<T, kResidual>(lc, qc, rp, qrow, v0, e, aligned);
-    int step = 0;
-    for (int wf = warp_first; wf < e; wf += kStride, v0 += kStride, ++step) {
-        if (v0 + kStride < e) load_quad<T, kResidual>(ln, qn, rp, qrow, v0 + kStride, e, aligned);
-        pull_threshold(st, s_thr, g_thr, step, g_seen);
-        const bool raised = race_step<T, kResidual>(st, s_thr, lc, qc, v0, e, invT, m, S, exclude,
-                                                    j, ireq, k0, k1);
-        push_threshold(st, g_thr, raised);
-#pragma unroll
-        for (int k = 0; k < static_cast<int>(sizeof(T)); ++k) lc[k] = ln[k];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) qc[k] = qn[k];
+    const int tid = threadIdx.x;
+    if (tid < kBins) {
+        sm.bin_n[tid] = 0;
+        sm.bin_max[tid] = 0u;
     }
-}
-
-// Block reduction of (key, idx); result valid in thread 0.
-__device__ __forceinline__ void block_reduce_race(float &kb, int &ib)
-{
-    __shared__ float sh_k[kThreads / 32];
-    __shared__ int sh_i[kThreads / 32];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float k2 = __shfl_xor_sync(0xFFFFFFFFu, kb, o);
-        const int i2 = __shfl_xor_sync(0xFFFFFFFFu, ib, o);
-        if (race_better(k2, i2, kb, ib)) {
-            kb = k2;
-            ib = i2;
-        }
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();  // sh_* may still be read by a previous reduction
-    if (lane == 0) {
-        sh_k[warp] = kb;
-        sh_i[warp] = ib;
+    if (tid == 0) {
+        sm.range[0] = 0u;
+        sm.range[1] = 0xFFFFFFFFu;
     }
     __syncthreads();
-    if (warp == 0) {
-        kb = lane < kThreads / 32 ? sh_k[lane] : -kInf;
-        ib = lane < kThreads / 32 ? sh_i[lane] : -1;
+    unsigned hi = 0u, lo = 0xFFFFFFFFu;
+    for (int e = tid; e < cnt; e += kThreads) {
+        const unsigned kb = static_cast<unsigned>(sm.buf[e] >> 32);
+        hi = max(hi, kb);
+        lo = min(lo, kb);
+    }
+    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
+    if ((tid & 31) == 0) {
+        atomicMax(&sm.range[0], hi);
+        atomicMin(&sm.range[1], lo);
+    }
+    __syncthreads();
+    const float top = key_dec(sm.range[0]);
+    const float bottom = fmaxf(key_dec(sm.range[1]), top - 40.0f);
+    const float inv_w = (top - bottom) > 0.0f ? kBins / (top - bottom) : 0.0f;
+    for (int e = tid; e < cnt; e += kThreads) {
+        const unsigned kb = static_cast<unsigned>(sm.buf[e] >> 32);
+        const float t = (top - key_dec(kb)) * inv_w;  // NaN / inf go to the last bin
+        const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
+        atomicAdd(&sm.bin_n[b], 1);
+        atomicMax(&sm.bin_max[b], kb);
+    }
+    __syncthreads();
+    if (tid < 32) {  // exclusive prefix of the bin counts (kBins == 32)
+        const int n = sm.bin_n[tid];
+        int x = n;
 #pragma unroll
-        for (int o = 4; o > 0; o >>= 1) {
-            const float k2 = __shfl_xor_sync(0xFFFFFFFFu, kb, o);
-            const int i2 = __shfl_xor_sync(0xFFFFFFFFu, ib, o);
-            if (race_better(k2, i2, kb, ib)) {
-                kb = k2;
-                ib = i2;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (tid >= o) x += y;
+        }
+        sm.bin_n[tid] = x - n;  // running cursor, starts at the bin's first slot
+    }
+    __syncthreads();
+    for (int e = tid; e < cnt; e += kThreads) {
+        const unsigned long long ent = sm.buf[e];
+        const float t = (top - key_dec(static_cast<unsigned>(ent >> 32))) * inv_w;
+        const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
+        const int pos = atomicAdd(&sm.bin_n[b], 1);
+        sm.tmp[pos] = (ent & 0xFFFFFFFF00000000ull) | (static_cast<unsigned long long>(b) << 24) |
+                      (ent & 0x00FFFFFFull);
+    }
+    __syncthreads();
+}
+
+// Best-first race over one row by the whole CTA. Returns the packed winner (key, ~v), 0 when no
+// token is a candidate. lm must hold the row's line maxima (it is overwritten).
+template <typename T, bool kRes>
+__device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &rl,
+                                          const SearchSmem &sm)
+{
+    constexpr int B = 4;  // groups per warp and step
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const unsigned long long mine = group_bounds<T>(r, rl, sm);
+    if (tid == 0) {
+        *sm.best = 0;
+        *sm.cnt = 0;
+    }
+    __syncthreads();  // bounds complete: lm is free from here on (buf reuses it)
+    // round 1: every warp evaluates its own best-bounded group
+    const unsigned long long wb = warp_max_u64(mine);
+    if (wb != 0) {
+        const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
+        eval_groups<T, kRes, 1>(r, gs, sm);
+        if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
+    }
+    __syncthreads();
+    // round 2: every group whose bound reaches the best key found so far, best bound first
+    const unsigned long long best1 = *sm.best;
+    const unsigned thr1 = static_cast<unsigned>(best1 >> 32);
+    for (int g0 = 0; g0 < r.G; g0 += kThreads) {
+        const int g = g0 + tid;
+        unsigned kb = 0;
+        bool take = false;
+        if (g < r.G) {
+            const float b = sm.pb[g];
+            if (b == b) {
+                kb = key_enc(key_bound(kRes ? __fsub_rn(b, r.m) : b));
+                take = best1 == 0 || kb >= thr1;
             }
         }
+        const unsigned msk = __ballot_sync(0xFFFFFFFFu, take);
+        int pos = 0;
+        if (lane == 0 && msk) pos = atomicAdd(sm.cnt, __popc(msk));
+        pos = __shfl_sync(0xFFFFFFFFu, pos, 0) + __popc(msk & ((1u << lane) - 1u));
+        if (take) sm.buf[pos] = (static_cast<unsigned long long>(kb) << 32) | static_cast<unsigned>(g);
     }
-}
-
-// Race over [b, e) of one row by the whole CTA. s_thr: the CTA's shared threshold word, set by
-// the caller before a __syncthreads; g_thr: the request's global threshold word or nullptr.
-template <typename T>
-__device__ void race_row(float &kb, int &ib, unsigned *s_thr, unsigned *g_thr, const T *rp,
-                         const float *qrow, int b, int e, float invT, float m, float S,
-                         int exclude, uint32_t j, uint32_t ireq, uint64_t seed, bool aligned)
-{
-    RaceState st;
-    refresh(st);
-    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-    if (qrow)
-        race_span<T, true>(st, s_thr, g_thr, rp, qrow, b, e, invT, m, S, exclude, j, ireq, k0, k1,
-                           aligned);
-    else
-        race_span<T, false>(st, s_thr, g_thr, rp, qrow, b, e, invT, m, S, exclude, j, ireq, k0, k1,
-                            aligned);
-    kb = st.kb;
-    ib = st.ib;
-    block_reduce_race(kb, ib);
-}
-
-// The raced rows of all sampling requests, concatenated and split evenly over the CTAs. Each
-// row occupies Vp = V rounded up to a multiple of 16 elements of that concatenation, so that
-// every segment starts on a clock-block boundary within its row; a CTA whose segment lies in
-// the padding publishes an empty partial.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 3)
-sv_race_kernel(const T *__restrict__ logits, int V, int chunk_fixed, int maxseg,
-               const ReqState *__restrict__ reqstate, const int *__restrict__ rand_req,
-               const int *__restrict__ n_rand, const int32_t *__restrict__ draft_ids,
-               const float *__restrict__ q, uint64_t seed, uint32_t req_base,
-               RacePart *__restrict__ part, unsigned *__restrict__ race_counter,
-               unsigned *__restrict__ race_thr, int32_t *__restrict__ sampled, int stride,
-               int32_t *__restrict__ num_sampled, int32_t *__restrict__ num_rejected,
-               const unsigned *__restrict__ flags, bool aligned)
-{
-    if (flags[0]) return;
-    const int Vp = (V + 15) & ~15;
-    const long long total = static_cast<long long>(*n_rand) * Vp;
-    long long chunk = chunk_fixed;
-    if (chunk <= 0) {
-        chunk = (total + gridDim.x - 1) / gridDim.x;
-        chunk = max((chunk + 15) / 16 * 16, static_cast<long long>(kMinChunk));
-    }
-    const long long start = static_cast<long long>(blockIdx.x) * chunk;
-    const long long stop = min(total, start + chunk);
-    if (start >= stop) return;
-
-    __shared__ unsigned s_thr;
-    __shared__ int s_last, s_token;
-    const int vr_first = static_cast<int>(start / Vp);
-    const int vr_last = static_cast<int>((stop - 1) / Vp);
-    for (int vr = vr_first; vr <= vr_last; ++vr) {
-        const long long vbase = static_cast<long long>(vr) * Vp;
-        const int b = static_cast<int>(max(start, vbase) - vbase);
-        const int e = static_cast<int>(min(min(stop, vbase + Vp) - vbase, static_cast<long long>(V)));
-        const int fk = static_cast<int>(vbase / chunk);
-        const int nseg = static_cast<int>((vbase + Vp - 1) / chunk) - fk + 1;
-        const int seg = static_cast<int>(blockIdx.x) - fk;
-        const int i = rand_req[vr];
-        const ReqState rq = reqstate[i];
-        const T *rp = logits + static_cast<size_t>(rq.row) * static_cast<size_t>(V);
-        const float *qrow = (rq.jstar < rq.K && q) ? q + static_cast<size_t>(rq.q0 + rq.jstar) * V
-                                                   : nullptr;
-        const uint32_t ireq = req_base + static_cast<uint32_t>(i);
-        if (threadIdx.x == 0) s_thr = rq.seed;  // the argmax token's key seeds the threshold
-        __syncthreads();
-        float kb;
-        int ib;
-        race_row<T>(kb, ib, &s_thr, &race_thr[i], rp, qrow, b, e, rq.invT, rq.m, rq.S, rq.excl,
-                    static_cast<uint32_t>(rq.jstar), ireq, seed, aligned);
-        if (nseg > 1) {
-            if (threadIdx.x == 0) {
-                part[static_cast<size_t>(i) * maxseg + seg] = RacePart{kb, ib};
-                __threadfence();
-                const unsigned ticket = atomicAdd(&race_counter[i], 1u);
-                s_last = ticket == static_cast<unsigned>(nseg - 1);
-            }
-            __syncthreads();
-            if (!s_last) continue;
-            __threadfence();
-            if (threadIdx.x < 32) {
-                float kw = -kInf;
-                int iw = -1;
-                for (int k = threadIdx.x; k < nseg; k += 32) {
-                    const float2 raw = __ldcg(reinterpret_cast<const float2 *>(part) +
-                                              static_cast<size_t>(i) * maxseg + k);
-                    const int i2 = __float_as_int(raw.y);
-                    if (race_better(raw.x, i2, kw, iw)) {
-                        kw = raw.x;
-                        iw = i2;
-                    }
-                }
+    __syncthreads();
+    const int cnt = *sm.cnt;
+    bin_order(sm, cnt);
+    for (int e0 = warp * B; e0 < cnt; e0 += kWarps * B) {
+        const unsigned long long cur = ld_best(sm.best);
+        const unsigned thr = static_cast<unsigned>(cur >> 32);
+        int gs[B];
+        bool done = false;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float k2 = __shfl_xor_sync(0xFFFFFFFFu, kw, o);
-                    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, iw, o);
-                    if (race_better(k2, i2, kw, iw)) {
-                        kw = k2;
-                        iw = i2;
-                    }
-                }
-                if (threadIdx.x == 0) {
-                    ib = iw;
-                    race_counter[i] = 0u;
+        for (int k = 0; k < B; ++k) {
+            gs[k] = -1;
+            const int e = e0 + k;
+            if (e < cnt && !done) {
+                const unsigned long long ent = sm.tmp[e];
+                const int bin = static_cast<int>((ent >> 24) & 0xFFu);
+                if (cur != 0 && sm.bin_max[bin] < thr) {
+                    done = true;  // this bin and every later one lie below the best key
+                } else if (cur == 0 || static_cast<unsigned>(ent >> 32) >= thr) {
+                    gs[k] = static_cast<int>(ent & 0x00FFFFFFull);
                 }
             }
         }
-        if (threadIdx.x == 0) s_token = ib;
-        __syncthreads();
-        int token = s_token;
-        if (token < 0) {
-            // Nothing left after rounding (residual with p <= q everywhere, or V == 1 with the
-            // only token excluded): draw from p itself so the output stays a target-side draw.
-            if (threadIdx.x == 0) s_thr = rq.seed_p;
-            __syncthreads();
-            race_row<T>(kb, ib, &s_thr, nullptr, rp, nullptr, 0, V, rq.invT, rq.m, rq.S, -1,
-                        static_cast<uint32_t>(rq.jstar), ireq, seed, aligned);
-            if (threadIdx.x == 0) s_token = ib;
-            __syncthreads();
-            token = s_token;
-        }
-        emit_row(i, rq.jstar, rq.K, rq.q0, token, draft_ids, sampled, stride, num_sampled,
-                 num_rejected, threadIdx.x, kThreads);
-        __syncthreads();  // s_thr / s_token are reused by the next row of this CTA
+        eval_groups<T, kRes, B>(r, gs, sm);
+        if (done) break;
     }
+    __syncthreads();
+    return *sm.best;
 }
 
-
-// ---------------------------------------------------------------------------------------
-// Race with the raced rows staged through shared memory: same partition and results as
-// sv_race_kernel, for rows that start on 16-byte boundaries. The CTA's segments are cut into
-// stages of up to kRaceStageTok tokens (never crossing a row); one thread issues bulk copies of
-// each stage's logits and q into a ring of kRaceStages buffers, so that several stages per CTA
-// are in flight while the warps screen the current one from shared memory.
-// ---------------------------------------------------------------------------------------
-constexpr int kRaceStageTok = 2048;
-constexpr int kRaceStages = 4;
-template <typename T> __host__ __device__ constexpr int race_stage_bytes() { return kRaceStageTok * (static_cast<int>(sizeof(T)) + 4); }
-
-// Segment of virtual row vr inside [start, stop): token range [b, e) of the real row.
-struct RaceSeg {
-    int b, e;
-};
-__device__ __forceinline__ RaceSeg race_seg(int vr, int Vp, int V, long long start, long long stop)
-{
-    const long long vbase = static_cast<long long>(vr) * Vp;
-    const int b = static_cast<int>(max(start, vbase) - vbase);
-    const int e = static_cast<int>(min(min(stop, vbase + Vp) - vbase, static_cast<long long>(V)));
-    return RaceSeg{b, max(b, e)};
-}
-
+// One CTA per request.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 2)
-sv_race_bulk_kernel(const T *__restrict__ logits, int V, int chunk_fixed, int maxseg,
-                    const ReqState *__restrict__ reqstate, const int *__restrict__ rand_req,
-                    const int *__restrict__ n_rand, const int32_t *__restrict__ draft_ids,
-                    const float *__restrict__ q, uint64_t seed, uint32_t req_base,
-                    RacePart *__restrict__ part, unsigned *__restrict__ race_counter,
-                    unsigned *__restrict__ race_thr, int32_t *__restrict__ sampled, int stride,
-                    int32_t *__restrict__ num_sampled, int32_t *__restrict__ num_rejected,
-                    unsigned *__restrict__ flags)
+sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, VerifyParams P)
 {
-    extern __shared__ __align__(128) unsigned char ring[];
-    __shared__ __align__(8) uint64_t full[kRaceStages];
-    __shared__ unsigned s_thr;
-    __shared__ int s_last, s_token, s_abort;
-    if (flags[0]) return;
-    const int Vp = (V + 15) & ~15;
-    const long long total = static_cast<long long>(*n_rand) * Vp;
-    long long chunk = chunk_fixed;
-    if (chunk <= 0) {
-        chunk = (total + gridDim.x - 1) / gridDim.x;
-        chunk = max((chunk + 15) / 16 * 16, static_cast<long long>(kMinChunk));
-    }
-    const long long start = static_cast<long long>(blockIdx.x) * chunk;
-    const long long stop = min(total, start + chunk);
-    if (start >= stop) return;
-    const int vr_first = static_cast<int>(start / Vp);
-    const int vr_last = static_cast<int>((stop - 1) / Vp);
-    constexpr int kStageBytes = race_stage_bytes<T>();
-    constexpr int kQOff = kRaceStageTok * static_cast<int>(sizeof(T));  // q part of a stage
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ int s_js;
+    __shared__ unsigned long long s_best;
+    __shared__ int s_cnt;
+    __shared__ int s_bin_n[kBins];
+    __shared__ unsigned s_bin_max[kBins];
+    __shared__ unsigned s_range[2];
+    const int i = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = P.rq.n;
+    const int32_t *__restrict__ cu = P.rq.cu;
+    const int stride = P.kmax + 1;
+    const VerifyLayout lay = verify_layout(P.V, P.kmax);
 
-    // producer (thread 0): walks the same stage sequence as the consumers, ahead of them
-    int p_vr = vr_first, p_tok = 0, p_end = 0, issued = 0;
-    const T *p_rp = nullptr;
-    const float *p_q = nullptr;
-    auto p_enter_row = [&]() {  // position the producer at the first stage of row p_vr
-        while (p_vr <= vr_last) {
-            const RaceSeg sg = race_seg(p_vr, Vp, V, start, stop);
-            if (sg.b < sg.e) {
-                const ReqState rq = reqstate[rand_req[p_vr]];
-                p_rp = logits + static_cast<size_t>(rq.row) * static_cast<size_t>(V);
-                p_q = (rq.jstar < rq.K && q) ? q + static_cast<size_t>(rq.q0 + rq.jstar) * V : nullptr;
-                p_tok = sg.b;
-                p_end = sg.e;
-                return;
-            }
-            ++p_vr;
+    // 0. the batch must be consistent; every CTA checks all of cu_num_draft (small, in L2)
+    const int q0 = __ldg(cu + i);
+    const int K = __ldg(cu + i + 1) - q0;
+    if (tid == 0) s_js = K;
+    int bad = 0;
+    for (int t = tid; t <= n; t += kThreads) {
+        const int c0 = __ldg(cu + t);
+        if (t == 0) bad |= c0 != 0;
+        if (t == n) bad |= c0 != P.nd;
+        if (t < n) {
+            const int c1 = __ldg(cu + t + 1);
+            bad |= (c1 < c0) | (static_cast<long long>(c1) - c0 > P.kmax) | (c0 < 0) | (c1 > P.nd);
         }
-    };
-    auto p_issue = [&](int buf) {  // issue the next stage into ring buffer buf, if any
-        if (p_vr > vr_last) return;
-        const int n = min(kRaceStageTok, p_end - p_tok);
-        const uint32_t lb = static_cast<uint32_t>(n) * sizeof(T);
-        const uint32_t qb = p_q ? static_cast<uint32_t>(n) * 4u : 0u;
-        unsigned char *dst = ring + buf * kStageBytes;
-        mbar_expect(&full[buf], lb + qb);
-        bulk_load(dst, p_rp + p_tok, lb, &full[buf]);
-        if (qb) bulk_load(dst + kQOff, p_q + p_tok, qb, &full[buf]);
-        ++issued;
-        p_tok += n;
-        if (p_tok >= p_end) {
-            ++p_vr;
-            p_enter_row();
+    }
+    if (__syncthreads_or(bad)) {  // an inconsistent batch emits nothing for any request
+        emit_row(i, -1, 0, 0, -1, nullptr, P.sampled, stride, P.num_sampled, P.num_rejected, tid,
+                 kThreads);
+        if (i == 0 && tid == 0) atomicOr(P.flags + 1, SV_ERR_BATCH);
+        return;
+    }
+    const int row0 = q0 + i;
+    bool greedy;
+    const float invT = request_invT(P.rq.temperature, P.rq.is_greedy, i, greedy);
+    const float c = invT * kLog2e;
+    const uint32_t ireq = P.req_base + static_cast<uint32_t>(i);
+    float *sm_m = reinterpret_cast<float *>(dyn + lay.rows), *sm_S = sm_m + stride;
+    int *sm_amax = reinterpret_cast<int *>(sm_m + 2 * stride);
+
+    // 1. row statistics from the partials (warp per row) and the acceptance tests
+    for (int j = warp; j <= K; j += kWarps) {
+        const int row = row0 + j;
+        const long long rbase = static_cast<long long>(row) * P.V;
+        const int nseg = static_cast<int>((P.base_off + rbase + P.V - 1) / P.chunk) -
+                         static_cast<int>((P.base_off + rbase) / P.chunk) + 1;
+        float L = -kInf, s = 0.0f;
+        int idx = INT_MAX;
+        for (int k = lane; k < nseg; k += 32) {
+            const float4 raw = __ldg(reinterpret_cast<const float4 *>(P.part) +
+                                     static_cast<size_t>(row) * P.maxseg + k);
+            combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
         }
-    };
-    if (threadIdx.x == 0) {
-        for (int b2 = 0; b2 < kRaceStages; ++b2) mbar_init(&full[b2], 1);
-        mbar_fence_init();
-        s_abort = 0;
-        p_enter_row();
-        for (int b2 = 0; b2 < kRaceStages; ++b2) p_issue(b2);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
+            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
+            const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
+            combine_stat(L, s, idx, L2, s2, i2, c);
+        }
+        if (lane == 0) {
+            const float m = __fmul_rn(L, invT);  // = max_v fl(l_v / T): rounding is monotone
+            const int amax = idx == INT_MAX ? 0 : idx;
+            sm_m[j] = m;
+            sm_S[j] = s;
+            sm_amax[j] = amax;
+            if (P.opt_max) P.opt_max[row] = m;
+            if (P.opt_sum) P.opt_sum[row] = s;
+            if (P.opt_amax) P.opt_amax[row] = amax;
+            if (j < K && !accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j, invT, m, s, amax,
+                                          P.draft_ids, P.q, P.seed, ireq))
+                atomicMin(&s_js, j);
+        }
     }
     __syncthreads();
+    const int js = s_js;  // [MTP-eagle] _rejection_sample_kernel: first rejection, K if none
+    if (greedy) {  // [spec-notes] 8.3: the target argmax at the mismatch, or of the bonus row
+        emit_row(i, js, K, q0, sm_amax[js], P.draft_ids, P.sampled, stride, P.num_sampled,
+                 P.num_rejected, tid, kThreads);
+        return;
+    }
 
-    const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-    int k = 0;  // consumer's stage counter
-    bool aborted = false;
-    for (int vr = vr_first; vr <= vr_last && !aborted; ++vr) {
-        const RaceSeg sg = race_seg(vr, Vp, V, start, stop);
-        const long long vbase = static_cast<long long>(vr) * Vp;
-        const int fk = static_cast<int>(vbase / chunk);
-        const int nseg = static_cast<int>((vbase + Vp - 1) / chunk) - fk + 1;
-        const int seg = static_cast<int>(blockIdx.x) - fk;
-        const int i = rand_req[vr];
-        const ReqState rq = reqstate[i];
-        const bool residual = rq.jstar < rq.K && q != nullptr;
-        const uint32_t ireq = req_base + static_cast<uint32_t>(i);
-        const uint32_t j = static_cast<uint32_t>(rq.jstar);
-        if (threadIdx.x == 0) s_thr = rq.seed;  // the argmax token's key seeds the threshold
+    // 2. the race at j*
+    const int row = row0 + js;
+    RaceRow<T> r;
+    r.rp = logits + static_cast<size_t>(row) * P.V;
+    r.V = P.V;
+    r.G = (P.V + kGroup - 1) / kGroup;
+    r.m = sm_m[js];
+    r.S = sm_S[js];
+    r.invT = invT;
+    r.j = static_cast<uint32_t>(js);
+    r.ireq = ireq;
+    r.k0 = static_cast<uint32_t>(P.seed);
+    r.k1 = static_cast<uint32_t>(P.seed >> 32);
+    const bool residual = js < K && P.q != nullptr;
+    r.qrow = residual ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
+    r.excl = (js < K && P.q == nullptr) ? __ldg(P.draft_ids + q0 + js) : -1;
+    SearchSmem sm;
+    sm.buf = reinterpret_cast<unsigned long long *>(dyn);
+    sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
+    sm.bin_n = s_bin_n;
+    sm.bin_max = s_bin_max;
+    sm.range = s_range;
+    sm.lm = reinterpret_cast<float *>(dyn);
+    sm.pb = reinterpret_cast<float *>(dyn + lay.pb);
+    sm.eg = reinterpret_cast<float *>(dyn + lay.eg);
+    sm.ag = dyn + lay.ag;
+    sm.best = &s_best;
+    sm.cnt = &s_cnt;
+    const RowLines rl = row_lines(row, P.V, P.base_off);
+    row_line_max<T>(r.rp, P.V, rl, lines, sm.lm);
+    __syncthreads();
+    unsigned long long best = residual ? race_search<T, true>(r, rl, sm)
+                                       : race_search<T, false>(r, rl, sm);
+    if (best == 0) {
+        // nothing left of max(0, p - q) after rounding, or V == 1 with the only token rejected:
+        // draw from p itself
+        row_line_max<T>(r.rp, P.V, rl, lines, sm.lm);
         __syncthreads();
-        RaceState st;
-        refresh(st);
-        unsigned g_seen = kKeyNone;
-        int step = 0;
-        for (int t0 = sg.b; t0 < sg.e; t0 += kRaceStageTok, ++k) {
-            const int n = min(kRaceStageTok, sg.e - t0);
-            const int buf = k % kRaceStages;
-            if (!mbar_wait(&full[buf], static_cast<uint32_t>(k / kRaceStages) & 1u, kWaitNs)) {
-                s_abort = 1;
-                atomicOr(&flags[1], SV_ERR_TIMEOUT);
-            }
-            const unsigned char *stage = ring + buf * kStageBytes;
-            for (int pass = 0; pass * 4 * kThreads < n; ++pass, ++step) {
-                const int tl = pass * 4 * kThreads + 4 * static_cast<int>(threadIdx.x);  // in stage
-                uint32_t lc[sizeof(T)], qc[4] = {0u, 0u, 0u, 0u};
-                if (tl < n) {
-                    if constexpr (sizeof(T) == 2) {
-                        const uint2 w = *reinterpret_cast<const uint2 *>(stage + tl * 2);
-                        lc[0] = w.x;
-                        lc[1] = w.y;
-                    } else {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(stage + tl * 4);
-                        lc[0] = w.x; lc[1] = w.y; lc[2] = w.z; lc[3] = w.w;
-                    }
-                    if (residual) {
-                        const uint4 w = *reinterpret_cast<const uint4 *>(stage + kQOff + tl * 4);
-                        qc[0] = w.x; qc[1] = w.y; qc[2] = w.z; qc[3] = w.w;
-                    }
-                } else {
-#pragma unroll
-                    for (int h = 0; h < static_cast<int>(sizeof(T)); ++h) lc[h] = 0xFF80FF80u;
-                }
-                pull_threshold(st, &s_thr, &race_thr[i], step, g_seen);
-                bool raised;
-                if (residual)
-                    raised = race_step<T, true>(st, &s_thr, lc, qc, t0 + tl, sg.e, rq.invT, rq.m,
-                                                rq.S, rq.excl, j, ireq, k0, k1);
-                else
-                    raised = race_step<T, false>(st, &s_thr, lc, qc, t0 + tl, sg.e, rq.invT, rq.m,
-                                                 rq.S, rq.excl, j, ireq, k0, k1);
-                push_threshold(st, &race_thr[i], raised);
-            }
-            __syncthreads();  // every thread is done with this buffer
-            if (s_abort) {
-                aborted = true;
-                break;
-            }
-            if (threadIdx.x == 0) {
-                fence_proxy_async_smem();
-                p_issue(buf);
-            }
-        }
-        if (aborted) break;
-        float kb = st.kb;
-        int ib = st.ib;
-        block_reduce_race(kb, ib);
-        if (nseg > 1) {
-            if (threadIdx.x == 0) {
-                part[static_cast<size_t>(i) * maxseg + seg] = RacePart{kb, ib};
-                __threadfence();
-                const unsigned ticket = atomicAdd(&race_counter[i], 1u);
-                s_last = ticket == static_cast<unsigned>(nseg - 1);
-            }
-            __syncthreads();
-            if (!s_last) continue;
-            __threadfence();
-            if (threadIdx.x < 32) {
-                float kw = -kInf;
-                int iw = -1;
-                for (int kk = threadIdx.x; kk < nseg; kk += 32) {
-                    const float2 raw = __ldcg(reinterpret_cast<const float2 *>(part) +
-                                              static_cast<size_t>(i) * maxseg + kk);
-                    const int i2 = __float_as_int(raw.y);
-                    if (race_better(raw.x, i2, kw, iw)) {
-                        kw = raw.x;
-                        iw = i2;
-                    }
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    const float k2 = __shfl_xor_sync(0xFFFFFFFFu, kw, o);
-                    const int i2 = __shfl_xor_sync(0xFFFFFFFFu, iw, o);
-                    if (race_better(k2, i2, kw, iw)) {
-                        kw = k2;
-                        iw = i2;
-                    }
-                }
-                if (threadIdx.x == 0) {
-                    ib = iw;
-                    race_counter[i] = 0u;
-                }
-            }
-        }
-        if (threadIdx.x == 0) s_token = ib;
-        __syncthreads();
-        int token = s_token;
-        if (token < 0) {
-            // nothing left of the residual after rounding: draw from p itself (global reads)
-            const T *rp = logits + static_cast<size_t>(rq.row) * static_cast<size_t>(V);
-            if (threadIdx.x == 0) s_thr = rq.seed_p;
-            __syncthreads();
-            race_row<T>(kb, ib, &s_thr, nullptr, rp, nullptr, 0, V, rq.invT, rq.m, rq.S, -1, j,
-                        ireq, seed, true);
-            if (threadIdx.x == 0) s_token = ib;
-            __syncthreads();
-            token = s_token;
-        }
-        emit_row(i, rq.jstar, rq.K, rq.q0, token, draft_ids, sampled, stride, num_sampled,
-                 num_rejected, threadIdx.x, kThreads);
-        __syncthreads();  // s_thr / s_token are reused by the next row of this CTA
+        r.excl = -1;
+        best = race_search<T, false>(r, rl, sm);
     }
-    if (aborted && threadIdx.x == 0) {
-        // let the copies still in flight land before the CTA's shared memory is released
-        for (int kk = k + 1; kk < issued; ++kk)
-            mbar_wait(&full[kk % kRaceStages], static_cast<uint32_t>(kk / kRaceStages) & 1u, kWaitNs / 4);
-    }
+    emit_row(i, js, K, q0, static_cast<int>(~static_cast<unsigned>(best)), P.draft_ids, P.sampled,
+             stride, P.num_sampled, P.num_rejected, tid, kThreads);
 }
 
 // ---------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------
 constexpr int kProfRing = 512;
-
-constexpr int kKernels = 4;  // plan, stats, finalize, race
+constexpr int kKernels = 2;  // stats, verify
+// static shared memory of a verify CTA besides the dynamic part (reserve)
+constexpr int kVerifyStaticSmem = 1024;
 
 struct ProfSlot {
     cudaEvent_t ev[kKernels + 1];
     bool pending;
 };
 
-int round_up8(int x) { return (x + 7) / 8 * 8; }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+size_t verify_smem_bytes(int V, int kmax) { return verify_layout(V, kmax).total; }
 
 }  // namespace
 
@@ -1344,18 +1021,11 @@ struct spec_verify_ctx {
     int device = 0;
     int max_num_reqs = 0, max_spec_len = 0, V = 0, dtype = SV_F32, has_q = 0;
     int max_rows = 0, maxseg = 0;
-    int stats_chunk = 0, race_chunk = 0;  // 0: automatic (even split over the grid)
-    int stats_ctas = 1, race_ctas = 1;    // one wave of each kernel (SMs x CTAs per SM)
-    int race_bulk_ctas = 1;
-    RowInfo *rowinfo = nullptr;
-    RowStat *rowstat = nullptr;
+    int stats_chunk = 0;   // 0: automatic (even split over whole waves)
+    int stats_ctas = 1;    // one wave of the statistics kernel (SMs x CTAs per SM)
     StatPart *statpart = nullptr;
-    ReqState *reqstate = nullptr;
-    RacePart *racepart = nullptr;
-    // [N] rows done | [N] race counters | [N] race thresholds | [N] sampling-request list |
-    // [1] its length
-    unsigned *counters = nullptr;
-    unsigned *flags = nullptr;  // [0] per-call batch-invalid, [1] sticky error word
+    void *lines = nullptr;      // largest logit of every 64-element line (logits dtype), or null
+    unsigned *flags = nullptr;  // [1] sticky error word
     // host-buffer staging
     void *io_logits = nullptr;
     float *io_q = nullptr;
@@ -1366,20 +1036,10 @@ struct spec_verify_ctx {
     bool prof = false;
     std::vector<ProfSlot> ring;
     int64_t prof_calls = 0, prof_done = 0;
-    double prof_ms[kKernels] = {0, 0, 0, 0};
+    double prof_ms[kKernels] = {0, 0};
 };
 
 namespace {
-
-constexpr size_t counter_words(size_t reqs) { return 4 * reqs + 1; }
-
-ReqWords req_words(spec_verify_ctx *ctx)
-{
-    unsigned *base = ctx->counters;
-    const size_t N = static_cast<size_t>(ctx->max_num_reqs);
-    return ReqWords{base, base + N, base + 2 * N, reinterpret_cast<int *>(base + 3 * N),
-                    reinterpret_cast<int *>(base + 4 * N)};
-}
 
 struct DeviceGuard {
     int prev = -1;
@@ -1413,12 +1073,8 @@ void prof_collect(spec_verify_ctx *ctx, ProfSlot &s)
 
 void free_all(spec_verify_ctx *ctx)
 {
-    cudaFree(ctx->rowinfo);
-    cudaFree(ctx->rowstat);
     cudaFree(ctx->statpart);
-    cudaFree(ctx->reqstate);
-    cudaFree(ctx->racepart);
-    cudaFree(ctx->counters);
+    cudaFree(ctx->lines);
     cudaFree(ctx->flags);
     cudaFree(ctx->io_logits);
     cudaFree(ctx->io_q);
@@ -1430,21 +1086,32 @@ void free_all(spec_verify_ctx *ctx)
     ctx->ring.clear();
 }
 
-// Allow the staged race its shared-memory ring and report how many CTAs of each kernel fit on
-// one SM (for the one-wave grids).
-template <typename T>
-cudaError_t occupancy(int *stats_per_sm, int *race_per_sm, int *race_bulk_per_sm)
+int optin_smem(int device)
 {
-    cudaError_t e = cudaFuncSetAttribute(sv_race_bulk_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kRaceStages * race_stage_bytes<T>());
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
+}
+
+// Largest dynamic shared memory a verify CTA may use on `device`.
+size_t verify_smem_limit(int device)
+{
+    return static_cast<size_t>(std::max(optin_smem(device) - kVerifyStaticSmem, 0));
+}
+
+// Allow the verify kernel the device's opt-in shared memory and report how many statistics
+// CTAs fit on one SM (for the whole-wave grid).
+template <typename T>
+cudaError_t setup_kernels(int device, int *stats_per_sm)
+{
+    const cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(verify_smem_limit(device)));
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T>, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(race_bulk_per_sm, sv_race_bulk_kernel<T>,
-                                                      kThreads, kRaceStages * race_stage_bytes<T>());
-    if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(race_per_sm, sv_race_kernel<T>, kThreads, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T>, kThreads, 0);
 }
 
 template <typename T>
@@ -1456,25 +1123,37 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
 {
     const int V = ctx->V;
     const int rows = nd + num_reqs;
-    const int stride = kmax + 1;
-    const ReqWords rw = req_words(ctx);
-
     // statistics: the flattened [rows x V] logits split evenly over kStatsWaves waves
     const long long total = static_cast<long long>(rows) * V;
+    const int base_off = static_cast<int>((reinterpret_cast<uintptr_t>(logits) % (kGroup * sizeof(T))) / sizeof(T));
     long long chunk1 = ctx->stats_chunk;
     if (chunk1 <= 0) chunk1 = (total + kStatsWaves * ctx->stats_ctas - 1) / (kStatsWaves * ctx->stats_ctas);
-    chunk1 = std::max<long long>((chunk1 + 7) / 8 * 8, kMinChunk);
-    const int grid1 = static_cast<int>((total + chunk1 - 1) / chunk1);
-    // Every row (and q row) starts on a 16-byte boundary when V is a multiple of 8 (bf16) or 4
-    // (fp32); base pointers are checked to be 16-byte aligned: the race can use vector loads and
-    // stage the rows through shared memory with bulk copies.
-    const bool aligned = V % static_cast<int>(16 / sizeof(T)) == 0;
-    // race: the raced rows (at most one per request) split evenly over kRaceWaves waves
-    const int grid2 = ctx->race_chunk > 0
-                          ? static_cast<int>((static_cast<long long>(num_reqs) * ((V + 15) & ~15) + ctx->race_chunk - 1) / ctx->race_chunk)
-                          : kRaceWaves * (aligned ? ctx->race_bulk_ctas : ctx->race_ctas);
-    const StatsOut so{ctx->rowstat, ctx->reqstate, rw.rows_done, sampled, num_sampled, num_rejected,
-                      stride, opt_max, opt_sum, opt_amax};
+    chunk1 = std::max<long long>((chunk1 + kGroup - 1) / kGroup * kGroup, kMinChunk);
+    const int grid1 = static_cast<int>((total + base_off + chunk1 - 1) / chunk1);
+    const RequestTable rq{cu, temperature, is_greedy, num_reqs};
+    T *lines = static_cast<T *>(ctx->lines);
+
+    VerifyParams P;
+    P.rq = rq;
+    P.draft_ids = draft_ids;
+    P.q = q;
+    P.part = ctx->statpart;
+    P.seed = seed;
+    P.req_base = base;
+    P.nd = nd;
+    P.kmax = kmax;
+    P.V = V;
+    P.maxseg = ctx->maxseg;
+    P.base_off = base_off;
+    P.chunk = chunk1;
+    P.sampled = sampled;
+    P.num_sampled = num_sampled;
+    P.num_rejected = num_rejected;
+    P.opt_max = opt_max;
+    P.opt_sum = opt_sum;
+    P.opt_amax = opt_amax;
+    P.flags = ctx->flags;
+    const size_t smem = verify_smem_bytes(V, kmax);
 
     ProfSlot *slot = nullptr;
     if (ctx->prof) {
@@ -1482,29 +1161,12 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
         prof_collect(ctx, *slot);
         cudaEventRecord(slot->ev[0], stream);
     }
-    sv_plan_kernel<<<1, kPlanThreads, 0, stream>>>(cu, temperature, is_greedy, num_reqs, nd, kmax,
-                                                   ctx->rowinfo, rw, sampled, stride, num_sampled,
-                                                   num_rejected, ctx->flags);
-    if (slot) cudaEventRecord(slot->ev[1], stream);
     sv_stats_kernel<T><<<grid1, kThreads, 0, stream>>>(logits, V, total, chunk1, ctx->maxseg,
-                                                       ctx->rowinfo, ctx->statpart, ctx->flags);
-    if (slot) cudaEventRecord(slot->ev[2], stream);
-    sv_finalize_kernel<T><<<(rows + kThreads / 32 - 1) / (kThreads / 32), kThreads, 0, stream>>>(
-        logits, V, rows, chunk1, ctx->maxseg, ctx->rowinfo, ctx->statpart, draft_ids, q, seed,
-        base, so, ctx->flags);
-    if (slot) cudaEventRecord(slot->ev[3], stream);
-    if (aligned)
-        sv_race_bulk_kernel<T><<<grid2, kThreads, kRaceStages * race_stage_bytes<T>(), stream>>>(
-            logits, V, ctx->race_chunk, ctx->maxseg, ctx->reqstate, rw.rand_req, rw.n_rand,
-            draft_ids, q, seed, base, ctx->racepart, rw.race_counter, rw.race_thr, sampled, stride,
-            num_sampled, num_rejected, ctx->flags);
-    else
-        sv_race_kernel<T><<<grid2, kThreads, 0, stream>>>(
-            logits, V, ctx->race_chunk, ctx->maxseg, ctx->reqstate, rw.rand_req, rw.n_rand,
-            draft_ids, q, seed, base, ctx->racepart, rw.race_counter, rw.race_thr, sampled, stride,
-            num_sampled, num_rejected, ctx->flags, aligned);
+                                                       base_off, rq, ctx->statpart, lines);
+    if (slot) cudaEventRecord(slot->ev[1], stream);
+    sv_verify_kernel<T><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
     if (slot) {
-        cudaEventRecord(slot->ev[4], stream);
+        cudaEventRecord(slot->ev[2], stream);
         slot->pending = true;
         ctx->prof_calls++;
     }
@@ -1541,7 +1203,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
     const long long rows = static_cast<long long>(max_num_reqs) * (max_spec_len + 1);
     const long long maxseg = ceil_div(vocab_size, kMinChunk) + 1;
-    if (rows > INT_MAX / 8 || rows * maxseg > (1LL << 31) || static_cast<long long>(max_num_reqs) * maxseg > (1LL << 31))
+    if (rows > INT_MAX / 8 || rows * maxseg > (1LL << 31) || max_spec_len > (1 << 16))
         return SV_ECAPACITY;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
@@ -1553,6 +1215,8 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     if (prop.major != 10 || prop.minor != 3) return SV_EDEVICE;  // built for sm_103a only
     DeviceGuard g(device);
     if (!g.ok) return SV_EDEVICE;
+    // the raced row's group bounds must fit in one CTA's shared memory
+    if (verify_smem_bytes(vocab_size, max_spec_len) > verify_smem_limit(device)) return SV_ECAPACITY;
 
     auto *ctx = new (std::nothrow) spec_verify_ctx();
     if (!ctx) return SV_ECAPACITY;
@@ -1564,22 +1228,16 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     ctx->has_q = has_draft_probs != 0;
     ctx->max_rows = static_cast<int>(rows);
     ctx->maxseg = static_cast<int>(maxseg);
-    const size_t R = static_cast<size_t>(rows), N = static_cast<size_t>(max_num_reqs);
-    const size_t P = static_cast<size_t>(maxseg);
-    const size_t W = counter_words(N);
-    bool ok = cudaMalloc(&ctx->rowinfo, R * sizeof(RowInfo)) == cudaSuccess &&
-              cudaMalloc(&ctx->rowstat, R * sizeof(RowStat)) == cudaSuccess &&
-              cudaMalloc(&ctx->statpart, R * P * sizeof(StatPart)) == cudaSuccess &&
-              cudaMalloc(&ctx->reqstate, N * sizeof(ReqState)) == cudaSuccess &&
-              cudaMalloc(&ctx->racepart, N * P * sizeof(RacePart)) == cudaSuccess &&
-              cudaMalloc(&ctx->counters, W * sizeof(unsigned)) == cudaSuccess &&
+    const size_t R = static_cast<size_t>(rows), S = static_cast<size_t>(maxseg);
+    const size_t nlines = (R * static_cast<size_t>(vocab_size) + 2 * kGroup) / kGroup;
+    const size_t eb = logits_dtype == SV_BF16 ? 2 : 4;
+    bool ok = cudaMalloc(&ctx->statpart, R * S * sizeof(StatPart)) == cudaSuccess &&
+              cudaMalloc(&ctx->lines, nlines * eb) == cudaSuccess &&
               cudaMalloc(&ctx->flags, 2 * sizeof(unsigned)) == cudaSuccess;
-    ok = ok && cudaMemset(ctx->counters, 0, W * sizeof(unsigned)) == cudaSuccess &&
-         cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
-    int stats_per_sm = 0, race_per_sm = 0, race_bulk_per_sm = 0;
-    ok = ok && (logits_dtype == SV_BF16
-                    ? occupancy<uint16_t>(&stats_per_sm, &race_per_sm, &race_bulk_per_sm)
-                    : occupancy<float>(&stats_per_sm, &race_per_sm, &race_bulk_per_sm)) == cudaSuccess;
+    ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
+    int stats_per_sm = 0;
+    ok = ok && (logits_dtype == SV_BF16 ? setup_kernels<uint16_t>(device, &stats_per_sm)
+                                        : setup_kernels<float>(device, &stats_per_sm)) == cudaSuccess;
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_all(ctx);
@@ -1588,8 +1246,6 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
         return SV_ECUDA;
     }
     ctx->stats_ctas = std::max(stats_per_sm, 1) * prop.multiProcessorCount;
-    ctx->race_ctas = std::max(race_per_sm, 1) * prop.multiProcessorCount;
-    ctx->race_bulk_ctas = std::max(race_bulk_per_sm, 1) * prop.multiProcessorCount;
     *out = ctx;
     return SV_OK;
 }
@@ -1744,7 +1400,7 @@ int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable)
     return SV_OK;
 }
 
-int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[4], int64_t *calls)
+int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls)
 {
     if (!ctx || !ms || !calls) return SV_EINVAL;
     DeviceGuard g(ctx->device);
@@ -1759,13 +1415,11 @@ int spec_verify_get_profile(spec_verify_ctx *ctx, double ms[4], int64_t *calls)
     return SV_OK;
 }
 
-int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk, int race_chunk)
+int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk)
 {
-    if (!ctx || stats_chunk < -1 || race_chunk < -1) return SV_EINVAL;
+    if (!ctx || stats_chunk < -1) return SV_EINVAL;
     if (stats_chunk == -1) ctx->stats_chunk = 0;
-    else if (stats_chunk) ctx->stats_chunk = round_up8(std::max(stats_chunk, kMinChunk));
-    if (race_chunk == -1) ctx->race_chunk = 0;
-    else if (race_chunk) ctx->race_chunk = (std::max(race_chunk, kMinChunk) + 15) / 16 * 16;
+    else if (stats_chunk) ctx->stats_chunk = (std::max(stats_chunk, kMinChunk) + kGroup - 1) / kGroup * kGroup;
     return SV_OK;
 }
 
@@ -1805,20 +1459,13 @@ namespace {
 constexpr int kNoAllocMaxReqs = SV_NOALLOC_MAX_REQS;
 constexpr int kNoAllocMaxRows = SV_NOALLOC_MAX_ROWS;
 constexpr int kNoAllocMaxVocab = SV_NOALLOC_MAX_VOCAB;
-// with the fixed chunk a row spans at most this many CTAs of either kernel
+// with the fixed chunk a row spans at most this many statistics CTAs
 constexpr int kNoAllocMaxSeg = (kNoAllocMaxVocab + kFixedChunk - 1) / kFixedChunk + 1;
 
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-constexpr size_t kOffRowInfo = 0;
-constexpr size_t kOffRowStat = kOffRowInfo + align256(sizeof(RowInfo) * kNoAllocMaxRows);
-constexpr size_t kOffStatPart = kOffRowStat + align256(sizeof(RowStat) * kNoAllocMaxRows);
-constexpr size_t kOffReqState =
-    kOffStatPart + align256(sizeof(StatPart) * size_t(kNoAllocMaxRows) * kNoAllocMaxSeg);
-constexpr size_t kOffRacePart = kOffReqState + align256(sizeof(ReqState) * kNoAllocMaxReqs);
-constexpr size_t kOffCounters =
-    kOffRacePart + align256(sizeof(RacePart) * size_t(kNoAllocMaxReqs) * kNoAllocMaxSeg);
+constexpr size_t kOffStatPart = 0;
 constexpr size_t kOffFlags =
-    kOffCounters + align256(sizeof(unsigned) * counter_words(kNoAllocMaxReqs));
+    kOffStatPart + align256(sizeof(StatPart) * size_t(kNoAllocMaxRows) * kNoAllocMaxSeg);
 constexpr size_t kNoAllocBytes = kOffFlags + align256(2 * sizeof(unsigned));
 
 // One copy per device that loads this library, kept until the process exits. Every call of
@@ -1830,7 +1477,8 @@ std::mutex g_noalloc_mutex;
 void *g_noalloc_base[kNoAllocMaxDevices] = {};
 
 // Device address of the static scratch on device `dev` (current), looked up once per device
-// (the host-side name of the array is not a device address).
+// (the host-side name of the array is not a device address); the kernels' shared-memory limits
+// are set at the same time.
 int noalloc_base(int dev, void **out)
 {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
@@ -1841,8 +1489,8 @@ int noalloc_base(int dev, void **out)
             cudaGetLastError();
             return SV_ECUDA;
         }
-        int a = 0, b = 0, c = 0;
-        if (occupancy<uint16_t>(&a, &b, &c) != cudaSuccess || occupancy<float>(&a, &b, &c) != cudaSuccess) {
+        int a = 0;
+        if (setup_kernels<uint16_t>(dev, &a) != cudaSuccess || setup_kernels<float>(dev, &a) != cudaSuccess) {
             cudaGetLastError();
             return SV_ECUDA;
         }
@@ -1869,6 +1517,7 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
         return SV_EINVAL;
     if (vocab_size > kNoAllocMaxVocab || num_reqs > kNoAllocMaxReqs ||
         static_cast<long long>(num_draft_tokens) + num_reqs > kNoAllocMaxRows ||
+        max_spec_len_this_batch >= kNoAllocMaxRows ||
         static_cast<long long>(num_draft_tokens) >
             static_cast<long long>(num_reqs) * max_spec_len_this_batch)
         return SV_ECAPACITY;
@@ -1887,13 +1536,16 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
     cudaDeviceProp prop;
     if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3)
         return SV_EDEVICE;
+    if (verify_smem_bytes(vocab_size, max_spec_len_this_batch) > verify_smem_limit(dev))
+        return SV_ECAPACITY;
     void *base = nullptr;
     const int rc = noalloc_base(dev, &base);
     if (rc != SV_OK) return rc;
     auto *bytes = static_cast<unsigned char *>(base);
 
-    // A context on the host stack whose scratch pointers are carved from the static array;
-    // both kernels use the fixed chunk, so a row never spans more than kNoAllocMaxSeg CTAs.
+    // A context on the host stack whose scratch pointers are carved from the static array; the
+    // fixed statistics chunk keeps every row within kNoAllocMaxSeg partials. There is no room for
+    // line maxima: the verify kernel takes them from the raced rows themselves.
     spec_verify_ctx view;
     view.device = dev;
     view.max_num_reqs = kNoAllocMaxReqs;
@@ -1904,13 +1556,7 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
     view.max_rows = kNoAllocMaxRows;
     view.maxseg = kNoAllocMaxSeg;
     view.stats_chunk = kFixedChunk;
-    view.race_chunk = kFixedChunk;
-    view.rowinfo = reinterpret_cast<RowInfo *>(bytes + kOffRowInfo);
-    view.rowstat = reinterpret_cast<RowStat *>(bytes + kOffRowStat);
     view.statpart = reinterpret_cast<StatPart *>(bytes + kOffStatPart);
-    view.reqstate = reinterpret_cast<ReqState *>(bytes + kOffReqState);
-    view.racepart = reinterpret_cast<RacePart *>(bytes + kOffRacePart);
-    view.counters = reinterpret_cast<unsigned *>(bytes + kOffCounters);
     view.flags = reinterpret_cast<unsigned *>(bytes + kOffFlags);
     auto stream = static_cast<cudaStream_t>(cuda_stream);
     if (logits_dtype == SV_BF16)

@@ -48,7 +48,7 @@ def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, 
                             batch.logits_dtype, batch.draft_probs is not None,
                             device=torch.device(device).index or 0)
     if chunks:
-        ctx.set_chunks(*chunks)
+        ctx.set_chunks(chunks)
     d = to_device(batch, device)
     outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
                    d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,

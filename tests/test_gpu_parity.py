@@ -68,7 +68,7 @@ def test_custom_parity(seed, V, Ks, dtype, q_mode):
     assert_parity(b, got, ref)
 
 
-@pytest.mark.parametrize("chunks", [(2048, 2048), (4096, 16384), (65536, 2048)])
+@pytest.mark.parametrize("chunks", [2048, 4096, 65536])
 def test_launch_shape_does_not_change_results(chunks):
     b = _custom(11, 30011, [3, 5, 0, 2, 4, 1, 3, 3], "bf16", "noisy", greedy_frac=0.2)
     base = gpu_run(b)

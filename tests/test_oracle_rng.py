@@ -90,22 +90,27 @@ def _u(w):
 
 
 def test_race_clock_layout_matches_triton(tmp_path):
-    """The race clock of token v (block g = v >> 4, slot s = v & 15) at (request i, position j):
-    counter (g, j, i, 8) gives W (word 0) and the argmin slot a (word 1 & 15); E_min = -ln(W)/16;
+    """The race clock of token v (group g = v >> 6, slot s = v & 63) at (request i, position j):
+    counter (g, j, i, 8) gives W (word 0) and the argmin slot a (word 1 & 63); E_min = -ln(W)/64;
     slot s != a adds -ln U_s, U_s word s & 3 of counter (g, j, i, 9 + s // 4)."""
-    seed, j, i, nblk = 0xDEADBEEF12345, 3, 17, 12
-    ctr = np.array([[g, j, i, 8 + k] for g in range(nblk) for k in range(5)], dtype=np.uint32)
-    pad = np.zeros((64 - ctr.shape[0], 4), dtype=np.uint32)
-    words = _triton_philox([(seed, np.vstack([ctr, pad]))], tmp_path)[0][: ctr.shape[0]]
-    want = np.empty(16 * nblk)
-    for g in range(nblk):
-        head = words[5 * g]
-        emin = -np.log(_u(head[0])) / 16.0
-        a = int(head[1]) & 15
-        for s_ in range(16):
-            v = 16 * g + s_
-            want[v] = emin if s_ == a else emin - np.log(_u(words[5 * g + 1 + s_ // 4][s_ % 4]))
-    got = oracle.race_clocks(seed, j, i, 16 * nblk).astype(np.float64)
+    seed, j, i = 0xDEADBEEF12345, 3, 17
+    groups = [(0, 1, 2), (3, 4, 5)]                # 17 calls per group; 64 counters per request
+    reqs = []
+    for gs in groups:
+        ctr = np.array([[g, j, i, 8 + k] for g in gs for k in range(17)], dtype=np.uint32)
+        reqs.append((seed, np.vstack([ctr, np.zeros((64 - ctr.shape[0], 4), np.uint32)])))
+    words = _triton_philox(reqs, tmp_path)
+    nblk = sum(len(gs) for gs in groups)
+    want = np.empty(64 * nblk)
+    for gs, w in zip(groups, words):
+        for k, g in enumerate(gs):
+            head = w[17 * k]
+            emin = -np.log(_u(head[0])) / 64.0
+            a = int(head[1]) & 63
+            for s_ in range(64):
+                v = 64 * g + s_
+                want[v] = emin if s_ == a else emin - np.log(_u(w[17 * k + 1 + s_ // 4][s_ % 4]))
+    got = oracle.race_clocks(seed, j, i, 64 * nblk).astype(np.float64)
     np.testing.assert_allclose(got, want, rtol=2e-6)
 
 
@@ -132,18 +137,18 @@ def test_uniforms_are_uniform_and_uncorrelated():
 
 
 def test_race_clocks_are_iid_exponential():
-    """The block construction (minimum of 16 and memoryless excesses) must give i.i.d. Exp(1)
-    clocks: the marginal of every slot, the argmin slot uniform, no correlation in a block."""
-    n = 16 * 40_000
+    """The group construction (minimum of 64 and memoryless excesses) must give i.i.d. Exp(1)
+    clocks: the marginal of every slot, the argmin slot uniform, no correlation in a group."""
+    n = 64 * 10_000
     e = oracle.race_clocks(2024, 1, 5, n).astype(np.float64)
     assert stats.kstest(e, "expon").pvalue > 1e-3
-    blocks = e.reshape(-1, 16)
-    for s_ in (0, 5, 15):
+    blocks = e.reshape(-1, 64)
+    for s_ in (0, 5, 63):
         assert stats.kstest(blocks[:, s_], "expon").pvalue > 1e-3
-    argmin = np.bincount(blocks.argmin(axis=1), minlength=16)
+    argmin = np.bincount(blocks.argmin(axis=1), minlength=64)
     assert stats.chisquare(argmin).pvalue > 1e-3
-    assert stats.kstest(blocks.min(axis=1) * 16, "expon").pvalue > 1e-3   # min of 16 ~ Exp(16)
-    c = np.corrcoef(blocks[:, 2], blocks[:, 9])[0, 1]
+    assert stats.kstest(blocks.min(axis=1) * 64, "expon").pvalue > 1e-3   # min of 64 ~ Exp(64)
+    c = np.corrcoef(blocks[:, 2], blocks[:, 41])[0, 1]
     assert abs(c) < 0.02
-    other = oracle.race_clocks(2024, 2, 5, 16 * 5000).astype(np.float64)  # another position
+    other = oracle.race_clocks(2024, 2, 5, 64 * 1250).astype(np.float64)  # another position
     assert abs(np.corrcoef(e[: other.size], other)[0, 1]) < 0.03
