@@ -35,16 +35,16 @@
  *     Philox4x32-10 (Salmon et al., SC'11), key = (lo32(seed), hi32(seed)), counter =
  *     (c0, j, req_index_base + i, tag), uniform U = ((w >> 9) + 1/2) / 2^23 of a 32-bit word w.
  *     The acceptance uniform u of position j is word 0 of counter (0, j, i', 0).
- *   - A draw from weights w_v is the exponential race argmax_v (log w_v - log E_v) over i.i.d.
- *     Exp(1) clocks E_v, lowest index on equal keys. The clocks come in groups of 64 tokens
+ *   - A draw from weights w_v is the exponential race argmax_v w_v / E_v over i.i.d. Exp(1)
+ *     clocks E_v (the key is the binary32 quotient), lowest index on equal keys. The clocks come in groups of 64 tokens
  *     (g = v >> 6, slot s = v & 63): counter (g, j, i', 8) gives W (word 0) and the slot
  *     a = word 1 & 63 that holds the group's smallest clock E_g = -log(W) / 64; slot s != a has
  *     clock E_g + (-log U_s), U_s word s & 3 of counter (g, j, i', 9 + s / 4). (By the
  *     memoryless property these are i.i.d. Exp(1); E_g bounds every key of the group, which
- *     lets the race skip whole groups.) Keys over p are x_v - log E_v. Residual weights are
- *     rr_v = fma(-S, q_v, exp(x_v - m)) (S times p_v - q_v, rounded once), candidates rr_v > 0,
- *     keys log rr_v - log E_v; if no candidate is left after rounding, the token is drawn from
- *     p. Without draft probabilities the rejected draft token is removed.
+ *     lets the race skip whole groups.) Over p the weights are t_v = exp(x_v - m); residual
+ *     weights are rr_v = fma(-S, q_v, t_v) (S times p_v - q_v, rounded once), candidates
+ *     rr_v > 0; if no candidate is left after rounding, the token is drawn from p. Without draft
+ *     probabilities the rejected draft token is removed.
  *   - Acceptance: 0 <= d < V and q(d) > 0 and p(d) / q(d) >= u (binary32), q(d) = 1 without
  *     draft probabilities. An out-of-range draft id is rejected, not an error.
  *   - exp / log inside these decisions are fixed binary32 functions (Cody-Waite reduction

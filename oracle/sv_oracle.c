@@ -23,14 +23,15 @@
  *   - Every random draw is keyed: Philox4x32-10, key = seed, counter words (c0, j, request,
  *     c3). The acceptance uniform of position j is word 0 of counter (0, j, request, 0).
  *   - Sampling from a distribution proportional to w_v is the exponential race
- *     argmax_v (log w_v - log E_v) over i.i.d. Exp(1) clocks E_v, lowest index on equal keys.
+ *     argmax_v w_v / E_v over i.i.d. Exp(1) clocks E_v (the key is the binary32 quotient),
+ *     lowest index on equal keys; over p the weight is t_v = exp(x_v - m).
  *     The clocks come in groups of 64 tokens (group g = v >> 6, slot s = v & 63): counter
  *     (g, j, request, 8) gives W (word 0) and the slot a = word 1 & 63 holding the group's
  *     smallest clock E_min = -log(W) / 64; the other slots' clocks are E_min + (-log U_s), U_s
  *     word s & 3 of counter (g, j, request, 9 + s / 4). By the memoryless property of the
  *     exponential these 64 clocks are i.i.d. Exp(1).
  *   - The residual weight is rr_v = fma(-S, q_v, t_v) with t_v = exp(x_v - m), i.e.
- *     S * (p_v - q_v) rounded once; the constant log S is left out of the keys.
+ *     S * (p_v - q_v) rounded once; the constant factor 1 / S is left out of the keys.
  *   - exp and log inside every decision are the binary32 functions below (Cody-Waite
  *     reduction + Taylor polynomial; reduction to [sqrt(1/2), sqrt(2)) + atanh series), so
  *     that any implementation that follows the same steps gets the same bits.
@@ -250,12 +251,13 @@ static inline void race_offer(race_t *r, float key, int32_t v, float *second)
 
 /* Exponential race over one row at position j of request ireq, [spec-notes] NO_DRAFT_PROBS
  * answer (argmax(prob / q) with q ~ Exp(1) needs no normalisation) and [spec-in-vllm] 7.3
- * (Gumbel argmax). Keys are taken in log form: key_v = log w_v - log E_v, E_v the token's race
- * clock.
- *   q == NULL : w_v proportional to p_v; key_v = x_v - log E_v; token `exclude` is left out
+ * (Gumbel argmax, the same race in log form). Keys: key_v = w_v / E_v, E_v the token's race
+ * clock, one binary32 division.
+ *   q == NULL : w_v = t_v = exp(x_v - m), proportional to p_v; token `exclude` is left out
  *               (the rejected draft token when there are no draft probabilities).
  *   q != NULL : residual weights rr_v = fma(-S, q_v, t_v) = S (p_v - q_v) rounded once,
- *               candidates rr_v > 0 ([spec-notes] residual distribution max(0, p - q)).  */
+ *               candidates rr_v > 0 ([spec-notes] residual distribution max(0, p - q)).
+ * The decision margin is the winner's key over the runner-up's, as log(key1) - log(key2).   */
 static race_t race_row(const void *logits, int bf16, size_t row, int V, float invT, float m,
                        float S_f, const float *q, int32_t exclude, uint64_t seed, uint32_t j,
                        uint32_t ireq)
@@ -266,20 +268,21 @@ static race_t race_row(const void *logits, int bf16, size_t row, int V, float in
     for (int v = 0; v < V; ++v) {
         if (v == exclude) continue;
         float x = logit_at(logits, bf16, base + (size_t)v) * invT;
-        float logw;
+        float t = spec_verify_ref_exp(x - m);
+        float w;
         if (q) {
-            float t = spec_verify_ref_exp(x - m);
             float rr = fmaf(-S_f, q[v], t);
             if (!(rr > 0.0f)) continue;
-            logw = spec_verify_ref_log(rr);
+            w = rr;
         } else {
-            logw = x;
+            w = t;
         }
         float E = spec_verify_ref_race_clock(seed, j, ireq, v);
-        float key = logw - spec_verify_ref_log(E);
+        float key = w / E;
         race_offer(&r, key, v, &second);
     }
-    if (r.idx >= 0 && r.ncand >= 2) r.gap = (double)r.key - (double)second;
+    if (r.idx >= 0 && r.ncand >= 2)
+        r.gap = second > 0.0f ? log((double)r.key) - log((double)second) : INFINITY;
     return r;
 }
 

@@ -17,15 +17,15 @@
 //                                the rejected draft, or over p for the bonus draw ([spec-notes]
 //                                residual and NO_DRAFT_PROBS answers, [spec-in-vllm] 7.3).
 //
-// The race is a best-first search, not a scan. A row's race clocks come in groups of 64 tokens
-// whose head Philox call gives the group's smallest clock E_g, so no key in group g exceeds
-// max_{v in g} x_v - log E_g (a race over p; the residual weight is at most exp(x - m), so its
-// keys are at most that minus m). The verify CTA takes the largest logit of every 64-element
-// line of the raced row, bounds every group with one Philox call, evaluates first the groups
-// with the best bounds and then only the groups whose bound still reaches the best key found --
-// a few dozen of the V / 64 groups on typical rows. Only exact keys decide, so the winner is the
-// argmax over all tokens, as a full scan would find it; only the raced row's logits and the q
-// entries of evaluated groups are read.
+// The race is a best-first search, not a scan. Keys are w_v / E_v with w_v = exp(x_v - m) (a
+// race over p) or the residual weight (at most exp(x_v - m)). A row's race clocks come in groups
+// of 64 tokens whose head Philox call gives the group's smallest clock E_g, so no key in group g
+// exceeds exp(max_{v in g} x_v - m) / E_g. The verify CTA takes the largest logit of every
+// 64-element line of the raced row (written by the statistics kernel), bounds every group with
+// one Philox call, evaluates first the groups with the best bounds and then only the groups whose
+// bound still reaches the best key found -- a few dozen of the V / 64 groups on typical rows. Only
+// exact keys decide, so the winner is the argmax over all tokens, as a full scan would find it;
+// only the line maxima of the raced row and the logits and q entries of evaluated groups are read.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -104,9 +104,10 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long p)
     return (static_cast<unsigned long long>(mh) << 32) | ml;
 }
 
-// Upper bound of a key computed as b with binary32 exp / log: covers the functions' few-ulp
-// errors and their possible non-monotonicity at that level, with a wide margin.
-__device__ __forceinline__ float key_bound(float b) { return b + (1e-3f + 1e-5f * fabsf(b)); }
+// Upper bound of every key whose weight is at most exp(y) for the y that gave b = exp(y) / E:
+// covers a possible few-ulp non-monotonicity of the binary32 exp, with a wide margin (keys are
+// >= 0; divisions round monotonically).
+__device__ __forceinline__ float key_bound(float b) { return b * 1.00002f; }
 
 // Group g's smallest clock: E_g = -log(W) / 64 from word 0 of its head call (exact scaling).
 __device__ __forceinline__ float group_emin(const sv::Philox4 &h)
@@ -167,10 +168,10 @@ struct OnlineMax {
     float s = 0.0f;    // running sum of 2^((l - L) c)
     float Lc = 0.0f;   // L * c once L is finite (0 before, so that -inf logits add 2^-inf = 0)
     int best_e = -1;   // element where L was first reached (scalar path), or -1
-    int best_u = -1;   // first vector of the batch where L was first reached, or -1
+    int best_p = -1;   // pair where L was first reached (vector path), or -1
 };
 
-// Fold one logit at index e (head / tail of a misaligned segment; indices increase).
+// Fold one logit at index e (head / tail of a segment; indices increase).
 __device__ __forceinline__ void fold1(OnlineMax &st, float l, int e, float c)
 {
     if (l > st.L) {
@@ -178,56 +179,134 @@ __device__ __forceinline__ void fold1(OnlineMax &st, float l, int e, float c)
         st.L = l;
         st.Lc = l * c;
         st.best_e = e;
-        st.best_u = -1;
+        st.best_p = -1;
     }
     st.s += sv::ex2_approx(fmaf(l, c, -st.Lc));
 }
 
-template <typename T>
-__device__ __forceinline__ void unpack(const uint4 &w, float (&l)[16 / sizeof(T)])
+// The statistics kernel streams 64-byte pairs: two 32-byte loads per lane and round, the lanes of
+// a warp on consecutive pairs (a 2 KB stretch per warp).
+constexpr int kPairBytes = 64;
+
+__device__ __forceinline__ void ldg_pair(const char *p, uint32_t (&w)[16])
 {
-    if constexpr (sizeof(T) == 2) {
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            l[2 * h] = __uint_as_float(ws[h] << 16);
-            l[2 * h + 1] = __uint_as_float(ws[h] & 0xFFFF0000u);
-        }
-    } else {
-        l[0] = __uint_as_float(w.x);
-        l[1] = __uint_as_float(w.y);
-        l[2] = __uint_as_float(w.z);
-        l[3] = __uint_as_float(w.w);
-    }
+    asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
+          "=r"(w[7])
+        : "l"(p));
+    asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]),
+          "=r"(w[15])
+        : "l"(p + 32));
 }
 
-// Fold a batch of NV 16-byte vectors (vectors u0, u0 + kThreads, ...; element indices increase
-// with the vector; nv of them valid) whose largest element is mx, without branches: one rescale
-// of the running sum, then the sum of 2^((l - L) c). Only the batch that first reached the max is
-// recorded; its lowest index is recovered at the end of the segment.
-template <typename T, int NV>
-__device__ __forceinline__ void fold_sum(OnlineMax &st, const uint4 (&w)[NV], int nv, int u0,
-                                         float c, float mx)
+// Element h of a pair (bf16: the low half of word h / 2 first).
+template <typename T>
+__device__ __forceinline__ float pair_elem(const uint32_t (&w)[16], int h)
 {
-    constexpr int kVec = 16 / sizeof(T);
+    if constexpr (sizeof(T) == 2)
+        return __uint_as_float((h & 1) ? (w[h >> 1] & 0xFFFF0000u) : (w[h >> 1] << 16));
+    else
+        return __uint_as_float(w[h]);
+}
+
+// Largest element of a pair in a form that combines cheaply (bf16: max.bf16x2 over the words,
+// two candidates per word; fp32: a float), and the largest over the lanes that share a
+// 64-element line (2 consecutive lanes for bf16, 4 for fp32; every lane must take part).
+template <typename T> struct PairMax;
+template <> struct PairMax<uint16_t> {
+    using P = uint32_t;
+    static constexpr int kLanes = 2;
+    static __device__ __forceinline__ P max2(P a, P b)
+    {
+        P d;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+        return d;
+    }
+    static __device__ __forceinline__ P of(const uint32_t (&w)[16])
+    {
+        P m[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] = max2(w[2 * k], w[2 * k + 1]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = max2(m[2 * k], m[2 * k + 1]);
+        return max2(max2(m[0], m[1]), max2(m[2], m[3]));
+    }
+    static __device__ __forceinline__ P none() { return 0xFF80FF80u; }
+    static __device__ __forceinline__ float value(P m)
+    {
+        return fmaxf(__uint_as_float(m << 16), __uint_as_float(m & 0xFFFF0000u));
+    }
+    static __device__ __forceinline__ P line(P m)
+    {
+        return max2(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+    }
+    static __device__ __forceinline__ uint16_t store(P m)  // a bf16 value: exact
+    {
+        return static_cast<uint16_t>(__float_as_uint(value(m)) >> 16);
+    }
+};
+template <> struct PairMax<float> {
+    using P = float;
+    static constexpr int kLanes = 4;
+    static __device__ __forceinline__ P max2(P a, P b) { return fmaxf(a, b); }
+    static __device__ __forceinline__ P of(const uint32_t (&w)[16])
+    {
+        float m[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m[k] = fmaxf(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[k] = fmaxf(m[2 * k], m[2 * k + 1]);
+        return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+    }
+    static __device__ __forceinline__ P none() { return -kInf; }
+    static __device__ __forceinline__ float value(P m) { return m; }
+    static __device__ __forceinline__ P line(P m)
+    {
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+        return fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+    }
+    static __device__ __forceinline__ float store(P m) { return m; }
+};
+
+// Fold pair p, whose largest element is mx, without branches: one rescale of the running sum,
+// then the sum of 2^((l - L) c). Only the pair that first reached the max is recorded; its lowest
+// index is recovered at the end of the segment.
+template <typename T>
+__device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16], int p, float c,
+                                          float mx)
+{
+    constexpr int kPE = kPairBytes / sizeof(T);
     const bool up = mx > st.L;
     st.s *= sv::ex2_approx(up ? (st.L - mx) * c : 0.0f);  // L = -inf: 2^-inf = 0 (s was 0)
-    st.best_u = up ? u0 : st.best_u;
+    st.best_p = up ? p : st.best_p;
     st.best_e = up ? -1 : st.best_e;
     st.L = up ? mx : st.L;
     st.Lc = st.L > -kInf ? st.L * c : 0.0f;
     float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-    for (int k = 0; k < NV; ++k) {
-        if (k < nv) {
-            float l[kVec];
-            unpack<T>(w[k], l);
-#pragma unroll
-            for (int h = 0; h < kVec; ++h)
-                ((h & 1) ? s1 : s0) += sv::ex2_approx(fmaf(l[h], c, -st.Lc));
-        }
-    }
+    for (int h = 0; h < kPE; ++h)
+        ((h & 1) ? s1 : s0) += sv::ex2_approx(fmaf(pair_elem<T>(w, h), c, -st.Lc));
     st.s += s0 + s1;
+}
+
+// Division by a launch constant d > 0 without a division instruction: with M = ceil(2^64 / d)
+// (0 stands for d = 1), floor(a * M / 2^64) is floor(a / d) or one more for 0 <= a < 2^63, and
+// one multiply decides which.
+struct Divisor {
+    long long d;
+    unsigned long long magic;
+};
+__host__ inline Divisor make_divisor(long long d)
+{
+    return Divisor{d, d == 1 ? 0ull : ~0ull / static_cast<unsigned long long>(d) + 1ull};
+}
+__device__ __forceinline__ long long div_floor(long long a, const Divisor &q)
+{
+    if (q.magic == 0ull) return a;
+    long long r = static_cast<long long>(__umul64hi(static_cast<unsigned long long>(a), q.magic));
+    if (r * q.d > a) --r;
+    return r;
 }
 
 // Largest element of a 16-byte vector in a form that combines cheaply (bf16: two halves packed
@@ -335,11 +414,10 @@ struct RequestTable {
 };
 
 // Segment [b, e) of row `row`, by the whole CTA: the elements before the first 64-element line
-// boundary one by one, then whole 16-byte vectors in batches of four loads per thread (the row's
-// request is looked up while the first batch is in flight), then the last few elements one by
-// one; reduce and publish the segment's partial statistics. With `lines`, the largest logit of
-// every line that the vectors cover completely is stored at lines[line] (line = (base_off +
-// flattened element) / 64).
+// boundary one by one, then 64-byte pairs, one per lane and round (the row's request is looked up
+// while the first round is in flight), then the last few elements one by one; reduce and publish
+// the segment's partial statistics. With `lines`, the largest logit of every line that the pairs
+// cover completely is stored at lines[line] (line = (base_off + flattened element) / 64).
 template <typename T>
 __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int V, int row, int b,
                                               int e, int seg, int maxseg, int base_off,
@@ -349,26 +427,21 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     __shared__ float s_c;
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
-    constexpr int kVec = 16 / sizeof(T);
-    constexpr int kVPL = VecMax<T>::kLanes;  // vectors per line
-    constexpr int kU = 4;
+    constexpr int kPE = kPairBytes / sizeof(T);  // elements per pair
+    constexpr int kPPL = PairMax<T>::kLanes;     // pairs per line
     const long long pos_b = base_off + rbase + b;  // line coordinate of element b
     const int head = static_cast<int>((kGroup - (pos_b & (kGroup - 1))) & (kGroup - 1));
-    const int a0 = min(e, b + head);  // on a line boundary (hence on a 16-byte boundary)
-    const int nvec = (e - a0) / kVec;
-    const int a1 = a0 + nvec * kVec;
-    const char *vbase = reinterpret_cast<const char *>(rp + a0);
-    const long long line0 = (pos_b + (a0 - b)) >> 6;  // line of vector 0 when a0 < e
+    const int a0 = min(e, b + head);  // on a line boundary: 64-element aligned in memory
+    const int npair = (e - a0) / kPE;
+    const int a1 = a0 + npair * kPE;
+    const char *pbase = reinterpret_cast<const char *>(rp + a0);
+    const long long line0 = (pos_b + (a0 - b)) >> 6;  // line of pair 0 when a0 < e
     const int lane = threadIdx.x & 31;
 
-    // the warp's vectors of a batch start at ub: the loop runs the same iterations in every lane
+    // the warp's pairs of a round start at ub: every lane runs the same rounds
     int ub = static_cast<int>(threadIdx.x) & ~31;
-    uint4 w[kU];
-#pragma unroll
-    for (int k = 0; k < kU; ++k) {
-        const int u = ub + lane + k * kThreads;
-        w[k] = u < nvec ? ldg_v4(vbase + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
-    }
+    uint32_t w[16];
+    if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w);
     if (threadIdx.x < 32) {
         const int i = row_request(rq.cu, rq.n, row, lane);
         if (threadIdx.x == 0) {
@@ -381,43 +454,28 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
-    while (ub < nvec) {
-        const int u0 = ub + lane;
-        const int nv = min(kU, (nvec - u0 + kThreads - 1) / kThreads);  // <= 0: nothing to fold
-        typename VecMax<T>::P bm = VecMax<T>::none();
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-            const typename VecMax<T>::P pm = VecMax<T>::of(w[k]);
-            if (k < nv) bm = VecMax<T>::max2(bm, pm);
-            if (lines) {
-                const int u = u0 + k * kThreads;
-                const typename VecMax<T>::P lm = VecMax<T>::line(pm);
-                if ((lane & (kVPL - 1)) == 0 && u + kVPL - 1 < nvec)
-                    lines[line0 + u / kVPL] = VecMax<T>::store(lm);
-            }
+    while (ub < npair) {
+        const int p = ub + lane;
+        const bool valid = p < npair;
+        const typename PairMax<T>::P pm = valid ? PairMax<T>::of(w) : PairMax<T>::none();
+        if (lines) {
+            const typename PairMax<T>::P lm = PairMax<T>::line(pm);
+            if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair)
+                lines[line0 + p / kPPL] = PairMax<T>::store(lm);
         }
-        fold_sum<T, kU>(st, w, nv, u0, c, VecMax<T>::value(bm));
-        ub += kThreads * kU;
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-            const int u = ub + lane + k * kThreads;
-            w[k] = u < nvec ? ldg_v4(vbase + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
-        }
+        if (valid) fold_pair<T>(st, w, p, c, PairMax<T>::value(pm));
+        ub += kThreads;
+        if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w);
     }
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
 
     // lowest index where this thread's max occurs
     int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
-    if (st.best_u >= 0) {
-        for (int k = 0; k < kU && idx == INT_MAX; ++k) {
-            const int u = st.best_u + k * kThreads;
-            if (u >= nvec) break;
-            float l[kVec];
-            unpack<T>(ldg_v4(vbase + static_cast<size_t>(u) * 16), l);
+    if (st.best_p >= 0) {
+        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w);
 #pragma unroll
-            for (int h = kVec - 1; h >= 0; --h)
-                if (l[h] == st.L) idx = a0 + u * kVec + h;
-        }
+        for (int h = kPE - 1; h >= 0; --h)
+            if (pair_elem<T>(w, h) == st.L) idx = a0 + st.best_p * kPE + h;
     }
     float L = st.L, s = st.s;
     block_reduce_stat(L, s, idx, c);
@@ -430,19 +488,20 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
 // segment. Pure streaming: no atomics, nothing waits on another CTA.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 5)
-sv_stats_kernel(const T *__restrict__ logits, int V, long long total, long long chunk, int maxseg,
-                int base_off, RequestTable rq, StatPart *__restrict__ part, T *__restrict__ lines)
+sv_stats_kernel(const T *__restrict__ logits, int V, long long total, Divisor chunk, Divisor dv,
+                int maxseg, int base_off, RequestTable rq, StatPart *__restrict__ part,
+                T *__restrict__ lines)
 {
-    const long long start = max(0LL, static_cast<long long>(blockIdx.x) * chunk - base_off);
-    const long long stop = min(total, static_cast<long long>(blockIdx.x + 1) * chunk - base_off);
+    const long long start = max(0LL, static_cast<long long>(blockIdx.x) * chunk.d - base_off);
+    const long long stop = min(total, static_cast<long long>(blockIdx.x + 1) * chunk.d - base_off);
     if (start >= stop) return;
-    const int r_first = static_cast<int>(start / V);
-    const int r_last = static_cast<int>((stop - 1) / V);
+    const int r_first = static_cast<int>(div_floor(start, dv));
+    const int r_last = static_cast<int>(div_floor(stop - 1, dv));
     for (int row = r_first; row <= r_last; ++row) {
         const long long rbase = static_cast<long long>(row) * V;
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
-        const int fk = static_cast<int>((base_off + rbase) / chunk);
+        const int fk = static_cast<int>(div_floor(base_off + rbase, chunk));
         stats_segment<T>(logits, V, row, b, e, static_cast<int>(blockIdx.x) - fk, maxseg, base_off,
                          rq, part, lines);
     }
@@ -459,7 +518,7 @@ struct VerifyParams {
     uint64_t seed;
     uint32_t req_base;
     int nd, kmax, V, maxseg, base_off;
-    long long chunk;
+    Divisor chunk;
     int32_t *sampled, *num_sampled, *num_rejected;
     float *opt_max, *opt_sum;
     int32_t *opt_amax;
@@ -617,9 +676,9 @@ __host__ __device__ inline VerifyLayout verify_layout(int V, int kmax)
     return l;
 }
 
-// pb[g] = bound of group g in a race over p, fl(x_max - log E_g) with x_max = fl(line max * invT);
-// eg[g] = E_g, ag[g] = a from the group's head call. Returns the thread's best (pb, g) packed, 0 if
-// it has no group.
+// pb[g] = bound of group g, fl(exp(fl(x_max - m)) / E_g) with x_max = fl(line max * invT) (before
+// key_bound); eg[g] = E_g, ag[g] = a from the group's head call. Returns the thread's best
+// (pb, g) packed, 0 if it has no group.
 template <typename T>
 __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &rl,
                                            const SearchSmem &sm)
@@ -641,7 +700,8 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
             const int g = g0 + k * kThreads;
             if (g < r.G) {
                 const float E = group_emin(h[k]);
-                const float b = __fsub_rn(__fmul_rn(lmax[k], r.invT), sv::log_f32(E));
+                const float t = sv::exp_f32(__fsub_rn(__fmul_rn(lmax[k], r.invT), r.m));
+                const float b = __fdiv_rn(t, E);
                 sm.pb[g] = b;
                 sm.eg[g] = E;
                 sm.ag[g] = static_cast<uint8_t>(h[k].y & 63u);
@@ -687,12 +747,13 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
         const int a = sm.ag[g];
         const int v0 = g * kGroup + 2 * lane, v1 = v0 + 1;
         const bool in0 = v0 < r.V, in1 = v1 < r.V;
-        const float x0 = __fmul_rn(l[k][0], r.invT), x1 = __fmul_rn(l[k][1], r.invT);
-        float w0 = 0.0f, w1 = 0.0f;
+        const float t0 = sv::exp_f32(__fsub_rn(__fmul_rn(l[k][0], r.invT), r.m));
+        const float t1 = sv::exp_f32(__fsub_rn(__fmul_rn(l[k][1], r.invT), r.m));
+        float w0, w1;
         bool c0, c1;
         if constexpr (kRes) {
-            w0 = __fmaf_rn(-r.S, qv[k][0], sv::exp_f32(__fsub_rn(x0, r.m)));
-            w1 = __fmaf_rn(-r.S, qv[k][1], sv::exp_f32(__fsub_rn(x1, r.m)));
+            w0 = __fmaf_rn(-r.S, qv[k][0], t0);
+            w1 = __fmaf_rn(-r.S, qv[k][1], t1);
             c0 = in0 && w0 > 0.0f;
             c1 = in1 && w1 > 0.0f;
             // the group's largest residual weight bounds its keys more tightly than its line max
@@ -700,10 +761,10 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
                 0xFFFFFFFFu, __float_as_uint(fmaxf(c0 ? w0 : 0.0f, c1 ? w1 : 0.0f))));
             if (!(wm > 0.0f)) continue;
             const unsigned long long cur = ld_best(sm.best);
-            if (cur != 0 && key_enc(key_bound(__fsub_rn(sv::log_f32(wm), sv::log_f32(E)))) <
-                                static_cast<unsigned>(cur >> 32))
-                continue;
+            if (cur != 0 && key_enc(__fdiv_rn(wm, E)) < static_cast<unsigned>(cur >> 32)) continue;
         } else {
+            w0 = t0;
+            w1 = t1;
             c0 = in0 && v0 != r.excl;
             c1 = in1 && v1 != r.excl;
         }
@@ -715,14 +776,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
         const uint32_t ws1 = (lane & 1) ? sl.w : sl.y;
         const float E0 = s0 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws0)));
         const float E1 = s1 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws1)));
-        float k0, k1;
-        if constexpr (kRes) {
-            k0 = __fsub_rn(sv::log_f32(w0), sv::log_f32(E0));
-            k1 = __fsub_rn(sv::log_f32(w1), sv::log_f32(E1));
-        } else {
-            k0 = __fsub_rn(x0, sv::log_f32(E0));
-            k1 = __fsub_rn(x1, sv::log_f32(E1));
-        }
+        const float k0 = __fdiv_rn(w0, E0), k1 = __fdiv_rn(w1, E1);
         unsigned long long p = 0;
         if (c0) p = pack_key(k0, v0);
         if (c1) p = max(p, pack_key(k1, v1));
@@ -732,8 +786,8 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
 }
 
 // Order the entries buf[0, cnt) roughly best first into tmp, by the whole CTA: kBins bins of
-// equal width in key bound, from the largest bound down to 40 below it (lower bounds share the
-// last bin), bin 0 first, any order inside a bin. The bin of an entry goes to bits 24..31 of its
+// equal width in log2 of the key bound, from the largest bound down to 2^-48 of it (lower bounds
+// share the last bin), bin 0 first, any order inside a bin (the order only affects speed). The bin of an entry goes to bits 24..31 of its
 // low word (groups are < 2^24); bin_max[b] is the largest bound in bin b.
 __device__ void bin_order(const SearchSmem &sm, int cnt)
 {
@@ -760,12 +814,12 @@ __device__ void bin_order(const SearchSmem &sm, int cnt)
         atomicMin(&sm.range[1], lo);
     }
     __syncthreads();
-    const float top = key_dec(sm.range[0]);
-    const float bottom = fmaxf(key_dec(sm.range[1]), top - 40.0f);
+    const float top = __log2f(key_dec(sm.range[0]));
+    const float bottom = fmaxf(__log2f(key_dec(sm.range[1])), top - 48.0f);
     const float inv_w = (top - bottom) > 0.0f ? kBins / (top - bottom) : 0.0f;
     for (int e = tid; e < cnt; e += kThreads) {
         const unsigned kb = static_cast<unsigned>(sm.buf[e] >> 32);
-        const float t = (top - key_dec(kb)) * inv_w;  // NaN / inf go to the last bin
+        const float t = (top - __log2f(key_dec(kb))) * inv_w;  // NaN / inf go to the last bin
         const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
         atomicAdd(&sm.bin_n[b], 1);
         atomicMax(&sm.bin_max[b], kb);
@@ -784,7 +838,7 @@ __device__ void bin_order(const SearchSmem &sm, int cnt)
     __syncthreads();
     for (int e = tid; e < cnt; e += kThreads) {
         const unsigned long long ent = sm.buf[e];
-        const float t = (top - key_dec(static_cast<unsigned>(ent >> 32))) * inv_w;
+        const float t = (top - __log2f(key_dec(static_cast<unsigned>(ent >> 32)))) * inv_w;
         const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
         const int pos = atomicAdd(&sm.bin_n[b], 1);
         sm.tmp[pos] = (ent & 0xFFFFFFFF00000000ull) | (static_cast<unsigned long long>(b) << 24) |
@@ -825,7 +879,7 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
         if (g < r.G) {
             const float b = sm.pb[g];
             if (b == b) {
-                kb = key_enc(key_bound(kRes ? __fsub_rn(b, r.m) : b));
+                kb = key_enc(key_bound(b));
                 take = best1 == 0 || kb >= thr1;
             }
         }
@@ -915,8 +969,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     for (int j = warp; j <= K; j += kWarps) {
         const int row = row0 + j;
         const long long rbase = static_cast<long long>(row) * P.V;
-        const int nseg = static_cast<int>((P.base_off + rbase + P.V - 1) / P.chunk) -
-                         static_cast<int>((P.base_off + rbase) / P.chunk) + 1;
+        const int nseg = static_cast<int>(div_floor(P.base_off + rbase + P.V - 1, P.chunk) -
+                                          div_floor(P.base_off + rbase, P.chunk)) + 1;
         float L = -kInf, s = 0.0f;
         int idx = INT_MAX;
         for (int k = lane; k < nseg; k += 32) {
@@ -1145,7 +1199,7 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
     P.V = V;
     P.maxseg = ctx->maxseg;
     P.base_off = base_off;
-    P.chunk = chunk1;
+    P.chunk = make_divisor(chunk1);
     P.sampled = sampled;
     P.num_sampled = num_sampled;
     P.num_rejected = num_rejected;
@@ -1161,8 +1215,9 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
         prof_collect(ctx, *slot);
         cudaEventRecord(slot->ev[0], stream);
     }
-    sv_stats_kernel<T><<<grid1, kThreads, 0, stream>>>(logits, V, total, chunk1, ctx->maxseg,
-                                                       base_off, rq, ctx->statpart, lines);
+    sv_stats_kernel<T><<<grid1, kThreads, 0, stream>>>(logits, V, total, make_divisor(chunk1),
+                                                       make_divisor(V), ctx->maxseg, base_off, rq,
+                                                       ctx->statpart, lines);
     if (slot) cudaEventRecord(slot->ev[1], stream);
     sv_verify_kernel<T><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
     if (slot) {
