@@ -1,8 +1,8 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 speculative-decoding verification sampler.
 
-One step = one call of the verification step (all three kernels) on one batch of the
-bandwidth workload: 256 requests x (K=5 draft positions + 1 bonus) = 1536 logit rows of a
+One step = one call of the verification step (both kernels: row statistics, then verify =
+acceptance + race + emit) on one batch of the bandwidth workload: 256 requests x (K=5 draft positions + 1 bonus) = 1536 logit rows of a
 151936-token vocabulary in bf16, fp32 draft distributions for the 1280 draft positions
 (1245 MB of inputs, larger than the 129 MB L2, so no flush is needed between steps).
 
@@ -360,7 +360,8 @@ def run_ours(args, world, rank, local):
         return
 
     peak, peak_kind = measured_peak_gbs()
-    stats_bytes = b.num_rows * V * b.elem_bytes   # every logit read once: R x V x element size
+    # every logit read once (R x V x element size) and one line maximum written per 64 logits
+    stats_bytes = b.num_rows * V * b.elem_bytes + (b.num_rows * V // 64) * b.elem_bytes
     achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
     traffic, traffic_src = recorded_traffic()
     cpu = None
@@ -377,7 +378,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "e2e": e2e, "gpu_launches": sv.spec_verify_launches_per_run() * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "sv_stats_kernel (row statistics, reads every logit once)",
+        "roofline": {"bound": "hbm", "kernel": "sv_stats_kernel (row statistics: reads every logit once, "
+                                               "writes one maximum per 64-element line)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "traffic_source": traffic_src,
@@ -386,7 +388,9 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "kernel_ms": {**kavg, "profiled_calls": calls},
         "rows_per_s": world * b.num_rows / (ms_per_step / 1e3),
-        "full_bytes_gbs": world * b.bytes_full() / (ms_per_step / 1e3) / 1e9,
+        # all input bytes of the batch (logits + every draft distribution) per step time; the
+        # path reads every logit but only the q entries it needs
+        "input_bytes_gbs": world * b.bytes_full() / (ms_per_step / 1e3) / 1e9,
         "mean_num_sampled": mean_sampled,
     }
     print(json.dumps(line), flush=True)

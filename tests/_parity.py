@@ -13,7 +13,7 @@ import numpy as np
 
 TIE_MARGIN = 1e-6
 S_RTOL = 1e-5
-RACE_RESIDUAL = 1
+RACE_NONE = 0
 
 
 def to_device(batch, device="cuda:0"):
@@ -79,7 +79,7 @@ def compare(batch, gpu: dict, ref: dict) -> dict:
         m = ref["accept_margin"][cu[i]:cu[i] + max(upto, -1) + 1]
         m = m[~np.isnan(m)]
         closest = float(m.min()) if m.size else np.inf
-        if js_ref == js_gpu and ref["race_kind"][i] == RACE_RESIDUAL:
+        if js_ref == js_gpu and ref["race_kind"][i] != RACE_NONE:
             closest = min(closest, float(ref["race_gap"][i]))
         (ties if closest < TIE_MARGIN else bad).append((i, closest))
     R = batch.num_rows

@@ -195,3 +195,51 @@ def test_repeatable_and_profiled():
     ms, calls = ctx.get_profile()
     assert calls == 2 and all(v > 0 for v in ms.values())
     ctx.close()
+
+
+def test_cuda_graph_capture_and_replay():
+    """spec_verify_run inside a captured CUDA graph: replays give the results of direct calls,
+    also after new inputs are copied into the captured buffers."""
+    import torch
+
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    b1 = workloads.workload(1)
+    b2 = _custom(15, b1.vocab_size, list(b1.cu_num_draft[1:] - b1.cu_num_draft[:-1]), "bf16", "noisy")
+    ctx = sv.SpecVerify(b1.num_reqs, b1.max_spec_len, b1.vocab_size, "bf16", True)
+    d = to_device(b1)
+    n, k = b1.num_reqs, b1.max_spec_len
+    outs = (torch.empty((n, k + 1), dtype=torch.int32, device="cuda"),
+            torch.empty(n, dtype=torch.int32, device="cuda"),
+            torch.empty(n, dtype=torch.int32, device="cuda"))
+
+    def call():
+        ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"], d["temperature"],
+                d["is_greedy"], b1.seed, out=outs)
+
+    call()
+    torch.cuda.synchronize()
+    direct1 = [o.clone() for o in outs]
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for o in outs:
+        o.fill_(-7)
+    g.replay()
+    torch.cuda.synchronize()
+    for a, c in zip(outs, direct1):
+        assert torch.equal(a, c)
+    # new inputs in the same buffers (same shapes and batch layout), replay again
+    d2 = to_device(b2)
+    for key in ("logits", "draft_ids", "draft_probs", "temperature", "is_greedy"):
+        d[key].copy_(d2[key])
+    g.replay()
+    torch.cuda.synchronize()
+    replayed2 = [o.clone() for o in outs]
+    call()
+    torch.cuda.synchronize()
+    for a, c in zip(replayed2, outs):
+        assert torch.equal(a, c)
+    assert not torch.equal(replayed2[0], direct1[0])  # the new inputs were used
+    del g
+    ctx.close()
