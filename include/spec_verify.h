@@ -182,7 +182,7 @@ int spec_verify_launches_per_run(void);
  * device memory is fully reserved up front. This entry point has no counterpart on the pages:
  * it is the same verification as spec_verify_run (same arguments, same results, the logits
  * type and vocabulary size given directly instead of through a context), but its scratch
- * space is a fixed static array inside the library (about 2.2 MB on every device that loads
+ * space is a fixed static array inside the library (about 9.4 MB on every device that loads
  * it, held until the process exits).
  *   Limits: vocab_size <= SV_NOALLOC_MAX_VOCAB, num_reqs <= SV_NOALLOC_MAX_REQS, and
  *   num_draft_tokens + num_reqs <= SV_NOALLOC_MAX_ROWS; larger batches return SV_ECAPACITY.

@@ -45,7 +45,7 @@ constexpr int kThreads = 256;       // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kMinChunk = 2048;     // smallest elements per statistics CTA (bounds the partials)
 constexpr int kStatsWaves = 2;      // automatic statistics grid: this many full waves of CTAs
-constexpr int kFixedChunk = 16384;  // statistics chunk of the static-scratch entry point
+constexpr int kFixedChunk = 32768;  // statistics chunk of the static-scratch entry point
 constexpr int kGroup = 64;          // tokens per race-clock group = elements per line
 constexpr float kLog2e = 0x1.715476p+0f;
 constexpr float kInf = __builtin_huge_valf();
@@ -372,37 +372,15 @@ __device__ __forceinline__ void combine_stat(float &L, float &s, int &idx, float
     idx = id;
 }
 
-// Warp then block reduction of (L, s, idx); result valid in thread 0.
-__device__ __forceinline__ void block_reduce_stat(float &L, float &s, int &idx, float c)
+// Warp reduction of (L, s, idx); the result is valid in every lane.
+__device__ __forceinline__ void warp_reduce_stat(float &L, float &s, int &idx, float c)
 {
-    __shared__ float sh_L[kWarps], sh_s[kWarps];
-    __shared__ int sh_i[kWarps];
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
         const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
         const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
         combine_stat(L, s, idx, L2, s2, i2, c);
-    }
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __syncthreads();  // sh_* may still be read by the previous segment's reduction
-    if (lane == 0) {
-        sh_L[warp] = L;
-        sh_s[warp] = s;
-        sh_i[warp] = idx;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        L = lane < kWarps ? sh_L[lane] : -kInf;
-        s = lane < kWarps ? sh_s[lane] : 0.0f;
-        idx = lane < kWarps ? sh_i[lane] : INT_MAX;
-#pragma unroll
-        for (int o = 4; o > 0; o >>= 1) {
-            const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
-            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
-            combine_stat(L, s, idx, L2, s2, i2, c);
-        }
     }
 }
 
@@ -413,18 +391,18 @@ struct RequestTable {
     int n;
 };
 
-// Segment [b, e) of row `row`, by the whole CTA: the elements before the first 64-element line
-// boundary one by one, then 64-byte pairs, one per lane and round (the row's request is looked up
-// while the first round is in flight), then the last few elements one by one; reduce and publish
-// the segment's partial statistics. With `lines`, the largest logit of every line that the pairs
-// cover completely is stored at lines[line] (line = (base_off + flattened element) / 64).
+// Segment [b, e) of row `row`, by the whole CTA without any barrier: the elements before the
+// first 64-element line boundary one by one, then 64-byte pairs, one per lane and round, then the
+// last few elements one by one. Every warp looks the row's request up itself (while its first
+// round is in flight) and publishes its own partial statistics of the segment, at
+// part[(row * maxseg + seg) * kWarps + warp]. With `lines`, the largest logit of every line that
+// the pairs cover completely is stored at lines[line] (line = (base_off + flattened element) / 64).
 template <typename T>
 __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int V, int row, int b,
                                               int e, int seg, int maxseg, int base_off,
                                               const RequestTable &rq, StatPart *__restrict__ part,
                                               T *__restrict__ lines)
 {
-    __shared__ float s_c;
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
     constexpr int kPE = kPairBytes / sizeof(T);  // elements per pair
@@ -438,34 +416,34 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     const long long line0 = (pos_b + (a0 - b)) >> 6;  // line of pair 0 when a0 < e
     const int lane = threadIdx.x & 31;
 
-    // the warp's pairs of a round start at ub: every lane runs the same rounds
+    // the warp's pairs of a round start at ub: every lane runs the same rounds; the next round's
+    // pair is requested before the current one is folded (two register buffers, alternating)
     int ub = static_cast<int>(threadIdx.x) & ~31;
-    uint32_t w[16];
+    uint32_t w[16], wn[16];
     if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w);
-    if (threadIdx.x < 32) {
-        const int i = row_request(rq.cu, rq.n, row, lane);
-        if (threadIdx.x == 0) {
-            bool greedy;
-            s_c = request_invT(rq.temperature, rq.is_greedy, i, greedy) * kLog2e;
-        }
-    }
-    __syncthreads();
-    const float c = s_c;
+    bool greedy;
+    const float c = request_invT(rq.temperature, rq.is_greedy, row_request(rq.cu, rq.n, row, lane),
+                                 greedy) * kLog2e;
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
-    while (ub < npair) {
+    auto round = [&](const uint32_t (&cur)[16], uint32_t (&nxt)[16]) {
         const int p = ub + lane;
         const bool valid = p < npair;
-        const typename PairMax<T>::P pm = valid ? PairMax<T>::of(w) : PairMax<T>::none();
+        if (p + kThreads < npair) ldg_pair(pbase + static_cast<size_t>(p + kThreads) * kPairBytes, nxt);
+        const typename PairMax<T>::P pm = valid ? PairMax<T>::of(cur) : PairMax<T>::none();
         if (lines) {
             const typename PairMax<T>::P lm = PairMax<T>::line(pm);
             if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair)
                 lines[line0 + p / kPPL] = PairMax<T>::store(lm);
         }
-        if (valid) fold_pair<T>(st, w, p, c, PairMax<T>::value(pm));
+        if (valid) fold_pair<T>(st, cur, p, c, PairMax<T>::value(pm));
         ub += kThreads;
-        if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w);
+    };
+    while (ub < npair) {
+        round(w, wn);
+        if (ub >= npair) break;
+        round(wn, w);
     }
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
 
@@ -478,8 +456,9 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
             if (pair_elem<T>(w, h) == st.L) idx = a0 + st.best_p * kPE + h;
     }
     float L = st.L, s = st.s;
-    block_reduce_stat(L, s, idx, c);
-    if (threadIdx.x == 0) part[static_cast<size_t>(row) * maxseg + seg] = StatPart{L, s, idx, 0};
+    warp_reduce_stat(L, s, idx, c);
+    if (lane == 0)
+        part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
 }
 
 // Row statistics over the flattened [rows x V] logits, split evenly: CTA k streams elements
@@ -487,7 +466,7 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
 // on line boundaries), which covers one or more row segments, and writes one partial per
 // segment. Pure streaming: no atomics, nothing waits on another CTA.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 5)
+__global__ void __launch_bounds__(kThreads, 4)
 sv_stats_kernel(const T *__restrict__ logits, int V, long long total, Divisor chunk, Divisor dv,
                 int maxseg, int base_off, RequestTable rq, StatPart *__restrict__ part,
                 T *__restrict__ lines)
@@ -973,9 +952,9 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
                                           div_floor(P.base_off + rbase, P.chunk)) + 1;
         float L = -kInf, s = 0.0f;
         int idx = INT_MAX;
-        for (int k = lane; k < nseg; k += 32) {
+        for (int k = lane; k < nseg * kWarps; k += 32) {  // every warp of every segment
             const float4 raw = __ldg(reinterpret_cast<const float4 *>(P.part) +
-                                     static_cast<size_t>(row) * P.maxseg + k);
+                                     static_cast<size_t>(row) * P.maxseg * kWarps + k);
             combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
         }
 #pragma unroll
@@ -1258,7 +1237,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
     const long long rows = static_cast<long long>(max_num_reqs) * (max_spec_len + 1);
     const long long maxseg = ceil_div(vocab_size, kMinChunk) + 1;
-    if (rows > INT_MAX / 8 || rows * maxseg > (1LL << 31) || max_spec_len > (1 << 16))
+    if (rows > INT_MAX / 8 || rows * maxseg * kWarps > (1LL << 31) || max_spec_len > (1 << 16))
         return SV_ECAPACITY;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
@@ -1286,7 +1265,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     const size_t R = static_cast<size_t>(rows), S = static_cast<size_t>(maxseg);
     const size_t nlines = (R * static_cast<size_t>(vocab_size) + 2 * kGroup) / kGroup;
     const size_t eb = logits_dtype == SV_BF16 ? 2 : 4;
-    bool ok = cudaMalloc(&ctx->statpart, R * S * sizeof(StatPart)) == cudaSuccess &&
+    bool ok = cudaMalloc(&ctx->statpart, R * S * kWarps * sizeof(StatPart)) == cudaSuccess &&
               cudaMalloc(&ctx->lines, nlines * eb) == cudaSuccess &&
               cudaMalloc(&ctx->flags, 2 * sizeof(unsigned)) == cudaSuccess;
     ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
@@ -1520,7 +1499,7 @@ constexpr int kNoAllocMaxSeg = (kNoAllocMaxVocab + kFixedChunk - 1) / kFixedChun
 constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr size_t kOffStatPart = 0;
 constexpr size_t kOffFlags =
-    kOffStatPart + align256(sizeof(StatPart) * size_t(kNoAllocMaxRows) * kNoAllocMaxSeg);
+    kOffStatPart + align256(sizeof(StatPart) * size_t(kNoAllocMaxRows) * kNoAllocMaxSeg * kWarps);
 constexpr size_t kNoAllocBytes = kOffFlags + align256(2 * sizeof(unsigned));
 
 // One copy per device that loads this library, kept until the process exits. Every call of
