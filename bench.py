@@ -344,13 +344,15 @@ def run_ours(args, world, rank, local):
             t = torch.tensor([te], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             te = float(t.item())
-        h2d = (h_logits.numel() * h_logits.element_size()
-               + (h_q.numel() * 4 if h_q is not None else 0)
-               + nd * 4 + (n + 1) * 4 + n * 4 + n)
+        # copied every step: the logits and the small per-request arrays; the page-locked draft
+        # distributions are read in place by the kernels (only the entries they need)
+        h2d = h_logits.numel() * h_logits.element_size() + nd * 4 + (n + 1) * 4 + n * 4 + n
         d2h = sum(t.numel() * 4 for t in h_out)
         e2e = {"value": world * nd * ke / te, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": ke, "ms_per_step": te / ke * 1e3,
-               "timing": "host wall clock around run_host (copies + kernels + stream sync)"}
+               "timing": "host wall clock around run_host (copies + kernels + stream sync)",
+               "in_place": "draft_probs (page-locked host memory) read over the host link by the "
+                           "verify kernel, only the entries it needs" if h_q is not None else None}
         if not np.array_equal(h_out[0].numpy(), outs[0].cpu().numpy()):
             raise RuntimeError("host-buffer path disagrees with the device path")
 

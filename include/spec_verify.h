@@ -138,10 +138,13 @@ int spec_verify_reserve_host_io(spec_verify_ctx *ctx);
 
 /*
  * Same as spec_verify_run but every pointer is a HOST pointer (page-locked memory gives
- * asynchronous copies; pageable memory works too). The inputs are copied to the context's
- * staging buffers, the batch is verified, and sampled / num_sampled / num_rejected are copied
- * back; the call returns after the stream has finished (the outputs are ready). Requires
- * spec_verify_reserve_host_io.
+ * asynchronous copies; pageable memory works too). The logits and the small per-request arrays
+ * are copied to the context's staging buffers, the batch is verified, and sampled / num_sampled /
+ * num_rejected are copied back; the call returns after the stream has finished (the outputs are
+ * ready). draft_probs, of which the verifier reads only the draft's entry per position and the
+ * entries of the few vocabulary groups its race evaluates, is read in place over the host link
+ * when it is page-locked (allocated or registered through CUDA), and copied otherwise.
+ * Requires spec_verify_reserve_host_io.
  */
 int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
                          const float *draft_probs, const int32_t *cu_num_draft,

@@ -306,7 +306,8 @@ class SpecVerify:
                  seed: int, sampled, num_sampled, num_rejected, *, req_index_base: int = 0,
                  max_spec_len: int | None = None, stream=None) -> None:
         """Verify a batch held in host memory (numpy arrays or CPU tensors; pinned memory
-        gives asynchronous copies); outputs are written to the host arrays given."""
+        gives asynchronous copies, and pinned draft_probs is read in place by the kernels);
+        outputs are written to the host arrays given."""
         num_reqs = len(cu_num_draft) - 1
         nd = len(draft_ids)
         kmax = self.max_spec_len if max_spec_len is None else max_spec_len

@@ -109,12 +109,6 @@ __device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long p)
 // >= 0; divisions round monotonically).
 __device__ __forceinline__ float key_bound(float b) { return b * 1.00002f; }
 
-// Group g's smallest clock: E_g = -log(W) / 64 from word 0 of its head call (exact scaling).
-__device__ __forceinline__ float group_emin(const sv::Philox4 &h)
-{
-    return __fmul_rn(-sv::log_f32(sv::uniform_from_word(h.x)), 0x1p-6f);
-}
-
 __device__ __forceinline__ void emit_row(int i, int jstar, int K, int q0, int token,
                                          const int32_t *__restrict__ draft_ids,
                                          int32_t *__restrict__ sampled, int stride,
@@ -619,20 +613,20 @@ struct SearchSmem {
     unsigned long long *tmp;  // [sp] the entries in bin order
     int *bin_n;               // [kBins + 1] entries per bin, then bin starts
     unsigned *bin_max;        // [kBins] largest key bound (encoded) of each bin
-    unsigned *range;          // [2] largest and smallest key bound (encoded) of the list
+    unsigned *top;            // largest group bound (encoded)
     float *lm;                // [G + 2] line maxima of the row, until the bounds are taken
-    float *pb;                // [G] p-race bound per group (NaN once evaluated)
-    float *eg;                // [G] smallest clock E_g of the group
-    uint8_t *ag;              // [G] slot that holds it
+    float *pb;                // [G] upper bound of the group's keys (NaN once evaluated)
+    uint32_t *ew;             // [G] word 0 of the group's head call (gives E_g)
+    uint8_t *ag;              // [G] slot that holds the group's smallest clock
     unsigned long long *best; // best candidate so far, packed (key, ~v); 0 = none
     int *cnt;
 };
 
 // Dynamic shared memory layout of a verify CTA (bytes): the candidate buffer (a power of two
 // >= G entries of 8 bytes, also holding the G + 2 line maxima), the binned copy of it, m / S /
-// argmax of the request's rows (kmax + 1 each), pb, eg, ag.
+// argmax of the request's rows (kmax + 1 each), pb, ew, ag.
 struct VerifyLayout {
-    size_t tmp, rows, pb, eg, ag, total;
+    size_t tmp, rows, pb, ew, ag, total;
 };
 __host__ __device__ inline int search_capacity(int G)
 {
@@ -649,14 +643,36 @@ __host__ __device__ inline VerifyLayout verify_layout(int V, int kmax)
     l.tmp = (buf + 15) / 16 * 16;
     l.rows = l.tmp + 8 * sp;
     l.pb = l.rows + 12 * (static_cast<size_t>(kmax) + 1);
-    l.eg = l.pb + 4 * G;
-    l.ag = l.eg + 4 * G;
+    l.ew = l.pb + 4 * G;
+    l.ag = l.ew + 4 * G;
     l.total = l.ag + G;
     return l;
 }
 
-// pb[g] = bound of group g, fl(exp(fl(x_max - m)) / E_g) with x_max = fl(line max * invT) (before
-// key_bound); eg[g] = E_g, ag[g] = a from the group's head call. Returns the thread's best
+// Group g's smallest clock, E_g = -log(W) / 64, from word 0 of its head call (exact scaling).
+__device__ __forceinline__ float group_emin_word(uint32_t w_head)
+{
+    return __fmul_rn(-sv::log_f32(sv::uniform_from_word(w_head)), 0x1p-6f);
+}
+
+// An upper bound of every key exp(y') / E' with y' <= y and E' >= E_g (W = word 0 of the group's
+// head call), from the hardware approximations: lg2.approx errs by less than 2^-22 absolute and
+// ex2.approx by a few 2^-23 relative on these ranges, and the fp32 product y log2(e) by
+// |y| 2^-23; the margins below (2^-20 absolute on -log2 W, 2^-12 relative twice) cover all of
+// that many times over. Only the evaluation of a group uses its exact E_g. +inf when -log W is
+// too small to bound from below (W within about 10^-6 of 1), and for a NaN y.
+__device__ __forceinline__ float group_bound(float y, uint32_t w_head)
+{
+    float l2;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(sv::uniform_from_word(w_head)));
+    const float nl = (-l2 - 0x1p-20f) * 0x1.62e2p-1f;  // <= -ln W (ln 2 rounded down)
+    const float tub = sv::ex2_approx(y * kLog2e) * (1.0f + 0x1p-12f);
+    const float b = __fdividef(tub, nl * 0x1p-6f) * (1.0f + 0x1p-12f);
+    return (nl > 0.0f && b == b) ? b : kInf;
+}
+
+// pb[g] = an upper bound of every key in group g (from x_max = fl(line max * invT) and the
+// group's head call), ew[g] / ag[g] = the head's word 0 and slot. Returns the thread's best
 // (pb, g) packed, 0 if it has no group.
 template <typename T>
 __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &rl,
@@ -678,11 +694,9 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
         for (int k = 0; k < kStep; ++k) {
             const int g = g0 + k * kThreads;
             if (g < r.G) {
-                const float E = group_emin(h[k]);
-                const float t = sv::exp_f32(__fsub_rn(__fmul_rn(lmax[k], r.invT), r.m));
-                const float b = __fdiv_rn(t, E);
+                const float b = group_bound(__fsub_rn(__fmul_rn(lmax[k], r.invT), r.m), h[k].x);
                 sm.pb[g] = b;
-                sm.eg[g] = E;
+                sm.ew[g] = h[k].x;
                 sm.ag[g] = static_cast<uint8_t>(h[k].y & 63u);
                 best = max(best, pack_key(b, g));
             }
@@ -722,7 +736,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
     for (int k = 0; k < B; ++k) {
         const int g = gs[k];
         if (g < 0) continue;
-        const float E = sm.eg[g];
+        const float E = group_emin_word(sm.ew[g]);
         const int a = sm.ag[g];
         const int v0 = g * kGroup + 2 * lane, v1 = v0 + 1;
         const bool in0 = v0 < r.V, in1 = v1 < r.V;
@@ -764,66 +778,13 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
     }
 }
 
-// Order the entries buf[0, cnt) roughly best first into tmp, by the whole CTA: kBins bins of
-// equal width in log2 of the key bound, from the largest bound down to 2^-48 of it (lower bounds
-// share the last bin), bin 0 first, any order inside a bin (the order only affects speed). The bin of an entry goes to bits 24..31 of its
-// low word (groups are < 2^24); bin_max[b] is the largest bound in bin b.
-__device__ void bin_order(const SearchSmem &sm, int cnt)
+// Bin of a key bound (encoded kb) among kBins log-spaced bins from log2(top) down to bottom
+// (bin 0 = the largest bounds; NaN / inf and anything lower go to the last bin). The bins only
+// order the evaluation: any placement is correct.
+__device__ __forceinline__ int bound_bin(unsigned kb, float top, float inv_w)
 {
-    const int tid = threadIdx.x;
-    if (tid < kBins) {
-        sm.bin_n[tid] = 0;
-        sm.bin_max[tid] = 0u;
-    }
-    if (tid == 0) {
-        sm.range[0] = 0u;
-        sm.range[1] = 0xFFFFFFFFu;
-    }
-    __syncthreads();
-    unsigned hi = 0u, lo = 0xFFFFFFFFu;
-    for (int e = tid; e < cnt; e += kThreads) {
-        const unsigned kb = static_cast<unsigned>(sm.buf[e] >> 32);
-        hi = max(hi, kb);
-        lo = min(lo, kb);
-    }
-    hi = __reduce_max_sync(0xFFFFFFFFu, hi);
-    lo = __reduce_min_sync(0xFFFFFFFFu, lo);
-    if ((tid & 31) == 0) {
-        atomicMax(&sm.range[0], hi);
-        atomicMin(&sm.range[1], lo);
-    }
-    __syncthreads();
-    const float top = __log2f(key_dec(sm.range[0]));
-    const float bottom = fmaxf(__log2f(key_dec(sm.range[1])), top - 48.0f);
-    const float inv_w = (top - bottom) > 0.0f ? kBins / (top - bottom) : 0.0f;
-    for (int e = tid; e < cnt; e += kThreads) {
-        const unsigned kb = static_cast<unsigned>(sm.buf[e] >> 32);
-        const float t = (top - __log2f(key_dec(kb))) * inv_w;  // NaN / inf go to the last bin
-        const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
-        atomicAdd(&sm.bin_n[b], 1);
-        atomicMax(&sm.bin_max[b], kb);
-    }
-    __syncthreads();
-    if (tid < 32) {  // exclusive prefix of the bin counts (kBins == 32)
-        const int n = sm.bin_n[tid];
-        int x = n;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-            if (tid >= o) x += y;
-        }
-        sm.bin_n[tid] = x - n;  // running cursor, starts at the bin's first slot
-    }
-    __syncthreads();
-    for (int e = tid; e < cnt; e += kThreads) {
-        const unsigned long long ent = sm.buf[e];
-        const float t = (top - __log2f(key_dec(static_cast<unsigned>(ent >> 32)))) * inv_w;
-        const int b = t < static_cast<float>(kBins - 1) ? static_cast<int>(t) : kBins - 1;
-        const int pos = atomicAdd(&sm.bin_n[b], 1);
-        sm.tmp[pos] = (ent & 0xFFFFFFFF00000000ull) | (static_cast<unsigned long long>(b) << 24) |
-                      (ent & 0x00FFFFFFull);
-    }
-    __syncthreads();
+    const float t = (top - __log2f(key_dec(kb))) * inv_w;
+    return t < static_cast<float>(kBins - 1) ? (t > 0.0f ? static_cast<int>(t) : 0) : kBins - 1;
 }
 
 // Best-first race over one row by the whole CTA. Returns the packed winner (key, ~v), 0 when no
@@ -838,19 +799,30 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
     if (tid == 0) {
         *sm.best = 0;
         *sm.cnt = 0;
+        *sm.top = 0u;
+    }
+    if (tid < kBins) {
+        sm.bin_n[tid] = 0;
+        sm.bin_max[tid] = 0u;
     }
     __syncthreads();  // bounds complete: lm is free from here on (buf reuses it)
     // round 1: every warp evaluates its own best-bounded group
     const unsigned long long wb = warp_max_u64(mine);
+    if (lane == 0) atomicMax(sm.top, static_cast<unsigned>(wb >> 32));
     if (wb != 0) {
         const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
         eval_groups<T, kRes, 1>(r, gs, sm);
         if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
     }
     __syncthreads();
-    // round 2: every group whose bound reaches the best key found so far, best bound first
+    // round 2: every group whose bound reaches the best key found so far, best bound first:
+    // the candidates are listed with their bin (log-spaced between the largest bound and the
+    // best key), counted per bin, then placed in bin order
     const unsigned long long best1 = *sm.best;
     const unsigned thr1 = static_cast<unsigned>(best1 >> 32);
+    const float top = __log2f(key_dec(*sm.top));
+    const float bottom = fmaxf(best1 != 0 ? __log2f(key_dec(thr1)) : -kInf, top - 48.0f);
+    const float inv_w = top - bottom > 0.0f ? kBins / (top - bottom) : 0.0f;
     for (int g0 = 0; g0 < r.G; g0 += kThreads) {
         const int g = g0 + tid;
         unsigned kb = 0;
@@ -862,15 +834,38 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
                 take = best1 == 0 || kb >= thr1;
             }
         }
+        int bin = 0;
+        if (take) {
+            bin = bound_bin(kb, top, inv_w);
+            atomicAdd(&sm.bin_n[bin], 1);
+            atomicMax(&sm.bin_max[bin], kb);
+        }
         const unsigned msk = __ballot_sync(0xFFFFFFFFu, take);
         int pos = 0;
         if (lane == 0 && msk) pos = atomicAdd(sm.cnt, __popc(msk));
         pos = __shfl_sync(0xFFFFFFFFu, pos, 0) + __popc(msk & ((1u << lane) - 1u));
-        if (take) sm.buf[pos] = (static_cast<unsigned long long>(kb) << 32) | static_cast<unsigned>(g);
+        if (take)
+            sm.buf[pos] = (static_cast<unsigned long long>(kb) << 32) |
+                          (static_cast<unsigned>(bin) << 24) | static_cast<unsigned>(g);
     }
     __syncthreads();
     const int cnt = *sm.cnt;
-    bin_order(sm, cnt);
+    if (tid < 32) {  // exclusive prefix of the bin counts (kBins == 32): the bins' cursors
+        const int nb = sm.bin_n[tid];
+        int x = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+            if (tid >= o) x += y;
+        }
+        sm.bin_n[tid] = x - nb;
+    }
+    __syncthreads();
+    for (int e = tid; e < cnt; e += kThreads) {
+        const unsigned long long ent = sm.buf[e];
+        sm.tmp[atomicAdd(&sm.bin_n[(ent >> 24) & 0xFFu], 1)] = ent;
+    }
+    __syncthreads();
     for (int e0 = warp * B; e0 < cnt; e0 += kWarps * B) {
         const unsigned long long cur = ld_best(sm.best);
         const unsigned thr = static_cast<unsigned>(cur >> 32);
@@ -908,7 +903,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     __shared__ int s_cnt;
     __shared__ int s_bin_n[kBins];
     __shared__ unsigned s_bin_max[kBins];
-    __shared__ unsigned s_range[2];
+    __shared__ unsigned s_top;
     const int i = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = P.rq.n;
@@ -1007,10 +1002,10 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
     sm.bin_n = s_bin_n;
     sm.bin_max = s_bin_max;
-    sm.range = s_range;
+    sm.top = &s_top;
     sm.lm = reinterpret_cast<float *>(dyn);
     sm.pb = reinterpret_cast<float *>(dyn + lay.pb);
-    sm.eg = reinterpret_cast<float *>(dyn + lay.eg);
+    sm.ew = reinterpret_cast<uint32_t *>(dyn + lay.ew);
     sm.ag = dyn + lay.ag;
     sm.best = &s_best;
     sm.cnt = &s_cnt;
@@ -1207,6 +1202,19 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
+// Device address of a host buffer that kernels can read in place: page-locked memory (allocated
+// or registered through CUDA) is addressable from the device under unified addressing. nullptr
+// for pageable memory, which is copied instead.
+const void *in_place(const void *p)
+{
+    cudaPointerAttributes a;
+    if (!p || cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 int check_run_args(const spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
                    const float *draft_probs, const int32_t *cu, const float *temperature,
                    const uint8_t *is_greedy, int num_reqs, int nd, int kmax,
@@ -1375,9 +1383,12 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
     int32_t *d_ns = d_sampled + N * (ctx->max_spec_len + 1);
     int32_t *d_nr = d_ns + N;
     const size_t stride = static_cast<size_t>(max_spec_len_this_batch) + 1;
+    // the verifier reads only a few entries of q: page-locked q is read in place, not copied
+    const float *q_dev = static_cast<const float *>(in_place(draft_probs));
     bool ok = cudaMemcpyAsync(ctx->io_logits, logits, rows * V * eb, cudaMemcpyHostToDevice, stream) == cudaSuccess &&
-              (!draft_probs || cudaMemcpyAsync(ctx->io_q, draft_probs, static_cast<size_t>(num_draft_tokens) * V * 4,
-                                               cudaMemcpyHostToDevice, stream) == cudaSuccess) &&
+              (!draft_probs || q_dev ||
+               cudaMemcpyAsync(ctx->io_q, draft_probs, static_cast<size_t>(num_draft_tokens) * V * 4,
+                               cudaMemcpyHostToDevice, stream) == cudaSuccess) &&
               (num_draft_tokens == 0 || cudaMemcpyAsync(d_ids, draft_ids, static_cast<size_t>(num_draft_tokens) * 4,
                                                         cudaMemcpyHostToDevice, stream) == cudaSuccess) &&
               cudaMemcpyAsync(d_cu, cu_num_draft, (static_cast<size_t>(num_reqs) + 1) * 4,
@@ -1387,7 +1398,7 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
               cudaMemcpyAsync(ctx->io_greedy, is_greedy, static_cast<size_t>(num_reqs),
                               cudaMemcpyHostToDevice, stream) == cudaSuccess;
     if (!ok) return SV_ECUDA;
-    rc = spec_verify_run(ctx, ctx->io_logits, d_ids, draft_probs ? ctx->io_q : nullptr, d_cu,
+    rc = spec_verify_run(ctx, ctx->io_logits, d_ids, draft_probs ? (q_dev ? q_dev : ctx->io_q) : nullptr, d_cu,
                          ctx->io_temp, ctx->io_greedy, seed, req_index_base, num_reqs,
                          num_draft_tokens, max_spec_len_this_batch, d_sampled, d_ns, d_nr,
                          nullptr, nullptr, nullptr, cuda_stream);

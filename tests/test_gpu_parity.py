@@ -243,3 +243,26 @@ def test_cuda_graph_capture_and_replay():
     assert not torch.equal(replayed2[0], direct1[0])  # the new inputs were used
     del g
     ctx.close()
+
+
+def test_host_entry_point_reads_page_locked_q_in_place():
+    """run_host with page-locked inputs (q read in place by the kernels) matches the device path."""
+    import torch
+
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    b = workloads.workload(1)
+    ctx = sv.SpecVerify(b.num_reqs, b.max_spec_len, b.vocab_size, "bf16", True)
+    ctx.reserve_host_io()
+    dev = gpu_run(b, ctx)
+    n, k = b.num_reqs, b.max_spec_len
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    outs = [torch.empty((n, k + 1), dtype=torch.int32).pin_memory(),
+            torch.empty(n, dtype=torch.int32).pin_memory(),
+            torch.empty(n, dtype=torch.int32).pin_memory()]
+    ctx.run_host(pin(b.logits.view(np.int16)), pin(b.draft_ids), pin(b.draft_probs),
+                 pin(b.cu_num_draft), pin(b.temperature), pin(b.is_greedy), b.seed, *outs)
+    np.testing.assert_array_equal(outs[0].numpy(), dev["sampled"])
+    np.testing.assert_array_equal(outs[1].numpy(), dev["num_sampled"])
+    np.testing.assert_array_equal(outs[2].numpy(), dev["num_rejected"])
+    ctx.close()
