@@ -44,6 +44,8 @@ namespace {
 constexpr int kThreads = 256;       // both kernels
 constexpr int kWarps = kThreads / 32;
 constexpr int kMinChunk = 2048;     // smallest elements per statistics CTA (bounds the partials)
+constexpr int kChunkAlign = 512;    // statistics chunks: whole 16-byte spans of the line array
+constexpr int kMaxChunk = 1 << 19;  // largest: its line maxima fit in 32 KB of shared memory
 constexpr int kStatsWaves = 2;      // automatic statistics grid: this many full waves of CTAs
 constexpr int kFixedChunk = 32768;  // statistics chunk of the static-scratch entry point
 constexpr int kGroup = 64;          // tokens per race-clock group = elements per line
@@ -263,9 +265,45 @@ template <> struct PairMax<float> {
     static __device__ __forceinline__ float store(P m) { return m; }
 };
 
+// Two fp32 values in one 64-bit register pair, and the packed fp32x2 operations of sm_100+
+// (each lane an ordinary correctly rounded fma / add).
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi)
+{
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
+                                                     unsigned long long c)
+{
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Elements 2k and 2k + 1 of a pair as an fp32x2 value.
+template <typename T>
+__device__ __forceinline__ unsigned long long pair_elems2(const uint32_t (&w)[16], int k)
+{
+    if constexpr (sizeof(T) == 2)
+        return f2_pack(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+    else
+        return f2_pack(__uint_as_float(w[2 * k]), __uint_as_float(w[2 * k + 1]));
+}
+
 // Fold pair p, whose largest element is mx, without branches: one rescale of the running sum,
-// then the sum of 2^((l - L) c). Only the pair that first reached the max is recorded; its lowest
-// index is recovered at the end of the segment.
+// then the sum of 2^((l - L) c), two elements per packed fma / add. Only the pair that first
+// reached the max is recorded; its lowest index is recovered at the end of the segment.
 template <typename T>
 __device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16], int p, float c,
                                           float mx)
@@ -277,11 +315,18 @@ __device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16]
     st.best_e = up ? -1 : st.best_e;
     st.L = up ? mx : st.L;
     st.Lc = st.L > -kInf ? st.L * c : 0.0f;
-    float s0 = 0.0f, s1 = 0.0f;
+    const unsigned long long c2 = f2_pack(c, c), nLc2 = f2_pack(-st.Lc, -st.Lc);
+    unsigned long long acc[2] = {0ull, 0ull};  // fp32x2 zeros
 #pragma unroll
-    for (int h = 0; h < kPE; ++h)
-        ((h & 1) ? s1 : s0) += sv::ex2_approx(fmaf(pair_elem<T>(w, h), c, -st.Lc));
-    st.s += s0 + s1;
+    for (int k = 0; k < kPE / 2; ++k) {
+        float y0, y1;
+        f2_unpack(f2_fma(pair_elems2<T>(w, k), c2, nLc2), y0, y1);
+        acc[k & 1] = f2_add(acc[k & 1], f2_pack(sv::ex2_approx(y0), sv::ex2_approx(y1)));
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(acc[0], a0, a1);
+    f2_unpack(acc[1], b0, b1);
+    st.s += (a0 + b0) + (a1 + b1);
 }
 
 // Division by a launch constant d > 0 without a division instruction: with M = ceil(2^64 / d)
@@ -389,13 +434,14 @@ struct RequestTable {
 // first 64-element line boundary one by one, then 64-byte pairs, one per lane and round, then the
 // last few elements one by one. Every warp looks the row's request up itself (while its first
 // round is in flight) and publishes its own partial statistics of the segment, at
-// part[(row * maxseg + seg) * kWarps + warp]. With `lines`, the largest logit of every line that
-// the pairs cover completely is stored at lines[line] (line = (base_off + flattened element) / 64).
+// part[(row * maxseg + seg) * kWarps + warp]. With `s_lines`, the largest logit of every line that
+// the pairs cover completely is stored at s_lines[line - line_base] in shared memory (line =
+// (base_off + flattened element) / 64).
 template <typename T>
 __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int V, int row, int b,
                                               int e, int seg, int maxseg, int base_off,
                                               const RequestTable &rq, StatPart *__restrict__ part,
-                                              T *__restrict__ lines)
+                                              T *__restrict__ s_lines, long long line_base)
 {
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
@@ -407,14 +453,17 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     const int npair = (e - a0) / kPE;
     const int a1 = a0 + npair * kPE;
     const char *pbase = reinterpret_cast<const char *>(rp + a0);
-    const long long line0 = (pos_b + (a0 - b)) >> 6;  // line of pair 0 when a0 < e
+    const int line0 = static_cast<int>(((pos_b + (a0 - b)) >> 6) - line_base);  // pair 0's line
     const int lane = threadIdx.x & 31;
 
-    // the warp's pairs of a round start at ub: every lane runs the same rounds; the next round's
-    // pair is requested before the current one is folded (two register buffers, alternating)
+    // the warp's pairs of a round start at ub: every lane runs the same rounds; the pair of the
+    // round after next is requested before the current one is folded (three register buffers in
+    // rotation: two rounds in flight while one is folded)
     int ub = static_cast<int>(threadIdx.x) & ~31;
-    uint32_t w[16], wn[16];
-    if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w);
+    uint32_t w0[16], w1[16], w2[16];
+    if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w0);
+    if (ub + lane + kThreads < npair)
+        ldg_pair(pbase + static_cast<size_t>(ub + lane + kThreads) * kPairBytes, w1);
     bool greedy;
     const float c = request_invT(rq.temperature, rq.is_greedy, row_request(rq.cu, rq.n, row, lane),
                                  greedy) * kLog2e;
@@ -424,30 +473,33 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     auto round = [&](const uint32_t (&cur)[16], uint32_t (&nxt)[16]) {
         const int p = ub + lane;
         const bool valid = p < npair;
-        if (p + kThreads < npair) ldg_pair(pbase + static_cast<size_t>(p + kThreads) * kPairBytes, nxt);
+        if (p + 2 * kThreads < npair)
+            ldg_pair(pbase + static_cast<size_t>(p + 2 * kThreads) * kPairBytes, nxt);
         const typename PairMax<T>::P pm = valid ? PairMax<T>::of(cur) : PairMax<T>::none();
-        if (lines) {
+        if (s_lines) {
             const typename PairMax<T>::P lm = PairMax<T>::line(pm);
             if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair)
-                lines[line0 + p / kPPL] = PairMax<T>::store(lm);
+                s_lines[line0 + p / kPPL] = PairMax<T>::store(lm);
         }
         if (valid) fold_pair<T>(st, cur, p, c, PairMax<T>::value(pm));
         ub += kThreads;
     };
     while (ub < npair) {
-        round(w, wn);
+        round(w0, w2);
         if (ub >= npair) break;
-        round(wn, w);
+        round(w1, w0);
+        if (ub >= npair) break;
+        round(w2, w1);
     }
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
 
     // lowest index where this thread's max occurs
     int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
     if (st.best_p >= 0) {
-        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w);
+        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w0);
 #pragma unroll
         for (int h = kPE - 1; h >= 0; --h)
-            if (pair_elem<T>(w, h) == st.L) idx = a0 + st.best_p * kPE + h;
+            if (pair_elem<T>(w0, h) == st.L) idx = a0 + st.best_p * kPE + h;
     }
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
@@ -456,18 +508,25 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
 }
 
 // Row statistics over the flattened [rows x V] logits, split evenly: CTA k streams elements
-// [k * chunk - base_off, (k + 1) * chunk - base_off) (chunk a multiple of 64, so that CTAs meet
-// on line boundaries), which covers one or more row segments, and writes one partial per
-// segment. Pure streaming: no atomics, nothing waits on another CTA.
+// [k * chunk - base_off, (k + 1) * chunk - base_off) (chunk a multiple of 512, so that CTAs meet
+// on line boundaries and own whole 16-byte spans of the line array), which covers one or more row
+// segments, and writes one partial per warp and segment. With `lines`, the CTA gathers its line
+// maxima in shared memory (chunk / 64 of them) and writes them out at the end in one coalesced
+// sweep, lines [k * chunk / 64, (k + 1) * chunk / 64); entries of lines that a row covers only in
+// part are left undefined (the verify kernel reads those lines from the logits). Nothing waits on
+// another CTA.
 template <typename T>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 3)
 sv_stats_kernel(const T *__restrict__ logits, int V, long long total, Divisor chunk, Divisor dv,
                 int maxseg, int base_off, RequestTable rq, StatPart *__restrict__ part,
                 T *__restrict__ lines)
 {
+    extern __shared__ __align__(16) unsigned char s_raw[];
     const long long start = max(0LL, static_cast<long long>(blockIdx.x) * chunk.d - base_off);
     const long long stop = min(total, static_cast<long long>(blockIdx.x + 1) * chunk.d - base_off);
     if (start >= stop) return;
+    T *s_lines = lines ? reinterpret_cast<T *>(s_raw) : nullptr;
+    const long long line_base = static_cast<long long>(blockIdx.x) * (chunk.d >> 6);
     const int r_first = static_cast<int>(div_floor(start, dv));
     const int r_last = static_cast<int>(div_floor(stop - 1, dv));
     for (int row = r_first; row <= r_last; ++row) {
@@ -476,7 +535,18 @@ sv_stats_kernel(const T *__restrict__ logits, int V, long long total, Divisor ch
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
         const int fk = static_cast<int>(div_floor(base_off + rbase, chunk));
         stats_segment<T>(logits, V, row, b, e, static_cast<int>(blockIdx.x) - fk, maxseg, base_off,
-                         rq, part, lines);
+                         rq, part, s_lines, line_base);
+    }
+    if (lines) {
+        __syncthreads();
+        const long long lines_end = (base_off + total + kGroup - 1) >> 6;
+        const int nl = static_cast<int>(min(chunk.d >> 6, lines_end - line_base));
+        const int nv = nl * static_cast<int>(sizeof(T)) / 16;  // whole 16-byte vectors
+        uint4 *dst = reinterpret_cast<uint4 *>(lines + line_base);
+        const uint4 *src = reinterpret_cast<const uint4 *>(s_raw);
+        for (int k = threadIdx.x; k < nv; k += kThreads) dst[k] = src[k];
+        for (int k = nv * 16 / static_cast<int>(sizeof(T)) + threadIdx.x; k < nl; k += kThreads)
+            lines[line_base + k] = s_lines[k];
     }
 }
 
@@ -1156,7 +1226,8 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
     const int base_off = static_cast<int>((reinterpret_cast<uintptr_t>(logits) % (kGroup * sizeof(T))) / sizeof(T));
     long long chunk1 = ctx->stats_chunk;
     if (chunk1 <= 0) chunk1 = (total + kStatsWaves * ctx->stats_ctas - 1) / (kStatsWaves * ctx->stats_ctas);
-    chunk1 = std::max<long long>((chunk1 + kGroup - 1) / kGroup * kGroup, kMinChunk);
+    chunk1 = std::min<long long>(std::max<long long>((chunk1 + kChunkAlign - 1) / kChunkAlign * kChunkAlign,
+                                                     kMinChunk), kMaxChunk);
     const int grid1 = static_cast<int>((total + base_off + chunk1 - 1) / chunk1);
     const RequestTable rq{cu, temperature, is_greedy, num_reqs};
     T *lines = static_cast<T *>(ctx->lines);
@@ -1189,7 +1260,8 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
         prof_collect(ctx, *slot);
         cudaEventRecord(slot->ev[0], stream);
     }
-    sv_stats_kernel<T><<<grid1, kThreads, 0, stream>>>(logits, V, total, make_divisor(chunk1),
+    const size_t smem1 = lines ? static_cast<size_t>(chunk1 / kGroup) * sizeof(T) : 0;
+    sv_stats_kernel<T><<<grid1, kThreads, smem1, stream>>>(logits, V, total, make_divisor(chunk1),
                                                        make_divisor(V), ctx->maxseg, base_off, rq,
                                                        ctx->statpart, lines);
     if (slot) cudaEventRecord(slot->ev[1], stream);
@@ -1464,7 +1536,7 @@ int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk)
 {
     if (!ctx || stats_chunk < -1) return SV_EINVAL;
     if (stats_chunk == -1) ctx->stats_chunk = 0;
-    else if (stats_chunk) ctx->stats_chunk = (std::max(stats_chunk, kMinChunk) + kGroup - 1) / kGroup * kGroup;
+    else if (stats_chunk) ctx->stats_chunk = (std::max(stats_chunk, kMinChunk) + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
     return SV_OK;
 }
 
