@@ -675,7 +675,9 @@ struct RaceRow {
     uint32_t j, ireq, k0, k1;  // Philox counter words 1, 2 and key
 };
 
-// Shared memory of the search (one CTA).
+// Shared memory of the search (one CTA). Each warp keeps a queue of candidate tokens (at most
+// 32 + 64: it is emptied once it holds 32, and a group adds at most 64).
+constexpr int kQueue = 96;
 constexpr int kBins = 32;  // candidate bins of the best-first order
 
 struct SearchSmem {
@@ -690,6 +692,8 @@ struct SearchSmem {
     uint8_t *ag;              // [G] slot that holds the group's smallest clock
     unsigned long long *best; // best candidate so far, packed (key, ~v); 0 = none
     int *cnt;
+    uint32_t *qgs;            // [kWarps][kQueue] candidate tokens of each warp: group << 6 | slot
+    float *ql, *qq;           // [kWarps][kQueue] their raw logits and q entries
 };
 
 // Dynamic shared memory layout of a verify CTA (bytes): the candidate buffer (a power of two
@@ -782,14 +786,63 @@ __device__ __forceinline__ unsigned long long ld_best(const unsigned long long *
     return __shfl_sync(0xFFFFFFFFu, v, 0);
 }
 
-// Exact keys of up to B groups by one warp (two adjacent tokens per lane and group; gs[k] < 0:
-// no group), merged into *sm.best. All loads are issued before the first group is evaluated.
+// An upper bound of 1 / E_g from the group's head word W (E_g = -log(W) / 64): hardware lg2 and
+// rcp with the margins of group_bound; +inf when -log W is too small to bound from below.
+__device__ __forceinline__ float inv_emin_bound(uint32_t w_head)
+{
+    float l2;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(sv::uniform_from_word(w_head)));
+    const float nl = (-l2 - 0x1p-20f) * 0x1.62e2p-1f;  // <= -ln W
+    return nl > 0.0f ? __frcp_rz(nl * 0x1p-6f) * (1.0f + 0x1p-12f) : kInf;
+}
+
+// Empty the warp's candidate queue (n entries): one token per lane, its exact weight, its race
+// clock and its key, merged into *sm.best. Entry: group g, slot s, raw logit, q entry.
 // Slot s = v & 63 of group g: its clock is E_g for the head's slot a, else fl(E_g + (-log U_s)),
 // U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4).
-template <typename T, bool kRes, int B>
-__device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm)
+template <typename T, bool kRes>
+__device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __syncwarp();
+    for (int e0 = 0; e0 < n; e0 += 32) {
+        const int e = e0 + lane;
+        unsigned long long p = 0;
+        if (e < n) {
+            const uint32_t gsl = sm.qgs[warp * kQueue + e];
+            const int g = static_cast<int>(gsl >> 6), slot = static_cast<int>(gsl & 63u);
+            const float t = sv::exp_f32(__fsub_rn(__fmul_rn(sm.ql[warp * kQueue + e], r.invT), r.m));
+            const float w = kRes ? __fmaf_rn(-r.S, sm.qq[warp * kQueue + e], t) : t;
+            if (!kRes || w > 0.0f) {
+                const uint32_t wh = sm.ew[g];
+                const float E = group_emin_word(wh);
+                float Ev = E;
+                if (slot != sm.ag[g]) {
+                    const sv::Philox4 sl = sv::philox4x32_10(
+                        static_cast<uint32_t>(g), r.j, r.ireq,
+                        sv::kClockHead + 1u + static_cast<uint32_t>(slot >> 2), r.k0, r.k1);
+                    const uint32_t ws = (slot & 2) ? ((slot & 1) ? sl.w : sl.z) : ((slot & 1) ? sl.y : sl.x);
+                    Ev = __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws)));
+                }
+                p = pack_key(__fdiv_rn(w, Ev), g * kGroup + slot);
+            }
+        }
+        p = warp_max_u64(p);
+        if (lane == 0 && p != 0) atomicMax(sm.best, p);
+    }
+    __syncwarp();
+}
+
+// Stage 1 of up to B groups by one warp (two adjacent tokens per lane and group; gs[k] < 0: no
+// group): every token whose key can still reach the best found so far joins the warp's queue,
+// by an upper bound from the hardware ex2 / lg2 / rcp with margins (key_v <= w_v / E_g; weights
+// at most exp(x - m), and the residual's fma is monotone in it). The queue is emptied through
+// flush_queue whenever it holds 32 tokens; qn is its length.
+template <typename T, bool kRes, int B>
+__device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm,
+                                            int &qn)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float l[B][2], qv[B][2];
 #pragma unroll
     for (int k = 0; k < B; ++k) {
@@ -802,49 +855,37 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
         }
     }
+    const unsigned long long cur = ld_best(sm.best);
+    const unsigned thr = static_cast<unsigned>(cur >> 32);
 #pragma unroll
     for (int k = 0; k < B; ++k) {
         const int g = gs[k];
         if (g < 0) continue;
-        const float E = group_emin_word(sm.ew[g]);
-        const int a = sm.ag[g];
-        const int v0 = g * kGroup + 2 * lane, v1 = v0 + 1;
-        const bool in0 = v0 < r.V, in1 = v1 < r.V;
-        const float t0 = sv::exp_f32(__fsub_rn(__fmul_rn(l[k][0], r.invT), r.m));
-        const float t1 = sv::exp_f32(__fsub_rn(__fmul_rn(l[k][1], r.invT), r.m));
-        float w0, w1;
-        bool c0, c1;
-        if constexpr (kRes) {
-            w0 = __fmaf_rn(-r.S, qv[k][0], t0);
-            w1 = __fmaf_rn(-r.S, qv[k][1], t1);
-            c0 = in0 && w0 > 0.0f;
-            c1 = in1 && w1 > 0.0f;
-            // the group's largest residual weight bounds its keys more tightly than its line max
-            const float wm = __uint_as_float(__reduce_max_sync(
-                0xFFFFFFFFu, __float_as_uint(fmaxf(c0 ? w0 : 0.0f, c1 ? w1 : 0.0f))));
-            if (!(wm > 0.0f)) continue;
-            const unsigned long long cur = ld_best(sm.best);
-            if (cur != 0 && key_enc(__fdiv_rn(wm, E)) < static_cast<unsigned>(cur >> 32)) continue;
-        } else {
-            w0 = t0;
-            w1 = t1;
-            c0 = in0 && v0 != r.excl;
-            c1 = in1 && v1 != r.excl;
+        const float inv = inv_emin_bound(sm.ew[g]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int v = g * kGroup + 2 * lane + h;
+            const float y = __fsub_rn(__fmul_rn(l[k][h], r.invT), r.m);
+            const float t_ub = sv::ex2_approx(y * kLog2e) * (1.0f + 0x1p-12f);
+            const float w_ub = kRes ? __fmaf_rn(-r.S, qv[k][h], t_ub) : t_ub;
+            bool take = v < r.V && (kRes ? w_ub > 0.0f : v != r.excl);
+            if (take && cur != 0) {
+                const float kb = w_ub * inv * (1.0f + 0x1p-12f);
+                take = !(kb == kb) || key_enc(kb) >= thr;  // NaN bounds are kept
+            }
+            const unsigned msk = __ballot_sync(0xFFFFFFFFu, take);
+            if (take) {
+                const int pos = warp * kQueue + qn + __popc(msk & ((1u << lane) - 1u));
+                sm.qgs[pos] = (static_cast<uint32_t>(g) << 6) | static_cast<uint32_t>(v & 63);
+                sm.ql[pos] = l[k][h];
+                sm.qq[pos] = qv[k][h];
+            }
+            qn += __popc(msk);
         }
-        const sv::Philox4 sl = sv::philox4x32_10(
-            static_cast<uint32_t>(g), r.j, r.ireq, sv::kClockHead + 1u + static_cast<uint32_t>(lane >> 1),
-            r.k0, r.k1);
-        const int s0 = 2 * lane, s1 = s0 + 1;  // slot words s & 3: 0 / 2 and 1 / 3
-        const uint32_t ws0 = (lane & 1) ? sl.z : sl.x;
-        const uint32_t ws1 = (lane & 1) ? sl.w : sl.y;
-        const float E0 = s0 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws0)));
-        const float E1 = s1 == a ? E : __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws1)));
-        const float k0 = __fdiv_rn(w0, E0), k1 = __fdiv_rn(w1, E1);
-        unsigned long long p = 0;
-        if (c0) p = pack_key(k0, v0);
-        if (c1) p = max(p, pack_key(k1, v1));
-        p = warp_max_u64(p);
-        if (lane == 0 && p != 0) atomicMax(sm.best, p);
+        if (qn >= 32) {
+            flush_queue<T, kRes>(r, sm, qn);
+            qn = 0;
+        }
     }
 }
 
@@ -881,7 +922,9 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
     if (lane == 0) atomicMax(sm.top, static_cast<unsigned>(wb >> 32));
     if (wb != 0) {
         const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
-        eval_groups<T, kRes, 1>(r, gs, sm);
+        int qn = 0;
+        eval_groups<T, kRes, 1>(r, gs, sm, qn);
+        flush_queue<T, kRes>(r, sm, qn);
         if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
     }
     __syncthreads();
@@ -936,6 +979,7 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
         sm.tmp[atomicAdd(&sm.bin_n[(ent >> 24) & 0xFFu], 1)] = ent;
     }
     __syncthreads();
+    int qn = 0;
     for (int e0 = warp * B; e0 < cnt; e0 += kWarps * B) {
         const unsigned long long cur = ld_best(sm.best);
         const unsigned thr = static_cast<unsigned>(cur >> 32);
@@ -955,7 +999,11 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
                 }
             }
         }
-        eval_groups<T, kRes, B>(r, gs, sm);
+        eval_groups<T, kRes, B>(r, gs, sm, qn);
+        if (qn > 0) {  // keys now: the best key prunes the next groups
+            flush_queue<T, kRes>(r, sm, qn);
+            qn = 0;
+        }
         if (done) break;
     }
     __syncthreads();
@@ -974,6 +1022,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     __shared__ int s_bin_n[kBins];
     __shared__ unsigned s_bin_max[kBins];
     __shared__ unsigned s_top;
+    __shared__ uint32_t s_qgs[kWarps * kQueue];
+    __shared__ float s_ql[kWarps * kQueue], s_qq[kWarps * kQueue];
     const int i = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = P.rq.n;
@@ -1073,6 +1123,9 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     sm.bin_n = s_bin_n;
     sm.bin_max = s_bin_max;
     sm.top = &s_top;
+    sm.qgs = s_qgs;
+    sm.ql = s_ql;
+    sm.qq = s_qq;
     sm.lm = reinterpret_cast<float *>(dyn);
     sm.pb = reinterpret_cast<float *>(dyn + lay.pb);
     sm.ew = reinterpret_cast<uint32_t *>(dyn + lay.ew);
@@ -1102,7 +1155,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
 constexpr int kProfRing = 512;
 constexpr int kKernels = 2;  // stats, verify
 // static shared memory of a verify CTA besides the dynamic part (reserve)
-constexpr int kVerifyStaticSmem = 1024;
+constexpr int kVerifyStaticSmem = 10240;
 
 struct ProfSlot {
     cudaEvent_t ev[kKernels + 1];
