@@ -67,6 +67,8 @@ def lib():
         for f in ("spec_verify_ref_exp_n", "spec_verify_ref_log_n"):
             getattr(L, f).argtypes = [vp, vp, ctypes.c_int64]
             getattr(L, f).restype = None
+        L.spec_verify_ref_draft_probs.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp]
+        L.spec_verify_ref_draft_probs.restype = None
         L.spec_verify_ref_race_clocks.argtypes = [u64, u32, u32, i32, vp]
         L.spec_verify_ref_race_clocks.restype = None
         _lib = L
@@ -136,6 +138,19 @@ def residual_row(logits_row: np.ndarray, bf16: bool, invT: float, q: np.ndarray)
     return t, rr, m.value, S.value
 
 
+def draft_probs(draft_logits: np.ndarray, bf16: bool, cu_num_draft, temperature, is_greedy):
+    """q = softmax(draft_logits / T_i) per draft row, as the draft-logits mode defines it."""
+    dl = np.ascontiguousarray(draft_logits)
+    cu = np.ascontiguousarray(cu_num_draft, dtype=np.int32)
+    n = cu.shape[0] - 1
+    V = dl.shape[-1]
+    q = np.zeros((int(cu[-1]), V), dtype=np.float32)
+    lib().spec_verify_ref_draft_probs(_p(dl), int(bf16), V, _p(cu),
+                                      _p(np.ascontiguousarray(temperature, dtype=np.float32)),
+                                      _p(np.ascontiguousarray(is_greedy, dtype=np.uint8)), n, _p(q))
+    return q
+
+
 def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_override=None,
         seed: int | None = None) -> dict:
     """Run the oracle on a ``workloads.Batch`` (or any object with the same fields).
@@ -154,6 +169,12 @@ def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_ov
     bf16 = batch.logits_dtype == "bf16"
     ids = np.ascontiguousarray(batch.draft_ids, dtype=np.int32)
     q = None if batch.draft_probs is None else np.ascontiguousarray(batch.draft_probs, dtype=np.float32)
+    if getattr(batch, "draft_logits", None) is not None:  # draft-logits mode: q from the logits
+        if cu.shape[0] - 1 > 0 and (cu[0] != 0 or np.any(np.diff(cu) < 0) or cu[-1] > len(batch.draft_ids)):
+            q = np.zeros((len(batch.draft_ids), int(batch.vocab_size)), np.float32)  # never read
+        else:
+            q = draft_probs(batch.draft_logits, batch.logits_dtype == "bf16", cu,
+                            batch.temperature, batch.is_greedy)
     T = np.ascontiguousarray(batch.temperature, dtype=np.float32)
     g = np.ascontiguousarray(batch.is_greedy, dtype=np.uint8)
     out = dict(

@@ -444,6 +444,46 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
     return REF_OK;
 }
 
+/*
+ * Draft distributions from draft logits ([spec-in-vllm] 7.1 probabilistic draft sampling keeps
+ * the draft logits; 7.4 block stats over target and draft logits): for draft row qrow of request
+ * i, q = softmax(draft_logits / T_i), with the request's own temperature (1 for a greedy request,
+ * whose q is never used):
+ *   x'_v = fl(dl_v * (1 / T_i)), m_d = max_v x'_v, S_d = (float) sum_v (double) exp(x'_v - m_d),
+ *   q_v = fl(exp(x'_v - m_d) / S_d),
+ * the same binary32 steps as the target's p = t / S. Rows of an inconsistent batch are skipped.
+ * q_out: [num_draft_tokens, V].
+ */
+void spec_verify_ref_draft_probs(const void *draft_logits, int logits_bf16, int vocab_size,
+                                 const int32_t *cu_num_draft, const float *temperature,
+                                 const uint8_t *is_greedy, int num_reqs, float *q_out)
+{
+    const int V = vocab_size;
+    for (int i = 0; i < num_reqs; ++i) {
+        const float T = temperature[i];
+        const int greedy = is_greedy[i] != 0 || !(T > 0.0f);
+        const float invT = greedy ? 1.0f : 1.0f / T;
+        for (int32_t r = cu_num_draft[i]; r < cu_num_draft[i + 1]; ++r) {
+            const size_t base = (size_t)r * V;
+            float m = -INFINITY;
+            for (int v = 0; v < V; ++v) {
+                float x = logit_at(draft_logits, logits_bf16, base + (size_t)v) * invT;
+                if (x > m) m = x;
+            }
+            double S = 0.0;
+            for (int v = 0; v < V; ++v) {
+                float x = logit_at(draft_logits, logits_bf16, base + (size_t)v) * invT;
+                S += (double)spec_verify_ref_exp(x - m);
+            }
+            const float S_f = (float)S;
+            for (int v = 0; v < V; ++v) {
+                float x = logit_at(draft_logits, logits_bf16, base + (size_t)v) * invT;
+                q_out[base + (size_t)v] = spec_verify_ref_exp(x - m) / S_f;
+            }
+        }
+    }
+}
+
 /* Residual weights of one row as the race uses them (for identity checks):
  * t_v = exp(x_v - m), rr_v = fma(-S, q_v, t_v); also returns m and S (binary32). */
 void spec_verify_ref_residual_row(const void *logits_row, int logits_bf16, int vocab_size,

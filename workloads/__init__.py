@@ -71,6 +71,8 @@ def _load():
         lib.gen_target_logits.argtypes = [u64, u64, i64, i64, d, d, i32, d, i32, vp]
         lib.gen_draft_probs.argtypes = [u64, u64, i64, i64, vp, vp, i32, d, i32, d, vp]
         lib.gen_sample_from_q.argtypes = [u64, u64, i64, i64, vp, vp]
+        lib.gen_draft_logits.argtypes = [u64, u64, i64, i64, vp, vp, i32, d, vp]
+        lib.gen_sample_from_logits.argtypes = [u64, u64, i64, i64, vp, i32, vp, vp]
         lib.gen_argmax_or_uniform.argtypes = [u64, u64, i64, i64, vp, vp, i32, d, vp]
         for f in ("gen_uniform", "gen_target_logits", "gen_draft_probs", "gen_sample_from_q",
                   "gen_argmax_or_uniform"):
@@ -115,6 +117,8 @@ class Batch:
     is_greedy: np.ndarray       # [num_reqs] uint8
     seed: int
     meta: dict = field(default_factory=dict)
+    # [N_d, V] draft logits in the logits' type (draft-logits mode: q = softmax(dl / T)), or None
+    draft_logits: np.ndarray | None = None
 
     @property
     def num_reqs(self) -> int:
@@ -148,6 +152,8 @@ class Batch:
         b = self.num_rows * self.vocab_size * self.elem_bytes
         if self.draft_probs is not None:
             b += self.random_draft_rows() * self.vocab_size * 4
+        if self.draft_logits is not None:
+            b += self.random_draft_rows() * self.vocab_size * self.elem_bytes
         return b
 
 
@@ -166,7 +172,9 @@ def make_batch(*, name: str, data_seed: int, verify_seed: int, K, vocab_size: in
 
     K: sequence of per-request draft lengths.
     q_mode: "noisy" (q = softmax(target + q_noise * N)), "indep" (q = softmax(q_indep_sigma * N)),
-            or "none" (draft ids only: argmax with probability p_argmax, else uniform).
+            "logits" (draft logits = target + q_noise * N in the logits' type, ids drawn from
+            softmax(draft logits / T) of the request), or "none" (draft ids only: argmax with
+            probability p_argmax, else uniform).
     temperature: float or per-request array. greedy: None or per-request bool array.
     """
     lib = _load()
@@ -193,6 +201,19 @@ def make_batch(*, name: str, data_seed: int, verify_seed: int, K, vocab_size: in
             lib.gen_draft_probs(data_seed, _S_Q, n_d, V, _ptr(src), _ptr(logits), int(bf16),
                                 q_noise, int(q_mode == "indep"), q_indep_sigma, _ptr(q))
             lib.gen_sample_from_q(data_seed, _S_IDS, n_d, V, _ptr(q), _ptr(ids))
+    elif q_mode == "logits":
+        temp_req = np.broadcast_to(np.asarray(temperature, dtype=np.float32), (num_reqs,))
+        g_req = np.zeros(num_reqs, np.uint8) if greedy is None else np.asarray(greedy, np.uint8)
+        dl = np.empty((n_d, V), dtype=np.uint16 if bf16 else np.float32)
+        if n_d:
+            lib.gen_draft_logits(data_seed, _S_Q, n_d, V, _ptr(src), _ptr(logits), int(bf16),
+                                 q_noise, _ptr(dl))
+            req_of_qrow = np.repeat(np.arange(num_reqs), Ks)
+            t = temp_req[req_of_qrow].astype(np.float64)
+            inv = np.where((g_req[req_of_qrow] != 0) | ~(t > 0), 1.0, 1.0 / np.where(t > 0, t, 1.0))
+            inv = np.ascontiguousarray(inv, dtype=np.float64)
+            lib.gen_sample_from_logits(data_seed, _S_IDS, n_d, V, _ptr(dl), int(bf16), _ptr(inv),
+                                       _ptr(ids))
     elif q_mode == "none":
         if n_d:
             lib.gen_argmax_or_uniform(data_seed, _S_IDS, n_d, V, _ptr(src), _ptr(logits),
@@ -202,7 +223,8 @@ def make_batch(*, name: str, data_seed: int, verify_seed: int, K, vocab_size: in
     temp = np.broadcast_to(np.asarray(temperature, dtype=np.float32), (num_reqs,)).copy()
     g = np.zeros(num_reqs, dtype=np.uint8) if greedy is None else np.asarray(greedy, dtype=np.uint8)
     return Batch(name=name, logits=logits, logits_dtype=logits_dtype, vocab_size=V, draft_ids=ids,
-                 draft_probs=q, cu_num_draft=cu, temperature=temp, is_greedy=g, seed=verify_seed)
+                 draft_probs=q, cu_num_draft=cu, temperature=temp, is_greedy=g, seed=verify_seed,
+                 draft_logits=dl if q_mode == "logits" else None)
 
 
 WORKLOADS = {

@@ -159,6 +159,61 @@ void gen_draft_probs(uint64_t seed, uint64_t stream, int64_t n_qrows, int64_t V,
 }
 
 /* Draft token ids drawn from q by inverse CDF in double (one uniform per row). */
+/* Draft logits: the target row plus N(0, noise^2) per entry, rounded to the logits' type. */
+void gen_draft_logits(uint64_t seed, uint64_t stream, int64_t n_qrows, int64_t V,
+                      const int32_t *src_row, const void *target, int bf16, double noise_sigma,
+                      void *out)
+{
+#pragma omp parallel for schedule(dynamic, 4)
+    for (int64_t k = 0; k < n_qrows; ++k) {
+        for (int64_t v = 0; v < V; ++v) {
+            const size_t idx = (size_t)k * (size_t)V + (size_t)v;
+            const double x = (double)load_logit(target, bf16, (size_t)src_row[k] * (size_t)V + (size_t)v) +
+                             noise_sigma * normal(seed, stream, (uint64_t)k, (uint64_t)v);
+            if (bf16)
+                ((uint16_t *)out)[idx] = f32_to_bf16((float)x);
+            else
+                ((float *)out)[idx] = (float)x;
+        }
+    }
+}
+
+/* Draft ids drawn by the draft model: from softmax(dl / T) of each draft row (inverse CDF in
+ * double with a uniform of (seed, stream, row)); inv_temp[k] = 1 / T of row k's request. */
+void gen_sample_from_logits(uint64_t seed, uint64_t stream, int64_t n_qrows, int64_t V,
+                            const void *dl, int bf16, const double *inv_temp, int32_t *ids)
+{
+#pragma omp parallel
+    {
+        double *z = (double *)malloc(sizeof(double) * (size_t)V);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t k = 0; k < n_qrows; ++k) {
+            double zmax = -INFINITY;
+            for (int64_t v = 0; v < V; ++v) {
+                z[v] = (double)load_logit(dl, bf16, (size_t)k * (size_t)V + (size_t)v) * inv_temp[k];
+                if (z[v] > zmax) zmax = z[v];
+            }
+            double total = 0.0;
+            for (int64_t v = 0; v < V; ++v) {
+                z[v] = exp(z[v] - zmax);
+                total += z[v];
+            }
+            const double target = u01(hash4(seed, stream, (uint64_t)k, 0)) * total;
+            double cum = 0.0;
+            int64_t pick = V - 1;
+            for (int64_t v = 0; v < V; ++v) {
+                cum += z[v];
+                if (cum > target) {
+                    pick = v;
+                    break;
+                }
+            }
+            ids[k] = (int32_t)pick;
+        }
+        free(z);
+    }
+}
+
 void gen_sample_from_q(uint64_t seed, uint64_t stream, int64_t n_qrows, int64_t V, const float *q,
                        int32_t *ids)
 {
