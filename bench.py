@@ -8,6 +8,9 @@ acceptance + race + emit) on one batch of the bandwidth workload: 256 requests x
 
 Prints one JSON line (rank 0). Metric: verified draft positions per second, whole job.
   python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload 0..4]
+                  [--draft-logits]
+--draft-logits measures the draft-logits input mode on the same recipe: the draft model's bf16
+logits replace the fp32 distributions, and q = softmax(draft logits / T) is computed in the call.
 Under torchrun (N > 1) every rank verifies its own batch (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 """
@@ -30,7 +33,7 @@ CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.a
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "stats_kernel_workload3.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCE = os.path.join(ROOT, "speculative_decoding_verification_rejection_gb300", "csrc",
                              "spec_verify.cu")
 
@@ -50,6 +53,8 @@ def parse_args():
                    help="CPU work of the oracle baseline sample (seconds)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--draft-logits", action="store_true",
+                   help="draft logits instead of draft probabilities (q computed in the call)")
     return p.parse_args()
 
 
@@ -70,7 +75,9 @@ def workload_config(b):
         "vocab": b.vocab_size,
         "logits_dtype": b.logits_dtype,
         "draft_probs": "fp32" if b.draft_probs is not None else "none",
-        "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)) / 1e6, 2),
+        "draft_logits": b.logits_dtype if b.draft_logits is not None else "none",
+        "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)
+                           + (b.draft_logits.nbytes if b.draft_logits is not None else 0)) / 1e6, 2),
     }
 
 
@@ -153,12 +160,12 @@ def measured_peak_gbs():
         return 6800.0, "fallback"
 
 
-def recorded_traffic():
+def recorded_traffic(summary: str):
     """DRAM bytes per launch of the stats kernel from the committed ncu summary, if the kernel
     source has not changed since it was taken (source hash recorded in the summary)."""
     import hashlib
     try:
-        with open(PROFILE_SUMMARY, encoding="utf-8") as f:
+        with open(os.path.join(PROFILE_DIR, summary), encoding="utf-8") as f:
             text = f.read()
         with open(KERNEL_SOURCE, "rb") as f:
             digest = hashlib.sha256(f.read()).hexdigest()[:16]
@@ -176,18 +183,18 @@ def recorded_traffic():
 # ---------------------------------------------------------------------------------------------
 # CPU oracle timing
 # ---------------------------------------------------------------------------------------------
-def time_oracle(workload_index: int, seconds: float):
+def time_oracle(workload_index: int, seconds: float, draft_logits: bool = False):
     """Time the oracle (as it stands, single-threaded) on the first requests of the workload,
     enough of them for about `seconds` of CPU work. Returns (positions/s, description)."""
     import oracle
     import workloads
 
-    one = workloads.workload(workload_index, num_reqs=2)
+    one = workloads.workload(workload_index, num_reqs=2, draft_logits=draft_logits)
     t = time.perf_counter()
     oracle.run(one)
     per_req = max((time.perf_counter() - t) / one.num_reqs, 1e-4)
     n = max(2, int(seconds / per_req))
-    b = workloads.workload(workload_index, num_reqs=n)
+    b = workloads.workload(workload_index, num_reqs=n, draft_logits=draft_logits)
     t = time.perf_counter()
     oracle.run(b)
     dt = time.perf_counter() - t
@@ -204,13 +211,13 @@ def run_reference(args, world, rank):
     import oracle
     import workloads
 
-    full = workloads.workload(args.workload, num_reqs=2)
+    full = workloads.workload(args.workload, num_reqs=2, draft_logits=args.draft_logits)
     t = time.perf_counter()
     oracle.run(full)
     per_req = max((time.perf_counter() - t) / 2, 1e-4)
     budget = 150.0
     n = int(max(1, min(256, budget / max(1, args.steps + args.warmup) / per_req)))
-    sample = workloads.workload(args.workload, num_reqs=n)
+    sample = workloads.workload(args.workload, num_reqs=n, draft_logits=args.draft_logits)
     for _ in range(args.warmup):
         oracle.run(sample)
     t0 = time.perf_counter()
@@ -218,7 +225,7 @@ def run_reference(args, world, rank):
         oracle.run(sample)
     dt = time.perf_counter() - t0
     value = sample.num_draft_tokens * args.steps / dt
-    cfg = workload_config(workloads.workload(args.workload))
+    cfg = workload_config(workloads.workload(args.workload, draft_logits=args.draft_logits))
     cfg["reference_sample_requests_per_step"] = n
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -251,17 +258,22 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     sv.lib()
 
-    b = workloads.workload(args.workload, num_reqs=args.num_reqs)
+    b = workloads.workload(args.workload, num_reqs=args.num_reqs, draft_logits=args.draft_logits)
     dev = torch.device("cuda", local)
     logits_np = b.logits.view(np.int16) if b.logits.dtype == np.uint16 else b.logits
     d_logits = torch.from_numpy(logits_np).to(dev)
+    dl_np = None
+    if b.draft_logits is not None:
+        dl_np = b.draft_logits.view(np.int16) if b.draft_logits.dtype == np.uint16 else b.draft_logits
+    d_dl = torch.from_numpy(dl_np).to(dev) if dl_np is not None else None
     d_q = torch.from_numpy(b.draft_probs).to(dev) if b.draft_probs is not None else None
     d_ids = torch.from_numpy(b.draft_ids).to(dev)
     d_cu = torch.from_numpy(b.cu_num_draft).to(dev)
     d_T = torch.from_numpy(b.temperature).to(dev)
     d_g = torch.from_numpy(b.is_greedy).to(dev)
     n, nd, kmax, V = b.num_reqs, b.num_draft_tokens, b.max_spec_len, b.vocab_size
-    ctx = sv.SpecVerify(n, kmax, V, b.logits_dtype, b.draft_probs is not None, device=local)
+    ctx = sv.SpecVerify(n, kmax, V, b.logits_dtype, b.draft_probs is not None, device=local,
+                        draft_logits=d_dl is not None)
     outs = (torch.empty((n, kmax + 1), dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev))
@@ -269,7 +281,7 @@ def run_ours(args, world, rank, local):
 
     def step():
         ctx.run(d_logits, d_ids, d_q, d_cu, d_T, d_g, b.seed, req_index_base=base,
-                max_spec_len=kmax, out=outs)
+                max_spec_len=kmax, out=outs, draft_logits=d_dl)
 
     for _ in range(args.warmup):
         step()
@@ -315,7 +327,9 @@ def run_ours(args, world, rank, local):
 
     # end to end through the host-buffer entry point: H2D of the inputs, verify, D2H of results
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and d_dl is not None:
+        e2e = e2e_draft_logits(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist)
+    elif not args.no_e2e:
         ctx.reserve_host_io()
         h_logits = torch.from_numpy(logits_np).pin_memory()
         h_q = torch.from_numpy(b.draft_probs).pin_memory() if b.draft_probs is not None else None
@@ -362,13 +376,17 @@ def run_ours(args, world, rank, local):
         return
 
     peak, peak_kind = measured_peak_gbs()
-    # every logit read once (R x V x element size) and one line maximum written per 64 logits
+    # every logit read once (R x V x element size) and one line maximum written per 64 logits;
+    # in the draft-logits mode every draft logit is read once as well
     stats_bytes = b.num_rows * V * b.elem_bytes + (b.num_rows * V // 64) * b.elem_bytes
+    if d_dl is not None:
+        stats_bytes += nd * V * b.elem_bytes
     achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
-    traffic, traffic_src = recorded_traffic()
+    traffic, traffic_src = recorded_traffic(
+        "stats_kernel_workload3_draft_logits.md" if d_dl is not None else "stats_kernel_workload3.md")
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        v, desc, _ = time_oracle(args.workload, args.cpu_seconds)
+        v, desc, _ = time_oracle(args.workload, args.cpu_seconds, args.draft_logits)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
     clocks = sampler.summary(t0, t1) if sampler else None
     cfg = workload_config(b)
@@ -381,7 +399,8 @@ def run_ours(args, world, rank, local):
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "e2e": e2e, "gpu_launches": sv.spec_verify_launches_per_run() * args.steps,
         "roofline": {"bound": "hbm", "kernel": "sv_stats_kernel (row statistics: reads every logit once, "
-                                               "writes one maximum per 64-element line)",
+                                               "writes one maximum per 64-element line"
+                                               + ("; also reads every draft logit once)" if d_dl is not None else ")"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "traffic_source": traffic_src,
@@ -399,6 +418,48 @@ def run_ours(args, world, rank, local):
     ctx.close()
     if dist:
         dist.destroy_process_group()
+
+
+def e2e_draft_logits(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist):
+    """End to end in the draft-logits mode through SpecVerify.run: every step copies the target
+    and draft logits and the small per-request arrays from page-locked host memory into the
+    device buffers, verifies, and reads the results back (host wall clock, stream synchronised)."""
+    import numpy as np
+    import torch
+
+    n, nd = b.num_reqs, b.num_draft_tokens
+    host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+            for a in (logits_np, dl_np, b.draft_ids, b.cu_num_draft, b.temperature, b.is_greedy)]
+    devb = [torch.empty_like(h, device=dev) for h in host]
+    h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+
+    def e2e_step():
+        for h, d in zip(host, devb):
+            d.copy_(h, non_blocking=True)
+        ctx.run(devb[0], devb[2], None, devb[3], devb[4], devb[5], b.seed, req_index_base=base,
+                max_spec_len=kmax, out=outs, draft_logits=devb[1])
+        for h, o in zip(h_out, outs):
+            h.copy_(o, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    ke = max(1, args.e2e_steps)
+    if dist:
+        dist.barrier()
+    te = time.perf_counter()
+    for _ in range(ke):
+        e2e_step()
+    te = time.perf_counter() - te
+    if dist:
+        t = torch.tensor([te], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        te = float(t.item())
+    h2d = sum(h.numel() * h.element_size() for h in host)
+    d2h = sum(h.numel() * h.element_size() for h in h_out)
+    return {"value": world * nd * ke / te, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "steps": ke, "ms_per_step": te / ke * 1e3,
+            "timing": "host wall clock around H2D copies + SpecVerify.run + D2H copies + stream sync"}
 
 
 def main():

@@ -82,6 +82,10 @@ extern "C" {
 #define SV_F32 0  /* IEEE binary32 */
 #define SV_BF16 1 /* bfloat16 (upper half of a binary32) */
 
+/* draft inputs a context accepts (bits of spec_verify_init's draft_input) */
+#define SV_DRAFT_PROBS 1  /* draft_probs may be given to spec_verify_run */
+#define SV_DRAFT_LOGITS 2 /* spec_verify_run_draft_logits may be called */
+
 /* bits of the device error word */
 #define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
 
@@ -90,8 +94,11 @@ typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
 /*
  * Create a context on `device` (a CUDA ordinal) for batches of at most max_num_reqs requests,
  * at most max_spec_len draft tokens each, vocabulary size vocab_size and logits of type
- * logits_dtype (SV_F32 / SV_BF16). has_draft_probs = 0 promises that draft_probs is always
- * NULL (only the host-buffer entry point sizes anything by it).
+ * logits_dtype (SV_F32 / SV_BF16). draft_input is 0 or an OR of SV_DRAFT_PROBS and
+ * SV_DRAFT_LOGITS: without SV_DRAFT_PROBS draft_probs must always be NULL (only the
+ * host-buffer entry point sizes anything by it); SV_DRAFT_LOGITS reserves the partial
+ * statistics of the draft rows (about 16 * 8 * (vocab_size / 2048 + 2) bytes per draft row of
+ * capacity) that spec_verify_run_draft_logits needs. Any other value returns SV_EINVAL.
  * The context owns its device scratch (the per-segment partial statistics and an error word),
  * allocated here once; spec_verify_run allocates nothing. Free with spec_verify_free.
  * Returns SV_ECAPACITY when the race's per-group bounds of one row (about 12 bytes per 64
@@ -99,7 +106,7 @@ typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
  * Returns SV_OK and *out, or an error with *out = NULL.
  */
 int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, int vocab_size,
-                     int logits_dtype, int has_draft_probs, int device);
+                     int logits_dtype, int draft_input, int device);
 
 /*
  * Verify one batch, asynchronously on `cuda_stream` (a cudaStream_t; NULL = legacy default
@@ -131,8 +138,35 @@ int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *dra
                     int32_t *opt_row_argmax, void *cuda_stream);
 
 /*
+ * Probabilistic drafting with the draft model's logits instead of its probabilities
+ * ([spec-in-vllm] 7.1: the probabilistic draft method keeps the full draft logits, one row of
+ * V per draft step; 7.4: the statistics kernel reduces the draft logits as well as the
+ * target's). q is computed inside the call and never written out:
+ *   q_v = exp(y_v - m_d) / S_d,  y_v = draft_logit_v * (1 / T),  m_d = max_v y_v,
+ *   S_d = sum_v exp(y_v - m_d),
+ * with the request's own temperature T (the draft samples with the same settings), exp the
+ * library's binary32 exp and the quotient correctly rounded in binary32; S_d is summed in an
+ * unspecified order (relative error far below 1e-5). Acceptance and the residual race then use
+ * this q exactly as spec_verify_run uses draft_probs. Greedy requests ignore q.
+ *   draft_logits  [num_draft_tokens, vocab_size] of the context's dtype, 16-byte aligned, row
+ *                 cu_num_draft[i] + j for draft j of request i (the layout of draft_probs).
+ * Every other argument, the outputs and the error behaviour are those of spec_verify_run.
+ * Returns SV_EINVAL if the context was created without SV_DRAFT_LOGITS. Both logits arrays
+ * are reduced by one statistics launch; the call stays allocation-free and graph-capturable.
+ */
+int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
+                                 const int32_t *draft_ids, const void *draft_logits,
+                                 const int32_t *cu_num_draft, const float *temperature,
+                                 const uint8_t *is_greedy, uint64_t seed,
+                                 uint32_t req_index_base, int num_reqs, int num_draft_tokens,
+                                 int max_spec_len_this_batch, int32_t *sampled,
+                                 int32_t *num_sampled, int32_t *num_rejected, float *opt_row_max,
+                                 float *opt_row_sumexp, int32_t *opt_row_argmax,
+                                 void *cuda_stream);
+
+/*
  * Allocate device staging buffers sized for the context's capacity (logits, draft_probs if
- * has_draft_probs, and the small per-request arrays) so that spec_verify_run_host can be used.
+ * SV_DRAFT_PROBS, and the small per-request arrays) so that spec_verify_run_host can be used.
  */
 int spec_verify_reserve_host_io(spec_verify_ctx *ctx);
 

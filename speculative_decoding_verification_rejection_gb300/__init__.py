@@ -28,6 +28,7 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 
 SV_OK, SV_EINVAL, SV_ECAPACITY, SV_EDTYPE, SV_ECUDA, SV_EDEVICE = 0, -1, -2, -3, -4, -5
 SV_F32, SV_BF16 = 0, 1
+SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 1, 2
 SV_ERR_BATCH = 1
 KERNELS = ("stats", "verify")
 
@@ -99,6 +100,7 @@ def lib():
     L.spec_verify_init.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32]
     L.spec_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp]
+    L.spec_verify_run_draft_logits.argtypes = list(L.spec_verify_run.argtypes)
     L.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp,
                                        vp, vp]
     L.spec_verify_run_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32,
@@ -113,7 +115,8 @@ def lib():
     L.spec_verify_free.restype = None
     L.spec_verify_status_string.argtypes = [i32]
     L.spec_verify_status_string.restype = ctypes.c_char_p
-    for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_host", "spec_verify_run_noalloc",
+    for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_draft_logits",
+              "spec_verify_run_host", "spec_verify_run_noalloc",
               "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
               "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
         getattr(L, f).restype = i32
@@ -160,10 +163,10 @@ def _stream_handle(stream):
 # ---- thin wrappers with the C names --------------------------------------------------------
 
 def spec_verify_init(max_num_reqs: int, max_spec_len: int, vocab_size: int, logits_dtype: int,
-                     has_draft_probs: int, device: int) -> int:
+                     draft_input: int, device: int) -> int:
     ctx = ctypes.c_void_p()
     _check(lib().spec_verify_init(ctypes.byref(ctx), max_num_reqs, max_spec_len, vocab_size,
-                                  logits_dtype, has_draft_probs, device), "spec_verify_init")
+                                  logits_dtype, draft_input, device), "spec_verify_init")
     return ctx.value
 
 
@@ -178,6 +181,19 @@ def spec_verify_run(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperatu
                                  _ptr(num_rejected), _ptr(opt_row_max), _ptr(opt_row_sumexp),
                                  _ptr(opt_row_argmax), _stream_handle(cuda_stream)),
            "spec_verify_run")
+
+
+def spec_verify_run_draft_logits(ctx, logits, draft_ids, draft_logits, cu_num_draft, temperature,
+                                 is_greedy, seed, req_index_base, num_reqs, num_draft_tokens,
+                                 max_spec_len_this_batch, sampled, num_sampled, num_rejected,
+                                 opt_row_max=None, opt_row_sumexp=None, opt_row_argmax=None,
+                                 cuda_stream=None) -> None:
+    _check(lib().spec_verify_run_draft_logits(
+        ctx, _ptr(logits), _ptr(draft_ids), _ptr(draft_logits), _ptr(cu_num_draft),
+        _ptr(temperature), _ptr(is_greedy), seed, req_index_base, num_reqs, num_draft_tokens,
+        max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled), _ptr(num_rejected),
+        _ptr(opt_row_max), _ptr(opt_row_sumexp), _ptr(opt_row_argmax),
+        _stream_handle(cuda_stream)), "spec_verify_run_draft_logits")
 
 
 def spec_verify_run_host(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
@@ -265,24 +281,34 @@ class SpecVerify:
     """Owns one context. Tensors passed to :meth:`run` must live on the context's device."""
 
     def __init__(self, max_num_reqs: int, max_spec_len: int, vocab_size: int, logits_dtype="bf16",
-                 has_draft_probs: bool = True, device: int = 0):
+                 has_draft_probs: bool = True, device: int = 0, *, draft_logits: bool = False):
         self.max_num_reqs, self.max_spec_len, self.vocab_size = max_num_reqs, max_spec_len, vocab_size
         self.dtype_code = _dtype_code(logits_dtype)
         self.device = device
+        draft_input = (SV_DRAFT_PROBS if has_draft_probs else 0) | (SV_DRAFT_LOGITS if draft_logits else 0)
         self.ctx = spec_verify_init(max_num_reqs, max_spec_len, vocab_size, self.dtype_code,
-                                    int(has_draft_probs), device)
+                                    draft_input, device)
 
     def run(self, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy, seed: int,
             *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
-            row_stats: bool = False, stream=None):
+            row_stats: bool = False, stream=None, draft_logits=None):
         """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
-        and, with row_stats=True, also (row_max, row_sumexp, row_argmax)."""
+        and, with row_stats=True, also (row_max, row_sumexp, row_argmax).
+
+        draft_logits ([num_draft_tokens, vocab_size], the logits' dtype) replaces draft_probs:
+        q is then computed inside the call (context created with draft_logits=True)."""
         import torch
         num_reqs = cu_num_draft.numel() - 1
         nd = draft_ids.numel()
         kmax = self.max_spec_len if max_spec_len is None else max_spec_len
         if logits.dim() != 2 or logits.shape[0] != nd + num_reqs or logits.shape[1] != self.vocab_size:
             raise ValueError("logits must be [num_draft_tokens + num_reqs, vocab_size]")
+        if draft_logits is not None:
+            if draft_probs is not None:
+                raise ValueError("give draft_probs or draft_logits, not both")
+            if (draft_logits.dim() != 2 or draft_logits.shape[0] != nd
+                    or draft_logits.shape[1] != self.vocab_size or draft_logits.dtype != logits.dtype):
+                raise ValueError("draft_logits must be [num_draft_tokens, vocab_size] of the logits' dtype")
         dev = logits.device
         if out is None:
             out = (torch.empty((num_reqs, kmax + 1), dtype=torch.int32, device=dev),
@@ -294,9 +320,14 @@ class SpecVerify:
             stats = (torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.int32, device=dev))
-        spec_verify_run(self.ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
-                        is_greedy, seed, req_index_base, num_reqs, nd, kmax, *out, *stats,
-                        cuda_stream=stream)
+        if draft_logits is not None:
+            spec_verify_run_draft_logits(self.ctx, logits, draft_ids, draft_logits, cu_num_draft,
+                                         temperature, is_greedy, seed, req_index_base, num_reqs,
+                                         nd, kmax, *out, *stats, cuda_stream=stream)
+        else:
+            spec_verify_run(self.ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
+                            is_greedy, seed, req_index_base, num_reqs, nd, kmax, *out, *stats,
+                            cuda_stream=stream)
         return (*out, *stats) if row_stats else out
 
     def reserve_host_io(self) -> None:

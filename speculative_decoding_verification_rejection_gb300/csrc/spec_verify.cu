@@ -130,15 +130,17 @@ __device__ __forceinline__ void emit_row(int i, int jstar, int K, int q0, int to
 // requests
 // ---------------------------------------------------------------------------------------
 // Request of logit row r: the largest i in [0, n) with cu[i] + i <= r (request i owns rows
-// cu[i] + i .. cu[i + 1] + i). A 32-way search by one full warp; the result stays in [0, n)
-// whatever cu holds.
-__device__ __forceinline__ int row_request(const int32_t *__restrict__ cu, int n, int r, int lane)
+// cu[i] + i .. cu[i + 1] + i); with draft_rows, of draft row r: the largest i with cu[i] <= r
+// (request i owns draft rows cu[i] .. cu[i + 1] - 1). A 32-way search by one full warp; the result
+// stays in [0, n) whatever cu holds.
+__device__ __forceinline__ int row_request(const int32_t *__restrict__ cu, int n, int r, int lane,
+                                           bool draft_rows = false)
 {
     int lo = 0, hi = n;
     while (hi - lo > 1) {
         const int step = (hi - lo + 31) >> 5;
         const int p = lo + lane * step;
-        const bool ok = lane == 0 || (p < hi && __ldg(cu + p) + p <= r);
+        const bool ok = lane == 0 || (p < hi && __ldg(cu + p) + (draft_rows ? 0 : p) <= r);
         const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
         lo += (31 - __clz(b)) * step;
         hi = min(hi, lo + step);
@@ -441,7 +443,8 @@ template <typename T>
 __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int V, int row, int b,
                                               int e, int seg, int maxseg, int base_off,
                                               const RequestTable &rq, StatPart *__restrict__ part,
-                                              T *__restrict__ s_lines, long long line_base)
+                                              T *__restrict__ s_lines, long long line_base,
+                                              bool draft_rows)
 {
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
@@ -465,8 +468,8 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     if (ub + lane + kThreads < npair)
         ldg_pair(pbase + static_cast<size_t>(ub + lane + kThreads) * kPairBytes, w1);
     bool greedy;
-    const float c = request_invT(rq.temperature, rq.is_greedy, row_request(rq.cu, rq.n, row, lane),
-                                 greedy) * kLog2e;
+    const float c = request_invT(rq.temperature, rq.is_greedy,
+                                 row_request(rq.cu, rq.n, row, lane, draft_rows), greedy) * kLog2e;
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
@@ -507,46 +510,62 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
         part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
 }
 
-// Row statistics over the flattened [rows x V] logits, split evenly: CTA k streams elements
-// [k * chunk - base_off, (k + 1) * chunk - base_off) (chunk a multiple of 512, so that CTAs meet
-// on line boundaries and own whole 16-byte spans of the line array), which covers one or more row
-// segments, and writes one partial per warp and segment. With `lines`, the CTA gathers its line
-// maxima in shared memory (chunk / 64 of them) and writes them out at the end in one coalesced
-// sweep, lines [k * chunk / 64, (k + 1) * chunk / 64); entries of lines that a row covers only in
-// part are left undefined (the verify kernel reads those lines from the logits). Nothing waits on
-// another CTA.
+// One [rows x V] array the statistics kernel streams: the target logits, or the draft logits of
+// the draft-logits mode (rows = draft tokens, each belonging to the request that drafted it).
+template <typename T>
+struct StatsArray {
+    const T *logits;
+    long long total;     // rows * V
+    Divisor chunk, dv;   // elements per CTA; V
+    int base_off;        // (address mod 64 elements) / element size
+    int grid;            // CTAs of this array
+    int draft_rows;      // row r is draft row r (request: largest i with cu[i] <= r)
+    StatPart *part;      // [rows x maxseg x kWarps] partials
+    T *lines;            // line maxima (target logits only), or nullptr
+};
+
+// Row statistics over a flattened [rows x V] array, split evenly: CTA k of an array streams
+// elements [k * chunk - base_off, (k + 1) * chunk - base_off) (chunk a multiple of 512, so that
+// CTAs meet on line boundaries and own whole 16-byte spans of the line array), which covers one
+// or more row segments, and writes one partial per warp and segment. With `lines`, the CTA
+// gathers its line maxima in shared memory (chunk / 64 of them) and writes them out at the end in
+// one coalesced sweep, lines [k * chunk / 64, (k + 1) * chunk / 64); entries of lines that a row
+// covers only in part are left undefined (the verify kernel reads those lines from the logits).
+// The first A.grid CTAs take the target logits, the rest the draft logits (if any). Nothing waits
+// on another CTA.
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 3)
-sv_stats_kernel(const T *__restrict__ logits, int V, long long total, Divisor chunk, Divisor dv,
-                int maxseg, int base_off, RequestTable rq, StatPart *__restrict__ part,
-                T *__restrict__ lines)
+sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTable rq)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
-    const long long start = max(0LL, static_cast<long long>(blockIdx.x) * chunk.d - base_off);
-    const long long stop = min(total, static_cast<long long>(blockIdx.x + 1) * chunk.d - base_off);
+    const bool second = static_cast<int>(blockIdx.x) >= A.grid;
+    const StatsArray<T> X = second ? D : A;
+    const int cta = second ? static_cast<int>(blockIdx.x) - A.grid : static_cast<int>(blockIdx.x);
+    const long long start = max(0LL, static_cast<long long>(cta) * X.chunk.d - X.base_off);
+    const long long stop = min(X.total, static_cast<long long>(cta + 1) * X.chunk.d - X.base_off);
     if (start >= stop) return;
-    T *s_lines = lines ? reinterpret_cast<T *>(s_raw) : nullptr;
-    const long long line_base = static_cast<long long>(blockIdx.x) * (chunk.d >> 6);
-    const int r_first = static_cast<int>(div_floor(start, dv));
-    const int r_last = static_cast<int>(div_floor(stop - 1, dv));
+    T *s_lines = X.lines ? reinterpret_cast<T *>(s_raw) : nullptr;
+    const long long line_base = static_cast<long long>(cta) * (X.chunk.d >> 6);
+    const int r_first = static_cast<int>(div_floor(start, X.dv));
+    const int r_last = static_cast<int>(div_floor(stop - 1, X.dv));
     for (int row = r_first; row <= r_last; ++row) {
         const long long rbase = static_cast<long long>(row) * V;
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
-        const int fk = static_cast<int>(div_floor(base_off + rbase, chunk));
-        stats_segment<T>(logits, V, row, b, e, static_cast<int>(blockIdx.x) - fk, maxseg, base_off,
-                         rq, part, s_lines, line_base);
+        const int fk = static_cast<int>(div_floor(X.base_off + rbase, X.chunk));
+        stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part, s_lines,
+                         line_base, X.draft_rows != 0);
     }
-    if (lines) {
+    if (X.lines) {
         __syncthreads();
-        const long long lines_end = (base_off + total + kGroup - 1) >> 6;
-        const int nl = static_cast<int>(min(chunk.d >> 6, lines_end - line_base));
+        const long long lines_end = (X.base_off + X.total + kGroup - 1) >> 6;
+        const int nl = static_cast<int>(min(X.chunk.d >> 6, lines_end - line_base));
         const int nv = nl * static_cast<int>(sizeof(T)) / 16;  // whole 16-byte vectors
-        uint4 *dst = reinterpret_cast<uint4 *>(lines + line_base);
+        uint4 *dst = reinterpret_cast<uint4 *>(X.lines + line_base);
         const uint4 *src = reinterpret_cast<const uint4 *>(s_raw);
         for (int k = threadIdx.x; k < nv; k += kThreads) dst[k] = src[k];
         for (int k = nv * 16 / static_cast<int>(sizeof(T)) + threadIdx.x; k < nl; k += kThreads)
-            lines[line_base + k] = s_lines[k];
+            X.lines[line_base + k] = s_lines[k];
     }
 }
 
@@ -557,6 +576,10 @@ struct VerifyParams {
     RequestTable rq;
     const int32_t *draft_ids;
     const float *q;
+    const void *dl;          // draft logits (logits' type), or nullptr
+    const StatPart *dpart;   // partials of the draft rows (draft-logits mode)
+    Divisor dchunk;          // statistics chunk of the draft logits
+    int dbase_off;           // their (address mod 64 elements) / element size
     const StatPart *part;
     uint64_t seed;
     uint32_t req_base;
@@ -574,8 +597,8 @@ template <typename T>
 __device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, int j, int qrow,
                                              float invT, float m, float S, int amax,
                                              const int32_t *__restrict__ draft_ids,
-                                             const float *__restrict__ q, uint64_t seed,
-                                             uint32_t ireq)
+                                             const float *__restrict__ q, const T *__restrict__ dl,
+                                             float md, float Sd, uint64_t seed, uint32_t ireq)
 {
     const int d = __ldg(draft_ids + qrow);
     if (greedy) return d == amax;
@@ -583,7 +606,13 @@ __device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, in
     const float x_d = __fmul_rn(Elem<T>::at(rp, d), invT);
     const float t_d = sv::exp_f32(__fsub_rn(x_d, m));
     const float p_d = __fdiv_rn(t_d, S);
-    const float q_d = q ? __ldg(q + static_cast<size_t>(qrow) * V + d) : 1.0f;
+    float q_d = 1.0f;
+    if (q) {
+        q_d = __ldg(q + static_cast<size_t>(qrow) * V + d);
+    } else if (dl) {  // q = softmax(draft logits / T), the target's steps on the draft row
+        const float xd = __fmul_rn(Elem<T>::at(dl + static_cast<size_t>(qrow) * V, d), invT);
+        q_d = __fdiv_rn(sv::exp_f32(__fsub_rn(xd, md)), Sd);
+    }
     const sv::Philox4 r = sv::philox4x32_10(0u, static_cast<uint32_t>(j), ireq, sv::kTagAccept,
                                             static_cast<uint32_t>(seed),
                                             static_cast<uint32_t>(seed >> 32));
@@ -669,6 +698,8 @@ template <typename T>
 struct RaceRow {
     const T *rp;        // logits row
     const float *qrow;  // draft distribution row (residual race) or nullptr
+    const T *dlrow;     // draft logits row (residual race in draft-logits mode) or nullptr
+    float md, Sd;       // its max and sum of exponentials
     int V, G;           // vocabulary, groups
     int excl;           // token left out (rejected draft without q), or -1
     float m, S, invT;
@@ -698,7 +729,7 @@ struct SearchSmem {
 
 // Dynamic shared memory layout of a verify CTA (bytes): the candidate buffer (a power of two
 // >= G entries of 8 bytes, also holding the G + 2 line maxima), the binned copy of it, m / S /
-// argmax of the request's rows (kmax + 1 each), pb, ew, ag.
+// argmax of the request's rows and m / S of its draft rows (kmax + 1 each), pb, ew, ag.
 struct VerifyLayout {
     size_t tmp, rows, pb, ew, ag, total;
 };
@@ -716,7 +747,7 @@ __host__ __device__ inline VerifyLayout verify_layout(int V, int kmax)
     const size_t buf = 8 * sp > 4 * (G + 2) ? 8 * sp : 4 * (G + 2);
     l.tmp = (buf + 15) / 16 * 16;
     l.rows = l.tmp + 8 * sp;
-    l.pb = l.rows + 12 * (static_cast<size_t>(kmax) + 1);
+    l.pb = l.rows + 20 * (static_cast<size_t>(kmax) + 1);
     l.ew = l.pb + 4 * G;
     l.ag = l.ew + 4 * G;
     l.total = l.ag + G;
@@ -800,7 +831,7 @@ __device__ __forceinline__ float inv_emin_bound(uint32_t w_head)
 // clock and its key, merged into *sm.best. Entry: group g, slot s, raw logit, q entry.
 // Slot s = v & 63 of group g: its clock is E_g for the head's slot a, else fl(E_g + (-log U_s)),
 // U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4).
-template <typename T, bool kRes>
+template <typename T, bool kRes, bool kDL>
 __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -812,7 +843,9 @@ __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
             const uint32_t gsl = sm.qgs[warp * kQueue + e];
             const int g = static_cast<int>(gsl >> 6), slot = static_cast<int>(gsl & 63u);
             const float t = sv::exp_f32(__fsub_rn(__fmul_rn(sm.ql[warp * kQueue + e], r.invT), r.m));
-            const float w = kRes ? __fmaf_rn(-r.S, sm.qq[warp * kQueue + e], t) : t;
+            float qv = sm.qq[warp * kQueue + e];  // q, or the raw draft logit (draft-logits mode)
+            if constexpr (kDL) qv = __fdiv_rn(sv::exp_f32(__fsub_rn(__fmul_rn(qv, r.invT), r.md)), r.Sd);
+            const float w = kRes ? __fmaf_rn(-r.S, qv, t) : t;
             if (!kRes || w > 0.0f) {
                 const uint32_t wh = sm.ew[g];
                 const float E = group_emin_word(wh);
@@ -837,8 +870,9 @@ __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 // group): every token whose key can still reach the best found so far joins the warp's queue,
 // by an upper bound from the hardware ex2 / lg2 / rcp with margins (key_v <= w_v / E_g; weights
 // at most exp(x - m), and the residual's fma is monotone in it). The queue is emptied through
-// flush_queue whenever it holds 32 tokens; qn is its length.
-template <typename T, bool kRes, int B>
+// flush_queue whenever it holds 32 tokens; qn is its length. In draft-logits mode q_v is bounded
+// from below the same way (hardware ex2 and a reciprocal of S_d, with margins).
+template <typename T, bool kRes, bool kDL, int B>
 __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm,
                                             int &qn)
 {
@@ -852,9 +886,11 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             const bool in = gs[k] >= 0 && v < r.V;
             l[k][h] = in ? Elem<T>::at(r.rp, v) : -kInf;
             qv[k][h] = 0.0f;
-            if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
+            if constexpr (kRes && kDL) qv[k][h] = in ? Elem<T>::at(r.dlrow, v) : 0.0f;
+            else if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
         }
     }
+    const float inv_sd = kDL ? __frcp_rz(r.Sd) * (1.0f - 0x1p-12f) : 0.0f;  // <= 1 / S_d
     const unsigned long long cur = ld_best(sm.best);
     const unsigned thr = static_cast<unsigned>(cur >> 32);
 #pragma unroll
@@ -867,7 +903,13 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             const int v = g * kGroup + 2 * lane + h;
             const float y = __fsub_rn(__fmul_rn(l[k][h], r.invT), r.m);
             const float t_ub = sv::ex2_approx(y * kLog2e) * (1.0f + 0x1p-12f);
-            const float w_ub = kRes ? __fmaf_rn(-r.S, qv[k][h], t_ub) : t_ub;
+            float q_lb = qv[k][h];
+            if constexpr (kDL) {
+                const float yd = __fsub_rn(__fmul_rn(qv[k][h], r.invT), r.md);
+                // exp_f32 is 0 below -87: the bound must be too
+                q_lb = yd >= -87.0f ? sv::ex2_approx(yd * kLog2e) * (1.0f - 0x1p-12f) * inv_sd : 0.0f;
+            }
+            const float w_ub = kRes ? __fmaf_rn(-r.S, q_lb, t_ub) : t_ub;
             bool take = v < r.V && (kRes ? w_ub > 0.0f : v != r.excl);
             if (take && cur != 0) {
                 const float kb = w_ub * inv * (1.0f + 0x1p-12f);
@@ -883,7 +925,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             qn += __popc(msk);
         }
         if (qn >= 32) {
-            flush_queue<T, kRes>(r, sm, qn);
+            flush_queue<T, kRes, kDL>(r, sm, qn);
             qn = 0;
         }
     }
@@ -900,7 +942,7 @@ __device__ __forceinline__ int bound_bin(unsigned kb, float top, float inv_w)
 
 // Best-first race over one row by the whole CTA. Returns the packed winner (key, ~v), 0 when no
 // token is a candidate. lm must hold the row's line maxima (it is overwritten).
-template <typename T, bool kRes>
+template <typename T, bool kRes, bool kDL = false>
 __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &rl,
                                           const SearchSmem &sm)
 {
@@ -923,8 +965,8 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
     if (wb != 0) {
         const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
         int qn = 0;
-        eval_groups<T, kRes, 1>(r, gs, sm, qn);
-        flush_queue<T, kRes>(r, sm, qn);
+        eval_groups<T, kRes, kDL, 1>(r, gs, sm, qn);
+        flush_queue<T, kRes, kDL>(r, sm, qn);
         if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
     }
     __syncthreads();
@@ -999,9 +1041,9 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
                 }
             }
         }
-        eval_groups<T, kRes, B>(r, gs, sm, qn);
+        eval_groups<T, kRes, kDL, B>(r, gs, sm, qn);
         if (qn > 0) {  // keys now: the best key prunes the next groups
-            flush_queue<T, kRes>(r, sm, qn);
+            flush_queue<T, kRes, kDL>(r, sm, qn);
             qn = 0;
         }
         if (done) break;
@@ -1010,8 +1052,30 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
     return *sm.best;
 }
 
-// One CTA per request.
-template <typename T>
+// The statistics of one row from its partials, by one warp: (max raw logit, sum of
+// 2^((l - L) c), lowest argmax); every warp of every segment wrote one partial, in segment order.
+__device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, long long row, int V,
+                                            int maxseg, int base_off, const Divisor &chunk, float c,
+                                            float &L, float &s, int &idx)
+{
+    const int lane = threadIdx.x & 31;
+    const long long rbase = row * V;
+    const int nseg = static_cast<int>(div_floor(base_off + rbase + V - 1, chunk) -
+                                      div_floor(base_off + rbase, chunk)) + 1;
+    L = -kInf;
+    s = 0.0f;
+    idx = INT_MAX;
+    for (int k = lane; k < nseg * kWarps; k += 32) {
+        const float4 raw = __ldg(reinterpret_cast<const float4 *>(part) +
+                                 static_cast<size_t>(row) * maxseg * kWarps + k);
+        combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
+    }
+    warp_reduce_stat(L, s, idx, c);
+}
+
+// One CTA per request. kDLMode: q comes from draft logits (P.dl), a separate instantiation so
+// that the other modes do not carry its registers.
+template <typename T, bool kDLMode>
 __global__ void __launch_bounds__(kThreads, 2)
 sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, VerifyParams P)
 {
@@ -1058,28 +1122,26 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     const uint32_t ireq = P.req_base + static_cast<uint32_t>(i);
     float *sm_m = reinterpret_cast<float *>(dyn + lay.rows), *sm_S = sm_m + stride;
     int *sm_amax = reinterpret_cast<int *>(sm_m + 2 * stride);
+    float *sm_md = sm_m + 3 * stride, *sm_Sd = sm_m + 4 * stride;  // draft rows (draft logits)
+    const T *dl = kDLMode ? static_cast<const T *>(P.dl) : nullptr;
 
     // 1. row statistics from the partials (warp per row) and the acceptance tests
     for (int j = warp; j <= K; j += kWarps) {
         const int row = row0 + j;
         const long long rbase = static_cast<long long>(row) * P.V;
-        const int nseg = static_cast<int>(div_floor(P.base_off + rbase + P.V - 1, P.chunk) -
-                                          div_floor(P.base_off + rbase, P.chunk)) + 1;
-        float L = -kInf, s = 0.0f;
-        int idx = INT_MAX;
-        for (int k = lane; k < nseg * kWarps; k += 32) {  // every warp of every segment
-            const float4 raw = __ldg(reinterpret_cast<const float4 *>(P.part) +
-                                     static_cast<size_t>(row) * P.maxseg * kWarps + k);
-            combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float L2 = __shfl_xor_sync(0xFFFFFFFFu, L, o);
-            const float s2 = __shfl_xor_sync(0xFFFFFFFFu, s, o);
-            const int i2 = __shfl_xor_sync(0xFFFFFFFFu, idx, o);
-            combine_stat(L, s, idx, L2, s2, i2, c);
+        float L, s;
+        int idx;
+        combine_row(P.part, row, P.V, P.maxseg, P.base_off, P.chunk, c, L, s, idx);
+        float md = 0.0f, Sd = 1.0f;
+        if (dl && j < K) {  // the draft row's q = softmax(draft logits / T): its m_d and S_d
+            float Ld;
+            int id;
+            combine_row(P.dpart, q0 + j, P.V, P.maxseg, P.dbase_off, P.dchunk, c, Ld, Sd, id);
+            md = __fmul_rn(Ld, invT);
         }
         if (lane == 0) {
+            sm_md[j] = md;
+            sm_Sd[j] = Sd;
             const float m = __fmul_rn(L, invT);  // = max_v fl(l_v / T): rounding is monotone
             const int amax = idx == INT_MAX ? 0 : idx;
             sm_m[j] = m;
@@ -1089,7 +1151,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
             if (P.opt_sum) P.opt_sum[row] = s;
             if (P.opt_amax) P.opt_amax[row] = amax;
             if (j < K && !accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j, invT, m, s, amax,
-                                          P.draft_ids, P.q, P.seed, ireq))
+                                          P.draft_ids, P.q, dl, md, Sd, P.seed, ireq))
                 atomicMin(&s_js, j);
         }
     }
@@ -1114,9 +1176,12 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     r.ireq = ireq;
     r.k0 = static_cast<uint32_t>(P.seed);
     r.k1 = static_cast<uint32_t>(P.seed >> 32);
-    const bool residual = js < K && P.q != nullptr;
-    r.qrow = residual ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
-    r.excl = (js < K && P.q == nullptr) ? __ldg(P.draft_ids + q0 + js) : -1;
+    const bool residual = js < K && (P.q != nullptr || dl != nullptr);
+    r.qrow = residual && P.q ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
+    r.dlrow = residual && dl ? dl + static_cast<size_t>(q0 + js) * P.V : nullptr;
+    r.md = js < K ? sm_md[js] : 0.0f;
+    r.Sd = js < K ? sm_Sd[js] : 1.0f;
+    r.excl = (js < K && !residual) ? __ldg(P.draft_ids + q0 + js) : -1;
     SearchSmem sm;
     sm.buf = reinterpret_cast<unsigned long long *>(dyn);
     sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
@@ -1135,7 +1200,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     const RowLines rl = row_lines(row, P.V, P.base_off);
     row_line_max<T>(r.rp, P.V, rl, lines, sm.lm);
     __syncthreads();
-    unsigned long long best = residual ? race_search<T, true>(r, rl, sm)
+    unsigned long long best = residual ? race_search<T, true, kDLMode>(r, rl, sm)
                                        : race_search<T, false>(r, rl, sm);
     if (best == 0) {
         // nothing left of max(0, p - q) after rounding, or V == 1 with the only token rejected:
@@ -1170,11 +1235,14 @@ size_t verify_smem_bytes(int V, int kmax) { return verify_layout(V, kmax).total;
 
 struct spec_verify_ctx {
     int device = 0;
-    int max_num_reqs = 0, max_spec_len = 0, V = 0, dtype = SV_F32, has_q = 0;
+    int max_num_reqs = 0, max_spec_len = 0, V = 0, dtype = SV_F32;
+    int has_q = 0;       // draft probabilities may be given
+    int has_dl = 0;      // draft logits may be given (spec_verify_run_draft_logits)
     int max_rows = 0, maxseg = 0;
     int stats_chunk = 0;   // 0: automatic (even split over whole waves)
     int stats_ctas = 1;    // one wave of the statistics kernel (SMs x CTAs per SM)
     StatPart *statpart = nullptr;
+    StatPart *dpart = nullptr;  // partials of the draft rows (draft-logits mode)
     void *lines = nullptr;      // largest logit of every 64-element line (logits dtype), or null
     unsigned *flags = nullptr;  // [1] sticky error word
     // host-buffer staging
@@ -1191,6 +1259,14 @@ struct spec_verify_ctx {
 };
 
 namespace {
+
+long long stats_chunk_for(const spec_verify_ctx *ctx, long long all)
+{
+    long long chunk = ctx->stats_chunk;
+    if (chunk <= 0) chunk = (all + kStatsWaves * ctx->stats_ctas - 1) / (kStatsWaves * ctx->stats_ctas);
+    return std::min<long long>(std::max<long long>((chunk + kChunkAlign - 1) / kChunkAlign * kChunkAlign,
+                                                   kMinChunk), kMaxChunk);
+}
 
 struct DeviceGuard {
     int prev = -1;
@@ -1225,6 +1301,7 @@ void prof_collect(spec_verify_ctx *ctx, ProfSlot &s)
 void free_all(spec_verify_ctx *ctx)
 {
     cudaFree(ctx->statpart);
+    cudaFree(ctx->dpart);
     cudaFree(ctx->lines);
     cudaFree(ctx->flags);
     cudaFree(ctx->io_logits);
@@ -1258,37 +1335,64 @@ size_t verify_smem_limit(int device)
 template <typename T>
 cudaError_t setup_kernels(int device, int *stats_per_sm)
 {
-    const cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(verify_smem_limit(device)));
+    const int limit = static_cast<int>(verify_smem_limit(device));
+    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(sv_verify_kernel<T, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T>, kThreads, 0);
 }
 
+// Statistics chunk for an array of `total` elements: the context's, or an even split over
+// kStatsWaves waves of the CTAs (shared with any other array of the same launch).
+long long stats_chunk_for(const spec_verify_ctx *ctx, long long all);
+
+template <typename T>
+StatsArray<T> stats_array(const T *logits, long long total, long long chunk, int V, int draft_rows,
+                          StatPart *part, T *lines)
+{
+    StatsArray<T> a;
+    a.logits = logits;
+    a.total = total;
+    a.chunk = make_divisor(chunk);
+    a.dv = make_divisor(V);
+    a.base_off = static_cast<int>((reinterpret_cast<uintptr_t>(logits) % (kGroup * sizeof(T))) / sizeof(T));
+    a.grid = total > 0 ? static_cast<int>((total + a.base_off + chunk - 1) / chunk) : 0;
+    a.draft_rows = draft_rows;
+    a.part = part;
+    a.lines = lines;
+    return a;
+}
+
 template <typename T>
 int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, const float *q,
-               const int32_t *cu, const float *temperature, const uint8_t *is_greedy,
+               const T *dl, const int32_t *cu, const float *temperature, const uint8_t *is_greedy,
                uint64_t seed, uint32_t base, int num_reqs, int nd, int kmax, int32_t *sampled,
                int32_t *num_sampled, int32_t *num_rejected, float *opt_max, float *opt_sum,
                int32_t *opt_amax, cudaStream_t stream)
 {
     const int V = ctx->V;
     const int rows = nd + num_reqs;
-    // statistics: the flattened [rows x V] logits split evenly over kStatsWaves waves
+    // statistics: the flattened [rows x V] logits (and [nd x V] draft logits) split evenly
     const long long total = static_cast<long long>(rows) * V;
-    const int base_off = static_cast<int>((reinterpret_cast<uintptr_t>(logits) % (kGroup * sizeof(T))) / sizeof(T));
-    long long chunk1 = ctx->stats_chunk;
-    if (chunk1 <= 0) chunk1 = (total + kStatsWaves * ctx->stats_ctas - 1) / (kStatsWaves * ctx->stats_ctas);
-    chunk1 = std::min<long long>(std::max<long long>((chunk1 + kChunkAlign - 1) / kChunkAlign * kChunkAlign,
-                                                     kMinChunk), kMaxChunk);
-    const int grid1 = static_cast<int>((total + base_off + chunk1 - 1) / chunk1);
+    const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
+    const long long chunk1 = stats_chunk_for(ctx, total + total_d);
     const RequestTable rq{cu, temperature, is_greedy, num_reqs};
     T *lines = static_cast<T *>(ctx->lines);
+    const StatsArray<T> A = stats_array<T>(logits, total, chunk1, V, 0, ctx->statpart, lines);
+    const StatsArray<T> D = stats_array<T>(dl, total_d, chunk1, V, 1, ctx->dpart, nullptr);
+    const int base_off = A.base_off;
 
     VerifyParams P;
     P.rq = rq;
     P.draft_ids = draft_ids;
     P.q = q;
+    P.dl = dl;
+    P.dpart = ctx->dpart;
+    P.dchunk = D.chunk;
+    P.dbase_off = D.base_off;
     P.part = ctx->statpart;
     P.seed = seed;
     P.req_base = base;
@@ -1314,11 +1418,12 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
         cudaEventRecord(slot->ev[0], stream);
     }
     const size_t smem1 = lines ? static_cast<size_t>(chunk1 / kGroup) * sizeof(T) : 0;
-    sv_stats_kernel<T><<<grid1, kThreads, smem1, stream>>>(logits, V, total, make_divisor(chunk1),
-                                                       make_divisor(V), ctx->maxseg, base_off, rq,
-                                                       ctx->statpart, lines);
+    sv_stats_kernel<T><<<A.grid + D.grid, kThreads, smem1, stream>>>(V, ctx->maxseg, A, D, rq);
     if (slot) cudaEventRecord(slot->ev[1], stream);
-    sv_verify_kernel<T><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
+    if (dl)
+        sv_verify_kernel<T, true><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
+    else
+        sv_verify_kernel<T, false><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
     if (slot) {
         cudaEventRecord(slot->ev[2], stream);
         slot->pending = true;
@@ -1341,7 +1446,7 @@ const void *in_place(const void *p)
 }
 
 int check_run_args(const spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
-                   const float *draft_probs, const int32_t *cu, const float *temperature,
+                   const void *draft_probs, const int32_t *cu, const float *temperature,
                    const uint8_t *is_greedy, int num_reqs, int nd, int kmax,
                    const int32_t *sampled, const int32_t *num_sampled, const int32_t *num_rejected)
 {
@@ -1362,11 +1467,12 @@ int check_run_args(const spec_verify_ctx *ctx, const void *logits, const int32_t
 extern "C" {
 
 int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, int vocab_size,
-                     int logits_dtype, int has_draft_probs, int device)
+                     int logits_dtype, int draft_input, int device)
 {
     if (!out) return SV_EINVAL;
     *out = nullptr;
     if (max_num_reqs <= 0 || max_spec_len < 0 || vocab_size <= 0) return SV_EINVAL;
+    if (draft_input < 0 || draft_input > (SV_DRAFT_PROBS | SV_DRAFT_LOGITS)) return SV_EINVAL;
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
     const long long rows = static_cast<long long>(max_num_reqs) * (max_spec_len + 1);
     const long long maxseg = ceil_div(vocab_size, kMinChunk) + 1;
@@ -1392,7 +1498,8 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     ctx->max_spec_len = max_spec_len;
     ctx->V = vocab_size;
     ctx->dtype = logits_dtype;
-    ctx->has_q = has_draft_probs != 0;
+    ctx->has_q = (draft_input & SV_DRAFT_PROBS) != 0;
+    ctx->has_dl = (draft_input & SV_DRAFT_LOGITS) != 0;
     ctx->max_rows = static_cast<int>(rows);
     ctx->maxseg = static_cast<int>(maxseg);
     const size_t R = static_cast<size_t>(rows), S = static_cast<size_t>(maxseg);
@@ -1401,6 +1508,9 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     bool ok = cudaMalloc(&ctx->statpart, R * S * kWarps * sizeof(StatPart)) == cudaSuccess &&
               cudaMalloc(&ctx->lines, nlines * eb) == cudaSuccess &&
               cudaMalloc(&ctx->flags, 2 * sizeof(unsigned)) == cudaSuccess;
+    const size_t D = static_cast<size_t>(max_num_reqs) * static_cast<size_t>(max_spec_len);
+    ok = ok && (!ctx->has_dl || D == 0 ||
+                cudaMalloc(&ctx->dpart, D * S * kWarps * sizeof(StatPart)) == cudaSuccess);
     ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
     int stats_per_sm = 0;
     ok = ok && (logits_dtype == SV_BF16 ? setup_kernels<uint16_t>(device, &stats_per_sm)
@@ -1438,14 +1548,53 @@ int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *dra
     auto stream = static_cast<cudaStream_t>(cuda_stream);
     if (ctx->dtype == SV_BF16)
         return launch_all<uint16_t>(ctx, static_cast<const uint16_t *>(logits), draft_ids,
-                                    draft_probs, cu_num_draft, temperature, is_greedy, seed,
-                                    req_index_base, num_reqs, num_draft_tokens,
+                                    draft_probs, nullptr, cu_num_draft, temperature, is_greedy,
+                                    seed, req_index_base, num_reqs, num_draft_tokens,
                                     max_spec_len_this_batch, sampled, num_sampled, num_rejected,
                                     opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
     return launch_all<float>(ctx, static_cast<const float *>(logits), draft_ids, draft_probs,
-                             cu_num_draft, temperature, is_greedy, seed, req_index_base, num_reqs,
-                             num_draft_tokens, max_spec_len_this_batch, sampled, num_sampled,
-                             num_rejected, opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
+                             nullptr, cu_num_draft, temperature, is_greedy, seed, req_index_base,
+                             num_reqs, num_draft_tokens, max_spec_len_this_batch, sampled,
+                             num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
+                             opt_row_argmax, stream);
+}
+
+int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
+                                 const int32_t *draft_ids, const void *draft_logits,
+                                 const int32_t *cu_num_draft, const float *temperature,
+                                 const uint8_t *is_greedy, uint64_t seed,
+                                 uint32_t req_index_base, int num_reqs, int num_draft_tokens,
+                                 int max_spec_len_this_batch, int32_t *sampled,
+                                 int32_t *num_sampled, int32_t *num_rejected, float *opt_row_max,
+                                 float *opt_row_sumexp, int32_t *opt_row_argmax,
+                                 void *cuda_stream)
+{
+    if (!ctx) return SV_EINVAL;
+    if (!ctx->has_dl) return SV_EINVAL;
+    int rc = check_run_args(ctx, logits, draft_ids, nullptr, cu_num_draft, temperature,
+                            is_greedy, num_reqs, num_draft_tokens, max_spec_len_this_batch,
+                            sampled, num_sampled, num_rejected);
+    if (rc != SV_OK || num_reqs == 0) return rc;
+    if (num_draft_tokens > 0 && !draft_logits) return SV_EINVAL;
+    if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(draft_logits) % 16 != 0)
+        return SV_EINVAL;
+    if (num_draft_tokens == 0) draft_logits = nullptr;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SV_EDEVICE;
+    auto stream = static_cast<cudaStream_t>(cuda_stream);
+    if (ctx->dtype == SV_BF16)
+        return launch_all<uint16_t>(ctx, static_cast<const uint16_t *>(logits), draft_ids,
+                                    nullptr, static_cast<const uint16_t *>(draft_logits),
+                                    cu_num_draft, temperature, is_greedy, seed, req_index_base,
+                                    num_reqs, num_draft_tokens, max_spec_len_this_batch, sampled,
+                                    num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
+                                    opt_row_argmax, stream);
+    return launch_all<float>(ctx, static_cast<const float *>(logits), draft_ids, nullptr,
+                             static_cast<const float *>(draft_logits), cu_num_draft, temperature,
+                             is_greedy, seed, req_index_base, num_reqs, num_draft_tokens,
+                             max_spec_len_this_batch, sampled, num_sampled, num_rejected,
+                             opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
 }
 
 int spec_verify_reserve_host_io(spec_verify_ctx *ctx)
@@ -1731,11 +1880,12 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
     auto stream = static_cast<cudaStream_t>(cuda_stream);
     if (logits_dtype == SV_BF16)
         return launch_all<uint16_t>(&view, static_cast<const uint16_t *>(logits), draft_ids,
-                                    draft_probs, cu_num_draft, temperature, is_greedy, seed,
+                                    draft_probs, nullptr, cu_num_draft, temperature, is_greedy, seed,
                                     req_index_base, num_reqs, num_draft_tokens,
                                     max_spec_len_this_batch, sampled, num_sampled, num_rejected,
                                     opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
     return launch_all<float>(&view, static_cast<const float *>(logits), draft_ids, draft_probs,
+                             nullptr,
                              cu_num_draft, temperature, is_greedy, seed, req_index_base, num_reqs,
                              num_draft_tokens, max_spec_len_this_batch, sampled, num_sampled,
                              num_rejected, opt_row_max, opt_row_sumexp, opt_row_argmax, stream);

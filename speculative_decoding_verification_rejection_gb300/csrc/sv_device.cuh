@@ -1,10 +1,10 @@
 // Device-side random numbers and binary32 elementary functions of the verification sampler.
 //
-// Race clocks: tokens come in blocks of 16 (block g = v >> 4, slot s = v & 15). Philox counter
-// (g, j, request, kClockHead) gives W (word 0) and the slot a (word 1 & 15) that holds the
-// block's smallest clock E_min = -log(W) / 16; slot s != a has clock E_min - log(U_s), U_s word
+// Race clocks: tokens come in groups of 64 (group g = v >> 6, slot s = v & 63). Philox counter
+// (g, j, request, kClockHead) gives W (word 0) and the slot a (word 1 & 63) that holds the
+// group's smallest clock E_g = -log(W) / 64; slot s != a has clock E_g - log(U_s), U_s word
 // s & 3 of counter (g, j, request, kClockHead + 1 + s / 4). By the memoryless property of the
-// exponential the 16 clocks are i.i.d. Exp(1), and E_min bounds every key of the block.
+// exponential the 64 clocks are i.i.d. Exp(1), and E_g bounds every key of the group.
 //
 // Every decision of the sampler (acceptance test, race keys) is defined with these functions,
 // so they use only correctly rounded binary32 operations written as explicit intrinsics
@@ -51,14 +51,10 @@ __device__ __forceinline__ float uniform_from_word(uint32_t w)
     return __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
 }
 
-// Counter word 3 of the acceptance uniform, of a race block's head call, and of its four slot
-// calls (kClockHead + 1 + slot / 4).
+// Counter word 3 of the acceptance uniform, of a race group's head call, and of its sixteen
+// slot calls (kClockHead + 1 + slot / 4).
 constexpr uint32_t kTagAccept = 0u;
 constexpr uint32_t kClockHead = 8u;
-
-// Largest value of -log(clock): the smallest clock is E_min = -log(W) / 16 with
-// W <= 1 - 2^-24, about 3.7e-9, so -log(clock) <= 19.41; padded.
-constexpr float kClockLogMax = 19.5f;
 
 // ---------------------------------------------------------------------------------------
 // binary32 exp: Cody & Waite (1980) reduction d = k ln2 + r with k = round(d log2 e) taken by

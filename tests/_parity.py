@@ -24,8 +24,13 @@ def to_device(batch, device="cuda:0"):
     q = None
     if batch.draft_probs is not None:
         q = torch.from_numpy(np.ascontiguousarray(batch.draft_probs, np.float32)).to(device)
+    dl = None
+    if getattr(batch, "draft_logits", None) is not None:
+        d = np.ascontiguousarray(batch.draft_logits)
+        dl = torch.from_numpy(d.view(np.int16) if d.dtype == np.uint16 else d).to(device)
     return dict(
         logits=lt,
+        draft_logits=dl,
         draft_ids=torch.from_numpy(np.ascontiguousarray(batch.draft_ids, np.int32)).to(device),
         draft_probs=q,
         cu_num_draft=torch.from_numpy(np.ascontiguousarray(batch.cu_num_draft, np.int32)).to(device),
@@ -36,23 +41,26 @@ def to_device(batch, device="cuda:0"):
 
 def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, chunks=None,
             device="cuda:0"):
-    """Run the library on a workloads.Batch; returns numpy outputs incl. row stats."""
+    """Run the library on a workloads.Batch (through the draft-logits entry point when the batch
+    carries draft logits); returns numpy outputs incl. row stats."""
     import torch
 
     import speculative_decoding_verification_rejection_gb300 as sv
 
     kmax = batch.max_spec_len if max_spec_len is None else max_spec_len
     own = ctx is None
+    has_dl = getattr(batch, "draft_logits", None) is not None
     if own:
         ctx = sv.SpecVerify(max(batch.num_reqs, 1), max(kmax, 0), batch.vocab_size,
                             batch.logits_dtype, batch.draft_probs is not None,
-                            device=torch.device(device).index or 0)
+                            device=torch.device(device).index or 0, draft_logits=has_dl)
     if chunks:
         ctx.set_chunks(chunks)
     d = to_device(batch, device)
     outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
                    d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,
-                   req_index_base=req_index_base, max_spec_len=kmax, row_stats=True)
+                   req_index_base=req_index_base, max_spec_len=kmax, row_stats=True,
+                   draft_logits=d["draft_logits"])
     torch.cuda.synchronize()
     names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
     res = {k: v.cpu().numpy() for k, v in zip(names, outs)}

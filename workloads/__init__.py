@@ -236,9 +236,11 @@ WORKLOADS = {
 }
 
 
-def workload(c: int, num_reqs: int | None = None) -> Batch:
+def workload(c: int, num_reqs: int | None = None, *, draft_logits: bool = False) -> Batch:
     """Named workload c (0..4). num_reqs, if given, keeps only the first num_reqs requests
-    of the recipe (same per-request draws), for bounded samples."""
+    of the recipe (same per-request draws), for bounded samples. draft_logits=True gives the
+    draft model's logits (target + q_noise * N, in the logits' type) instead of probabilities,
+    for the recipes that have a draft distribution."""
     seed = c
     if c == 0:
         n = 4
@@ -280,7 +282,15 @@ def workload(c: int, num_reqs: int | None = None) -> Batch:
             b["temperature"] = b["temperature"][:num_reqs]
         if b.get("greedy") is not None:
             b["greedy"] = b["greedy"][:num_reqs]
-    out = make_batch(name=f"workload{c}", data_seed=seed, verify_seed=seed, **b)
-    out.meta["workload"] = WORKLOADS[c]
+    name = f"workload{c}"
+    if draft_logits:
+        if b["q_mode"] not in ("noisy", "indep"):
+            raise ValueError(f"workload {c} has no draft distribution")
+        b["q_mode"] = "logits"
+        b.setdefault("q_noise", 2.0)
+        b.pop("q_indep_sigma", None)
+        name += "-draft-logits"
+    out = make_batch(name=name, data_seed=seed, verify_seed=seed, **b)
+    out.meta["workload"] = WORKLOADS[c] + (", draft logits" if draft_logits else "")
     out.meta["index"] = c
     return out
