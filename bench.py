@@ -11,6 +11,7 @@ Prints one JSON line (rank 0). Metric: verified draft positions per second, whol
                   [--draft-logits]
 --draft-logits measures the draft-logits input mode on the same recipe: the draft model's bf16
 logits replace the fp32 distributions, and q = softmax(draft logits / T) is computed in the call.
+--synthetic-length L measures synthetic acceptance (per-position rates of mean length L).
 Under torchrun (N > 1) every rank verifies its own batch (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 """
@@ -55,6 +56,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--draft-logits", action="store_true",
                    help="draft logits instead of draft probabilities (q computed in the call)")
+    p.add_argument("--synthetic-length", type=float, default=None,
+                   help="synthetic acceptance with the minimum-variance rates of this mean length")
     return p.parse_args()
 
 
@@ -63,6 +66,17 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def load_workload(args, num_reqs=None):
+    """The bench's batch: workload recipe, draft-logits and synthetic options applied."""
+    import workloads
+
+    b = workloads.workload(args.workload, num_reqs=num_reqs, draft_logits=args.draft_logits)
+    if args.synthetic_length is not None:
+        import speculative_decoding_verification_rejection_gb300 as sv
+        b.synthetic_rates = sv.spec_verify_synthetic_rates(args.synthetic_length, b.max_spec_len)
+    return b
 
 
 def workload_config(b):
@@ -76,6 +90,7 @@ def workload_config(b):
         "logits_dtype": b.logits_dtype,
         "draft_probs": "fp32" if b.draft_probs is not None else "none",
         "draft_logits": b.logits_dtype if b.draft_logits is not None else "none",
+        "synthetic_rates": None if b.synthetic_rates is None else [float(x) for x in b.synthetic_rates],
         "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)
                            + (b.draft_logits.nbytes if b.draft_logits is not None else 0)) / 1e6, 2),
     }
@@ -183,18 +198,17 @@ def recorded_traffic(summary: str):
 # ---------------------------------------------------------------------------------------------
 # CPU oracle timing
 # ---------------------------------------------------------------------------------------------
-def time_oracle(workload_index: int, seconds: float, draft_logits: bool = False):
+def time_oracle(args, seconds: float):
     """Time the oracle (as it stands, single-threaded) on the first requests of the workload,
     enough of them for about `seconds` of CPU work. Returns (positions/s, description)."""
     import oracle
-    import workloads
 
-    one = workloads.workload(workload_index, num_reqs=2, draft_logits=draft_logits)
+    one = load_workload(args, num_reqs=2)
     t = time.perf_counter()
     oracle.run(one)
     per_req = max((time.perf_counter() - t) / one.num_reqs, 1e-4)
     n = max(2, int(seconds / per_req))
-    b = workloads.workload(workload_index, num_reqs=n, draft_logits=draft_logits)
+    b = load_workload(args, num_reqs=n)
     t = time.perf_counter()
     oracle.run(b)
     dt = time.perf_counter() - t
@@ -209,15 +223,14 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     import oracle
-    import workloads
 
-    full = workloads.workload(args.workload, num_reqs=2, draft_logits=args.draft_logits)
+    full = load_workload(args, num_reqs=2)
     t = time.perf_counter()
     oracle.run(full)
     per_req = max((time.perf_counter() - t) / 2, 1e-4)
     budget = 150.0
     n = int(max(1, min(256, budget / max(1, args.steps + args.warmup) / per_req)))
-    sample = workloads.workload(args.workload, num_reqs=n, draft_logits=args.draft_logits)
+    sample = load_workload(args, num_reqs=n)
     for _ in range(args.warmup):
         oracle.run(sample)
     t0 = time.perf_counter()
@@ -225,7 +238,7 @@ def run_reference(args, world, rank):
         oracle.run(sample)
     dt = time.perf_counter() - t0
     value = sample.num_draft_tokens * args.steps / dt
-    cfg = workload_config(workloads.workload(args.workload, draft_logits=args.draft_logits))
+    cfg = workload_config(load_workload(args))
     cfg["reference_sample_requests_per_step"] = n
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -258,7 +271,7 @@ def run_ours(args, world, rank, local):
         dist.barrier()
     sv.lib()
 
-    b = workloads.workload(args.workload, num_reqs=args.num_reqs, draft_logits=args.draft_logits)
+    b = load_workload(args, num_reqs=args.num_reqs)
     dev = torch.device("cuda", local)
     logits_np = b.logits.view(np.int16) if b.logits.dtype == np.uint16 else b.logits
     d_logits = torch.from_numpy(logits_np).to(dev)
@@ -274,6 +287,8 @@ def run_ours(args, world, rank, local):
     n, nd, kmax, V = b.num_reqs, b.num_draft_tokens, b.max_spec_len, b.vocab_size
     ctx = sv.SpecVerify(n, kmax, V, b.logits_dtype, b.draft_probs is not None, device=local,
                         draft_logits=d_dl is not None)
+    if b.synthetic_rates is not None:
+        ctx.set_synthetic(b.synthetic_rates)
     outs = (torch.empty((n, kmax + 1), dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev))
@@ -386,7 +401,7 @@ def run_ours(args, world, rank, local):
         "stats_kernel_workload3_draft_logits.md" if d_dl is not None else "stats_kernel_workload3.md")
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        v, desc, _ = time_oracle(args.workload, args.cpu_seconds, args.draft_logits)
+        v, desc, _ = time_oracle(args, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
     clocks = sampler.summary(t0, t1) if sampler else None
     cfg = workload_config(b)

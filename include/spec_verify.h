@@ -86,6 +86,9 @@ extern "C" {
 #define SV_DRAFT_PROBS 1  /* draft_probs may be given to spec_verify_run */
 #define SV_DRAFT_LOGITS 2 /* spec_verify_run_draft_logits may be called */
 
+/* most draft positions a synthetic acceptance setting can name */
+#define SV_MAX_SYNTHETIC 64
+
 /* bits of the device error word */
 #define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
 
@@ -163,6 +166,76 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
                                  int32_t *num_sampled, int32_t *num_rejected, float *opt_row_max,
                                  float *opt_row_sumexp, int32_t *opt_row_argmax,
                                  void *cuda_stream);
+
+/*
+ * One batch with every per-call input in one struct (device pointers, as spec_verify_run).
+ * Fields: the arguments of spec_verify_run of the same names, and
+ *   draft_logits     [num_draft_tokens, vocab_size] or NULL: as spec_verify_run_draft_logits
+ *                    (needs SV_DRAFT_LOGITS; draft_probs must then be NULL)
+ *   partial_prefill  [num_reqs] uint8 or NULL: requests whose prompt is still being prefilled
+ *                    in chunks. Such a request reports num_sampled = num_rejected = 0 and a
+ *                    row of -1 ([MTP-eagle] get_num_sampled_and_rejected: the count correction
+ *                    for chunked prefill); its row statistics are still written.
+ */
+typedef struct spec_verify_batch {
+    const void *logits;
+    const int32_t *draft_ids;
+    const float *draft_probs;
+    const void *draft_logits;
+    const int32_t *cu_num_draft;
+    const float *temperature;
+    const uint8_t *is_greedy;
+    const uint8_t *partial_prefill;
+    uint64_t seed;
+    uint32_t req_index_base;
+    int32_t num_reqs;
+    int32_t num_draft_tokens;
+    int32_t max_spec_len_this_batch;
+} spec_verify_batch;
+
+/* Outputs of one batch (device pointers): sampled, num_sampled, num_rejected as in
+ * spec_verify_run; row_max, row_sumexp, row_argmax optional (NULL to skip). */
+typedef struct spec_verify_outputs {
+    int32_t *sampled;
+    int32_t *num_sampled;
+    int32_t *num_rejected;
+    float *row_max;
+    float *row_sumexp;
+    int32_t *row_argmax;
+} spec_verify_outputs;
+
+/*
+ * Verify the batch described by *batch into *out on `cuda_stream`. Same behaviour, errors and
+ * guarantees as spec_verify_run (allocation-free, graph-capturable); spec_verify_run and
+ * spec_verify_run_draft_logits are this call with the extra fields NULL.
+ */
+int spec_verify_run_batch(spec_verify_ctx *ctx, const spec_verify_batch *batch,
+                          const spec_verify_outputs *out, void *cuda_stream);
+
+/*
+ * Synthetic acceptance ([spec-in-vllm] 7.2 and 7.4: instead of the acceptance test, draft
+ * position j is accepted with a preset rate). rates[0..n) are the UNCONDITIONAL acceptance
+ * rates a_j of positions j (the probability that position j is reached and accepted), each in
+ * [0, 1] and non-increasing; positions j >= n have rate 0. Draft j is accepted iff
+ * 0 <= d < V and c_j >= u_j, c_j = a_j / a_{j-1} (binary32 division, a_{-1} = 1; 0 when
+ * a_{j-1} = 0) and u_j the acceptance uniform of the conventions above. The token at the
+ * first rejection, or the bonus token, is the target's own choice: the argmax for greedy
+ * requests, a draw from p (the race over p, nothing excluded) otherwise. draft_probs and
+ * draft_logits are not used in this mode. Applies to every later call on the context;
+ * n = 0 turns it off. rates is a HOST array, copied. Returns SV_EINVAL for n outside
+ * [0, SV_MAX_SYNTHETIC], a rate outside [0, 1] (or NaN) or an increasing pair.
+ */
+int spec_verify_set_synthetic(spec_verify_ctx *ctx, const float *rates, int n);
+
+/*
+ * Per-position rates for a target mean accepted length ([spec-in-vllm] 7.2: a length in
+ * [1, num_spec + 1] is turned into minimum-variance per-position rates). With A = mean_length
+ * - 1 accepted drafts on average, the integer-valued count with the least variance takes only
+ * floor(A) and floor(A) + 1: rates[j] = 1 for j < floor(A), A - floor(A) at j = floor(A), 0
+ * after. Writes rates[0..num_spec) (a host array). Returns SV_EINVAL if mean_length is outside
+ * [1, num_spec + 1] or num_spec is outside [0, SV_MAX_SYNTHETIC]. Needs no context or device.
+ */
+int spec_verify_synthetic_rates(double mean_length, int num_spec, float *rates);
 
 /*
  * Allocate device staging buffers sized for the context's capacity (logits, draft_probs if

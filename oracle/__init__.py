@@ -19,7 +19,12 @@ _SRC = os.path.join(_HERE, "sv_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "libsvoracle.so")
 _lib = None
 
-RACE_NONE, RACE_RESIDUAL, RACE_EXCLUDE, RACE_BONUS, RACE_FALLBACK = range(5)
+RACE_NONE, RACE_RESIDUAL, RACE_EXCLUDE, RACE_BONUS, RACE_FALLBACK, RACE_TARGET = range(6)
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("synthetic_rates", ctypes.c_void_p), ("num_synthetic_rates", ctypes.c_int32),
+                ("partial_prefill", ctypes.c_void_p)]
 EBATCH = 1
 
 # Strict IEEE binary32: no contraction of a*b+c into fma (only the explicit fmaf calls
@@ -60,7 +65,10 @@ def lib():
         L.spec_verify_ref_log.argtypes = [f32]
         L.spec_verify_ref_log.restype = f32
         L.spec_verify_ref_run.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32,
-                                          vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+                                          vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          ctypes.POINTER(_Options)]
+        L.spec_verify_ref_synthetic_rates.argtypes = [ctypes.c_double, i32, vp]
+        L.spec_verify_ref_synthetic_rates.restype = i32
         L.spec_verify_ref_run.restype = i32
         L.spec_verify_ref_residual_row.argtypes = [vp, i32, i32, f32, vp, vp, vp, vp, vp]
         L.spec_verify_ref_residual_row.restype = None
@@ -121,6 +129,14 @@ def race_clocks(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
     """Race clocks E_v (binary32) of tokens 0..n-1 of (request ireq, position j)."""
     out = np.empty(n, dtype=np.float32)
     lib().spec_verify_ref_race_clocks(seed, j, ireq, n, _p(out))
+    return out
+
+
+def synthetic_rates(mean_length: float, num_spec: int) -> np.ndarray:
+    """Minimum-variance per-position rates for a target mean accepted length."""
+    out = np.empty(max(num_spec, 0), dtype=np.float32)
+    if lib().spec_verify_ref_synthetic_rates(float(mean_length), num_spec, _p(out)) != 0:
+        raise ValueError("mean length must lie in [1, num_spec + 1]")
     return out
 
 
@@ -191,11 +207,21 @@ def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_ov
     )
     uo = None if u_override is None else np.ascontiguousarray(u_override, dtype=np.float32)
     s = batch.seed if seed is None else seed
+    opts = _Options()
+    rates = getattr(batch, "synthetic_rates", None)
+    if rates is not None:
+        rates = np.ascontiguousarray(rates, dtype=np.float32)
+        opts.synthetic_rates = rates.ctypes.data
+        opts.num_synthetic_rates = rates.size
+    partial = getattr(batch, "partial_prefill", None)
+    if partial is not None:
+        partial = np.ascontiguousarray(partial, dtype=np.uint8)
+        opts.partial_prefill = partial.ctypes.data
     rc = lib().spec_verify_ref_run(
         _p(logits), int(bf16), V, _p(ids), _p(q), _p(cu), _p(T), _p(g), s, req_index_base, n, nd,
         kmax, _p(out["sampled"]), _p(out["num_sampled"]), _p(out["num_rejected"]), _p(out["row_max"]),
         _p(out["row_sumexp"]), _p(out["row_argmax"]), _p(out["accept_margin"]), _p(out["race_gap"]),
-        _p(out["race_kind"]), _p(out["jstar"]), _p(uo))
+        _p(out["race_kind"]), _p(out["jstar"]), _p(uo), ctypes.byref(opts))
     out["accept_margin"] = out["accept_margin"][:nd]
     for k in ("race_gap", "race_kind", "jstar"):
         out[k] = out[k][:n]

@@ -181,7 +181,48 @@ float spec_verify_ref_race_clock(uint64_t seed, uint32_t j, uint32_t ireq, int32
 /* ------------------------------------------------------------------------------------ */
 enum { REF_OK = 0, REF_EINVAL = -1, REF_EBATCH = 1 };
 enum { REF_RACE_NONE = 0, REF_RACE_RESIDUAL = 1, REF_RACE_EXCLUDE = 2, REF_RACE_BONUS = 3,
-       REF_RACE_FALLBACK = 4 };
+       REF_RACE_FALLBACK = 4, REF_RACE_TARGET = 5 };
+
+/* Options of a verification call (NULL pointer = all off).
+ *   synthetic_rates: synthetic acceptance ([spec-in-vllm] 7.2): the unconditional acceptance
+ *       rate a_j of draft positions j < num_synthetic_rates (a_j = 0 beyond), in [0, 1] and
+ *       non-increasing. Replaces every request's acceptance test (7.4: the rejection kernel
+ *       compares with the preset rate in this mode).
+ *   partial_prefill: [num_reqs] or NULL; a request still in a chunked prefill reports no
+ *       token ([MTP-eagle] get_num_sampled_and_rejected: the count correction for chunked
+ *       prefill). */
+typedef struct {
+    const float *synthetic_rates;
+    int32_t num_synthetic_rates;
+    const uint8_t *partial_prefill;
+} ref_options_t;
+
+/* Conditional acceptance probability of position j given that positions 0..j-1 were
+ * accepted: a_j / a_{j-1} (a_{-1} = 1), so that position j is reached and accepted with
+ * probability a_j. A position that cannot be reached (a_{j-1} = 0) gets 0. */
+static float synthetic_conditional(const ref_options_t *o, int j)
+{
+    const float a = j < o->num_synthetic_rates ? o->synthetic_rates[j] : 0.0f;
+    if (j == 0) return a;
+    const float prev = j - 1 < o->num_synthetic_rates ? o->synthetic_rates[j - 1] : 0.0f;
+    return prev > 0.0f ? a / prev : 0.0f;
+}
+
+/* Per-position rates for a target mean accepted length L in [1, num_spec + 1]
+ * ([spec-in-vllm] 7.2: the length is turned into minimum-variance per-position rates).
+ * The number of accepted drafts N has mean L - 1; among laws of an integer N with that mean the
+ * variance is smallest when N takes only floor(L - 1) and floor(L - 1) + 1, so
+ * a_j = P(N > j) = 1 for j < floor(L - 1), the fractional part of L - 1 at j = floor(L - 1),
+ * and 0 after. Returns REF_EINVAL if L is out of range. */
+int spec_verify_ref_synthetic_rates(double mean_length, int num_spec, float *rates)
+{
+    if (num_spec < 0 || !(mean_length >= 1.0 && mean_length <= num_spec + 1.0)) return REF_EINVAL;
+    const double a = mean_length - 1.0;
+    const int n = (int)floor(a);
+    for (int j = 0; j < num_spec; ++j)
+        rates[j] = j < n ? 1.0f : (j == n ? (float)(a - n) : 0.0f);
+    return REF_OK;
+}
 
 static inline float logit_at(const void *logits, int bf16, size_t idx)
 {
@@ -298,6 +339,7 @@ static race_t race_row(const void *logits, int bf16, size_t row, int V, float in
  * accept_margin per draft position (|u - p/q| in double; +inf for greedy or invalid ids;
  * NaN where not evaluated); race_gap, race_kind, jstar per request.
  * u_override (test hook, NULL normally): acceptance uniforms per draft position.
+ * opts: synthetic acceptance and chunked-prefill flags (see ref_options_t), or NULL.
  * Returns 0; REF_EBATCH when cu_num_draft is inconsistent (then every request emits
  * num_sampled = num_rejected = 0 and a row of -1); REF_EINVAL for bad arguments.
  */
@@ -309,7 +351,7 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
                         int32_t *num_sampled, int32_t *num_rejected, float *row_max,
                         float *row_sumexp, int32_t *row_argmax, double *accept_margin,
                         double *race_gap, int32_t *race_kind, int32_t *jstar_out,
-                        const float *u_override)
+                        const float *u_override, const ref_options_t *opts)
 {
     if (num_reqs < 0 || num_draft_tokens < 0 || max_spec_len < 0 || vocab_size <= 0) return REF_EINVAL;
     const int V = vocab_size;
@@ -352,6 +394,18 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             if (row_argmax) row_argmax[row0 + j] = st[j].amax;
         }
 
+        /* a request still in its chunked prefill reports no token and no rejection */
+        if (opts && opts->partial_prefill && opts->partial_prefill[i]) {
+            for (int s = 0; s < stride; ++s) sampled[(size_t)i * stride + s] = -1;
+            num_sampled[i] = 0;
+            num_rejected[i] = 0;
+            if (race_gap) race_gap[i] = INFINITY;
+            if (race_kind) race_kind[i] = REF_RACE_NONE;
+            if (jstar_out) jstar_out[i] = -1;
+            continue;
+        }
+        const int synthetic = opts && opts->synthetic_rates;
+
         /* [MTP-eagle] _rejection_sample_kernel: walk the draft positions, stop at the
          * first rejection; [spec-notes] 8.3 greedy and stochastic rules. */
         int jstar = K;
@@ -359,7 +413,16 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             const int32_t d = draft_ids[q0 + j];
             int acc;
             double margin;
-            if (greedy) {
+            if (synthetic) {
+                /* [spec-in-vllm] 7.2 / 7.4: accept with the preset rate, whatever the tokens */
+                const float c = synthetic_conditional(opts, j);
+                const float u = u_override
+                                    ? u_override[q0 + j]
+                                    : spec_verify_ref_uniform(seed, 0u, (uint32_t)j, ireq,
+                                                              REF_TAG_ACCEPT, 0);
+                acc = d >= 0 && d < V && c >= u; /* an invalid id is still rejected */
+                margin = d >= 0 && d < V ? fabs((double)u - (double)c) : INFINITY;
+            } else if (greedy) {
                 acc = d == st[j].amax;
                 margin = INFINITY;
             } else if (d < 0 || d >= V) {
@@ -393,6 +456,14 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             /* [spec-notes] 8.3 greedy: output the target argmax at the mismatch; the bonus is
              * the argmax of the bonus row. */
             token = st[jstar].amax;
+        } else if (synthetic) {
+            /* synthetic mode has no draft distribution: the token at j* is the target's own
+             * draw from p ([MTP-eagle]: the target token is written whether accepted or not) */
+            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
+                                st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+            token = r.idx;
+            gap = r.gap;
+            kind = REF_RACE_TARGET;
         } else if (jstar == K) {
             /* [spec-notes] bonus token: sampled from p at the position after the last draft;
              * K = 0 is the plain Gumbel-max sample of a non-speculative request. */

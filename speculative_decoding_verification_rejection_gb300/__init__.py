@@ -29,6 +29,25 @@ NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", 
 SV_OK, SV_EINVAL, SV_ECAPACITY, SV_EDTYPE, SV_ECUDA, SV_EDEVICE = 0, -1, -2, -3, -4, -5
 SV_F32, SV_BF16 = 0, 1
 SV_DRAFT_PROBS, SV_DRAFT_LOGITS = 1, 2
+SV_MAX_SYNTHETIC = 64
+
+
+class Batch(ctypes.Structure):
+    """spec_verify_batch of include/spec_verify.h."""
+    _fields_ = [("logits", ctypes.c_void_p), ("draft_ids", ctypes.c_void_p),
+                ("draft_probs", ctypes.c_void_p), ("draft_logits", ctypes.c_void_p),
+                ("cu_num_draft", ctypes.c_void_p), ("temperature", ctypes.c_void_p),
+                ("is_greedy", ctypes.c_void_p), ("partial_prefill", ctypes.c_void_p),
+                ("seed", ctypes.c_uint64), ("req_index_base", ctypes.c_uint32),
+                ("num_reqs", ctypes.c_int32), ("num_draft_tokens", ctypes.c_int32),
+                ("max_spec_len_this_batch", ctypes.c_int32)]
+
+
+class Outputs(ctypes.Structure):
+    """spec_verify_outputs of include/spec_verify.h."""
+    _fields_ = [("sampled", ctypes.c_void_p), ("num_sampled", ctypes.c_void_p),
+                ("num_rejected", ctypes.c_void_p), ("row_max", ctypes.c_void_p),
+                ("row_sumexp", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p)]
 SV_ERR_BATCH = 1
 KERNELS = ("stats", "verify")
 
@@ -101,6 +120,9 @@ def lib():
     L.spec_verify_run.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp, vp,
                                   vp, vp, vp, vp]
     L.spec_verify_run_draft_logits.argtypes = list(L.spec_verify_run.argtypes)
+    L.spec_verify_run_batch.argtypes = [vp, ctypes.POINTER(Batch), ctypes.POINTER(Outputs), vp]
+    L.spec_verify_set_synthetic.argtypes = [vp, vp, i32]
+    L.spec_verify_synthetic_rates.argtypes = [ctypes.c_double, i32, vp]
     L.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp,
                                        vp, vp]
     L.spec_verify_run_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32,
@@ -116,6 +138,7 @@ def lib():
     L.spec_verify_status_string.argtypes = [i32]
     L.spec_verify_status_string.restype = ctypes.c_char_p
     for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_draft_logits",
+              "spec_verify_run_batch", "spec_verify_set_synthetic", "spec_verify_synthetic_rates",
               "spec_verify_run_host", "spec_verify_run_noalloc",
               "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
               "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
@@ -194,6 +217,29 @@ def spec_verify_run_draft_logits(ctx, logits, draft_ids, draft_logits, cu_num_dr
         max_spec_len_this_batch, _ptr(sampled), _ptr(num_sampled), _ptr(num_rejected),
         _ptr(opt_row_max), _ptr(opt_row_sumexp), _ptr(opt_row_argmax),
         _stream_handle(cuda_stream)), "spec_verify_run_draft_logits")
+
+
+def spec_verify_run_batch(ctx, batch: Batch, out: Outputs, cuda_stream=None) -> None:
+    _check(lib().spec_verify_run_batch(ctx, ctypes.byref(batch), ctypes.byref(out),
+                                       _stream_handle(cuda_stream)), "spec_verify_run_batch")
+
+
+def spec_verify_set_synthetic(ctx, rates) -> None:
+    """rates: host sequence of unconditional per-position acceptance rates ([] = off)."""
+    import numpy as np
+    r = np.ascontiguousarray(np.asarray(rates, dtype=np.float32).reshape(-1))
+    _check(lib().spec_verify_set_synthetic(ctx, r.ctypes.data if r.size else None, r.size),
+           "spec_verify_set_synthetic")
+
+
+def spec_verify_synthetic_rates(mean_length: float, num_spec: int):
+    """Minimum-variance per-position rates for a target mean accepted length (numpy float32)."""
+    import numpy as np
+    out = np.zeros(max(num_spec, 0), dtype=np.float32)
+    _check(lib().spec_verify_synthetic_rates(float(mean_length), num_spec,
+                                             out.ctypes.data if out.size else None),
+           "spec_verify_synthetic_rates")
+    return out
 
 
 def spec_verify_run_host(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
@@ -291,12 +337,14 @@ class SpecVerify:
 
     def run(self, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy, seed: int,
             *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
-            row_stats: bool = False, stream=None, draft_logits=None):
+            row_stats: bool = False, stream=None, draft_logits=None, partial_prefill=None):
         """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
         and, with row_stats=True, also (row_max, row_sumexp, row_argmax).
 
         draft_logits ([num_draft_tokens, vocab_size], the logits' dtype) replaces draft_probs:
-        q is then computed inside the call (context created with draft_logits=True)."""
+        q is then computed inside the call (context created with draft_logits=True).
+        partial_prefill ([num_reqs] uint8): requests still in a chunked prefill, which report
+        no token (spec_verify_run_batch)."""
         import torch
         num_reqs = cu_num_draft.numel() - 1
         nd = draft_ids.numel()
@@ -320,7 +368,13 @@ class SpecVerify:
             stats = (torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.int32, device=dev))
-        if draft_logits is not None:
+        if partial_prefill is not None:
+            b = Batch(_ptr(logits), _ptr(draft_ids), _ptr(draft_probs), _ptr(draft_logits),
+                      _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy),
+                      _ptr(partial_prefill), seed, req_index_base, num_reqs, nd, kmax)
+            o = Outputs(*(_ptr(t) for t in (*out, *stats)))
+            spec_verify_run_batch(self.ctx, b, o, cuda_stream=stream)
+        elif draft_logits is not None:
             spec_verify_run_draft_logits(self.ctx, logits, draft_ids, draft_logits, cu_num_draft,
                                          temperature, is_greedy, seed, req_index_base, num_reqs,
                                          nd, kmax, *out, *stats, cuda_stream=stream)
@@ -354,6 +408,15 @@ class SpecVerify:
 
     def get_profile(self):
         return spec_verify_get_profile(self.ctx)
+
+    def set_synthetic(self, rates) -> None:
+        """Synthetic acceptance with these unconditional per-position rates ([] = off)."""
+        spec_verify_set_synthetic(self.ctx, rates)
+
+    def set_synthetic_length(self, mean_length: float, num_spec: int | None = None) -> None:
+        """Synthetic acceptance with the minimum-variance rates of a target mean length."""
+        n = self.max_spec_len if num_spec is None else num_spec
+        spec_verify_set_synthetic(self.ctx, spec_verify_synthetic_rates(mean_length, n))
 
     def set_chunks(self, stats_chunk: int = 0) -> None:
         spec_verify_set_chunks(self.ctx, stats_chunk)

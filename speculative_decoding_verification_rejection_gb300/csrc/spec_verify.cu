@@ -30,6 +30,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -589,7 +590,30 @@ struct VerifyParams {
     float *opt_max, *opt_sum;
     int32_t *opt_amax;
     unsigned *flags;
+    const uint8_t *partial;      // [n] requests in a chunked prefill, or nullptr
+    int nsyn;                    // synthetic acceptance: rates of positions < nsyn (0 = off)
+    float syn[SV_MAX_SYNTHETIC]; // unconditional rate a_j of position j
 };
+
+// Synthetic acceptance of draft j ([spec-in-vllm] 7.2 / 7.4): accepted iff the id is valid and
+// the conditional rate a_j / a_{j-1} (a_{-1} = 1, 0 once a rate is 0) is >= the position's
+// uniform. One thread.
+__device__ __forceinline__ bool accept_synthetic(const VerifyParams &P, int j, int qrow,
+                                                 uint32_t ireq)
+{
+    const int d = __ldg(P.draft_ids + qrow);
+    if (d < 0 || d >= P.V) return false;
+    const float a = j < P.nsyn ? P.syn[j] : 0.0f;
+    float c = a;
+    if (j > 0) {
+        const float prev = j - 1 < P.nsyn ? P.syn[j - 1] : 0.0f;
+        c = prev > 0.0f ? __fdiv_rn(a, prev) : 0.0f;
+    }
+    const sv::Philox4 r = sv::philox4x32_10(0u, static_cast<uint32_t>(j), ireq, sv::kTagAccept,
+                                            static_cast<uint32_t>(P.seed),
+                                            static_cast<uint32_t>(P.seed >> 32));
+    return c >= sv::uniform_from_word(r.x);
+}
 
 // Acceptance test of draft j ([spec-notes] answer code: draft_prob > 0 and
 // target_prob / draft_prob >= uniform; greedy: d == argmax, [spec-notes] 8.3). One thread.
@@ -1077,7 +1101,8 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
 // that the other modes do not carry its registers.
 template <typename T, bool kDLMode>
 __global__ void __launch_bounds__(kThreads, 2)
-sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, VerifyParams P)
+sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
+                 const __grid_constant__ VerifyParams P)
 {
     extern __shared__ __align__(16) unsigned char dyn[];
     __shared__ int s_js;
@@ -1118,6 +1143,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     const int row0 = q0 + i;
     bool greedy;
     const float invT = request_invT(P.rq.temperature, P.rq.is_greedy, i, greedy);
+    const bool partial = P.partial && __ldg(P.partial + i) != 0;  // no token: only row stats
+    const bool synthetic = P.nsyn > 0;
     const float c = invT * kLog2e;
     const uint32_t ireq = P.req_base + static_cast<uint32_t>(i);
     float *sm_m = reinterpret_cast<float *>(dyn + lay.rows), *sm_S = sm_m + stride;
@@ -1150,12 +1177,19 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
             if (P.opt_max) P.opt_max[row] = m;
             if (P.opt_sum) P.opt_sum[row] = s;
             if (P.opt_amax) P.opt_amax[row] = amax;
-            if (j < K && !accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j, invT, m, s, amax,
-                                          P.draft_ids, P.q, dl, md, Sd, P.seed, ireq))
+            if (j < K && !partial &&
+                !(synthetic ? accept_synthetic(P, j, q0 + j, ireq)
+                            : accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j, invT, m, s,
+                                              amax, P.draft_ids, P.q, dl, md, Sd, P.seed, ireq)))
                 atomicMin(&s_js, j);
         }
     }
     __syncthreads();
+    if (partial) {  // [MTP-eagle] get_num_sampled_and_rejected: chunked prefill emits nothing
+        emit_row(i, -1, K, q0, -1, nullptr, P.sampled, stride, P.num_sampled, P.num_rejected, tid,
+                 kThreads);
+        return;
+    }
     const int js = s_js;  // [MTP-eagle] _rejection_sample_kernel: first rejection, K if none
     if (greedy) {  // [spec-notes] 8.3: the target argmax at the mismatch, or of the bonus row
         emit_row(i, js, K, q0, sm_amax[js], P.draft_ids, P.sampled, stride, P.num_sampled,
@@ -1176,12 +1210,13 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines, Veri
     r.ireq = ireq;
     r.k0 = static_cast<uint32_t>(P.seed);
     r.k1 = static_cast<uint32_t>(P.seed >> 32);
-    const bool residual = js < K && (P.q != nullptr || dl != nullptr);
+    // synthetic mode: the token at j* is the target's own draw from p, nothing excluded
+    const bool residual = !synthetic && js < K && (P.q != nullptr || dl != nullptr);
     r.qrow = residual && P.q ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
     r.dlrow = residual && dl ? dl + static_cast<size_t>(q0 + js) * P.V : nullptr;
     r.md = js < K ? sm_md[js] : 0.0f;
     r.Sd = js < K ? sm_Sd[js] : 1.0f;
-    r.excl = (js < K && !residual) ? __ldg(P.draft_ids + q0 + js) : -1;
+    r.excl = (!synthetic && js < K && !residual) ? __ldg(P.draft_ids + q0 + js) : -1;
     SearchSmem sm;
     sm.buf = reinterpret_cast<unsigned long long *>(dyn);
     sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
@@ -1238,6 +1273,8 @@ struct spec_verify_ctx {
     int max_num_reqs = 0, max_spec_len = 0, V = 0, dtype = SV_F32;
     int has_q = 0;       // draft probabilities may be given
     int has_dl = 0;      // draft logits may be given (spec_verify_run_draft_logits)
+    int nsyn = 0;        // synthetic acceptance rates (0 = off)
+    float syn[SV_MAX_SYNTHETIC] = {};
     int max_rows = 0, maxseg = 0;
     int stats_chunk = 0;   // 0: automatic (even split over whole waves)
     int stats_ctas = 1;    // one wave of the statistics kernel (SMs x CTAs per SM)
@@ -1366,20 +1403,22 @@ StatsArray<T> stats_array(const T *logits, long long total, long long chunk, int
     return a;
 }
 
+// Both launches of one call (arguments already checked).
 template <typename T>
-int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, const float *q,
-               const T *dl, const int32_t *cu, const float *temperature, const uint8_t *is_greedy,
-               uint64_t seed, uint32_t base, int num_reqs, int nd, int kmax, int32_t *sampled,
-               int32_t *num_sampled, int32_t *num_rejected, float *opt_max, float *opt_sum,
-               int32_t *opt_amax, cudaStream_t stream)
+int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_verify_outputs &o,
+               cudaStream_t stream)
 {
+    const T *logits = static_cast<const T *>(b.logits);
+    const T *dl = b.num_draft_tokens > 0 ? static_cast<const T *>(b.draft_logits) : nullptr;
+    const int num_reqs = b.num_reqs, nd = b.num_draft_tokens, kmax = b.max_spec_len_this_batch;
+    const int32_t *cu = b.cu_num_draft;
     const int V = ctx->V;
     const int rows = nd + num_reqs;
     // statistics: the flattened [rows x V] logits (and [nd x V] draft logits) split evenly
     const long long total = static_cast<long long>(rows) * V;
     const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
     const long long chunk1 = stats_chunk_for(ctx, total + total_d);
-    const RequestTable rq{cu, temperature, is_greedy, num_reqs};
+    const RequestTable rq{cu, b.temperature, b.is_greedy, num_reqs};
     T *lines = static_cast<T *>(ctx->lines);
     const StatsArray<T> A = stats_array<T>(logits, total, chunk1, V, 0, ctx->statpart, lines);
     const StatsArray<T> D = stats_array<T>(dl, total_d, chunk1, V, 1, ctx->dpart, nullptr);
@@ -1387,28 +1426,31 @@ int launch_all(spec_verify_ctx *ctx, const T *logits, const int32_t *draft_ids, 
 
     VerifyParams P;
     P.rq = rq;
-    P.draft_ids = draft_ids;
-    P.q = q;
+    P.draft_ids = b.draft_ids;
+    P.q = b.draft_probs;
     P.dl = dl;
     P.dpart = ctx->dpart;
     P.dchunk = D.chunk;
     P.dbase_off = D.base_off;
     P.part = ctx->statpart;
-    P.seed = seed;
-    P.req_base = base;
+    P.seed = b.seed;
+    P.req_base = b.req_index_base;
     P.nd = nd;
     P.kmax = kmax;
     P.V = V;
     P.maxseg = ctx->maxseg;
     P.base_off = base_off;
     P.chunk = make_divisor(chunk1);
-    P.sampled = sampled;
-    P.num_sampled = num_sampled;
-    P.num_rejected = num_rejected;
-    P.opt_max = opt_max;
-    P.opt_sum = opt_sum;
-    P.opt_amax = opt_amax;
+    P.sampled = o.sampled;
+    P.num_sampled = o.num_sampled;
+    P.num_rejected = o.num_rejected;
+    P.opt_max = o.row_max;
+    P.opt_sum = o.row_sumexp;
+    P.opt_amax = o.row_argmax;
     P.flags = ctx->flags;
+    P.partial = b.partial_prefill;
+    P.nsyn = ctx->nsyn;
+    for (int k = 0; k < SV_MAX_SYNTHETIC; ++k) P.syn[k] = k < ctx->nsyn ? ctx->syn[k] : 0.0f;
     const size_t smem = verify_smem_bytes(V, kmax);
 
     ProfSlot *slot = nullptr;
@@ -1445,20 +1487,26 @@ const void *in_place(const void *p)
     return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
-int check_run_args(const spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
-                   const void *draft_probs, const int32_t *cu, const float *temperature,
-                   const uint8_t *is_greedy, int num_reqs, int nd, int kmax,
-                   const int32_t *sampled, const int32_t *num_sampled, const int32_t *num_rejected)
+// Host-visible argument checks of one call (nothing is launched when they fail); `aligned`:
+// the arrays are the kernels' own (device) inputs, whose 16-byte alignment is required.
+int check_run_args(const spec_verify_ctx *ctx, const spec_verify_batch &b,
+                   const spec_verify_outputs &o, bool aligned = true)
 {
+    const int num_reqs = b.num_reqs, nd = b.num_draft_tokens, kmax = b.max_spec_len_this_batch;
     if (num_reqs < 0 || nd < 0 || kmax < 0) return SV_EINVAL;
     if (num_reqs > ctx->max_num_reqs || kmax > ctx->max_spec_len ||
         static_cast<long long>(nd) > static_cast<long long>(num_reqs) * kmax)
         return SV_ECAPACITY;
     if (num_reqs == 0) return SV_OK;
-    if (!logits || !cu || !temperature || !is_greedy || !sampled || !num_sampled ||
-        !num_rejected || (nd > 0 && !draft_ids))
+    if (!b.logits || !b.cu_num_draft || !b.temperature || !b.is_greedy || !o.sampled ||
+        !o.num_sampled || !o.num_rejected || (nd > 0 && !b.draft_ids))
         return SV_EINVAL;
-    if (draft_probs && !ctx->has_q) return SV_EINVAL;
+    if (b.draft_probs && !ctx->has_q) return SV_EINVAL;
+    if (b.draft_logits && (!ctx->has_dl || b.draft_probs)) return SV_EINVAL;
+    if (aligned && (reinterpret_cast<uintptr_t>(b.logits) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(b.draft_probs) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(b.draft_logits) % 16 != 0))
+        return SV_EINVAL;
     return SV_OK;
 }
 
@@ -1527,6 +1575,19 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     return SV_OK;
 }
 
+int spec_verify_run_batch(spec_verify_ctx *ctx, const spec_verify_batch *batch,
+                          const spec_verify_outputs *out, void *cuda_stream)
+{
+    if (!ctx || !batch || !out) return SV_EINVAL;
+    const int rc = check_run_args(ctx, *batch, *out);
+    if (rc != SV_OK || batch->num_reqs == 0) return rc;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SV_EDEVICE;
+    auto stream = static_cast<cudaStream_t>(cuda_stream);
+    return ctx->dtype == SV_BF16 ? launch_all<uint16_t>(ctx, *batch, *out, stream)
+                                 : launch_all<float>(ctx, *batch, *out, stream);
+}
+
 int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *draft_ids,
                     const float *draft_probs, const int32_t *cu_num_draft,
                     const float *temperature, const uint8_t *is_greedy, uint64_t seed,
@@ -1535,28 +1596,12 @@ int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *dra
                     int32_t *num_rejected, float *opt_row_max, float *opt_row_sumexp,
                     int32_t *opt_row_argmax, void *cuda_stream)
 {
-    if (!ctx) return SV_EINVAL;
-    int rc = check_run_args(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
-                            is_greedy, num_reqs, num_draft_tokens, max_spec_len_this_batch,
-                            sampled, num_sampled, num_rejected);
-    if (rc != SV_OK || num_reqs == 0) return rc;
-    if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 ||
-        reinterpret_cast<uintptr_t>(draft_probs) % 16 != 0)
-        return SV_EINVAL;
-    DeviceGuard g(ctx->device);
-    if (!g.ok) return SV_EDEVICE;
-    auto stream = static_cast<cudaStream_t>(cuda_stream);
-    if (ctx->dtype == SV_BF16)
-        return launch_all<uint16_t>(ctx, static_cast<const uint16_t *>(logits), draft_ids,
-                                    draft_probs, nullptr, cu_num_draft, temperature, is_greedy,
-                                    seed, req_index_base, num_reqs, num_draft_tokens,
-                                    max_spec_len_this_batch, sampled, num_sampled, num_rejected,
-                                    opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
-    return launch_all<float>(ctx, static_cast<const float *>(logits), draft_ids, draft_probs,
-                             nullptr, cu_num_draft, temperature, is_greedy, seed, req_index_base,
-                             num_reqs, num_draft_tokens, max_spec_len_this_batch, sampled,
-                             num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
-                             opt_row_argmax, stream);
+    const spec_verify_batch b{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
+                              is_greedy, nullptr, seed, req_index_base, num_reqs,
+                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
+                                opt_row_argmax};
+    return spec_verify_run_batch(ctx, &b, &o, cuda_stream);
 }
 
 int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
@@ -1570,31 +1615,37 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
                                  void *cuda_stream)
 {
     if (!ctx) return SV_EINVAL;
-    if (!ctx->has_dl) return SV_EINVAL;
-    int rc = check_run_args(ctx, logits, draft_ids, nullptr, cu_num_draft, temperature,
-                            is_greedy, num_reqs, num_draft_tokens, max_spec_len_this_batch,
-                            sampled, num_sampled, num_rejected);
-    if (rc != SV_OK || num_reqs == 0) return rc;
-    if (num_draft_tokens > 0 && !draft_logits) return SV_EINVAL;
-    if (reinterpret_cast<uintptr_t>(logits) % 16 != 0 ||
-        reinterpret_cast<uintptr_t>(draft_logits) % 16 != 0)
+    if (!ctx->has_dl || (num_reqs > 0 && num_draft_tokens > 0 && !draft_logits)) return SV_EINVAL;
+    const spec_verify_batch b{logits, draft_ids, nullptr, draft_logits, cu_num_draft, temperature,
+                              is_greedy, nullptr, seed, req_index_base, num_reqs,
+                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
+                                opt_row_argmax};
+    return spec_verify_run_batch(ctx, &b, &o, cuda_stream);
+}
+
+int spec_verify_set_synthetic(spec_verify_ctx *ctx, const float *rates, int n)
+{
+    if (!ctx || n < 0 || n > SV_MAX_SYNTHETIC || (n > 0 && !rates)) return SV_EINVAL;
+    for (int k = 0; k < n; ++k) {
+        if (!(rates[k] >= 0.0f && rates[k] <= 1.0f)) return SV_EINVAL;
+        if (k > 0 && rates[k] > rates[k - 1]) return SV_EINVAL;
+    }
+    for (int k = 0; k < SV_MAX_SYNTHETIC; ++k) ctx->syn[k] = k < n ? rates[k] : 0.0f;
+    ctx->nsyn = n;
+    return SV_OK;
+}
+
+int spec_verify_synthetic_rates(double mean_length, int num_spec, float *rates)
+{
+    if (num_spec < 0 || num_spec > SV_MAX_SYNTHETIC || (num_spec > 0 && !rates) ||
+        !(mean_length >= 1.0 && mean_length <= num_spec + 1.0))
         return SV_EINVAL;
-    if (num_draft_tokens == 0) draft_logits = nullptr;
-    DeviceGuard g(ctx->device);
-    if (!g.ok) return SV_EDEVICE;
-    auto stream = static_cast<cudaStream_t>(cuda_stream);
-    if (ctx->dtype == SV_BF16)
-        return launch_all<uint16_t>(ctx, static_cast<const uint16_t *>(logits), draft_ids,
-                                    nullptr, static_cast<const uint16_t *>(draft_logits),
-                                    cu_num_draft, temperature, is_greedy, seed, req_index_base,
-                                    num_reqs, num_draft_tokens, max_spec_len_this_batch, sampled,
-                                    num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
-                                    opt_row_argmax, stream);
-    return launch_all<float>(ctx, static_cast<const float *>(logits), draft_ids, nullptr,
-                             static_cast<const float *>(draft_logits), cu_num_draft, temperature,
-                             is_greedy, seed, req_index_base, num_reqs, num_draft_tokens,
-                             max_spec_len_this_batch, sampled, num_sampled, num_rejected,
-                             opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
+    const double accepted = mean_length - 1.0;  // mean number of accepted drafts
+    const double whole = std::floor(accepted);
+    for (int j = 0; j < num_spec; ++j)
+        rates[j] = j < whole ? 1.0f : (j == static_cast<int>(whole) ? static_cast<float>(accepted - whole) : 0.0f);
+    return SV_OK;
 }
 
 int spec_verify_reserve_host_io(spec_verify_ctx *ctx)
@@ -1639,9 +1690,12 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
 {
     if (!ctx) return SV_EINVAL;
     if (!ctx->io_logits) return SV_EINVAL;
-    int rc = check_run_args(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,
-                            is_greedy, num_reqs, num_draft_tokens, max_spec_len_this_batch,
-                            sampled, num_sampled, num_rejected);
+    // the device path's checks, less alignment: host arrays are staged or read in place
+    const spec_verify_batch hb{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
+                               is_greedy, nullptr, seed, req_index_base, num_reqs,
+                               num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_outputs ho{sampled, num_sampled, num_rejected, nullptr, nullptr, nullptr};
+    int rc = check_run_args(ctx, hb, ho, false);
     if (rc != SV_OK || num_reqs == 0) return rc;
     DeviceGuard g(ctx->device);
     if (!g.ok) return SV_EDEVICE;
@@ -1878,15 +1932,11 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
     view.statpart = reinterpret_cast<StatPart *>(bytes + kOffStatPart);
     view.flags = reinterpret_cast<unsigned *>(bytes + kOffFlags);
     auto stream = static_cast<cudaStream_t>(cuda_stream);
-    if (logits_dtype == SV_BF16)
-        return launch_all<uint16_t>(&view, static_cast<const uint16_t *>(logits), draft_ids,
-                                    draft_probs, nullptr, cu_num_draft, temperature, is_greedy, seed,
-                                    req_index_base, num_reqs, num_draft_tokens,
-                                    max_spec_len_this_batch, sampled, num_sampled, num_rejected,
-                                    opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
-    return launch_all<float>(&view, static_cast<const float *>(logits), draft_ids, draft_probs,
-                             nullptr,
-                             cu_num_draft, temperature, is_greedy, seed, req_index_base, num_reqs,
-                             num_draft_tokens, max_spec_len_this_batch, sampled, num_sampled,
-                             num_rejected, opt_row_max, opt_row_sumexp, opt_row_argmax, stream);
+    const spec_verify_batch b{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
+                              is_greedy, nullptr, seed, req_index_base, num_reqs,
+                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
+                                opt_row_argmax};
+    return logits_dtype == SV_BF16 ? launch_all<uint16_t>(&view, b, o, stream)
+                                   : launch_all<float>(&view, b, o, stream);
 }

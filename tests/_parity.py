@@ -28,9 +28,13 @@ def to_device(batch, device="cuda:0"):
     if getattr(batch, "draft_logits", None) is not None:
         d = np.ascontiguousarray(batch.draft_logits)
         dl = torch.from_numpy(d.view(np.int16) if d.dtype == np.uint16 else d).to(device)
+    pp = None
+    if getattr(batch, "partial_prefill", None) is not None:
+        pp = torch.from_numpy(np.ascontiguousarray(batch.partial_prefill, np.uint8)).to(device)
     return dict(
         logits=lt,
         draft_logits=dl,
+        partial_prefill=pp,
         draft_ids=torch.from_numpy(np.ascontiguousarray(batch.draft_ids, np.int32)).to(device),
         draft_probs=q,
         cu_num_draft=torch.from_numpy(np.ascontiguousarray(batch.cu_num_draft, np.int32)).to(device),
@@ -56,11 +60,13 @@ def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, 
                             device=torch.device(device).index or 0, draft_logits=has_dl)
     if chunks:
         ctx.set_chunks(chunks)
+    rates = getattr(batch, "synthetic_rates", None)
+    ctx.set_synthetic([] if rates is None else rates)
     d = to_device(batch, device)
     outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
                    d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,
                    req_index_base=req_index_base, max_spec_len=kmax, row_stats=True,
-                   draft_logits=d["draft_logits"])
+                   draft_logits=d["draft_logits"], partial_prefill=d["partial_prefill"])
     torch.cuda.synchronize()
     names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
     res = {k: v.cpu().numpy() for k, v in zip(names, outs)}

@@ -3,6 +3,9 @@ that include/spec_verify.h declares (no compute call is made here)."""
 import ctypes
 import re
 
+import numpy as np
+import pytest
+
 import speculative_decoding_verification_rejection_gb300 as sv
 
 
@@ -53,3 +56,16 @@ def test_product_path_does_not_use_the_oracle():
         text = f.read_text(encoding="utf-8")
         assert "import oracle" not in text and "from oracle" not in text, f
         assert "sv_oracle" not in text and "spec_verify_ref" not in text, f
+
+
+def test_synthetic_rates_helper_matches_the_oracle():
+    """The library's host helper (no device involved) against the oracle's own conversion."""
+    import oracle
+
+    for K in (0, 1, 3, 5, 8):
+        for L in np.linspace(1.0, K + 1.0, 17):
+            got = sv.spec_verify_synthetic_rates(L, K)
+            np.testing.assert_array_equal(got, oracle.synthetic_rates(L, K))
+    for L, K in ((0.5, 3), (4.5, 3), (float("nan"), 2), (2.0, sv.SV_MAX_SYNTHETIC + 1)):
+        with pytest.raises(sv.SpecVerifyError):
+            sv.spec_verify_synthetic_rates(L, K)

@@ -119,6 +119,10 @@ class Batch:
     meta: dict = field(default_factory=dict)
     # [N_d, V] draft logits in the logits' type (draft-logits mode: q = softmax(dl / T)), or None
     draft_logits: np.ndarray | None = None
+    # [num_reqs] uint8: requests still in a chunked prefill (they report no token), or None
+    partial_prefill: np.ndarray | None = None
+    # synthetic acceptance: unconditional rate per draft position (verifier setting), or None
+    synthetic_rates: np.ndarray | None = None
 
     @property
     def num_reqs(self) -> int:
