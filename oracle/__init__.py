@@ -24,7 +24,10 @@ RACE_NONE, RACE_RESIDUAL, RACE_EXCLUDE, RACE_BONUS, RACE_FALLBACK, RACE_TARGET =
 
 class _Options(ctypes.Structure):
     _fields_ = [("synthetic_rates", ctypes.c_void_p), ("num_synthetic_rates", ctypes.c_int32),
-                ("partial_prefill", ctypes.c_void_p)]
+                ("partial_prefill", ctypes.c_void_p), ("frequency_penalty", ctypes.c_void_p),
+                ("output_bin_counts", ctypes.c_void_p), ("counts_row", ctypes.c_void_p),
+                ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p),
+                ("row_select_margin", ctypes.c_void_p)]
 EBATCH = 1
 
 # Strict IEEE binary32: no contraction of a*b+c into fma (only the explicit fmaf calls
@@ -77,6 +80,8 @@ def lib():
             getattr(L, f).restype = None
         L.spec_verify_ref_draft_probs.argtypes = [vp, i32, i32, vp, vp, vp, i32, vp]
         L.spec_verify_ref_draft_probs.restype = None
+        L.spec_verify_ref_select_row.argtypes = [vp, i32, i32, f32, vp, vp, vp]
+        L.spec_verify_ref_select_row.restype = None
         L.spec_verify_ref_race_clocks.argtypes = [u64, u32, u32, i32, vp]
         L.spec_verify_ref_race_clocks.restype = None
         _lib = L
@@ -138,6 +143,17 @@ def synthetic_rates(mean_length: float, num_spec: int) -> np.ndarray:
     if lib().spec_verify_ref_synthetic_rates(float(mean_length), num_spec, _p(out)) != 0:
         raise ValueError("mean length must lie in [1, num_spec + 1]")
     return out
+
+
+def select_row(x: np.ndarray, top_k: int, top_p: float):
+    """(tau, kept mass, top-p margin) of the sampling constraints on one processed row."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    tau = ctypes.c_float()
+    Sk = ctypes.c_double()
+    margin = ctypes.c_double()
+    lib().spec_verify_ref_select_row(_p(x), x.size, int(top_k), float(top_p), ctypes.byref(tau),
+                                     ctypes.byref(Sk), ctypes.byref(margin))
+    return tau.value, Sk.value, margin.value
 
 
 def residual_row(logits_row: np.ndarray, bf16: bool, invT: float, q: np.ndarray):
@@ -217,12 +233,30 @@ def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_ov
     if partial is not None:
         partial = np.ascontiguousarray(partial, dtype=np.uint8)
         opts.partial_prefill = partial.ctypes.data
+    keep = []  # arrays whose addresses the options hold
+
+    def _opt(name, dtype):
+        a = getattr(batch, name, None)
+        if a is None:
+            return None
+        a = np.ascontiguousarray(a, dtype=dtype)
+        keep.append(a)
+        return a.ctypes.data
+
+    opts.frequency_penalty = _opt("frequency_penalty", np.float32)
+    opts.output_bin_counts = _opt("output_bin_counts", np.int32)
+    opts.counts_row = _opt("counts_row", np.int32)
+    opts.top_k = _opt("top_k", np.int32)
+    opts.top_p = _opt("top_p", np.float32)
+    out["row_select_margin"] = np.empty(max(R, 1), dtype=np.float64)
+    opts.row_select_margin = out["row_select_margin"].ctypes.data
     rc = lib().spec_verify_ref_run(
         _p(logits), int(bf16), V, _p(ids), _p(q), _p(cu), _p(T), _p(g), s, req_index_base, n, nd,
         kmax, _p(out["sampled"]), _p(out["num_sampled"]), _p(out["num_rejected"]), _p(out["row_max"]),
         _p(out["row_sumexp"]), _p(out["row_argmax"]), _p(out["accept_margin"]), _p(out["race_gap"]),
         _p(out["race_kind"]), _p(out["jstar"]), _p(uo), ctypes.byref(opts))
     out["accept_margin"] = out["accept_margin"][:nd]
+    out["row_select_margin"] = out["row_select_margin"][:R]
     for k in ("race_gap", "race_kind", "jstar"):
         out[k] = out[k][:n]
     out["status"] = rc

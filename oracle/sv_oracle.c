@@ -39,6 +39,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define REF_TAG_ACCEPT 0u  /* counter word 3 of the acceptance uniform */
@@ -190,11 +191,23 @@ enum { REF_RACE_NONE = 0, REF_RACE_RESIDUAL = 1, REF_RACE_EXCLUDE = 2, REF_RACE_
  *       compares with the preset rate in this mode).
  *   partial_prefill: [num_reqs] or NULL; a request still in a chunked prefill reports no
  *       token ([MTP-eagle] get_num_sampled_and_rejected: the count correction for chunked
- *       prefill). */
+ *       prefill).
+ *   frequency_penalty [num_reqs], output_bin_counts [rows x V] with counts_row [num_reqs]
+ *       (the counts row of each request; NULL = row i): the frequency penalty (see
+ *       processed_row). Either pointer NULL: no penalty.
+ *   top_k [num_reqs] int32, top_p [num_reqs] binary32, each or NULL: sampling constraints of
+ *       sampling requests (see select_row). top_k == 1 makes a request greedy.
+ *   row_select_margin [rows] (output, NULL to skip): the top-p decision margin of each row. */
 typedef struct {
     const float *synthetic_rates;
     int32_t num_synthetic_rates;
     const uint8_t *partial_prefill;
+    const float *frequency_penalty;
+    const int32_t *output_bin_counts;
+    const int32_t *counts_row;
+    const int32_t *top_k;
+    const float *top_p;
+    double *row_select_margin;
 } ref_options_t;
 
 /* Conditional acceptance probability of position j given that positions 0..j-1 were
@@ -230,39 +243,128 @@ static inline float logit_at(const void *logits, int bf16, size_t idx)
     return ((const float *)logits)[idx];
 }
 
-typedef struct {
-    float m;      /* max_v x_v */
-    double S;     /* sum_v exp(x_v - m), accumulated in double in index order */
-    float S_f;    /* S rounded to binary32: the value the decisions use */
-    int32_t amax; /* argmax of the raw logits, lowest index on ties */
-} row_stats_t;
-
-/* Softmax statistics of one row: [spec-in-vllm] 7.4 (block stats: max, argmax, sum of exp,
- * for a log-sum-exp) and [spec-notes] 8.2 (target probs = softmax of the processed logits). */
-static row_stats_t row_stats(const void *logits, int bf16, size_t row, int V, float invT)
+/* Processed logits of one row ([spec-notes] 8.2: the logits processors run before the
+ * softmax):
+ *   y_v = fma(-f, c_v, l_v)  ([MTP-eagle] frequency penalty: logit -= penalty * count), and
+ *   y_v = l_v where f = 0 or c_v = 0;
+ *   x_v = y_v * (1 / T).
+ * c_v is the token's count in `counts` (none without counts) plus the number of drafts before
+ * this position that equal v: the drafts before position j are output the target conditions
+ * on at j. */
+static void processed_row(const void *logits, int bf16, size_t row, int V, float invT, float f,
+                          const int32_t *counts, const int32_t *prev, int nprev, float *y, float *x)
 {
     const size_t base = row * (size_t)V;
+    for (int v = 0; v < V; ++v) {
+        const float l = logit_at(logits, bf16, base + (size_t)v);
+        int64_t c = counts ? counts[v] : 0;
+        for (int k = 0; k < nprev; ++k) c += prev[k] == v;
+        y[v] = (f == 0.0f || c == 0) ? l : fmaf(-f, (float)c, l);
+        x[v] = y[v] * invT;
+    }
+}
+
+typedef struct {
+    float m;       /* max_v x_v */
+    double S;      /* sum_v exp(x_v - m), accumulated in double in index order */
+    float S_f;     /* S rounded to binary32 */
+    int32_t amax;  /* argmax of y (the processed logits before temperature), lowest index */
+    float tau;     /* kept tokens: x_v >= tau (-inf: all) */
+    double Sk;     /* sum over the kept tokens of exp(x_v - m), double, index order */
+    float Sk_f;    /* Sk rounded to binary32: the normaliser of p' that the decisions use */
+    double margin; /* top-p decision margin relative to its total (+inf without top-p) */
+} row_stats_t;
+
+/* Softmax statistics of one processed row: [spec-in-vllm] 7.4 (block stats: max, argmax, sum
+ * of exp, for a log-sum-exp) and [spec-notes] 8.2 (target probs = softmax of the processed
+ * logits). */
+static row_stats_t row_stats(const float *y, const float *x, int V)
+{
     row_stats_t st;
     st.m = -INFINITY;
     st.amax = 0;
-    float best_raw = logit_at(logits, bf16, base);
     for (int v = 0; v < V; ++v) {
-        float l = logit_at(logits, bf16, base + (size_t)v);
-        float x = l * invT;
-        if (x > st.m) st.m = x;
-        if (l > best_raw) {
-            best_raw = l;
-            st.amax = v;
-        }
+        if (x[v] > st.m) st.m = x[v];
+        if (y[v] > y[st.amax]) st.amax = v;
     }
     double S = 0.0;
-    for (int v = 0; v < V; ++v) {
-        float x = logit_at(logits, bf16, base + (size_t)v) * invT;
-        S += (double)spec_verify_ref_exp(x - st.m);
-    }
+    for (int v = 0; v < V; ++v) S += (double)spec_verify_ref_exp(x[v] - st.m);
     st.S = S;
     st.S_f = (float)S;
+    st.tau = -INFINITY;
+    st.Sk = S;
+    st.Sk_f = st.S_f;
+    st.margin = INFINITY;
     return st;
+}
+
+typedef struct {
+    float x;
+    int32_t v;
+} xv_t;
+
+static int by_value_desc(const void *a, const void *b)
+{
+    const xv_t *p = (const xv_t *)a, *q = (const xv_t *)b;
+    if (p->x != q->x) return p->x > q->x ? -1 : 1;
+    return p->v < q->v ? -1 : (p->v > q->v);
+}
+
+/* Sampling constraints ([spec-notes] 8.2 apply_sampling_constraints; [mini-sglang]: top_k < 1
+ * means the whole vocabulary, top_p is clamped to [1e-6, 1]). With the values sorted from the
+ * largest:
+ *   top-k keeps every token whose value is at least the k-th largest (ties at the boundary are
+ *         all kept), for 1 <= k < V;
+ *   top-p then keeps, among those, every token whose strictly larger tokens hold less than
+ *         P * Z of the mass, Z the mass of the top-k set (mass t_v = exp(x_v - m), summed in
+ *         double), for P < 1.
+ * Both keep a set {x_v >= tau}; p' is p restricted to it and renormalised by Sk. */
+static void select_row(const float *x, int V, int top_k, float top_p, row_stats_t *st)
+{
+    const int use_k = top_k >= 1 && top_k < V;
+    const int use_p = top_p < 1.0f; /* NaN or >= 1: no top-p */
+    if (!use_k && !use_p) return;
+    const double P = top_p < 1e-6f ? 1e-6 : (double)top_p;
+    xv_t *s = (xv_t *)malloc((size_t)V * sizeof(xv_t));
+    for (int v = 0; v < V; ++v) {
+        s[v].x = x[v];
+        s[v].v = v;
+    }
+    qsort(s, (size_t)V, sizeof(xv_t), by_value_desc);
+    const float tau_k = use_k ? s[top_k - 1].x : -INFINITY;
+    double Z = 0.0;
+    for (int v = 0; v < V; ++v)
+        if (x[v] >= tau_k) Z += (double)spec_verify_ref_exp(x[v] - st->m);
+    float tau = tau_k;
+    double margin = INFINITY;
+    if (use_p) {
+        const double target = P * Z;
+        double above = 0.0; /* mass of the tokens strictly larger than the current group */
+        int k = 0;
+        while (k < V && s[k].x >= tau_k) {
+            const float xv = s[k].x;
+            double gm = 0.0;
+            int e = k;
+            for (; e < V && s[e].x == xv; ++e) gm += (double)spec_verify_ref_exp(xv - st->m);
+            if (above < target) {
+                tau = xv;
+                if ((target - above) / Z < margin) margin = (target - above) / Z;
+                above += gm;
+                k = e;
+            } else {
+                if ((above - target) / Z < margin) margin = (above - target) / Z;
+                break;
+            }
+        }
+    }
+    free(s);
+    double Sk = 0.0;
+    for (int v = 0; v < V; ++v)
+        if (x[v] >= tau) Sk += (double)spec_verify_ref_exp(x[v] - st->m);
+    st->tau = tau;
+    st->Sk = Sk;
+    st->Sk_f = (float)Sk;
+    st->margin = margin;
 }
 
 typedef struct {
@@ -294,22 +396,21 @@ static inline void race_offer(race_t *r, float key, int32_t v, float *second)
  * answer (argmax(prob / q) with q ~ Exp(1) needs no normalisation) and [spec-in-vllm] 7.3
  * (Gumbel argmax, the same race in log form). Keys: key_v = w_v / E_v, E_v the token's race
  * clock, one binary32 division.
+ * Only the tokens the sampling constraints keep (x_v >= tau) take part; S is the normaliser of
+ * p over them.
  *   q == NULL : w_v = t_v = exp(x_v - m), proportional to p_v; token `exclude` is left out
  *               (the rejected draft token when there are no draft probabilities).
  *   q != NULL : residual weights rr_v = fma(-S, q_v, t_v) = S (p_v - q_v) rounded once,
  *               candidates rr_v > 0 ([spec-notes] residual distribution max(0, p - q)).
  * The decision margin is the winner's key over the runner-up's, as log(key1) - log(key2).   */
-static race_t race_row(const void *logits, int bf16, size_t row, int V, float invT, float m,
-                       float S_f, const float *q, int32_t exclude, uint64_t seed, uint32_t j,
-                       uint32_t ireq)
+static race_t race_row(const float *x, int V, float m, float tau, float S_f, const float *q,
+                       int32_t exclude, uint64_t seed, uint32_t j, uint32_t ireq)
 {
     race_t r = {-1, -INFINITY, INFINITY, 0};
     float second = -INFINITY;
-    const size_t base = row * (size_t)V;
     for (int v = 0; v < V; ++v) {
-        if (v == exclude) continue;
-        float x = logit_at(logits, bf16, base + (size_t)v) * invT;
-        float t = spec_verify_ref_exp(x - m);
+        if (v == exclude || !(x[v] >= tau)) continue; /* only kept tokens take part */
+        float t = spec_verify_ref_exp(x[v] - m);
         float w;
         if (q) {
             float rr = fmaf(-S_f, q[v], t);
@@ -381,17 +482,34 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
         const size_t row0 = (size_t)q0 + (size_t)i;
         const uint32_t ireq = req_index_base + (uint32_t)i;
         const float T = temperature[i];
-        /* greedy: flag set, or temperature 0 ([spec-in-vllm] 7.0.1; [mini-sglang] T <= 0) */
-        const int greedy = is_greedy[i] != 0 || !(T > 0.0f);
+        const int top_k = opts && opts->top_k ? opts->top_k[i] : 0;
+        const float top_p = opts && opts->top_p ? opts->top_p[i] : 1.0f;
+        /* greedy: flag set, or temperature 0 ([spec-in-vllm] 7.0.1; [mini-sglang] T <= 0, and
+         * top_k == 1 keeps only the largest logit) */
+        const int greedy = is_greedy[i] != 0 || !(T > 0.0f) || top_k == 1;
         const float invT = greedy ? 1.0f : 1.0f / T;
+        const int pen = opts && opts->frequency_penalty && opts->output_bin_counts;
+        const float f = pen ? opts->frequency_penalty[i] : 0.0f;
+        const int32_t *counts =
+            pen ? opts->output_bin_counts +
+                      (size_t)(opts->counts_row ? opts->counts_row[i] : i) * (size_t)V
+                : NULL;
 
-        /* stats of every row (rows after a rejection are reported too, for inspection) */
+        /* processed logits and stats of every row (rows after a rejection are reported too,
+         * for inspection); row j conditions on the drafts before it */
+        float *ybuf = (float *)malloc((size_t)(K + 1) * V * sizeof(float));
+        float *xbuf = (float *)malloc((size_t)(K + 1) * V * sizeof(float));
         row_stats_t st[K + 1];
         for (int j = 0; j <= K; ++j) {
-            st[j] = row_stats(logits, logits_bf16, row0 + (size_t)j, V, invT);
+            float *y = ybuf + (size_t)j * V, *x = xbuf + (size_t)j * V;
+            processed_row(logits, logits_bf16, row0 + (size_t)j, V, invT, f, counts,
+                          draft_ids + q0, pen ? j : 0, y, x);
+            st[j] = row_stats(y, x, V);
+            if (!greedy) select_row(x, V, top_k, top_p, &st[j]);
             if (row_max) row_max[row0 + j] = st[j].m;
-            if (row_sumexp) row_sumexp[row0 + j] = st[j].S_f;
+            if (row_sumexp) row_sumexp[row0 + j] = st[j].Sk_f;
             if (row_argmax) row_argmax[row0 + j] = st[j].amax;
+            if (opts && opts->row_select_margin) opts->row_select_margin[row0 + j] = st[j].margin;
         }
 
         /* a request still in its chunked prefill reports no token and no rejection */
@@ -402,6 +520,8 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             if (race_gap) race_gap[i] = INFINITY;
             if (race_kind) race_kind[i] = REF_RACE_NONE;
             if (jstar_out) jstar_out[i] = -1;
+            free(ybuf);
+            free(xbuf);
             continue;
         }
         const int synthetic = opts && opts->synthetic_rates;
@@ -429,9 +549,10 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
                 acc = 0; /* [spec-notes] accept only when draft_token_id < vocab_size */
                 margin = INFINITY;
             } else {
-                const float x_d = logit_at(logits, logits_bf16, (row0 + j) * (size_t)V + d) * invT;
-                const float t_d = spec_verify_ref_exp(x_d - st[j].m);
-                const float p_d = t_d / st[j].S_f;
+                /* p' of the processed, constrained target ([spec-notes] 8.2) */
+                const float x_d = xbuf[(size_t)j * V + d];
+                const float t_d = x_d >= st[j].tau ? spec_verify_ref_exp(x_d - st[j].m) : 0.0f;
+                const float p_d = t_d / st[j].Sk_f;
                 const float q_d = draft_probs ? draft_probs[(size_t)(q0 + j) * V + d] : 1.0f;
                 const float u = u_override
                                     ? u_override[q0 + j]
@@ -439,7 +560,7 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
                                                               REF_TAG_ACCEPT, 0);
                 /* [spec-notes] answer code: draft_prob > 0 and target_prob / draft_prob >= uniform */
                 acc = q_d > 0.0f && p_d / q_d >= u;
-                margin = q_d > 0.0f ? fabs((double)u - (double)t_d / st[j].S / (double)q_d)
+                margin = q_d > 0.0f ? fabs((double)u - (double)t_d / st[j].Sk / (double)q_d)
                                     : INFINITY;
             }
             if (accept_margin) accept_margin[q0 + j] = margin;
@@ -459,29 +580,29 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
         } else if (synthetic) {
             /* synthetic mode has no draft distribution: the token at j* is the target's own
              * draw from p ([MTP-eagle]: the target token is written whether accepted or not) */
-            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
-                                st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+            race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
+                                st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_TARGET;
         } else if (jstar == K) {
             /* [spec-notes] bonus token: sampled from p at the position after the last draft;
              * K = 0 is the plain Gumbel-max sample of a non-speculative request. */
-            race_t r = race_row(logits, logits_bf16, row0 + K, V, invT, st[K].m, st[K].S_f, NULL,
-                                -1, seed, (uint32_t)K, ireq);
+            race_t r = race_row(xbuf + (size_t)K * V, V, st[K].m, st[K].tau, st[K].Sk_f, NULL, -1,
+                                seed, (uint32_t)K, ireq);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_BONUS;
         } else if (draft_probs) {
             const float *q = draft_probs + (size_t)(q0 + jstar) * V;
-            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
-                                st[jstar].S_f, q, -1, seed, (uint32_t)jstar, ireq);
+            race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
+                                st[jstar].Sk_f, q, -1, seed, (uint32_t)jstar, ireq);
             kind = REF_RACE_RESIDUAL;
             if (r.idx < 0) {
                 /* nothing left of max(0, p - q) after rounding: sample from p itself so that
                  * the emitted token is still a target-side draw */
-                r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
-                             st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
+                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
                 kind = REF_RACE_FALLBACK;
             }
             token = r.idx;
@@ -490,11 +611,11 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             /* [spec-notes] NO_DRAFT_PROBS: q is a point mass on d, so the residual is p with d
              * removed; an out-of-range d removes nothing. */
             const int32_t d = draft_ids[q0 + jstar];
-            race_t r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
-                                st[jstar].S_f, NULL, d, seed, (uint32_t)jstar, ireq);
+            race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
+                                st[jstar].Sk_f, NULL, d, seed, (uint32_t)jstar, ireq);
             if (r.idx < 0) /* V == 1 and d == 0: nothing else to draw */
-                r = race_row(logits, logits_bf16, row0 + jstar, V, invT, st[jstar].m,
-                             st[jstar].S_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
+                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_EXCLUDE;
@@ -511,6 +632,8 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
         if (race_gap) race_gap[i] = gap;
         if (race_kind) race_kind[i] = kind;
         if (jstar_out) jstar_out[i] = jstar;
+        free(ybuf);
+        free(xbuf);
     }
     return REF_OK;
 }
@@ -561,14 +684,30 @@ void spec_verify_ref_residual_row(const void *logits_row, int logits_bf16, int v
                                   float invT, const float *q, float *t_out, float *rr_out,
                                   float *m_out, float *S_out)
 {
-    row_stats_t st = row_stats(logits_row, logits_bf16, 0, vocab_size, invT);
+    float *y = (float *)malloc((size_t)vocab_size * sizeof(float));
+    float *x = (float *)malloc((size_t)vocab_size * sizeof(float));
+    processed_row(logits_row, logits_bf16, 0, vocab_size, invT, 0.0f, NULL, NULL, 0, y, x);
+    row_stats_t st = row_stats(y, x, vocab_size);
     for (int v = 0; v < vocab_size; ++v) {
-        float x = logit_at(logits_row, logits_bf16, (size_t)v) * invT;
-        t_out[v] = spec_verify_ref_exp(x - st.m);
+        t_out[v] = spec_verify_ref_exp(x[v] - st.m);
         if (rr_out) rr_out[v] = fmaf(-st.S_f, q[v], t_out[v]);
     }
     *m_out = st.m;
     *S_out = st.S_f;
+    free(y);
+    free(x);
+}
+
+/* The sampling constraints of one processed row x[0..V) (for the checks of select_row):
+ * writes the threshold tau (kept: x >= tau), the kept mass Sk (double) and the top-p margin. */
+void spec_verify_ref_select_row(const float *x, int V, int top_k, float top_p, float *tau,
+                                double *Sk, double *margin)
+{
+    row_stats_t st = row_stats(x, x, V);
+    select_row(x, V, top_k, top_p, &st);
+    *tau = st.tau;
+    *Sk = st.Sk;
+    *margin = st.margin;
 }
 
 /* Element-wise exp / log over arrays (for the accuracy checks of the two functions). */

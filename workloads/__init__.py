@@ -123,6 +123,13 @@ class Batch:
     partial_prefill: np.ndarray | None = None
     # synthetic acceptance: unconditional rate per draft position (verifier setting), or None
     synthetic_rates: np.ndarray | None = None
+    # logits processors: [num_reqs] float32 frequency penalty with [rows, V] int32 output token
+    # counts (row counts_row[i], or i, per request); [num_reqs] int32 top_k, float32 top_p
+    frequency_penalty: np.ndarray | None = None
+    output_bin_counts: np.ndarray | None = None
+    counts_row: np.ndarray | None = None
+    top_k: np.ndarray | None = None
+    top_p: np.ndarray | None = None
 
     @property
     def num_reqs(self) -> int:
