@@ -12,6 +12,7 @@ Prints one JSON line (rank 0). Metric: verified draft positions per second, whol
 --draft-logits measures the draft-logits input mode on the same recipe: the draft model's bf16
 logits replace the fp32 distributions, and q = softmax(draft logits / T) is computed in the call.
 --synthetic-length L measures synthetic acceptance (per-position rates of mean length L).
+--top-p P, --top-k K and --frequency-penalty measure the logits processors on the same recipe.
 Under torchrun (N > 1) every rank verifies its own batch (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 """
@@ -58,6 +59,10 @@ def parse_args():
                    help="draft logits instead of draft probabilities (q computed in the call)")
     p.add_argument("--synthetic-length", type=float, default=None,
                    help="synthetic acceptance with the minimum-variance rates of this mean length")
+    p.add_argument("--top-p", type=float, default=None, help="top-p of every request")
+    p.add_argument("--top-k", type=int, default=None, help="top-k of every request")
+    p.add_argument("--frequency-penalty", action="store_true",
+                   help="a frequency penalty with seeded output-token counts per request")
     return p.parse_args()
 
 
@@ -76,6 +81,13 @@ def load_workload(args, num_reqs=None):
     if args.synthetic_length is not None:
         import speculative_decoding_verification_rejection_gb300 as sv
         b.synthetic_rates = sv.spec_verify_synthetic_rates(args.synthetic_length, b.max_spec_len)
+    import numpy as np
+    if args.top_p is not None:
+        b.top_p = np.full(b.num_reqs, args.top_p, np.float32)
+    if args.top_k is not None:
+        b.top_k = np.full(b.num_reqs, args.top_k, np.int32)
+    if args.frequency_penalty:
+        workloads.add_penalty(b, args.workload)
     return b
 
 
@@ -91,6 +103,9 @@ def workload_config(b):
         "draft_probs": "fp32" if b.draft_probs is not None else "none",
         "draft_logits": b.logits_dtype if b.draft_logits is not None else "none",
         "synthetic_rates": None if b.synthetic_rates is None else [float(x) for x in b.synthetic_rates],
+        "top_p": None if b.top_p is None else float(b.top_p[0]),
+        "top_k": None if b.top_k is None else int(b.top_k[0]),
+        "frequency_penalty": b.frequency_penalty is not None,
         "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)
                            + (b.draft_logits.nbytes if b.draft_logits is not None else 0)) / 1e6, 2),
     }
@@ -279,6 +294,11 @@ def run_ours(args, world, rank, local):
     if b.draft_logits is not None:
         dl_np = b.draft_logits.view(np.int16) if b.draft_logits.dtype == np.uint16 else b.draft_logits
     d_dl = torch.from_numpy(dl_np).to(dev) if dl_np is not None else None
+    extras = {}
+    for name in ("frequency_penalty", "output_bin_counts", "counts_row", "top_k", "top_p"):
+        a = getattr(b, name, None)
+        if a is not None:
+            extras[name] = torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     d_q = torch.from_numpy(b.draft_probs).to(dev) if b.draft_probs is not None else None
     d_ids = torch.from_numpy(b.draft_ids).to(dev)
     d_cu = torch.from_numpy(b.cu_num_draft).to(dev)
@@ -296,7 +316,7 @@ def run_ours(args, world, rank, local):
 
     def step():
         ctx.run(d_logits, d_ids, d_q, d_cu, d_T, d_g, b.seed, req_index_base=base,
-                max_spec_len=kmax, out=outs, draft_logits=d_dl)
+                max_spec_len=kmax, out=outs, draft_logits=d_dl, **extras)
 
     for _ in range(args.warmup):
         step()
@@ -342,8 +362,8 @@ def run_ours(args, world, rank, local):
 
     # end to end through the host-buffer entry point: H2D of the inputs, verify, D2H of results
     e2e = None
-    if not args.no_e2e and d_dl is not None:
-        e2e = e2e_draft_logits(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist)
+    if not args.no_e2e and (d_dl is not None or extras):
+        e2e = e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist)
     elif not args.no_e2e:
         ctx.reserve_host_io()
         h_logits = torch.from_numpy(logits_np).pin_memory()
@@ -396,9 +416,13 @@ def run_ours(args, world, rank, local):
     stats_bytes = b.num_rows * V * b.elem_bytes + (b.num_rows * V // 64) * b.elem_bytes
     if d_dl is not None:
         stats_bytes += nd * V * b.elem_bytes
+    if b.frequency_penalty is not None:    # every request's counts row read once
+        stats_bytes += n * V * 4
     achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
-    traffic, traffic_src = recorded_traffic(
-        "stats_kernel_workload3_draft_logits.md" if d_dl is not None else "stats_kernel_workload3.md")
+    plain = not extras and b.synthetic_rates is None
+    traffic, traffic_src = (recorded_traffic("stats_kernel_workload3_draft_logits.md" if d_dl is not None
+                                             else "stats_kernel_workload3.md")
+                            if plain and args.workload == 3 else (None, "no ncu summary for this mode"))
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         v, desc, _ = time_oracle(args, args.cpu_seconds)
@@ -435,24 +459,41 @@ def run_ours(args, world, rank, local):
         dist.destroy_process_group()
 
 
-def e2e_draft_logits(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist):
-    """End to end in the draft-logits mode through SpecVerify.run: every step copies the target
-    and draft logits and the small per-request arrays from page-locked host memory into the
-    device buffers, verifies, and reads the results back (host wall clock, stream synchronised)."""
+def e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist):
+    """End to end through SpecVerify.run (draft-logits mode, logits processors): every step
+    copies the step's inputs (logits, draft logits or probabilities, the per-request arrays and
+    the processors' inputs) from page-locked host memory into device buffers, verifies, and
+    reads the results back (host wall clock, stream synchronised)."""
     import numpy as np
     import torch
 
     n, nd = b.num_reqs, b.num_draft_tokens
-    host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-            for a in (logits_np, dl_np, b.draft_ids, b.cu_num_draft, b.temperature, b.is_greedy)]
+    names = ["logits", "draft_ids", "cu_num_draft", "temperature", "is_greedy"]
+    arrays = [logits_np, b.draft_ids, b.cu_num_draft, b.temperature, b.is_greedy]
+    if dl_np is not None:
+        names.append("draft_logits")
+        arrays.append(dl_np)
+    elif b.draft_probs is not None:
+        names.append("draft_probs")
+        arrays.append(b.draft_probs)
+    for name in ("frequency_penalty", "output_bin_counts", "counts_row", "top_k", "top_p"):
+        if getattr(b, name, None) is not None:
+            names.append(name)
+            arrays.append(getattr(b, name))
+    host = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory() for a in arrays]
     devb = [torch.empty_like(h, device=dev) for h in host]
     h_out = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    kw = dict(zip(names, devb))
 
     def e2e_step():
         for h, d in zip(host, devb):
             d.copy_(h, non_blocking=True)
-        ctx.run(devb[0], devb[2], None, devb[3], devb[4], devb[5], b.seed, req_index_base=base,
-                max_spec_len=kmax, out=outs, draft_logits=devb[1])
+        ctx.run(kw["logits"], kw["draft_ids"], kw.get("draft_probs"),
+                kw["cu_num_draft"], kw["temperature"], kw["is_greedy"], b.seed,
+                req_index_base=base, max_spec_len=kmax, out=outs,
+                **{k: v for k, v in kw.items() if k in ("draft_logits", "frequency_penalty",
+                                                         "output_bin_counts", "counts_row",
+                                                         "top_k", "top_p")})
         for h, o in zip(h_out, outs):
             h.copy_(o, non_blocking=True)
         torch.cuda.current_stream().synchronize()

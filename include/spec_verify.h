@@ -91,6 +91,7 @@ extern "C" {
 
 /* bits of the device error word */
 #define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
+#define SV_ERR_COUNTS 2u  /* a counts_row outside [0, counts_rows): that request got no penalty */
 
 typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
 
@@ -176,6 +177,33 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
  *                    in chunks. Such a request reports num_sampled = num_rejected = 0 and a
  *                    row of -1 ([MTP-eagle] get_num_sampled_and_rejected: the count correction
  *                    for chunked prefill); its row statistics are still written.
+ *   frequency_penalty [num_reqs] binary32, output_bin_counts [counts_rows, vocab_size] int32,
+ *                    counts_row [num_reqs] int32 or NULL (= request i): the frequency penalty
+ *                    ([MTP-eagle] 其他 / 重复惩罚: logit -= penalty * output_bin_counts[req],
+ *                    applied before the temperature and the softmax, [spec-notes] 8.2). At
+ *                    position j of request i the count of token v is
+ *                    c = output_bin_counts[counts_row[i], v] + #{k < j : draft_k == v} (the
+ *                    drafts before j are output the target conditions on there), and the
+ *                    processed logit is fma(-penalty, c, logit) (one rounding) where
+ *                    penalty != 0 and c != 0, the logit itself otherwise; x = processed / T.
+ *                    Greedy requests take the argmax of the processed logits; row_max /
+ *                    row_argmax report them. The draft logits are not penalised. Both
+ *                    frequency_penalty and output_bin_counts NULL: no penalty; one of them NULL
+ *                    or counts_rows < 1 with the other set: SV_EINVAL. A counts_row outside
+ *                    [0, counts_rows) gives that request no penalty and sets SV_ERR_COUNTS.
+ *   top_k [num_reqs] int32, top_p [num_reqs] binary32, each or NULL: sampling constraints
+ *                    applied to the processed logits before the softmax ([spec-notes] 8.2
+ *                    apply_sampling_constraints; [mini-sglang]: top_k < 1 means the whole
+ *                    vocabulary, top_p at most 1 and taken as at least 1e-6). For a sampling
+ *                    request, with x sorted from the largest, top-k (1 <= k < V) keeps every
+ *                    token at least the k-th largest value (ties kept); top-p (P < 1) then keeps,
+ *                    among those, every token whose strictly larger tokens hold less than P of
+ *                    their mass exp(x - m). p' = p on the kept set, renormalised, replaces p in
+ *                    the acceptance test, the residual and every draw; row_sumexp reports the
+ *                    kept mass. top_k == 1 makes the request greedy; greedy requests ignore
+ *                    both. The kept masses are summed in binary32 (hardware exp2), so a top-p
+ *                    boundary within about 1e-6 of the total may fall either way. These calls
+ *                    launch one more kernel; spec_verify_run_noalloc does not take them.
  */
 typedef struct spec_verify_batch {
     const void *logits;
@@ -186,11 +214,17 @@ typedef struct spec_verify_batch {
     const float *temperature;
     const uint8_t *is_greedy;
     const uint8_t *partial_prefill;
+    const float *frequency_penalty;
+    const int32_t *output_bin_counts;
+    const int32_t *counts_row;
+    const int32_t *top_k;
+    const float *top_p;
     uint64_t seed;
     uint32_t req_index_base;
     int32_t num_reqs;
     int32_t num_draft_tokens;
     int32_t max_spec_len_this_batch;
+    int32_t counts_rows;
 } spec_verify_batch;
 
 /* Outputs of one batch (device pointers): sampled, num_sampled, num_rejected as in
@@ -267,12 +301,13 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
 int spec_verify_last_error(spec_verify_ctx *ctx, uint32_t *err_word);
 
 /*
- * Kernel timing. With enable != 0, each later spec_verify_run records CUDA events around its
- * kernels on the call's stream. spec_verify_get_profile waits for the recorded work and
- * returns, per kernel (0 = row statistics, 1 = verify: acceptance, race and emit), the summed
- * milliseconds in ms[0..1] (ms holds spec_verify_launches_per_run() entries) and the number of
- * timed calls in *calls, then resets the sums.
+ * Kernel timing. With enable != 0, each later call records CUDA events around its kernels on
+ * the call's stream. spec_verify_get_profile waits for the recorded work and returns, per
+ * kernel, the summed milliseconds in ms[0 .. SV_PROFILE_SLOTS): 0 = row statistics, 1 = verify
+ * (acceptance, race and emit), 2 = the top-k / top-p selection (0 in calls without it); and the
+ * number of timed calls in *calls, then resets the sums.
  */
+#define SV_PROFILE_SLOTS 3
 int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable);
 int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls);
 
@@ -282,7 +317,8 @@ int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls);
  * not depend on it (S, a sum, up to rounding). */
 int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk);
 
-/* Number of kernel launches one spec_verify_run makes for a non-empty batch. */
+/* Number of kernel launches one call makes for a non-empty batch without top_k / top_p (one
+ * more, the selection kernel, with them). */
 int spec_verify_launches_per_run(void);
 
 /*

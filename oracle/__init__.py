@@ -26,7 +26,8 @@ class _Options(ctypes.Structure):
     _fields_ = [("synthetic_rates", ctypes.c_void_p), ("num_synthetic_rates", ctypes.c_int32),
                 ("partial_prefill", ctypes.c_void_p), ("frequency_penalty", ctypes.c_void_p),
                 ("output_bin_counts", ctypes.c_void_p), ("counts_row", ctypes.c_void_p),
-                ("top_k", ctypes.c_void_p), ("top_p", ctypes.c_void_p),
+                ("counts_rows", ctypes.c_int32), ("top_k", ctypes.c_void_p),
+                ("top_p", ctypes.c_void_p),
                 ("row_select_margin", ctypes.c_void_p)]
 EBATCH = 1
 
@@ -246,6 +247,8 @@ def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_ov
     opts.frequency_penalty = _opt("frequency_penalty", np.float32)
     opts.output_bin_counts = _opt("output_bin_counts", np.int32)
     opts.counts_row = _opt("counts_row", np.int32)
+    if getattr(batch, "output_bin_counts", None) is not None:
+        opts.counts_rows = int(np.asarray(batch.output_bin_counts).shape[0])
     opts.top_k = _opt("top_k", np.int32)
     opts.top_p = _opt("top_p", np.float32)
     out["row_select_margin"] = np.empty(max(R, 1), dtype=np.float64)

@@ -192,9 +192,10 @@ enum { REF_RACE_NONE = 0, REF_RACE_RESIDUAL = 1, REF_RACE_EXCLUDE = 2, REF_RACE_
  *   partial_prefill: [num_reqs] or NULL; a request still in a chunked prefill reports no
  *       token ([MTP-eagle] get_num_sampled_and_rejected: the count correction for chunked
  *       prefill).
- *   frequency_penalty [num_reqs], output_bin_counts [rows x V] with counts_row [num_reqs]
- *       (the counts row of each request; NULL = row i): the frequency penalty (see
- *       processed_row). Either pointer NULL: no penalty.
+ *   frequency_penalty [num_reqs], output_bin_counts [counts_rows x V] with counts_row
+ *       [num_reqs] (the counts row of each request; NULL = row i): the frequency penalty (see
+ *       processed_row). Either pointer NULL: no penalty; a counts row outside
+ *       [0, counts_rows): no penalty for that request.
  *   top_k [num_reqs] int32, top_p [num_reqs] binary32, each or NULL: sampling constraints of
  *       sampling requests (see select_row). top_k == 1 makes a request greedy.
  *   row_select_margin [rows] (output, NULL to skip): the top-p decision margin of each row. */
@@ -205,6 +206,7 @@ typedef struct {
     const float *frequency_penalty;
     const int32_t *output_bin_counts;
     const int32_t *counts_row;
+    int32_t counts_rows;
     const int32_t *top_k;
     const float *top_p;
     double *row_select_margin;
@@ -488,12 +490,11 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
          * top_k == 1 keeps only the largest logit) */
         const int greedy = is_greedy[i] != 0 || !(T > 0.0f) || top_k == 1;
         const float invT = greedy ? 1.0f : 1.0f / T;
-        const int pen = opts && opts->frequency_penalty && opts->output_bin_counts;
+        const int32_t crow = opts && opts->counts_row ? opts->counts_row[i] : i;
+        const int pen = opts && opts->frequency_penalty && opts->output_bin_counts && crow >= 0 &&
+                        crow < opts->counts_rows;
         const float f = pen ? opts->frequency_penalty[i] : 0.0f;
-        const int32_t *counts =
-            pen ? opts->output_bin_counts +
-                      (size_t)(opts->counts_row ? opts->counts_row[i] : i) * (size_t)V
-                : NULL;
+        const int32_t *counts = pen ? opts->output_bin_counts + (size_t)crow * (size_t)V : NULL;
 
         /* processed logits and stats of every row (rows after a rejection are reported too,
          * for inspection); row j conditions on the drafts before it */

@@ -38,9 +38,12 @@ class Batch(ctypes.Structure):
                 ("draft_probs", ctypes.c_void_p), ("draft_logits", ctypes.c_void_p),
                 ("cu_num_draft", ctypes.c_void_p), ("temperature", ctypes.c_void_p),
                 ("is_greedy", ctypes.c_void_p), ("partial_prefill", ctypes.c_void_p),
+                ("frequency_penalty", ctypes.c_void_p), ("output_bin_counts", ctypes.c_void_p),
+                ("counts_row", ctypes.c_void_p), ("top_k", ctypes.c_void_p),
+                ("top_p", ctypes.c_void_p),
                 ("seed", ctypes.c_uint64), ("req_index_base", ctypes.c_uint32),
                 ("num_reqs", ctypes.c_int32), ("num_draft_tokens", ctypes.c_int32),
-                ("max_spec_len_this_batch", ctypes.c_int32)]
+                ("max_spec_len_this_batch", ctypes.c_int32), ("counts_rows", ctypes.c_int32)]
 
 
 class Outputs(ctypes.Structure):
@@ -48,8 +51,8 @@ class Outputs(ctypes.Structure):
     _fields_ = [("sampled", ctypes.c_void_p), ("num_sampled", ctypes.c_void_p),
                 ("num_rejected", ctypes.c_void_p), ("row_max", ctypes.c_void_p),
                 ("row_sumexp", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p)]
-SV_ERR_BATCH = 1
-KERNELS = ("stats", "verify")
+SV_ERR_BATCH, SV_ERR_COUNTS = 1, 2
+KERNELS = ("stats", "verify", "select")  # profiling slots (select: top-k / top-p calls)
 
 _lib = None
 
@@ -337,14 +340,19 @@ class SpecVerify:
 
     def run(self, logits, draft_ids, draft_probs, cu_num_draft, temperature, is_greedy, seed: int,
             *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
-            row_stats: bool = False, stream=None, draft_logits=None, partial_prefill=None):
+            row_stats: bool = False, stream=None, draft_logits=None, partial_prefill=None,
+            frequency_penalty=None, output_bin_counts=None, counts_row=None, top_k=None,
+            top_p=None):
         """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
         and, with row_stats=True, also (row_max, row_sumexp, row_argmax).
 
         draft_logits ([num_draft_tokens, vocab_size], the logits' dtype) replaces draft_probs:
         q is then computed inside the call (context created with draft_logits=True).
         partial_prefill ([num_reqs] uint8): requests still in a chunked prefill, which report
-        no token (spec_verify_run_batch)."""
+        no token. frequency_penalty ([num_reqs] float32) with output_bin_counts ([rows, V]
+        int32) and counts_row ([num_reqs] int32, optional): the frequency penalty. top_k
+        ([num_reqs] int32), top_p ([num_reqs] float32): sampling constraints. Any of these
+        goes through spec_verify_run_batch."""
         import torch
         num_reqs = cu_num_draft.numel() - 1
         nd = draft_ids.numel()
@@ -368,10 +376,17 @@ class SpecVerify:
             stats = (torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.int32, device=dev))
-        if partial_prefill is not None:
+        extras = (partial_prefill, frequency_penalty, output_bin_counts, counts_row, top_k, top_p)
+        if any(x is not None for x in extras):
+            if output_bin_counts is not None and (output_bin_counts.dim() != 2
+                                                  or output_bin_counts.shape[1] != self.vocab_size):
+                raise ValueError("output_bin_counts must be [rows, vocab_size]")
             b = Batch(_ptr(logits), _ptr(draft_ids), _ptr(draft_probs), _ptr(draft_logits),
                       _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy),
-                      _ptr(partial_prefill), seed, req_index_base, num_reqs, nd, kmax)
+                      _ptr(partial_prefill), _ptr(frequency_penalty), _ptr(output_bin_counts),
+                      _ptr(counts_row), _ptr(top_k), _ptr(top_p), seed, req_index_base,
+                      num_reqs, nd, kmax,
+                      output_bin_counts.shape[0] if output_bin_counts is not None else 0)
             o = Outputs(*(_ptr(t) for t in (*out, *stats)))
             spec_verify_run_batch(self.ctx, b, o, cuda_stream=stream)
         elif draft_logits is not None:

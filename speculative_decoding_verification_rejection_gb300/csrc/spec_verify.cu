@@ -150,13 +150,81 @@ __device__ __forceinline__ int row_request(const int32_t *__restrict__ cu, int n
 }
 
 // 1 / T of request i, or 1 for a greedy request (flag set, or !(T > 0)).
-__device__ __forceinline__ float request_invT(const float *__restrict__ temperature,
-                                              const uint8_t *__restrict__ is_greedy, int i,
-                                              bool &greedy)
+struct RequestTable {
+    const int32_t *cu;
+    const float *temperature;
+    const uint8_t *is_greedy;
+    const int32_t *top_k;  // or nullptr; top_k == 1 keeps only the largest logit: greedy
+    int n;
+};
+
+// 1 / T of request i, 1 for a greedy request: flag set, T <= 0 ([spec-in-vllm] 7.0.1;
+// [mini-sglang] T <= 0) or top_k == 1 ([mini-sglang]: only the largest logit is kept).
+__device__ __forceinline__ float request_invT(const RequestTable &rq, int i, bool &greedy)
 {
-    const float T = __ldg(temperature + i);
-    greedy = __ldg(is_greedy + i) != 0 || !(T > 0.0f);
+    const float T = __ldg(rq.temperature + i);
+    greedy = __ldg(rq.is_greedy + i) != 0 || !(T > 0.0f) || (rq.top_k && __ldg(rq.top_k + i) == 1);
     return greedy ? 1.0f : __frcp_rn(T);
+}
+
+// ---------------------------------------------------------------------------------------
+// logits processors: the frequency penalty ([MTP-eagle] 其他 / 重复惩罚: logit -= penalty *
+// output_bin_counts), applied before the temperature and the softmax ([spec-notes] 8.2)
+// ---------------------------------------------------------------------------------------
+struct PenTable {
+    const float *f;             // [n] frequency penalty, or nullptr (no penalty)
+    const int32_t *counts;      // [counts_rows, V] output token counts
+    const int32_t *counts_row;  // [n] counts row of each request, or nullptr (row i)
+    int counts_rows;
+};
+
+// The penalty of one logit row: y_v = fma(-f, c_v, l_v) where f != 0 and c_v != 0, else l_v;
+// c_v = the request's count of v plus the drafts before this position equal to v (the target
+// conditions on them there).
+struct PenRow {
+    float f;               // 0: no penalty
+    const int32_t *cnt;    // the request's counts row
+    const int32_t *prev;   // drafts before this position
+    int nprev;
+};
+
+// Request i, position j (drafts from q0). A counts row outside [0, counts_rows) gives no penalty
+// (and is reported by the verify kernel).
+__device__ __forceinline__ PenRow pen_row(const PenTable &pt, const int32_t *draft_ids, int i,
+                                          int q0, int j, int V)
+{
+    PenRow r{0.0f, nullptr, nullptr, 0};
+    if (!pt.f) return r;
+    const int crow = pt.counts_row ? __ldg(pt.counts_row + i) : i;
+    if (crow < 0 || crow >= pt.counts_rows) return r;
+    r.f = __ldg(pt.f + i);
+    r.cnt = pt.counts + static_cast<size_t>(crow) * V;
+    r.prev = draft_ids + q0;
+    r.nprev = j;
+    return r;
+}
+
+__device__ __forceinline__ bool pen_counts_row_bad(const PenTable &pt, int i)
+{
+    if (!pt.f) return false;
+    const int crow = pt.counts_row ? __ldg(pt.counts_row + i) : i;
+    return crow < 0 || crow >= pt.counts_rows;
+}
+
+__device__ __forceinline__ float pen_apply(const PenRow &r, float l, int v)
+{
+    if (r.f == 0.0f) return l;
+    int c = __ldg(r.cnt + v);
+    for (int k = 0; k < r.nprev; ++k) c += __ldg(r.prev + k) == v;
+    return c == 0 ? l : __fmaf_rn(-r.f, __int2float_rn(c), l);
+}
+
+// bf16 upper bound of an fp32 value (rounded toward +inf), for line maxima of penalised rows.
+__device__ __forceinline__ uint16_t bf16_round_up(float v)
+{
+    const uint32_t u = __float_as_uint(v);
+    if ((u & 0xFFFFu) == 0u || v != v) return static_cast<uint16_t>(u >> 16);
+    return static_cast<uint16_t>((u >> 31) ? (u >> 16) : (u >> 16) + 1u);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -332,6 +400,71 @@ __device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16]
     st.s += (a0 + b0) + (a1 + b1);
 }
 
+// fold_pair over values already processed (the penalty path): the same steps on y[0..n).
+template <int n>
+__device__ __forceinline__ void fold_vals(OnlineMax &st, const float (&y)[n], int p, float c,
+                                          float mx)
+{
+    const bool up = mx > st.L;
+    st.s *= sv::ex2_approx(up ? (st.L - mx) * c : 0.0f);
+    st.best_p = up ? p : st.best_p;
+    st.best_e = up ? -1 : st.best_e;
+    st.L = up ? mx : st.L;
+    st.Lc = st.L > -kInf ? st.L * c : 0.0f;
+    const unsigned long long c2 = f2_pack(c, c), nLc2 = f2_pack(-st.Lc, -st.Lc);
+    unsigned long long acc[2] = {0ull, 0ull};
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(y[2 * k], y[2 * k + 1]), c2, nLc2), y0, y1);
+        acc[k & 1] = f2_add(acc[k & 1], f2_pack(sv::ex2_approx(y0), sv::ex2_approx(y1)));
+    }
+    float a0, a1, b0, b1;
+    f2_unpack(acc[0], a0, a1);
+    f2_unpack(acc[1], b0, b1);
+    st.s += (a0 + b0) + (a1 + b1);
+}
+
+// The processed values of a pair whose first element is token v0 of a penalised row: counts as
+// 16-byte vectors where aligned (the same for every pair of a segment), the earlier drafts added
+// where one falls in the pair (rare).
+template <typename T>
+__device__ __forceinline__ void pen_pair(const PenRow &pr, const uint32_t (&w)[16], int v0,
+                                         bool aligned, float (&y)[kPairBytes / sizeof(T)])
+{
+    constexpr int kPE = kPairBytes / sizeof(T);
+    int c[kPE];
+    if (aligned) {
+        const int4 *cp = reinterpret_cast<const int4 *>(pr.cnt + v0);
+#pragma unroll
+        for (int q = 0; q < kPE / 4; ++q) {
+            const int4 t = __ldg(cp + q);
+            c[4 * q] = t.x;
+            c[4 * q + 1] = t.y;
+            c[4 * q + 2] = t.z;
+            c[4 * q + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < kPE; ++e) c[e] = __ldg(pr.cnt + v0 + e);
+    }
+    bool hit = false;
+    for (int k = 0; k < pr.nprev; ++k)
+        hit |= static_cast<unsigned>(__ldg(pr.prev + k) - v0) < static_cast<unsigned>(kPE);
+    if (hit) {
+        for (int k = 0; k < pr.nprev; ++k) {
+            const int d = __ldg(pr.prev + k) - v0;
+#pragma unroll
+            for (int e = 0; e < kPE; ++e) c[e] += d == e;
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < kPE; ++e) {
+        const float l = pair_elem<T>(w, e);
+        y[e] = c[e] == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(c[e]), l);
+    }
+}
+
 // Division by a launch constant d > 0 without a division instruction: with M = ceil(2^64 / d)
 // (0 stands for d = 1), floor(a * M / 2^64) is floor(a / d) or one more for 0 <= a < 2^63, and
 // one multiply decides which.
@@ -426,13 +559,6 @@ __device__ __forceinline__ void warp_reduce_stat(float &L, float &s, int &idx, f
     }
 }
 
-struct RequestTable {
-    const int32_t *cu;
-    const float *temperature;
-    const uint8_t *is_greedy;
-    int n;
-};
-
 // Segment [b, e) of row `row`, by the whole CTA without any barrier: the elements before the
 // first 64-element line boundary one by one, then 64-byte pairs, one per lane and round, then the
 // last few elements one by one. Every warp looks the row's request up itself (while its first
@@ -469,8 +595,7 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     if (ub + lane + kThreads < npair)
         ldg_pair(pbase + static_cast<size_t>(ub + lane + kThreads) * kPairBytes, w1);
     bool greedy;
-    const float c = request_invT(rq.temperature, rq.is_greedy,
-                                 row_request(rq.cu, rq.n, row, lane, draft_rows), greedy) * kLog2e;
+    const float c = request_invT(rq, row_request(rq.cu, rq.n, row, lane, draft_rows), greedy) * kLog2e;
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
@@ -511,6 +636,74 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
         part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
 }
 
+// stats_segment for a penalised row: the same partials over the processed values y (see
+// PenRow), and line maxima rounded up to the logits' type (an upper bound of the line's y).
+// c = (1 / T) log2(e) of the row's request.
+template <typename T>
+__device__ __noinline__ void stats_segment_pen(const T *__restrict__ logits, int V, int row, int b,
+                                               int e, int seg, int maxseg, int base_off, float c,
+                                               const PenRow &pr, StatPart *__restrict__ part,
+                                               T *__restrict__ s_lines, long long line_base)
+{
+    const long long rbase = static_cast<long long>(row) * V;
+    const T *rp = logits + rbase;
+    constexpr int kPE = kPairBytes / sizeof(T);
+    constexpr int kPPL = PairMax<T>::kLanes;
+    const long long pos_b = base_off + rbase + b;
+    const int head = static_cast<int>((kGroup - (pos_b & (kGroup - 1))) & (kGroup - 1));
+    const int a0 = min(e, b + head);
+    const int npair = (e - a0) / kPE;
+    const int a1 = a0 + npair * kPE;
+    const char *pbase = reinterpret_cast<const char *>(rp + a0);
+    const int line0 = static_cast<int>(((pos_b + (a0 - b)) >> 6) - line_base);
+    const int lane = threadIdx.x & 31;
+    const bool aligned = (reinterpret_cast<uintptr_t>(pr.cnt + a0) & 15u) == 0u;
+
+    OnlineMax st;
+    for (int ee = b + threadIdx.x; ee < a0; ee += kThreads)
+        fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
+    for (int ub = static_cast<int>(threadIdx.x) & ~31; ub < npair; ub += kThreads) {
+        const int p = ub + lane;
+        const bool valid = p < npair;
+        float y[kPE];
+        float mx = -kInf;
+        if (valid) {
+            uint32_t w[16];
+            ldg_pair(pbase + static_cast<size_t>(p) * kPairBytes, w);
+            pen_pair<T>(pr, w, a0 + p * kPE, aligned, y);
+#pragma unroll
+            for (int k = 0; k < kPE; ++k) mx = fmaxf(mx, y[k]);
+        }
+        if (s_lines) {
+            float lm = mx;
+#pragma unroll
+            for (int o = 1; o < kPPL; o <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
+            if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair) {
+                if constexpr (sizeof(T) == 2) s_lines[line0 + p / kPPL] = bf16_round_up(lm);
+                else s_lines[line0 + p / kPPL] = lm;
+            }
+        }
+        if (valid) fold_vals<kPE>(st, y, p, c, mx);
+    }
+    for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads)
+        fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
+
+    int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
+    if (st.best_p >= 0) {
+        uint32_t w[16];
+        float y[kPE];
+        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w);
+        pen_pair<T>(pr, w, a0 + st.best_p * kPE, aligned, y);
+#pragma unroll
+        for (int h = kPE - 1; h >= 0; --h)
+            if (y[h] == st.L) idx = a0 + st.best_p * kPE + h;
+    }
+    float L = st.L, s = st.s;
+    warp_reduce_stat(L, s, idx, c);
+    if (lane == 0)
+        part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
+}
+
 // One [rows x V] array the statistics kernel streams: the target logits, or the draft logits of
 // the draft-logits mode (rows = draft tokens, each belonging to the request that drafted it).
 template <typename T>
@@ -534,9 +727,11 @@ struct StatsArray {
 // covers only in part are left undefined (the verify kernel reads those lines from the logits).
 // The first A.grid CTAs take the target logits, the rest the draft logits (if any). Nothing waits
 // on another CTA.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 3)
-sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTable rq)
+// kPen: the batch has a frequency penalty (penalised rows take stats_segment_pen).
+template <typename T, bool kPen>
+__global__ void __launch_bounds__(kThreads, kPen ? 2 : 3)
+sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTable rq,
+                PenTable pt, const int32_t *__restrict__ draft_ids)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     const bool second = static_cast<int>(blockIdx.x) >= A.grid;
@@ -554,6 +749,20 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
         const int fk = static_cast<int>(div_floor(X.base_off + rbase, X.chunk));
+        if constexpr (kPen) {
+            if (!X.draft_rows) {  // penalties act on the target logits only
+                const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31);
+                const int q0 = __ldg(rq.cu + i);
+                const PenRow pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
+                if (pr.f != 0.0f) {
+                    bool greedy;
+                    const float c = request_invT(rq, i, greedy) * kLog2e;
+                    stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c,
+                                         pr, X.part, s_lines, line_base);
+                    continue;
+                }
+            }
+        }
         stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part, s_lines,
                          line_base, X.draft_rows != 0);
     }
@@ -591,6 +800,10 @@ struct VerifyParams {
     int32_t *opt_amax;
     unsigned *flags;
     const uint8_t *partial;      // [n] requests in a chunked prefill, or nullptr
+    PenTable pen;                // frequency penalty (pen.f == nullptr: none)
+    const float *top_p;          // [n] or nullptr (top_k is in rq)
+    const float *sel_tau;        // [rows] thresholds of constrained rows (nullptr: none)
+    const float *sel_S;          // [rows] their kept mass
     int nsyn;                    // synthetic acceptance: rates of positions < nsyn (0 = off)
     float syn[SV_MAX_SYNTHETIC]; // unconditional rate a_j of position j
 };
@@ -619,7 +832,8 @@ __device__ __forceinline__ bool accept_synthetic(const VerifyParams &P, int j, i
 // target_prob / draft_prob >= uniform; greedy: d == argmax, [spec-notes] 8.3). One thread.
 template <typename T>
 __device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, int j, int qrow,
-                                             float invT, float m, float S, int amax,
+                                             const PenRow &pr, float invT, float m, float S,
+                                             float tau, int amax,
                                              const int32_t *__restrict__ draft_ids,
                                              const float *__restrict__ q, const T *__restrict__ dl,
                                              float md, float Sd, uint64_t seed, uint32_t ireq)
@@ -627,8 +841,9 @@ __device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, in
     const int d = __ldg(draft_ids + qrow);
     if (greedy) return d == amax;
     if (d < 0 || d >= V) return false;
-    const float x_d = __fmul_rn(Elem<T>::at(rp, d), invT);
-    const float t_d = sv::exp_f32(__fsub_rn(x_d, m));
+    const float x_d = __fmul_rn(pen_apply(pr, Elem<T>::at(rp, d), d), invT);
+    // p' of the constrained target: 0 outside the kept set, S the kept mass
+    const float t_d = x_d >= tau ? sv::exp_f32(__fsub_rn(x_d, m)) : 0.0f;
     const float p_d = __fdiv_rn(t_d, S);
     float q_d = 1.0f;
     if (q) {
@@ -670,9 +885,10 @@ __device__ __forceinline__ RowLines row_lines(long long row, int V, int base_off
 // lm[k] = largest raw logit of the row on line L0 + k (the row's own elements only). The lines
 // inside the row come from `lines` (written by the statistics kernel) or, without it, from
 // coalesced 16-byte loads of the row; a partial first / last line is read by warp 0 / 1.
-template <typename T>
+template <typename T, bool kPen>
 __device__ void row_line_max(const T *__restrict__ rp, int V, const RowLines &rl,
-                             const T *__restrict__ lines, float *__restrict__ lm)
+                             const T *__restrict__ lines, float *__restrict__ lm,
+                             const PenRow &pr)
 {
     constexpr int kVPL = VecMax<T>::kLanes;  // vectors per line
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -709,7 +925,10 @@ __device__ void row_line_max(const T *__restrict__ rp, int V, const RowLines &rl
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const long long v = p + h * 32 + lane - rl.P0;  // token of the row
-            if (v >= 0 && v < V) mx = fmaxf(mx, Elem<T>::at(rp, static_cast<size_t>(v)));
+            if (v >= 0 && v < V) {
+                const float l = Elem<T>::at(rp, static_cast<size_t>(v));
+                mx = fmaxf(mx, kPen ? pen_apply(pr, l, static_cast<int>(v)) : l);
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
@@ -723,6 +942,8 @@ struct RaceRow {
     const T *rp;        // logits row
     const float *qrow;  // draft distribution row (residual race) or nullptr
     const T *dlrow;     // draft logits row (residual race in draft-logits mode) or nullptr
+    PenRow pr;          // the row's frequency penalty
+    float tau;          // kept tokens: x >= tau (sampling constraints; -inf: all)
     float md, Sd;       // its max and sum of exponentials
     int V, G;           // vocabulary, groups
     int excl;           // token left out (rejected draft without q), or -1
@@ -771,7 +992,7 @@ __host__ __device__ inline VerifyLayout verify_layout(int V, int kmax)
     const size_t buf = 8 * sp > 4 * (G + 2) ? 8 * sp : 4 * (G + 2);
     l.tmp = (buf + 15) / 16 * 16;
     l.rows = l.tmp + 8 * sp;
-    l.pb = l.rows + 20 * (static_cast<size_t>(kmax) + 1);
+    l.pb = l.rows + 24 * (static_cast<size_t>(kmax) + 1);  // m, S, argmax, m_d, S_d, tau
     l.ew = l.pb + 4 * G;
     l.ag = l.ew + 4 * G;
     l.total = l.ag + G;
@@ -896,7 +1117,7 @@ __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 // at most exp(x - m), and the residual's fma is monotone in it). The queue is emptied through
 // flush_queue whenever it holds 32 tokens; qn is its length. In draft-logits mode q_v is bounded
 // from below the same way (hardware ex2 and a reciprocal of S_d, with margins).
-template <typename T, bool kRes, bool kDL, int B>
+template <typename T, bool kRes, bool kDL, bool kPen, int B>
 __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm,
                                             int &qn)
 {
@@ -908,7 +1129,8 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
         for (int h = 0; h < 2; ++h) {
             const int v = gs[k] * kGroup + 2 * lane + h;
             const bool in = gs[k] >= 0 && v < r.V;
-            l[k][h] = in ? Elem<T>::at(r.rp, v) : -kInf;
+            const float raw = in ? Elem<T>::at(r.rp, v) : -kInf;
+            l[k][h] = kPen && in ? pen_apply(r.pr, raw, v) : raw;
             qv[k][h] = 0.0f;
             if constexpr (kRes && kDL) qv[k][h] = in ? Elem<T>::at(r.dlrow, v) : 0.0f;
             else if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
@@ -925,7 +1147,8 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int v = g * kGroup + 2 * lane + h;
-            const float y = __fsub_rn(__fmul_rn(l[k][h], r.invT), r.m);
+            const float xv = __fmul_rn(l[k][h], r.invT);
+            const float y = __fsub_rn(xv, r.m);
             const float t_ub = sv::ex2_approx(y * kLog2e) * (1.0f + 0x1p-12f);
             float q_lb = qv[k][h];
             if constexpr (kDL) {
@@ -934,7 +1157,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
                 q_lb = yd >= -87.0f ? sv::ex2_approx(yd * kLog2e) * (1.0f - 0x1p-12f) * inv_sd : 0.0f;
             }
             const float w_ub = kRes ? __fmaf_rn(-r.S, q_lb, t_ub) : t_ub;
-            bool take = v < r.V && (kRes ? w_ub > 0.0f : v != r.excl);
+            bool take = v < r.V && (kRes ? w_ub > 0.0f : v != r.excl) && xv >= r.tau;
             if (take && cur != 0) {
                 const float kb = w_ub * inv * (1.0f + 0x1p-12f);
                 take = !(kb == kb) || key_enc(kb) >= thr;  // NaN bounds are kept
@@ -966,7 +1189,7 @@ __device__ __forceinline__ int bound_bin(unsigned kb, float top, float inv_w)
 
 // Best-first race over one row by the whole CTA. Returns the packed winner (key, ~v), 0 when no
 // token is a candidate. lm must hold the row's line maxima (it is overwritten).
-template <typename T, bool kRes, bool kDL = false>
+template <typename T, bool kRes, bool kDL, bool kPen>
 __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &rl,
                                           const SearchSmem &sm)
 {
@@ -989,7 +1212,7 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
     if (wb != 0) {
         const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
         int qn = 0;
-        eval_groups<T, kRes, kDL, 1>(r, gs, sm, qn);
+        eval_groups<T, kRes, kDL, kPen, 1>(r, gs, sm, qn);
         flush_queue<T, kRes, kDL>(r, sm, qn);
         if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
     }
@@ -1065,7 +1288,7 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
                 }
             }
         }
-        eval_groups<T, kRes, kDL, B>(r, gs, sm, qn);
+        eval_groups<T, kRes, kDL, kPen, B>(r, gs, sm, qn);
         if (qn > 0) {  // keys now: the best key prunes the next groups
             flush_queue<T, kRes, kDL>(r, sm, qn);
             qn = 0;
@@ -1097,9 +1320,440 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
     warp_reduce_stat(L, s, idx, c);
 }
 
-// One CTA per request. kDLMode: q comes from draft logits (P.dl), a separate instantiation so
-// that the other modes do not carry its registers.
-template <typename T, bool kDLMode>
+// ---------------------------------------------------------------------------------------
+// 3. sampling constraints: top-k / top-p of one row ([spec-notes] 8.2
+//    apply_sampling_constraints; [mini-sglang] "how tokens are sampled")
+// ---------------------------------------------------------------------------------------
+// The kept tokens of a constrained row are {x_v >= tau}:
+//   top-k: tau_k = the k-th largest x (ties at it are kept), for 1 <= k < V;
+//   top-p: among those, every token whose strictly larger tokens hold less than P * Z of the
+//          mass t_v = exp(x_v - m), Z the mass of the top-k set, for P < 1 (at least 1e-6).
+// One CTA per row finds tau without sorting the row: a histogram of count and mass over 256 bins
+// of 1/8 nat below the row maximum (one pass over the row); then the bin where the k-th token or
+// the P * Z mass falls is refined on the order-preserving integer key of x, 8 bits per level,
+// over the row (from L2) until its tokens fit in shared memory, then over those, down to a
+// single value (a group of equal values is kept or dropped as a whole). Masses come from the
+// hardware ex2, summed in fp32.
+constexpr int kSelBins = 256;
+constexpr int kSelPool = 2048;
+constexpr float kSelBinsPerNat = 8.0f;
+static_assert(kSelBins == kThreads, "one histogram bin per thread");
+
+struct SelectParams {
+    RequestTable rq;
+    PenTable pen;
+    const int32_t *draft_ids;
+    const int32_t *top_k;
+    const float *top_p;
+    const StatPart *part;
+    int V, maxseg, base_off;
+    Divisor chunk;
+    float *sel_tau;  // [rows] threshold of each constrained row
+    float *sel_S;    // [rows] its kept mass: the normaliser of p'
+};
+
+// Does request i sample under constraints? (k, P as given; greedy requests never do.)
+__device__ __forceinline__ bool sel_active(const int32_t *top_k, const float *top_p, int i, int V,
+                                           bool greedy, int &k, float &P)
+{
+    k = top_k ? __ldg(top_k + i) : 0;
+    P = top_p ? __ldg(top_p + i) : 1.0f;
+    return !greedy && ((k >= 1 && k < V) || P < 1.0f);
+}
+
+// Integer key in the order of the values; -0 takes the key of +0, so that equal values have
+// equal keys.
+__device__ __forceinline__ uint32_t ord_key(float x)
+{
+    const uint32_t u = x == 0.0f ? 0u : __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// Level-1 bin: 0 holds the values less than 1/8 nat below m, 255 everything from 31.875 down.
+__device__ __forceinline__ int sel_bin1(float x, float m)
+{
+    const float u = __fmul_rn(__fsub_rn(m, x), kSelBinsPerNat);
+    return u < 255.0f ? (u > 0.0f ? static_cast<int>(u) : 0) : 255;  // NaN: 255
+}
+__device__ __forceinline__ float sel_mass(float x, float m)
+{
+    return sv::ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
+}
+
+struct SelSmem {
+    uint32_t hc[kWarps][kSelBins];
+    float hm[kWarps][kSelBins];
+    float pool[kSelPool], pool2[kSelPool];
+    uint32_t wc[kWarps];
+    float wm[kWarps];
+    uint32_t kmin, kmax, n;
+    int cross;
+    uint32_t cabove;
+    float mabove;
+};
+
+// Every element of a row once, as x = processed logit * (1 / T), with its token index; 16-byte
+// loads over the aligned body.
+template <typename T, bool kPen, typename F>
+__device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, float invT,
+                                            const PenRow &pr, F &&f)
+{
+    constexpr int kEV = 16 / static_cast<int>(sizeof(T));
+    const int head = min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rp) & 15u)) & 15u) / sizeof(T)));
+    auto proc = [&](float l, int v) { return __fmul_rn(kPen ? pen_apply(pr, l, v) : l, invT); };
+    for (int v = threadIdx.x; v < head; v += kThreads) f(proc(Elem<T>::at(rp, v), v), v);
+    const int nvec = (V - head) / kEV;
+    const char *base = reinterpret_cast<const char *>(rp + head);
+    for (int u = threadIdx.x; u < nvec; u += kThreads) {
+        const uint4 w = ldg_v4(base + static_cast<size_t>(u) * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int e = 0; e < kEV; ++e) {
+            float l;
+            if constexpr (sizeof(T) == 2)
+                l = __uint_as_float((e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16));
+            else
+                l = __uint_as_float(ws[e]);
+            const int v = head + u * kEV + e;
+            f(proc(l, v), v);
+        }
+    }
+    for (int v = head + nvec * kEV + threadIdx.x; v < V; v += kThreads)
+        f(proc(Elem<T>::at(rp, v), v), v);
+}
+
+__device__ __forceinline__ void sel_clear(SelSmem &sm)
+{
+    for (int w = 0; w < kWarps; ++w) {
+        sm.hc[w][threadIdx.x] = 0u;
+        sm.hm[w][threadIdx.x] = 0.0f;
+    }
+}
+
+// After the per-warp histograms are complete: merge them and find the crossing bin (bin 0 holds
+// the largest values). mode 0: the first bin where ca + count >= k; mode 1: the first bin where
+// ma + mass >= target (the last non-empty bin when rounding leaves the total short). Adds the
+// count / mass strictly above the crossing bin to ca / ma; returns the bin and its count.
+__device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32_t &ca,
+                         float &ma, uint32_t &cnt, float &bmass)
+{
+    const int b = threadIdx.x, lane = b & 31, warp = b >> 5;
+    uint32_t c = 0u;
+    float mm = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+        c += sm.hc[w][b];
+        mm += sm.hm[w][b];
+    }
+    // inclusive scan over the bins; excl(b) is exactly incl(b - 1)
+    uint32_t ci = c;
+    float mi = mm;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t c2 = __shfl_up_sync(0xFFFFFFFFu, ci, o);
+        const float m2 = __shfl_up_sync(0xFFFFFFFFu, mi, o);
+        if (lane >= o) {
+            ci += c2;
+            mi = m2 + mi;
+        }
+    }
+    const uint32_t cprev = __shfl_up_sync(0xFFFFFFFFu, ci, 1);
+    const float mprev = __shfl_up_sync(0xFFFFFFFFu, mi, 1);
+    if (lane == 31) {
+        sm.wc[warp] = ci;
+        sm.wm[warp] = mi;
+    }
+    if (b == 0) sm.cross = -1;
+    __syncthreads();
+    uint32_t coff = 0u;
+    float moff = 0.0f;
+    for (int w = 0; w < warp; ++w) {
+        coff += sm.wc[w];
+        moff = moff + sm.wm[w];
+    }
+    const uint32_t cin = ca + coff + ci, cex = ca + coff + (lane ? cprev : 0u);
+    const float min_ = ma + (moff + mi), mex = ma + (lane ? moff + mprev : moff);
+    const bool hit = mode == 0 ? (cex < k && cin >= k) : (mex < target && min_ >= target);
+    if (hit) {
+        sm.cross = b;
+        sm.cabove = cex;
+        sm.mabove = mex;
+    }
+    __syncthreads();
+    if (sm.cross < 0) {  // mode 1 short of the target: the last non-empty bin
+        const unsigned nz = __ballot_sync(0xFFFFFFFFu, c > 0u);
+        if (lane == 0) sm.wc[warp] = nz;
+        __syncthreads();
+        if (b == 0) {
+            for (int w = kWarps - 1; w >= 0; --w)
+                if (sm.wc[w]) {
+                    sm.cross = w * 32 + 31 - __clz(sm.wc[w]);
+                    break;
+                }
+        }
+        __syncthreads();
+        if (b == sm.cross) {
+            sm.cabove = cex;
+            sm.mabove = mex;
+        }
+        __syncthreads();
+    }
+    const int x = sm.cross;
+    ca = sm.cabove;
+    ma = sm.mabove;
+    uint32_t total = 0u;
+    float tm = 0.0f;
+    for (int w = 0; w < kWarps; ++w) {
+        total += sm.hc[w][x];
+        tm += sm.hm[w][x];
+    }
+    cnt = total;
+    bmass = tm;
+    __syncthreads();
+    return x;
+}
+
+// Key-level sub-bin of key kv in [klo, khi] with shift sh: 0 holds the largest keys.
+__device__ __forceinline__ int sel_sub(uint32_t kv, uint32_t khi, int sh)
+{
+    return static_cast<int>((khi - kv) >> sh);
+}
+// The key range of sub-bin sb of [klo, khi] with shift sh.
+__device__ __forceinline__ void sel_narrow(uint32_t &klo, uint32_t &khi, int sb, int sh)
+{
+    const uint32_t nhi = khi - (static_cast<uint32_t>(sb) << sh);
+    const uint32_t w = (1u << sh) - 1u;
+    klo = nhi - klo >= w ? nhi - w : klo;
+    khi = nhi;
+}
+__device__ __forceinline__ int sel_shift(uint32_t klo, uint32_t khi)
+{
+    const uint32_t r = khi - klo;
+    const int bits = r ? 32 - __clz(r) : 0;
+    return bits > 8 ? bits - 8 : 0;
+}
+
+// Resolve the crossing among the candidates: the row's tokens with x >= xmin and, if b1 >= 0,
+// level-1 bin b1 (count `cnt`), with ca / ma tokens strictly above them. Returns x*, the single
+// value where the goal crosses, with ca / ma = count / mass strictly above x* and gcnt / gmass
+// its group's.
+template <typename T, bool kPen>
+__device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float m,
+                             const PenRow &pr, int b1, float xmin, uint32_t cnt, float cmass,
+                             int mode, uint32_t k, float target, uint32_t &ca, float &ma,
+                             uint32_t &gcnt, float &gmass)
+{
+    const int warp = threadIdx.x >> 5;
+    auto in_set = [&](float x, uint32_t klo, uint32_t khi) {
+        const uint32_t kv = ord_key(x);
+        return x >= xmin && kv >= klo && kv <= khi && (b1 < 0 || sel_bin1(x, m) == b1);
+    };
+    uint32_t klo = 0u, khi = 0xFFFFFFFFu;
+    if (cnt > static_cast<uint32_t>(kSelPool)) {
+        // too many to collect: the key range of the candidates, then refine it over the row
+        if (threadIdx.x == 0) {
+            sm.kmin = 0xFFFFFFFFu;
+            sm.kmax = 0u;
+        }
+        __syncthreads();
+        uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+        sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+            if (in_set(x, 0u, 0xFFFFFFFFu)) {
+                const uint32_t kv = ord_key(x);
+                lo = min(lo, kv);
+                hi = max(hi, kv);
+            }
+        });
+        atomicMin(&sm.kmin, lo);
+        atomicMax(&sm.kmax, hi);
+        __syncthreads();
+        klo = sm.kmin;
+        khi = sm.kmax;
+        __syncthreads();
+    }
+    while (cnt > static_cast<uint32_t>(kSelPool) && klo < khi) {
+        const int sh = sel_shift(klo, khi);
+        sel_clear(sm);
+        __syncthreads();
+        sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+            if (in_set(x, klo, khi)) {
+                const int sb = sel_sub(ord_key(x), khi, sh);
+                atomicAdd(&sm.hc[warp][sb], 1u);
+                atomicAdd(&sm.hm[warp][sb], sel_mass(x, m));
+            }
+        });
+        __syncthreads();
+        const int sb = sel_cross(sm, mode, k, target, ca, ma, cnt, cmass);
+        sel_narrow(klo, khi, sb, sh);
+    }
+    if (cnt > static_cast<uint32_t>(kSelPool)) {  // one value held by more tokens than fit
+        gcnt = cnt;
+        gmass = cmass;
+        return key_value(khi);
+    }
+    // collect them and go on in shared memory
+    if (threadIdx.x == 0) sm.n = 0u;
+    __syncthreads();
+    sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+        if (in_set(x, klo, khi)) {
+            const uint32_t at = atomicAdd(&sm.n, 1u);
+            if (at < static_cast<uint32_t>(kSelPool)) sm.pool[at] = x;
+        }
+    });
+    __syncthreads();
+    uint32_t n = min(sm.n, static_cast<uint32_t>(kSelPool));
+    for (;;) {
+        // one value left (keys of -0 / +0 differ, values do not)?
+        if (threadIdx.x == 0) {
+            sm.kmin = 0xFFFFFFFFu;
+            sm.kmax = 0u;
+        }
+        __syncthreads();
+        uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+        for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
+            const uint32_t kv = ord_key(sm.pool[e]);
+            lo = min(lo, kv);
+            hi = max(hi, kv);
+        }
+        atomicMin(&sm.kmin, lo);
+        atomicMax(&sm.kmax, hi);
+        __syncthreads();
+        klo = sm.kmin;
+        khi = sm.kmax;
+        __syncthreads();
+        if (n == 0u || key_value(klo) == key_value(khi)) break;
+        const int sh = sel_shift(klo, khi);
+        sel_clear(sm);
+        __syncthreads();
+        for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
+            const float x = sm.pool[e];
+            const int sb = sel_sub(ord_key(x), khi, sh);
+            atomicAdd(&sm.hc[warp][sb], 1u);
+            atomicAdd(&sm.hm[warp][sb], sel_mass(x, m));
+        }
+        __syncthreads();
+        uint32_t c2;
+        float m2;
+        const int sb = sel_cross(sm, mode, k, target, ca, ma, c2, m2);
+        uint32_t nlo = klo, nhi = khi;
+        sel_narrow(nlo, nhi, sb, sh);
+        if (threadIdx.x == 0) sm.n = 0u;
+        __syncthreads();
+        for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
+            const float x = sm.pool[e];
+            const uint32_t kv = ord_key(x);
+            if (kv >= nlo && kv <= nhi) sm.pool2[atomicAdd(&sm.n, 1u)] = x;
+        }
+        __syncthreads();
+        n = sm.n;
+        for (uint32_t e = threadIdx.x; e < n; e += kThreads) sm.pool[e] = sm.pool2[e];
+        __syncthreads();
+    }
+    // the group of x*: count and mass
+    const float xs = n ? key_value(khi) : -kInf;
+    float gm = 0.0f;
+    for (uint32_t e = threadIdx.x; e < n; e += kThreads) gm += sel_mass(sm.pool[e], m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm += __shfl_xor_sync(0xFFFFFFFFu, gm, o);
+    if ((threadIdx.x & 31) == 0) sm.wm[warp] = gm;
+    __syncthreads();
+    float tot = 0.0f;
+    for (int w = 0; w < kWarps; ++w) tot += sm.wm[w];
+    gcnt = n;
+    gmass = tot;
+    __syncthreads();
+    return xs;
+}
+
+// The threshold and the kept mass of every constrained row: one CTA per logit row.
+template <typename T, bool kPen>
+__global__ void __launch_bounds__(kThreads, 2)
+sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectParams P)
+{
+    __shared__ SelSmem sm;
+    const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i = row_request(P.rq.cu, P.rq.n, row, lane);
+    bool greedy;
+    const float invT = request_invT(P.rq, i, greedy);
+    int k;
+    float Pp;
+    if (!sel_active(P.top_k, P.top_p, i, P.V, greedy, k, Pp)) return;
+    const bool use_k = k >= 1 && k < P.V, use_p = Pp < 1.0f;
+    const int q0 = __ldg(P.rq.cu + i);
+    const PenRow pr = kPen ? pen_row(P.pen, P.draft_ids, i, q0, row - q0 - i, P.V)
+                           : PenRow{0.0f, nullptr, nullptr, 0};
+    const T *rp = logits + static_cast<size_t>(row) * P.V;
+    // the row maximum from the statistics partials (every warp the same)
+    float L, s0;
+    int idx;
+    combine_row(P.part, row, P.V, P.maxseg, P.base_off, P.chunk, invT * kLog2e, L, s0, idx);
+    const float m = __fmul_rn(L, invT);
+
+    // level 1: count and mass per bin of 1/8 nat
+    sel_clear(sm);
+    __syncthreads();
+    sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
+        const int b = sel_bin1(x, m);
+        atomicAdd(&sm.hc[warp][b], 1u);
+        atomicAdd(&sm.hm[warp][b], sel_mass(x, m));
+    });
+    __syncthreads();
+    // Z: the mass of the top-k set, or of the row
+    float Z = 0.0f, tau = -kInf, Sk = 0.0f;
+    uint32_t gcnt;
+    float gmass;
+    if (use_k) {
+        uint32_t ca = 0u, cnt;
+        float ma = 0.0f, bm;
+        const int bk = sel_cross(sm, 0, static_cast<uint32_t>(k), 0.0f, ca, ma, cnt, bm);
+        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, -kInf, cnt, bm, 0,
+                                   static_cast<uint32_t>(k), 0.0f, ca, ma, gcnt, gmass);
+        Z = ma + gmass;
+    } else {
+        float t = 0.0f;
+        for (int w = 0; w < kWarps; ++w) t += sm.hm[w][threadIdx.x];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
+        if (lane == 0) sm.wm[warp] = t;
+        __syncthreads();
+        for (int w = 0; w < kWarps; ++w) Z += sm.wm[w];
+        __syncthreads();
+    }
+    Sk = Z;
+    if (use_p) {
+        const float target = __fmul_rn(fmaxf(Pp, 1e-6f), Z);
+        // level 1 again over the top-k set only (the bins hold tokens >= tau_k)
+        if (use_k) {
+            sel_clear(sm);
+            __syncthreads();
+            sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
+                if (x >= tau) {
+                    const int b = sel_bin1(x, m);
+                    atomicAdd(&sm.hc[warp][b], 1u);
+                    atomicAdd(&sm.hm[warp][b], sel_mass(x, m));
+                }
+            });
+            __syncthreads();
+        }
+        uint32_t ca = 0u, cnt;
+        float ma = 0.0f, bm;
+        const int bp = sel_cross(sm, 1, 0u, target, ca, ma, cnt, bm);
+        const float xs = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bp, tau, cnt, bm, 1, 0u,
+                                              target, ca, ma, gcnt, gmass);
+        tau = xs;
+        Sk = ma + gmass;
+    }
+    if (threadIdx.x == 0) {
+        P.sel_tau[row] = tau;
+        P.sel_S[row] = Sk;
+    }
+}
+
+// One CTA per request. kDLMode: q comes from draft logits (P.dl); kPen: the batch has a
+// frequency penalty. Separate instantiations, so that the plain path carries neither.
+template <typename T, bool kDLMode, bool kPen>
 __global__ void __launch_bounds__(kThreads, 2)
 sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
                  const __grid_constant__ VerifyParams P)
@@ -1142,7 +1796,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     }
     const int row0 = q0 + i;
     bool greedy;
-    const float invT = request_invT(P.rq.temperature, P.rq.is_greedy, i, greedy);
+    const float invT = request_invT(P.rq, i, greedy);
+    if (tid == 0 && pen_counts_row_bad(P.pen, i)) atomicOr(P.flags + 1, SV_ERR_COUNTS);
     const bool partial = P.partial && __ldg(P.partial + i) != 0;  // no token: only row stats
     const bool synthetic = P.nsyn > 0;
     const float c = invT * kLog2e;
@@ -1150,6 +1805,10 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     float *sm_m = reinterpret_cast<float *>(dyn + lay.rows), *sm_S = sm_m + stride;
     int *sm_amax = reinterpret_cast<int *>(sm_m + 2 * stride);
     float *sm_md = sm_m + 3 * stride, *sm_Sd = sm_m + 4 * stride;  // draft rows (draft logits)
+    float *sm_tau = sm_m + 5 * stride;                              // sampling constraints
+    int sel_k;
+    float sel_p;
+    const bool constrained = P.sel_tau && sel_active(P.rq.top_k, P.top_p, i, P.V, greedy, sel_k, sel_p);
     const T *dl = kDLMode ? static_cast<const T *>(P.dl) : nullptr;
 
     // 1. row statistics from the partials (warp per row) and the acceptance tests
@@ -1166,9 +1825,15 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             combine_row(P.dpart, q0 + j, P.V, P.maxseg, P.dbase_off, P.dchunk, c, Ld, Sd, id);
             md = __fmul_rn(Ld, invT);
         }
+        float tau = -kInf;
+        if (constrained) {  // the kept set and its mass, from the select kernel
+            tau = __ldg(P.sel_tau + row);
+            s = __ldg(P.sel_S + row);
+        }
         if (lane == 0) {
             sm_md[j] = md;
             sm_Sd[j] = Sd;
+            sm_tau[j] = tau;
             const float m = __fmul_rn(L, invT);  // = max_v fl(l_v / T): rounding is monotone
             const int amax = idx == INT_MAX ? 0 : idx;
             sm_m[j] = m;
@@ -1179,7 +1844,10 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             if (P.opt_amax) P.opt_amax[row] = amax;
             if (j < K && !partial &&
                 !(synthetic ? accept_synthetic(P, j, q0 + j, ireq)
-                            : accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j, invT, m, s,
+                            : accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j,
+                                              kPen ? pen_row(P.pen, P.draft_ids, i, q0, j, P.V)
+                                                   : PenRow{0.0f, nullptr, nullptr, 0},
+                                              invT, m, s, tau,
                                               amax, P.draft_ids, P.q, dl, md, Sd, P.seed, ireq)))
                 atomicMin(&s_js, j);
         }
@@ -1214,6 +1882,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     const bool residual = !synthetic && js < K && (P.q != nullptr || dl != nullptr);
     r.qrow = residual && P.q ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
     r.dlrow = residual && dl ? dl + static_cast<size_t>(q0 + js) * P.V : nullptr;
+    r.pr = kPen ? pen_row(P.pen, P.draft_ids, i, q0, js, P.V) : PenRow{0.0f, nullptr, nullptr, 0};
+    r.tau = sm_tau[js];
     r.md = js < K ? sm_md[js] : 0.0f;
     r.Sd = js < K ? sm_Sd[js] : 1.0f;
     r.excl = (!synthetic && js < K && !residual) ? __ldg(P.draft_ids + q0 + js) : -1;
@@ -1233,17 +1903,17 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     sm.best = &s_best;
     sm.cnt = &s_cnt;
     const RowLines rl = row_lines(row, P.V, P.base_off);
-    row_line_max<T>(r.rp, P.V, rl, lines, sm.lm);
+    row_line_max<T, kPen>(r.rp, P.V, rl, lines, sm.lm, r.pr);
     __syncthreads();
-    unsigned long long best = residual ? race_search<T, true, kDLMode>(r, rl, sm)
-                                       : race_search<T, false>(r, rl, sm);
+    unsigned long long best = residual ? race_search<T, true, kDLMode, kPen>(r, rl, sm)
+                                       : race_search<T, false, false, kPen>(r, rl, sm);
     if (best == 0) {
         // nothing left of max(0, p - q) after rounding, or V == 1 with the only token rejected:
         // draw from p itself
-        row_line_max<T>(r.rp, P.V, rl, lines, sm.lm);
+        row_line_max<T, kPen>(r.rp, P.V, rl, lines, sm.lm, r.pr);
         __syncthreads();
         r.excl = -1;
-        best = race_search<T, false>(r, rl, sm);
+        best = race_search<T, false, false, kPen>(r, rl, sm);
     }
     emit_row(i, js, K, q0, static_cast<int>(~static_cast<unsigned>(best)), P.draft_ids, P.sampled,
              stride, P.num_sampled, P.num_rejected, tid, kThreads);
@@ -1253,12 +1923,13 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
 // host side
 // ---------------------------------------------------------------------------------------
 constexpr int kProfRing = 512;
-constexpr int kKernels = 2;  // stats, verify
+constexpr int kKernels = 2;     // launches of a call without sampling constraints: stats, verify
+constexpr int kProfSlots = 3;   // profiled kernels: stats, verify, select (top-k / top-p)
 // static shared memory of a verify CTA besides the dynamic part (reserve)
 constexpr int kVerifyStaticSmem = 10240;
 
 struct ProfSlot {
-    cudaEvent_t ev[kKernels + 1];
+    cudaEvent_t ev[kProfSlots + 1];  // before stats, after stats, after select, after verify
     bool pending;
 };
 
@@ -1280,6 +1951,8 @@ struct spec_verify_ctx {
     int stats_ctas = 1;    // one wave of the statistics kernel (SMs x CTAs per SM)
     StatPart *statpart = nullptr;
     StatPart *dpart = nullptr;  // partials of the draft rows (draft-logits mode)
+    float *sel_tau = nullptr;   // [max_rows] top-k / top-p threshold per row
+    float *sel_S = nullptr;     // [max_rows] kept mass per row
     void *lines = nullptr;      // largest logit of every 64-element line (logits dtype), or null
     unsigned *flags = nullptr;  // [1] sticky error word
     // host-buffer staging
@@ -1292,7 +1965,7 @@ struct spec_verify_ctx {
     bool prof = false;
     std::vector<ProfSlot> ring;
     int64_t prof_calls = 0, prof_done = 0;
-    double prof_ms[kKernels] = {0, 0};
+    double prof_ms[kProfSlots] = {0, 0, 0};
 };
 
 namespace {
@@ -1326,11 +1999,13 @@ struct DeviceGuard {
 void prof_collect(spec_verify_ctx *ctx, ProfSlot &s)
 {
     if (!s.pending) return;
-    cudaEventSynchronize(s.ev[kKernels]);
-    for (int k = 0; k < kKernels; ++k) {
-        float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, s.ev[k], s.ev[k + 1]) == cudaSuccess) ctx->prof_ms[k] += ms;
-    }
+    cudaEventSynchronize(s.ev[kProfSlots]);
+    // events: 0 before stats, 1 after it, 2 after select (right after 1 without it), 3 after verify
+    float ms[kProfSlots] = {0.f, 0.f, 0.f};
+    cudaEventElapsedTime(&ms[0], s.ev[0], s.ev[1]);
+    cudaEventElapsedTime(&ms[2], s.ev[1], s.ev[2]);
+    cudaEventElapsedTime(&ms[1], s.ev[2], s.ev[3]);
+    for (int k = 0; k < kProfSlots; ++k) ctx->prof_ms[k] += ms[k];
     s.pending = false;
     ctx->prof_done++;
 }
@@ -1339,6 +2014,8 @@ void free_all(spec_verify_ctx *ctx)
 {
     cudaFree(ctx->statpart);
     cudaFree(ctx->dpart);
+    cudaFree(ctx->sel_tau);
+    cudaFree(ctx->sel_S);
     cudaFree(ctx->lines);
     cudaFree(ctx->flags);
     cudaFree(ctx->io_logits);
@@ -1373,13 +2050,17 @@ template <typename T>
 cudaError_t setup_kernels(int device, int *stats_per_sm)
 {
     const int limit = static_cast<int>(verify_smem_limit(device));
-    cudaError_t e = cudaFuncSetAttribute(sv_verify_kernel<T, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(sv_verify_kernel<T, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
+    const void *kernels[] = {reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
+                             reinterpret_cast<const void *>(sv_verify_kernel<T, true, false>),
+                             reinterpret_cast<const void *>(sv_verify_kernel<T, false, true>),
+                             reinterpret_cast<const void *>(sv_verify_kernel<T, true, true>)};
+    cudaError_t e = cudaSuccess;
+    for (const void *k : kernels)
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T>, kThreads, 0);
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T, false>,
+                                                         kThreads, 0);
 }
 
 // Statistics chunk for an array of `total` elements: the context's, or an even split over
@@ -1418,7 +2099,9 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     const long long total = static_cast<long long>(rows) * V;
     const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
     const long long chunk1 = stats_chunk_for(ctx, total + total_d);
-    const RequestTable rq{cu, b.temperature, b.is_greedy, num_reqs};
+    const RequestTable rq{cu, b.temperature, b.is_greedy, b.top_k, num_reqs};
+    const PenTable pen{b.frequency_penalty, b.output_bin_counts, b.counts_row, b.counts_rows};
+    const bool pen_on = b.frequency_penalty != nullptr;
     T *lines = static_cast<T *>(ctx->lines);
     const StatsArray<T> A = stats_array<T>(logits, total, chunk1, V, 0, ctx->statpart, lines);
     const StatsArray<T> D = stats_array<T>(dl, total_d, chunk1, V, 1, ctx->dpart, nullptr);
@@ -1449,6 +2132,11 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     P.opt_amax = o.row_argmax;
     P.flags = ctx->flags;
     P.partial = b.partial_prefill;
+    P.pen = pen_on ? pen : PenTable{nullptr, nullptr, nullptr, 0};
+    const bool sel_on = b.top_k != nullptr || b.top_p != nullptr;
+    P.top_p = b.top_p;
+    P.sel_tau = sel_on ? ctx->sel_tau : nullptr;
+    P.sel_S = sel_on ? ctx->sel_S : nullptr;
     P.nsyn = ctx->nsyn;
     for (int k = 0; k < SV_MAX_SYNTHETIC; ++k) P.syn[k] = k < ctx->nsyn ? ctx->syn[k] : 0.0f;
     const size_t smem = verify_smem_bytes(V, kmax);
@@ -1460,14 +2148,38 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         cudaEventRecord(slot->ev[0], stream);
     }
     const size_t smem1 = lines ? static_cast<size_t>(chunk1 / kGroup) * sizeof(T) : 0;
-    sv_stats_kernel<T><<<A.grid + D.grid, kThreads, smem1, stream>>>(V, ctx->maxseg, A, D, rq);
-    if (slot) cudaEventRecord(slot->ev[1], stream);
-    if (dl)
-        sv_verify_kernel<T, true><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
+    if (pen_on)
+        sv_stats_kernel<T, true><<<A.grid + D.grid, kThreads, smem1, stream>>>(
+            V, ctx->maxseg, A, D, rq, pen, b.draft_ids);
     else
-        sv_verify_kernel<T, false><<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
+        sv_stats_kernel<T, false><<<A.grid + D.grid, kThreads, smem1, stream>>>(
+            V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids);
+    if (slot) cudaEventRecord(slot->ev[1], stream);
+    if (sel_on) {  // top-k / top-p: the kept set of every constrained row
+        SelectParams SP;
+        SP.rq = rq;
+        SP.pen = P.pen;
+        SP.draft_ids = b.draft_ids;
+        SP.top_k = b.top_k;
+        SP.top_p = b.top_p;
+        SP.part = ctx->statpart;
+        SP.V = V;
+        SP.maxseg = ctx->maxseg;
+        SP.base_off = base_off;
+        SP.chunk = P.chunk;
+        SP.sel_tau = ctx->sel_tau;
+        SP.sel_S = ctx->sel_S;
+        if (pen_on)
+            sv_select_kernel<T, true><<<rows, kThreads, 0, stream>>>(logits, SP);
+        else
+            sv_select_kernel<T, false><<<rows, kThreads, 0, stream>>>(logits, SP);
+    }
+    if (slot) cudaEventRecord(slot->ev[2], stream);
+    auto verify = dl ? (pen_on ? sv_verify_kernel<T, true, true> : sv_verify_kernel<T, true, false>)
+                     : (pen_on ? sv_verify_kernel<T, false, true> : sv_verify_kernel<T, false, false>);
+    verify<<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
     if (slot) {
-        cudaEventRecord(slot->ev[2], stream);
+        cudaEventRecord(slot->ev[3], stream);
         slot->pending = true;
         ctx->prof_calls++;
     }
@@ -1487,6 +2199,28 @@ const void *in_place(const void *p)
     return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
 }
 
+// A batch with the arguments of the plain entry points; the other fields NULL / 0.
+spec_verify_batch plain_batch(const void *logits, const int32_t *draft_ids, const float *q,
+                              const void *dl, const int32_t *cu, const float *temperature,
+                              const uint8_t *is_greedy, uint64_t seed, uint32_t base, int n,
+                              int nd, int kmax)
+{
+    spec_verify_batch b{};
+    b.logits = logits;
+    b.draft_ids = draft_ids;
+    b.draft_probs = q;
+    b.draft_logits = dl;
+    b.cu_num_draft = cu;
+    b.temperature = temperature;
+    b.is_greedy = is_greedy;
+    b.seed = seed;
+    b.req_index_base = base;
+    b.num_reqs = n;
+    b.num_draft_tokens = nd;
+    b.max_spec_len_this_batch = kmax;
+    return b;
+}
+
 // Host-visible argument checks of one call (nothing is launched when they fail); `aligned`:
 // the arrays are the kernels' own (device) inputs, whose 16-byte alignment is required.
 int check_run_args(const spec_verify_ctx *ctx, const spec_verify_batch &b,
@@ -1503,6 +2237,10 @@ int check_run_args(const spec_verify_ctx *ctx, const spec_verify_batch &b,
         return SV_EINVAL;
     if (b.draft_probs && !ctx->has_q) return SV_EINVAL;
     if (b.draft_logits && (!ctx->has_dl || b.draft_probs)) return SV_EINVAL;
+    if ((b.frequency_penalty != nullptr) != (b.output_bin_counts != nullptr) ||
+        (b.frequency_penalty && b.counts_rows < 1))
+        return SV_EINVAL;
+    if ((b.top_k || b.top_p) && !ctx->sel_tau) return SV_EINVAL;  // not in the static-scratch path
     if (aligned && (reinterpret_cast<uintptr_t>(b.logits) % 16 != 0 ||
         reinterpret_cast<uintptr_t>(b.draft_probs) % 16 != 0 ||
         reinterpret_cast<uintptr_t>(b.draft_logits) % 16 != 0))
@@ -1557,6 +2295,8 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
               cudaMalloc(&ctx->lines, nlines * eb) == cudaSuccess &&
               cudaMalloc(&ctx->flags, 2 * sizeof(unsigned)) == cudaSuccess;
     const size_t D = static_cast<size_t>(max_num_reqs) * static_cast<size_t>(max_spec_len);
+    ok = ok && cudaMalloc(&ctx->sel_tau, R * sizeof(float)) == cudaSuccess &&
+         cudaMalloc(&ctx->sel_S, R * sizeof(float)) == cudaSuccess;
     ok = ok && (!ctx->has_dl || D == 0 ||
                 cudaMalloc(&ctx->dpart, D * S * kWarps * sizeof(StatPart)) == cudaSuccess);
     ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
@@ -1596,9 +2336,9 @@ int spec_verify_run(spec_verify_ctx *ctx, const void *logits, const int32_t *dra
                     int32_t *num_rejected, float *opt_row_max, float *opt_row_sumexp,
                     int32_t *opt_row_argmax, void *cuda_stream)
 {
-    const spec_verify_batch b{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
-                              is_greedy, nullptr, seed, req_index_base, num_reqs,
-                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_batch b = plain_batch(logits, draft_ids, draft_probs, nullptr, cu_num_draft,
+                                            temperature, is_greedy, seed, req_index_base,
+                                            num_reqs, num_draft_tokens, max_spec_len_this_batch);
     const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
                                 opt_row_argmax};
     return spec_verify_run_batch(ctx, &b, &o, cuda_stream);
@@ -1616,9 +2356,9 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
 {
     if (!ctx) return SV_EINVAL;
     if (!ctx->has_dl || (num_reqs > 0 && num_draft_tokens > 0 && !draft_logits)) return SV_EINVAL;
-    const spec_verify_batch b{logits, draft_ids, nullptr, draft_logits, cu_num_draft, temperature,
-                              is_greedy, nullptr, seed, req_index_base, num_reqs,
-                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_batch b = plain_batch(logits, draft_ids, nullptr, draft_logits, cu_num_draft,
+                                            temperature, is_greedy, seed, req_index_base,
+                                            num_reqs, num_draft_tokens, max_spec_len_this_batch);
     const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
                                 opt_row_argmax};
     return spec_verify_run_batch(ctx, &b, &o, cuda_stream);
@@ -1691,9 +2431,9 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
     if (!ctx) return SV_EINVAL;
     if (!ctx->io_logits) return SV_EINVAL;
     // the device path's checks, less alignment: host arrays are staged or read in place
-    const spec_verify_batch hb{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
-                               is_greedy, nullptr, seed, req_index_base, num_reqs,
-                               num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_batch hb = plain_batch(logits, draft_ids, draft_probs, nullptr, cu_num_draft,
+                                             temperature, is_greedy, seed, req_index_base,
+                                             num_reqs, num_draft_tokens, max_spec_len_this_batch);
     const spec_verify_outputs ho{sampled, num_sampled, num_rejected, nullptr, nullptr, nullptr};
     int rc = check_run_args(ctx, hb, ho, false);
     if (rc != SV_OK || num_reqs == 0) return rc;
@@ -1779,7 +2519,7 @@ int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls)
     DeviceGuard g(ctx->device);
     if (!g.ok) return SV_EDEVICE;
     for (auto &s : ctx->ring) prof_collect(ctx, s);
-    for (int k = 0; k < kKernels; ++k) {
+    for (int k = 0; k < kProfSlots; ++k) {
         ms[k] = ctx->prof_ms[k];
         ctx->prof_ms[k] = 0.0;
     }
@@ -1932,9 +2672,9 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
     view.statpart = reinterpret_cast<StatPart *>(bytes + kOffStatPart);
     view.flags = reinterpret_cast<unsigned *>(bytes + kOffFlags);
     auto stream = static_cast<cudaStream_t>(cuda_stream);
-    const spec_verify_batch b{logits, draft_ids, draft_probs, nullptr, cu_num_draft, temperature,
-                              is_greedy, nullptr, seed, req_index_base, num_reqs,
-                              num_draft_tokens, max_spec_len_this_batch};
+    const spec_verify_batch b = plain_batch(logits, draft_ids, draft_probs, nullptr, cu_num_draft,
+                                            temperature, is_greedy, seed, req_index_base,
+                                            num_reqs, num_draft_tokens, max_spec_len_this_batch);
     const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
                                 opt_row_argmax};
     return logits_dtype == SV_BF16 ? launch_all<uint16_t>(&view, b, o, stream)

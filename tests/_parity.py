@@ -4,14 +4,18 @@ Token ids and accept lengths must match bit for bit. The only exception is a req
 outputs differ after a decision the oracle calls too close to call: an acceptance test with
 |u - p/q| < 1e-6 at a position both sides evaluated, or a residual race whose two best keys
 are closer than 1e-6 (the residual depends on the row's sum of exponentials S, which the two
-sides accumulate in different orders). Such a request is a counted tie and the rest of it is
-not compared. The row statistics must match: m and the argmax exactly, S to 1e-5 relative.
+sides accumulate in different orders), or a top-p boundary within 1e-4 of the total mass at a
+row both sides used (the kept mass is summed in binary32 on the GPU). Such a request is a
+counted tie and the rest of it is not compared. The row statistics must match: m and the
+argmax exactly, S (the kept mass under top-k / top-p) to 1e-5 relative, except at rows whose
+top-p boundary is that close, where S is not compared (the boundary group may fall either way).
 """
 from __future__ import annotations
 
 import numpy as np
 
 TIE_MARGIN = 1e-6
+SEL_MARGIN = 1e-4
 S_RTOL = 1e-5
 RACE_NONE = 0
 
@@ -31,7 +35,13 @@ def to_device(batch, device="cuda:0"):
     pp = None
     if getattr(batch, "partial_prefill", None) is not None:
         pp = torch.from_numpy(np.ascontiguousarray(batch.partial_prefill, np.uint8)).to(device)
+    extra = {}
+    for name, dt in (("frequency_penalty", np.float32), ("output_bin_counts", np.int32),
+                     ("counts_row", np.int32), ("top_k", np.int32), ("top_p", np.float32)):
+        a = getattr(batch, name, None)
+        extra[name] = None if a is None else torch.from_numpy(np.ascontiguousarray(a, dt)).to(device)
     return dict(
+        **extra,
         logits=lt,
         draft_logits=dl,
         partial_prefill=pp,
@@ -66,7 +76,9 @@ def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, 
     outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
                    d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,
                    req_index_base=req_index_base, max_spec_len=kmax, row_stats=True,
-                   draft_logits=d["draft_logits"], partial_prefill=d["partial_prefill"])
+                   draft_logits=d["draft_logits"], partial_prefill=d["partial_prefill"],
+                   frequency_penalty=d["frequency_penalty"], output_bin_counts=d["output_bin_counts"],
+                   counts_row=d["counts_row"], top_k=d["top_k"], top_p=d["top_p"])
     torch.cuda.synchronize()
     names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
     res = {k: v.cpu().numpy() for k, v in zip(names, outs)}
@@ -95,6 +107,11 @@ def compare(batch, gpu: dict, ref: dict) -> dict:
         closest = float(m.min()) if m.size else np.inf
         if js_ref == js_gpu and ref["race_kind"][i] != RACE_NONE:
             closest = min(closest, float(ref["race_gap"][i]))
+        sel = ref.get("row_select_margin")
+        if sel is not None and upto >= 0:
+            r0 = cu[i] + i
+            if np.min(sel[r0:r0 + upto + 1]) < SEL_MARGIN:
+                closest = min(closest, 0.0)
         (ties if closest < TIE_MARGIN else bad).append((i, closest))
     R = batch.num_rows
     stats_ok = dict(
@@ -103,6 +120,9 @@ def compare(batch, gpu: dict, ref: dict) -> dict:
     )
     rel = np.abs(gpu["row_sumexp"][:R].astype(np.float64) - ref["row_sumexp"][:R]) / \
         np.maximum(np.abs(ref["row_sumexp"][:R].astype(np.float64)), 1e-30)
+    sel = ref.get("row_select_margin")
+    if sel is not None:                       # a top-p boundary too close to call: S is loose
+        rel = np.where(sel[:R] < SEL_MARGIN, 0.0, rel)
     stats_ok["row_sumexp"] = bool(np.all(rel <= S_RTOL))
     out = dict(requests=n, positions=int(cu[-1]), ties=len(ties), mismatches=bad,
                max_sumexp_rel=float(rel.max()) if R else 0.0, **stats_ok)

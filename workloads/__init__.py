@@ -238,6 +238,34 @@ def make_batch(*, name: str, data_seed: int, verify_seed: int, K, vocab_size: in
                  draft_logits=dl if q_mode == "logits" else None)
 
 
+def add_penalty(b: Batch, seed: int, *, history=(50, 500), top_share=0.5, top_n=50,
+                penalty=(-0.5, 1.5), extra_rows: int = 0, shuffle_rows: bool = False) -> Batch:
+    """Give a batch a frequency penalty: per request a token history of U{history} tokens, each
+    with probability top_share one of the top_n logits of the request's first row (the tokens a
+    model tends to repeat), else uniform over the vocabulary; output_bin_counts = the history's
+    counts; penalty ~ U(penalty). extra_rows unused count rows are added, and with shuffle_rows
+    the requests' rows are permuted (counts_row maps them)."""
+    rng = np.random.default_rng([seed, 0x5EED])
+    n, V = b.num_reqs, b.vocab_size
+    rows = n + extra_rows
+    counts = np.zeros((rows, V), np.int32)
+    perm = rng.permutation(rows)[:n] if shuffle_rows else np.arange(n)
+    logits = b.logits
+    for i in range(n):
+        r0 = int(b.cu_num_draft[i]) + i
+        row = logits[r0]
+        vals = (row.astype(np.uint32) << 16).view(np.float32) if row.dtype == np.uint16 else row
+        top = np.argsort(-vals, kind="stable")[:top_n]
+        h = int(rng.integers(history[0], history[1] + 1))
+        pick_top = rng.random(h) < top_share
+        toks = np.where(pick_top, top[rng.integers(0, top.size, h)], rng.integers(0, V, h))
+        np.add.at(counts[perm[i]], toks, 1)
+    b.output_bin_counts = counts
+    b.counts_row = perm.astype(np.int32) if shuffle_rows else None
+    b.frequency_penalty = rng.uniform(*penalty, n).astype(np.float32)
+    return b
+
+
 WORKLOADS = {
     0: "tiny: 4 req, K=3, V=1024, fp32, q noisy, T=1",
     1: "64 req, K=4, V=32000, bf16 boosted, q noisy, T~U[0.5,1.2], 25% greedy",
