@@ -1328,16 +1328,17 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
 //   top-k: tau_k = the k-th largest x (ties at it are kept), for 1 <= k < V;
 //   top-p: among those, every token whose strictly larger tokens hold less than P * Z of the
 //          mass t_v = exp(x_v - m), Z the mass of the top-k set, for P < 1 (at least 1e-6).
-// One CTA per row finds tau without sorting the row: a histogram of count and mass over 256 bins
-// of 1/8 nat below the row maximum (one pass over the row); then the bin where the k-th token or
-// the P * Z mass falls is refined on the order-preserving integer key of x, 8 bits per level,
-// over the row (from L2) until its tokens fit in shared memory, then over those, down to a
-// single value (a group of equal values is kept or dropped as a whole). Masses come from the
-// hardware ex2, summed in fp32.
-constexpr int kSelBins = 256;
-constexpr int kSelPool = 2048;
+// One CTA per row finds tau without sorting the row: a histogram of counts (top-k) or masses
+// (top-p) over 256 bins of 1/8 nat below the row maximum, one atomic per token into its warp's
+// copy (one pass over the row); then the bin where the k-th token or the P * Z mass falls is
+// collected into shared memory (a second pass, from L2) and refined there on the
+// order-preserving integer key of x, 8 bits per level, down to a single value (a group of equal
+// values is kept or dropped as a whole); a bin too large to collect is refined over the row
+// first. Masses come from the hardware ex2, summed in fp32.
+constexpr int kSelBins = 256;           // bins per level: 1/8 nat below the row maximum, then 8 key bits
 constexpr float kSelBinsPerNat = 8.0f;
-static_assert(kSelBins == kThreads, "one histogram bin per thread");
+constexpr int kSelPool = 4096;          // tokens refined in shared memory
+static_assert(kSelBins == kThreads, "one bin per thread");
 
 struct SelectParams {
     RequestTable rq;
@@ -1378,47 +1379,59 @@ __device__ __forceinline__ int sel_bin1(float x, float m)
     const float u = __fmul_rn(__fsub_rn(m, x), kSelBinsPerNat);
     return u < 255.0f ? (u > 0.0f ? static_cast<int>(u) : 0) : 255;  // NaN: 255
 }
+// A token's mass exp(x - m), by the hardware ex2.
 __device__ __forceinline__ float sel_mass(float x, float m)
 {
     return sv::ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
 struct SelSmem {
-    uint32_t hc[kWarps][kSelBins];
-    float hm[kWarps][kSelBins];
+    uint32_t h[kWarps][kSelBins];  // per-warp counts (top-k) or masses (top-p, as float bits)
     float pool[kSelPool], pool2[kSelPool];
     uint32_t wc[kWarps];
     float wm[kWarps];
     uint32_t kmin, kmax, n;
     int cross;
+    float fsum;
     uint32_t cabove;
     float mabove;
 };
 
-// Every element of a row once, as x = processed logit * (1 / T), with its token index; 16-byte
-// loads over the aligned body.
+// Every element of a row once, as x = processed logit * (1 / T), with its token index: 16-byte
+// loads over the aligned body, four in flight per thread.
 template <typename T, bool kPen, typename F>
 __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, float invT,
                                             const PenRow &pr, F &&f)
 {
     constexpr int kEV = 16 / static_cast<int>(sizeof(T));
+    constexpr int kIn = 4;
     const int head = min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rp) & 15u)) & 15u) / sizeof(T)));
     auto proc = [&](float l, int v) { return __fmul_rn(kPen ? pen_apply(pr, l, v) : l, invT); };
     for (int v = threadIdx.x; v < head; v += kThreads) f(proc(Elem<T>::at(rp, v), v), v);
     const int nvec = (V - head) / kEV;
     const char *base = reinterpret_cast<const char *>(rp + head);
-    for (int u = threadIdx.x; u < nvec; u += kThreads) {
-        const uint4 w = ldg_v4(base + static_cast<size_t>(u) * 16);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    for (int u0 = threadIdx.x; u0 < nvec; u0 += kIn * kThreads) {
+        uint4 w[kIn];
 #pragma unroll
-        for (int e = 0; e < kEV; ++e) {
-            float l;
-            if constexpr (sizeof(T) == 2)
-                l = __uint_as_float((e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16));
-            else
-                l = __uint_as_float(ws[e]);
-            const int v = head + u * kEV + e;
-            f(proc(l, v), v);
+        for (int q = 0; q < kIn; ++q) {
+            const int u = u0 + q * kThreads;
+            w[q] = u < nvec ? ldg_v4(base + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < kIn; ++q) {
+            const int u = u0 + q * kThreads;
+            if (u >= nvec) break;
+            const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+            for (int e = 0; e < kEV; ++e) {
+                float l;
+                if constexpr (sizeof(T) == 2)
+                    l = __uint_as_float((e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16));
+                else
+                    l = __uint_as_float(ws[e]);
+                const int v = head + u * kEV + e;
+                f(proc(l, v), v);
+            }
         }
     }
     for (int v = head + nvec * kEV + threadIdx.x; v < V; v += kThreads)
@@ -1427,27 +1440,43 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
 
 __device__ __forceinline__ void sel_clear(SelSmem &sm)
 {
-    for (int w = 0; w < kWarps; ++w) {
-        sm.hc[w][threadIdx.x] = 0u;
-        sm.hm[w][threadIdx.x] = 0.0f;
-    }
+    for (int w = 0; w < kWarps; ++w) sm.h[w][threadIdx.x] = 0u;
+}
+__device__ __forceinline__ void sel_add(SelSmem &sm, int mode, int b, float t)
+{
+    const int warp = threadIdx.x >> 5;
+    if (mode == 0) atomicAdd(&sm.h[warp][b], 1u);
+    else atomicAdd(reinterpret_cast<float *>(&sm.h[warp][b]), t);
 }
 
-// After the per-warp histograms are complete: merge them and find the crossing bin (bin 0 holds
-// the largest values). mode 0: the first bin where ca + count >= k; mode 1: the first bin where
-// ma + mass >= target (the last non-empty bin when rounding leaves the total short). Adds the
-// count / mass strictly above the crossing bin to ca / ma; returns the bin and its count.
-__device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32_t &ca,
-                         float &ma, uint32_t &cnt, float &bmass)
+// Sum of a float over the CTA (every thread gets it).
+__device__ __forceinline__ float sel_block_sum(SelSmem &sm, float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) sm.wm[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float t = 0.0f;
+    for (int w = 0; w < kWarps; ++w) t += sm.wm[w];
+    __syncthreads();
+    return t;
+}
+
+// After the per-warp histograms are complete (bin 0 holds the largest values): the crossing bin.
+// mode 0 (counts): the first bin where ca + count >= k; mode 1 (masses): the first bin where
+// ma + mass >= target, or the last non-empty bin if rounding leaves the total short. Adds the
+// count (mode 0) or mass (mode 1) strictly above the crossing bin to ca / ma.
+__device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32_t &ca, float &ma)
 {
     const int b = threadIdx.x, lane = b & 31, warp = b >> 5;
     uint32_t c = 0u;
     float mm = 0.0f;
     for (int w = 0; w < kWarps; ++w) {
-        c += sm.hc[w][b];
-        mm += sm.hm[w][b];
+        if (mode == 0) c += sm.h[w][b];
+        else mm += __uint_as_float(sm.h[w][b]);
     }
-    // inclusive scan over the bins; excl(b) is exactly incl(b - 1)
+    // inclusive scans; excl(b) is exactly incl(b - 1)
     uint32_t ci = c;
     float mi = mm;
 #pragma unroll
@@ -1482,11 +1511,12 @@ __device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32
         sm.mabove = mex;
     }
     __syncthreads();
-    if (sm.cross < 0) {  // mode 1 short of the target: the last non-empty bin
-        const unsigned nz = __ballot_sync(0xFFFFFFFFu, c > 0u);
+    if (sm.cross < 0) {  // short of the target: the last non-empty bin
+        const unsigned nz = __ballot_sync(0xFFFFFFFFu, mode == 0 ? c > 0u : mm > 0.0f);
         if (lane == 0) sm.wc[warp] = nz;
         __syncthreads();
         if (b == 0) {
+            sm.cross = 0;
             for (int w = kWarps - 1; w >= 0; --w)
                 if (sm.wc[w]) {
                     sm.cross = w * 32 + 31 - __clz(sm.wc[w]);
@@ -1503,14 +1533,6 @@ __device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32
     const int x = sm.cross;
     ca = sm.cabove;
     ma = sm.mabove;
-    uint32_t total = 0u;
-    float tm = 0.0f;
-    for (int w = 0; w < kWarps; ++w) {
-        total += sm.hc[w][x];
-        tm += sm.hm[w][x];
-    }
-    cnt = total;
-    bmass = tm;
     __syncthreads();
     return x;
 }
@@ -1535,77 +1557,86 @@ __device__ __forceinline__ int sel_shift(uint32_t klo, uint32_t khi)
     return bits > 8 ? bits - 8 : 0;
 }
 
-// Resolve the crossing among the candidates: the row's tokens with x >= xmin and, if b1 >= 0,
-// level-1 bin b1 (count `cnt`), with ca / ma tokens strictly above them. Returns x*, the single
-// value where the goal crosses, with ca / ma = count / mass strictly above x* and gcnt / gmass
-// its group's.
+// Resolve the crossing among the candidates: the row's tokens with x >= xmin in level-1 bin b1,
+// with ca / ma tokens strictly above them (ca in mode 0, ma in mode 1). The first pass collects
+// them into shared memory, counting them and taking their key range (and the mass of the tokens
+// in the bins above b1 with x >= xmin, returned in above_mass); only if they do not fit are finer
+// levels taken over the row first. Returns x*, the single value where the goal crosses, with
+// ca / ma counting / weighing the tokens strictly above x*, inbin_above the mass of the
+// candidates strictly above x* (mode 0) and gmass the mass of its group (all tokens equal x*).
 template <typename T, bool kPen>
 __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float m,
-                             const PenRow &pr, int b1, float xmin, uint32_t cnt, float cmass,
-                             int mode, uint32_t k, float target, uint32_t &ca, float &ma,
-                             uint32_t &gcnt, float &gmass)
+                             const PenRow &pr, int b1, float xmin, int mode, uint32_t k,
+                             float target, uint32_t &ca, float &ma, float &above_mass,
+                             float &inbin_above, float &gmass)
 {
-    const int warp = threadIdx.x >> 5;
     auto in_set = [&](float x, uint32_t klo, uint32_t khi) {
         const uint32_t kv = ord_key(x);
-        return x >= xmin && kv >= klo && kv <= khi && (b1 < 0 || sel_bin1(x, m) == b1);
+        return x >= xmin && kv >= klo && kv <= khi && sel_bin1(x, m) == b1;
     };
-    uint32_t klo = 0u, khi = 0xFFFFFFFFu;
-    if (cnt > static_cast<uint32_t>(kSelPool)) {
-        // too many to collect: the key range of the candidates, then refine it over the row
+    uint32_t klo = 0u, khi = 0xFFFFFFFFu, n = 0u;
+    bool first = true, big = false;
+    inbin_above = 0.0f;
+    for (;;) {
+        if (big && klo < khi) {
+            // too many for shared memory: one finer level over the row
+            const int sh = sel_shift(klo, khi);
+            sel_clear(sm);
+            __syncthreads();
+            sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+                if (in_set(x, klo, khi)) sel_add(sm, mode, sel_sub(ord_key(x), khi, sh), sel_mass(x, m));
+            });
+            __syncthreads();
+            const int sb = sel_cross(sm, mode, k, target, ca, ma);
+            const uint32_t olo = klo, ohi = khi;
+            sel_narrow(klo, khi, sb, sh);
+            if (mode == 0) {  // the mass of the candidates left above (counts were kept)
+                float a = 0.0f;
+                const uint32_t nh = khi;
+                sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+                    if (in_set(x, olo, ohi) && ord_key(x) > nh) a += sel_mass(x, m);
+                });
+                inbin_above += sel_block_sum(sm, a);
+            }
+        }
+        // collect the candidates (counting them, with their key range)
         if (threadIdx.x == 0) {
+            sm.n = 0u;
             sm.kmin = 0xFFFFFFFFu;
             sm.kmax = 0u;
         }
         __syncthreads();
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+        float am = 0.0f;
         sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
-            if (in_set(x, 0u, 0xFFFFFFFFu)) {
+            if (first && x >= xmin && sel_bin1(x, m) < b1) am += sel_mass(x, m);
+            if (in_set(x, klo, khi)) {
                 const uint32_t kv = ord_key(x);
                 lo = min(lo, kv);
                 hi = max(hi, kv);
+                const uint32_t at = atomicAdd(&sm.n, 1u);
+                if (at < static_cast<uint32_t>(kSelPool)) sm.pool[at] = x;
             }
         });
         atomicMin(&sm.kmin, lo);
         atomicMax(&sm.kmax, hi);
+        if (first) above_mass = sel_block_sum(sm, am);  // (synchronises)
         __syncthreads();
-        klo = sm.kmin;
-        khi = sm.kmax;
+        first = false;
+        n = sm.n;
+        const uint32_t nlo = sm.kmin, nhi = sm.kmax;
         __syncthreads();
-    }
-    while (cnt > static_cast<uint32_t>(kSelPool) && klo < khi) {
-        const int sh = sel_shift(klo, khi);
-        sel_clear(sm);
-        __syncthreads();
-        sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
-            if (in_set(x, klo, khi)) {
-                const int sb = sel_sub(ord_key(x), khi, sh);
-                atomicAdd(&sm.hc[warp][sb], 1u);
-                atomicAdd(&sm.hm[warp][sb], sel_mass(x, m));
-            }
-        });
-        __syncthreads();
-        const int sb = sel_cross(sm, mode, k, target, ca, ma, cnt, cmass);
-        sel_narrow(klo, khi, sb, sh);
-    }
-    if (cnt > static_cast<uint32_t>(kSelPool)) {  // one value held by more tokens than fit
-        gcnt = cnt;
-        gmass = cmass;
-        return key_value(khi);
-    }
-    // collect them and go on in shared memory
-    if (threadIdx.x == 0) sm.n = 0u;
-    __syncthreads();
-    sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
-        if (in_set(x, klo, khi)) {
-            const uint32_t at = atomicAdd(&sm.n, 1u);
-            if (at < static_cast<uint32_t>(kSelPool)) sm.pool[at] = x;
+        if (n <= static_cast<uint32_t>(kSelPool)) break;
+        klo = nlo;
+        khi = nhi;
+        big = true;
+        if (klo == khi) {  // one value held by more tokens than fit
+            gmass = static_cast<float>(n) * sel_mass(key_value(khi), m);
+            return key_value(khi);
         }
-    });
-    __syncthreads();
-    uint32_t n = min(sm.n, static_cast<uint32_t>(kSelPool));
+    }
+    // in shared memory: one finer level at a time down to a single value
     for (;;) {
-        // one value left (keys of -0 / +0 differ, values do not)?
         if (threadIdx.x == 0) {
             sm.kmin = 0xFFFFFFFFu;
             sm.kmax = 0u;
@@ -1623,47 +1654,36 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         klo = sm.kmin;
         khi = sm.kmax;
         __syncthreads();
-        if (n == 0u || key_value(klo) == key_value(khi)) break;
+        if (n == 0u || klo == khi) break;  // one value left
         const int sh = sel_shift(klo, khi);
         sel_clear(sm);
         __syncthreads();
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
             const float x = sm.pool[e];
-            const int sb = sel_sub(ord_key(x), khi, sh);
-            atomicAdd(&sm.hc[warp][sb], 1u);
-            atomicAdd(&sm.hm[warp][sb], sel_mass(x, m));
+            sel_add(sm, mode, sel_sub(ord_key(x), khi, sh), sel_mass(x, m));
         }
         __syncthreads();
-        uint32_t c2;
-        float m2;
-        const int sb = sel_cross(sm, mode, k, target, ca, ma, c2, m2);
+        const int sb = sel_cross(sm, mode, k, target, ca, ma);
         uint32_t nlo = klo, nhi = khi;
         sel_narrow(nlo, nhi, sb, sh);
         if (threadIdx.x == 0) sm.n = 0u;
         __syncthreads();
+        float a = 0.0f;
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
             const float x = sm.pool[e];
             const uint32_t kv = ord_key(x);
             if (kv >= nlo && kv <= nhi) sm.pool2[atomicAdd(&sm.n, 1u)] = x;
+            else if (kv > nhi) a += sel_mass(x, m);
         }
-        __syncthreads();
+        inbin_above += sel_block_sum(sm, a);  // (synchronises)
         n = sm.n;
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) sm.pool[e] = sm.pool2[e];
         __syncthreads();
     }
-    // the group of x*: count and mass
     const float xs = n ? key_value(khi) : -kInf;
     float gm = 0.0f;
     for (uint32_t e = threadIdx.x; e < n; e += kThreads) gm += sel_mass(sm.pool[e], m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) gm += __shfl_xor_sync(0xFFFFFFFFu, gm, o);
-    if ((threadIdx.x & 31) == 0) sm.wm[warp] = gm;
-    __syncthreads();
-    float tot = 0.0f;
-    for (int w = 0; w < kWarps; ++w) tot += sm.wm[w];
-    gcnt = n;
-    gmass = tot;
-    __syncthreads();
+    gmass = sel_block_sum(sm, gm);
     return xs;
 }
 
@@ -1673,7 +1693,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectParams P)
 {
     __shared__ SelSmem sm;
-    const int row = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row = blockIdx.x, lane = threadIdx.x & 31;
     const int i = row_request(P.rq.cu, P.rq.n, row, lane);
     bool greedy;
     const float invT = request_invT(P.rq, i, greedy);
@@ -1691,59 +1711,42 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     combine_row(P.part, row, P.V, P.maxseg, P.base_off, P.chunk, invT * kLog2e, L, s0, idx);
     const float m = __fmul_rn(L, invT);
 
-    // level 1: count and mass per bin of 1/8 nat
-    sel_clear(sm);
-    __syncthreads();
-    sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
-        const int b = sel_bin1(x, m);
-        atomicAdd(&sm.hc[warp][b], 1u);
-        atomicAdd(&sm.hm[warp][b], sel_mass(x, m));
-    });
-    __syncthreads();
-    // Z: the mass of the top-k set, or of the row
-    float Z = 0.0f, tau = -kInf, Sk = 0.0f;
-    uint32_t gcnt;
-    float gmass;
-    if (use_k) {
-        uint32_t ca = 0u, cnt;
-        float ma = 0.0f, bm;
-        const int bk = sel_cross(sm, 0, static_cast<uint32_t>(k), 0.0f, ca, ma, cnt, bm);
-        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, -kInf, cnt, bm, 0,
-                                   static_cast<uint32_t>(k), 0.0f, ca, ma, gcnt, gmass);
-        Z = ma + gmass;
-    } else {
-        float t = 0.0f;
-        for (int w = 0; w < kWarps; ++w) t += sm.hm[w][threadIdx.x];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xFFFFFFFFu, t, o);
-        if (lane == 0) sm.wm[warp] = t;
+    float tau = -kInf, Z = 0.0f, Sk;
+    if (use_k) {  // level 1 by counts: tau_k, then Z = the mass of the top-k set
+        sel_clear(sm);
         __syncthreads();
-        for (int w = 0; w < kWarps; ++w) Z += sm.wm[w];
+        sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) { sel_add(sm, 0, sel_bin1(x, m), 0.0f); });
         __syncthreads();
+        uint32_t ca = 0u;
+        float ma = 0.0f, above, inbin, gm;
+        const int bk = sel_cross(sm, 0, static_cast<uint32_t>(k), 0.0f, ca, ma);
+        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, -kInf, 0, static_cast<uint32_t>(k),
+                                   0.0f, ca, ma, above, inbin, gm);
+        Z = above + (inbin + gm);  // the bins above bk, then bk's tokens at or above tau_k
     }
     Sk = Z;
     if (use_p) {
+        // level 1 by masses, over the top-k set (every token without top-k)
+        sel_clear(sm);
+        __syncthreads();
+        const float tk = tau;
+        float zt = 0.0f;
+        sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
+            if (x >= tk) {
+                const float t = sel_mass(x, m);
+                zt += t;
+                sel_add(sm, 1, sel_bin1(x, m), t);
+            }
+        });
+        const float zsum = sel_block_sum(sm, zt);  // (synchronises)
+        if (!use_k) Z = zsum;
         const float target = __fmul_rn(fmaxf(Pp, 1e-6f), Z);
-        // level 1 again over the top-k set only (the bins hold tokens >= tau_k)
-        if (use_k) {
-            sel_clear(sm);
-            __syncthreads();
-            sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
-                if (x >= tau) {
-                    const int b = sel_bin1(x, m);
-                    atomicAdd(&sm.hc[warp][b], 1u);
-                    atomicAdd(&sm.hm[warp][b], sel_mass(x, m));
-                }
-            });
-            __syncthreads();
-        }
-        uint32_t ca = 0u, cnt;
-        float ma = 0.0f, bm;
-        const int bp = sel_cross(sm, 1, 0u, target, ca, ma, cnt, bm);
-        const float xs = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bp, tau, cnt, bm, 1, 0u,
-                                              target, ca, ma, gcnt, gmass);
-        tau = xs;
-        Sk = ma + gmass;
+        uint32_t ca = 0u;
+        float ma = 0.0f, above, inbin, gm;
+        const int bp = sel_cross(sm, 1, 0u, target, ca, ma);
+        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bp, tk, 1, 0u, target, ca, ma, above,
+                                   inbin, gm);
+        Sk = ma + gm;
     }
     if (threadIdx.x == 0) {
         P.sel_tau[row] = tau;
