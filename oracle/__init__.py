@@ -83,6 +83,13 @@ def lib():
         L.spec_verify_ref_draft_probs.restype = None
         L.spec_verify_ref_select_row.argtypes = [vp, i32, i32, f32, vp, vp, vp]
         L.spec_verify_ref_select_row.restype = None
+        L.spec_verify_ref_shard_stats.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
+        L.spec_verify_ref_shard_stats.restype = None
+        L.spec_verify_ref_shard_race.argtypes = [vp, i32, i32, i32, i32, vp, i32, vp, vp, vp, vp, vp,
+                                                 u64, u32, i32, i32, vp]
+        L.spec_verify_ref_shard_race.restype = None
+        L.spec_verify_ref_shard_finish.argtypes = [vp, i32, vp, vp, i32, i32, vp, vp, vp]
+        L.spec_verify_ref_shard_finish.restype = None
         L.spec_verify_ref_race_clocks.argtypes = [u64, u32, u32, i32, vp]
         L.spec_verify_ref_race_clocks.restype = None
         _lib = L
@@ -144,6 +151,56 @@ def synthetic_rates(mean_length: float, num_spec: int) -> np.ndarray:
     if lib().spec_verify_ref_synthetic_rates(float(mean_length), num_spec, _p(out)) != 0:
         raise ValueError("mean length must lie in [1, num_spec + 1]")
     return out
+
+
+SHARD_STATS = np.dtype([("ymax", "<f4"), ("amax", "<i4"), ("s", "<f8"), ("ld", "<f4"),
+                        ("qd", "<f4")], align=True)
+SHARD_RACE = np.dtype([("jstar", "<i4"), ("token", "<i4"), ("res_key", "<f4"), ("res_idx", "<i4"),
+                       ("p_key", "<f4"), ("p_idx", "<i4")], align=True)
+
+
+class ShardOracle:
+    """The two-exchange protocol of vocabulary-sharded verification, one rank's side: the
+    arrays passed in are this rank's columns [v0, v0 + Vs) of the logits (and of the draft
+    probabilities). Exchange records are numpy structured arrays (SHARD_STATS / SHARD_RACE)."""
+
+    def __init__(self, batch, v0: int, shard_vocab: int):
+        self.b, self.v0, self.Vs = batch, int(v0), int(shard_vocab)
+        lg = np.ascontiguousarray(batch.logits)
+        self.logits = np.ascontiguousarray(lg[:, self.v0:self.v0 + self.Vs])
+        self.q = None if batch.draft_probs is None else np.ascontiguousarray(
+            np.asarray(batch.draft_probs, np.float32)[:, self.v0:self.v0 + self.Vs])
+        self.ids = np.ascontiguousarray(batch.draft_ids, np.int32)
+        self.cu = np.ascontiguousarray(batch.cu_num_draft, np.int32)
+        self.T = np.ascontiguousarray(batch.temperature, np.float32)
+        self.g = np.ascontiguousarray(batch.is_greedy, np.uint8)
+        self.bf16 = int(batch.logits_dtype == "bf16")
+
+    def stats(self) -> np.ndarray:
+        out = np.zeros(self.b.num_rows, SHARD_STATS)
+        lib().spec_verify_ref_shard_stats(_p(self.logits), self.bf16, self.Vs, self.v0, _p(self.ids),
+                                          _p(self.q), _p(self.cu), _p(self.T), _p(self.g),
+                                          self.b.num_reqs, _p(out))
+        return out
+
+    def race(self, all_stats: np.ndarray, world: int) -> np.ndarray:
+        all_stats = np.ascontiguousarray(all_stats, SHARD_STATS)
+        out = np.zeros(self.b.num_reqs, SHARD_RACE)
+        lib().spec_verify_ref_shard_race(_p(self.logits), self.bf16, self.Vs, self.v0,
+                                         self.b.vocab_size, _p(all_stats), world, _p(self.ids),
+                                         _p(self.q), _p(self.cu), _p(self.T), _p(self.g), self.b.seed,
+                                         0, self.b.num_reqs, self.b.num_draft_tokens, _p(out))
+        return out
+
+    def finish(self, all_races: np.ndarray, world: int, max_spec_len: int):
+        all_races = np.ascontiguousarray(all_races, SHARD_RACE)
+        n = self.b.num_reqs
+        sampled = np.empty((n, max_spec_len + 1), np.int32)
+        ns = np.empty(n, np.int32)
+        nr = np.empty(n, np.int32)
+        lib().spec_verify_ref_shard_finish(_p(all_races), world, _p(self.ids), _p(self.cu), n,
+                                           max_spec_len, _p(sampled), _p(ns), _p(nr))
+        return sampled, ns, nr
 
 
 def select_row(x: np.ndarray, top_k: int, top_p: float):

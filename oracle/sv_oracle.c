@@ -727,3 +727,219 @@ void spec_verify_ref_race_clocks(uint64_t seed, uint32_t j, uint32_t ireq, int32
 {
     for (int32_t v = 0; v < n; ++v) out[v] = spec_verify_ref_race_clock(seed, j, ireq, v);
 }
+
+/* ------------------------------------------------------------------------------------ */
+/* Vocabulary-sharded verification. The logits (and draft probabilities) of every row are   */
+/* split by vocabulary over `world` ranks, rank r holding the columns [v0_r, v0_r + Vs_r)   */
+/* with v0_r a multiple of 64 (race-clock groups stay whole). Two exchanges reproduce the   */
+/* unsharded step: the shard statistics of every row (after which every rank evaluates the  */
+/* same acceptance tests), then each shard's best race key at the row of the first          */
+/* rejection; the largest key over the shards is the winner of the whole row's race.        */
+/* Plain processing only (x = logit / T).                                                   */
+/* ------------------------------------------------------------------------------------ */
+typedef struct {
+    float ymax;   /* largest logit of the shard */
+    int32_t amax; /* its first global index */
+    double s;     /* sum over the shard of exp(x_v - fl(ymax / T)), double, index order */
+    float ld;     /* logit of the row's draft token if the shard holds it, else NaN */
+    float qd;     /* its draft probability (1 without draft probabilities), else NaN */
+} ref_shard_stats_t;
+
+typedef struct {
+    int32_t jstar;   /* first rejection (K if none): the same on every rank */
+    int32_t token;   /* a greedy request's token (the combined argmax), else -1 */
+    float res_key;   /* the shard's best residual / exclusion key, */
+    int32_t res_idx; /* and its global index (-1: no candidate in the shard) */
+    float p_key;     /* the shard's best key of the race over p (the fallback and the bonus) */
+    int32_t p_idx;
+} ref_shard_race_t;
+
+void spec_verify_ref_shard_stats(const void *logits, int logits_bf16, int shard_vocab, int v0,
+                                 const int32_t *draft_ids, const float *draft_probs,
+                                 const int32_t *cu_num_draft, const float *temperature,
+                                 const uint8_t *is_greedy, int num_reqs,
+                                 ref_shard_stats_t *out)
+{
+    const int Vs = shard_vocab;
+    for (int i = 0; i < num_reqs; ++i) {
+        const int q0 = cu_num_draft[i], K = cu_num_draft[i + 1] - q0;
+        const float T = temperature[i];
+        const int greedy = is_greedy[i] != 0 || !(T > 0.0f);
+        const float invT = greedy ? 1.0f : 1.0f / T;
+        for (int j = 0; j <= K; ++j) {
+            const size_t row = (size_t)q0 + (size_t)i + (size_t)j, base = row * (size_t)Vs;
+            ref_shard_stats_t st;
+            st.ymax = -INFINITY;
+            st.amax = v0;
+            for (int v = 0; v < Vs; ++v) {
+                const float l = logit_at(logits, logits_bf16, base + (size_t)v);
+                if (l > st.ymax) {
+                    st.ymax = l;
+                    st.amax = v0 + v;
+                }
+            }
+            const float mr = st.ymax * invT;
+            st.s = 0.0;
+            for (int v = 0; v < Vs; ++v)
+                st.s += (double)spec_verify_ref_exp(logit_at(logits, logits_bf16, base + (size_t)v) * invT - mr);
+            st.ld = NAN;
+            st.qd = NAN;
+            if (j < K) {
+                const int32_t d = draft_ids[q0 + j];
+                if (d >= v0 && d < v0 + Vs) {
+                    st.ld = logit_at(logits, logits_bf16, base + (size_t)(d - v0));
+                    st.qd = draft_probs ? draft_probs[(size_t)(q0 + j) * Vs + (size_t)(d - v0)] : 1.0f;
+                }
+            }
+            out[row] = st;
+        }
+    }
+}
+
+/* The best key of the shard's race at row `row` (global indices; lowest index on equal keys). */
+static void shard_race_best(const void *logits, int bf16, int Vs, int v0, size_t row, float invT,
+                            float m, float S_f, const float *q, int32_t exclude, uint64_t seed,
+                            uint32_t j, uint32_t ireq, float *key, int32_t *idx)
+{
+    *key = -INFINITY;
+    *idx = -1;
+    for (int v = 0; v < Vs; ++v) {
+        const int32_t g = v0 + v;
+        if (g == exclude) continue;
+        const float x = logit_at(logits, bf16, row * (size_t)Vs + (size_t)v) * invT;
+        const float t = spec_verify_ref_exp(x - m);
+        float w = t;
+        if (q) {
+            w = fmaf(-S_f, q[v], t);
+            if (!(w > 0.0f)) continue;
+        }
+        const float k = w / spec_verify_ref_race_clock(seed, j, ireq, g);
+        if (*idx < 0 || k > *key) {
+            *key = k;
+            *idx = g;
+        }
+    }
+}
+
+void spec_verify_ref_shard_race(const void *logits, int logits_bf16, int shard_vocab, int v0,
+                                int vocab_size, const ref_shard_stats_t *all_stats, int world,
+                                const int32_t *draft_ids, const float *draft_probs,
+                                const int32_t *cu_num_draft, const float *temperature,
+                                const uint8_t *is_greedy, uint64_t seed, uint32_t req_index_base,
+                                int num_reqs, int num_draft_tokens, ref_shard_race_t *out)
+{
+    const int Vs = shard_vocab, V = vocab_size;
+    const size_t R = (size_t)num_draft_tokens + (size_t)num_reqs;
+    for (int i = 0; i < num_reqs; ++i) {
+        const int q0 = cu_num_draft[i], K = cu_num_draft[i + 1] - q0;
+        const uint32_t ireq = req_index_base + (uint32_t)i;
+        const float T = temperature[i];
+        const int greedy = is_greedy[i] != 0 || !(T > 0.0f);
+        const float invT = greedy ? 1.0f : 1.0f / T;
+        float m[K + 1], S_f[K + 1];
+        int32_t amax[K + 1];
+        int jstar = K;
+        for (int j = 0; j <= K; ++j) {
+            const size_t row = (size_t)q0 + (size_t)i + (size_t)j;
+            /* combine the shards: the largest logit (first index on ties) and the sum */
+            float ymax = -INFINITY;
+            amax[j] = 0;
+            for (int r = 0; r < world; ++r) {
+                const ref_shard_stats_t *st = all_stats + (size_t)r * R + row;
+                if (st->ymax > ymax || (st->ymax == ymax && st->amax < amax[j])) {
+                    ymax = st->ymax;
+                    amax[j] = st->amax;
+                }
+            }
+            m[j] = ymax * invT;
+            double S = 0.0;
+            for (int r = 0; r < world; ++r) {
+                const ref_shard_stats_t *st = all_stats + (size_t)r * R + row;
+                S += st->s * exp((double)(st->ymax * invT) - (double)m[j]);
+            }
+            S_f[j] = (float)S;
+            if (j < K && jstar == K) {
+                const int32_t d = draft_ids[q0 + j];
+                int acc;
+                if (greedy) {
+                    acc = d == amax[j];
+                } else if (d < 0 || d >= V) {
+                    acc = 0;
+                } else {
+                    float ld = NAN, qd = NAN;
+                    for (int r = 0; r < world; ++r) {
+                        const ref_shard_stats_t *st = all_stats + (size_t)r * R + row;
+                        if (st->ld == st->ld) {
+                            ld = st->ld;
+                            qd = st->qd;
+                        }
+                    }
+                    const float t_d = spec_verify_ref_exp(ld * invT - m[j]);
+                    const float u = spec_verify_ref_uniform(seed, 0u, (uint32_t)j, ireq, REF_TAG_ACCEPT, 0);
+                    acc = qd > 0.0f && (t_d / S_f[j]) / qd >= u;
+                }
+                if (!acc) jstar = j;
+            }
+        }
+        ref_shard_race_t o;
+        o.jstar = jstar;
+        o.token = greedy ? amax[jstar] : -1;
+        o.res_key = o.p_key = -INFINITY;
+        o.res_idx = o.p_idx = -1;
+        if (!greedy) {
+            const size_t row = (size_t)q0 + (size_t)i + (size_t)jstar;
+            if (jstar < K) {
+                const float *q = draft_probs ? draft_probs + (size_t)(q0 + jstar) * Vs : NULL;
+                const int32_t excl = draft_probs ? -1 : draft_ids[q0 + jstar];
+                shard_race_best(logits, logits_bf16, Vs, v0, row, invT, m[jstar], S_f[jstar], q, excl,
+                                seed, (uint32_t)jstar, ireq, &o.res_key, &o.res_idx);
+            }
+            shard_race_best(logits, logits_bf16, Vs, v0, row, invT, m[jstar], S_f[jstar], NULL, -1,
+                            seed, (uint32_t)jstar, ireq, &o.p_key, &o.p_idx);
+        }
+        out[i] = o;
+    }
+}
+
+/* The winner over the shards, and the emitted row: the residual (or exclusion) race when j* < K
+ * and some shard has a candidate, else the race over p. */
+void spec_verify_ref_shard_finish(const ref_shard_race_t *all_races, int world,
+                                  const int32_t *draft_ids, const int32_t *cu_num_draft,
+                                  int num_reqs, int max_spec_len, int32_t *sampled,
+                                  int32_t *num_sampled, int32_t *num_rejected)
+{
+    const int stride = max_spec_len + 1;
+    for (int i = 0; i < num_reqs; ++i) {
+        const int q0 = cu_num_draft[i], K = cu_num_draft[i + 1] - q0;
+        const ref_shard_race_t *o0 = all_races + i;
+        const int jstar = o0->jstar;
+        int32_t token = o0->token;
+        if (token < 0) {
+            float best = -INFINITY;
+            int32_t bi = -1;
+            if (jstar < K)
+                for (int r = 0; r < world; ++r) {
+                    const ref_shard_race_t *o = all_races + (size_t)r * num_reqs + i;
+                    if (o->res_idx >= 0 && (bi < 0 || o->res_key > best || (o->res_key == best && o->res_idx < bi))) {
+                        best = o->res_key;
+                        bi = o->res_idx;
+                    }
+                }
+            if (bi < 0)
+                for (int r = 0; r < world; ++r) {
+                    const ref_shard_race_t *o = all_races + (size_t)r * num_reqs + i;
+                    if (o->p_idx >= 0 && (bi < 0 || o->p_key > best || (o->p_key == best && o->p_idx < bi))) {
+                        best = o->p_key;
+                        bi = o->p_idx;
+                    }
+                }
+            token = bi;
+        }
+        int32_t *out = sampled + (size_t)i * stride;
+        for (int j = 0; j < jstar; ++j) out[j] = draft_ids[q0 + j];
+        out[jstar] = token;
+        for (int s = jstar + 1; s < stride; ++s) out[s] = -1;
+        num_sampled[i] = jstar + 1;
+        num_rejected[i] = K - jstar;
+    }
+}

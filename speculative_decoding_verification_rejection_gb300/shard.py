@@ -61,3 +61,43 @@ def make_shard(cu_num_draft, lo: int, hi: int) -> Shard:
 
 def shards(cu_num_draft, world_size: int) -> list[Shard]:
     return [make_shard(cu_num_draft, lo, hi) for lo, hi in shard_bounds(cu_num_draft, world_size)]
+
+
+# ---------------------------------------------------------------------------------------------
+# Vocabulary sharding: every rank holds a column range of every logit row (a tensor-parallel LM
+# head's output), and two small exchanges replace gathering the rows.
+# ---------------------------------------------------------------------------------------------
+VOCAB_ALIGN = 64  # shard boundaries on race-clock groups of 64 tokens
+
+
+def vocab_bounds(vocab_size: int, world_size: int) -> list[tuple[int, int]]:
+    """Column ranges [v0, v1), one per rank, each starting on a multiple of 64 tokens (a race
+    clock group never straddles two ranks), as even as that allows; trailing ranks may be empty."""
+    if world_size < 1 or vocab_size < 1:
+        raise ValueError("world_size and vocab_size must be >= 1")
+    step = -(-vocab_size // world_size)
+    step = -(-step // VOCAB_ALIGN) * VOCAB_ALIGN
+    return [(min(vocab_size, r * step), min(vocab_size, (r + 1) * step)) for r in range(world_size)]
+
+
+def sharded_verify(backend, all_gather, world_size: int, max_spec_len: int):
+    """One verification step over vocabulary shards, on one rank.
+
+    backend: this rank's side of the protocol, with
+      stats()                      -> this rank's statistics record of every logit row
+      race(all_stats, world_size)  -> this rank's race record of every request, given the
+                                      statistics of all ranks (rank-major)
+      finish(all_races, world_size, max_spec_len) -> (sampled, num_sampled, num_rejected)
+    all_gather(x): the records of every rank stacked in rank order (the exchange).
+
+    Exchange 1 carries, per row, the shard's largest logit with its first index, its sum of
+    exponentials and, from the shard holding the row's draft token, that token's logit and draft
+    probability: every rank then combines the same numbers in the same order and takes the same
+    acceptance decisions. Exchange 2 carries, per request, each shard's best race key at the row
+    of the first rejection (residual or exclusion race, and the race over p for the fallback and
+    the bonus); the largest key over the shards is the winner of the whole row, since every key
+    is computed with the combined maximum and sum and the global race clocks.
+    """
+    all_stats = all_gather(backend.stats())
+    all_races = all_gather(backend.race(all_stats, world_size))
+    return backend.finish(all_races, world_size, max_spec_len)
