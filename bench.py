@@ -13,6 +13,7 @@ Prints one JSON line (rank 0). Metric: verified draft positions per second, whol
 logits replace the fp32 distributions, and q = softmax(draft logits / T) is computed in the call.
 --synthetic-length L measures synthetic acceptance (per-position rates of mean length L).
 --top-p P, --top-k K and --frequency-penalty measure the logits processors on the same recipe.
+--vocab-shards N measures the vocabulary-sharded protocol (N ranks' calls in turn on one GPU).
 Under torchrun (N > 1) every rank verifies its own batch (weak scaling, no collective on the
 data path); the step time is the maximum over ranks.
 """
@@ -63,6 +64,9 @@ def parse_args():
     p.add_argument("--top-k", type=int, default=None, help="top-k of every request")
     p.add_argument("--frequency-penalty", action="store_true",
                    help="a frequency penalty with seeded output-token counts per request")
+    p.add_argument("--vocab-shards", type=int, default=1,
+                   help="vocabulary-sharded verification with N shards, their calls emulated in "
+                        "turn on one GPU (the exchange a concatenation)")
     return p.parse_args()
 
 
@@ -318,6 +322,26 @@ def run_ours(args, world, rank, local):
         ctx.run(d_logits, d_ids, d_q, d_cu, d_T, d_g, b.seed, req_index_base=base,
                 max_spec_len=kmax, out=outs, draft_logits=d_dl, **extras)
 
+    if args.vocab_shards > 1:
+        from speculative_decoding_verification_rejection_gb300.shard import ShardBackend, vocab_bounds
+        sides = []
+        for lo, hi in [bd for bd in vocab_bounds(V, args.vocab_shards) if bd[1] > bd[0]]:
+            sl = torch.from_numpy(np.ascontiguousarray(logits_np[:, lo:hi])).to(dev)
+            sq = torch.from_numpy(np.ascontiguousarray(b.draft_probs[:, lo:hi])).to(dev) \
+                if b.draft_probs is not None else None
+            sctx = sv.SpecVerify(n, kmax, hi - lo, b.logits_dtype, b.draft_probs is not None,
+                                 device=local)
+            sides.append(ShardBackend(sctx, lo, V, sl, d_ids, sq, d_cu, d_T, d_g, b.seed,
+                                      req_index_base=base, max_spec_len=kmax))
+        del d_logits, d_q
+
+        def step():  # noqa: F811 - the sharded step replaces the plain one
+            all_stats = torch.cat([sd.stats() for sd in sides])
+            all_races = torch.cat([sd.race(all_stats, len(sides)) for sd in sides])
+            out = sides[0].finish(all_races, len(sides), kmax)
+            for o, t in zip(outs, out):
+                o.copy_(t)
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -351,18 +375,23 @@ def run_ours(args, world, rank, local):
     mean_sampled = float(outs[1].float().mean().item())
 
     # per-kernel durations: CUDA events between the kernels, on the launching stream
-    ctx.set_profiling(True)
-    prof_steps = max(1, min(args.profile_steps, args.steps))
-    for _ in range(prof_steps):
-        step()
-    torch.cuda.synchronize()
-    kms, calls = ctx.get_profile()
-    ctx.set_profiling(False)
-    kavg = {k: v / max(calls, 1) for k, v in kms.items()}
+    sharded = args.vocab_shards > 1
+    kavg, calls = None, 0
+    if not sharded:
+        ctx.set_profiling(True)
+        prof_steps = max(1, min(args.profile_steps, args.steps))
+        for _ in range(prof_steps):
+            step()
+        torch.cuda.synchronize()
+        kms, calls = ctx.get_profile()
+        ctx.set_profiling(False)
+        kavg = {k: v / max(calls, 1) for k, v in kms.items()}
 
     # end to end through the host-buffer entry point: H2D of the inputs, verify, D2H of results
     e2e = None
-    if not args.no_e2e and (d_dl is not None or extras):
+    if sharded:
+        pass  # the emulated ranks share one GPU: no end-to-end figure
+    elif not args.no_e2e and (d_dl is not None or extras):
         e2e = e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist)
     elif not args.no_e2e:
         ctx.reserve_host_io()
@@ -418,8 +447,15 @@ def run_ours(args, world, rank, local):
         stats_bytes += nd * V * b.elem_bytes
     if b.frequency_penalty is not None:    # every request's counts row read once
         stats_bytes += n * V * 4
-    achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
-    plain = not extras and b.synthetic_rates is None
+    if sharded:  # the whole emulated step: every shard's statistics pass reads its columns once
+        achieved = stats_bytes / (ms_per_step / 1e3) / 1e9
+    else:
+        achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
+    plain = not extras and b.synthetic_rates is None and not sharded
+    # our kernels per step: statistics + verify (+ the top-k / top-p selection); sharded: each
+    # shard's statistics, export and race, and one finish
+    launches_per_step = (3 * len(sides) + 1 if sharded else
+                         sv.spec_verify_launches_per_run() + int(b.top_k is not None or b.top_p is not None))
     traffic, traffic_src = (recorded_traffic("stats_kernel_workload3_draft_logits.md" if d_dl is not None
                                              else "stats_kernel_workload3.md")
                             if plain and args.workload == 3 else (None, "no ncu summary for this mode"))
@@ -432,21 +468,25 @@ def run_ours(args, world, rank, local):
     cfg.update({"l2": "inputs larger than L2 (no flush between steps)", "parallelism":
                 f"replicas x{world}" if world > 1 else "single GPU",
                 "req_index_base": "rank * num_reqs"})
+    if sharded:
+        cfg["vocab_shards"] = f"{len(sides)} shards on 64-token boundaries, their calls in turn on one GPU"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
-        "e2e": e2e, "gpu_launches": sv.spec_verify_launches_per_run() * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "sv_stats_kernel (row statistics: reads every logit once, "
-                                               "writes one maximum per 64-element line"
-                                               + ("; also reads every draft logit once)" if d_dl is not None else ")"),
+        "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "kernel": ("whole sharded step (every shard's kernels, the bytes of "
+                                                "the statistics passes)") if sharded else
+                     "sv_stats_kernel (row statistics: reads every logit once, "
+                     "writes one maximum per 64-element line"
+                     + ("; also reads every draft logit once)" if d_dl is not None else ")"),
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes_per_launch": stats_bytes},
         "cpu_baseline": cpu,
         "clocks": clocks,
-        "kernel_ms": {**kavg, "profiled_calls": calls},
+        "kernel_ms": {**kavg, "profiled_calls": calls} if kavg else None,
         "rows_per_s": world * b.num_rows / (ms_per_step / 1e3),
         # all input bytes of the batch (logits + every draft distribution) per step time; the
         # path reads every logit but only the q entries it needs

@@ -272,6 +272,66 @@ int spec_verify_set_synthetic(spec_verify_ctx *ctx, const float *rates, int n);
 int spec_verify_synthetic_rates(double mean_length, int num_spec, float *rates);
 
 /*
+ * Vocabulary-sharded verification: the logits arrive split by vocabulary over `world` ranks (a
+ * tensor-parallel LM head), rank r holding columns [v0_r, v0_r + Vs_r) of every row, each v0 a
+ * multiple of 64 (race-clock groups stay on one rank). Instead of gathering the rows, each rank
+ * makes three calls around two all-gathers of small records (the caller's collective):
+ *   1. spec_verify_shard_stats: the shard's statistics record of every logit row;
+ *      all-gather them (rank-major: [world][rows]);
+ *   2. spec_verify_shard_race: every rank combines the records in rank order (so all take the
+ *      same acceptance decisions, [spec-notes] 8.2 / 8.3), then races its shard at the row of
+ *      the first rejection with the combined maximum and sum and the global race clocks; one
+ *      record per request; all-gather them ([world][num_reqs]);
+ *   3. spec_verify_shard_finish: the largest key over the shards wins (the residual or
+ *      exclusion race where some shard has a candidate, else the race over p), and the outputs
+ *      are written as by spec_verify_run.
+ * The result equals spec_verify_run on the whole rows (up to S, summed in another order). The
+ * context is created for the SHARD: vocab_size = Vs. Calls 1 and 2 of a step use the same
+ * context on the same stream (2 reads what 1 left in its scratch). All pointers are device
+ * pointers; draft_probs is the shard's columns [num_draft_tokens, Vs] or NULL. The batch must be
+ * consistent (cu_num_draft as for spec_verify_run); logits processors, draft logits and
+ * synthetic acceptance are not offered here.
+ */
+typedef struct spec_verify_shard_stat {
+    float max_logit;    /* largest logit of the shard's part of the row */
+    float sumexp;       /* sum over it of exp((logit - max_logit) / T) (greedy: T = 1) */
+    int32_t argmax;     /* global index of the first largest logit */
+    float draft_logit;  /* the row's draft token's logit if this shard holds it, else NaN */
+    float draft_prob;   /* its draft probability (1 without draft_probs) if held, else NaN */
+    int32_t reserved;
+} spec_verify_shard_stat;
+
+typedef struct spec_verify_shard_key {
+    int32_t jstar;          /* first rejected position (K if none), the same on every rank */
+    int32_t token;          /* a greedy request's token, else -1 */
+    float residual_key;     /* the shard's best key of the residual / exclusion race */
+    int32_t residual_index; /* its global token, -1 if the shard has no candidate */
+    float p_key;            /* the shard's best key of the race over p (the bonus; the fallback,
+                               taken only where the shard's own residual is empty) */
+    int32_t p_index;
+} spec_verify_shard_key;
+
+int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int v0,
+                            const int32_t *draft_ids, const float *draft_probs_shard,
+                            const int32_t *cu_num_draft, const float *temperature,
+                            const uint8_t *is_greedy, int num_reqs, int num_draft_tokens,
+                            int max_spec_len_this_batch, spec_verify_shard_stat *out,
+                            void *cuda_stream);
+
+int spec_verify_shard_race(spec_verify_ctx *ctx, const void *logits_shard, int v0, int vocab_size,
+                           const spec_verify_shard_stat *all_stats, int world,
+                           const int32_t *draft_ids, const float *draft_probs_shard,
+                           const int32_t *cu_num_draft, const float *temperature,
+                           const uint8_t *is_greedy, uint64_t seed, uint32_t req_index_base,
+                           int num_reqs, int num_draft_tokens, int max_spec_len_this_batch,
+                           spec_verify_shard_key *out, void *cuda_stream);
+
+int spec_verify_shard_finish(spec_verify_ctx *ctx, const spec_verify_shard_key *all_races,
+                             int world, const int32_t *draft_ids, const int32_t *cu_num_draft,
+                             int num_reqs, int max_spec_len_this_batch, int32_t *sampled,
+                             int32_t *num_sampled, int32_t *num_rejected, void *cuda_stream);
+
+/*
  * Allocate device staging buffers sized for the context's capacity (logits, draft_probs if
  * SV_DRAFT_PROBS, and the small per-request arrays) so that spec_verify_run_host can be used.
  */

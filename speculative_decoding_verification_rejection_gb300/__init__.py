@@ -125,6 +125,10 @@ def lib():
     L.spec_verify_run_draft_logits.argtypes = list(L.spec_verify_run.argtypes)
     L.spec_verify_run_batch.argtypes = [vp, ctypes.POINTER(Batch), ctypes.POINTER(Outputs), vp]
     L.spec_verify_set_synthetic.argtypes = [vp, vp, i32]
+    L.spec_verify_shard_stats.argtypes = [vp, vp, i32, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp]
+    L.spec_verify_shard_race.argtypes = [vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp, u64, u32,
+                                         i32, i32, i32, vp, vp]
+    L.spec_verify_shard_finish.argtypes = [vp, vp, i32, vp, vp, i32, i32, vp, vp, vp, vp]
     L.spec_verify_synthetic_rates.argtypes = [ctypes.c_double, i32, vp]
     L.spec_verify_run_host.argtypes = [vp, vp, vp, vp, vp, vp, vp, u64, u32, i32, i32, i32, vp, vp,
                                        vp, vp]
@@ -142,6 +146,7 @@ def lib():
     L.spec_verify_status_string.restype = ctypes.c_char_p
     for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_draft_logits",
               "spec_verify_run_batch", "spec_verify_set_synthetic", "spec_verify_synthetic_rates",
+              "spec_verify_shard_stats", "spec_verify_shard_race", "spec_verify_shard_finish",
               "spec_verify_run_host", "spec_verify_run_noalloc",
               "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
               "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
@@ -243,6 +248,40 @@ def spec_verify_synthetic_rates(mean_length: float, num_spec: int):
                                              out.ctypes.data if out.size else None),
            "spec_verify_synthetic_rates")
     return out
+
+
+SHARD_RECORD_BYTES = 24  # spec_verify_shard_stat and spec_verify_shard_key
+
+
+def spec_verify_shard_stats(ctx, logits_shard, v0, draft_ids, draft_probs_shard, cu_num_draft,
+                            temperature, is_greedy, num_reqs, num_draft_tokens,
+                            max_spec_len_this_batch, out, cuda_stream=None) -> None:
+    _check(lib().spec_verify_shard_stats(ctx, _ptr(logits_shard), v0, _ptr(draft_ids),
+                                         _ptr(draft_probs_shard), _ptr(cu_num_draft),
+                                         _ptr(temperature), _ptr(is_greedy), num_reqs,
+                                         num_draft_tokens, max_spec_len_this_batch, _ptr(out),
+                                         _stream_handle(cuda_stream)), "spec_verify_shard_stats")
+
+
+def spec_verify_shard_race(ctx, logits_shard, v0, vocab_size, all_stats, world, draft_ids,
+                           draft_probs_shard, cu_num_draft, temperature, is_greedy, seed,
+                           req_index_base, num_reqs, num_draft_tokens, max_spec_len_this_batch,
+                           out, cuda_stream=None) -> None:
+    _check(lib().spec_verify_shard_race(ctx, _ptr(logits_shard), v0, vocab_size, _ptr(all_stats),
+                                        world, _ptr(draft_ids), _ptr(draft_probs_shard),
+                                        _ptr(cu_num_draft), _ptr(temperature), _ptr(is_greedy),
+                                        seed, req_index_base, num_reqs, num_draft_tokens,
+                                        max_spec_len_this_batch, _ptr(out),
+                                        _stream_handle(cuda_stream)), "spec_verify_shard_race")
+
+
+def spec_verify_shard_finish(ctx, all_races, world, draft_ids, cu_num_draft, num_reqs,
+                             max_spec_len_this_batch, sampled, num_sampled, num_rejected,
+                             cuda_stream=None) -> None:
+    _check(lib().spec_verify_shard_finish(ctx, _ptr(all_races), world, _ptr(draft_ids),
+                                          _ptr(cu_num_draft), num_reqs, max_spec_len_this_batch,
+                                          _ptr(sampled), _ptr(num_sampled), _ptr(num_rejected),
+                                          _stream_handle(cuda_stream)), "spec_verify_shard_finish")
 
 
 def spec_verify_run_host(ctx, logits, draft_ids, draft_probs, cu_num_draft, temperature,

@@ -949,6 +949,7 @@ struct RaceRow {
     int excl;           // token left out (rejected draft without q), or -1
     float m, S, invT;
     uint32_t j, ireq, k0, k1;  // Philox counter words 1, 2 and key
+    uint32_t g0;               // group of the row's token 0 (a vocabulary shard's first group)
 };
 
 // Shared memory of the search (one CTA). Each warp keeps a queue of candidate tokens (at most
@@ -1038,7 +1039,7 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
             const int g = min(g0 + k * kThreads, r.G - 1);
             const int v0 = g * kGroup, v1 = min(v0 + kGroup, r.V) - 1;
             lmax[k] = fmaxf(sm.lm[rl.of(v0)], sm.lm[rl.of(v1)]);
-            h[k] = sv::philox4x32_10(static_cast<uint32_t>(g), r.j, r.ireq, sv::kClockHead, r.k0, r.k1);
+            h[k] = sv::philox4x32_10(static_cast<uint32_t>(g) + r.g0, r.j, r.ireq, sv::kClockHead, r.k0, r.k1);
         }
 #pragma unroll
         for (int k = 0; k < kStep; ++k) {
@@ -1097,7 +1098,7 @@ __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
                 float Ev = E;
                 if (slot != sm.ag[g]) {
                     const sv::Philox4 sl = sv::philox4x32_10(
-                        static_cast<uint32_t>(g), r.j, r.ireq,
+                        static_cast<uint32_t>(g) + r.g0, r.j, r.ireq,
                         sv::kClockHead + 1u + static_cast<uint32_t>(slot >> 2), r.k0, r.k1);
                     const uint32_t ws = (slot & 2) ? ((slot & 1) ? sl.w : sl.z) : ((slot & 1) ? sl.y : sl.x);
                     Ev = __fadd_rn(E, -sv::log_f32(sv::uniform_from_word(ws)));
@@ -1754,6 +1755,266 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// 4. vocabulary shards: this rank holds columns [v0, v0 + Vs) of every row, v0 a multiple of 64
+// ---------------------------------------------------------------------------------------
+// Exchange 1: each row's statistics record, from the statistics partials of the shard.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+sv_shard_export_kernel(const T *__restrict__ logits, RequestTable rq,
+                       const int32_t *__restrict__ draft_ids, const float *__restrict__ q,
+                       const StatPart *__restrict__ part, int Vs, int v0, int maxseg,
+                       int base_off, Divisor chunk, int R, spec_verify_shard_stat *__restrict__ out)
+{
+    const int lane = threadIdx.x & 31;
+    const int row = static_cast<int>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
+    if (row >= R) return;  // whole warps
+    const int i = row_request(rq.cu, rq.n, row, lane);
+    const int q0 = __ldg(rq.cu + i), K = __ldg(rq.cu + i + 1) - q0, j = row - q0 - i;
+    bool greedy;
+    const float invT = request_invT(rq, i, greedy);
+    float L, sx;
+    int idx;
+    combine_row(part, row, Vs, maxseg, base_off, chunk, invT * kLog2e, L, sx, idx);
+    if (lane == 0) {
+        spec_verify_shard_stat rec;
+        rec.max_logit = L;
+        rec.sumexp = sx;
+        rec.argmax = v0 + (idx == INT_MAX ? 0 : idx);
+        rec.draft_logit = __int_as_float(0x7FC00000);
+        rec.draft_prob = __int_as_float(0x7FC00000);
+        rec.reserved = 0;
+        if (j >= 0 && j < K && q0 + j < R - rq.n) {  // (a malformed cu_num_draft reads nothing)
+            const int d = __ldg(draft_ids + q0 + j);
+            if (d >= v0 && d < v0 + Vs) {
+                rec.draft_logit = Elem<T>::at(logits + static_cast<size_t>(row) * Vs, d - v0);
+                rec.draft_prob = q ? __ldg(q + static_cast<size_t>(q0 + j) * Vs + (d - v0)) : 1.0f;
+            }
+        }
+        out[row] = rec;
+    }
+}
+
+struct ShardParams {
+    RequestTable rq;
+    const int32_t *draft_ids;
+    const float *q;                        // the shard's columns [nd, Vs], or nullptr
+    const spec_verify_shard_stat *recs;    // [world][R]
+    int world, R, V, Vs, v0, kmax, base_off;
+    uint64_t seed;
+    uint32_t req_base;
+    spec_verify_shard_key *out;
+};
+
+// Exchange 2: combine every rank's records (rank order: the same numbers on every rank), take
+// the acceptance decisions, and race this shard at the row of the first rejection. One CTA per
+// request.
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
+                     const __grid_constant__ ShardParams P)
+{
+    extern __shared__ __align__(16) unsigned char dyn[];
+    __shared__ int s_js;
+    __shared__ unsigned long long s_best;
+    __shared__ int s_cnt;
+    __shared__ int s_bin_n[kBins];
+    __shared__ unsigned s_bin_max[kBins];
+    __shared__ unsigned s_top;
+    __shared__ uint32_t s_qgs[kWarps * kQueue];
+    __shared__ float s_ql[kWarps * kQueue], s_qq[kWarps * kQueue];
+    const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q0 = __ldg(P.rq.cu + i), K = __ldg(P.rq.cu + i + 1) - q0;
+    const VerifyLayout lay = verify_layout(P.Vs, P.kmax);
+    {  // the batch must be consistent (as in the verify kernel); otherwise j* = -1: nothing emitted
+        const int n = P.rq.n, nd = P.R - n;
+        int bad = 0;
+        for (int t = tid; t <= n; t += kThreads) {
+            const int c0 = __ldg(P.rq.cu + t);
+            if (t == 0) bad |= c0 != 0;
+            if (t == n) bad |= c0 != nd;
+            if (t < n) {
+                const int c1 = __ldg(P.rq.cu + t + 1);
+                bad |= (c1 < c0) | (static_cast<long long>(c1) - c0 > P.kmax) | (c0 < 0) | (c1 > nd);
+            }
+        }
+        if (__syncthreads_or(bad)) {
+            if (tid == 0) P.out[i] = spec_verify_shard_key{-1, -1, 0.0f, -1, 0.0f, -1};
+            return;
+        }
+    }
+    bool greedy;
+    const float invT = request_invT(P.rq, i, greedy);
+    const float c = invT * kLog2e;
+    const uint32_t ireq = P.req_base + static_cast<uint32_t>(i);
+    const int stride = P.kmax + 1;
+    float *sm_m = reinterpret_cast<float *>(dyn + lay.rows), *sm_S = sm_m + stride;
+    int *sm_amax = reinterpret_cast<int *>(sm_m + 2 * stride);
+    if (tid == 0) s_js = K;
+    __syncthreads();
+    for (int j = warp; j <= K; j += kWarps) {
+        const int row = q0 + i + j;
+        float L = -kInf, sx = 0.0f, ld = __int_as_float(0x7FC00000), qd = ld;
+        int idx = INT_MAX;
+        for (int r = lane; r < P.world; r += 32) {
+            const spec_verify_shard_stat rec = P.recs[static_cast<size_t>(r) * P.R + row];
+            combine_stat(L, sx, idx, rec.max_logit, rec.sumexp, rec.argmax, c);
+            if (rec.draft_logit == rec.draft_logit) {
+                ld = rec.draft_logit;
+                qd = rec.draft_prob;
+            }
+        }
+        warp_reduce_stat(L, sx, idx, c);
+        const unsigned own = __ballot_sync(0xFFFFFFFFu, ld == ld);
+        if (own) {
+            const int src = __ffs(own) - 1;
+            ld = __shfl_sync(0xFFFFFFFFu, ld, src);
+            qd = __shfl_sync(0xFFFFFFFFu, qd, src);
+        }
+        if (lane == 0) {
+            const float m = __fmul_rn(L, invT);
+            const int amax = idx == INT_MAX ? 0 : idx;
+            sm_m[j] = m;
+            sm_S[j] = sx;
+            sm_amax[j] = amax;
+            if (j < K) {
+                const int d = __ldg(P.draft_ids + q0 + j);
+                bool acc;
+                if (greedy) {
+                    acc = d == amax;  // [spec-notes] 8.3
+                } else if (d < 0 || d >= P.V || !own) {
+                    acc = false;
+                } else {  // [spec-notes] answer code: q > 0 and p / q >= u
+                    const float t_d = sv::exp_f32(__fsub_rn(__fmul_rn(ld, invT), m));
+                    const sv::Philox4 u4 = sv::philox4x32_10(0u, static_cast<uint32_t>(j), ireq,
+                                                             sv::kTagAccept,
+                                                             static_cast<uint32_t>(P.seed),
+                                                             static_cast<uint32_t>(P.seed >> 32));
+                    acc = qd > 0.0f && __fdiv_rn(__fdiv_rn(t_d, sx), qd) >= sv::uniform_from_word(u4.x);
+                }
+                if (!acc) atomicMin(&s_js, j);
+            }
+        }
+    }
+    __syncthreads();
+    const int js = s_js;
+    spec_verify_shard_key o;
+    o.jstar = js;
+    o.token = greedy ? sm_amax[js] : -1;
+    o.residual_key = 0.0f;
+    o.residual_index = -1;
+    o.p_key = 0.0f;
+    o.p_index = -1;
+    if (!greedy) {
+        const int row = q0 + i + js;
+        RaceRow<T> r;
+        r.g0 = static_cast<uint32_t>(P.v0 / kGroup);
+        r.rp = logits + static_cast<size_t>(row) * P.Vs;
+        r.V = P.Vs;
+        r.G = (P.Vs + kGroup - 1) / kGroup;
+        r.m = sm_m[js];
+        r.S = sm_S[js];
+        r.invT = invT;
+        r.j = static_cast<uint32_t>(js);
+        r.ireq = ireq;
+        r.k0 = static_cast<uint32_t>(P.seed);
+        r.k1 = static_cast<uint32_t>(P.seed >> 32);
+        r.dlrow = nullptr;
+        r.md = 0.0f;
+        r.Sd = 1.0f;
+        r.pr = PenRow{0.0f, nullptr, nullptr, 0};
+        r.tau = -kInf;
+        r.qrow = nullptr;
+        r.excl = -1;
+        SearchSmem sm;
+        sm.buf = reinterpret_cast<unsigned long long *>(dyn);
+        sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
+        sm.bin_n = s_bin_n;
+        sm.bin_max = s_bin_max;
+        sm.top = &s_top;
+        sm.qgs = s_qgs;
+        sm.ql = s_ql;
+        sm.qq = s_qq;
+        sm.lm = reinterpret_cast<float *>(dyn);
+        sm.pb = reinterpret_cast<float *>(dyn + lay.pb);
+        sm.ew = reinterpret_cast<uint32_t *>(dyn + lay.ew);
+        sm.ag = dyn + lay.ag;
+        sm.best = &s_best;
+        sm.cnt = &s_cnt;
+        const RowLines rl = row_lines(row, P.Vs, P.base_off);
+        if (js < K) {  // the residual (with q) or the exclusion race (without) of this shard
+            const bool residual = P.q != nullptr;
+            const int d = __ldg(P.draft_ids + q0 + js);
+            r.qrow = residual ? P.q + static_cast<size_t>(q0 + js) * P.Vs : nullptr;
+            r.excl = (!residual && d >= P.v0 && d < P.v0 + P.Vs) ? d - P.v0 : -1;
+            row_line_max<T, false>(r.rp, P.Vs, rl, lines, sm.lm, r.pr);
+            __syncthreads();
+            const unsigned long long b = residual ? race_search<T, true, false, false>(r, rl, sm)
+                                                  : race_search<T, false, false, false>(r, rl, sm);
+            if (b) {
+                o.residual_key = key_dec(static_cast<unsigned>(b >> 32));
+                o.residual_index = P.v0 + static_cast<int>(~static_cast<unsigned>(b));
+            }
+            r.qrow = nullptr;
+            r.excl = -1;
+            __syncthreads();
+        }
+        // the race over p: the bonus token, and the fallback of a residual empty on every
+        // shard, which needs it only from shards whose own residual is empty
+        if (js == K || o.residual_index < 0) {
+            row_line_max<T, false>(r.rp, P.Vs, rl, lines, sm.lm, r.pr);
+            __syncthreads();
+            const unsigned long long b = race_search<T, false, false, false>(r, rl, sm);
+            if (b) {
+                o.p_key = key_dec(static_cast<unsigned>(b >> 32));
+                o.p_index = P.v0 + static_cast<int>(~static_cast<unsigned>(b));
+            }
+        }
+    }
+    if (tid == 0) P.out[i] = o;
+}
+
+// The winner over the shards and the emitted row of each request (one thread per request).
+__global__ void sv_shard_finish_kernel(const spec_verify_shard_key *__restrict__ races, int world,
+                                       const int32_t *__restrict__ draft_ids,
+                                       const int32_t *__restrict__ cu, int n, int kmax,
+                                       int32_t *__restrict__ sampled,
+                                       int32_t *__restrict__ num_sampled,
+                                       int32_t *__restrict__ num_rejected)
+{
+    const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+    if (i >= n) return;
+    const int q0 = __ldg(cu + i), K = __ldg(cu + i + 1) - q0;
+    const spec_verify_shard_key o0 = races[i];
+    const int js = o0.jstar;
+    const int stride = kmax + 1;
+    if (js < 0 || js > K || K > kmax) {  // an inconsistent batch: nothing emitted
+        for (int s = 0; s < stride; ++s) sampled[static_cast<size_t>(i) * stride + s] = -1;
+        num_sampled[i] = 0;
+        num_rejected[i] = 0;
+        return;
+    }
+    int token = o0.token;
+    if (token < 0) {
+        unsigned long long best = 0ull;
+        if (js < K)
+            for (int r = 0; r < world; ++r) {
+                const spec_verify_shard_key o = races[static_cast<size_t>(r) * n + i];
+                if (o.residual_index >= 0) best = max(best, pack_key(o.residual_key, o.residual_index));
+            }
+        if (!best)
+            for (int r = 0; r < world; ++r) {
+                const spec_verify_shard_key o = races[static_cast<size_t>(r) * n + i];
+                if (o.p_index >= 0) best = max(best, pack_key(o.p_key, o.p_index));
+            }
+        token = best ? static_cast<int>(~static_cast<unsigned>(best)) : 0;
+    }
+    int32_t *out = sampled + static_cast<size_t>(i) * stride;
+    for (int s = 0; s < stride; ++s) out[s] = s < js ? __ldg(draft_ids + q0 + s) : (s == js ? token : -1);
+    num_sampled[i] = js + 1;
+    num_rejected[i] = K - js;
+}
+
 // One CTA per request. kDLMode: q comes from draft logits (P.dl); kPen: the batch has a
 // frequency penalty. Separate instantiations, so that the plain path carries neither.
 template <typename T, bool kDLMode, bool kPen>
@@ -1871,6 +2132,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     // 2. the race at j*
     const int row = row0 + js;
     RaceRow<T> r;
+    r.g0 = 0u;
     r.rp = logits + static_cast<size_t>(row) * P.V;
     r.V = P.V;
     r.G = (P.V + kGroup - 1) / kGroup;
@@ -2053,7 +2315,8 @@ template <typename T>
 cudaError_t setup_kernels(int device, int *stats_per_sm)
 {
     const int limit = static_cast<int>(verify_smem_limit(device));
-    const void *kernels[] = {reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
+    const void *kernels[] = {reinterpret_cast<const void *>(sv_shard_race_kernel<T>),
+                             reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, true, false>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, false, true>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, true, true>)};
@@ -2365,6 +2628,110 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
     const spec_verify_outputs o{sampled, num_sampled, num_rejected, opt_row_max, opt_row_sumexp,
                                 opt_row_argmax};
     return spec_verify_run_batch(ctx, &b, &o, cuda_stream);
+}
+
+int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int v0,
+                            const int32_t *draft_ids, const float *draft_probs_shard,
+                            const int32_t *cu_num_draft, const float *temperature,
+                            const uint8_t *is_greedy, int num_reqs, int num_draft_tokens,
+                            int max_spec_len_this_batch, spec_verify_shard_stat *out,
+                            void *cuda_stream)
+{
+    if (!ctx || !out || v0 < 0 || v0 % kGroup != 0) return SV_EINVAL;
+    const spec_verify_batch b = plain_batch(logits_shard, draft_ids, draft_probs_shard, nullptr,
+                                            cu_num_draft, temperature, is_greedy, 0, 0, num_reqs,
+                                            num_draft_tokens, max_spec_len_this_batch);
+    int32_t dummy;
+    const spec_verify_outputs o{&dummy, &dummy, &dummy, nullptr, nullptr, nullptr};
+    int rc = check_run_args(ctx, b, o);
+    if (rc != SV_OK || num_reqs == 0) return rc;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SV_EDEVICE;
+    auto stream = static_cast<cudaStream_t>(cuda_stream);
+    const int Vs = ctx->V, R = num_draft_tokens + num_reqs;
+    const RequestTable rq{cu_num_draft, temperature, is_greedy, nullptr, num_reqs};
+    const long long total = static_cast<long long>(R) * Vs;
+    const long long chunk1 = stats_chunk_for(ctx, total);
+    auto launch = [&](auto tag) -> int {
+        using T = decltype(tag);
+        const T *lg = static_cast<const T *>(logits_shard);
+        T *lines = static_cast<T *>(ctx->lines);
+        const StatsArray<T> A = stats_array<T>(lg, total, chunk1, Vs, 0, ctx->statpart, lines);
+        const StatsArray<T> D = stats_array<T>(nullptr, 0, chunk1, Vs, 1, nullptr, nullptr);
+        const size_t smem1 = static_cast<size_t>(chunk1 / kGroup) * sizeof(T);
+        sv_stats_kernel<T, false><<<A.grid, kThreads, smem1, stream>>>(
+            Vs, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, draft_ids);
+        sv_shard_export_kernel<T><<<(R + kWarps - 1) / kWarps, kThreads, 0, stream>>>(
+            lg, rq, draft_ids, draft_probs_shard, ctx->statpart, Vs, v0, ctx->maxseg, A.base_off,
+            A.chunk, R, out);
+        return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+    };
+    return ctx->dtype == SV_BF16 ? launch(uint16_t{}) : launch(float{});
+}
+
+int spec_verify_shard_race(spec_verify_ctx *ctx, const void *logits_shard, int v0, int vocab_size,
+                           const spec_verify_shard_stat *all_stats, int world,
+                           const int32_t *draft_ids, const float *draft_probs_shard,
+                           const int32_t *cu_num_draft, const float *temperature,
+                           const uint8_t *is_greedy, uint64_t seed, uint32_t req_index_base,
+                           int num_reqs, int num_draft_tokens, int max_spec_len_this_batch,
+                           spec_verify_shard_key *out, void *cuda_stream)
+{
+    if (!ctx || !out || !all_stats || world < 1 || v0 < 0 || v0 % kGroup != 0 ||
+        vocab_size < v0 + ctx->V)
+        return SV_EINVAL;
+    const spec_verify_batch b = plain_batch(logits_shard, draft_ids, draft_probs_shard, nullptr,
+                                            cu_num_draft, temperature, is_greedy, seed,
+                                            req_index_base, num_reqs, num_draft_tokens,
+                                            max_spec_len_this_batch);
+    int32_t dummy;
+    const spec_verify_outputs o{&dummy, &dummy, &dummy, nullptr, nullptr, nullptr};
+    int rc = check_run_args(ctx, b, o);
+    if (rc != SV_OK || num_reqs == 0) return rc;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SV_EDEVICE;
+    auto stream = static_cast<cudaStream_t>(cuda_stream);
+    ShardParams P;
+    P.rq = RequestTable{cu_num_draft, temperature, is_greedy, nullptr, num_reqs};
+    P.draft_ids = draft_ids;
+    P.q = draft_probs_shard;
+    P.recs = all_stats;
+    P.world = world;
+    P.R = num_draft_tokens + num_reqs;
+    P.V = vocab_size;
+    P.Vs = ctx->V;
+    P.v0 = v0;
+    P.kmax = max_spec_len_this_batch;
+    P.seed = seed;
+    P.req_base = req_index_base;
+    P.out = out;
+    const size_t smem = verify_smem_bytes(ctx->V, max_spec_len_this_batch);
+    auto launch = [&](auto tag) -> int {
+        using T = decltype(tag);
+        const T *lg = static_cast<const T *>(logits_shard);
+        P.base_off = static_cast<int>((reinterpret_cast<uintptr_t>(lg) % (kGroup * sizeof(T))) / sizeof(T));
+        sv_shard_race_kernel<T><<<num_reqs, kThreads, smem, stream>>>(
+            lg, static_cast<const T *>(ctx->lines), P);
+        return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
+    };
+    return ctx->dtype == SV_BF16 ? launch(uint16_t{}) : launch(float{});
+}
+
+int spec_verify_shard_finish(spec_verify_ctx *ctx, const spec_verify_shard_key *all_races,
+                             int world, const int32_t *draft_ids, const int32_t *cu_num_draft,
+                             int num_reqs, int max_spec_len_this_batch, int32_t *sampled,
+                             int32_t *num_sampled, int32_t *num_rejected, void *cuda_stream)
+{
+    if (!ctx || world < 1 || num_reqs < 0 || max_spec_len_this_batch < 0) return SV_EINVAL;
+    if (num_reqs == 0) return SV_OK;
+    if (!all_races || !cu_num_draft || !sampled || !num_sampled || !num_rejected) return SV_EINVAL;
+    DeviceGuard g(ctx->device);
+    if (!g.ok) return SV_EDEVICE;
+    sv_shard_finish_kernel<<<(num_reqs + kThreads - 1) / kThreads, kThreads, 0,
+                             static_cast<cudaStream_t>(cuda_stream)>>>(
+        all_races, world, draft_ids, cu_num_draft, num_reqs, max_spec_len_this_batch, sampled,
+        num_sampled, num_rejected);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ECUDA;
 }
 
 int spec_verify_set_synthetic(spec_verify_ctx *ctx, const float *rates, int n)

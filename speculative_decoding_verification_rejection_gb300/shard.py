@@ -101,3 +101,63 @@ def sharded_verify(backend, all_gather, world_size: int, max_spec_len: int):
     all_stats = all_gather(backend.stats())
     all_races = all_gather(backend.race(all_stats, world_size))
     return backend.finish(all_races, world_size, max_spec_len)
+
+
+class ShardBackend:
+    """This rank's side of sharded_verify on its GPU: device tensors for its columns
+    [v0, v0 + Vs) of the logits (and draft probabilities); records are uint8 device tensors
+    (24 bytes per row, then per request) ready for an all-gather."""
+
+    def __init__(self, ctx, v0: int, vocab_size: int, logits_shard, draft_ids, draft_probs_shard,
+                 cu_num_draft, temperature, is_greedy, seed: int, req_index_base: int = 0,
+                 max_spec_len: int | None = None, stream=None):
+        from . import SHARD_RECORD_BYTES
+        self.ctx, self.v0, self.V = ctx, int(v0), int(vocab_size)
+        self.logits, self.ids, self.q = logits_shard, draft_ids, draft_probs_shard
+        self.cu, self.T, self.g = cu_num_draft, temperature, is_greedy
+        self.seed, self.base, self.stream = seed, req_index_base, stream
+        self.n = cu_num_draft.numel() - 1
+        self.nd = draft_ids.numel()
+        self.kmax = ctx.max_spec_len if max_spec_len is None else max_spec_len
+        self.rec = SHARD_RECORD_BYTES
+
+    def stats(self):
+        import torch
+        from . import spec_verify_shard_stats
+        out = torch.empty((self.nd + self.n) * self.rec, dtype=torch.uint8, device=self.logits.device)
+        spec_verify_shard_stats(self.ctx.ctx, self.logits, self.v0, self.ids, self.q, self.cu, self.T,
+                                self.g, self.n, self.nd, self.kmax, out, cuda_stream=self.stream)
+        return out
+
+    def race(self, all_stats, world_size: int):
+        import torch
+        from . import spec_verify_shard_race
+        out = torch.empty(self.n * self.rec, dtype=torch.uint8, device=self.logits.device)
+        spec_verify_shard_race(self.ctx.ctx, self.logits, self.v0, self.V, all_stats.contiguous(),
+                               world_size, self.ids, self.q, self.cu, self.T, self.g, self.seed,
+                               self.base, self.n, self.nd, self.kmax, out, cuda_stream=self.stream)
+        return out
+
+    def finish(self, all_races, world_size: int, max_spec_len: int):
+        import torch
+        from . import spec_verify_shard_finish
+        dev = self.logits.device
+        sampled = torch.empty((self.n, max_spec_len + 1), dtype=torch.int32, device=dev)
+        ns = torch.empty(self.n, dtype=torch.int32, device=dev)
+        nr = torch.empty(self.n, dtype=torch.int32, device=dev)
+        spec_verify_shard_finish(self.ctx.ctx, all_races.contiguous(), world_size, self.ids, self.cu,
+                                 self.n, max_spec_len, sampled, ns, nr, cuda_stream=self.stream)
+        return sampled, ns, nr
+
+
+def nccl_all_gather(group=None):
+    """The exchange of sharded_verify over torch.distributed: the ranks' byte records stacked
+    in rank order."""
+    def gather(rec):
+        import torch
+        import torch.distributed as dist
+        world = dist.get_world_size(group)
+        out = torch.empty(world * rec.numel(), dtype=rec.dtype, device=rec.device)
+        dist.all_gather_into_tensor(out, rec.contiguous(), group=group)
+        return out
+    return gather
