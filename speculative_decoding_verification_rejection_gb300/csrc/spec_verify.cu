@@ -636,67 +636,125 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
         part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
 }
 
-// stats_segment for a penalised row: the same partials over the processed values y (see
-// PenRow), and line maxima rounded up to the logits' type (an upper bound of the line's y).
-// c = (1 / T) log2(e) of the row's request.
+// stats_segment for a batch with a frequency penalty: the same partials over the processed values
+// y (see PenRow), and line maxima rounded up to the logits' type (an upper bound of the line's y).
+// The row is streamed as 16-byte vectors (8 bf16 / 4 fp32 elements, a lane each) with their
+// counts (16-byte vectors where the counts row is so aligned: the same for every vector of the
+// segment), two rounds in flight while one is processed. c = (1 / T) log2(e) of the row's request.
 template <typename T>
-__device__ __noinline__ void stats_segment_pen(const T *__restrict__ logits, int V, int row, int b,
-                                               int e, int seg, int maxseg, int base_off, float c,
-                                               const PenRow &pr, StatPart *__restrict__ part,
-                                               T *__restrict__ s_lines, long long line_base)
+__device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, int V, int row, int b,
+                                                  int e, int seg, int maxseg, int base_off, float c,
+                                                  const PenRow &pr, StatPart *__restrict__ part,
+                                                  T *__restrict__ s_lines, long long line_base)
 {
+    constexpr int kEV = 16 / static_cast<int>(sizeof(T));  // elements per vector
+    constexpr int kVPL = kGroup / kEV;                      // vectors per 64-element line
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
-    constexpr int kPE = kPairBytes / sizeof(T);
-    constexpr int kPPL = PairMax<T>::kLanes;
     const long long pos_b = base_off + rbase + b;
     const int head = static_cast<int>((kGroup - (pos_b & (kGroup - 1))) & (kGroup - 1));
-    const int a0 = min(e, b + head);
-    const int npair = (e - a0) / kPE;
-    const int a1 = a0 + npair * kPE;
-    const char *pbase = reinterpret_cast<const char *>(rp + a0);
+    const int a0 = min(e, b + head);  // on a line boundary: 16-byte aligned in memory
+    const int nvec = (e - a0) / kEV;
+    const int a1 = a0 + nvec * kEV;
+    const char *vbase = reinterpret_cast<const char *>(rp + a0);
     const int line0 = static_cast<int>(((pos_b + (a0 - b)) >> 6) - line_base);
     const int lane = threadIdx.x & 31;
-    const bool aligned = (reinterpret_cast<uintptr_t>(pr.cnt + a0) & 15u) == 0u;
+    const bool pen = pr.f != 0.0f;
+    const bool aligned = pen && (reinterpret_cast<uintptr_t>(pr.cnt + a0) & 15u) == 0u;
+
+    struct Vec {
+        uint4 w;
+        int c[kEV];
+    };
+    auto load = [&](int u, Vec &x) {
+        if (u >= nvec) return;
+        x.w = ldg_v4(vbase + static_cast<size_t>(u) * 16);
+        if (!pen) return;
+        const int v = a0 + u * kEV;
+        if (aligned) {
+#pragma unroll
+            for (int q = 0; q < kEV / 4; ++q) {
+                const int4 t = __ldg(reinterpret_cast<const int4 *>(pr.cnt + v) + q);
+                x.c[4 * q] = t.x;
+                x.c[4 * q + 1] = t.y;
+                x.c[4 * q + 2] = t.z;
+                x.c[4 * q + 3] = t.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kEV; ++k) x.c[k] = __ldg(pr.cnt + v + k);
+        }
+    };
+    // the processed values of vector u
+    auto values = [&](int u, const Vec &x, float (&y)[kEV]) {
+        const uint32_t ws[4] = {x.w.x, x.w.y, x.w.z, x.w.w};
+        const int v = a0 + u * kEV;
+        bool hit = false;
+        if (pen)
+            for (int k = 0; k < pr.nprev; ++k)
+                hit |= static_cast<unsigned>(__ldg(pr.prev + k) - v) < static_cast<unsigned>(kEV);
+#pragma unroll
+        for (int k = 0; k < kEV; ++k) {
+            float l;
+            if constexpr (sizeof(T) == 2)
+                l = __uint_as_float((k & 1) ? (ws[k >> 1] & 0xFFFF0000u) : (ws[k >> 1] << 16));
+            else
+                l = __uint_as_float(ws[k]);
+            int cnt = pen ? x.c[k] : 0;
+            if (hit)
+                for (int q = 0; q < pr.nprev; ++q) cnt += __ldg(pr.prev + q) == v + k;
+            y[k] = cnt == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(cnt), l);
+        }
+    };
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
-    for (int ub = static_cast<int>(threadIdx.x) & ~31; ub < npair; ub += kThreads) {
-        const int p = ub + lane;
-        const bool valid = p < npair;
-        float y[kPE];
+    int ub = static_cast<int>(threadIdx.x) & ~31;
+    Vec x0, x1, x2;
+    load(ub + lane, x0);
+    load(ub + lane + kThreads, x1);
+    auto round = [&](const Vec &cur, Vec &nxt) {
+        const int u = ub + lane;
+        load(u + 2 * kThreads, nxt);
+        float y[kEV];
         float mx = -kInf;
-        if (valid) {
-            uint32_t w[16];
-            ldg_pair(pbase + static_cast<size_t>(p) * kPairBytes, w);
-            pen_pair<T>(pr, w, a0 + p * kPE, aligned, y);
+        if (u < nvec) {
+            values(u, cur, y);
 #pragma unroll
-            for (int k = 0; k < kPE; ++k) mx = fmaxf(mx, y[k]);
+            for (int k = 0; k < kEV; ++k) mx = fmaxf(mx, y[k]);
         }
         if (s_lines) {
             float lm = mx;
 #pragma unroll
-            for (int o = 1; o < kPPL; o <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
-            if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair) {
-                if constexpr (sizeof(T) == 2) s_lines[line0 + p / kPPL] = bf16_round_up(lm);
-                else s_lines[line0 + p / kPPL] = lm;
+            for (int o = 1; o < kVPL; o <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
+            if ((lane & (kVPL - 1)) == 0 && u + kVPL - 1 < nvec) {
+                if constexpr (sizeof(T) == 2) s_lines[line0 + u / kVPL] = bf16_round_up(lm);
+                else s_lines[line0 + u / kVPL] = lm;
             }
         }
-        if (valid) fold_vals<kPE>(st, y, p, c, mx);
+        if (u < nvec) fold_vals<kEV>(st, y, u, c, mx);
+        ub += kThreads;
+    };
+    while (ub < nvec) {
+        round(x0, x2);
+        if (ub >= nvec) break;
+        round(x1, x0);
+        if (ub >= nvec) break;
+        round(x2, x1);
     }
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
 
     int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
-    if (st.best_p >= 0) {
-        uint32_t w[16];
-        float y[kPE];
-        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w);
-        pen_pair<T>(pr, w, a0 + st.best_p * kPE, aligned, y);
+    if (st.best_p >= 0) {  // the vector that first reached the max: its lowest index
+        Vec x;
+        load(st.best_p, x);
+        float y[kEV];
+        values(st.best_p, x, y);
 #pragma unroll
-        for (int h = kPE - 1; h >= 0; --h)
-            if (y[h] == st.L) idx = a0 + st.best_p * kPE + h;
+        for (int h = kEV - 1; h >= 0; --h)
+            if (y[h] == st.L) idx = a0 + st.best_p * kEV + h;
     }
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
@@ -749,22 +807,19 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
         const int fk = static_cast<int>(div_floor(X.base_off + rbase, X.chunk));
-        if constexpr (kPen) {
-            if (!X.draft_rows) {  // penalties act on the target logits only
-                const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31);
-                const int q0 = __ldg(rq.cu + i);
-                const PenRow pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
-                if (pr.f != 0.0f) {
-                    bool greedy;
-                    const float c = request_invT(rq, i, greedy) * kLog2e;
-                    stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c,
-                                         pr, X.part, s_lines, line_base);
-                    continue;
-                }
-            }
+        if constexpr (kPen) {  // every row takes the penalty path (penalties: target logits only)
+            const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31, X.draft_rows != 0);
+            const int q0 = __ldg(rq.cu + i);
+            const PenRow pr = X.draft_rows ? PenRow{0.0f, nullptr, nullptr, 0}
+                                           : pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
+            bool greedy;
+            const float c = request_invT(rq, i, greedy) * kLog2e;
+            stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c, pr,
+                                 X.part, s_lines, line_base);
+        } else {
+            stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part,
+                             s_lines, line_base, X.draft_rows != 0);
         }
-        stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part, s_lines,
-                         line_base, X.draft_rows != 0);
     }
     if (X.lines) {
         __syncthreads();
@@ -1336,10 +1391,11 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
 // order-preserving integer key of x, 8 bits per level, down to a single value (a group of equal
 // values is kept or dropped as a whole); a bin too large to collect is refined over the row
 // first. Masses come from the hardware ex2, summed in fp32.
-constexpr int kSelBins = 256;           // bins per level: 1/8 nat below the row maximum, then 8 key bits
-constexpr float kSelBinsPerNat = 8.0f;
+constexpr int kSelBins1 = 2048;         // level 1: counts in bins of 1/64 nat below the maximum
+constexpr float kSelBinsPerNat = 64.0f;
+constexpr int kSelBins = 256;           // the finer levels: 8 key bits each
 constexpr int kSelPool = 4096;          // tokens refined in shared memory
-static_assert(kSelBins == kThreads, "one bin per thread");
+static_assert(kSelBins == kThreads && kSelBins1 % kThreads == 0, "bins per thread");
 
 struct SelectParams {
     RequestTable rq;
@@ -1374,11 +1430,13 @@ __device__ __forceinline__ float key_value(uint32_t k)
 {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
-// Level-1 bin: 0 holds the values less than 1/8 nat below m, 255 everything from 31.875 down.
+// Level-1 bin: 0 holds the values less than 1/64 nat below m, the last everything further down
+// than 2047/64 nats.
 __device__ __forceinline__ int sel_bin1(float x, float m)
 {
     const float u = __fmul_rn(__fsub_rn(m, x), kSelBinsPerNat);
-    return u < 255.0f ? (u > 0.0f ? static_cast<int>(u) : 0) : 255;  // NaN: 255
+    return u < static_cast<float>(kSelBins1 - 1) ? (u > 0.0f ? static_cast<int>(u) : 0)
+                                                  : kSelBins1 - 1;  // NaN: the last bin
 }
 // A token's mass exp(x - m), by the hardware ex2.
 __device__ __forceinline__ float sel_mass(float x, float m)
@@ -1386,9 +1444,26 @@ __device__ __forceinline__ float sel_mass(float x, float m)
     return sv::ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
+// Dynamic shared memory of the select kernel: [kWarps][kSelBins] per-warp counts or masses
+// (float bits) of the finer levels, the level-1 counts [kWarps][kSelBins1] (a copy per warp),
+// then two pools of kSelPool tokens.
+extern __shared__ __align__(16) unsigned char sv_sel_dyn[];
+
 struct SelSmem {
-    uint32_t h[kWarps][kSelBins];  // per-warp counts (top-k) or masses (top-p, as float bits)
-    float pool[kSelPool], pool2[kSelPool];
+    __device__ __forceinline__ uint32_t *hist() const { return reinterpret_cast<uint32_t *>(sv_sel_dyn); }
+    __device__ __forceinline__ uint32_t *cnt1() const { return hist() + kWarps * kSelBins; }
+    __device__ __forceinline__ float *pool_a() const
+    {
+        return reinterpret_cast<float *>(cnt1() + kWarps * kSelBins1);
+    }
+    // a level-1 bin's count over the warps
+    __device__ __forceinline__ uint32_t count1(int b) const
+    {
+        uint32_t c = 0u;
+        for (int w = 0; w < kWarps; ++w) c += cnt1()[w * kSelBins1 + b];
+        return c;
+    }
+    __device__ __forceinline__ float *pool_b() const { return pool_a() + kSelPool; }
     uint32_t wc[kWarps];
     float wm[kWarps];
     uint32_t kmin, kmax, n;
@@ -1423,6 +1498,31 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
             const int u = u0 + q * kThreads;
             if (u >= nvec) break;
             const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+            const int v0 = head + u * kEV;
+            int cnt[kEV];
+            bool hit = false;
+            if constexpr (kPen) {  // the vector's counts at once, the earlier drafts by one test
+                if (pr.f != 0.0f) {
+                    if ((reinterpret_cast<uintptr_t>(pr.cnt + v0) & 15u) == 0u) {
+#pragma unroll
+                        for (int g = 0; g < kEV / 4; ++g) {
+                            const int4 t = __ldg(reinterpret_cast<const int4 *>(pr.cnt + v0) + g);
+                            cnt[4 * g] = t.x;
+                            cnt[4 * g + 1] = t.y;
+                            cnt[4 * g + 2] = t.z;
+                            cnt[4 * g + 3] = t.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < kEV; ++e) cnt[e] = __ldg(pr.cnt + v0 + e);
+                    }
+                    for (int g = 0; g < pr.nprev; ++g)
+                        hit |= static_cast<unsigned>(__ldg(pr.prev + g) - v0) < static_cast<unsigned>(kEV);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < kEV; ++e) cnt[e] = 0;
+                }
+            }
 #pragma unroll
             for (int e = 0; e < kEV; ++e) {
                 float l;
@@ -1430,8 +1530,16 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
                     l = __uint_as_float((e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16));
                 else
                     l = __uint_as_float(ws[e]);
-                const int v = head + u * kEV + e;
-                f(proc(l, v), v);
+                const int v = v0 + e;
+                if constexpr (kPen) {
+                    int c = cnt[e];
+                    if (hit)
+                        for (int g = 0; g < pr.nprev; ++g) c += __ldg(pr.prev + g) == v;
+                    const float y = c == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(c), l);
+                    f(__fmul_rn(y, invT), v);
+                } else {
+                    f(__fmul_rn(l, invT), v);
+                }
             }
         }
     }
@@ -1439,15 +1547,18 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
         f(proc(Elem<T>::at(rp, v), v), v);
 }
 
-__device__ __forceinline__ void sel_clear(SelSmem &sm)
+constexpr size_t kSelDynSmem =
+    (static_cast<size_t>(kWarps) * (kSelBins + kSelBins1) + 2 * kSelPool) * 4;
+
+__device__ __forceinline__ void sel_clear(SelSmem &sm, int nbins)
 {
-    for (int w = 0; w < kWarps; ++w) sm.h[w][threadIdx.x] = 0u;
+    for (int k = threadIdx.x; k < kWarps * nbins; k += kThreads) sm.hist()[k] = 0u;
 }
 __device__ __forceinline__ void sel_add(SelSmem &sm, int mode, int b, float t)
 {
-    const int warp = threadIdx.x >> 5;
-    if (mode == 0) atomicAdd(&sm.h[warp][b], 1u);
-    else atomicAdd(reinterpret_cast<float *>(&sm.h[warp][b]), t);
+    uint32_t *cell = sm.hist() + (threadIdx.x >> 5) * kSelBins + b;
+    if (mode == 0) atomicAdd(cell, 1u);
+    else atomicAdd(reinterpret_cast<float *>(cell), t);
 }
 
 // Sum of a float over the CTA (every thread gets it).
@@ -1464,22 +1575,37 @@ __device__ __forceinline__ float sel_block_sum(SelSmem &sm, float v)
     return t;
 }
 
-// After the per-warp histograms are complete (bin 0 holds the largest values): the crossing bin.
-// mode 0 (counts): the first bin where ca + count >= k; mode 1 (masses): the first bin where
-// ma + mass >= target, or the last non-empty bin if rounding leaves the total short. Adds the
-// count (mode 0) or mass (mode 1) strictly above the crossing bin to ca / ma.
-__device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32_t &ca, float &ma)
+// After the per-warp histograms over nbins bins are complete (bin 0 holds the largest values):
+// the crossing bin. mode 0 (counts): the first bin where ca + count >= k; mode 1 (masses): the
+// first bin where ma + mass >= target, or the last non-empty bin if rounding leaves the total
+// short. Adds the count (mode 0) or mass (mode 1) strictly above the crossing bin to ca / ma.
+// Thread t scans bins [t * per, (t + 1) * per); the prefix of bin b is formed in one fixed
+// order, so the excluded sum of a bin is exactly the included sum of the one before.
+__device__ int sel_cross(SelSmem &sm, int nbins, int mode, uint32_t k, float target, uint32_t &ca,
+                         float &ma)
 {
-    const int b = threadIdx.x, lane = b & 31, warp = b >> 5;
-    uint32_t c = 0u;
-    float mm = 0.0f;
-    for (int w = 0; w < kWarps; ++w) {
-        if (mode == 0) c += sm.h[w][b];
-        else mm += __uint_as_float(sm.h[w][b]);
+    const int per = nbins / kThreads, b0 = threadIdx.x * per;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // nbins == kSelBins1: the level-1 counts; else the per-warp copies of the finer levels
+    auto bin_c = [&](int b) {
+        if (nbins == kSelBins1) return sm.count1(b);
+        uint32_t c = 0u;
+        for (int w = 0; w < kWarps; ++w) c += sm.hist()[w * kSelBins + b];
+        return c;
+    };
+    auto bin_m = [&](int b) {
+        float m = 0.0f;
+        for (int w = 0; w < kWarps; ++w) m += __uint_as_float(sm.hist()[w * kSelBins + b]);
+        return m;
+    };
+    uint32_t tc = 0u;
+    float tm = 0.0f;
+    for (int q = 0; q < per; ++q) {
+        if (mode == 0) tc += bin_c(b0 + q);
+        else tm = tm + bin_m(b0 + q);
     }
-    // inclusive scans; excl(b) is exactly incl(b - 1)
-    uint32_t ci = c;
-    float mi = mm;
+    uint32_t ci = tc;
+    float mi = tm;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const uint32_t c2 = __shfl_up_sync(0xFFFFFFFFu, ci, o);
@@ -1495,7 +1621,7 @@ __device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32
         sm.wc[warp] = ci;
         sm.wm[warp] = mi;
     }
-    if (b == 0) sm.cross = -1;
+    if (threadIdx.x == 0) sm.cross = -1;
     __syncthreads();
     uint32_t coff = 0u;
     float moff = 0.0f;
@@ -1503,39 +1629,119 @@ __device__ int sel_cross(SelSmem &sm, int mode, uint32_t k, float target, uint32
         coff += sm.wc[w];
         moff = moff + sm.wm[w];
     }
-    const uint32_t cin = ca + coff + ci, cex = ca + coff + (lane ? cprev : 0u);
-    const float min_ = ma + (moff + mi), mex = ma + (lane ? moff + mprev : moff);
-    const bool hit = mode == 0 ? (cex < k && cin >= k) : (mex < target && min_ >= target);
-    if (hit) {
-        sm.cross = b;
-        sm.cabove = cex;
-        sm.mabove = mex;
-    }
-    __syncthreads();
-    if (sm.cross < 0) {  // short of the target: the last non-empty bin
-        const unsigned nz = __ballot_sync(0xFFFFFFFFu, mode == 0 ? c > 0u : mm > 0.0f);
-        if (lane == 0) sm.wc[warp] = nz;
-        __syncthreads();
-        if (b == 0) {
-            sm.cross = 0;
-            for (int w = kWarps - 1; w >= 0; --w)
-                if (sm.wc[w]) {
-                    sm.cross = w * 32 + 31 - __clz(sm.wc[w]);
-                    break;
-                }
-        }
-        __syncthreads();
-        if (b == sm.cross) {
+    uint32_t cex = ca + coff + (lane ? cprev : 0u);
+    float mex = ma + (lane ? moff + mprev : moff);
+    int last = -1;
+    for (int q = 0; q < per; ++q) {
+        const uint32_t c = mode == 0 ? bin_c(b0 + q) : 0u;
+        const float mm = mode == 1 ? bin_m(b0 + q) : 0.0f;
+        const uint32_t cin = cex + c;
+        const float min_ = mex + mm;
+        const bool hit = mode == 0 ? (cex < k && cin >= k) : (mex < target && min_ >= target);
+        if (hit) {
+            sm.cross = b0 + q;
             sm.cabove = cex;
             sm.mabove = mex;
         }
+        if (mode == 0 ? c > 0u : mm > 0.0f) last = b0 + q;
+        cex = cin;
+        mex = min_;
+    }
+    __syncthreads();
+    if (sm.cross < 0) {  // short of the target: the last non-empty bin
+        if (threadIdx.x == 0) sm.n = 0u;
+        __syncthreads();
+        atomicMax(&sm.n, static_cast<uint32_t>(last + 1));
+        __syncthreads();
+        const int lb = static_cast<int>(sm.n) - 1;
+        if (lb >= b0 && lb < b0 + per) {
+            uint32_t c2 = ca + coff + (lane ? cprev : 0u);
+            float m2 = ma + (lane ? moff + mprev : moff);
+            for (int q = b0; q < lb; ++q) {
+                if (mode == 0) c2 += bin_c(q);
+                else m2 = m2 + bin_m(q);
+            }
+            sm.cross = lb;
+            sm.cabove = c2;
+            sm.mabove = m2;
+        }
         __syncthreads();
     }
-    const int x = sm.cross;
+    const int x = max(sm.cross, 0);
     ca = sm.cabove;
     ma = sm.mabove;
     __syncthreads();
     return x;
+}
+
+// The level-1 bins where the top-p crossing can lie, from the counts alone: a token of bin b has
+// mass in (e^-(b+1)/128, e^-b/128] (the last bin: (0, e^-4095/128]), so the mass up to and
+// including bin b lies between the sums of count * lower and count * upper bound (with margins
+// for the hardware ex2). Returns the first bin whose upper sum reaches target (no earlier bin can
+// hold the crossing) in lo and the first whose lower sum reaches it (no later one can) in hi (the
+// last non-empty bin if none does).
+__device__ void sel_bounds(SelSmem &sm, float target, int &lo, int &hi)
+{
+    constexpr int per = kSelBins1 / kThreads;
+    const int b0 = threadIdx.x * per, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t cb[per];  // this thread's bins' counts
+    for (int q = 0; q < per; ++q) cb[q] = sm.count1(b0 + q);
+    auto bound = [&](int q, bool upper) {
+        const int b = b0 + q;
+        const float c = static_cast<float>(cb[q]);
+        if (!upper && b == kSelBins1 - 1) return 0.0f;
+        const float e = sv::ex2_approx(-static_cast<float>(upper ? b : b + 1) * (kLog2e / kSelBinsPerNat));
+        return c * e * (upper ? 1.0f + 0x1p-10f : 1.0f - 0x1p-10f);
+    };
+    float tl = 0.0f, th = 0.0f;
+    int last = -1;
+    for (int q = 0; q < per; ++q) {
+        tl += bound(q, false);
+        th += bound(q, true);
+        if (cb[q]) last = b0 + q;
+    }
+    float il = tl, ih = th;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float l2 = __shfl_up_sync(0xFFFFFFFFu, il, o), h2 = __shfl_up_sync(0xFFFFFFFFu, ih, o);
+        if (lane >= o) {
+            il += l2;
+            ih += h2;
+        }
+    }
+    __shared__ float s_wh[kWarps];
+    __shared__ int s_lo, s_hi, s_last;
+    if (lane == 31) {
+        sm.wm[warp] = il;
+        s_wh[warp] = ih;
+    }
+    if (threadIdx.x == 0) {
+        s_lo = INT_MAX;
+        s_hi = INT_MAX;
+        s_last = -1;
+    }
+    __syncthreads();
+    float ol = 0.0f, oh = 0.0f;
+    for (int w = 0; w < warp; ++w) {
+        ol += sm.wm[w];
+        oh += s_wh[w];
+    }
+    // sums before this thread's first bin (threads differ in rounding; the margins cover it)
+    float cl = ol + il - tl, ch = oh + ih - th;
+    int flo = INT_MAX, fhi = INT_MAX;
+    for (int q = 0; q < per; ++q) {
+        cl += bound(q, false);
+        ch += bound(q, true);
+        if (ch >= target) flo = min(flo, b0 + q);
+        if (cl >= target) fhi = min(fhi, b0 + q);
+    }
+    atomicMin(&s_lo, flo);
+    atomicMin(&s_hi, fhi);
+    atomicMax(&s_last, last);
+    __syncthreads();
+    hi = s_hi != INT_MAX ? s_hi : max(s_last, 0);
+    lo = min(s_lo != INT_MAX ? s_lo : hi, hi);
+    __syncthreads();
 }
 
 // Key-level sub-bin of key kv in [klo, khi] with shift sh: 0 holds the largest keys.
@@ -1567,13 +1773,14 @@ __device__ __forceinline__ int sel_shift(uint32_t klo, uint32_t khi)
 // candidates strictly above x* (mode 0) and gmass the mass of its group (all tokens equal x*).
 template <typename T, bool kPen>
 __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float m,
-                             const PenRow &pr, int b1, float xmin, int mode, uint32_t k,
+                             const PenRow &pr, int b1, int b1hi, float xmin, int mode, uint32_t k,
                              float target, uint32_t &ca, float &ma, float &above_mass,
                              float &inbin_above, float &gmass)
 {
     auto in_set = [&](float x, uint32_t klo, uint32_t khi) {
         const uint32_t kv = ord_key(x);
-        return x >= xmin && kv >= klo && kv <= khi && sel_bin1(x, m) == b1;
+        const int bx = sel_bin1(x, m);
+        return x >= xmin && kv >= klo && kv <= khi && bx >= b1 && bx <= b1hi;
     };
     uint32_t klo = 0u, khi = 0xFFFFFFFFu, n = 0u;
     bool first = true, big = false;
@@ -1582,13 +1789,13 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         if (big && klo < khi) {
             // too many for shared memory: one finer level over the row
             const int sh = sel_shift(klo, khi);
-            sel_clear(sm);
+            sel_clear(sm, kSelBins);
             __syncthreads();
             sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
                 if (in_set(x, klo, khi)) sel_add(sm, mode, sel_sub(ord_key(x), khi, sh), sel_mass(x, m));
             });
             __syncthreads();
-            const int sb = sel_cross(sm, mode, k, target, ca, ma);
+            const int sb = sel_cross(sm, kSelBins, mode, k, target, ca, ma);
             const uint32_t olo = klo, ohi = khi;
             sel_narrow(klo, khi, sb, sh);
             if (mode == 0) {  // the mass of the candidates left above (counts were kept)
@@ -1610,18 +1817,26 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
         float am = 0.0f;
         sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
-            if (first && x >= xmin && sel_bin1(x, m) < b1) am += sel_mass(x, m);
-            if (in_set(x, klo, khi)) {
-                const uint32_t kv = ord_key(x);
+            const int bx = sel_bin1(x, m);
+            if (bx > b1hi || !(x >= xmin)) return;
+            if (bx < b1) {
+                if (first) am += sel_mass(x, m);
+                return;
+            }
+            const uint32_t kv = ord_key(x);
+            if (kv >= klo && kv <= khi) {
                 lo = min(lo, kv);
                 hi = max(hi, kv);
                 const uint32_t at = atomicAdd(&sm.n, 1u);
-                if (at < static_cast<uint32_t>(kSelPool)) sm.pool[at] = x;
+                if (at < static_cast<uint32_t>(kSelPool)) sm.pool_a()[at] = x;
             }
         });
         atomicMin(&sm.kmin, lo);
         atomicMax(&sm.kmax, hi);
-        if (first) above_mass = sel_block_sum(sm, am);  // (synchronises)
+        if (first) {
+            above_mass = sel_block_sum(sm, am);  // (synchronises)
+            if (mode == 1) ma = above_mass;      // the exact mass above the candidates
+        }
         __syncthreads();
         first = false;
         n = sm.n;
@@ -1645,7 +1860,7 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         __syncthreads();
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
-            const uint32_t kv = ord_key(sm.pool[e]);
+            const uint32_t kv = ord_key(sm.pool_a()[e]);
             lo = min(lo, kv);
             hi = max(hi, kv);
         }
@@ -1657,33 +1872,33 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         __syncthreads();
         if (n == 0u || klo == khi) break;  // one value left
         const int sh = sel_shift(klo, khi);
-        sel_clear(sm);
+        sel_clear(sm, kSelBins);
         __syncthreads();
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
-            const float x = sm.pool[e];
+            const float x = sm.pool_a()[e];
             sel_add(sm, mode, sel_sub(ord_key(x), khi, sh), sel_mass(x, m));
         }
         __syncthreads();
-        const int sb = sel_cross(sm, mode, k, target, ca, ma);
+        const int sb = sel_cross(sm, kSelBins, mode, k, target, ca, ma);
         uint32_t nlo = klo, nhi = khi;
         sel_narrow(nlo, nhi, sb, sh);
         if (threadIdx.x == 0) sm.n = 0u;
         __syncthreads();
         float a = 0.0f;
         for (uint32_t e = threadIdx.x; e < n; e += kThreads) {
-            const float x = sm.pool[e];
+            const float x = sm.pool_a()[e];
             const uint32_t kv = ord_key(x);
-            if (kv >= nlo && kv <= nhi) sm.pool2[atomicAdd(&sm.n, 1u)] = x;
+            if (kv >= nlo && kv <= nhi) sm.pool_b()[atomicAdd(&sm.n, 1u)] = x;
             else if (kv > nhi) a += sel_mass(x, m);
         }
         inbin_above += sel_block_sum(sm, a);  // (synchronises)
         n = sm.n;
-        for (uint32_t e = threadIdx.x; e < n; e += kThreads) sm.pool[e] = sm.pool2[e];
+        for (uint32_t e = threadIdx.x; e < n; e += kThreads) sm.pool_a()[e] = sm.pool_b()[e];
         __syncthreads();
     }
     const float xs = n ? key_value(khi) : -kInf;
     float gm = 0.0f;
-    for (uint32_t e = threadIdx.x; e < n; e += kThreads) gm += sel_mass(sm.pool[e], m);
+    for (uint32_t e = threadIdx.x; e < n; e += kThreads) gm += sel_mass(sm.pool_a()[e], m);
     gmass = sel_block_sum(sm, gm);
     return xs;
 }
@@ -1712,41 +1927,37 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     combine_row(P.part, row, P.V, P.maxseg, P.base_off, P.chunk, invT * kLog2e, L, s0, idx);
     const float m = __fmul_rn(L, invT);
 
-    float tau = -kInf, Z = 0.0f, Sk;
-    if (use_k) {  // level 1 by counts: tau_k, then Z = the mass of the top-k set
-        sel_clear(sm);
+    // level 1: counts per bin of 1/128 nat (integer atomics) of the tokens x >= xmin
+    auto count_level1 = [&](float xmin) {
+        for (int b = threadIdx.x; b < kWarps * kSelBins1; b += kThreads) sm.cnt1()[b] = 0u;
         __syncthreads();
-        sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) { sel_add(sm, 0, sel_bin1(x, m), 0.0f); });
-        __syncthreads();
-        uint32_t ca = 0u;
-        float ma = 0.0f, above, inbin, gm;
-        const int bk = sel_cross(sm, 0, static_cast<uint32_t>(k), 0.0f, ca, ma);
-        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, -kInf, 0, static_cast<uint32_t>(k),
-                                   0.0f, ca, ma, above, inbin, gm);
-        Z = above + (inbin + gm);  // the bins above bk, then bk's tokens at or above tau_k
-    }
-    Sk = Z;
-    if (use_p) {
-        // level 1 by masses, over the top-k set (every token without top-k)
-        sel_clear(sm);
-        __syncthreads();
-        const float tk = tau;
-        float zt = 0.0f;
+        uint32_t *mine = sm.cnt1() + (threadIdx.x >> 5) * kSelBins1;
         sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
-            if (x >= tk) {
-                const float t = sel_mass(x, m);
-                zt += t;
-                sel_add(sm, 1, sel_bin1(x, m), t);
-            }
+            if (x >= xmin) atomicAdd(mine + sel_bin1(x, m), 1u);
         });
-        const float zsum = sel_block_sum(sm, zt);  // (synchronises)
-        if (!use_k) Z = zsum;
-        const float target = __fmul_rn(fmaxf(Pp, 1e-6f), Z);
+        __syncthreads();
+    };
+    float tau = -kInf, Z = s0, Sk = s0;  // Z: the mass of the top-k set, or of the row
+    if (use_k) {
+        count_level1(-kInf);
         uint32_t ca = 0u;
         float ma = 0.0f, above, inbin, gm;
-        const int bp = sel_cross(sm, 1, 0u, target, ca, ma);
-        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bp, tk, 1, 0u, target, ca, ma, above,
-                                   inbin, gm);
+        const int bk = sel_cross(sm, kSelBins1, 0, static_cast<uint32_t>(k), 0.0f, ca, ma);
+        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, bk, -kInf, 0,
+                                   static_cast<uint32_t>(k), 0.0f, ca, ma, above, inbin, gm);
+        Z = above + (inbin + gm);  // the bins above bk, then bk's tokens at or above tau_k
+        Sk = Z;
+    }
+    if (use_p) {
+        const float tk = tau;
+        count_level1(tk);  // over the top-k set (every token without top-k)
+        const float target = __fmul_rn(fmaxf(Pp, 1e-6f), Z);
+        int blo, bhi;
+        sel_bounds(sm, target, blo, bhi);
+        uint32_t ca = 0u;
+        float ma = 0.0f, above, inbin, gm;
+        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, blo, bhi, tk, 1, 0u, target, ca, ma,
+                                   above, inbin, gm);
         Sk = ma + gm;
     }
     if (threadIdx.x == 0) {
@@ -2315,6 +2526,14 @@ template <typename T>
 cudaError_t setup_kernels(int device, int *stats_per_sm)
 {
     const int limit = static_cast<int>(verify_smem_limit(device));
+    cudaError_t es = cudaFuncSetAttribute(sv_select_kernel<T, false>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          static_cast<int>(kSelDynSmem));
+    if (es == cudaSuccess)
+        es = cudaFuncSetAttribute(sv_select_kernel<T, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kSelDynSmem));
+    if (es != cudaSuccess) return es;
     const void *kernels[] = {reinterpret_cast<const void *>(sv_shard_race_kernel<T>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, true, false>),
@@ -2436,9 +2655,9 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         SP.sel_tau = ctx->sel_tau;
         SP.sel_S = ctx->sel_S;
         if (pen_on)
-            sv_select_kernel<T, true><<<rows, kThreads, 0, stream>>>(logits, SP);
+            sv_select_kernel<T, true><<<rows, kThreads, kSelDynSmem, stream>>>(logits, SP);
         else
-            sv_select_kernel<T, false><<<rows, kThreads, 0, stream>>>(logits, SP);
+            sv_select_kernel<T, false><<<rows, kThreads, kSelDynSmem, stream>>>(logits, SP);
     }
     if (slot) cudaEventRecord(slot->ev[2], stream);
     auto verify = dl ? (pen_on ? sv_verify_kernel<T, true, true> : sv_verify_kernel<T, true, false>)
