@@ -74,6 +74,13 @@ template <> struct Elem<uint16_t> {
     }
 };
 
+// Programmatic dependent launch: a statistics CTA lets the verify grid be scheduled once every
+// statistics CTA is running (griddepcontrol.launch_dependents); the verify kernel, after a
+// prologue that reads only inputs, waits there until the statistics grid has completed and its
+// writes are visible (griddepcontrol.wait; returns at once without such a predecessor).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ldg_v4(const void *p)
 {
     return __ldg(reinterpret_cast<const uint4 *>(p));
@@ -792,6 +799,7 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
                 PenTable pt, const int32_t *__restrict__ draft_ids)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
+    pdl_launch_dependents();
     const bool second = static_cast<int>(blockIdx.x) >= A.grid;
     const StatsArray<T> X = second ? D : A;
     const int cta = second ? static_cast<int>(blockIdx.x) - A.grid : static_cast<int>(blockIdx.x);
@@ -2284,6 +2292,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     int sel_k;
     float sel_p;
     const bool constrained = P.sel_tau && sel_active(P.rq.top_k, P.top_p, i, P.V, greedy, sel_k, sel_p);
+    pdl_wait();  // the statistics partials and line maxima from here on
     const T *dl = kDLMode ? static_cast<const T *>(P.dl) : nullptr;
 
     // 1. row statistics from the partials (warp per row) and the acceptance tests
@@ -2662,7 +2671,17 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     if (slot) cudaEventRecord(slot->ev[2], stream);
     auto verify = dl ? (pen_on ? sv_verify_kernel<T, true, true> : sv_verify_kernel<T, true, false>)
                      : (pen_on ? sv_verify_kernel<T, false, true> : sv_verify_kernel<T, false, false>);
-    verify<<<num_reqs, kThreads, smem, stream>>>(logits, lines, P);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(num_reqs));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, verify, logits, lines, P);
     if (slot) {
         cudaEventRecord(slot->ev[3], stream);
         slot->pending = true;
