@@ -240,7 +240,7 @@ __device__ __forceinline__ uint16_t bf16_round_up(float v)
 struct OnlineMax {
     float L = -kInf;   // running max of raw logits
     float s = 0.0f;    // running sum of 2^((l - L) c)
-    float Lc = 0.0f;   // L * c once L is finite (0 before, so that -inf logits add 2^-inf = 0)
+    float Ls = 0.0f;   // the shift: L once L is finite (0 before, so that -inf logits add 2^-inf = 0)
     int best_e = -1;   // element where L was first reached (scalar path), or -1
     int best_p = -1;   // pair where L was first reached (vector path), or -1
 };
@@ -251,11 +251,12 @@ __device__ __forceinline__ void fold1(OnlineMax &st, float l, int e, float c)
     if (l > st.L) {
         st.s = st.s == 0.0f ? 0.0f : st.s * sv::ex2_approx((st.L - l) * c);
         st.L = l;
-        st.Lc = l * c;
+        st.Ls = l;
         st.best_e = e;
         st.best_p = -1;
     }
-    st.s += sv::ex2_approx(fmaf(l, c, -st.Lc));
+    // 2^((l - L) c): the difference first, so that a large L c loses nothing to rounding
+    st.s += sv::ex2_approx((l - st.Ls) * c);
 }
 
 // The statistics kernel streams 64-byte pairs: two 32-byte loads per lane and round, the lanes of
@@ -368,6 +369,12 @@ __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsig
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b)
+{
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 
 // Elements 2k and 2k + 1 of a pair as an fp32x2 value.
 template <typename T>
@@ -380,7 +387,8 @@ __device__ __forceinline__ unsigned long long pair_elems2(const uint32_t (&w)[16
 }
 
 // Fold pair p, whose largest element is mx, without branches: one rescale of the running sum,
-// then the sum of 2^((l - L) c), two elements per packed fma / add. Only the pair that first
+// then the sum of 2^((l - L) c), two elements per packed add, multiply and add (the difference
+// is taken before the scaling: l c - L c would lose the low bits of a large L c). Only the pair that first
 // reached the max is recorded; its lowest index is recovered at the end of the segment.
 template <typename T>
 __device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16], int p, float c,
@@ -392,13 +400,13 @@ __device__ __forceinline__ void fold_pair(OnlineMax &st, const uint32_t (&w)[16]
     st.best_p = up ? p : st.best_p;
     st.best_e = up ? -1 : st.best_e;
     st.L = up ? mx : st.L;
-    st.Lc = st.L > -kInf ? st.L * c : 0.0f;
-    const unsigned long long c2 = f2_pack(c, c), nLc2 = f2_pack(-st.Lc, -st.Lc);
+    st.Ls = st.L > -kInf ? st.L : 0.0f;
+    const unsigned long long c2 = f2_pack(c, c), nL2 = f2_pack(-st.Ls, -st.Ls);
     unsigned long long acc[2] = {0ull, 0ull};  // fp32x2 zeros
 #pragma unroll
     for (int k = 0; k < kPE / 2; ++k) {
         float y0, y1;
-        f2_unpack(f2_fma(pair_elems2<T>(w, k), c2, nLc2), y0, y1);
+        f2_unpack(f2_mul(f2_add(pair_elems2<T>(w, k), nL2), c2), y0, y1);
         acc[k & 1] = f2_add(acc[k & 1], f2_pack(sv::ex2_approx(y0), sv::ex2_approx(y1)));
     }
     float a0, a1, b0, b1;
@@ -417,13 +425,13 @@ __device__ __forceinline__ void fold_vals(OnlineMax &st, const float (&y)[n], in
     st.best_p = up ? p : st.best_p;
     st.best_e = up ? -1 : st.best_e;
     st.L = up ? mx : st.L;
-    st.Lc = st.L > -kInf ? st.L * c : 0.0f;
-    const unsigned long long c2 = f2_pack(c, c), nLc2 = f2_pack(-st.Lc, -st.Lc);
+    st.Ls = st.L > -kInf ? st.L : 0.0f;
+    const unsigned long long c2 = f2_pack(c, c), nL2 = f2_pack(-st.Ls, -st.Ls);
     unsigned long long acc[2] = {0ull, 0ull};
 #pragma unroll
     for (int k = 0; k < n / 2; ++k) {
         float y0, y1;
-        f2_unpack(f2_fma(f2_pack(y[2 * k], y[2 * k + 1]), c2, nLc2), y0, y1);
+        f2_unpack(f2_mul(f2_add(f2_pack(y[2 * k], y[2 * k + 1]), nL2), c2), y0, y1);
         acc[k & 1] = f2_add(acc[k & 1], f2_pack(sv::ex2_approx(y0), sv::ex2_approx(y1)));
     }
     float a0, a1, b0, b1;
