@@ -901,26 +901,51 @@ __device__ __forceinline__ bool accept_synthetic(const VerifyParams &P, int j, i
 
 // Acceptance test of draft j ([spec-notes] answer code: draft_prob > 0 and
 // target_prob / draft_prob >= uniform; greedy: d == argmax, [spec-notes] 8.3). One thread.
+// The inputs of an acceptance test read ahead (before the statistics are complete): the draft
+// token, its target logit and its q entry (or draft logit). have == false: read them here.
+struct AcceptInputs {
+    bool have;
+    int d;
+    float l, qv;
+};
+
+template <typename T>
+__device__ __forceinline__ AcceptInputs accept_inputs(const T *rp, int V, int qrow,
+                                                      const int32_t *__restrict__ draft_ids,
+                                                      const float *__restrict__ q,
+                                                      const T *__restrict__ dl)
+{
+    AcceptInputs a{true, __ldg(draft_ids + qrow), 0.0f, 1.0f};
+    if (a.d >= 0 && a.d < V) {
+        a.l = Elem<T>::at(rp, a.d);
+        if (q) a.qv = __ldg(q + static_cast<size_t>(qrow) * V + a.d);
+        else if (dl) a.qv = Elem<T>::at(dl + static_cast<size_t>(qrow) * V, a.d);
+    }
+    return a;
+}
+
 template <typename T>
 __device__ __forceinline__ bool accept_draft(const T *rp, int V, bool greedy, int j, int qrow,
                                              const PenRow &pr, float invT, float m, float S,
                                              float tau, int amax,
                                              const int32_t *__restrict__ draft_ids,
                                              const float *__restrict__ q, const T *__restrict__ dl,
-                                             float md, float Sd, uint64_t seed, uint32_t ireq)
+                                             float md, float Sd, uint64_t seed, uint32_t ireq,
+                                             AcceptInputs in)
 {
-    const int d = __ldg(draft_ids + qrow);
+    if (!in.have) in = accept_inputs<T>(rp, V, qrow, draft_ids, q, dl);
+    const int d = in.d;
     if (greedy) return d == amax;
     if (d < 0 || d >= V) return false;
-    const float x_d = __fmul_rn(pen_apply(pr, Elem<T>::at(rp, d), d), invT);
+    const float x_d = __fmul_rn(pen_apply(pr, in.l, d), invT);
     // p' of the constrained target: 0 outside the kept set, S the kept mass
     const float t_d = x_d >= tau ? sv::exp_f32(__fsub_rn(x_d, m)) : 0.0f;
     const float p_d = __fdiv_rn(t_d, S);
     float q_d = 1.0f;
     if (q) {
-        q_d = __ldg(q + static_cast<size_t>(qrow) * V + d);
+        q_d = in.qv;
     } else if (dl) {  // q = softmax(draft logits / T), the target's steps on the draft row
-        const float xd = __fmul_rn(Elem<T>::at(dl + static_cast<size_t>(qrow) * V, d), invT);
+        const float xd = __fmul_rn(in.qv, invT);
         q_d = __fdiv_rn(sv::exp_f32(__fsub_rn(xd, md)), Sd);
     }
     const sv::Philox4 r = sv::philox4x32_10(0u, static_cast<uint32_t>(j), ireq, sv::kTagAccept,
@@ -2300,8 +2325,13 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     int sel_k;
     float sel_p;
     const bool constrained = P.sel_tau && sel_active(P.rq.top_k, P.top_p, i, P.V, greedy, sel_k, sel_p);
-    pdl_wait();  // the statistics partials and line maxima from here on
     const T *dl = kDLMode ? static_cast<const T *>(P.dl) : nullptr;
+    // this warp's first acceptance test: its inputs are read before the wait
+    AcceptInputs ahead{false, 0, 0.0f, 1.0f};
+    if (lane == 0 && warp < K && !partial && !synthetic && !greedy)
+        ahead = accept_inputs<T>(logits + static_cast<size_t>(row0 + warp) * P.V, P.V, q0 + warp,
+                                 P.draft_ids, P.q, dl);
+    pdl_wait();  // the statistics partials and line maxima from here on
 
     // 1. row statistics from the partials (warp per row) and the acceptance tests
     for (int j = warp; j <= K; j += kWarps) {
@@ -2339,8 +2369,9 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
                             : accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j,
                                               kPen ? pen_row(P.pen, P.draft_ids, i, q0, j, P.V)
                                                    : PenRow{0.0f, nullptr, nullptr, 0},
-                                              invT, m, s, tau,
-                                              amax, P.draft_ids, P.q, dl, md, Sd, P.seed, ireq)))
+                                              invT, m, s, tau, amax, P.draft_ids, P.q, dl, md,
+                                              Sd, P.seed, ireq,
+                                              j == warp ? ahead : AcceptInputs{false, 0, 0.0f, 1.0f})))
                 atomicMin(&s_js, j);
         }
     }
