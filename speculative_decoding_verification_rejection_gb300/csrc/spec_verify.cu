@@ -345,7 +345,7 @@ template <> struct PairMax<float> {
 };
 
 // Two fp32 values in one 64-bit register pair, and the packed fp32x2 operations of sm_100+
-// (each lane an ordinary correctly rounded fma / add).
+// (each lane an ordinary correctly rounded add / multiply).
 __device__ __forceinline__ unsigned long long f2_pack(float lo, float hi)
 {
     unsigned long long r;
@@ -355,13 +355,6 @@ __device__ __forceinline__ unsigned long long f2_pack(float lo, float hi)
 __device__ __forceinline__ void f2_unpack(unsigned long long v, float &lo, float &hi)
 {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b,
-                                                     unsigned long long c)
-{
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
 }
 __device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b)
 {
@@ -438,46 +431,6 @@ __device__ __forceinline__ void fold_vals(OnlineMax &st, const float (&y)[n], in
     f2_unpack(acc[0], a0, a1);
     f2_unpack(acc[1], b0, b1);
     st.s += (a0 + b0) + (a1 + b1);
-}
-
-// The processed values of a pair whose first element is token v0 of a penalised row: counts as
-// 16-byte vectors where aligned (the same for every pair of a segment), the earlier drafts added
-// where one falls in the pair (rare).
-template <typename T>
-__device__ __forceinline__ void pen_pair(const PenRow &pr, const uint32_t (&w)[16], int v0,
-                                         bool aligned, float (&y)[kPairBytes / sizeof(T)])
-{
-    constexpr int kPE = kPairBytes / sizeof(T);
-    int c[kPE];
-    if (aligned) {
-        const int4 *cp = reinterpret_cast<const int4 *>(pr.cnt + v0);
-#pragma unroll
-        for (int q = 0; q < kPE / 4; ++q) {
-            const int4 t = __ldg(cp + q);
-            c[4 * q] = t.x;
-            c[4 * q + 1] = t.y;
-            c[4 * q + 2] = t.z;
-            c[4 * q + 3] = t.w;
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < kPE; ++e) c[e] = __ldg(pr.cnt + v0 + e);
-    }
-    bool hit = false;
-    for (int k = 0; k < pr.nprev; ++k)
-        hit |= static_cast<unsigned>(__ldg(pr.prev + k) - v0) < static_cast<unsigned>(kPE);
-    if (hit) {
-        for (int k = 0; k < pr.nprev; ++k) {
-            const int d = __ldg(pr.prev + k) - v0;
-#pragma unroll
-            for (int e = 0; e < kPE; ++e) c[e] += d == e;
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < kPE; ++e) {
-        const float l = pair_elem<T>(w, e);
-        y[e] = c[e] == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(c[e]), l);
-    }
 }
 
 // Division by a launch constant d > 0 without a division instruction: with M = ceil(2^64 / d)
@@ -651,16 +604,54 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
         part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
 }
 
-// stats_segment for a batch with a frequency penalty: the same partials over the processed values
-// y (see PenRow), and line maxima rounded up to the logits' type (an upper bound of the line's y).
-// The row is streamed as 16-byte vectors (8 bf16 / 4 fp32 elements, a lane each) with their
-// counts (16-byte vectors where the counts row is so aligned: the same for every vector of the
-// segment), two rounds in flight while one is processed. c = (1 / T) log2(e) of the row's request.
+// Asynchronous 16- and 4-byte copies global -> shared (cp.async), tracked per thread in commit
+// groups: wait_group<n> returns once at most n of the thread's latest groups are still in flight,
+// and the thread then sees what its completed copies wrote.
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// through L1 (.ca): the two halves of a 32-byte sector that two copies of one lane read are
+// fetched from L2 once
+__device__ __forceinline__ void cp_async16_l1(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int n>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
+
+// Staging ring of the penalised statistics path: per warp kPenStages rounds, per round and lane
+// one slot of 48 bytes (a 16-byte logit vector, then its counts: 8 ints for bf16, 4 for fp32).
+// 48-byte slots keep the lanes' 16-byte shared loads free of bank conflicts.
+constexpr int kPenStages = 4;
+constexpr int kPenSlot = 48;
+constexpr int kPenRingBytes = kWarps * kPenStages * 32 * kPenSlot;
+
+// stats_segment for a penalised row (PenRow with f != 0): the same partials over the processed
+// values y (see PenRow), and line maxima rounded up to the logits' type (an upper bound of the
+// line's y). The row is streamed as 16-byte vectors (8 bf16 / 4 fp32 elements, a lane each), each
+// with its counts, copied asynchronously into the lane's own slots of the warp's ring (`ring`,
+// kPenStages rounds of 32 slots): kPenStages - 1 rounds are in flight while one is processed, and
+// no register holds data in flight. Counts are copied as 16-byte vectors through L1 where the
+// counts row is so aligned (the same for every vector of the segment), else as single ints. The earlier drafts
+// of the position (at most 32 of them in the lanes' registers) are tested once per round against
+// the warp's window of tokens; only a round that holds one adds them lane by lane.
+// c = (1 / T) log2(e) of the row's request.
 template <typename T>
 __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, int V, int row, int b,
                                                   int e, int seg, int maxseg, int base_off, float c,
                                                   const PenRow &pr, StatPart *__restrict__ part,
-                                                  T *__restrict__ s_lines, long long line_base)
+                                                  T *__restrict__ s_lines, long long line_base,
+                                                  unsigned char *ring)
 {
     constexpr int kEV = 16 / static_cast<int>(sizeof(T));  // elements per vector
     constexpr int kVPL = kGroup / kEV;                      // vectors per 64-element line
@@ -672,42 +663,59 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
     const int nvec = (e - a0) / kEV;
     const int a1 = a0 + nvec * kEV;
     const char *vbase = reinterpret_cast<const char *>(rp + a0);
+    const int32_t *cbase = pr.cnt + a0;
     const int line0 = static_cast<int>(((pos_b + (a0 - b)) >> 6) - line_base);
     const int lane = threadIdx.x & 31;
-    const bool pen = pr.f != 0.0f;
-    const bool aligned = pen && (reinterpret_cast<uintptr_t>(pr.cnt + a0) & 15u) == 0u;
+    const bool aligned = (reinterpret_cast<uintptr_t>(cbase) & 15u) == 0u;
+    const uint32_t slot0 = smem_u32(ring) + lane * kPenSlot;
+    constexpr uint32_t kStageBytes = 32 * kPenSlot;
 
-    struct Vec {
-        uint4 w;
-        int c[kEV];
-    };
-    auto load = [&](int u, Vec &x) {
-        if (u >= nvec) return;
-        x.w = ldg_v4(vbase + static_cast<size_t>(u) * 16);
-        if (!pen) return;
-        const int v = a0 + u * kEV;
-        if (aligned) {
+    auto issue = [&](int u, int stage) {
+        if (u < nvec) {
+            const uint32_t d = slot0 + stage * kStageBytes;
+            cp_async16(d, vbase + static_cast<size_t>(u) * 16);
+            const int32_t *cs = cbase + u * kEV;
+            if (aligned) {
 #pragma unroll
-            for (int q = 0; q < kEV / 4; ++q) {
-                const int4 t = __ldg(reinterpret_cast<const int4 *>(pr.cnt + v) + q);
-                x.c[4 * q] = t.x;
-                x.c[4 * q + 1] = t.y;
-                x.c[4 * q + 2] = t.z;
-                x.c[4 * q + 3] = t.w;
+                for (int q = 0; q < kEV / 4; ++q) cp_async16_l1(d + 16 + 16 * q, cs + 4 * q);
+            } else {
+#pragma unroll
+                for (int k = 0; k < kEV; ++k) cp_async4(d + 16 + 4 * k, cs + k);
             }
-        } else {
-#pragma unroll
-            for (int k = 0; k < kEV; ++k) x.c[k] = __ldg(pr.cnt + v + k);
         }
+        cp_async_commit();
     };
-    // the processed values of vector u
-    auto values = [&](int u, const Vec &x, float (&y)[kEV]) {
-        const uint32_t ws[4] = {x.w.x, x.w.y, x.w.z, x.w.w};
-        const int v = a0 + u * kEV;
-        bool hit = false;
-        if (pen)
+    // y of the kEV tokens from v: logits words ws, counts cnt, plus the earlier drafts if `scan`.
+    // A count in [0, 2^23) becomes a float exactly by placing it in the significand of 2^23 and
+    // subtracting 2^23 (full-rate integer and float operations instead of a conversion); a vector
+    // with any other count converts them.
+    auto values = [&](int v, const uint32_t (&ws)[4], const int (&cnt)[kEV], bool scan,
+                      float (&y)[kEV]) {
+        int n[kEV];
+#pragma unroll
+        for (int k = 0; k < kEV; ++k) n[k] = cnt[k];
+        if (scan) {
+            bool hit = false;
             for (int k = 0; k < pr.nprev; ++k)
                 hit |= static_cast<unsigned>(__ldg(pr.prev + k) - v) < static_cast<unsigned>(kEV);
+            if (hit)
+                for (int q = 0; q < pr.nprev; ++q) {
+                    const int d = __ldg(pr.prev + q) - v;
+#pragma unroll
+                    for (int k = 0; k < kEV; ++k) n[k] += d == k;
+                }
+        }
+        int any = 0;
+#pragma unroll
+        for (int k = 0; k < kEV; ++k) any |= n[k];
+        float fn[kEV];
+        if ((static_cast<unsigned>(any) >> 23) == 0u) {
+#pragma unroll
+            for (int k = 0; k < kEV; ++k) fn[k] = __int_as_float(n[k] | 0x4B000000) - 8388608.0f;
+        } else {
+#pragma unroll
+            for (int k = 0; k < kEV; ++k) fn[k] = __int2float_rn(n[k]);
+        }
 #pragma unroll
         for (int k = 0; k < kEV; ++k) {
             float l;
@@ -715,27 +723,45 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
                 l = __uint_as_float((k & 1) ? (ws[k >> 1] & 0xFFFF0000u) : (ws[k >> 1] << 16));
             else
                 l = __uint_as_float(ws[k]);
-            int cnt = pen ? x.c[k] : 0;
-            if (hit)
-                for (int q = 0; q < pr.nprev; ++q) cnt += __ldg(pr.prev + q) == v + k;
-            y[k] = cnt == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(cnt), l);
+            y[k] = n[k] == 0 ? l : __fmaf_rn(-pr.f, fn[k], l);
         }
     };
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
+    // earlier drafts: lane k holds the k-th (k < 32); more than 32 are scanned every round
+    const int np = pr.nprev;
+    const int pv = lane < np ? __ldg(pr.prev + lane) : -1;
     int ub = static_cast<int>(threadIdx.x) & ~31;
-    Vec x0, x1, x2;
-    load(ub + lane, x0);
-    load(ub + lane + kThreads, x1);
-    auto round = [&](const Vec &cur, Vec &nxt) {
+#pragma unroll
+    for (int s = 0; s < kPenStages - 1; ++s) issue(ub + lane + s * kThreads, s);
+    int stage = 0;
+    for (; ub < nvec; ub += kThreads) {
         const int u = ub + lane;
-        load(u + 2 * kThreads, nxt);
+        // the stage read in the previous round takes the round kPenStages - 1 ahead
+        issue(u + (kPenStages - 1) * kThreads, stage == 0 ? kPenStages - 1 : stage - 1);
+        const int wlo = a0 + ub * kEV;  // the warp's tokens this round: [wlo, wlo + 32 kEV)
+        const bool scan = np > 32 ||
+                          __ballot_sync(0xFFFFFFFFu, static_cast<unsigned>(pv - wlo) <
+                                                          static_cast<unsigned>(32 * kEV)) != 0u;
+        cp_async_wait<kPenStages - 1>();
         float y[kEV];
         float mx = -kInf;
         if (u < nvec) {
-            values(u, cur, y);
+            const unsigned char *sl = ring + stage * kStageBytes + lane * kPenSlot;
+            const uint4 w = *reinterpret_cast<const uint4 *>(sl);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            int cnt[kEV];
+#pragma unroll
+            for (int q = 0; q < kEV / 4; ++q) {
+                const int4 t = *reinterpret_cast<const int4 *>(sl + 16 + 16 * q);
+                cnt[4 * q] = t.x;
+                cnt[4 * q + 1] = t.y;
+                cnt[4 * q + 2] = t.z;
+                cnt[4 * q + 3] = t.w;
+            }
+            values(a0 + u * kEV, ws, cnt, scan, y);
 #pragma unroll
             for (int k = 0; k < kEV; ++k) mx = fmaxf(mx, y[k]);
         }
@@ -749,27 +775,25 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
             }
         }
         if (u < nvec) fold_vals<kEV>(st, y, u, c, mx);
-        ub += kThreads;
-    };
-    while (ub < nvec) {
-        round(x0, x2);
-        if (ub >= nvec) break;
-        round(x1, x0);
-        if (ub >= nvec) break;
-        round(x2, x1);
+        stage = stage + 1 == kPenStages ? 0 : stage + 1;
     }
+    cp_async_wait<0>();  // (the groups past the segment hold no copies) the ring is free again
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
 
     int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
     if (st.best_p >= 0) {  // the vector that first reached the max: its lowest index
-        Vec x;
-        load(st.best_p, x);
+        const int v = a0 + st.best_p * kEV;
+        const uint4 w = ldg_v4(vbase + static_cast<size_t>(st.best_p) * 16);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        int cnt[kEV];
+#pragma unroll
+        for (int k = 0; k < kEV; ++k) cnt[k] = __ldg(cbase + st.best_p * kEV + k);
         float y[kEV];
-        values(st.best_p, x, y);
+        values(v, ws, cnt, true, y);
 #pragma unroll
         for (int h = kEV - 1; h >= 0; --h)
-            if (y[h] == st.L) idx = a0 + st.best_p * kEV + h;
+            if (y[h] == st.L) idx = v + h;
     }
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
@@ -800,11 +824,12 @@ struct StatsArray {
 // covers only in part are left undefined (the verify kernel reads those lines from the logits).
 // The first A.grid CTAs take the target logits, the rest the draft logits (if any). Nothing waits
 // on another CTA.
-// kPen: the batch has a frequency penalty (penalised rows take stats_segment_pen).
+// kPen: the batch has a frequency penalty (penalised rows take stats_segment_pen, with the
+// staging ring at ring_off bytes into the dynamic shared memory, after the line maxima).
 template <typename T, bool kPen>
 __global__ void __launch_bounds__(kThreads, kPen ? 2 : 3)
 sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTable rq,
-                PenTable pt, const int32_t *__restrict__ draft_ids)
+                PenTable pt, const int32_t *__restrict__ draft_ids, int ring_off)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     pdl_launch_dependents();
@@ -823,19 +848,26 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
         const int fk = static_cast<int>(div_floor(X.base_off + rbase, X.chunk));
-        if constexpr (kPen) {  // every row takes the penalty path (penalties: target logits only)
-            const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31, X.draft_rows != 0);
-            const int q0 = __ldg(rq.cu + i);
-            const PenRow pr = X.draft_rows ? PenRow{0.0f, nullptr, nullptr, 0}
-                                           : pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
-            bool greedy;
-            const float c = request_invT(rq, i, greedy) * kLog2e;
-            stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c, pr,
-                                 X.part, s_lines, line_base);
-        } else {
+        bool plain = true;
+        if constexpr (kPen) {  // a penalised row takes the penalty path (target logits only)
+            if (!X.draft_rows) {
+                const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31);
+                const int q0 = __ldg(rq.cu + i);
+                const PenRow pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
+                if (pr.f != 0.0f) {
+                    bool greedy;
+                    const float c = request_invT(rq, i, greedy) * kLog2e;
+                    stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c,
+                                         pr, X.part, s_lines, line_base,
+                                         s_raw + ring_off + (threadIdx.x >> 5) *
+                                                                (kPenRingBytes / kWarps));
+                    plain = false;
+                }
+            }
+        }
+        if (plain)
             stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part,
                              s_lines, line_base, X.draft_rows != 0);
-        }
     }
     if (X.lines) {
         __syncthreads();
@@ -2581,6 +2613,10 @@ cudaError_t setup_kernels(int device, int *stats_per_sm)
         es = cudaFuncSetAttribute(sv_select_kernel<T, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(kSelDynSmem));
+    if (es == cudaSuccess)  // line maxima of the largest chunk, then the staging ring
+        es = cudaFuncSetAttribute(sv_stats_kernel<T, true>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(kMaxChunk / kGroup * sizeof(T) + kPenRingBytes));
     if (es != cudaSuccess) return es;
     const void *kernels[] = {reinterpret_cast<const void *>(sv_shard_race_kernel<T>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
@@ -2681,12 +2717,13 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         cudaEventRecord(slot->ev[0], stream);
     }
     const size_t smem1 = lines ? static_cast<size_t>(chunk1 / kGroup) * sizeof(T) : 0;
+    const size_t ring_off = (smem1 + 15) / 16 * 16;
     if (pen_on)
-        sv_stats_kernel<T, true><<<A.grid + D.grid, kThreads, smem1, stream>>>(
-            V, ctx->maxseg, A, D, rq, pen, b.draft_ids);
+        sv_stats_kernel<T, true><<<A.grid + D.grid, kThreads, ring_off + kPenRingBytes, stream>>>(
+            V, ctx->maxseg, A, D, rq, pen, b.draft_ids, static_cast<int>(ring_off));
     else
         sv_stats_kernel<T, false><<<A.grid + D.grid, kThreads, smem1, stream>>>(
-            V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids);
+            V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids, 0);
     if (slot) cudaEventRecord(slot->ev[1], stream);
     if (sel_on) {  // top-k / top-p: the kept set of every constrained row
         SelectParams SP;
@@ -2937,7 +2974,7 @@ int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int 
         const StatsArray<T> D = stats_array<T>(nullptr, 0, chunk1, Vs, 1, nullptr, nullptr);
         const size_t smem1 = static_cast<size_t>(chunk1 / kGroup) * sizeof(T);
         sv_stats_kernel<T, false><<<A.grid, kThreads, smem1, stream>>>(
-            Vs, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, draft_ids);
+            Vs, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, draft_ids, 0);
         sv_shard_export_kernel<T><<<(R + kWarps - 1) / kWarps, kThreads, 0, stream>>>(
             lg, rq, draft_ids, draft_probs_shard, ctx->statpart, Vs, v0, ctx->maxseg, A.base_off,
             A.chunk, R, out);
