@@ -1504,12 +1504,14 @@ __device__ __forceinline__ float key_value(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 // Level-1 bin: 0 holds the values less than 1/64 nat below m, the last everything further down
-// than 2047/64 nats.
+// than 2047/64 nats. u = (m - x) 64 is clamped to [0, 2047] (NaN: the last bin) and truncated by
+// a round-toward-zero add into the significand of 2^23 (full-rate float and integer operations
+// instead of a conversion).
 __device__ __forceinline__ int sel_bin1(float x, float m)
 {
-    const float u = __fmul_rn(__fsub_rn(m, x), kSelBinsPerNat);
-    return u < static_cast<float>(kSelBins1 - 1) ? (u > 0.0f ? static_cast<int>(u) : 0)
-                                                  : kSelBins1 - 1;  // NaN: the last bin
+    const float u = fmaxf(fminf(__fmul_rn(__fsub_rn(m, x), kSelBinsPerNat),
+                                static_cast<float>(kSelBins1 - 1)), 0.0f);
+    return __float_as_int(__fadd_rz(u, 8388608.0f)) - 0x4B000000;
 }
 // A token's mass exp(x - m), by the hardware ex2.
 __device__ __forceinline__ float sel_mass(float x, float m)
@@ -1517,9 +1519,10 @@ __device__ __forceinline__ float sel_mass(float x, float m)
     return sv::ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
-// Dynamic shared memory of the select kernel: [kWarps][kSelBins] per-warp counts or masses
-// (float bits) of the finer levels, the level-1 counts [kWarps][kSelBins1] (a copy per warp),
-// then two pools of kSelPool tokens.
+// Dynamic shared memory of the select kernel (72 KB: three CTAs per SM): [kWarps][kSelBins]
+// per-warp counts or masses (float bits) of the finer levels, the level-1 counts
+// [kSel1Copies][kSelBins1] (a copy per pair of warps), then two pools of kSelPool tokens.
+constexpr int kSel1Copies = kWarps / 2;
 extern __shared__ __align__(16) unsigned char sv_sel_dyn[];
 
 struct SelSmem {
@@ -1527,13 +1530,13 @@ struct SelSmem {
     __device__ __forceinline__ uint32_t *cnt1() const { return hist() + kWarps * kSelBins; }
     __device__ __forceinline__ float *pool_a() const
     {
-        return reinterpret_cast<float *>(cnt1() + kWarps * kSelBins1);
+        return reinterpret_cast<float *>(cnt1() + kSel1Copies * kSelBins1);
     }
-    // a level-1 bin's count over the warps
+    // a level-1 bin's count over the copies
     __device__ __forceinline__ uint32_t count1(int b) const
     {
         uint32_t c = 0u;
-        for (int w = 0; w < kWarps; ++w) c += cnt1()[w * kSelBins1 + b];
+        for (int w = 0; w < kSel1Copies; ++w) c += cnt1()[w * kSelBins1 + b];
         return c;
     }
     __device__ __forceinline__ float *pool_b() const { return pool_a() + kSelPool; }
@@ -1547,24 +1550,46 @@ struct SelSmem {
 };
 
 // Every element of a row once, as x = processed logit * (1 / T), with its token index: 16-byte
-// loads over the aligned body, four in flight per thread.
+// loads over the aligned body, four in flight per thread (with a penalty, each with its counts,
+// 16-byte loads where the counts row is so aligned). The rounds are uniform over the warp (a
+// lane past the end takes part without an element), so that the earlier drafts (lane k holding
+// the k-th, k < 32) are tested against the warp's window of tokens by one ballot per vector
+// round; only a window that holds one adds them token by token.
 template <typename T, bool kPen, typename F>
 __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, float invT,
                                             const PenRow &pr, F &&f)
 {
     constexpr int kEV = 16 / static_cast<int>(sizeof(T));
     constexpr int kIn = 4;
+    constexpr int kCV = kPen ? kEV / 4 : 1;  // 16-byte count vectors per logit vector
     const int head = min(V, static_cast<int>(((16u - (reinterpret_cast<uintptr_t>(rp) & 15u)) & 15u) / sizeof(T)));
     auto proc = [&](float l, int v) { return __fmul_rn(kPen ? pen_apply(pr, l, v) : l, invT); };
     for (int v = threadIdx.x; v < head; v += kThreads) f(proc(Elem<T>::at(rp, v), v), v);
     const int nvec = (V - head) / kEV;
     const char *base = reinterpret_cast<const char *>(rp + head);
-    for (int u0 = threadIdx.x; u0 < nvec; u0 += kIn * kThreads) {
+    const int lane = threadIdx.x & 31;
+    const bool pen = kPen && pr.f != 0.0f;
+    const bool al = pen && (reinterpret_cast<uintptr_t>(pr.cnt + head) & 15u) == 0u;
+    const int pv = pen && lane < pr.nprev ? __ldg(pr.prev + lane) : -1;
+    for (int u0 = threadIdx.x; (u0 & ~31) < nvec; u0 += kIn * kThreads) {
         uint4 w[kIn];
+        int4 cv[kIn][kCV];
+        bool scan[kIn];
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
             const int u = u0 + q * kThreads;
             w[q] = u < nvec ? ldg_v4(base + static_cast<size_t>(u) * 16) : make_uint4(0, 0, 0, 0);
+            if constexpr (kPen) {
+#pragma unroll
+                for (int g = 0; g < kCV; ++g)
+                    cv[q][g] = al && u < nvec
+                                   ? __ldg(reinterpret_cast<const int4 *>(pr.cnt + head + u * kEV) + g)
+                                   : make_int4(0, 0, 0, 0);
+                const int wlo = head + ((u0 & ~31) + q * kThreads) * kEV;  // the warp's window
+                scan[q] = pen && (pr.nprev > 32 ||
+                                  __ballot_sync(0xFFFFFFFFu, static_cast<unsigned>(pv - wlo) <
+                                                                 static_cast<unsigned>(32 * kEV)) != 0u);
+            }
         }
 #pragma unroll
         for (int q = 0; q < kIn; ++q) {
@@ -1573,28 +1598,25 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
             const uint32_t ws[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
             const int v0 = head + u * kEV;
             int cnt[kEV];
-            bool hit = false;
-            if constexpr (kPen) {  // the vector's counts at once, the earlier drafts by one test
-                if (pr.f != 0.0f) {
-                    if ((reinterpret_cast<uintptr_t>(pr.cnt + v0) & 15u) == 0u) {
+            if constexpr (kPen) {
+                if (al) {
 #pragma unroll
-                        for (int g = 0; g < kEV / 4; ++g) {
-                            const int4 t = __ldg(reinterpret_cast<const int4 *>(pr.cnt + v0) + g);
-                            cnt[4 * g] = t.x;
-                            cnt[4 * g + 1] = t.y;
-                            cnt[4 * g + 2] = t.z;
-                            cnt[4 * g + 3] = t.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < kEV; ++e) cnt[e] = __ldg(pr.cnt + v0 + e);
+                    for (int g = 0; g < kCV; ++g) {
+                        cnt[4 * g] = cv[q][g].x;
+                        cnt[4 * g + 1] = cv[q][g].y;
+                        cnt[4 * g + 2] = cv[q][g].z;
+                        cnt[4 * g + 3] = cv[q][g].w;
                     }
-                    for (int g = 0; g < pr.nprev; ++g)
-                        hit |= static_cast<unsigned>(__ldg(pr.prev + g) - v0) < static_cast<unsigned>(kEV);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < kEV; ++e) cnt[e] = 0;
+                    for (int e = 0; e < kEV; ++e) cnt[e] = pen ? __ldg(pr.cnt + v0 + e) : 0;
                 }
+                if (scan[q])
+                    for (int g = 0; g < pr.nprev; ++g) {
+                        const int d = __ldg(pr.prev + g) - v0;
+#pragma unroll
+                        for (int e = 0; e < kEV; ++e) cnt[e] += d == e;
+                    }
             }
 #pragma unroll
             for (int e = 0; e < kEV; ++e) {
@@ -1605,10 +1627,7 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
                     l = __uint_as_float(ws[e]);
                 const int v = v0 + e;
                 if constexpr (kPen) {
-                    int c = cnt[e];
-                    if (hit)
-                        for (int g = 0; g < pr.nprev; ++g) c += __ldg(pr.prev + g) == v;
-                    const float y = c == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(c), l);
+                    const float y = cnt[e] == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(cnt[e]), l);
                     f(__fmul_rn(y, invT), v);
                 } else {
                     f(__fmul_rn(l, invT), v);
@@ -1621,7 +1640,8 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
 }
 
 constexpr size_t kSelDynSmem =
-    (static_cast<size_t>(kWarps) * (kSelBins + kSelBins1) + 2 * kSelPool) * 4;
+    (static_cast<size_t>(kWarps) * kSelBins + static_cast<size_t>(kSel1Copies) * kSelBins1 +
+     2 * kSelPool) * 4;
 
 __device__ __forceinline__ void sel_clear(SelSmem &sm, int nbins)
 {
@@ -1978,7 +1998,7 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
 
 // The threshold and the kept mass of every constrained row: one CTA per logit row.
 template <typename T, bool kPen>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kPen ? 2 : 3)
 sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectParams P)
 {
     __shared__ SelSmem sm;
@@ -2002,9 +2022,9 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
 
     // level 1: counts per bin of 1/128 nat (integer atomics) of the tokens x >= xmin
     auto count_level1 = [&](float xmin) {
-        for (int b = threadIdx.x; b < kWarps * kSelBins1; b += kThreads) sm.cnt1()[b] = 0u;
+        for (int b = threadIdx.x; b < kSel1Copies * kSelBins1; b += kThreads) sm.cnt1()[b] = 0u;
         __syncthreads();
-        uint32_t *mine = sm.cnt1() + (threadIdx.x >> 5) * kSelBins1;
+        uint32_t *mine = sm.cnt1() + (threadIdx.x >> 6) * kSelBins1;  // two warps per copy
         sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
             if (x >= xmin) atomicAdd(mine + sel_bin1(x, m), 1u);
         });
