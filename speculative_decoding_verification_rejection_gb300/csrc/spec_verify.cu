@@ -1173,7 +1173,10 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
         for (int k = 0; k < kStep; ++k) {
             const int g = g0 + k * kThreads;
             if (g < r.G) {
-                const float b = group_bound(__fsub_rn(__fmul_rn(lmax[k], r.invT), r.m), h[k].x);
+                // a group whose largest x is below the kept set's threshold holds no candidate
+                // (x_v = fl(l_v / T) <= fl(lmax / T)): bound 0 (NaN groups stay in the race)
+                const float xg = __fmul_rn(lmax[k], r.invT);
+                const float b = !(xg < r.tau) ? group_bound(__fsub_rn(xg, r.m), h[k].x) : 0.0f;
                 sm.pb[g] = b;
                 sm.ew[g] = h[k].x;
                 sm.ag[g] = static_cast<uint8_t>(h[k].y & 63u);
