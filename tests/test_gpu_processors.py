@@ -159,3 +159,38 @@ def test_constrained_workload_style():
     got = gpu_run(b)
     r = assert_parity(b, got, oracle.run(b))
     print(f"workload 3 (48 requests) with top-p 0.9 / top-k 50: ties {r['ties']}")
+
+
+@pytest.mark.parametrize("dtype,V", [("bf16", 5000), ("f32", 3001)])
+def test_penalty_long_drafts_and_extreme_counts(dtype, V):
+    """More than 32 earlier drafts (the statistics and selection passes then add them in every
+    round), counts of 2^23 and beyond (converted by the exact fallback) and negative counts,
+    with and without top-k / top-p."""
+    b = _batch(110, V, [40, 3, 0, 35, 2], dtype, "noisy", greedy_frac=0.0)
+    workloads.add_penalty(b, 110, history=(20, 80), top_n=20)
+    rng = np.random.default_rng([110, V])
+    cols = rng.choice(V, 8, replace=False)
+    b.output_bin_counts[0, cols[:4]] = [1 << 23, (1 << 24) + 1, (1 << 30) + 3, -3]
+    b.output_bin_counts[3, cols[4:]] = [(1 << 23) + 5, -1, 7, (1 << 25) - 1]
+    b.draft_ids[5:12] = b.draft_ids[0]          # repeated drafts: counted at later positions
+    b.draft_ids[45:50] = b.draft_ids[44]
+    assert_parity(b, gpu_run(b), oracle.run(b))
+    _constrain(b, 110, [0, 30], [0.9, 1.0])
+    assert_parity(b, gpu_run(b), oracle.run(b))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_constraints_on_masked_and_huge_logits(dtype):
+    """top-k / top-p over rows with a masked vocabulary (-inf on 70 % of tokens) and dominant
+    tokens: most 64-token groups lie below the threshold and are left out of the race."""
+    V = 3000
+    b = _batch(111, V, [3, 2, 0, 4, 1, 3], dtype, "none")
+    rng = np.random.default_rng(111)
+    x = rng.normal(0, 2, (b.num_rows, V)).astype(np.float32)
+    x[:, rng.random(V) < 0.7] = -np.inf
+    x[1, 5] = 1.0e4
+    x[3, 7] = x[3, 9] = 3.0e3
+    x[:, 11] = np.maximum(x[:, 11], -50.0)
+    b.logits = x if dtype == "f32" else (x.view(np.uint32) >> 16).astype(np.uint16)  # truncated
+    _constrain(b, 111, [0, 1, 3, 40], [0.5, 0.95, 1.0])
+    assert_parity(b, gpu_run(b), oracle.run(b))
