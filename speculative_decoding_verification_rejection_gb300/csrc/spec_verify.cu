@@ -1470,7 +1470,7 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
 constexpr int kSelBins1 = 2048;         // level 1: counts in bins of 1/64 nat below the maximum
 constexpr float kSelBinsPerNat = 64.0f;
 constexpr int kSelBins = 256;           // the finer levels: 8 key bits each
-constexpr int kSelPool = 4096;          // tokens refined in shared memory
+constexpr int kSelPool = 2048;          // tokens refined in shared memory
 static_assert(kSelBins == kThreads && kSelBins1 % kThreads == 0, "bins per thread");
 
 struct SelectParams {
@@ -1522,10 +1522,10 @@ __device__ __forceinline__ float sel_mass(float x, float m)
     return sv::ex2_approx(__fmul_rn(__fsub_rn(x, m), kLog2e));
 }
 
-// Dynamic shared memory of the select kernel (72 KB: three CTAs per SM): [kWarps][kSelBins]
-// per-warp counts or masses (float bits) of the finer levels, the level-1 counts
-// [kSel1Copies][kSelBins1] (a copy per pair of warps), then two pools of kSelPool tokens.
-constexpr int kSel1Copies = kWarps / 2;
+// Dynamic shared memory of the select kernel (40 KB: four CTAs per SM at 64 registers):
+// [kWarps][kSelBins] per-warp counts or masses (float bits) of the finer levels, the level-1
+// counts [kSel1Copies][kSelBins1] (a copy per four warps), then two pools of kSelPool tokens.
+constexpr int kSel1Copies = kWarps / 4;
 extern __shared__ __align__(16) unsigned char sv_sel_dyn[];
 
 struct SelSmem {
@@ -2001,7 +2001,7 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
 
 // The threshold and the kept mass of every constrained row: one CTA per logit row.
 template <typename T, bool kPen>
-__global__ void __launch_bounds__(kThreads, kPen ? 2 : 3)
+__global__ void __launch_bounds__(kThreads, kPen ? 2 : 4)
 sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectParams P)
 {
     __shared__ SelSmem sm;
@@ -2027,7 +2027,7 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     auto count_level1 = [&](float xmin) {
         for (int b = threadIdx.x; b < kSel1Copies * kSelBins1; b += kThreads) sm.cnt1()[b] = 0u;
         __syncthreads();
-        uint32_t *mine = sm.cnt1() + (threadIdx.x >> 6) * kSelBins1;  // two warps per copy
+        uint32_t *mine = sm.cnt1() + (threadIdx.x >> 7) * kSelBins1;  // four warps per copy
         sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
             if (x >= xmin) atomicAdd(mine + sel_bin1(x, m), 1u);
         });
