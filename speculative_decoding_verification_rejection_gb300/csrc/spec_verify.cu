@@ -708,6 +708,16 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
         int any = 0;
 #pragma unroll
         for (int k = 0; k < kEV; ++k) any |= n[k];
+        if (any == 0) {  // (almost every vector: counts are sparse) y = l
+#pragma unroll
+            for (int k = 0; k < kEV; ++k) {
+                if constexpr (sizeof(T) == 2)
+                    y[k] = __uint_as_float((k & 1) ? (ws[k >> 1] & 0xFFFF0000u) : (ws[k >> 1] << 16));
+                else
+                    y[k] = __uint_as_float(ws[k]);
+            }
+            return;
+        }
         float fn[kEV];
         if ((static_cast<unsigned>(any) >> 23) == 0u) {
 #pragma unroll
