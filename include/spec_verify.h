@@ -184,7 +184,8 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
  *                    position j of request i the count of token v is
  *                    c = output_bin_counts[counts_row[i], v] + #{k < j : draft_k == v} (the
  *                    drafts before j are output the target conditions on there), and the
- *                    processed logit is fma(-penalty, c, logit) (one rounding) where
+ *                    processed logit is fma(-penalty, c, logit) (one rounding; c as a
+ *                    binary32 value rounded to nearest, exact below 2^24) where
  *                    penalty != 0 and c != 0, the logit itself otherwise; x = processed / T.
  *                    Greedy requests take the argmax of the processed logits; row_max /
  *                    row_argmax report them. The draft logits are not penalised. Both

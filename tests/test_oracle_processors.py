@@ -184,3 +184,32 @@ def test_constraints_do_not_touch_greedy_requests_and_the_max_is_always_kept():
         tok = r["sampled"][i, js]
         x = np.float32(logits[row, tok]) * np.float32(np.float32(1.0) / b.temperature[i])
         assert x == r["row_max"][row]                              # a token of the maximum
+
+
+def test_large_and_negative_counts():
+    """The count enters the one-rounding fma as a binary32 value (rounded to nearest): 2^24 + 1
+    becomes 2^24, so a token with that count ties one with count 2^24 and the lower index wins;
+    with the count taken exactly it would lose by 2^-20. A negative count raises the logit."""
+    V = 64
+    row = np.full(V, -5.0, np.float32)
+    row[3] = row[9] = 16.0
+    b = _one_request(V, 0, row[None, :], [], greedy=1)
+    b.frequency_penalty = np.array([2.0 ** -20], np.float32)
+    counts = np.zeros((1, V), np.int32)
+    counts[0, 3] = (1 << 24) + 1
+    counts[0, 9] = 1 << 24
+    b.output_bin_counts = counts
+    r = oracle.run(b)
+    assert r["row_max"][0] == np.float32(0.0)     # 16 - 2^-20 * 2^24 for both tokens
+    assert r["sampled"][0, 0] == 3                # a tie: the lower index
+
+    row = np.zeros(V, np.float32)
+    row[5], row[7] = 2.0, 1.0
+    b = _one_request(V, 0, row[None, :], [], greedy=1)
+    b.frequency_penalty = np.array([0.5], np.float32)
+    counts = np.zeros((1, V), np.int32)
+    counts[0, 7] = -3                              # 1 + 0.5 * 3 = 2.5 > 2
+    b.output_bin_counts = counts
+    r = oracle.run(b)
+    assert r["row_max"][0] == np.float32(2.5)
+    assert r["sampled"][0, 0] == 7
