@@ -28,7 +28,7 @@ class _Options(ctypes.Structure):
                 ("output_bin_counts", ctypes.c_void_p), ("counts_row", ctypes.c_void_p),
                 ("counts_rows", ctypes.c_int32), ("top_k", ctypes.c_void_p),
                 ("top_p", ctypes.c_void_p),
-                ("row_select_margin", ctypes.c_void_p)]
+                ("row_select_margin", ctypes.c_void_p), ("fp64_gumbel", ctypes.c_int32)]
 EBATCH = 1
 
 # Strict IEEE binary32: no contraction of a*b+c into fma (only the explicit fmaf calls
@@ -92,6 +92,14 @@ def lib():
         L.spec_verify_ref_shard_finish.restype = None
         L.spec_verify_ref_race_clocks.argtypes = [u64, u32, u32, i32, vp]
         L.spec_verify_ref_race_clocks.restype = None
+        L.spec_verify_ref_race_clocks64.argtypes = [u64, u32, u32, i32, vp]
+        L.spec_verify_ref_race_clocks64.restype = None
+        L.spec_verify_ref_log64_n.argtypes = [vp, vp, ctypes.c_int64]
+        L.spec_verify_ref_log64_n.restype = None
+        L.spec_verify_ref_log64.argtypes = [ctypes.c_double]
+        L.spec_verify_ref_log64.restype = ctypes.c_double
+        L.spec_verify_ref_uniform64.argtypes = [u32, u32]
+        L.spec_verify_ref_uniform64.restype = ctypes.c_double
         _lib = L
     return _lib
 
@@ -143,6 +151,29 @@ def race_clocks(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
     out = np.empty(n, dtype=np.float32)
     lib().spec_verify_ref_race_clocks(seed, j, ireq, n, _p(out))
     return out
+
+
+def race_clocks64(seed: int, j: int, ireq: int, n: int) -> np.ndarray:
+    """Race clocks E_v drawn in binary64 (the fp64 Gumbel option) of tokens 0..n-1."""
+    out = np.empty(n, dtype=np.float64)
+    lib().spec_verify_ref_race_clocks64(seed, j, ireq, n, _p(out))
+    return out
+
+
+def log64(x: float) -> float:
+    return lib().spec_verify_ref_log64(x)
+
+
+def log64_n(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty_like(x)
+    lib().spec_verify_ref_log64_n(_p(x), _p(out), x.size)
+    return out
+
+
+def uniform64(hi: int, lo: int) -> float:
+    """52-bit uniform of the binary64 clocks from two Philox words."""
+    return lib().spec_verify_ref_uniform64(hi, lo)
 
 
 def synthetic_rates(mean_length: float, num_spec: int) -> np.ndarray:
@@ -308,6 +339,7 @@ def run(batch, *, max_spec_len: int | None = None, req_index_base: int = 0, u_ov
         opts.counts_rows = int(np.asarray(batch.output_bin_counts).shape[0])
     opts.top_k = _opt("top_k", np.int32)
     opts.top_p = _opt("top_p", np.float32)
+    opts.fp64_gumbel = int(bool(getattr(batch, "fp64_gumbel", False)))
     out["row_select_margin"] = np.empty(max(R, 1), dtype=np.float64)
     opts.row_select_margin = out["row_select_margin"].ctypes.data
     rc = lib().spec_verify_ref_run(

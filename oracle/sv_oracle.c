@@ -178,6 +178,96 @@ float spec_verify_ref_race_clock(uint64_t seed, uint32_t j, uint32_t ireq, int32
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Race clocks drawn in binary64 ([spec-in-vllm] 7.3: use_fp64_gumbel, the race noise      */
+/* generated in double precision). Same layout idea as the binary32 clocks, 52-bit          */
+/* uniforms from two Philox words each, a separate counter range (word 3 = 32 .. 64).      */
+/* ------------------------------------------------------------------------------------ */
+#define REF_CLOCK_HEAD64 32u /* counter word 3 of a group's binary64 head call; slots use 33..64 */
+
+static inline double bits_d(uint64_t b) { double d; memcpy(&d, &b, 8); return d; }
+static inline uint64_t d_bits(double d) { uint64_t b; memcpy(&b, &d, 8); return b; }
+
+/* Uniform in (0,1) from two Philox words: the top 52 bits of (hi, lo), centred in their cell,
+ * U = (m + 1/2) / 2^52 with m = hi * 2^20 + (lo >> 12). m + 1/2 has 53 significant bits, so
+ * every step is exact in binary64; U lies in [2^-53, 1 - 2^-53]. */
+double spec_verify_ref_uniform64(uint32_t hi, uint32_t lo)
+{
+    const uint64_t m = ((uint64_t)hi << 20) | (uint64_t)(lo >> 12);
+    return ((double)m + 0.5) * 0x1p-52;
+}
+
+#define REF_LN2_HI64 0x1.62e42fefa3800p-1  /* ln 2 rounded to 42 significant bits: k ln2_hi exact */
+#define REF_LN2_LO64 0x1.ef35793c76730p-45 /* ln 2 - REF_LN2_HI64, rounded to binary64 */
+
+/* binary64 log for x > 0, the same method as the binary32 log: x = 2^k f with f in
+ * [sqrt(1/2), sqrt(2)), ln f = 2 atanh(s), s = (f - 1) / (f + 1), |s| < 0.1716, summed as
+ * 2s + s z P(z), z = s^2, P(z) = 2/3 + z (2/5 + z (... + z 2/19)) (the terms 2 s^(2n+1)/(2n+1)
+ * up to n = 9; the first one left out, 2 s^21 / 21, is below 0.15 ulp of the result); ln x =
+ * k ln 2 + ln f with the two-part ln 2 above. Subnormals are scaled by 2^54 first. 0 -> -inf,
+ * negative or NaN -> NaN, +inf -> +inf. */
+double spec_verify_ref_log64(double x)
+{
+    if (x != x || x < 0.0) return NAN;
+    if (x == 0.0) return -INFINITY;
+    if (x == INFINITY) return INFINITY;
+    int k = 0;
+    uint64_t b = d_bits(x);
+    if (b < 0x0010000000000000ull) {
+        b = d_bits(x * 0x1p+54);
+        k = -54;
+    }
+    k += (int)(b >> 52) - 1023;
+    uint64_t fb = (b & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull;
+    if (fb > 0x3FF6A09E667F3BCCull) { /* f > sqrt(2) (the largest double below it is ...BCC) */
+        fb -= 0x0010000000000000ull;
+        k += 1;
+    }
+    const double f = bits_d(fb);
+    const double g = f - 1.0;
+    const double s = g / (g + 2.0);
+    const double z = s * s;
+    double P = fma(z, 0x1.af286bca1af28p-4, 0x1.e1e1e1e1e1e1ep-4); /* 2/19, 2/17 */
+    P = fma(z, P, 0x1.1111111111111p-3);                          /* 2/15 */
+    P = fma(z, P, 0x1.3b13b13b13b14p-3);                          /* 2/13 */
+    P = fma(z, P, 0x1.745d1745d1746p-3);                          /* 2/11 */
+    P = fma(z, P, 0x1.c71c71c71c71cp-3);                          /* 2/9 */
+    P = fma(z, P, 0x1.2492492492492p-2);                          /* 2/7 */
+    P = fma(z, P, 0x1.999999999999ap-2);                          /* 2/5 */
+    P = fma(z, P, 0x1.5555555555555p-1);                          /* 2/3 */
+    const double R = z * P;
+    const double lnf = fma(s, R, s + s);
+    const double kf = (double)k;
+    return fma(kf, REF_LN2_HI64, fma(kf, REF_LN2_LO64, lnf));
+}
+
+/* Race clock of token v at position j of request ireq, drawn in binary64: group g = v >> 6,
+ * slot s = v & 63; counter (g, j, ireq, 32) gives W = uniform64(word 0, word 1) and the slot
+ * a = word 2 & 63 holding the group's smallest clock E_min = -log(W) / 64; slot s != a has
+ * clock E_min + (-log U_s), U_s = uniform64 of words (0, 1) (s even) or (2, 3) (s odd) of
+ * counter (g, j, ireq, 33 + s / 2). By the memoryless property the 64 clocks are i.i.d.
+ * Exp(1), as in binary32, with 52-bit instead of 23-bit uniforms (the largest clock is
+ * 53 ln 2 = 36.7 instead of 24 ln 2 = 16.6). */
+double spec_verify_ref_race_clock64(uint64_t seed, uint32_t j, uint32_t ireq, int32_t v)
+{
+    const uint32_t g = (uint32_t)v >> 6;
+    const uint32_t slot = (uint32_t)v & 63u;
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t ctr[4] = {g, j, ireq, REF_CLOCK_HEAD64};
+    uint32_t head[4];
+    spec_verify_ref_philox(ctr, key, head);
+    const double W = spec_verify_ref_uniform64(head[0], head[1]);
+    const uint32_t a = head[2] & 63u;
+    const double emin = -spec_verify_ref_log64(W) * 0x1p-6; /* exact scaling */
+    if (slot == a) return emin;
+    ctr[3] = REF_CLOCK_HEAD64 + 1u + slot / 2u;
+    uint32_t words[4];
+    spec_verify_ref_philox(ctr, key, words);
+    const int h = (slot & 1u) ? 2 : 0;
+    const double U = spec_verify_ref_uniform64(words[h], words[h + 1]);
+    return emin + (-spec_verify_ref_log64(U));
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* The verification step.                                                                */
 /* ------------------------------------------------------------------------------------ */
 enum { REF_OK = 0, REF_EINVAL = -1, REF_EBATCH = 1 };
@@ -198,7 +288,10 @@ enum { REF_RACE_NONE = 0, REF_RACE_RESIDUAL = 1, REF_RACE_EXCLUDE = 2, REF_RACE_
  *       [0, counts_rows): no penalty for that request.
  *   top_k [num_reqs] int32, top_p [num_reqs] binary32, each or NULL: sampling constraints of
  *       sampling requests (see select_row). top_k == 1 makes a request greedy.
- *   row_select_margin [rows] (output, NULL to skip): the top-p decision margin of each row. */
+ *   row_select_margin [rows] (output, NULL to skip): the top-p decision margin of each row.
+ *   fp64_gumbel: nonzero draws every race's clocks in binary64 (spec_verify_ref_race_clock64)
+ *       and compares its keys w_v / E_v as binary64 quotients ([spec-in-vllm] 7.3
+ *       use_fp64_gumbel); the acceptance uniforms are unchanged. */
 typedef struct {
     const float *synthetic_rates;
     int32_t num_synthetic_rates;
@@ -210,6 +303,7 @@ typedef struct {
     const int32_t *top_k;
     const float *top_p;
     double *row_select_margin;
+    int32_t fp64_gumbel;
 } ref_options_t;
 
 /* Conditional acceptance probability of position j given that positions 0..j-1 were
@@ -371,7 +465,7 @@ static void select_row(const float *x, int V, int top_k, float top_p, row_stats_
 
 typedef struct {
     int32_t idx;   /* winner, or -1 when no candidate */
-    float key;     /* winner's key */
+    double key;    /* winner's key (a binary32 value unless the clocks are binary64) */
     double gap;    /* winner's key minus the runner-up's (+inf with fewer than two) */
     int64_t ncand; /* number of candidates */
 } race_t;
@@ -379,7 +473,7 @@ typedef struct {
 /* Offer candidate v (offered in increasing v): the larger key wins, and an equal key at a
  * higher index loses to the earlier one, so the winner is the lowest index among the largest
  * keys. `second` tracks the runner-up key for the decision margin. */
-static inline void race_offer(race_t *r, float key, int32_t v, float *second)
+static inline void race_offer(race_t *r, double key, int32_t v, double *second)
 {
     r->ncand++;
     if (r->idx < 0) {
@@ -404,12 +498,14 @@ static inline void race_offer(race_t *r, float key, int32_t v, float *second)
  *               (the rejected draft token when there are no draft probabilities).
  *   q != NULL : residual weights rr_v = fma(-S, q_v, t_v) = S (p_v - q_v) rounded once,
  *               candidates rr_v > 0 ([spec-notes] residual distribution max(0, p - q)).
- * The decision margin is the winner's key over the runner-up's, as log(key1) - log(key2).   */
+ * The decision margin is the winner's key over the runner-up's, as log(key1) - log(key2).
+ * fp64: the clocks are binary64 (spec_verify_ref_race_clock64) and the key is the binary64
+ * quotient (double) w_v / E_v.                                                              */
 static race_t race_row(const float *x, int V, float m, float tau, float S_f, const float *q,
-                       int32_t exclude, uint64_t seed, uint32_t j, uint32_t ireq)
+                       int32_t exclude, uint64_t seed, uint32_t j, uint32_t ireq, int fp64)
 {
     race_t r = {-1, -INFINITY, INFINITY, 0};
-    float second = -INFINITY;
+    double second = -INFINITY;
     for (int v = 0; v < V; ++v) {
         if (v == exclude || !(x[v] >= tau)) continue; /* only kept tokens take part */
         float t = spec_verify_ref_exp(x[v] - m);
@@ -421,12 +517,17 @@ static race_t race_row(const float *x, int V, float m, float tau, float S_f, con
         } else {
             w = t;
         }
-        float E = spec_verify_ref_race_clock(seed, j, ireq, v);
-        float key = w / E;
+        double key;
+        if (fp64) {
+            key = (double)w / spec_verify_ref_race_clock64(seed, j, ireq, v);
+        } else {
+            const float E = spec_verify_ref_race_clock(seed, j, ireq, v);
+            key = (double)(w / E); /* the binary32 quotient */
+        }
         race_offer(&r, key, v, &second);
     }
     if (r.idx >= 0 && r.ncand >= 2)
-        r.gap = second > 0.0f ? log((double)r.key) - log((double)second) : INFINITY;
+        r.gap = second > 0.0 ? log(r.key) - log(second) : INFINITY;
     return r;
 }
 
@@ -526,6 +627,7 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             continue;
         }
         const int synthetic = opts && opts->synthetic_rates;
+        const int fp64 = opts && opts->fp64_gumbel;
 
         /* [MTP-eagle] _rejection_sample_kernel: walk the draft positions, stop at the
          * first rejection; [spec-notes] 8.3 greedy and stochastic rules. */
@@ -582,7 +684,7 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             /* synthetic mode has no draft distribution: the token at j* is the target's own
              * draw from p ([MTP-eagle]: the target token is written whether accepted or not) */
             race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
-                                st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                                st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq, fp64);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_TARGET;
@@ -590,20 +692,20 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
             /* [spec-notes] bonus token: sampled from p at the position after the last draft;
              * K = 0 is the plain Gumbel-max sample of a non-speculative request. */
             race_t r = race_row(xbuf + (size_t)K * V, V, st[K].m, st[K].tau, st[K].Sk_f, NULL, -1,
-                                seed, (uint32_t)K, ireq);
+                                seed, (uint32_t)K, ireq, fp64);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_BONUS;
         } else if (draft_probs) {
             const float *q = draft_probs + (size_t)(q0 + jstar) * V;
             race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
-                                st[jstar].Sk_f, q, -1, seed, (uint32_t)jstar, ireq);
+                                st[jstar].Sk_f, q, -1, seed, (uint32_t)jstar, ireq, fp64);
             kind = REF_RACE_RESIDUAL;
             if (r.idx < 0) {
                 /* nothing left of max(0, p - q) after rounding: sample from p itself so that
                  * the emitted token is still a target-side draw */
                 r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
-                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq, fp64);
                 kind = REF_RACE_FALLBACK;
             }
             token = r.idx;
@@ -613,10 +715,10 @@ int spec_verify_ref_run(const void *logits, int logits_bf16, int vocab_size,
              * removed; an out-of-range d removes nothing. */
             const int32_t d = draft_ids[q0 + jstar];
             race_t r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
-                                st[jstar].Sk_f, NULL, d, seed, (uint32_t)jstar, ireq);
+                                st[jstar].Sk_f, NULL, d, seed, (uint32_t)jstar, ireq, fp64);
             if (r.idx < 0) /* V == 1 and d == 0: nothing else to draw */
                 r = race_row(xbuf + (size_t)jstar * V, V, st[jstar].m, st[jstar].tau,
-                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq);
+                             st[jstar].Sk_f, NULL, -1, seed, (uint32_t)jstar, ireq, fp64);
             token = r.idx;
             gap = r.gap;
             kind = REF_RACE_EXCLUDE;
@@ -726,6 +828,18 @@ void spec_verify_ref_log_n(const float *in, float *out, int64_t n)
 void spec_verify_ref_race_clocks(uint64_t seed, uint32_t j, uint32_t ireq, int32_t n, float *out)
 {
     for (int32_t v = 0; v < n; ++v) out[v] = spec_verify_ref_race_clock(seed, j, ireq, v);
+}
+
+/* The same in binary64. */
+void spec_verify_ref_race_clocks64(uint64_t seed, uint32_t j, uint32_t ireq, int32_t n, double *out)
+{
+    for (int32_t v = 0; v < n; ++v) out[v] = spec_verify_ref_race_clock64(seed, j, ireq, v);
+}
+
+/* binary64 log over an array (for the accuracy checks). */
+void spec_verify_ref_log64_n(const double *in, double *out, int64_t n)
+{
+    for (int64_t k = 0; k < n; ++k) out[k] = spec_verify_ref_log64(in[k]);
 }
 
 /* ------------------------------------------------------------------------------------ */

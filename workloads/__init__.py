@@ -130,6 +130,8 @@ class Batch:
     counts_row: np.ndarray | None = None
     top_k: np.ndarray | None = None
     top_p: np.ndarray | None = None
+    # race noise drawn in binary64 (the fp64 Gumbel option, a per-call verifier setting)
+    fp64_gumbel: bool = False
 
     @property
     def num_reqs(self) -> int:
