@@ -217,9 +217,64 @@ def recorded_traffic(summary: str):
 # ---------------------------------------------------------------------------------------------
 # CPU oracle timing
 # ---------------------------------------------------------------------------------------------
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo", encoding="utf-8") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def request_slice(b, lo: int, hi: int):
+    """Requests [lo, hi) of a batch as a batch of their own (verified with req_index_base = lo,
+    which keys every draw as in the whole batch)."""
+    import numpy as np
+    import workloads
+
+    cu = b.cu_num_draft
+    r0, r1 = int(cu[lo]) + lo, int(cu[hi]) + hi
+    q0, q1 = int(cu[lo]), int(cu[hi])
+    return workloads.Batch(
+        name=f"{b.name}[{lo}:{hi}]", logits=b.logits[r0:r1], logits_dtype=b.logits_dtype,
+        vocab_size=b.vocab_size, draft_ids=b.draft_ids[q0:q1],
+        draft_probs=None if b.draft_probs is None else b.draft_probs[q0:q1],
+        cu_num_draft=(cu[lo:hi + 1] - cu[lo]).astype(np.int32),
+        temperature=b.temperature[lo:hi], is_greedy=b.is_greedy[lo:hi], seed=b.seed,
+        draft_logits=None if b.draft_logits is None else b.draft_logits[q0:q1],
+        synthetic_rates=b.synthetic_rates,
+        frequency_penalty=None if b.frequency_penalty is None else b.frequency_penalty[lo:hi],
+        output_bin_counts=b.output_bin_counts,
+        counts_row=(np.arange(lo, hi, dtype=np.int32) if b.counts_row is None else b.counts_row[lo:hi])
+        if b.frequency_penalty is not None else None,
+        top_k=None if b.top_k is None else b.top_k[lo:hi],
+        top_p=None if b.top_p is None else b.top_p[lo:hi])
+
+
 def time_oracle(args, seconds: float):
-    """Time the oracle (as it stands, single-threaded) on the first requests of the workload,
-    enough of them for about `seconds` of CPU work. Returns (positions/s, description)."""
+    """Time the oracle (as it stands: single-threaded C) on the first requests of the workload,
+    enough of them for about `seconds` of CPU work on one core: once on one thread, then split
+    by requests over every host core (one thread per core, each running the unchanged oracle
+    on its own requests; ctypes releases the interpreter lock during the call)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
     one = load_workload(args, num_reqs=2)
@@ -231,9 +286,22 @@ def time_oracle(args, seconds: float):
     t = time.perf_counter()
     oracle.run(b)
     dt = time.perf_counter() - t
-    desc = (f"oracle (single thread) on the first {b.num_reqs} requests of the workload "
-            f"({b.num_draft_tokens} draft positions, {b.num_rows} rows), {dt:.1f} s")
-    return b.num_draft_tokens / dt, desc, b.num_rows / dt
+    cores = host_cores()
+    n = b.num_reqs
+    parts = [(n * k // cores, n * (k + 1) // cores) for k in range(cores)]
+    subs = [(lo, request_slice(b, lo, hi)) for lo, hi in parts if hi > lo]
+    with ThreadPoolExecutor(max_workers=len(subs)) as pool:
+        t = time.perf_counter()
+        list(pool.map(lambda s: oracle.run(s[1], req_index_base=s[0]), subs))
+        dtm = time.perf_counter() - t
+    model = cpu_model()
+    desc = (f"oracle (plain C, single-threaded code) on the first {b.num_reqs} requests of the "
+            f"workload ({b.num_draft_tokens} draft positions, {b.num_rows} rows): {dt:.1f} s on "
+            f"1 core; {dtm:.2f} s split by requests over {len(subs)} threads on {cores} cores; "
+            f"CPU {model}")
+    return {"value": b.num_draft_tokens / dt, "rows_per_s": b.num_rows / dt,
+            "value_multi": b.num_draft_tokens / dtm, "cores_multi": len(subs),
+            "cpu_model": model, "sample": desc}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -349,6 +417,19 @@ def run_ours(args, world, rank, local):
     sampler = ClockSampler(gpu_index_for(local)) if rank == 0 else None
     if sampler:
         time.sleep(0.3)
+
+    def load_for(seconds):
+        """The same step back to back (untimed), so that the clock samples around the timed
+        region see the GPU under the timed load: the timed region itself (K steps of about a
+        tenth of a millisecond) is much shorter than the sampling period."""
+        t = time.perf_counter()
+        while time.perf_counter() - t < seconds:
+            for _ in range(50):
+                step()
+            torch.cuda.synchronize()
+        return t
+
+    t_load0 = load_for(0.3) if sampler else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist:
         dist.barrier()
@@ -368,6 +449,8 @@ def run_ours(args, world, rank, local):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
     if sampler:
+        load_for(0.3)
+        t_load1 = time.perf_counter()
         time.sleep(0.1)
         sampler.stop()
     ms_per_step = elapsed_ms / args.steps
@@ -431,6 +514,8 @@ def run_ours(args, world, rank, local):
                "timing": "host wall clock around run_host (copies + kernels + stream sync)",
                "in_place": "draft_probs (page-locked host memory) read over the host link by the "
                            "verify kernel, only the entries it needs" if h_q is not None else None}
+        e2e["host_link"] = host_link_ceiling(h_logits, d_logits, ke)
+        e2e["link_frac"] = (h2d / (te / ke)) / 1e9 / e2e["host_link"]["h2d_gbs"]
         if not np.array_equal(h_out[0].numpy(), outs[0].cpu().numpy()):
             raise RuntimeError("host-buffer path disagrees with the device path")
 
@@ -459,11 +544,31 @@ def run_ours(args, world, rank, local):
     traffic, traffic_src = (recorded_traffic("stats_kernel_workload3_draft_logits.md" if d_dl is not None
                                              else "stats_kernel_workload3.md")
                             if plain and args.workload == 3 else (None, "no ncu summary for this mode"))
+    b_full, b_alg = step_bytes(b, outs[1].cpu().numpy())
+    step_s = ms_per_step / 1e3
+    step_roofline = {
+        "bytes_full": b_full, "bytes_alg": b_alg,
+        "gbs_full": b_full / step_s / 1e9, "gbs_alg": b_alg / step_s / 1e9,
+        "peak_nominal_gbs": 8000.0, "frac_alg_of_nominal": b_alg / step_s / 1e9 / 8000.0,
+        "frac_full_of_nominal": b_full / step_s / 1e9 / 8000.0,
+        "peak_measured_gbs": peak, "frac_alg_of_measured": b_alg / step_s / 1e9 / peak,
+        "note": "whole step (every kernel) against the method's bytes: logits once, plus the "
+                "draft rows the method needs (alg) or every sampling request's draft rows (full)"}
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        v, desc, _ = time_oracle(args, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
-    clocks = sampler.summary(t0, t1) if sampler else None
+        o = time_oracle(args, args.cpu_seconds)
+        cpu = {"value": o["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": o["sample"], "value_multi": o["value_multi"],
+               "cores_multi": o["cores_multi"], "cpu_model": o["cpu_model"]}
+    clocks = None
+    if sampler:
+        clocks = sampler.summary(t0, t1)
+        if clocks.get("note", "").startswith("timed region shorter"):
+            # the window of back-to-back steps around the timed region (0.3 s on each side)
+            clocks = sampler.summary(t_load0, t_load1)
+            clocks["note"] = ("samples while the timed step ran back to back for 0.3 s before "
+                              "and after the timed region (which is shorter than the 50 ms "
+                              "sampling period), the timed region included")
     cfg = workload_config(b)
     cfg.update({"l2": "inputs larger than L2 (no flush between steps)", "parallelism":
                 f"replicas x{world}" if world > 1 else "single GPU",
@@ -475,7 +580,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": cfg,
         "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": ("whole sharded step (every shard's kernels, the bytes of "
+        "roofline": {"bound": "hbm", "scope": "per kernel (the dominant one)",
+                     "kernel": ("whole sharded step (every shard's kernels, the bytes of "
                                                 "the statistics passes)") if sharded else
                      "sv_stats_kernel (row statistics: reads every logit once, "
                      "writes one maximum per 64-element line"
@@ -484,6 +590,7 @@ def run_ours(args, world, rank, local):
                      "peak_kind": f"{peak_kind} (copy bandwidth, MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes_per_launch": stats_bytes},
+        "step_roofline": step_roofline,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "kernel_ms": {**kavg, "profiled_calls": calls} if kavg else None,
@@ -497,6 +604,48 @@ def run_ours(args, world, rank, local):
     ctx.close()
     if dist:
         dist.destroy_process_group()
+
+
+def host_link_ceiling(h_src, d_dst, steps):
+    """The plain host-to-device copy rate of the same bytes: one cudaMemcpyAsync per step of a
+    page-locked host tensor into device memory (torch's non-blocking copy), timed with CUDA
+    events on the current stream. What the e2e step's input copies could reach at best."""
+    import torch
+
+    for _ in range(2):
+        d_dst.copy_(h_src, non_blocking=True)
+    torch.cuda.synchronize()
+    a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        d_dst.copy_(h_src, non_blocking=True)
+    z.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(z) / steps
+    nbytes = h_src.numel() * h_src.element_size()
+    return {"h2d_gbs": nbytes / (ms / 1e3) / 1e9, "bytes": int(nbytes), "ms_per_copy": ms,
+            "how": "one cudaMemcpyAsync H2D of the logits from page-locked memory per step, "
+                   "CUDA events"}
+
+
+def step_bytes(b, num_sampled):
+    """Algorithmic bytes of one step (the method's reads): every logit row once, plus
+    (full) every sampling request's draft rows once, or (alg) only the draft rows the method
+    needs: the rejected row of each sampling request in draft-probability mode (its residual),
+    every draft row in the draft-logits mode (q needs each row's S_d). Draft ids, outputs and
+    the small per-request arrays are left out (under 0.01 %)."""
+    import numpy as np
+
+    full = b.bytes_full()
+    alg = b.num_rows * b.vocab_size * b.elem_bytes
+    k = np.diff(b.cu_num_draft)
+    greedy = (b.is_greedy != 0) | ~(b.temperature > 0)
+    if b.draft_logits is not None:
+        alg = full
+    elif b.draft_probs is not None and b.synthetic_rates is None:
+        rejected = (~greedy) & (np.asarray(num_sampled) - 1 < k)
+        alg += int(rejected.sum()) * b.vocab_size * 4
+    return full, alg
 
 
 def e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist):

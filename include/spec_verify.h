@@ -48,8 +48,14 @@
  *   - Acceptance: 0 <= d < V and q(d) > 0 and p(d) / q(d) >= u (binary32), q(d) = 1 without
  *     draft probabilities. An out-of-range draft id is rejected, not an error.
  *   - exp / log inside these decisions are fixed binary32 functions (Cody-Waite reduction
- *     with a degree-7 Taylor polynomial; atanh series on [sqrt(1/2), sqrt(2))), so decisions
- *     are reproducible bit for bit on any implementation that follows them.
+ *     with a degree-7 Taylor polynomial; atanh series on [sqrt(1/2), sqrt(2))). The one input
+ *     they take that is not fixed bit for bit is S, the sum of exponentials: it is summed with
+ *     the hardware's approximate 2^x, in an order of the kernel's choosing, and matches the
+ *     exactly summed S to about 1e-6 relative (1e-5 is the tested bound). p(d) = t_d / S and the
+ *     residual weights use it, so an acceptance whose |u - p(d)/q(d)|, or a residual race whose
+ *     two best keys, lie within that margin may be decided differently from an implementation
+ *     that sums S exactly; every other decision is reproducible bit for bit from these
+ *     definitions.
  *   - sampled[i, :] holds the accepted drafts, then the recovered or bonus token, then -1.
  *     num_sampled[i] = accepted + 1, num_rejected[i] = K_i - accepted.
  *
@@ -393,12 +399,16 @@ int spec_verify_launches_per_run(void);
  * it, held until the process exits).
  *   Limits: vocab_size <= SV_NOALLOC_MAX_VOCAB, num_reqs <= SV_NOALLOC_MAX_REQS, and
  *   num_draft_tokens + num_reqs <= SV_NOALLOC_MAX_ROWS; larger batches return SV_ECAPACITY.
- * It runs on the current device. Its first call on a device looks up the array's device
- * address (once per device); make that first call before any stream capture. All calls on a
- * device share the array, so calls that overlap on the GPU (different streams, or different
- * host threads) race with each other and must be serialised by the caller. The device error
- * word of spec_verify_last_error is not available here: an inconsistent cu_num_draft shows
- * as num_sampled = num_rejected = 0 and a row of -1 for every request.
+ * It runs on the current device. Its first call on a device (or the first call of
+ * spec_verify_noalloc_last_error there) sets the device up, once: it checks that the device
+ * is an sm_103 part, looks up the array's device address and sets the kernels' shared-memory
+ * limits; make that first call before any stream capture. Later calls on the device make no
+ * CUDA runtime query besides the launches. All calls on a device share the array, so calls
+ * that overlap on the GPU (different streams, or different host threads) race with each other
+ * and must be serialised by the caller. An inconsistent cu_num_draft makes every request emit
+ * num_sampled = num_rejected = 0 and a row of -1 and sets SV_ERR_BATCH in the array's error
+ * word, which spec_verify_noalloc_last_error reads and clears. The frequency penalty, top-k /
+ * top-p, draft logits and synthetic acceptance are not offered here.
  */
 #define SV_NOALLOC_MAX_REQS 1024
 #define SV_NOALLOC_MAX_ROWS 8192
@@ -411,6 +421,14 @@ int spec_verify_run_noalloc(const void *logits, int logits_dtype, int vocab_size
                             int32_t *sampled, int32_t *num_sampled, int32_t *num_rejected,
                             float *opt_row_max, float *opt_row_sumexp, int32_t *opt_row_argmax,
                             void *cuda_stream);
+
+/*
+ * Read and clear the error word of spec_verify_run_noalloc on the current device (SV_ERR_*
+ * bits of every call since the last read), into *err_word. Like spec_verify_last_error it
+ * waits for the device (synchronises it), so call it outside any stream capture. Allocates
+ * nothing. Has no counterpart on the pages.
+ */
+int spec_verify_noalloc_last_error(uint32_t *err_word);
 
 /* Release the context and its device memory. NULL is a no-op. */
 void spec_verify_free(spec_verify_ctx *ctx);

@@ -112,11 +112,13 @@ def lib():
     if _lib is not None:
         return _lib
     if _stale():
+        # a library older than its sources is never loaded: a failed rebuild raises, so that a
+        # compile error cannot leave the previous binary running (and measured) in its place
         try:
             build()
         except (OSError, RuntimeError) as e:
-            if not os.path.exists(LIB_PATH):
-                raise RuntimeError("libspecverify.so is missing and could not be built: " + str(e))
+            raise RuntimeError("libspecverify.so is out of date and could not be rebuilt: "
+                               + str(e)) from e
     L = ctypes.CDLL(LIB_PATH)
     vp, i32, u32, u64, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint64, ctypes.c_int64
     L.spec_verify_init.argtypes = [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32]
@@ -134,6 +136,7 @@ def lib():
                                        vp, vp]
     L.spec_verify_run_noalloc.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp, u64, u32, i32, i32,
                                           i32, vp, vp, vp, vp, vp, vp, vp]
+    L.spec_verify_noalloc_last_error.argtypes = [ctypes.POINTER(u32)]
     L.spec_verify_reserve_host_io.argtypes = [vp]
     L.spec_verify_last_error.argtypes = [vp, ctypes.POINTER(u32)]
     L.spec_verify_set_profiling.argtypes = [vp, i32]
@@ -147,7 +150,7 @@ def lib():
     for f in ("spec_verify_init", "spec_verify_run", "spec_verify_run_draft_logits",
               "spec_verify_run_batch", "spec_verify_set_synthetic", "spec_verify_synthetic_rates",
               "spec_verify_shard_stats", "spec_verify_shard_race", "spec_verify_shard_finish",
-              "spec_verify_run_host", "spec_verify_run_noalloc",
+              "spec_verify_run_host", "spec_verify_run_noalloc", "spec_verify_noalloc_last_error",
               "spec_verify_reserve_host_io", "spec_verify_last_error", "spec_verify_set_profiling",
               "spec_verify_get_profile", "spec_verify_set_chunks", "spec_verify_launches_per_run"):
         getattr(L, f).restype = i32
@@ -316,6 +319,14 @@ def spec_verify_run_noalloc(logits, logits_dtype, vocab_size, draft_ids, draft_p
            "spec_verify_run_noalloc")
 
 
+def spec_verify_noalloc_last_error() -> int:
+    """Read and clear the error word of spec_verify_run_noalloc on the current device (waits
+    for the device)."""
+    w = ctypes.c_uint32()
+    _check(lib().spec_verify_noalloc_last_error(ctypes.byref(w)), "spec_verify_noalloc_last_error")
+    return w.value
+
+
 def spec_verify_reserve_host_io(ctx) -> None:
     _check(lib().spec_verify_reserve_host_io(ctx), "spec_verify_reserve_host_io")
 
@@ -381,7 +392,7 @@ class SpecVerify:
             *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
             row_stats: bool = False, stream=None, draft_logits=None, partial_prefill=None,
             frequency_penalty=None, output_bin_counts=None, counts_row=None, top_k=None,
-            top_p=None):
+            top_p=None, stats_out=None):
         """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
         and, with row_stats=True, also (row_max, row_sumexp, row_argmax).
 
@@ -391,7 +402,8 @@ class SpecVerify:
         no token. frequency_penalty ([num_reqs] float32) with output_bin_counts ([rows, V]
         int32) and counts_row ([num_reqs] int32, optional): the frequency penalty. top_k
         ([num_reqs] int32), top_p ([num_reqs] float32): sampling constraints. Any of these
-        goes through spec_verify_run_batch."""
+        goes through spec_verify_run_batch. out / stats_out: caller-provided output tensors
+        (sampled, num_sampled, num_rejected) / (row_max, row_sumexp, row_argmax)."""
         import torch
         num_reqs = cu_num_draft.numel() - 1
         nd = draft_ids.numel()
@@ -410,7 +422,9 @@ class SpecVerify:
                    torch.empty(num_reqs, dtype=torch.int32, device=dev),
                    torch.empty(num_reqs, dtype=torch.int32, device=dev))
         stats = (None, None, None)
-        if row_stats:
+        if row_stats and stats_out is not None:
+            stats = tuple(stats_out)
+        elif row_stats:
             R = nd + num_reqs
             stats = (torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.float32, device=dev),

@@ -27,6 +27,7 @@
 // exact keys decide, so the winner is the argmax over all tokens, as a full scan would find it;
 // only the line maxima of the raced row and the logits and q entries of evaluated groups are read.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <climits>
@@ -183,6 +184,8 @@ struct PenTable {
     const int32_t *counts;      // [counts_rows, V] output token counts
     const int32_t *counts_row;  // [n] counts row of each request, or nullptr (row i)
     int counts_rows;
+    int nd;                     // draft tokens of the batch (length of draft_ids)
+    int kmax;                   // most drafts of one request
 };
 
 // The penalty of one logit row: y_v = fma(-f, c_v, l_v) where f != 0 and c_v != 0, else l_v;
@@ -196,12 +199,16 @@ struct PenRow {
 };
 
 // Request i, position j (drafts from q0). A counts row outside [0, counts_rows) gives no penalty
-// (and is reported by the verify kernel).
+// (and is reported by the verify kernel). The statistics and selection kernels run before the
+// verify kernel has checked cu_num_draft, so q0 and j come from unchecked device data there:
+// a position whose earlier drafts would lie outside draft_ids[0, nd) gets no penalty either
+// (such a batch emits nothing, by the verify kernel's check).
 __device__ __forceinline__ PenRow pen_row(const PenTable &pt, const int32_t *draft_ids, int i,
                                           int q0, int j, int V)
 {
     PenRow r{0.0f, nullptr, nullptr, 0};
     if (!pt.f) return r;
+    if (q0 < 0 || q0 > pt.nd || j < 0 || j > pt.kmax || j > pt.nd - q0) return r;
     const int crow = pt.counts_row ? __ldg(pt.counts_row + i) : i;
     if (crow < 0 || crow >= pt.counts_rows) return r;
     r.f = __ldg(pt.f + i);
@@ -1022,7 +1029,10 @@ __device__ __forceinline__ RowLines row_lines(long long row, int V, int base_off
 
 // lm[k] = largest raw logit of the row on line L0 + k (the row's own elements only). The lines
 // inside the row come from `lines` (written by the statistics kernel) or, without it, from
-// coalesced 16-byte loads of the row; a partial first / last line is read by warp 0 / 1.
+// coalesced 16-byte loads of the row; a partial first / last line is read by warp 0 / 1. The
+// loads without `lines` take the raw logits, which bound a penalised row only for penalties of
+// one sign: launch_all therefore refuses a penalty without a line buffer (the static-scratch
+// entry point, the one caller without it, takes no penalty).
 template <typename T, bool kPen>
 __device__ void row_line_max(const T *__restrict__ rp, int V, const RowLines &rl,
                              const T *__restrict__ lines, float *__restrict__ lm,
@@ -2524,6 +2534,15 @@ struct ProfSlot {
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// An NVTX range named after the entry point around each call, for profilers that attach an NVTX
+// tool (Nsight Systems, Nsight Compute's --nvtx filters); without one it is a call into a no-op.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 size_t verify_smem_bytes(int V, int kmax) { return verify_layout(V, kmax).total; }
 
 }  // namespace
@@ -2702,9 +2721,11 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
     const long long chunk1 = stats_chunk_for(ctx, total + total_d);
     const RequestTable rq{cu, b.temperature, b.is_greedy, b.top_k, num_reqs};
-    const PenTable pen{b.frequency_penalty, b.output_bin_counts, b.counts_row, b.counts_rows};
+    const PenTable pen{b.frequency_penalty, b.output_bin_counts, b.counts_row, b.counts_rows, nd,
+                       kmax};
     const bool pen_on = b.frequency_penalty != nullptr;
     T *lines = static_cast<T *>(ctx->lines);
+    if (pen_on && !lines) return SV_EINVAL;  // the race's line maxima of a penalised row
     const StatsArray<T> A = stats_array<T>(logits, total, chunk1, V, 0, ctx->statpart, lines);
     const StatsArray<T> D = stats_array<T>(dl, total_d, chunk1, V, 1, ctx->dpart, nullptr);
     const int base_off = A.base_off;
@@ -2931,6 +2952,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
 int spec_verify_run_batch(spec_verify_ctx *ctx, const spec_verify_batch *batch,
                           const spec_verify_outputs *out, void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_run_batch");
     if (!ctx || !batch || !out) return SV_EINVAL;
     const int rc = check_run_args(ctx, *batch, *out);
     if (rc != SV_OK || batch->num_reqs == 0) return rc;
@@ -2984,6 +3006,7 @@ int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int 
                             int max_spec_len_this_batch, spec_verify_shard_stat *out,
                             void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_shard_stats");
     if (!ctx || !out || v0 < 0 || v0 % kGroup != 0) return SV_EINVAL;
     const spec_verify_batch b = plain_batch(logits_shard, draft_ids, draft_probs_shard, nullptr,
                                             cu_num_draft, temperature, is_greedy, 0, 0, num_reqs,
@@ -3024,6 +3047,7 @@ int spec_verify_shard_race(spec_verify_ctx *ctx, const void *logits_shard, int v
                            int num_reqs, int num_draft_tokens, int max_spec_len_this_batch,
                            spec_verify_shard_key *out, void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_shard_race");
     if (!ctx || !out || !all_stats || world < 1 || v0 < 0 || v0 % kGroup != 0 ||
         vocab_size < v0 + ctx->V)
         return SV_EINVAL;
@@ -3069,6 +3093,7 @@ int spec_verify_shard_finish(spec_verify_ctx *ctx, const spec_verify_shard_key *
                              int num_reqs, int max_spec_len_this_batch, int32_t *sampled,
                              int32_t *num_sampled, int32_t *num_rejected, void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_shard_finish");
     if (!ctx || world < 1 || num_reqs < 0 || max_spec_len_this_batch < 0) return SV_EINVAL;
     if (num_reqs == 0) return SV_OK;
     if (!all_races || !cu_num_draft || !sampled || !num_sampled || !num_rejected) return SV_EINVAL;
@@ -3145,6 +3170,7 @@ int spec_verify_run_host(spec_verify_ctx *ctx, const void *logits, const int32_t
                          int max_spec_len_this_batch, int32_t *sampled, int32_t *num_sampled,
                          int32_t *num_rejected, void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_run_host");
     if (!ctx) return SV_EINVAL;
     if (!ctx->io_logits) return SV_EINVAL;
     // the device path's checks, less alignment: host arrays are staged or read in place
@@ -3304,15 +3330,28 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void *g_noalloc_base[kNoAllocMaxDevices] = {};
+struct NoAllocDevice {
+    void *base = nullptr;     // device address of g_noalloc_scratch on this device
+    size_t smem_limit = 0;    // largest dynamic shared memory of a verify CTA here
+};
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 
-// Device address of the static scratch on device `dev` (current), looked up once per device
-// (the host-side name of the array is not a device address); the kernels' shared-memory limits
-// are set at the same time.
-int noalloc_base(int dev, void **out)
+// Set-up of device `dev` (current), once per device and then cached: the device must be an
+// sm_103 part; the device address of the static scratch is looked up (the host-side name of
+// the array is not a device address); the kernels' shared-memory limits are set. Later calls
+// only read the cache, so a call on a device already set up makes no CUDA runtime query.
+int noalloc_device(int dev, NoAllocDevice *out)
 {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_base[dev]) {
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (!d.base) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return SV_EDEVICE;
+        }
+        if (major != 10 || minor != 3) return SV_EDEVICE;  // built for sm_103a only
         void *p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
@@ -3324,9 +3363,20 @@ int noalloc_base(int dev, void **out)
             cudaGetLastError();
             return SV_ECUDA;
         }
-        g_noalloc_base[dev] = p;
+        d.smem_limit = verify_smem_limit(dev);
+        d.base = p;
     }
-    *out = g_noalloc_base[dev];
+    *out = d;
+    return SV_OK;
+}
+
+// The current device, if it is one this entry point can keep state for.
+int noalloc_current(int *dev)
+{
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kNoAllocMaxDevices) {
+        cudaGetLastError();
+        return SV_EDEVICE;
+    }
     return SV_OK;
 }
 
@@ -3342,6 +3392,7 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
                                        float *opt_row_max, float *opt_row_sumexp,
                                        int32_t *opt_row_argmax, void *cuda_stream)
 {
+    const NvtxRange nvtx("spec_verify_run_noalloc");
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
     if (vocab_size <= 0 || num_reqs < 0 || num_draft_tokens < 0 || max_spec_len_this_batch < 0)
         return SV_EINVAL;
@@ -3359,19 +3410,13 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
         reinterpret_cast<uintptr_t>(draft_probs) % 16 != 0)
         return SV_EINVAL;
     int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) {
-        cudaGetLastError();
-        return SV_EDEVICE;
-    }
-    cudaDeviceProp prop;
-    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess || prop.major != 10 || prop.minor != 3)
-        return SV_EDEVICE;
-    if (verify_smem_bytes(vocab_size, max_spec_len_this_batch) > verify_smem_limit(dev))
-        return SV_ECAPACITY;
-    void *base = nullptr;
-    const int rc = noalloc_base(dev, &base);
+    int rc = noalloc_current(&dev);
     if (rc != SV_OK) return rc;
-    auto *bytes = static_cast<unsigned char *>(base);
+    NoAllocDevice nd;
+    rc = noalloc_device(dev, &nd);
+    if (rc != SV_OK) return rc;
+    if (verify_smem_bytes(vocab_size, max_spec_len_this_batch) > nd.smem_limit) return SV_ECAPACITY;
+    auto *bytes = static_cast<unsigned char *>(nd.base);
 
     // A context on the host stack whose scratch pointers are carved from the static array; the
     // fixed statistics chunk keeps every row within kNoAllocMaxSeg partials. There is no room for
@@ -3396,4 +3441,24 @@ extern "C" int spec_verify_run_noalloc(const void *logits, int logits_dtype, int
                                 opt_row_argmax};
     return logits_dtype == SV_BF16 ? launch_all<uint16_t>(&view, b, o, stream)
                                    : launch_all<float>(&view, b, o, stream);
+}
+
+extern "C" int spec_verify_noalloc_last_error(uint32_t *err_word)
+{
+    if (!err_word) return SV_EINVAL;
+    int dev = -1;
+    int rc = noalloc_current(&dev);
+    if (rc != SV_OK) return rc;
+    NoAllocDevice nd;
+    rc = noalloc_device(dev, &nd);
+    if (rc != SV_OK) return rc;
+    unsigned *word = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(nd.base) + kOffFlags) + 1;
+    unsigned w = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&w, word, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(word, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+        return SV_ECUDA;
+    *err_word = w;
+    return SV_OK;
 }

@@ -117,6 +117,63 @@ __device__ __forceinline__ float log_f32(float x)
     return __fmaf_rn(kf, 0x1.62e430p-1f, __fmaf_rn(kf, -0x1.05c610p-29f, lnf));
 }
 
+// ---------------------------------------------------------------------------------------
+// Race clocks in binary64 (the fp64 Gumbel option): the same group layout with 52-bit uniforms.
+// Counter (g, j, request, kClockHead64) gives W = uniform64(word 0, word 1) and the slot
+// a = word 2 & 63 of the group's smallest clock E_g = -log(W) / 64; slot s != a has clock
+// E_g + (-log U_s), U_s = uniform64 of words (0, 1) (even s) or (2, 3) (odd s) of counter
+// (g, j, request, kClockHead64 + 1 + s / 2).
+// ---------------------------------------------------------------------------------------
+constexpr uint32_t kClockHead64 = 32u;
+
+// U in (0,1) from two words: (m + 1/2) * 2^-52, m = hi * 2^20 + (lo >> 12); exact in binary64.
+__device__ __forceinline__ double uniform64_from_words(uint32_t hi, uint32_t lo)
+{
+    const unsigned long long m = (static_cast<unsigned long long>(hi) << 20) | (lo >> 12);
+    return __dmul_rn(__dadd_rn(__ull2double_rn(m), 0.5), 0x1p-52);
+}
+
+// binary64 log for x > 0, the binary32 log's method in double: x = 2^k f with f in
+// [sqrt(1/2), sqrt(2)), ln f = 2 atanh(s), s = (f - 1) / (f + 1), summed as 2s + s z P(z),
+// z = s^2, P(z) = 2/3 + z (2/5 + ... + z 2/19) (the series 2 s^(2n+1) / (2n+1) to n = 9; the
+// first term left out is below 0.15 ulp of the result); ln x = k ln 2 + ln f with ln 2 split
+// into a 42-bit part (k ln2_hi exact) and its binary64 remainder. Subnormals are scaled by 2^54
+// first. 0 -> -inf, negative or NaN -> NaN, +inf -> +inf.
+__device__ __forceinline__ double log_f64(double x)
+{
+    if (x != x || x < 0.0) return __longlong_as_double(0x7FF8000000000000ll);
+    if (x == 0.0) return __longlong_as_double(static_cast<long long>(0xFFF0000000000000ull));
+    if (x == __longlong_as_double(0x7FF0000000000000ll)) return x;
+    int k = 0;
+    unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(x));
+    if (b < 0x0010000000000000ull) {
+        b = static_cast<unsigned long long>(__double_as_longlong(__dmul_rn(x, 0x1p+54)));
+        k = -54;
+    }
+    k += static_cast<int>(b >> 52) - 1023;
+    unsigned long long fb = (b & 0x000FFFFFFFFFFFFFull) | 0x3FF0000000000000ull;
+    if (fb > 0x3FF6A09E667F3BCCull) {  // f > sqrt(2): halve it
+        fb -= 0x0010000000000000ull;
+        k += 1;
+    }
+    const double f = __longlong_as_double(static_cast<long long>(fb));
+    const double g = __dsub_rn(f, 1.0);
+    const double s = __ddiv_rn(g, __dadd_rn(g, 2.0));
+    const double z = __dmul_rn(s, s);
+    double P = __fma_rn(z, 0x1.af286bca1af28p-4, 0x1.e1e1e1e1e1e1ep-4);  // 2/19, 2/17
+    P = __fma_rn(z, P, 0x1.1111111111111p-3);                             // 2/15
+    P = __fma_rn(z, P, 0x1.3b13b13b13b14p-3);                             // 2/13
+    P = __fma_rn(z, P, 0x1.745d1745d1746p-3);                             // 2/11
+    P = __fma_rn(z, P, 0x1.c71c71c71c71cp-3);                             // 2/9
+    P = __fma_rn(z, P, 0x1.2492492492492p-2);                             // 2/7
+    P = __fma_rn(z, P, 0x1.999999999999ap-2);                             // 2/5
+    P = __fma_rn(z, P, 0x1.5555555555555p-1);                             // 2/3
+    const double R = __dmul_rn(z, P);
+    const double lnf = __fma_rn(s, R, __dadd_rn(s, s));
+    const double kf = static_cast<double>(k);
+    return __fma_rn(kf, 0x1.62e42fefa3800p-1, __fma_rn(kf, 0x1.ef35793c76730p-45, lnf));
+}
+
 // Fast 2^x (MUFU), for sums and for conservative screening only -- never for a decision.
 __device__ __forceinline__ float ex2_approx(float x)
 {

@@ -53,6 +53,35 @@ def to_device(batch, device="cuda:0"):
     )
 
 
+CANARY_PAD = 64            # 4-byte words of sentinel before and after every output buffer
+CANARY_WORD = -0x21524111  # 0xDEADBEEF
+
+
+def canary_buffer(shape, dtype, device):
+    """An output tensor of `shape` inside a larger buffer whose CANARY_PAD words before and
+    after it hold CANARY_WORD: (buffer, view). A kernel writing past either end of the output
+    changes a canary (compute-sanitizer is not available on the GPU machines; this catches
+    out-of-bounds stores into the neighbours of every output)."""
+    import torch
+
+    n = 1
+    for s in shape:
+        n *= s
+    buf = torch.full((n + 2 * CANARY_PAD,), CANARY_WORD, dtype=torch.int32, device=device)
+    view = buf[CANARY_PAD:CANARY_PAD + n]
+    if dtype != torch.int32:
+        view = view.view(dtype)
+    return buf, view.view(shape)
+
+
+def check_canaries(buf, name):
+    import torch
+
+    pad = torch.cat([buf[:CANARY_PAD], buf[-CANARY_PAD:]]).cpu().numpy()
+    bad = np.flatnonzero(pad != CANARY_WORD)
+    assert bad.size == 0, f"{name}: {bad.size} canary words overwritten (first at {bad[:4]})"
+
+
 def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, chunks=None,
             device="cuda:0"):
     """Run the library on a workloads.Batch (through the draft-logits entry point when the batch
@@ -73,14 +102,22 @@ def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, 
     rates = getattr(batch, "synthetic_rates", None)
     ctx.set_synthetic([] if rates is None else rates)
     d = to_device(batch, device)
+    n, R = batch.num_reqs, batch.num_rows
+    shapes = (((n, kmax + 1), torch.int32), ((n,), torch.int32), ((n,), torch.int32),
+              ((R,), torch.float32), ((R,), torch.float32), ((R,), torch.int32))
+    padded = [canary_buffer(shape, dt, device) for shape, dt in shapes]
+    views = [v for _, v in padded]
     outs = ctx.run(d["logits"], d["draft_ids"], d["draft_probs"], d["cu_num_draft"],
                    d["temperature"], d["is_greedy"], batch.seed if seed is None else seed,
                    req_index_base=req_index_base, max_spec_len=kmax, row_stats=True,
+                   out=tuple(views[:3]), stats_out=tuple(views[3:]),
                    draft_logits=d["draft_logits"], partial_prefill=d["partial_prefill"],
                    frequency_penalty=d["frequency_penalty"], output_bin_counts=d["output_bin_counts"],
                    counts_row=d["counts_row"], top_k=d["top_k"], top_p=d["top_p"])
     torch.cuda.synchronize()
     names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
+    for name, (buf, _) in zip(names, padded):
+        check_canaries(buf, name)
     res = {k: v.cpu().numpy() for k, v in zip(names, outs)}
     res["error_word"] = ctx.last_error()
     if own:

@@ -82,6 +82,32 @@ def test_bad_counts_row_is_reported_and_skips_the_penalty():
     assert got["error_word"] & sv.SV_ERR_COUNTS
 
 
+def test_malformed_cu_num_draft_with_penalty_and_constraints():
+    """The statistics and selection kernels read cu_num_draft before the verify kernel has
+    checked it; with a penalty they take each position's earlier drafts from it. A malformed
+    prefix sum (an entry far below 0, one far above the number of drafts, a decreasing pair)
+    must only produce empty rows and SV_ERR_BATCH, and leave the context usable."""
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    b = _constrain(_batch(111, 3001, [2, 3, 1, 0, 4], "bf16", "noisy"), 111, [0, 40], [0.9, 1.0])
+    workloads.add_penalty(b, 111, history=(20, 80), top_n=20)
+    nd = b.num_draft_tokens
+    ctx = sv.SpecVerify(8, 6, 3001, "bf16", True)
+    try:
+        for cu in ([0, -1000000, 5, 6, 6, nd], [0, 2, 1 << 30, 6, 6, nd], [0, 2, 5, 4, 6, nd],
+                   [0, 2, 5, 6, 6, nd + 7], [7, 2, 5, 6, 6, nd]):
+            bad = workloads.Batch(**{**b.__dict__})
+            bad.cu_num_draft = np.array(cu, np.int32)
+            got = gpu_run(bad, ctx, max_spec_len=6)
+            assert got["error_word"] & sv.SV_ERR_BATCH, cu
+            assert np.all(got["num_sampled"] == 0) and np.all(got["sampled"] == -1), cu
+        ok = gpu_run(b, ctx, max_spec_len=6)
+        assert ok["error_word"] == 0
+        assert_parity(b, ok, oracle.run(b, max_spec_len=6))
+    finally:
+        ctx.close()
+
+
 def test_penalty_arguments_must_come_together():
     import torch
 

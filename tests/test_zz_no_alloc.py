@@ -11,8 +11,9 @@ outputs must equal those of spec_verify_run on the same inputs.
 import numpy as np
 import pytest
 
+import oracle
 import workloads
-from _parity import S_RTOL, to_device
+from _parity import S_RTOL, assert_parity, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -73,6 +74,37 @@ def test_noalloc_matches_context_entry_point_on_two_calls_in_a_row():
         greedy=np.array([0, 0, 1, 0, 0, 0, 1, 0], np.uint8))
     for batch in (first, second):
         _same(_noalloc_run(batch), _context_run(batch))
+
+
+NAMES = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
+
+
+@pytest.mark.parametrize("c", [0, 1, 2, 3, 4])
+def test_noalloc_matches_the_oracle_on_the_workloads(c):
+    """Every workload at full size fits the static array; this entry point takes its race's
+    line maxima from the raced rows themselves (it has no room to keep them), so it is checked
+    against the oracle directly, by the parity rules of every other GPU test."""
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    b = workloads.workload(c)
+    got = dict(zip(NAMES, _noalloc_run(b)))
+    r = assert_parity(b, got, oracle.run(b))
+    assert sv.spec_verify_noalloc_last_error() == 0
+    print(f"workload {c}: {r['requests']} requests, ties {r['ties']}")
+
+
+def test_noalloc_error_word_reports_an_inconsistent_batch_and_is_cleared():
+    import speculative_decoding_verification_rejection_gb300 as sv
+
+    b = workloads.workload(0)
+    assert sv.spec_verify_noalloc_last_error() == 0
+    bad = workloads.Batch(**{**b.__dict__})
+    bad.cu_num_draft = np.array([0, 3, 2, 9, 12], np.int32)          # decreasing pair
+    got = _noalloc_run(bad)
+    assert np.all(got[1] == 0) and np.all(got[0] == -1)
+    assert sv.spec_verify_noalloc_last_error() & sv.SV_ERR_BATCH
+    assert sv.spec_verify_noalloc_last_error() == 0                  # read and cleared
+    _same(_noalloc_run(b), _context_run(b))                          # the array is still fine
 
 
 def test_noalloc_rejects_sizes_beyond_its_limits():
