@@ -64,6 +64,10 @@ def parse_args():
     p.add_argument("--top-k", type=int, default=None, help="top-k of every request")
     p.add_argument("--frequency-penalty", action="store_true",
                    help="a frequency penalty with seeded output-token counts per request")
+    p.add_argument("--stats-chunk", type=int, default=0,
+                   help="elements per statistics CTA (0: the library's automatic split)")
+    p.add_argument("--fp64-gumbel", action="store_true",
+                   help="race noise drawn in binary64 (the fp64 Gumbel option)")
     p.add_argument("--vocab-shards", type=int, default=1,
                    help="vocabulary-sharded verification with N shards, their calls emulated in "
                         "turn on one GPU (the exchange a concatenation)")
@@ -92,6 +96,7 @@ def load_workload(args, num_reqs=None):
         b.top_k = np.full(b.num_reqs, args.top_k, np.int32)
     if args.frequency_penalty:
         workloads.add_penalty(b, args.workload)
+    b.fp64_gumbel = bool(args.fp64_gumbel)
     return b
 
 
@@ -110,6 +115,7 @@ def workload_config(b):
         "top_p": None if b.top_p is None else float(b.top_p[0]),
         "top_k": None if b.top_k is None else int(b.top_k[0]),
         "frequency_penalty": b.frequency_penalty is not None,
+        "fp64_gumbel": bool(b.fp64_gumbel),
         "input_mb": round((b.logits.nbytes + (b.draft_probs.nbytes if b.draft_probs is not None else 0)
                            + (b.draft_logits.nbytes if b.draft_logits is not None else 0)) / 1e6, 2),
     }
@@ -265,7 +271,7 @@ def request_slice(b, lo: int, hi: int):
         counts_row=(np.arange(lo, hi, dtype=np.int32) if b.counts_row is None else b.counts_row[lo:hi])
         if b.frequency_penalty is not None else None,
         top_k=None if b.top_k is None else b.top_k[lo:hi],
-        top_p=None if b.top_p is None else b.top_p[lo:hi])
+        top_p=None if b.top_p is None else b.top_p[lo:hi], fp64_gumbel=b.fp64_gumbel)
 
 
 def time_oracle(args, seconds: float):
@@ -381,6 +387,8 @@ def run_ours(args, world, rank, local):
                         draft_logits=d_dl is not None)
     if b.synthetic_rates is not None:
         ctx.set_synthetic(b.synthetic_rates)
+    if args.stats_chunk:
+        ctx.set_chunks(args.stats_chunk)
     outs = (torch.empty((n, kmax + 1), dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev),
             torch.empty(n, dtype=torch.int32, device=dev))
@@ -388,7 +396,8 @@ def run_ours(args, world, rank, local):
 
     def step():
         ctx.run(d_logits, d_ids, d_q, d_cu, d_T, d_g, b.seed, req_index_base=base,
-                max_spec_len=kmax, out=outs, draft_logits=d_dl, **extras)
+                max_spec_len=kmax, out=outs, draft_logits=d_dl, fp64_gumbel=b.fp64_gumbel,
+                **extras)
 
     if args.vocab_shards > 1:
         from speculative_decoding_verification_rejection_gb300.shard import ShardBackend, vocab_bounds
@@ -474,7 +483,7 @@ def run_ours(args, world, rank, local):
     e2e = None
     if sharded:
         pass  # the emulated ranks share one GPU: no end-to-end figure
-    elif not args.no_e2e and (d_dl is not None or extras):
+    elif not args.no_e2e and (d_dl is not None or extras or b.fp64_gumbel):
         e2e = e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, dist)
     elif not args.no_e2e:
         ctx.reserve_host_io()
@@ -536,7 +545,7 @@ def run_ours(args, world, rank, local):
         achieved = stats_bytes / (ms_per_step / 1e3) / 1e9
     else:
         achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
-    plain = not extras and b.synthetic_rates is None and not sharded
+    plain = not extras and b.synthetic_rates is None and not sharded and not b.fp64_gumbel
     # our kernels per step: statistics + verify (+ the top-k / top-p selection); sharded: each
     # shard's statistics, export and race, and one finish
     launches_per_step = (3 * len(sides) + 1 if sharded else
@@ -679,7 +688,7 @@ def e2e_via_run(ctx, b, logits_np, dl_np, outs, base, kmax, args, world, dev, di
             d.copy_(h, non_blocking=True)
         ctx.run(kw["logits"], kw["draft_ids"], kw.get("draft_probs"),
                 kw["cu_num_draft"], kw["temperature"], kw["is_greedy"], b.seed,
-                req_index_base=base, max_spec_len=kmax, out=outs,
+                req_index_base=base, max_spec_len=kmax, out=outs, fp64_gumbel=b.fp64_gumbel,
                 **{k: v for k, v in kw.items() if k in ("draft_logits", "frequency_penalty",
                                                          "output_bin_counts", "counts_row",
                                                          "top_k", "top_p")})

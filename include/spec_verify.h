@@ -98,6 +98,11 @@ extern "C" {
 /* bits of the device error word */
 #define SV_ERR_BATCH 1u   /* inconsistent cu_num_draft / draft lengths in some call */
 #define SV_ERR_COUNTS 2u  /* a counts_row outside [0, counts_rows): that request got no penalty */
+#define SV_ERR_BOUNDS 4u  /* (a library built with SV_DEBUG_BOUNDS only) a kernel tried to read or
+                             write outside the arrays of the call; the access was skipped */
+#define SV_ERR_SELECT 8u  /* the top-k / top-p threshold of some row was not found within the
+                             selection's pass limit (not expected to happen): that row was
+                             left without the constraint */
 
 typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
 
@@ -211,6 +216,21 @@ int spec_verify_run_draft_logits(spec_verify_ctx *ctx, const void *logits,
  *                    both. The kept masses are summed in binary32 (hardware exp2), so a top-p
  *                    boundary within about 1e-6 of the total may fall either way. These calls
  *                    launch one more kernel; spec_verify_run_noalloc does not take them.
+ *   fp64_gumbel      0, or nonzero to draw the race noise in binary64 ([spec-in-vllm] 7.3:
+ *                    use_fp64_gumbel, the Gumbel noise generated in double precision). Every
+ *                    race of the call (residual, without the rejected draft, bonus, non-spec
+ *                    Gumbel-max, synthetic mode's draw) then uses binary64 clocks with 52-bit
+ *                    uniforms and compares binary64 keys: the same group layout as above, the
+ *                    head call (g, j, i', 32) giving W = (m + 1/2) / 2^52 with
+ *                    m = word0 * 2^20 + (word1 >> 12) and the slot a = word 2 & 63, slot s != a
+ *                    taking U_s from words (0, 1) (even s) or (2, 3) (odd s) of counter
+ *                    (g, j, i', 33 + s / 2), clocks E_g = -log(W) / 64 and E_g + (-log U_s) in
+ *                    binary64 (log: the same reduction and atanh series, to the term 2/19), key
+ *                    (double) w_v / E_v. The largest clock is then 53 ln 2 = 36.7 instead of
+ *                    24 ln 2 = 16.6, so the noise's tail is no longer cut short in the far
+ *                    tail of p. Acceptance tests are unchanged. Costs binary64 arithmetic (a
+ *                    slow unit on this part) for the few tokens whose keys are evaluated
+ *                    exactly. Not offered by the vocabulary-shard or no-alloc entry points.
  */
 typedef struct spec_verify_batch {
     const void *logits;
@@ -232,6 +252,7 @@ typedef struct spec_verify_batch {
     int32_t num_draft_tokens;
     int32_t max_spec_len_this_batch;
     int32_t counts_rows;
+    int32_t fp64_gumbel;
 } spec_verify_batch;
 
 /* Outputs of one batch (device pointers): sampled, num_sampled, num_rejected as in

@@ -21,7 +21,13 @@ _ROOT = os.path.dirname(_PKG)
 _INCLUDE = os.path.join(_ROOT, "include")
 _HEADER = os.path.join(_INCLUDE, "spec_verify.h")
 _SOURCES = [os.path.join(_PKG, "csrc", "spec_verify.cu"), os.path.join(_PKG, "csrc", "sv_device.cuh")]
-LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+# SPEC_VERIFY_DEBUG_BOUNDS=1 in the environment selects the checked build (-DSV_DEBUG_BOUNDS): every
+# global load and store of the kernels is checked against the call's arrays, and an access
+# outside them is skipped and reported as SV_ERR_BOUNDS in the error word. For tests only.
+DEBUG_BOUNDS = os.environ.get("SPEC_VERIFY_DEBUG_BOUNDS", "0") not in ("", "0")
+RELEASE_LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+DEBUG_LIB_PATH = os.path.join(_PKG, "libspecverify_debug.so")
+LIB_PATH = DEBUG_LIB_PATH if DEBUG_BOUNDS else RELEASE_LIB_PATH
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-shared", "-Xcompiler", "-fPIC", "-I" + _INCLUDE]
@@ -43,7 +49,8 @@ class Batch(ctypes.Structure):
                 ("top_p", ctypes.c_void_p),
                 ("seed", ctypes.c_uint64), ("req_index_base", ctypes.c_uint32),
                 ("num_reqs", ctypes.c_int32), ("num_draft_tokens", ctypes.c_int32),
-                ("max_spec_len_this_batch", ctypes.c_int32), ("counts_rows", ctypes.c_int32)]
+                ("max_spec_len_this_batch", ctypes.c_int32), ("counts_rows", ctypes.c_int32),
+                ("fp64_gumbel", ctypes.c_int32)]
 
 
 class Outputs(ctypes.Structure):
@@ -51,7 +58,7 @@ class Outputs(ctypes.Structure):
     _fields_ = [("sampled", ctypes.c_void_p), ("num_sampled", ctypes.c_void_p),
                 ("num_rejected", ctypes.c_void_p), ("row_max", ctypes.c_void_p),
                 ("row_sumexp", ctypes.c_void_p), ("row_argmax", ctypes.c_void_p)]
-SV_ERR_BATCH, SV_ERR_COUNTS = 1, 2
+SV_ERR_BATCH, SV_ERR_COUNTS, SV_ERR_BOUNDS, SV_ERR_SELECT = 1, 2, 4, 8
 KERNELS = ("stats", "verify", "select")  # profiling slots (select: top-k / top-p calls)
 
 _lib = None
@@ -71,31 +78,56 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str | None = None) -> bool:
+    path = path or LIB_PATH
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(s) > t for s in _SOURCES + [_HEADER])
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile libspecverify.so for sm_103a next to this file (atomic replace)."""
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, debug: bool | None = None) -> str:
+    """Compile libspecverify.so (or, with debug=True, the checked libspecverify_debug.so) for
+    sm_103a next to this file (atomic replace). debug=None: the build this process loads."""
+    debug = DEBUG_BOUNDS if debug is None else debug
+    path = DEBUG_LIB_PATH if debug else RELEASE_LIB_PATH
+    if not force and not _stale(path):
+        return path
     fd, tmp = tempfile.mkstemp(suffix=".so", dir=_PKG)
     os.close(fd)
-    cmd = [_nvcc(), *NVCC_FLAGS, "-o", tmp, _SOURCES[0]]
+    cmd = [_nvcc(), *NVCC_FLAGS, *(["-DSV_DEBUG_BOUNDS"] if debug else []), "-o", tmp, _SOURCES[0]]
     try:
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + r.stderr[-4000:])
         if verbose:
             print(r.stderr)
-        os.replace(tmp, LIB_PATH)
+        os.replace(tmp, path)
     finally:
         if os.path.exists(tmp):
             os.unlink(tmp)
-    return LIB_PATH
+    return path
+
+
+def build_all(force: bool = False) -> None:
+    """Both builds (the library and its checked debug variant), compiled in parallel."""
+    import threading
+
+    errors = []
+
+    def one(debug):
+        try:
+            build(force=force, debug=debug)
+        except Exception as e:  # noqa: BLE001 - re-raised below
+            errors.append(e)
+
+    threads = [threading.Thread(target=one, args=(d,)) for d in (False, True)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    if errors:
+        raise errors[0]
 
 
 def declared_symbols() -> list[str]:
@@ -392,7 +424,7 @@ class SpecVerify:
             *, req_index_base: int = 0, max_spec_len: int | None = None, out=None,
             row_stats: bool = False, stream=None, draft_logits=None, partial_prefill=None,
             frequency_penalty=None, output_bin_counts=None, counts_row=None, top_k=None,
-            top_p=None, stats_out=None):
+            top_p=None, stats_out=None, fp64_gumbel: bool = False):
         """Verify a batch held in device tensors. Returns (sampled, num_sampled, num_rejected)
         and, with row_stats=True, also (row_max, row_sumexp, row_argmax).
 
@@ -403,7 +435,8 @@ class SpecVerify:
         int32) and counts_row ([num_reqs] int32, optional): the frequency penalty. top_k
         ([num_reqs] int32), top_p ([num_reqs] float32): sampling constraints. Any of these
         goes through spec_verify_run_batch. out / stats_out: caller-provided output tensors
-        (sampled, num_sampled, num_rejected) / (row_max, row_sumexp, row_argmax)."""
+        (sampled, num_sampled, num_rejected) / (row_max, row_sumexp, row_argmax).
+        fp64_gumbel=True draws the race noise in binary64 (the fp64 Gumbel option)."""
         import torch
         num_reqs = cu_num_draft.numel() - 1
         nd = draft_ids.numel()
@@ -430,7 +463,7 @@ class SpecVerify:
                      torch.empty(R, dtype=torch.float32, device=dev),
                      torch.empty(R, dtype=torch.int32, device=dev))
         extras = (partial_prefill, frequency_penalty, output_bin_counts, counts_row, top_k, top_p)
-        if any(x is not None for x in extras):
+        if any(x is not None for x in extras) or fp64_gumbel:
             if output_bin_counts is not None and (output_bin_counts.dim() != 2
                                                   or output_bin_counts.shape[1] != self.vocab_size):
                 raise ValueError("output_bin_counts must be [rows, vocab_size]")
@@ -439,7 +472,8 @@ class SpecVerify:
                       _ptr(partial_prefill), _ptr(frequency_penalty), _ptr(output_bin_counts),
                       _ptr(counts_row), _ptr(top_k), _ptr(top_p), seed, req_index_base,
                       num_reqs, nd, kmax,
-                      output_bin_counts.shape[0] if output_bin_counts is not None else 0)
+                      output_bin_counts.shape[0] if output_bin_counts is not None else 0,
+                      int(bool(fp64_gumbel)))
             o = Outputs(*(_ptr(t) for t in (*out, *stats)))
             spec_verify_run_batch(self.ctx, b, o, cuda_stream=stream)
         elif draft_logits is not None:

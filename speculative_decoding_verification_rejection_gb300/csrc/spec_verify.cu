@@ -34,6 +34,7 @@
 #include <cmath>
 #include <cstddef>
 #include <cstdint>
+#include <cstdlib>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -62,16 +63,65 @@ struct __align__(16) StatPart {
 };
 
 // ---------------------------------------------------------------------------------------
+// checked global memory access (debug builds)
+// ---------------------------------------------------------------------------------------
+// Built with -DSV_DEBUG_BOUNDS, the library checks every global load and store of its kernels
+// against the arrays of the current call (their address ranges, registered by the host before
+// the launches): an access outside all of them is skipped (a load gives 0) and sets
+// SV_ERR_BOUNDS in the call's error word, and the kernel goes on, so the context stays usable.
+// A stand-in for a memory checker where none can be run. In a normal build sv_ldg is __ldg,
+// sv_ld a plain load, sv_st a plain store, and no check exists.
+#ifdef SV_DEBUG_BOUNDS
+constexpr int kDbgRanges = 32;
+struct DbgRanges {
+    unsigned long long lo[kDbgRanges], hi[kDbgRanges];  // [lo, hi) byte ranges
+    int n;
+    unsigned *flags;  // the call's error word pair (bit SV_ERR_BOUNDS goes to flags[1])
+};
+__device__ DbgRanges g_dbg;
+
+__device__ __noinline__ bool dbg_ok(const void *p, unsigned bytes)
+{
+    const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+    for (int k = 0; k < g_dbg.n; ++k)
+        if (a >= g_dbg.lo[k] && a + bytes <= g_dbg.hi[k]) return true;
+    if (g_dbg.flags) atomicOr(g_dbg.flags + 1, SV_ERR_BOUNDS);
+    return false;
+}
+#define SV_CHECK(p, bytes) dbg_ok((p), (bytes))
+#else
+#define SV_CHECK(p, bytes) true
+#endif
+
+template <typename T>
+__device__ __forceinline__ T sv_ldg(const T *p)
+{
+    if (!SV_CHECK(p, sizeof(T))) return T{};
+    return __ldg(p);
+}
+template <typename T>
+__device__ __forceinline__ T sv_ld(const T *p)
+{
+    if (!SV_CHECK(p, sizeof(T))) return T{};
+    return *p;
+}
+template <typename T, typename U>
+__device__ __forceinline__ void sv_st(T *p, const U &v)
+{
+    if (SV_CHECK(p, sizeof(T))) *p = v;
+}
+
+// ---------------------------------------------------------------------------------------
 // element loads
 // ---------------------------------------------------------------------------------------
 template <typename T> struct Elem;
 template <> struct Elem<float> {
-    static __device__ __forceinline__ float at(const float *p, size_t k) { return __ldg(p + k); }
+    static __device__ __forceinline__ float at(const float *p, size_t k) { return sv_ldg(p + k); }
 };
 template <> struct Elem<uint16_t> {
     static __device__ __forceinline__ float at(const uint16_t *p, size_t k)
     {
-        return __uint_as_float(static_cast<uint32_t>(__ldg(p + k)) << 16);
+        return __uint_as_float(static_cast<uint32_t>(sv_ldg(p + k)) << 16);
     }
 };
 
@@ -84,7 +134,7 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 
 __device__ __forceinline__ uint4 ldg_v4(const void *p)
 {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+    return sv_ldg(reinterpret_cast<const uint4 *>(p));
 }
 
 // ---------------------------------------------------------------------------------------
@@ -128,10 +178,10 @@ __device__ __forceinline__ void emit_row(int i, int jstar, int K, int q0, int to
 {
     int32_t *out = sampled + static_cast<size_t>(i) * stride;
     for (int s = tid; s < stride; s += nthreads)
-        out[s] = s < jstar ? draft_ids[q0 + s] : (s == jstar ? token : -1);
+        sv_st(out + s, s < jstar ? sv_ld(draft_ids + q0 + s) : (s == jstar ? token : -1));
     if (tid == 0) {
-        num_sampled[i] = jstar + 1;
-        num_rejected[i] = jstar < 0 ? 0 : K - jstar;
+        sv_st(num_sampled + i, jstar + 1);
+        sv_st(num_rejected + i, jstar < 0 ? 0 : K - jstar);
     }
 }
 
@@ -149,7 +199,7 @@ __device__ __forceinline__ int row_request(const int32_t *__restrict__ cu, int n
     while (hi - lo > 1) {
         const int step = (hi - lo + 31) >> 5;
         const int p = lo + lane * step;
-        const bool ok = lane == 0 || (p < hi && __ldg(cu + p) + (draft_rows ? 0 : p) <= r);
+        const bool ok = lane == 0 || (p < hi && sv_ldg(cu + p) + (draft_rows ? 0 : p) <= r);
         const unsigned b = __ballot_sync(0xFFFFFFFFu, ok);
         lo += (31 - __clz(b)) * step;
         hi = min(hi, lo + step);
@@ -170,8 +220,8 @@ struct RequestTable {
 // [mini-sglang] T <= 0) or top_k == 1 ([mini-sglang]: only the largest logit is kept).
 __device__ __forceinline__ float request_invT(const RequestTable &rq, int i, bool &greedy)
 {
-    const float T = __ldg(rq.temperature + i);
-    greedy = __ldg(rq.is_greedy + i) != 0 || !(T > 0.0f) || (rq.top_k && __ldg(rq.top_k + i) == 1);
+    const float T = sv_ldg(rq.temperature + i);
+    greedy = sv_ldg(rq.is_greedy + i) != 0 || !(T > 0.0f) || (rq.top_k && sv_ldg(rq.top_k + i) == 1);
     return greedy ? 1.0f : __frcp_rn(T);
 }
 
@@ -209,9 +259,9 @@ __device__ __forceinline__ PenRow pen_row(const PenTable &pt, const int32_t *dra
     PenRow r{0.0f, nullptr, nullptr, 0};
     if (!pt.f) return r;
     if (q0 < 0 || q0 > pt.nd || j < 0 || j > pt.kmax || j > pt.nd - q0) return r;
-    const int crow = pt.counts_row ? __ldg(pt.counts_row + i) : i;
+    const int crow = pt.counts_row ? sv_ldg(pt.counts_row + i) : i;
     if (crow < 0 || crow >= pt.counts_rows) return r;
-    r.f = __ldg(pt.f + i);
+    r.f = sv_ldg(pt.f + i);
     r.cnt = pt.counts + static_cast<size_t>(crow) * V;
     r.prev = draft_ids + q0;
     r.nprev = j;
@@ -221,15 +271,15 @@ __device__ __forceinline__ PenRow pen_row(const PenTable &pt, const int32_t *dra
 __device__ __forceinline__ bool pen_counts_row_bad(const PenTable &pt, int i)
 {
     if (!pt.f) return false;
-    const int crow = pt.counts_row ? __ldg(pt.counts_row + i) : i;
+    const int crow = pt.counts_row ? sv_ldg(pt.counts_row + i) : i;
     return crow < 0 || crow >= pt.counts_rows;
 }
 
 __device__ __forceinline__ float pen_apply(const PenRow &r, float l, int v)
 {
     if (r.f == 0.0f) return l;
-    int c = __ldg(r.cnt + v);
-    for (int k = 0; k < r.nprev; ++k) c += __ldg(r.prev + k) == v;
+    int c = sv_ldg(r.cnt + v);
+    for (int k = 0; k < r.nprev; ++k) c += sv_ldg(r.prev + k) == v;
     return c == 0 ? l : __fmaf_rn(-r.f, __int2float_rn(c), l);
 }
 
@@ -272,6 +322,11 @@ constexpr int kPairBytes = 64;
 
 __device__ __forceinline__ void ldg_pair(const char *p, uint32_t (&w)[16])
 {
+    if (!SV_CHECK(p, kPairBytes)) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) w[k] = 0u;
+        return;
+    }
     asm("ld.global.nc.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
         : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]),
           "=r"(w[7])
@@ -608,7 +663,7 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
     if (lane == 0)
-        part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
+        sv_st(part + (static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5), StatPart{L, s, idx, 0});
 }
 
 // Asynchronous 16- and 4-byte copies global -> shared (cp.async), tracked per thread in commit
@@ -620,16 +675,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p)
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
 {
+    if (!SV_CHECK(src, 16)) return;  // (the slot keeps what it held)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 // through L1 (.ca): the two halves of a 32-byte sector that two copies of one lane read are
 // fetched from L2 once
 __device__ __forceinline__ void cp_async16_l1(uint32_t dst, const void *src)
 {
+    if (!SV_CHECK(src, 16)) return;  // (the slot keeps what it held)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
 {
+    if (!SV_CHECK(src, 4)) return;  // (the slot keeps what it held)
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -704,10 +762,10 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
         if (scan) {
             bool hit = false;
             for (int k = 0; k < pr.nprev; ++k)
-                hit |= static_cast<unsigned>(__ldg(pr.prev + k) - v) < static_cast<unsigned>(kEV);
+                hit |= static_cast<unsigned>(sv_ldg(pr.prev + k) - v) < static_cast<unsigned>(kEV);
             if (hit)
                 for (int q = 0; q < pr.nprev; ++q) {
-                    const int d = __ldg(pr.prev + q) - v;
+                    const int d = sv_ldg(pr.prev + q) - v;
 #pragma unroll
                     for (int k = 0; k < kEV; ++k) n[k] += d == k;
                 }
@@ -749,7 +807,7 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
     // earlier drafts: lane k holds the k-th (k < 32); more than 32 are scanned every round
     const int np = pr.nprev;
-    const int pv = lane < np ? __ldg(pr.prev + lane) : -1;
+    const int pv = lane < np ? sv_ldg(pr.prev + lane) : -1;
     int ub = static_cast<int>(threadIdx.x) & ~31;
 #pragma unroll
     for (int s = 0; s < kPenStages - 1; ++s) issue(ub + lane + s * kThreads, s);
@@ -805,7 +863,7 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
         int cnt[kEV];
 #pragma unroll
-        for (int k = 0; k < kEV; ++k) cnt[k] = __ldg(cbase + st.best_p * kEV + k);
+        for (int k = 0; k < kEV; ++k) cnt[k] = sv_ldg(cbase + st.best_p * kEV + k);
         float y[kEV];
         values(v, ws, cnt, true, y);
 #pragma unroll
@@ -815,7 +873,7 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
     if (lane == 0)
-        part[(static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5)] = StatPart{L, s, idx, 0};
+        sv_st(part + (static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5), StatPart{L, s, idx, 0});
 }
 
 // One [rows x V] array the statistics kernel streams: the target logits, or the draft logits of
@@ -869,7 +927,7 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         if constexpr (kPen) {  // a penalised row takes the penalty path (target logits only)
             if (!X.draft_rows) {
                 const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31);
-                const int q0 = __ldg(rq.cu + i);
+                const int q0 = sv_ldg(rq.cu + i);
                 const PenRow pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
                 if (pr.f != 0.0f) {
                     bool greedy;
@@ -893,9 +951,9 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         const int nv = nl * static_cast<int>(sizeof(T)) / 16;  // whole 16-byte vectors
         uint4 *dst = reinterpret_cast<uint4 *>(X.lines + line_base);
         const uint4 *src = reinterpret_cast<const uint4 *>(s_raw);
-        for (int k = threadIdx.x; k < nv; k += kThreads) dst[k] = src[k];
+        for (int k = threadIdx.x; k < nv; k += kThreads) sv_st(dst + k, src[k]);
         for (int k = nv * 16 / static_cast<int>(sizeof(T)) + threadIdx.x; k < nl; k += kThreads)
-            X.lines[line_base + k] = s_lines[k];
+            sv_st(X.lines + line_base + k, s_lines[k]);
     }
 }
 
@@ -925,6 +983,7 @@ struct VerifyParams {
     const float *sel_tau;        // [rows] thresholds of constrained rows (nullptr: none)
     const float *sel_S;          // [rows] their kept mass
     int nsyn;                    // synthetic acceptance: rates of positions < nsyn (0 = off)
+    int f64;                     // race clocks and keys in binary64 (the fp64 Gumbel option)
     float syn[SV_MAX_SYNTHETIC]; // unconditional rate a_j of position j
 };
 
@@ -934,7 +993,7 @@ struct VerifyParams {
 __device__ __forceinline__ bool accept_synthetic(const VerifyParams &P, int j, int qrow,
                                                  uint32_t ireq)
 {
-    const int d = __ldg(P.draft_ids + qrow);
+    const int d = sv_ldg(P.draft_ids + qrow);
     if (d < 0 || d >= P.V) return false;
     const float a = j < P.nsyn ? P.syn[j] : 0.0f;
     float c = a;
@@ -964,10 +1023,10 @@ __device__ __forceinline__ AcceptInputs accept_inputs(const T *rp, int V, int qr
                                                       const float *__restrict__ q,
                                                       const T *__restrict__ dl)
 {
-    AcceptInputs a{true, __ldg(draft_ids + qrow), 0.0f, 1.0f};
+    AcceptInputs a{true, sv_ldg(draft_ids + qrow), 0.0f, 1.0f};
     if (a.d >= 0 && a.d < V) {
         a.l = Elem<T>::at(rp, a.d);
-        if (q) a.qv = __ldg(q + static_cast<size_t>(qrow) * V + a.d);
+        if (q) a.qv = sv_ldg(q + static_cast<size_t>(qrow) * V + a.d);
         else if (dl) a.qv = Elem<T>::at(dl + static_cast<size_t>(qrow) * V, a.d);
     }
     return a;
@@ -1098,6 +1157,7 @@ struct RaceRow {
     float m, S, invT;
     uint32_t j, ireq, k0, k1;  // Philox counter words 1, 2 and key
     uint32_t g0;               // group of the row's token 0 (a vocabulary shard's first group)
+    bool f64;                  // race clocks and keys in binary64 (the fp64 Gumbel option)
 };
 
 // Shared memory of the search (one CTA). Each warp keeps a queue of candidate tokens (at most
@@ -1115,7 +1175,11 @@ struct SearchSmem {
     float *pb;                // [G] upper bound of the group's keys (NaN once evaluated)
     uint32_t *ew;             // [G] word 0 of the group's head call (gives E_g)
     uint8_t *ag;              // [G] slot that holds the group's smallest clock
-    unsigned long long *best; // best candidate so far, packed (key, ~v); 0 = none
+    unsigned long long *best; // best candidate so far, packed (key, ~v); 0 = none. With binary64
+                              // keys: (key rounded down to binary32, ~v), a lower bound that only
+                              // prunes; the exact best is kept per warp in wbk / wbv
+    unsigned long long *wbk;  // [kWarps] binary64 races: each warp's best key (bits + 1; 0 = none)
+    int *wbv;                 // [kWarps] and its token
     int *cnt;
     uint32_t *qgs;            // [kWarps][kQueue] candidate tokens of each warp: group << 6 | slot
     float *ql, *qq;           // [kWarps][kQueue] their raw logits and q entries
@@ -1154,16 +1218,25 @@ __device__ __forceinline__ float group_emin_word(uint32_t w_head)
     return __fmul_rn(-sv::log_f32(sv::uniform_from_word(w_head)), 0x1p-6f);
 }
 
-// An upper bound of every key exp(y') / E' with y' <= y and E' >= E_g (W = word 0 of the group's
-// head call), from the hardware approximations: lg2.approx errs by less than 2^-22 absolute and
+// The group's head uniform W as a binary32 value that is never below it: exact for the binary32
+// clocks; for the binary64 ones (52 bits from words 0 and 1) an upper bound from word 0 alone,
+// (word 0 + 1) / 2^32 rounded up, which makes -log W and the bounds below only smaller / larger.
+__device__ __forceinline__ float head_uniform_ub(uint32_t w0, bool f64)
+{
+    return f64 ? __fmul_rn(__ull2float_ru(static_cast<unsigned long long>(w0) + 1ull), 0x1p-32f)
+               : sv::uniform_from_word(w0);
+}
+
+// An upper bound of every key exp(y') / E' with y' <= y and E' >= E_g (W >= the group's head
+// uniform, head_uniform_ub), from the hardware approximations: lg2.approx errs by less than 2^-22 absolute and
 // ex2.approx by a few 2^-23 relative on these ranges, and the fp32 product y log2(e) by
 // |y| 2^-23; the margins below (2^-20 absolute on -log2 W, 2^-12 relative twice) cover all of
 // that many times over. Only the evaluation of a group uses its exact E_g. +inf when -log W is
 // too small to bound from below (W within about 10^-6 of 1), and for a NaN y.
-__device__ __forceinline__ float group_bound(float y, uint32_t w_head)
+__device__ __forceinline__ float group_bound(float y, float W)
 {
     float l2;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(sv::uniform_from_word(w_head)));
+    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(W));
     const float nl = (-l2 - 0x1p-20f) * 0x1.62e2p-1f;  // <= -ln W (ln 2 rounded down)
     const float tub = sv::ex2_approx(y * kLog2e) * (1.0f + 0x1p-12f);
     const float b = __fdividef(tub, nl * 0x1p-6f) * (1.0f + 0x1p-12f);
@@ -1171,8 +1244,8 @@ __device__ __forceinline__ float group_bound(float y, uint32_t w_head)
 }
 
 // pb[g] = an upper bound of every key in group g (from x_max = fl(line max * invT) and the
-// group's head call), ew[g] / ag[g] = the head's word 0 and slot. Returns the thread's best
-// (pb, g) packed, 0 if it has no group.
+// group's head call), ew[g] / ag[g] = the head's word 0 and slot (binary64 clocks: word 2 gives
+// the slot). Returns the thread's best (pb, g) packed, 0 if it has no group.
 template <typename T>
 __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &rl,
                                            const SearchSmem &sm)
@@ -1187,7 +1260,8 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
             const int g = min(g0 + k * kThreads, r.G - 1);
             const int v0 = g * kGroup, v1 = min(v0 + kGroup, r.V) - 1;
             lmax[k] = fmaxf(sm.lm[rl.of(v0)], sm.lm[rl.of(v1)]);
-            h[k] = sv::philox4x32_10(static_cast<uint32_t>(g) + r.g0, r.j, r.ireq, sv::kClockHead, r.k0, r.k1);
+            h[k] = sv::philox4x32_10(static_cast<uint32_t>(g) + r.g0, r.j, r.ireq,
+                                     r.f64 ? sv::kClockHead64 : sv::kClockHead, r.k0, r.k1);
         }
 #pragma unroll
         for (int k = 0; k < kStep; ++k) {
@@ -1196,10 +1270,12 @@ __device__ unsigned long long group_bounds(const RaceRow<T> &r, const RowLines &
                 // a group whose largest x is below the kept set's threshold holds no candidate
                 // (x_v = fl(l_v / T) <= fl(lmax / T)): bound 0 (NaN groups stay in the race)
                 const float xg = __fmul_rn(lmax[k], r.invT);
-                const float b = !(xg < r.tau) ? group_bound(__fsub_rn(xg, r.m), h[k].x) : 0.0f;
+                const float b = !(xg < r.tau)
+                                    ? group_bound(__fsub_rn(xg, r.m), head_uniform_ub(h[k].x, r.f64))
+                                    : 0.0f;
                 sm.pb[g] = b;
                 sm.ew[g] = h[k].x;
-                sm.ag[g] = static_cast<uint8_t>(h[k].y & 63u);
+                sm.ag[g] = static_cast<uint8_t>((r.f64 ? h[k].z : h[k].y) & 63u);
                 best = max(best, pack_key(b, g));
             }
         }
@@ -1214,35 +1290,116 @@ __device__ __forceinline__ unsigned long long ld_best(const unsigned long long *
     return __shfl_sync(0xFFFFFFFFu, v, 0);
 }
 
-// An upper bound of 1 / E_g from the group's head word W (E_g = -log(W) / 64): hardware lg2 and
-// rcp with the margins of group_bound; +inf when -log W is too small to bound from below.
-__device__ __forceinline__ float inv_emin_bound(uint32_t w_head)
+// An upper bound of 1 / E_g from W >= the group's head uniform (E_g = -log(W) / 64): hardware
+// lg2 and rcp with the margins of group_bound; +inf when -log W is too small to bound from below.
+__device__ __forceinline__ float inv_emin_bound(float W)
 {
     float l2;
-    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(sv::uniform_from_word(w_head)));
+    asm("lg2.approx.f32 %0, %1;" : "=f"(l2) : "f"(W));
     const float nl = (-l2 - 0x1p-20f) * 0x1.62e2p-1f;  // <= -ln W
     return nl > 0.0f ? __frcp_rz(nl * 0x1p-6f) * (1.0f + 0x1p-12f) : kInf;
+}
+
+// The binary64 key w / E_v of slot `slot` of group gg (a = the slot of the group's smallest
+// clock), with the binary64 clocks of sv_device.cuh.
+__device__ __forceinline__ double key_f64(float w, uint32_t gg, int slot, int a, uint32_t j,
+                                          uint32_t ireq, uint32_t k0, uint32_t k1)
+{
+    const sv::Philox4 hd = sv::philox4x32_10(gg, j, ireq, sv::kClockHead64, k0, k1);
+    const double E = __dmul_rn(-sv::log_f64(sv::uniform64_from_words(hd.x, hd.y)), 0x1p-6);
+    double Ev = E;
+    if (slot != a) {
+        const sv::Philox4 sl = sv::philox4x32_10(
+            gg, j, ireq, sv::kClockHead64 + 1u + static_cast<uint32_t>(slot >> 1), k0, k1);
+        const double U = (slot & 1) ? sv::uniform64_from_words(sl.z, sl.w)
+                                    : sv::uniform64_from_words(sl.x, sl.y);
+        Ev = __dadd_rn(E, -sv::log_f64(U));
+    }
+    return __ddiv_rn(static_cast<double>(w), Ev);  // >= 0 and finite: E_v >= E_g >= 2^-59
 }
 
 // Empty the warp's candidate queue (n entries): one token per lane, its exact weight, its race
 // clock and its key, merged into *sm.best. Entry: group g, slot s, raw logit, q entry.
 // Slot s = v & 63 of group g: its clock is E_g for the head's slot a, else fl(E_g + (-log U_s)),
-// U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4).
+// U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4). With binary64 clocks
+// (r.f64) the same in double: E_g from the head's words 0 and 1, U_s from words (0, 1) or (2, 3)
+// of slot call s / 2 (tag kClockHead64 + 1 + s / 2), the key the binary64 quotient; *sm.best then
+// receives the key rounded down (a lower bound, for pruning) and the warp's exact best goes to
+// wbk / wbv.
+// One queue entry's exact weight (t, or the residual rr; NaN-free, may be <= 0) and token.
+template <typename T, bool kRes, bool kDL>
+__device__ __forceinline__ float queue_weight(const RaceRow<T> &r, const SearchSmem &sm, int e)
+{
+    const int warp = threadIdx.x >> 5;
+    const float t = sv::exp_f32(__fsub_rn(__fmul_rn(sm.ql[warp * kQueue + e], r.invT), r.m));
+    float qv = sm.qq[warp * kQueue + e];  // q, or the raw draft logit (draft-logits mode)
+    if constexpr (kDL) qv = __fdiv_rn(sv::exp_f32(__fsub_rn(__fmul_rn(qv, r.invT), r.md)), r.Sd);
+    return kRes ? __fmaf_rn(-r.S, qv, t) : t;
+}
+
+// flush_queue with binary64 clocks and keys (r.f64): *sm.best receives each key rounded down to
+// binary32 (a lower bound, used only to prune), and each warp's exact best (the largest binary64
+// key, lowest token on equal keys) goes to wbk / wbv.
+template <typename T, bool kRes, bool kDL>
+__device__ void flush_queue_f64(const RaceRow<T> &r, const SearchSmem &sm, int n)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int e0 = 0; e0 < n; e0 += 32) {
+        const int e = e0 + lane;
+        unsigned long long p = 0, kb = 0;  // kb: binary64 key bits + 1 (0: no candidate)
+        int kv = INT_MAX;
+        if (e < n) {
+            const uint32_t gsl = sm.qgs[warp * kQueue + e];
+            const int g = static_cast<int>(gsl >> 6), slot = static_cast<int>(gsl & 63u);
+            const float w = queue_weight<T, kRes, kDL>(r, sm, e);
+            if (!kRes || w > 0.0f) {
+                const double k64 = key_f64(w, static_cast<uint32_t>(g) + r.g0, slot, sm.ag[g], r.j,
+                                           r.ireq, r.k0, r.k1);
+                kb = static_cast<unsigned long long>(__double_as_longlong(k64)) + 1ull;
+                kv = g * kGroup + slot;
+                p = pack_key(__double2float_rd(k64), kv);
+            }
+        }
+        p = warp_max_u64(p);
+        if (lane == 0 && p != 0) atomicMax(sm.best, p);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long k2 = __shfl_xor_sync(0xFFFFFFFFu, kb, o);
+            const int v2 = __shfl_xor_sync(0xFFFFFFFFu, kv, o);
+            if (k2 > kb || (k2 == kb && v2 < kv)) {
+                kb = k2;
+                kv = v2;
+            }
+        }
+        if (lane == 0 && (kb > sm.wbk[warp] || (kb == sm.wbk[warp] && kb != 0 && kv < sm.wbv[warp]))) {
+            sm.wbk[warp] = kb;
+            sm.wbv[warp] = kv;
+        }
+    }
+    __syncwarp();
+}
+
+// Empty the warp's candidate queue (n entries): one token per lane, its exact weight, its race
+// clock and its key, merged into *sm.best. Entry: group g, slot s, raw logit, q entry.
+// Slot s = v & 63 of group g: its clock is E_g for the head's slot a, else fl(E_g + (-log U_s)),
+// U_s from word s & 3 of slot call s / 4 (tag kClockHead + 1 + s / 4). Binary64 races take
+// flush_queue_f64.
 template <typename T, bool kRes, bool kDL>
 __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     __syncwarp();
+    if (r.f64) {
+        flush_queue_f64<T, kRes, kDL>(r, sm, n);
+        return;
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int e0 = 0; e0 < n; e0 += 32) {
         const int e = e0 + lane;
         unsigned long long p = 0;
         if (e < n) {
             const uint32_t gsl = sm.qgs[warp * kQueue + e];
             const int g = static_cast<int>(gsl >> 6), slot = static_cast<int>(gsl & 63u);
-            const float t = sv::exp_f32(__fsub_rn(__fmul_rn(sm.ql[warp * kQueue + e], r.invT), r.m));
-            float qv = sm.qq[warp * kQueue + e];  // q, or the raw draft logit (draft-logits mode)
-            if constexpr (kDL) qv = __fdiv_rn(sv::exp_f32(__fsub_rn(__fmul_rn(qv, r.invT), r.md)), r.Sd);
-            const float w = kRes ? __fmaf_rn(-r.S, qv, t) : t;
+            const float w = queue_weight<T, kRes, kDL>(r, sm, e);
             if (!kRes || w > 0.0f) {
                 const uint32_t wh = sm.ew[g];
                 const float E = group_emin_word(wh);
@@ -1285,7 +1442,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             l[k][h] = kPen && in ? pen_apply(r.pr, raw, v) : raw;
             qv[k][h] = 0.0f;
             if constexpr (kRes && kDL) qv[k][h] = in ? Elem<T>::at(r.dlrow, v) : 0.0f;
-            else if constexpr (kRes) qv[k][h] = in ? __ldg(r.qrow + v) : 0.0f;
+            else if constexpr (kRes) qv[k][h] = in ? sv_ldg(r.qrow + v) : 0.0f;
         }
     }
     const float inv_sd = kDL ? __frcp_rz(r.Sd) * (1.0f - 0x1p-12f) : 0.0f;  // <= 1 / S_d
@@ -1295,7 +1452,7 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
     for (int k = 0; k < B; ++k) {
         const int g = gs[k];
         if (g < 0) continue;
-        const float inv = inv_emin_bound(sm.ew[g]);
+        const float inv = inv_emin_bound(head_uniform_ub(sm.ew[g], r.f64));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int v = g * kGroup + 2 * lane + h;
@@ -1340,7 +1497,8 @@ __device__ __forceinline__ int bound_bin(unsigned kb, float top, float inv_w)
 }
 
 // Best-first race over one row by the whole CTA. Returns the packed winner (key, ~v), 0 when no
-// token is a candidate. lm must hold the row's line maxima (it is overwritten).
+// token is a candidate (binary64 races: the winner's key rounded down to binary32). lm must
+// hold the row's line maxima (it is overwritten).
 template <typename T, bool kRes, bool kDL, bool kPen>
 __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &rl,
                                           const SearchSmem &sm)
@@ -1352,6 +1510,10 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
         *sm.best = 0;
         *sm.cnt = 0;
         *sm.top = 0u;
+    }
+    if (lane == 0) {
+        sm.wbk[warp] = 0ull;
+        sm.wbv[warp] = INT_MAX;
     }
     if (tid < kBins) {
         sm.bin_n[tid] = 0;
@@ -1448,6 +1610,18 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
         if (done) break;
     }
     __syncthreads();
+    if (r.f64) {  // the exact winner over the warps' binary64 bests
+        unsigned long long kb = 0ull;
+        int kv = INT_MAX;
+        for (int w = 0; w < kWarps; ++w)
+            if (sm.wbk[w] > kb || (sm.wbk[w] == kb && kb != 0ull && sm.wbv[w] < kv)) {
+                kb = sm.wbk[w];
+                kv = sm.wbv[w];
+            }
+        __syncthreads();  // every thread has read wbk / wbv before a next race resets them
+        return kb ? pack_key(__double2float_rd(__longlong_as_double(static_cast<long long>(kb - 1ull))), kv)
+                  : 0ull;
+    }
     return *sm.best;
 }
 
@@ -1465,7 +1639,7 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
     s = 0.0f;
     idx = INT_MAX;
     for (int k = lane; k < nseg * kWarps; k += 32) {
-        const float4 raw = __ldg(reinterpret_cast<const float4 *>(part) +
+        const float4 raw = sv_ldg(reinterpret_cast<const float4 *>(part) +
                                  static_cast<size_t>(row) * maxseg * kWarps + k);
         combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
     }
@@ -1504,14 +1678,16 @@ struct SelectParams {
     Divisor chunk;
     float *sel_tau;  // [rows] threshold of each constrained row
     float *sel_S;    // [rows] its kept mass: the normaliser of p'
+    int lmx_cap;     // line maxima the dynamic shared memory holds after the pools
+    unsigned *flags; // the call's error word pair
 };
 
 // Does request i sample under constraints? (k, P as given; greedy requests never do.)
 __device__ __forceinline__ bool sel_active(const int32_t *top_k, const float *top_p, int i, int V,
                                            bool greedy, int &k, float &P)
 {
-    k = top_k ? __ldg(top_k + i) : 0;
-    P = top_p ? __ldg(top_p + i) : 1.0f;
+    k = top_k ? sv_ldg(top_k + i) : 0;
+    P = top_p ? sv_ldg(top_p + i) : 1.0f;
     return !greedy && ((k >= 1 && k < V) || P < 1.0f);
 }
 
@@ -1563,6 +1739,13 @@ struct SelSmem {
         return c;
     }
     __device__ __forceinline__ float *pool_b() const { return pool_a() + kSelPool; }
+    // the row's line maxima in x units (rows read by lines only), after the pools, then the
+    // warps' vector queues (kWarps x kSelQueue) after lmx_cap of them
+    __device__ __forceinline__ float *lmx() const { return pool_b() + kSelPool; }
+    __device__ __forceinline__ uint32_t *wq(int lmx_cap) const
+    {
+        return reinterpret_cast<uint32_t *>(lmx() + lmx_cap);
+    }
     uint32_t wc[kWarps];
     float wm[kWarps];
     uint32_t kmin, kmax, n;
@@ -1593,7 +1776,7 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
     const int lane = threadIdx.x & 31;
     const bool pen = kPen && pr.f != 0.0f;
     const bool al = pen && (reinterpret_cast<uintptr_t>(pr.cnt + head) & 15u) == 0u;
-    const int pv = pen && lane < pr.nprev ? __ldg(pr.prev + lane) : -1;
+    const int pv = pen && lane < pr.nprev ? sv_ldg(pr.prev + lane) : -1;
     for (int u0 = threadIdx.x; (u0 & ~31) < nvec; u0 += kIn * kThreads) {
         uint4 w[kIn];
         int4 cv[kIn][kCV];
@@ -1606,7 +1789,7 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
 #pragma unroll
                 for (int g = 0; g < kCV; ++g)
                     cv[q][g] = al && u < nvec
-                                   ? __ldg(reinterpret_cast<const int4 *>(pr.cnt + head + u * kEV) + g)
+                                   ? sv_ldg(reinterpret_cast<const int4 *>(pr.cnt + head + u * kEV) + g)
                                    : make_int4(0, 0, 0, 0);
                 const int wlo = head + ((u0 & ~31) + q * kThreads) * kEV;  // the warp's window
                 scan[q] = pen && (pr.nprev > 32 ||
@@ -1632,11 +1815,11 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < kEV; ++e) cnt[e] = pen ? __ldg(pr.cnt + v0 + e) : 0;
+                    for (int e = 0; e < kEV; ++e) cnt[e] = pen ? sv_ldg(pr.cnt + v0 + e) : 0;
                 }
                 if (scan[q])
                     for (int g = 0; g < pr.nprev; ++g) {
-                        const int d = __ldg(pr.prev + g) - v0;
+                        const int d = sv_ldg(pr.prev + g) - v0;
 #pragma unroll
                         for (int e = 0; e < kEV; ++e) cnt[e] += d == e;
                     }
@@ -1665,6 +1848,207 @@ __device__ __forceinline__ void sel_for_row(const T *__restrict__ rp, int V, flo
 constexpr size_t kSelDynSmem =
     (static_cast<size_t>(kWarps) * kSelBins + static_cast<size_t>(kSel1Copies) * kSelBins1 +
      2 * kSelPool) * 4;
+
+// Every element of a row whose x = fl(l * invT) can reach xmin, as (x, token), reading only the
+// 64-element lines whose largest x (lmx[k], from the statistics pass's line maxima) reaches
+// xmin and, inside them, only the 16-byte vectors whose largest x does: x is monotone in l, so
+// a vector's largest x is fl(vector max * invT) and a line's is lmx. The vectors that pass are
+// queued per warp (their index in wq, their data in wqd: kSelQueue entries per warp, in shared
+// memory) and processed 32 at a time, one per lane, so that the few that pass do not each hold
+// a mostly idle warp through their elements. The loads of a step are issued before the step
+// before it is processed (two register buffers in rotation). Elements below xmin may still be
+// passed (callers test x); the partial first and last lines of the row go element by element.
+// f takes no warp-wide step.
+constexpr int kSelQueue = 64;
+constexpr int kSelUnroll = 2;  // vectors per lane and buffer
+static_assert(kWarps * kSelQueue * 16 == kSelPool * 4, "the queued vectors' data fills pool_b");
+
+template <typename T>
+struct RowSteps {  // the whole lines of a row, in steps of kWarps * kLPW * kSelUnroll lines
+    static constexpr int kEV = 16 / static_cast<int>(sizeof(T));  // elements per vector
+    static constexpr int kVPL = kGroup / kEV;                      // vectors per line
+    static constexpr int kLPW = 32 / kVPL;                         // lines per warp and unit
+    static constexpr int kStep = kWarps * kLPW * kSelUnroll;       // lines per CTA step
+    const char *base;  // line kf's first byte
+    int nfull, kf, tok0, sub, lsub;
+    __device__ __forceinline__ RowSteps(const T *rp, const RowLines &rl)
+    {
+        nfull = max(0, rl.kl - rl.kf + 1);
+        kf = rl.kf;
+        tok0 = static_cast<int>((rl.L0 + rl.kf) * kGroup - rl.P0);
+        base = reinterpret_cast<const char *>(rp + tok0);
+        sub = (threadIdx.x & 31) % kVPL;
+        lsub = (threadIdx.x & 31) / kVPL;
+    }
+    // line of unit u of the step starting at lb (lb uniform over the warp)
+    __device__ __forceinline__ int line(int lb, int u) const { return lb + u * kWarps * kLPW + lsub; }
+    // issue the loads of the step at lb: vectors of lines whose maximum reaches xmin
+    __device__ __forceinline__ void load(int lb, const float *lmx, float xmin, uint4 (&w)[kSelUnroll],
+                                         bool (&act)[kSelUnroll]) const
+    {
+#pragma unroll
+        for (int u = 0; u < kSelUnroll; ++u) {
+            const int ln = line(lb, u);
+            act[u] = ln < nfull && lmx[kf + ln] >= xmin;
+            w[u] = act[u] ? ldg_v4(base + (static_cast<size_t>(ln) * kVPL + sub) * 16)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+};
+
+// The partial first (warp 0) and last (warp 1) lines of a row, element by element.
+template <typename T, typename F>
+__device__ __forceinline__ void sel_partial_lines(const T *__restrict__ rp, int V, float invT,
+                                                  const RowLines &rl, const float *lmx, float xmin,
+                                                  F &&f)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int k = -1;
+    if (warp == 0 && rl.kf == 1) k = 0;
+    if (warp == 1 && rl.kl == rl.nl - 2 && (rl.nl > 1 || rl.kf == 0)) k = rl.nl - 1;
+    if (k >= 0 && lmx[k] >= xmin) {
+        const long long p = (rl.L0 + k) * kGroup;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const long long v = p + h * 32 + lane - rl.P0;
+            if (v >= 0 && v < V) f(__fmul_rn(Elem<T>::at(rp, static_cast<size_t>(v)), invT), static_cast<int>(v));
+        }
+    }
+}
+
+template <typename T, typename F>
+__device__ __forceinline__ void sel_for_row_lines(const T *__restrict__ rp, int V, float invT,
+                                                  const RowLines &rl, const float *lmx, float xmin,
+                                                  uint32_t *wq, uint4 *wqd, F &&f)
+{
+    using RS = RowSteps<T>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    sel_partial_lines<T>(rp, V, invT, rl, lmx, xmin, [&](float x, int v) {
+        if (x >= xmin) f(x, v);
+    });
+    const RS rs(rp, rl);
+    uint32_t *q = wq + warp * kSelQueue;
+    uint4 *qd = wqd + warp * kSelQueue;
+    int qn = 0;
+    auto elems = [&](const uint4 &w, uint32_t vi) {  // the elements of vector vi (from line kf)
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const int v0 = rs.tok0 + static_cast<int>(vi) * RS::kEV;
+#pragma unroll
+        for (int e = 0; e < RS::kEV; ++e) {
+            float l;
+            if constexpr (sizeof(T) == 2)
+                l = __uint_as_float((e & 1) ? (ws[e >> 1] & 0xFFFF0000u) : (ws[e >> 1] << 16));
+            else
+                l = __uint_as_float(ws[e]);
+            const float x = __fmul_rn(l, invT);
+            if (x >= xmin) f(x, v0 + e);
+        }
+    };
+    // queue the vectors of a loaded step that can reach xmin; process 32 of them whenever 32 wait
+    auto step = [&](int lb, const uint4 (&w)[kSelUnroll], const bool (&act)[kSelUnroll]) {
+#pragma unroll
+        for (int u = 0; u < kSelUnroll; ++u) {
+            const bool pass = act[u] && __fmul_rn(VecMax<T>::value(VecMax<T>::of(w[u])), invT) >= xmin;
+            const unsigned msk = __ballot_sync(0xFFFFFFFFu, pass);
+            if (pass) {
+                const int at = qn + __popc(msk & ((1u << lane) - 1u));
+                q[at] = static_cast<uint32_t>(rs.line(lb, u) * RS::kVPL + rs.sub);
+                qd[at] = w[u];
+            }
+            qn += __popc(msk);
+            if (qn >= 32) {  // the last 32 queued vectors, one per lane
+                __syncwarp();
+                elems(qd[qn - 32 + lane], q[qn - 32 + lane]);
+                qn -= 32;
+                __syncwarp();
+            }
+        }
+    };
+    uint4 wa[kSelUnroll], wb[kSelUnroll];
+    bool aa[kSelUnroll], ab[kSelUnroll];
+    int lb = warp * RS::kLPW;  // uniform over the warp
+    rs.load(lb, lmx, xmin, wa, aa);
+    while (lb < rs.nfull) {
+        rs.load(lb + RS::kStep, lmx, xmin, wb, ab);
+        step(lb, wa, aa);
+        lb += RS::kStep;
+        if (lb >= rs.nfull) break;
+        rs.load(lb + RS::kStep, lmx, xmin, wa, aa);
+        step(lb, wb, ab);
+        lb += RS::kStep;
+    }
+    __syncwarp();
+    if (lane < qn) elems(qd[lane], q[lane]);
+    __syncwarp();
+}
+
+// Level-1 counts (into `cnt`, one shared atomic per token) of a row's tokens with x >= xmin, read
+// as sel_for_row_lines reads them (lines and vectors that cannot reach xmin are skipped, loads a
+// step ahead), with the per-token work cut down: x = fl(l * invT) and the bin's fl(m - x) * 64
+// (the value sel_bin1 clamps, so both passes bin every token alike) two tokens per packed
+// binary32 instruction. Vectors are processed where they were loaded (almost all of them are,
+// in this pass).
+template <typename T>
+__device__ __forceinline__ void sel_count_lines(const T *__restrict__ rp, int V, float invT, float m,
+                                                const RowLines &rl, const float *lmx, float xmin,
+                                                uint32_t *cnt)
+{
+    using RS = RowSteps<T>;
+    sel_partial_lines<T>(rp, V, invT, rl, lmx, xmin, [&](float x, int) {
+        if (x >= xmin) atomicAdd(cnt + sel_bin1(x, m), 1u);
+    });
+    const RS rs(rp, rl);
+    const int warp = threadIdx.x >> 5;
+    const unsigned long long ninv2 = f2_pack(-invT, -invT), m2 = f2_pack(m, m);
+    const unsigned long long s2 = f2_pack(kSelBinsPerNat, kSelBinsPerNat);
+    const float nxmin = -xmin;
+    auto step = [&](const uint4 (&w)[kSelUnroll], const bool (&act)[kSelUnroll]) {
+#pragma unroll
+        for (int u = 0; u < kSelUnroll; ++u) {
+            if (!act[u]) continue;
+            if (!(__fmul_rn(VecMax<T>::value(VecMax<T>::of(w[u])), invT) >= xmin)) continue;
+            const uint32_t ws[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+            for (int q = 0; q < RS::kEV / 2; ++q) {
+                unsigned long long l2;
+                if constexpr (sizeof(T) == 2)
+                    l2 = f2_pack(__uint_as_float(ws[q] << 16), __uint_as_float(ws[q] & 0xFFFF0000u));
+                else
+                    l2 = f2_pack(__uint_as_float(ws[2 * q]), __uint_as_float(ws[2 * q + 1]));
+                const unsigned long long nx2 = f2_mul(l2, ninv2);           // -x = fl(l * -invT)
+                const unsigned long long u2 = f2_mul(f2_add(m2, nx2), s2);  // fl(m - x) * 64
+                float nx0, nx1, u0, u1;
+                f2_unpack(nx2, nx0, nx1);
+                f2_unpack(u2, u0, u1);
+                // x >= xmin (false for NaN); the bin as sel_bin1 clamps and truncates it
+                if (nx0 <= nxmin)
+                    atomicAdd(cnt + (__float_as_int(__fadd_rz(fmaxf(fminf(u0, static_cast<float>(kSelBins1 - 1)), 0.0f), 8388608.0f)) - 0x4B000000), 1u);
+                if (nx1 <= nxmin)
+                    atomicAdd(cnt + (__float_as_int(__fadd_rz(fmaxf(fminf(u1, static_cast<float>(kSelBins1 - 1)), 0.0f), 8388608.0f)) - 0x4B000000), 1u);
+            }
+        }
+    };
+    uint4 wa[kSelUnroll], wb[kSelUnroll];
+    bool aa[kSelUnroll], ab[kSelUnroll];
+    int lb = warp * RS::kLPW;
+    rs.load(lb, lmx, xmin, wa, aa);
+    while (lb < rs.nfull) {
+        rs.load(lb + RS::kStep, lmx, xmin, wb, ab);
+        step(wa, aa);
+        lb += RS::kStep;
+        if (lb >= rs.nfull) break;
+        rs.load(lb + RS::kStep, lmx, xmin, wa, aa);
+        step(wb, ab);
+        lb += RS::kStep;
+    }
+}
+
+// The smallest x that can lie in level-1 bins 0 .. b (one bin of slack against the rounding of
+// sel_bin1); -inf for the last bins, which take everything below.
+__device__ __forceinline__ float sel_bin1_floor(int b, float m)
+{
+    return b < kSelBins1 - 2 ? __fsub_rn(m, static_cast<float>(b + 2) * (1.0f / kSelBinsPerNat)) : -kInf;
+}
 
 __device__ __forceinline__ void sel_clear(SelSmem &sm, int nbins)
 {
@@ -1880,19 +2264,25 @@ __device__ __forceinline__ int sel_shift(uint32_t klo, uint32_t khi)
     return bits > 8 ? bits - 8 : 0;
 }
 
-// Resolve the crossing among the candidates: the row's tokens with x >= xmin in level-1 bin b1,
+// Resolve the crossing among the candidates (each(xmin_hint, f) passes the row's tokens, at least
+// those with x >= xmin_hint, to f): the row's tokens with x >= xmin in level-1 bins b1 .. b1hi,
 // with ca / ma tokens strictly above them (ca in mode 0, ma in mode 1). The first pass collects
 // them into shared memory, counting them and taking their key range (and the mass of the tokens
 // in the bins above b1 with x >= xmin, returned in above_mass); only if they do not fit are finer
 // levels taken over the row first. Returns x*, the single value where the goal crosses, with
 // ca / ma counting / weighing the tokens strictly above x*, inbin_above the mass of the
 // candidates strictly above x* (mode 0) and gmass the mass of its group (all tokens equal x*).
-template <typename T, bool kPen>
-__device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float m,
-                             const PenRow &pr, int b1, int b1hi, float xmin, int mode, uint32_t k,
-                             float target, uint32_t &ca, float &ma, float &above_mass,
-                             float &inbin_above, float &gmass)
+template <typename Each>
+__device__ float sel_resolve(SelSmem &sm, Each &&each, float m, int b1, int b1hi, float xmin,
+                             int mode, uint32_t k, float target, uint32_t &ca, float &ma,
+                             float &above_mass, float &inbin_above, float &gmass, bool &gave_up)
 {
+    // each pass below narrows a window of 32-bit keys at least 128-fold, so a handful of passes
+    // always suffice; the limits only turn a defect into a reported error instead of a hang
+    constexpr int kMaxRowPasses = 8, kMaxPoolPasses = 8;
+    gave_up = false;
+    // every token these passes use lies in bins <= b1hi with x >= xmin
+    const float hint = fmaxf(xmin, sel_bin1_floor(b1hi, m));
     auto in_set = [&](float x, uint32_t klo, uint32_t khi) {
         const uint32_t kv = ord_key(x);
         const int bx = sel_bin1(x, m);
@@ -1901,13 +2291,18 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
     uint32_t klo = 0u, khi = 0xFFFFFFFFu, n = 0u;
     bool first = true, big = false;
     inbin_above = 0.0f;
-    for (;;) {
+    for (int pass = 0;; ++pass) {
+        if (pass == kMaxRowPasses) {
+            gave_up = true;
+            gmass = 0.0f;
+            return -kInf;
+        }
         if (big && klo < khi) {
             // too many for shared memory: one finer level over the row
             const int sh = sel_shift(klo, khi);
             sel_clear(sm, kSelBins);
             __syncthreads();
-            sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+            each(hint, [&](float x, int) {
                 if (in_set(x, klo, khi)) sel_add(sm, mode, sel_sub(ord_key(x), khi, sh), sel_mass(x, m));
             });
             __syncthreads();
@@ -1917,7 +2312,7 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
             if (mode == 0) {  // the mass of the candidates left above (counts were kept)
                 float a = 0.0f;
                 const uint32_t nh = khi;
-                sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+                each(hint, [&](float x, int) {
                     if (in_set(x, olo, ohi) && ord_key(x) > nh) a += sel_mass(x, m);
                 });
                 inbin_above += sel_block_sum(sm, a);
@@ -1932,7 +2327,7 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         __syncthreads();
         uint32_t lo = 0xFFFFFFFFu, hi = 0u;
         float am = 0.0f;
-        sel_for_row<T, kPen>(rp, V, invT, pr, [&](float x, int) {
+        each(hint, [&](float x, int) {
             const int bx = sel_bin1(x, m);
             if (bx > b1hi || !(x >= xmin)) return;
             if (bx < b1) {
@@ -1968,7 +2363,12 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
         }
     }
     // in shared memory: one finer level at a time down to a single value
-    for (;;) {
+    for (int pass = 0;; ++pass) {
+        if (pass == kMaxPoolPasses) {
+            gave_up = true;
+            gmass = 0.0f;
+            return -kInf;
+        }
         if (threadIdx.x == 0) {
             sm.kmin = 0xFFFFFFFFu;
             sm.kmax = 0u;
@@ -2019,10 +2419,146 @@ __device__ float sel_resolve(SelSmem &sm, const T *rp, int V, float invT, float 
     return xs;
 }
 
-// The threshold and the kept mass of every constrained row: one CTA per logit row.
+// A lower bound of a row's threshold from its line maxima (lmx[0 .. nl), x units): mode 0
+// (top-k): every token below the returned value has at least k line maxima, distinct tokens,
+// above it; mode 1 (top-p): every token below it has line maxima of at least `target` mass above
+// it (masses bounded from below by their 1/64-nat level-1 bin). The line maxima are counted into
+// level-1 bins (copy 0 of the level-1 counts), the first bin whose cumulative count / mass bound
+// reaches the goal is found, and the bound is the smallest line maximum in that bin or above.
+// -inf when the line maxima alone never reach the goal (e.g. rows flat within their lines).
+// Mode 2 (top-p, `target` = the mass (1 - P) Z that may lie below the kept set): y_e = m - e / 64
+// for the smallest bin edge e whose upper bound of the mass of all tokens at or below y_e,
+//   64 [ sum over lines in bins b >= e of e^(-b/64) + (lines in bins < e) e^(-e/64) ]
+// (each line has at most 64 tokens, none above its maximum), stays within `target`: every token
+// at or below y_e has at least Z - target = P Z of mass strictly above it, so it is dropped.
+// sel_line_bound's mode 2, after the line maxima are counted into cnt[0 .. kSelBins1).
+__device__ float sel_below_bound(SelSmem &sm, const uint32_t *cnt, float m, float budget, int per,
+                                 int lane, int warp, int b0)
+{
+    __shared__ int s_edge;
+    // this thread's bins: their counts and upper mass bounds (the last bin takes its lower edge)
+    float tc = 0.0f, tm = 0.0f;
+    for (int q = 0; q < per; ++q) {
+        const float c = static_cast<float>(cnt[b0 + q]);
+        tc += c;
+        tm += c * sv::ex2_approx(-static_cast<float>(b0 + q) * (kLog2e / kSelBinsPerNat));
+    }
+    float ic = tc, im = tm;  // inclusive prefix sums over the threads, in bin order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float yc = __shfl_up_sync(0xFFFFFFFFu, ic, o), ym = __shfl_up_sync(0xFFFFFFFFu, im, o);
+        if (lane >= o) {
+            ic += yc;
+            im += ym;
+        }
+    }
+    __shared__ float s_wc[kWarps], s_wm[kWarps];
+    if (lane == 31) {
+        s_wc[warp] = ic;
+        s_wm[warp] = im;
+    }
+    if (threadIdx.x == 0) s_edge = INT_MAX;
+    __syncthreads();
+    float call = 0.0f, mall = 0.0f, cbef = ic - tc, mbef = im - tm;
+    for (int w = 0; w < kWarps; ++w) {
+        call += s_wc[w];
+        mall += s_wm[w];
+        if (w < warp) {
+            cbef += s_wc[w];
+            mbef += s_wm[w];
+        }
+    }
+    // edge e = b0 + q: lines in bins < e counted in cb (before), the mass of bins >= e in ma
+    float cb = cbef, mb = mbef;
+    for (int q = 0; q < per; ++q) {
+        const int e = b0 + q;
+        const float ma = mall - mb;  // bins >= e
+        const float ub = 64.0f * (ma + cb * sv::ex2_approx(-static_cast<float>(e) * (kLog2e / kSelBinsPerNat))) *
+                         (1.0f + 0x1p-8f);  // margins for ex2 and the float sums
+        if (ub <= budget) {
+            atomicMin(&s_edge, e);
+            break;
+        }
+        const float c = static_cast<float>(cnt[e]);
+        cb += c;
+        mb += c * sv::ex2_approx(-static_cast<float>(e) * (kLog2e / kSelBinsPerNat));
+    }
+    __syncthreads();
+    const int e = s_edge;
+    __syncthreads();
+    // the edge value y_e = m - e / 64, rounded down (a smaller bound drops fewer tokens: safe)
+    return e != INT_MAX ? __fsub_rd(m, static_cast<float>(e) * (1.0f / kSelBinsPerNat)) : -kInf;
+}
+
+__device__ float sel_line_bound(SelSmem &sm, const float *lmx, int nl, float m, int mode,
+                                uint32_t k, float target)
+{
+    constexpr int per = kSelBins1 / kThreads;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, b0 = threadIdx.x * per;
+    uint32_t *cnt = sm.cnt1();
+    __shared__ int s_bin;
+    __shared__ uint32_t s_kmin;
+    for (int b = threadIdx.x; b < kSelBins1; b += kThreads) cnt[b] = 0u;
+    if (threadIdx.x == 0) {
+        s_bin = INT_MAX;
+        s_kmin = 0xFFFFFFFFu;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < nl; q += kThreads) {
+        const float x = lmx[q];
+        if (x == x) atomicAdd(cnt + sel_bin1(x, m), 1u);
+    }
+    __syncthreads();
+    if (mode == 2) return sel_below_bound(sm, cnt, m, target, per, lane, warp, b0);
+    auto value = [&](int b) {  // a bin's count, or a lower bound of its mass
+        const float c = static_cast<float>(cnt[b]);
+        if (mode == 0) return c;
+        if (b == kSelBins1 - 1) return 0.0f;
+        return c * sv::ex2_approx(-static_cast<float>(b + 1) * (kLog2e / kSelBinsPerNat)) *
+               (1.0f - 0x1p-10f);
+    };
+    float t = 0.0f;
+    for (int q = 0; q < per; ++q) t += value(b0 + q);
+    float incl = t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sm.wm[warp] = incl;
+    __syncthreads();
+    float c = incl - t;  // before this thread's first bin
+    for (int w = 0; w < warp; ++w) c += sm.wm[w];
+    const float goal = mode == 0 ? static_cast<float>(k) : target;
+    for (int q = 0; q < per; ++q) {
+        c += value(b0 + q);
+        if (c >= goal) {
+            atomicMin(&s_bin, b0 + q);
+            break;
+        }
+    }
+    __syncthreads();
+    const int bstar = s_bin;
+    if (bstar != INT_MAX)
+        for (int q = threadIdx.x; q < nl; q += kThreads) {
+            const float x = lmx[q];
+            if (x == x && sel_bin1(x, m) <= bstar) atomicMin(&s_kmin, ord_key(x));
+        }
+    __syncthreads();
+    const float out = bstar != INT_MAX ? key_value(s_kmin) : -kInf;
+    __syncthreads();
+    return out;
+}
+
+// The threshold and the kept mass of every constrained row: one CTA per logit row. Rows without a
+// penalty are read through their line maxima (sel_for_row_lines): a lower bound of the threshold
+// from the line maxima alone (sel_line_bound), then passes that read only the lines and vectors
+// that can reach the current bound. Penalised rows (whose line maxima are upper bounds, not
+// values of tokens) read every element.
 template <typename T, bool kPen>
 __global__ void __launch_bounds__(kThreads, kPen ? 2 : 4)
-sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectParams P)
+sv_select_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
+                 const __grid_constant__ SelectParams P)
 {
     __shared__ SelSmem sm;
     const int row = blockIdx.x, lane = threadIdx.x & 31;
@@ -2033,7 +2569,7 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     float Pp;
     if (!sel_active(P.top_k, P.top_p, i, P.V, greedy, k, Pp)) return;
     const bool use_k = k >= 1 && k < P.V, use_p = Pp < 1.0f;
-    const int q0 = __ldg(P.rq.cu + i);
+    const int q0 = sv_ldg(P.rq.cu + i);
     const PenRow pr = kPen ? pen_row(P.pen, P.draft_ids, i, q0, row - q0 - i, P.V)
                            : PenRow{0.0f, nullptr, nullptr, 0};
     const T *rp = logits + static_cast<size_t>(row) * P.V;
@@ -2043,42 +2579,99 @@ sv_select_kernel(const T *__restrict__ logits, const __grid_constant__ SelectPar
     combine_row(P.part, row, P.V, P.maxseg, P.base_off, P.chunk, invT * kLog2e, L, s0, idx);
     const float m = __fmul_rn(L, invT);
 
-    // level 1: counts per bin of 1/128 nat (integer atomics) of the tokens x >= xmin
+    // the row's line maxima in x units, for rows without a penalty (every row of the kernel
+    // without penalties: the host launches it with a line buffer of lmx_cap >= nl lines)
+    const RowLines rl = row_lines(row, P.V, P.base_off);
+    const bool by_lines = !kPen || (lines != nullptr && pr.f == 0.0f && rl.nl <= P.lmx_cap);
+    float *lmx = sm.lmx();
+    if (by_lines) {
+        row_line_max<T, false>(rp, P.V, rl, lines, lmx, PenRow{0.0f, nullptr, nullptr, 0});
+        __syncthreads();
+        for (int q = threadIdx.x; q < rl.nl; q += kThreads) lmx[q] = __fmul_rn(lmx[q], invT);
+        __syncthreads();
+    }
+    uint32_t *wq = sm.wq(P.lmx_cap);
+    // the queued vectors' data in pool_b, which the row passes leave unused (kWarps * kSelQueue
+    // 16-byte entries = kSelPool words)
+    uint4 *wqd = reinterpret_cast<uint4 *>(sm.pool_b());
+    auto each = [&](float xmin, auto &&f) {
+        if constexpr (kPen) {
+            if (!by_lines) {
+                sel_for_row<T, kPen>(rp, P.V, invT, pr, f);
+                return;
+            }
+        }
+        sel_for_row_lines<T>(rp, P.V, invT, rl, lmx, xmin, wq, wqd, f);
+    };
+
+    // level 1: counts per bin of 1/64 nat (integer atomics) of the tokens x >= xmin
     auto count_level1 = [&](float xmin) {
         for (int b = threadIdx.x; b < kSel1Copies * kSelBins1; b += kThreads) sm.cnt1()[b] = 0u;
         __syncthreads();
         uint32_t *mine = sm.cnt1() + (threadIdx.x >> 7) * kSelBins1;  // four warps per copy
-        sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
-            if (x >= xmin) atomicAdd(mine + sel_bin1(x, m), 1u);
-        });
+        bool done = false;
+        if constexpr (kPen) {
+            if (!by_lines) {
+                sel_for_row<T, kPen>(rp, P.V, invT, pr, [&](float x, int) {
+                    if (x >= xmin) atomicAdd(mine + sel_bin1(x, m), 1u);
+                });
+                done = true;
+            }
+        }
+        if (!done) sel_count_lines<T>(rp, P.V, invT, m, rl, lmx, xmin, mine);
         __syncthreads();
     };
     float tau = -kInf, Z = s0, Sk = s0;  // Z: the mass of the top-k set, or of the row
-    if (use_k) {
-        count_level1(-kInf);
-        uint32_t ca = 0u;
-        float ma = 0.0f, above, inbin, gm;
-        const int bk = sel_cross(sm, kSelBins1, 0, static_cast<uint32_t>(k), 0.0f, ca, ma);
-        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, bk, bk, -kInf, 0,
-                                   static_cast<uint32_t>(k), 0.0f, ca, ma, above, inbin, gm);
-        Z = above + (inbin + gm);  // the bins above bk, then bk's tokens at or above tau_k
-        Sk = Z;
-    }
-    if (use_p) {
+    bool failed = false;
+    // phase 0: top-k (its threshold, and Z = the mass of the kept set); phase 1: top-p within it.
+    // One loop, so that the selection's code (sel_resolve with its row passes) exists once.
+    for (int phase = use_k ? 0 : 1; phase <= (use_p ? 1 : 0); ++phase) {
         const float tk = tau;
-        count_level1(tk);  // over the top-k set (every token without top-k)
         const float target = __fmul_rn(fmaxf(Pp, 1e-6f), Z);
-        int blo, bhi;
-        sel_bounds(sm, target, blo, bhi);
+        float xmin;
+        if (phase == 0) {
+            // the k-th largest token is at least the bound from the line maxima
+            xmin = by_lines ? sel_line_bound(sm, lmx, rl.nl, m, 0, static_cast<uint32_t>(k), 0.0f) : -kInf;
+        } else {
+            // within a top-k set every kept token is at least tau_k; without one, bounds from the
+            // line maxima (a lower bound of the mass above, an upper bound of the mass below)
+            xmin = tk;
+            if (!use_k && by_lines) {
+                const float budget = __fmul_rd(__fmul_rd(__fsub_rd(1.0f, fmaxf(Pp, 1e-6f)), Z), 1.0f - 0x1p-10f);
+                xmin = fmaxf(sel_line_bound(sm, lmx, rl.nl, m, 1, 0u, target),
+                             sel_line_bound(sm, lmx, rl.nl, m, 2, 0u, budget));
+            }
+        }
+        count_level1(xmin);
         uint32_t ca = 0u;
         float ma = 0.0f, above, inbin, gm;
-        tau = sel_resolve<T, kPen>(sm, rp, P.V, invT, m, pr, blo, bhi, tk, 1, 0u, target, ca, ma,
-                                   above, inbin, gm);
-        Sk = ma + gm;
+        int blo, bhi;
+        if (phase == 0) {
+            blo = bhi = sel_cross(sm, kSelBins1, 0, static_cast<uint32_t>(k), 0.0f, ca, ma);
+        } else {
+            sel_bounds(sm, target, blo, bhi);
+        }
+        bool gave_up;
+        const float t = sel_resolve(sm, each, m, blo, bhi, phase == 0 ? xmin : fmaxf(tk, xmin), phase,
+                                    phase == 0 ? static_cast<uint32_t>(k) : 0u, phase == 0 ? 0.0f : target,
+                                    ca, ma, above, inbin, gm, gave_up);
+        tau = t;
+        if (phase == 0) {
+            Z = above + (inbin + gm);  // the bins above bk, then bk's tokens at or above tau_k
+            Sk = Z;
+        } else {
+            Sk = ma + gm;
+        }
+        if (gave_up) failed = true;
+    }
+    if (failed) {  // (never expected) the row is left unconstrained and the call reports it
+        tau = -kInf;
+        Sk = s0;
+        if (threadIdx.x == 0) atomicOr(P.flags + 1, SV_ERR_SELECT);
     }
     if (threadIdx.x == 0) {
-        P.sel_tau[row] = tau;
-        P.sel_S[row] = Sk;
+        sv_st(P.sel_tau + row, tau);
+        sv_st(P.sel_S + row, Sk);
     }
 }
 
@@ -2097,7 +2690,7 @@ sv_shard_export_kernel(const T *__restrict__ logits, RequestTable rq,
     const int row = static_cast<int>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
     if (row >= R) return;  // whole warps
     const int i = row_request(rq.cu, rq.n, row, lane);
-    const int q0 = __ldg(rq.cu + i), K = __ldg(rq.cu + i + 1) - q0, j = row - q0 - i;
+    const int q0 = sv_ldg(rq.cu + i), K = sv_ldg(rq.cu + i + 1) - q0, j = row - q0 - i;
     bool greedy;
     const float invT = request_invT(rq, i, greedy);
     float L, sx;
@@ -2112,13 +2705,13 @@ sv_shard_export_kernel(const T *__restrict__ logits, RequestTable rq,
         rec.draft_prob = __int_as_float(0x7FC00000);
         rec.reserved = 0;
         if (j >= 0 && j < K && q0 + j < R - rq.n) {  // (a malformed cu_num_draft reads nothing)
-            const int d = __ldg(draft_ids + q0 + j);
+            const int d = sv_ldg(draft_ids + q0 + j);
             if (d >= v0 && d < v0 + Vs) {
                 rec.draft_logit = Elem<T>::at(logits + static_cast<size_t>(row) * Vs, d - v0);
-                rec.draft_prob = q ? __ldg(q + static_cast<size_t>(q0 + j) * Vs + (d - v0)) : 1.0f;
+                rec.draft_prob = q ? sv_ldg(q + static_cast<size_t>(q0 + j) * Vs + (d - v0)) : 1.0f;
             }
         }
-        out[row] = rec;
+        sv_st(out + row, rec);
     }
 }
 
@@ -2150,23 +2743,25 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     __shared__ unsigned s_top;
     __shared__ uint32_t s_qgs[kWarps * kQueue];
     __shared__ float s_ql[kWarps * kQueue], s_qq[kWarps * kQueue];
+    __shared__ unsigned long long s_wbk[kWarps];
+    __shared__ int s_wbv[kWarps];
     const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int q0 = __ldg(P.rq.cu + i), K = __ldg(P.rq.cu + i + 1) - q0;
+    const int q0 = sv_ldg(P.rq.cu + i), K = sv_ldg(P.rq.cu + i + 1) - q0;
     const VerifyLayout lay = verify_layout(P.Vs, P.kmax);
     {  // the batch must be consistent (as in the verify kernel); otherwise j* = -1: nothing emitted
         const int n = P.rq.n, nd = P.R - n;
         int bad = 0;
         for (int t = tid; t <= n; t += kThreads) {
-            const int c0 = __ldg(P.rq.cu + t);
+            const int c0 = sv_ldg(P.rq.cu + t);
             if (t == 0) bad |= c0 != 0;
             if (t == n) bad |= c0 != nd;
             if (t < n) {
-                const int c1 = __ldg(P.rq.cu + t + 1);
+                const int c1 = sv_ldg(P.rq.cu + t + 1);
                 bad |= (c1 < c0) | (static_cast<long long>(c1) - c0 > P.kmax) | (c0 < 0) | (c1 > nd);
             }
         }
         if (__syncthreads_or(bad)) {
-            if (tid == 0) P.out[i] = spec_verify_shard_key{-1, -1, 0.0f, -1, 0.0f, -1};
+            if (tid == 0) sv_st(P.out + i, spec_verify_shard_key{-1, -1, 0.0f, -1, 0.0f, -1});
             return;
         }
     }
@@ -2184,7 +2779,7 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
         float L = -kInf, sx = 0.0f, ld = __int_as_float(0x7FC00000), qd = ld;
         int idx = INT_MAX;
         for (int r = lane; r < P.world; r += 32) {
-            const spec_verify_shard_stat rec = P.recs[static_cast<size_t>(r) * P.R + row];
+            const spec_verify_shard_stat rec = sv_ld(P.recs + static_cast<size_t>(r) * P.R + row);
             combine_stat(L, sx, idx, rec.max_logit, rec.sumexp, rec.argmax, c);
             if (rec.draft_logit == rec.draft_logit) {
                 ld = rec.draft_logit;
@@ -2205,7 +2800,7 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             sm_S[j] = sx;
             sm_amax[j] = amax;
             if (j < K) {
-                const int d = __ldg(P.draft_ids + q0 + j);
+                const int d = sv_ldg(P.draft_ids + q0 + j);
                 bool acc;
                 if (greedy) {
                     acc = d == amax;  // [spec-notes] 8.3
@@ -2253,6 +2848,7 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
         r.tau = -kInf;
         r.qrow = nullptr;
         r.excl = -1;
+        r.f64 = false;
         SearchSmem sm;
         sm.buf = reinterpret_cast<unsigned long long *>(dyn);
         sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
@@ -2267,11 +2863,13 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
         sm.ew = reinterpret_cast<uint32_t *>(dyn + lay.ew);
         sm.ag = dyn + lay.ag;
         sm.best = &s_best;
+        sm.wbk = s_wbk;
+        sm.wbv = s_wbv;
         sm.cnt = &s_cnt;
         const RowLines rl = row_lines(row, P.Vs, P.base_off);
         if (js < K) {  // the residual (with q) or the exclusion race (without) of this shard
             const bool residual = P.q != nullptr;
-            const int d = __ldg(P.draft_ids + q0 + js);
+            const int d = sv_ldg(P.draft_ids + q0 + js);
             r.qrow = residual ? P.q + static_cast<size_t>(q0 + js) * P.Vs : nullptr;
             r.excl = (!residual && d >= P.v0 && d < P.v0 + P.Vs) ? d - P.v0 : -1;
             row_line_max<T, false>(r.rp, P.Vs, rl, lines, sm.lm, r.pr);
@@ -2298,7 +2896,7 @@ sv_shard_race_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             }
         }
     }
-    if (tid == 0) P.out[i] = o;
+    if (tid == 0) sv_st(P.out + i, o);
 }
 
 // The winner over the shards and the emitted row of each request (one thread per request).
@@ -2311,14 +2909,14 @@ __global__ void sv_shard_finish_kernel(const spec_verify_shard_key *__restrict__
 {
     const int i = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
     if (i >= n) return;
-    const int q0 = __ldg(cu + i), K = __ldg(cu + i + 1) - q0;
-    const spec_verify_shard_key o0 = races[i];
+    const int q0 = sv_ldg(cu + i), K = sv_ldg(cu + i + 1) - q0;
+    const spec_verify_shard_key o0 = sv_ld(races + i);
     const int js = o0.jstar;
     const int stride = kmax + 1;
     if (js < 0 || js > K || K > kmax) {  // an inconsistent batch: nothing emitted
-        for (int s = 0; s < stride; ++s) sampled[static_cast<size_t>(i) * stride + s] = -1;
-        num_sampled[i] = 0;
-        num_rejected[i] = 0;
+        for (int s = 0; s < stride; ++s) sv_st(sampled + static_cast<size_t>(i) * stride + s, -1);
+        sv_st(num_sampled + i, 0);
+        sv_st(num_rejected + i, 0);
         return;
     }
     int token = o0.token;
@@ -2326,20 +2924,20 @@ __global__ void sv_shard_finish_kernel(const spec_verify_shard_key *__restrict__
         unsigned long long best = 0ull;
         if (js < K)
             for (int r = 0; r < world; ++r) {
-                const spec_verify_shard_key o = races[static_cast<size_t>(r) * n + i];
+                const spec_verify_shard_key o = sv_ld(races + static_cast<size_t>(r) * n + i);
                 if (o.residual_index >= 0) best = max(best, pack_key(o.residual_key, o.residual_index));
             }
         if (!best)
             for (int r = 0; r < world; ++r) {
-                const spec_verify_shard_key o = races[static_cast<size_t>(r) * n + i];
+                const spec_verify_shard_key o = sv_ld(races + static_cast<size_t>(r) * n + i);
                 if (o.p_index >= 0) best = max(best, pack_key(o.p_key, o.p_index));
             }
         token = best ? static_cast<int>(~static_cast<unsigned>(best)) : 0;
     }
     int32_t *out = sampled + static_cast<size_t>(i) * stride;
-    for (int s = 0; s < stride; ++s) out[s] = s < js ? __ldg(draft_ids + q0 + s) : (s == js ? token : -1);
-    num_sampled[i] = js + 1;
-    num_rejected[i] = K - js;
+    for (int s = 0; s < stride; ++s) sv_st(out + s, s < js ? sv_ldg(draft_ids + q0 + s) : (s == js ? token : -1));
+    sv_st(num_sampled + i, js + 1);
+    sv_st(num_rejected + i, K - js);
 }
 
 // One CTA per request. kDLMode: q comes from draft logits (P.dl); kPen: the batch has a
@@ -2358,6 +2956,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     __shared__ unsigned s_top;
     __shared__ uint32_t s_qgs[kWarps * kQueue];
     __shared__ float s_ql[kWarps * kQueue], s_qq[kWarps * kQueue];
+    __shared__ unsigned long long s_wbk[kWarps];
+    __shared__ int s_wbv[kWarps];
     const int i = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = P.rq.n;
@@ -2366,16 +2966,16 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     const VerifyLayout lay = verify_layout(P.V, P.kmax);
 
     // 0. the batch must be consistent; every CTA checks all of cu_num_draft (small, in L2)
-    const int q0 = __ldg(cu + i);
-    const int K = __ldg(cu + i + 1) - q0;
+    const int q0 = sv_ldg(cu + i);
+    const int K = sv_ldg(cu + i + 1) - q0;
     if (tid == 0) s_js = K;
     int bad = 0;
     for (int t = tid; t <= n; t += kThreads) {
-        const int c0 = __ldg(cu + t);
+        const int c0 = sv_ldg(cu + t);
         if (t == 0) bad |= c0 != 0;
         if (t == n) bad |= c0 != P.nd;
         if (t < n) {
-            const int c1 = __ldg(cu + t + 1);
+            const int c1 = sv_ldg(cu + t + 1);
             bad |= (c1 < c0) | (static_cast<long long>(c1) - c0 > P.kmax) | (c0 < 0) | (c1 > P.nd);
         }
     }
@@ -2389,7 +2989,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     bool greedy;
     const float invT = request_invT(P.rq, i, greedy);
     if (tid == 0 && pen_counts_row_bad(P.pen, i)) atomicOr(P.flags + 1, SV_ERR_COUNTS);
-    const bool partial = P.partial && __ldg(P.partial + i) != 0;  // no token: only row stats
+    const bool partial = P.partial && sv_ldg(P.partial + i) != 0;  // no token: only row stats
     const bool synthetic = P.nsyn > 0;
     const float c = invT * kLog2e;
     const uint32_t ireq = P.req_base + static_cast<uint32_t>(i);
@@ -2424,8 +3024,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
         }
         float tau = -kInf;
         if (constrained) {  // the kept set and its mass, from the select kernel
-            tau = __ldg(P.sel_tau + row);
-            s = __ldg(P.sel_S + row);
+            tau = sv_ldg(P.sel_tau + row);
+            s = sv_ldg(P.sel_S + row);
         }
         if (lane == 0) {
             sm_md[j] = md;
@@ -2436,9 +3036,9 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             sm_m[j] = m;
             sm_S[j] = s;
             sm_amax[j] = amax;
-            if (P.opt_max) P.opt_max[row] = m;
-            if (P.opt_sum) P.opt_sum[row] = s;
-            if (P.opt_amax) P.opt_amax[row] = amax;
+            if (P.opt_max) sv_st(P.opt_max + row, m);
+            if (P.opt_sum) sv_st(P.opt_sum + row, s);
+            if (P.opt_amax) sv_st(P.opt_amax + row, amax);
             if (j < K && !partial &&
                 !(synthetic ? accept_synthetic(P, j, q0 + j, ireq)
                             : accept_draft<T>(logits + rbase, P.V, greedy, j, q0 + j,
@@ -2477,6 +3077,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     r.ireq = ireq;
     r.k0 = static_cast<uint32_t>(P.seed);
     r.k1 = static_cast<uint32_t>(P.seed >> 32);
+    r.f64 = P.f64 != 0;
     // synthetic mode: the token at j* is the target's own draw from p, nothing excluded
     const bool residual = !synthetic && js < K && (P.q != nullptr || dl != nullptr);
     r.qrow = residual && P.q ? P.q + static_cast<size_t>(q0 + js) * P.V : nullptr;
@@ -2485,7 +3086,7 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     r.tau = sm_tau[js];
     r.md = js < K ? sm_md[js] : 0.0f;
     r.Sd = js < K ? sm_Sd[js] : 1.0f;
-    r.excl = (!synthetic && js < K && !residual) ? __ldg(P.draft_ids + q0 + js) : -1;
+    r.excl = (!synthetic && js < K && !residual) ? sv_ldg(P.draft_ids + q0 + js) : -1;
     SearchSmem sm;
     sm.buf = reinterpret_cast<unsigned long long *>(dyn);
     sm.tmp = reinterpret_cast<unsigned long long *>(dyn + lay.tmp);
@@ -2500,6 +3101,8 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
     sm.ew = reinterpret_cast<uint32_t *>(dyn + lay.ew);
     sm.ag = dyn + lay.ag;
     sm.best = &s_best;
+    sm.wbk = s_wbk;
+    sm.wbv = s_wbv;
     sm.cnt = &s_cnt;
     const RowLines rl = row_lines(row, P.V, P.base_off);
     row_line_max<T, kPen>(r.rp, P.V, rl, lines, sm.lm, r.pr);
@@ -2658,13 +3261,12 @@ template <typename T>
 cudaError_t setup_kernels(int device, int *stats_per_sm)
 {
     const int limit = static_cast<int>(verify_smem_limit(device));
+    // select: its fixed part and one row's line maxima; as much as a verify CTA may use
     cudaError_t es = cudaFuncSetAttribute(sv_select_kernel<T, false>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(kSelDynSmem));
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (es == cudaSuccess)
         es = cudaFuncSetAttribute(sv_select_kernel<T, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kSelDynSmem));
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (es == cudaSuccess)  // line maxima of the largest chunk, then the staging ring
         es = cudaFuncSetAttribute(sv_stats_kernel<T, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2704,6 +3306,47 @@ StatsArray<T> stats_array(const T *logits, long long total, long long chunk, int
     a.lines = lines;
     return a;
 }
+
+#ifdef SV_DEBUG_BOUNDS
+// The arrays one call may touch, registered in g_dbg (stream-ordered) before its launches. The
+// environment variable SV_DEBUG_SHRINK (bytes, default 0) leaves that many bytes of the end of
+// the first registered array (the logits) out, so that tests can check that the check fires
+// on memory the kernels may really read.
+struct DbgList {
+    DbgRanges r{};
+    void add(const void *p, size_t bytes)
+    {
+        if (!p || bytes == 0 || r.n >= kDbgRanges) return;
+        r.lo[r.n] = reinterpret_cast<unsigned long long>(p);
+        r.hi[r.n] = r.lo[r.n] + bytes;
+        r.n++;
+    }
+    int push(unsigned *flags, cudaStream_t stream)
+    {
+        r.flags = flags;
+        if (const char *e = getenv("SV_DEBUG_SHRINK")) {
+            const unsigned long long cut = strtoull(e, nullptr, 10);
+            if (r.n > 0 && r.hi[0] - r.lo[0] > cut) r.hi[0] -= cut;
+        }
+        return cudaMemcpyToSymbolAsync(g_dbg, &r, sizeof(r), 0, cudaMemcpyHostToDevice, stream) ==
+                       cudaSuccess ? SV_OK : SV_ECUDA;
+    }
+};
+
+// The context's own scratch.
+void dbg_add_ctx(DbgList &d, const spec_verify_ctx *ctx)
+{
+    const size_t rows = static_cast<size_t>(ctx->max_rows), seg = static_cast<size_t>(ctx->maxseg);
+    const size_t eb = ctx->dtype == SV_BF16 ? 2 : 4, V = static_cast<size_t>(ctx->V);
+    const size_t drows = static_cast<size_t>(ctx->max_num_reqs) * static_cast<size_t>(ctx->max_spec_len);
+    d.add(ctx->statpart, rows * seg * kWarps * sizeof(StatPart));
+    d.add(ctx->dpart, drows * seg * kWarps * sizeof(StatPart));
+    d.add(ctx->sel_tau, rows * 4);
+    d.add(ctx->sel_S, rows * 4);
+    d.add(ctx->lines, (rows * V + 2 * kGroup) / kGroup * eb);
+    d.add(ctx->flags, 2 * sizeof(unsigned));
+}
+#endif
 
 // Both launches of one call (arguments already checked).
 template <typename T>
@@ -2761,9 +3404,38 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     P.sel_tau = sel_on ? ctx->sel_tau : nullptr;
     P.sel_S = sel_on ? ctx->sel_S : nullptr;
     P.nsyn = ctx->nsyn;
+    P.f64 = b.fp64_gumbel != 0;
     for (int k = 0; k < SV_MAX_SYNTHETIC; ++k) P.syn[k] = k < ctx->nsyn ? ctx->syn[k] : 0.0f;
     const size_t smem = verify_smem_bytes(V, kmax);
 
+#ifdef SV_DEBUG_BOUNDS
+    {
+        const size_t n = static_cast<size_t>(num_reqs), R = static_cast<size_t>(rows);
+        const size_t Vz = static_cast<size_t>(V), ndz = static_cast<size_t>(nd);
+        DbgList d;
+        d.add(logits, R * Vz * sizeof(T));
+        d.add(b.draft_ids, ndz * 4);
+        d.add(b.draft_probs, ndz * Vz * 4);
+        d.add(b.draft_logits, ndz * Vz * sizeof(T));
+        d.add(cu, (n + 1) * 4);
+        d.add(b.temperature, n * 4);
+        d.add(b.is_greedy, n);
+        d.add(b.partial_prefill, n);
+        d.add(b.frequency_penalty, n * 4);
+        d.add(b.output_bin_counts, static_cast<size_t>(std::max(b.counts_rows, 0)) * Vz * 4);
+        d.add(b.counts_row, n * 4);
+        d.add(b.top_k, n * 4);
+        d.add(b.top_p, n * 4);
+        d.add(o.sampled, n * (static_cast<size_t>(kmax) + 1) * 4);
+        d.add(o.num_sampled, n * 4);
+        d.add(o.num_rejected, n * 4);
+        d.add(o.row_max, R * 4);
+        d.add(o.row_sumexp, R * 4);
+        d.add(o.row_argmax, R * 4);
+        dbg_add_ctx(d, ctx);
+        if (d.push(ctx->flags, stream) != SV_OK) return SV_ECUDA;
+    }
+#endif
     ProfSlot *slot = nullptr;
     if (ctx->prof) {
         slot = &ctx->ring[static_cast<size_t>(ctx->prof_calls % kProfRing)];
@@ -2779,6 +3451,7 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         sv_stats_kernel<T, false><<<A.grid + D.grid, kThreads, smem1, stream>>>(
             V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids, 0);
     if (slot) cudaEventRecord(slot->ev[1], stream);
+    if (sel_on && !lines) return SV_EINVAL;  // the selection reads rows through their line maxima
     if (sel_on) {  // top-k / top-p: the kept set of every constrained row
         SelectParams SP;
         SP.rq = rq;
@@ -2793,10 +3466,15 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         SP.chunk = P.chunk;
         SP.sel_tau = ctx->sel_tau;
         SP.sel_S = ctx->sel_S;
+        // the line maxima of one row (at most ceil(V / 64) + 1 lines) after the pools
+        SP.lmx_cap = ceil_div(V, kGroup) + 2;
+        SP.flags = ctx->flags;
+        const size_t sel_smem = kSelDynSmem + static_cast<size_t>(SP.lmx_cap) * 4 +
+                                static_cast<size_t>(kWarps) * kSelQueue * 4;
         if (pen_on)
-            sv_select_kernel<T, true><<<rows, kThreads, kSelDynSmem, stream>>>(logits, SP);
+            sv_select_kernel<T, true><<<rows, kThreads, sel_smem, stream>>>(logits, lines, SP);
         else
-            sv_select_kernel<T, false><<<rows, kThreads, kSelDynSmem, stream>>>(logits, SP);
+            sv_select_kernel<T, false><<<rows, kThreads, sel_smem, stream>>>(logits, lines, SP);
     }
     if (slot) cudaEventRecord(slot->ev[2], stream);
     auto verify = dl ? (pen_on ? sv_verify_kernel<T, true, true> : sv_verify_kernel<T, true, false>)
@@ -3022,6 +3700,22 @@ int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int 
     const RequestTable rq{cu_num_draft, temperature, is_greedy, nullptr, num_reqs};
     const long long total = static_cast<long long>(R) * Vs;
     const long long chunk1 = stats_chunk_for(ctx, total);
+#ifdef SV_DEBUG_BOUNDS
+    {
+        const size_t n = static_cast<size_t>(num_reqs), Rz = static_cast<size_t>(R);
+        const size_t eb = ctx->dtype == SV_BF16 ? 2 : 4, ndz = static_cast<size_t>(num_draft_tokens);
+        DbgList d;
+        d.add(logits_shard, Rz * static_cast<size_t>(Vs) * eb);
+        d.add(draft_ids, ndz * 4);
+        d.add(draft_probs_shard, ndz * static_cast<size_t>(Vs) * 4);
+        d.add(cu_num_draft, (n + 1) * 4);
+        d.add(temperature, n * 4);
+        d.add(is_greedy, n);
+        d.add(out, Rz * sizeof(spec_verify_shard_stat));
+        dbg_add_ctx(d, ctx);
+        if (d.push(ctx->flags, stream) != SV_OK) return SV_ECUDA;
+    }
+#endif
     auto launch = [&](auto tag) -> int {
         using T = decltype(tag);
         const T *lg = static_cast<const T *>(logits_shard);
@@ -3077,6 +3771,23 @@ int spec_verify_shard_race(spec_verify_ctx *ctx, const void *logits_shard, int v
     P.req_base = req_index_base;
     P.out = out;
     const size_t smem = verify_smem_bytes(ctx->V, max_spec_len_this_batch);
+#ifdef SV_DEBUG_BOUNDS
+    {
+        const size_t n = static_cast<size_t>(num_reqs), Rz = static_cast<size_t>(P.R);
+        const size_t eb = ctx->dtype == SV_BF16 ? 2 : 4, ndz = static_cast<size_t>(num_draft_tokens);
+        DbgList d;
+        d.add(logits_shard, Rz * static_cast<size_t>(P.Vs) * eb);
+        d.add(all_stats, static_cast<size_t>(world) * Rz * sizeof(spec_verify_shard_stat));
+        d.add(draft_ids, ndz * 4);
+        d.add(draft_probs_shard, ndz * static_cast<size_t>(P.Vs) * 4);
+        d.add(cu_num_draft, (n + 1) * 4);
+        d.add(temperature, n * 4);
+        d.add(is_greedy, n);
+        d.add(out, n * sizeof(spec_verify_shard_key));
+        dbg_add_ctx(d, ctx);
+        if (d.push(ctx->flags, stream) != SV_OK) return SV_ECUDA;
+    }
+#endif
     auto launch = [&](auto tag) -> int {
         using T = decltype(tag);
         const T *lg = static_cast<const T *>(logits_shard);
@@ -3099,6 +3810,22 @@ int spec_verify_shard_finish(spec_verify_ctx *ctx, const spec_verify_shard_key *
     if (!all_races || !cu_num_draft || !sampled || !num_sampled || !num_rejected) return SV_EINVAL;
     DeviceGuard g(ctx->device);
     if (!g.ok) return SV_EDEVICE;
+#ifdef SV_DEBUG_BOUNDS
+    {
+        const size_t n = static_cast<size_t>(num_reqs);
+        DbgList d;
+        d.add(all_races, static_cast<size_t>(world) * n * sizeof(spec_verify_shard_key));
+        // draft ids: at most cu_num_draft[num_reqs] of them; the count is on the device, so the
+        // whole capacity of the context is allowed
+        d.add(draft_ids, static_cast<size_t>(ctx->max_num_reqs) * static_cast<size_t>(ctx->max_spec_len) * 4);
+        d.add(cu_num_draft, (n + 1) * 4);
+        d.add(sampled, n * (static_cast<size_t>(max_spec_len_this_batch) + 1) * 4);
+        d.add(num_sampled, n * 4);
+        d.add(num_rejected, n * 4);
+        dbg_add_ctx(d, ctx);
+        if (d.push(ctx->flags, static_cast<cudaStream_t>(cuda_stream)) != SV_OK) return SV_ECUDA;
+    }
+#endif
     sv_shard_finish_kernel<<<(num_reqs + kThreads - 1) / kThreads, kThreads, 0,
                              static_cast<cudaStream_t>(cuda_stream)>>>(
         all_races, world, draft_ids, cu_num_draft, num_reqs, max_spec_len_this_batch, sampled,

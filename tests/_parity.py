@@ -113,7 +113,8 @@ def gpu_run(batch, ctx=None, *, max_spec_len=None, req_index_base=0, seed=None, 
                    out=tuple(views[:3]), stats_out=tuple(views[3:]),
                    draft_logits=d["draft_logits"], partial_prefill=d["partial_prefill"],
                    frequency_penalty=d["frequency_penalty"], output_bin_counts=d["output_bin_counts"],
-                   counts_row=d["counts_row"], top_k=d["top_k"], top_p=d["top_p"])
+                   counts_row=d["counts_row"], top_k=d["top_k"], top_p=d["top_p"],
+                   fp64_gumbel=bool(getattr(batch, "fp64_gumbel", False)))
     torch.cuda.synchronize()
     names = ("sampled", "num_sampled", "num_rejected", "row_max", "row_sumexp", "row_argmax")
     for name, (buf, _) in zip(names, padded):
