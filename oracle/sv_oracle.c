@@ -16,7 +16,7 @@
  *                   example), 7.0.1 (greedy), 7.0.2 (bonus), 7.3 (Gumbel argmax), 7.4 (kernels).
  *   [mini-sglang]   "mini-sglang" (blog.thunguo.space): "how tokens are sampled" (greedy rule).
  *
- * Readings where the pages leave a step open (each one is also listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - p = softmax(logits / T) with x_v = logit_v * (1/T) in binary32; T <= 0 (or a set greedy
  *     flag) means greedy verification.
  *   - Acceptance test p(d)/q(d) >= u with u in (0,1); q(d) = 1 without draft probabilities.
