@@ -58,9 +58,16 @@ constexpr float kInf = __builtin_huge_valf();
 struct __align__(16) StatPart {
     float L;       // max raw logit of the segment
     float s;       // sum of 2^((l - L) c) over the segment
-    int32_t idx;   // lowest index of L
+    int32_t idx;   // where L first occurs, as a candidate (see argmax_candidate)
     int32_t pad;
 };
+
+// A partial's first occurrence of its maximum, ordered like the index it stands for: 2 e for
+// element e of the row, 2 a + 1 for the 64-byte pair starting at element a (its lowest element
+// equal to the maximum is the one; the reader resolves it, only when it needs the index), and
+// INT_MAX for none. Elements and pairs of one row never overlap, so the smallest candidate among
+// partials tied at the row maximum holds the row's first occurrence. Indices stay below 2^30.
+__device__ __forceinline__ int argmax_candidate(int e, bool pair) { return (e << 1) | (pair ? 1 : 0); }
 
 // ---------------------------------------------------------------------------------------
 // checked global memory access (debug builds)
@@ -652,14 +659,9 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
     }
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads) fold1(st, Elem<T>::at(rp, ee), ee, c);
 
-    // lowest index where this thread's max occurs
-    int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
-    if (st.best_p >= 0) {
-        ldg_pair(pbase + static_cast<size_t>(st.best_p) * kPairBytes, w0);
-#pragma unroll
-        for (int h = kPE - 1; h >= 0; --h)
-            if (pair_elem<T>(w0, h) == st.L) idx = a0 + st.best_p * kPE + h;
-    }
+    // where this thread's max first occurs: an element, or the pair that first reached it
+    int idx = st.best_e >= 0 ? argmax_candidate(st.best_e, false) : INT_MAX;
+    if (st.best_p >= 0) idx = argmax_candidate(a0 + st.best_p * kPE, true);
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
     if (lane == 0)
@@ -856,7 +858,7 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
 
-    int idx = st.best_e >= 0 ? st.best_e : INT_MAX;
+    int idx = st.best_e >= 0 ? argmax_candidate(st.best_e, false) : INT_MAX;
     if (st.best_p >= 0) {  // the vector that first reached the max: its lowest index
         const int v = a0 + st.best_p * kEV;
         const uint4 w = ldg_v4(vbase + static_cast<size_t>(st.best_p) * 16);
@@ -868,7 +870,7 @@ __device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, 
         values(v, ws, cnt, true, y);
 #pragma unroll
         for (int h = kEV - 1; h >= 0; --h)
-            if (y[h] == st.L) idx = v + h;
+            if (y[h] == st.L) idx = argmax_candidate(v + h, false);
     }
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
@@ -1644,6 +1646,22 @@ __device__ __forceinline__ void combine_row(const StatPart *__restrict__ part, l
         combine_stat(L, s, idx, raw.x, raw.y, __float_as_int(raw.z), c);
     }
     warp_reduce_stat(L, s, idx, c);
+}
+
+// The row's lowest index of its maximum L from the combined candidate `cand` (argmax_candidate;
+// 0 for none), by the whole warp: a pair is read once, an element per lane, and the lowest lane
+// holding L is the index.
+template <typename T>
+__device__ __forceinline__ int resolve_argmax(const T *__restrict__ rp, int cand, float L)
+{
+    if (cand == INT_MAX) return 0;
+    const int a = cand >> 1;
+    if (!(cand & 1)) return a;
+    constexpr int kPE = kPairBytes / static_cast<int>(sizeof(T));
+    const int lane = threadIdx.x & 31;
+    const bool hit = lane < kPE && Elem<T>::at(rp, a + lane) == L;
+    const unsigned b = __ballot_sync(0xFFFFFFFFu, hit);
+    return b ? a + __ffs(b) - 1 : a;  // (a pair always holds its maximum)
 }
 
 // ---------------------------------------------------------------------------------------
@@ -2696,11 +2714,12 @@ sv_shard_export_kernel(const T *__restrict__ logits, RequestTable rq,
     float L, sx;
     int idx;
     combine_row(part, row, Vs, maxseg, base_off, chunk, invT * kLog2e, L, sx, idx);
+    const int amax = resolve_argmax<T>(logits + static_cast<size_t>(row) * Vs, idx, L);
     if (lane == 0) {
         spec_verify_shard_stat rec;
         rec.max_logit = L;
         rec.sumexp = sx;
-        rec.argmax = v0 + (idx == INT_MAX ? 0 : idx);
+        rec.argmax = v0 + amax;
         rec.draft_logit = __int_as_float(0x7FC00000);
         rec.draft_prob = __int_as_float(0x7FC00000);
         rec.reserved = 0;
@@ -3027,12 +3046,13 @@ sv_verify_kernel(const T *__restrict__ logits, const T *__restrict__ lines,
             tau = sv_ldg(P.sel_tau + row);
             s = sv_ldg(P.sel_S + row);
         }
+        // the argmax only where it is used: a greedy request's tests and output, the row output
+        const int amax = greedy || P.opt_amax ? resolve_argmax<T>(logits + rbase, idx, L) : 0;
         if (lane == 0) {
             sm_md[j] = md;
             sm_Sd[j] = Sd;
             sm_tau[j] = tau;
             const float m = __fmul_rn(L, invT);  // = max_v fl(l_v / T): rounding is monotone
-            const int amax = idx == INT_MAX ? 0 : idx;
             sm_m[j] = m;
             sm_S[j] = s;
             sm_amax[j] = amax;
@@ -3574,7 +3594,8 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     if (logits_dtype != SV_F32 && logits_dtype != SV_BF16) return SV_EDTYPE;
     const long long rows = static_cast<long long>(max_num_reqs) * (max_spec_len + 1);
     const long long maxseg = ceil_div(vocab_size, kMinChunk) + 1;
-    if (rows > INT_MAX / 8 || rows * maxseg * kWarps > (1LL << 31) || max_spec_len > (1 << 16))
+    if (rows > INT_MAX / 8 || rows * maxseg * kWarps > (1LL << 31) || max_spec_len > (1 << 16) ||
+        vocab_size >= (1 << 30))  // (argmax candidates hold 2 x an index in an int)
         return SV_ECAPACITY;
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {

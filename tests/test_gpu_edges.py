@@ -90,3 +90,38 @@ def test_large_vocabulary():
 def test_extreme_temperatures(T):
     b = _batch(207, 20011, [3, 2, 4, 0, 1, 3], "bf16", "noisy", greedy_frac=0.0, temps=(T, T))
     assert_parity(b, gpu_run(b), oracle.run(b))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,chunks", [(1001, 0), (1001, 512), (20011, 512), (20011, 0), (151936, 0)])
+def test_tied_maxima_first_occurrence(dtype, V, chunks):
+    """The row maximum planted several times per row: runs of consecutive copies (inside one
+    64-byte pair and across the pairs of neighbouring lanes), copies far apart (other warps and,
+    with small statistics chunks, other segments), at the first and the last element. The first
+    occurrence is the argmax: in the row output and in what greedy requests emit."""
+    Ks = [2, 3, 0, 4, 1, 2, 3, 1]
+    b = _batch(208, V, Ks, dtype, "noisy", greedy_frac=0.5)
+    rng = np.random.default_rng(208)
+    x = np.minimum(rng.normal(0, 2, (b.num_rows, V)), 10.0).astype(np.float32)
+    M = np.float32(16.0)
+    for r in range(b.num_rows):
+        kind = r % 5
+        if kind == 0:      # a run: the same pair and the pairs after it
+            j = int(rng.integers(0, V - 40))
+            x[r, j:j + 40] = M
+        elif kind == 1:    # two copies far apart
+            j = int(rng.integers(0, V // 2))
+            x[r, [j, j + V // 2]] = M
+        elif kind == 2:    # the first element and elsewhere
+            x[r, [0, int(rng.integers(1, V))]] = M
+        elif kind == 3:    # the last element only
+            x[r, V - 1] = M
+        else:              # copies inside one 64-element line, then scattered
+            j = int(rng.integers(0, V - 64)) & ~63
+            x[r, [j + 37, j + 50, j + 63]] = M
+            x[r, rng.integers(j + 64, V, 5) if j + 64 < V else []] = M
+    b.logits = _as_dtype(x, dtype)
+    got = gpu_run(b, chunks=chunks or None)
+    assert_parity(b, got, oracle.run(b))
+    first = np.argmax(x == M, axis=1)
+    np.testing.assert_array_equal(got["row_argmax"], first)

@@ -88,6 +88,36 @@ def test_shard_records_match_the_oracle_side():
         np.testing.assert_allclose(got["sumexp"], want["s"], rtol=1e-5)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_shard_records_keep_the_first_of_tied_maxima(dtype):
+    """Each row's maximum planted as runs and scattered copies, some in both shards: every rank's
+    record holds the first occurrence in its own slice, and the step the lowest overall."""
+    V = 8192 + 64 * 5
+    rng = np.random.default_rng(209)
+    Ks = [2, 3, 1, 0, 2]
+    b = workloads.make_batch(name="shard-ties", data_seed=209, verify_seed=210, K=Ks, vocab_size=V,
+                             logits_dtype=dtype, sigma=2.0, q_mode="noisy", q_noise=1.0,
+                             temperature=rng.uniform(0.5, 1.5, len(Ks)).astype(np.float32),
+                             greedy=np.array([1, 0, 1, 1, 0], np.uint8))
+    x = np.minimum(rng.normal(0, 2, (b.num_rows, V)), 10.0).astype(np.float32)
+    for r in range(b.num_rows):
+        j = int(rng.integers(0, V - 40))
+        x[r, j:j + 1 + r % 40] = 16.0
+        x[r, rng.integers(0, V, 4)] = 16.0
+    b.logits = (x.view(np.uint32) >> 16).astype(np.uint16) if dtype == "bf16" else x
+    vals = (b.logits.astype(np.uint32) << 16).view(np.float32) if dtype == "bf16" else x
+    (sampled, ns, nr), bounds, recs = _run_sharded(b, 2)
+    for (lo, hi), rec in zip(bounds, recs):
+        got = rec.view(np.dtype([("max_logit", "<f4"), ("sumexp", "<f4"), ("argmax", "<i4"),
+                                 ("draft_logit", "<f4"), ("draft_prob", "<f4"), ("r", "<i4")]))
+        xs = vals[:, lo:hi]
+        first = lo + np.argmax(xs == xs.max(axis=1, keepdims=True), axis=1)
+        np.testing.assert_array_equal(got["argmax"], first)
+    ref = oracle.run(b)
+    assert_parity(b, dict(sampled=sampled, num_sampled=ns, num_rejected=nr, row_max=ref["row_max"],
+                          row_sumexp=ref["row_sumexp"], row_argmax=ref["row_argmax"]), ref)
+
+
 def test_misaligned_shard_is_refused():
     import torch
 
