@@ -1427,8 +1427,10 @@ __device__ void flush_queue(const RaceRow<T> &r, const SearchSmem &sm, int n)
 // by an upper bound from the hardware ex2 / lg2 / rcp with margins (key_v <= w_v / E_g; weights
 // at most exp(x - m), and the residual's fma is monotone in it). The queue is emptied through
 // flush_queue whenever it holds 32 tokens; qn is its length. In draft-logits mode q_v is bounded
-// from below the same way (hardware ex2 and a reciprocal of S_d, with margins).
-template <typename T, bool kRes, bool kDL, bool kPen, int B>
+// from below the same way (hardware ex2 and a reciprocal of S_d, with margins). kOnePerLane: of
+// its two tokens a lane queues only the one with the larger bound (a first threshold from at most
+// 32 exact keys; the group's other tokens are left to a later evaluation).
+template <typename T, bool kRes, bool kDL, bool kPen, int B, bool kOnePerLane = false>
 __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)[B], const SearchSmem &sm,
                                             int &qn)
 {
@@ -1455,6 +1457,8 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
         const int g = gs[k];
         if (g < 0) continue;
         const float inv = inv_emin_bound(head_uniform_ub(sm.ew[g], r.f64));
+        bool tk[2];
+        float kbv[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int v = g * kGroup + 2 * lane + h;
@@ -1469,10 +1473,20 @@ __device__ __forceinline__ void eval_groups(const RaceRow<T> &r, const int (&gs)
             }
             const float w_ub = kRes ? __fmaf_rn(-r.S, q_lb, t_ub) : t_ub;
             bool take = v < r.V && (kRes ? w_ub > 0.0f : v != r.excl) && xv >= r.tau;
-            if (take && cur != 0) {
-                const float kb = w_ub * inv * (1.0f + 0x1p-12f);
-                take = !(kb == kb) || key_enc(kb) >= thr;  // NaN bounds are kept
+            kbv[h] = w_ub * inv * (1.0f + 0x1p-12f);
+            if (take && cur != 0) take = !(kbv[h] == kbv[h]) || key_enc(kbv[h]) >= thr;  // NaN kept
+            tk[h] = take;
+        }
+        if constexpr (kOnePerLane) {
+            if (tk[0] && tk[1]) {
+                if (kbv[1] > kbv[0]) tk[0] = false;
+                else tk[1] = false;
             }
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int v = g * kGroup + 2 * lane + h;
+            const bool take = tk[h];
             const unsigned msk = __ballot_sync(0xFFFFFFFFu, take);
             if (take) {
                 const int pos = warp * kQueue + qn + __popc(msk & ((1u << lane) - 1u));
@@ -1522,15 +1536,14 @@ __device__ unsigned long long race_search(const RaceRow<T> &r, const RowLines &r
         sm.bin_max[tid] = 0u;
     }
     __syncthreads();  // bounds complete: lm is free from here on (buf reuses it)
-    // round 1: every warp evaluates its own best-bounded group
+    // round 1: every warp evaluates one token per lane of its own best-bounded group
     const unsigned long long wb = warp_max_u64(mine);
     if (lane == 0) atomicMax(sm.top, static_cast<unsigned>(wb >> 32));
-    if (wb != 0) {
+    if (wb != 0) {  // (the group stays a candidate: half of it is evaluated here)
         const int gs[1] = {static_cast<int>(~static_cast<unsigned>(wb))};
         int qn = 0;
-        eval_groups<T, kRes, kDL, kPen, 1>(r, gs, sm, qn);
+        eval_groups<T, kRes, kDL, kPen, 1, true>(r, gs, sm, qn);
         flush_queue<T, kRes, kDL>(r, sm, qn);
-        if (lane == 0) sm.pb[gs[0]] = __int_as_float(0x7FC00000);  // evaluated
     }
     __syncthreads();
     // round 2: every group whose bound reaches the best key found so far, best bound first:

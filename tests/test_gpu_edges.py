@@ -93,7 +93,8 @@ def test_extreme_temperatures(T):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
-@pytest.mark.parametrize("V,chunks", [(1001, 0), (1001, 512), (20011, 512), (20011, 0), (151936, 0)])
+@pytest.mark.parametrize("V,chunks", [(1001, 0), (1001, 512), (20011, 512), (20011, 0), (20011, 32768),
+                                      (151936, 0)])
 def test_tied_maxima_first_occurrence(dtype, V, chunks):
     """The row maximum planted several times per row: runs of consecutive copies (inside one
     64-byte pair and across the pairs of neighbouring lanes), copies far apart (other warps and,
