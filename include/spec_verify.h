@@ -114,10 +114,12 @@ typedef struct spec_verify_ctx spec_verify_ctx; /* opaque */
  * host-buffer entry point sizes anything by it); SV_DRAFT_LOGITS reserves the partial
  * statistics of the draft rows (about 16 * 8 * (vocab_size / 2048 + 2) bytes per draft row of
  * capacity) that spec_verify_run_draft_logits needs. Any other value returns SV_EINVAL.
- * The context owns its device scratch (the per-segment partial statistics and an error word),
- * allocated here once; spec_verify_run allocates nothing. Free with spec_verify_free.
+ * The context owns its device scratch (the per-segment partial statistics, the frequency
+ * penalty's counts mask of 4 * max_num_reqs * (ceil(vocab_size / 32) + 1) bytes, and an error
+ * word), allocated here once; spec_verify_run allocates nothing. Free with spec_verify_free.
  * Returns SV_ECAPACITY when the race's per-group bounds of one row (about 12 bytes per 64
- * tokens) do not fit in one CTA's shared memory (vocab_size above about a million).
+ * tokens) do not fit in one CTA's shared memory (vocab_size above about a million), and for
+ * vocab_size >= 2^30.
  * Returns SV_OK and *out, or an error with *out = NULL.
  */
 int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, int vocab_size,

@@ -243,6 +243,8 @@ struct PenTable {
     int counts_rows;
     int nd;                     // draft tokens of the batch (length of draft_ids)
     int kmax;                   // most drafts of one request
+    const uint32_t *mask;       // [n][mask_stride] nonzero bits of each request's counts, or nullptr
+    int mask_stride;            // words per request: ceil(V / 32) + 1 (a zero word last)
 };
 
 // The penalty of one logit row: y_v = fma(-f, c_v, l_v) where f != 0 and c_v != 0, else l_v;
@@ -253,6 +255,7 @@ struct PenRow {
     const int32_t *cnt;    // the request's counts row
     const int32_t *prev;   // drafts before this position
     int nprev;
+    const uint32_t *mask;  // the counts row's nonzero bits (sv_pen_mask_kernel), or nullptr
 };
 
 // Request i, position j (drafts from q0). A counts row outside [0, counts_rows) gives no penalty
@@ -272,6 +275,7 @@ __device__ __forceinline__ PenRow pen_row(const PenTable &pt, const int32_t *dra
     r.cnt = pt.counts + static_cast<size_t>(crow) * V;
     r.prev = draft_ids + q0;
     r.nprev = j;
+    r.mask = pt.mask ? pt.mask + static_cast<size_t>(i) * pt.mask_stride : nullptr;
     return r;
 }
 
@@ -668,210 +672,170 @@ __device__ __forceinline__ void stats_segment(const T *__restrict__ logits, int 
         sv_st(part + (static_cast<size_t>(row) * maxseg + seg) * kWarps + (threadIdx.x >> 5), StatPart{L, s, idx, 0});
 }
 
-// Asynchronous 16- and 4-byte copies global -> shared (cp.async), tracked per thread in commit
-// groups: wait_group<n> returns once at most n of the thread's latest groups are still in flight,
-// and the thread then sees what its completed copies wrote.
-__device__ __forceinline__ uint32_t smem_u32(const void *p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    if (!SV_CHECK(src, 16)) return;  // (the slot keeps what it held)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-// through L1 (.ca): the two halves of a 32-byte sector that two copies of one lane read are
-// fetched from L2 once
-__device__ __forceinline__ void cp_async16_l1(uint32_t dst, const void *src)
-{
-    if (!SV_CHECK(src, 16)) return;  // (the slot keeps what it held)
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src)
-{
-    if (!SV_CHECK(src, 4)) return;  // (the slot keeps what it held)
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int n>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(n) : "memory"); }
-
-// Staging ring of the penalised statistics path: per warp kPenStages rounds, per round and lane
-// one slot of 48 bytes (a 16-byte logit vector, then its counts: 8 ints for bf16, 4 for fp32).
-// 48-byte slots keep the lanes' 16-byte shared loads free of bank conflicts.
-constexpr int kPenStages = 4;
-constexpr int kPenSlot = 48;
-constexpr int kPenRingBytes = kWarps * kPenStages * 32 * kPenSlot;
-
-// stats_segment for a penalised row (PenRow with f != 0): the same partials over the processed
-// values y (see PenRow), and line maxima rounded up to the logits' type (an upper bound of the
-// line's y). The row is streamed as 16-byte vectors (8 bf16 / 4 fp32 elements, a lane each), each
-// with its counts, copied asynchronously into the lane's own slots of the warp's ring (`ring`,
-// kPenStages rounds of 32 slots): kPenStages - 1 rounds are in flight while one is processed, and
-// no register holds data in flight. Counts are copied as 16-byte vectors through L1 where the
-// counts row is so aligned (the same for every vector of the segment), else as single ints. The earlier drafts
-// of the position (at most 32 of them in the lanes' registers) are tested once per round against
-// the warp's window of tokens; only a round that holds one adds them lane by lane.
-// c = (1 / T) log2(e) of the row's request.
+// stats_segment for the rows of a batch with a frequency penalty, over the processed values y
+// (see pen_apply): the plain path's pair stream, each pair requested with the two words of the
+// row's counts mask (sv_pen_mask_kernel) that hold its tokens' bits. A pair's counted tokens
+// (count bits, and earlier drafts) are set to -inf in its buffer and the pair is folded as raw
+// logits, which its other tokens' values are; the counted ones, few since counts are sparse,
+// then take their counts and drafts one by one (y = l - f n, as pen_apply). A maximum of a pair
+// with counted tokens is recorded by its exact index (a reader can only resolve a pair of raw
+// values). A row without a penalty (or a draft row) has no mask and no drafts: every pair folds
+// as raw logits. Line maxima are those of y rounded up to the logits' type: upper bounds.
 template <typename T>
-__device__ __forceinline__ void stats_segment_pen(const T *__restrict__ logits, int V, int row, int b,
-                                                  int e, int seg, int maxseg, int base_off, float c,
-                                                  const PenRow &pr, StatPart *__restrict__ part,
-                                                  T *__restrict__ s_lines, long long line_base,
-                                                  unsigned char *ring)
+__device__ __forceinline__ void stats_segment_mask(const T *__restrict__ logits, int V, int row, int b,
+                                                   int e, int seg, int maxseg, int base_off,
+                                                   const RequestTable &rq, const PenTable &pt,
+                                                   const int32_t *__restrict__ draft_ids,
+                                                   bool draft_rows, StatPart *__restrict__ part,
+                                                   T *__restrict__ s_lines, long long line_base)
 {
-    constexpr int kEV = 16 / static_cast<int>(sizeof(T));  // elements per vector
-    constexpr int kVPL = kGroup / kEV;                      // vectors per 64-element line
     const long long rbase = static_cast<long long>(row) * V;
     const T *rp = logits + rbase;
+    constexpr int kPE = kPairBytes / sizeof(T);  // elements per pair
+    constexpr int kPPL = PairMax<T>::kLanes;     // pairs per line
     const long long pos_b = base_off + rbase + b;
     const int head = static_cast<int>((kGroup - (pos_b & (kGroup - 1))) & (kGroup - 1));
-    const int a0 = min(e, b + head);  // on a line boundary: 16-byte aligned in memory
-    const int nvec = (e - a0) / kEV;
-    const int a1 = a0 + nvec * kEV;
-    const char *vbase = reinterpret_cast<const char *>(rp + a0);
-    const int32_t *cbase = pr.cnt + a0;
+    const int a0 = min(e, b + head);
+    const int npair = (e - a0) / kPE;
+    const int a1 = a0 + npair * kPE;
+    const char *pbase = reinterpret_cast<const char *>(rp + a0);
     const int line0 = static_cast<int>(((pos_b + (a0 - b)) >> 6) - line_base);
     const int lane = threadIdx.x & 31;
-    const bool aligned = (reinterpret_cast<uintptr_t>(cbase) & 15u) == 0u;
-    const uint32_t slot0 = smem_u32(ring) + lane * kPenSlot;
-    constexpr uint32_t kStageBytes = 32 * kPenSlot;
+    int ub = static_cast<int>(threadIdx.x) & ~31;
+    uint32_t w0[16], w1[16], w2[16];
+    if (ub + lane < npair) ldg_pair(pbase + static_cast<size_t>(ub + lane) * kPairBytes, w0);
+    if (ub + lane + kThreads < npair)
+        ldg_pair(pbase + static_cast<size_t>(ub + lane + kThreads) * kPairBytes, w1);
+    // the row's request and penalty, while the first rounds are in flight
+    const int i = row_request(rq.cu, rq.n, row, lane, draft_rows);
+    PenRow pr{0.0f, nullptr, nullptr, 0, nullptr};
+    if (!draft_rows) {
+        const int q0 = sv_ldg(rq.cu + i);
+        pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
+        if (pr.f == 0.0f) pr = PenRow{0.0f, nullptr, nullptr, 0, nullptr};
+    }
+    bool greedy;
+    const float c = request_invT(rq, i, greedy) * kLog2e;
+    const int np = pr.nprev;
+    const int pv = lane < np ? sv_ldg(pr.prev + lane) : -1;  // earlier drafts: lane k the k-th
 
-    auto issue = [&](int u, int stage) {
-        if (u < nvec) {
-            const uint32_t d = slot0 + stage * kStageBytes;
-            cp_async16(d, vbase + static_cast<size_t>(u) * 16);
-            const int32_t *cs = cbase + u * kEV;
-            if (aligned) {
-#pragma unroll
-                for (int q = 0; q < kEV / 4; ++q) cp_async16_l1(d + 16 + 16 * q, cs + 4 * q);
-            } else {
-#pragma unroll
-                for (int k = 0; k < kEV; ++k) cp_async4(d + 16 + 4 * k, cs + k);
-            }
-        }
-        cp_async_commit();
+    // the mask words of pair p's tokens [t, t + kPE): word t / 32 and the next (at most the zero
+    // word after the row's last, since t + kPE <= V)
+    auto load_mask = [&](int p, uint2 &m) {
+        if (!pr.mask) return;
+        const int t = a0 + p * kPE;
+        m.x = sv_ldg(pr.mask + (t >> 5));
+        m.y = sv_ldg(pr.mask + (t >> 5) + 1);
     };
-    // y of the kEV tokens from v: logits words ws, counts cnt, plus the earlier drafts if `scan`.
-    // A count in [0, 2^23) becomes a float exactly by placing it in the significand of 2^23 and
-    // subtracting 2^23 (full-rate integer and float operations instead of a conversion); a vector
-    // with any other count converts them.
-    auto values = [&](int v, const uint32_t (&ws)[4], const int (&cnt)[kEV], bool scan,
-                      float (&y)[kEV]) {
-        int n[kEV];
-#pragma unroll
-        for (int k = 0; k < kEV; ++k) n[k] = cnt[k];
-        if (scan) {
-            bool hit = false;
-            for (int k = 0; k < pr.nprev; ++k)
-                hit |= static_cast<unsigned>(sv_ldg(pr.prev + k) - v) < static_cast<unsigned>(kEV);
-            if (hit)
-                for (int q = 0; q < pr.nprev; ++q) {
-                    const int d = sv_ldg(pr.prev + q) - v;
-#pragma unroll
-                    for (int k = 0; k < kEV; ++k) n[k] += d == k;
-                }
-        }
-        int any = 0;
-#pragma unroll
-        for (int k = 0; k < kEV; ++k) any |= n[k];
-        if (any == 0) {  // (almost every vector: counts are sparse) y = l
-#pragma unroll
-            for (int k = 0; k < kEV; ++k) {
-                if constexpr (sizeof(T) == 2)
-                    y[k] = __uint_as_float((k & 1) ? (ws[k >> 1] & 0xFFFF0000u) : (ws[k >> 1] << 16));
-                else
-                    y[k] = __uint_as_float(ws[k]);
-            }
-            return;
-        }
-        float fn[kEV];
-        if ((static_cast<unsigned>(any) >> 23) == 0u) {
-#pragma unroll
-            for (int k = 0; k < kEV; ++k) fn[k] = __int_as_float(n[k] | 0x4B000000) - 8388608.0f;
-        } else {
-#pragma unroll
-            for (int k = 0; k < kEV; ++k) fn[k] = __int2float_rn(n[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < kEV; ++k) {
-            float l;
-            if constexpr (sizeof(T) == 2)
-                l = __uint_as_float((k & 1) ? (ws[k >> 1] & 0xFFFF0000u) : (ws[k >> 1] << 16));
-            else
-                l = __uint_as_float(ws[k]);
-            y[k] = n[k] == 0 ? l : __fmaf_rn(-pr.f, fn[k], l);
-        }
+    auto load = [&](int p, uint32_t (&w)[16], uint2 &m) {
+        ldg_pair(pbase + static_cast<size_t>(p) * kPairBytes, w);
+        load_mask(p, m);
     };
+    auto drafts_at = [&](int v) {  // how many earlier drafts are token v
+        int n = 0;
+        for (int k = 0; k < np; ++k) n += sv_ldg(pr.prev + k) == v;
+        return n;
+    };
+    uint2 m0 = make_uint2(0u, 0u), m1 = m0, m2 = m0;
+    if (ub + lane < npair) load_mask(ub + lane, m0);
+    if (ub + lane + kThreads < npair) load_mask(ub + lane + kThreads, m1);
 
     OnlineMax st;
     for (int ee = b + threadIdx.x; ee < a0; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
-    // earlier drafts: lane k holds the k-th (k < 32); more than 32 are scanned every round
-    const int np = pr.nprev;
-    const int pv = lane < np ? sv_ldg(pr.prev + lane) : -1;
-    int ub = static_cast<int>(threadIdx.x) & ~31;
-#pragma unroll
-    for (int s = 0; s < kPenStages - 1; ++s) issue(ub + lane + s * kThreads, s);
-    int stage = 0;
-    for (; ub < nvec; ub += kThreads) {
-        const int u = ub + lane;
-        // the stage read in the previous round takes the round kPenStages - 1 ahead
-        issue(u + (kPenStages - 1) * kThreads, stage == 0 ? kPenStages - 1 : stage - 1);
-        const int wlo = a0 + ub * kEV;  // the warp's tokens this round: [wlo, wlo + 32 kEV)
-        const bool scan = np > 32 ||
-                          __ballot_sync(0xFFFFFFFFu, static_cast<unsigned>(pv - wlo) <
-                                                          static_cast<unsigned>(32 * kEV)) != 0u;
-        cp_async_wait<kPenStages - 1>();
-        float y[kEV];
-        float mx = -kInf;
-        if (u < nvec) {
-            const unsigned char *sl = ring + stage * kStageBytes + lane * kPenSlot;
-            const uint4 w = *reinterpret_cast<const uint4 *>(sl);
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-            int cnt[kEV];
-#pragma unroll
-            for (int q = 0; q < kEV / 4; ++q) {
-                const int4 t = *reinterpret_cast<const int4 *>(sl + 16 + 16 * q);
-                cnt[4 * q] = t.x;
-                cnt[4 * q + 1] = t.y;
-                cnt[4 * q + 2] = t.z;
-                cnt[4 * q + 3] = t.w;
+    // round: fold pair p of `cur` (modified in place: the buffer is reloaded only in the next
+    // round) and request the pair two rounds ahead into `nxt`
+    auto round = [&](uint32_t (&cur)[16], const uint2 &mc, uint32_t (&nxt)[16], uint2 &mn) {
+        const int p = ub + lane;
+        const bool valid = p < npair;
+        if (p + 2 * kThreads < npair) load(p + 2 * kThreads, nxt, mn);
+        const int t = a0 + p * kPE;
+        const int wlo = a0 + ub * kPE;  // the warp's tokens this round: [wlo, wlo + 32 kPE)
+        const bool scan = np > 32 || __ballot_sync(0xFFFFFFFFu, static_cast<unsigned>(pv - wlo) <
+                                                                    static_cast<unsigned>(32 * kPE)) != 0u;
+        // the pair's counted tokens (count bits, and earlier drafts in scan rounds)
+        const int sh = t & 31;
+        uint32_t bits = mc.x >> sh;
+        if (sh) bits |= mc.y << (32 - sh);
+        if constexpr (kPE < 32) bits &= (1u << kPE) - 1u;
+        uint32_t xb = valid ? bits : 0u;
+        if (scan && valid)
+            for (int k = 0; k < np; ++k) {
+                const unsigned d = static_cast<unsigned>(sv_ldg(pr.prev + k) - t);
+                if (d < static_cast<unsigned>(kPE)) xb |= 1u << d;
             }
-            values(a0 + u * kEV, ws, cnt, scan, y);
+        // the others fold as raw logits: the counted ones are set to -inf in the buffer first
+        if (xb) {
 #pragma unroll
-            for (int k = 0; k < kEV; ++k) mx = fmaxf(mx, y[k]);
+            for (int jw = 0; jw < 16; ++jw) {
+                if constexpr (sizeof(T) == 2) {
+                    const uint32_t b2 = (xb >> (2 * jw)) & 3u;
+                    const uint32_t m = ((b2 & 1u) ? 0x0000FFFFu : 0u) | ((b2 & 2u) ? 0xFFFF0000u : 0u);
+                    cur[jw] = (cur[jw] & ~m) | (0xFF80FF80u & m);
+                } else {
+                    if ((xb >> jw) & 1u) cur[jw] = 0xFF800000u;
+                }
+            }
+        }
+        const typename PairMax<T>::P pm = valid ? PairMax<T>::of(cur) : PairMax<T>::none();
+        float lmv = PairMax<T>::value(pm);  // the pair's largest processed value
+        if (valid) {
+            const float L0 = st.L;
+            fold_pair<T>(st, cur, p, c, lmv);
+            if (xb && st.L != L0) {  // a new maximum among raw values next to counted ones:
+                int hh = kPE - 1;     // a reader could not tell them apart, so the exact index
+#pragma unroll
+                for (int h = kPE - 1; h >= 0; --h)
+                    if (pair_elem<T>(cur, h) == st.L) hh = h;
+                st.best_e = t + hh;
+                st.best_p = -1;
+            }
+        }
+        // the counted tokens one by one (a tie with a maximum inside this pair keeps the lower
+        // index; an earlier pair's maximum has a lower index than any of them)
+        while (xb) {
+            const int k = __ffs(xb) - 1;
+            xb &= xb - 1u;
+            const int v = t + k;
+            const float l = Elem<T>::at(rp, v);
+            int n = (bits >> k) & 1u ? sv_ldg(pr.cnt + v) : 0;
+            if (scan) n += drafts_at(v);
+            const float y = n == 0 ? l : __fmaf_rn(-pr.f, __int2float_rn(n), l);
+            if (y > st.L) {
+                st.s = st.s == 0.0f ? 0.0f : st.s * sv::ex2_approx((st.L - y) * c);
+                st.L = y;
+                st.Ls = y;
+                st.best_e = v;
+                st.best_p = -1;
+            } else if (y == st.L && st.best_e >= t && v < st.best_e) {
+                st.best_e = v;
+            }
+            st.s += sv::ex2_approx((y - st.Ls) * c);
+            lmv = fmaxf(lmv, y);
         }
         if (s_lines) {
-            float lm = mx;
+            float lm = lmv;
 #pragma unroll
-            for (int o = 1; o < kVPL; o <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
-            if ((lane & (kVPL - 1)) == 0 && u + kVPL - 1 < nvec) {
-                if constexpr (sizeof(T) == 2) s_lines[line0 + u / kVPL] = bf16_round_up(lm);
-                else s_lines[line0 + u / kVPL] = lm;
+            for (int o = 1; o < kPPL; o <<= 1) lm = fmaxf(lm, __shfl_xor_sync(0xFFFFFFFFu, lm, o));
+            if ((lane & (kPPL - 1)) == 0 && p + kPPL - 1 < npair) {
+                if constexpr (sizeof(T) == 2) s_lines[line0 + p / kPPL] = bf16_round_up(lm);
+                else s_lines[line0 + p / kPPL] = lm;
             }
         }
-        if (u < nvec) fold_vals<kEV>(st, y, u, c, mx);
-        stage = stage + 1 == kPenStages ? 0 : stage + 1;
+        ub += kThreads;
+    };
+    while (ub < npair) {
+        round(w0, m0, w2, m2);
+        if (ub >= npair) break;
+        round(w1, m1, w0, m0);
+        if (ub >= npair) break;
+        round(w2, m2, w1, m1);
     }
-    cp_async_wait<0>();  // (the groups past the segment hold no copies) the ring is free again
     for (int ee = a1 + threadIdx.x; ee < e; ee += kThreads)
         fold1(st, pen_apply(pr, Elem<T>::at(rp, ee), ee), ee, c);
 
     int idx = st.best_e >= 0 ? argmax_candidate(st.best_e, false) : INT_MAX;
-    if (st.best_p >= 0) {  // the vector that first reached the max: its lowest index
-        const int v = a0 + st.best_p * kEV;
-        const uint4 w = ldg_v4(vbase + static_cast<size_t>(st.best_p) * 16);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-        int cnt[kEV];
-#pragma unroll
-        for (int k = 0; k < kEV; ++k) cnt[k] = sv_ldg(cbase + st.best_p * kEV + k);
-        float y[kEV];
-        values(v, ws, cnt, true, y);
-#pragma unroll
-        for (int h = kEV - 1; h >= 0; --h)
-            if (y[h] == st.L) idx = argmax_candidate(v + h, false);
-    }
+    if (st.best_p >= 0) idx = argmax_candidate(a0 + st.best_p * kPE, true);
     float L = st.L, s = st.s;
     warp_reduce_stat(L, s, idx, c);
     if (lane == 0)
@@ -901,12 +865,12 @@ struct StatsArray {
 // covers only in part are left undefined (the verify kernel reads those lines from the logits).
 // The first A.grid CTAs take the target logits, the rest the draft logits (if any). Nothing waits
 // on another CTA.
-// kPen: the batch has a frequency penalty (penalised rows take stats_segment_pen, with the
-// staging ring at ring_off bytes into the dynamic shared memory, after the line maxima).
+// kPen: the batch has a frequency penalty; every row takes stats_segment_mask (one segment
+// function per instantiation: the two together need more than a CTA's registers).
 template <typename T, bool kPen>
 __global__ void __launch_bounds__(kThreads, kPen ? 2 : 3)
 sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTable rq,
-                PenTable pt, const int32_t *__restrict__ draft_ids, int ring_off)
+                PenTable pt, const int32_t *__restrict__ draft_ids)
 {
     extern __shared__ __align__(16) unsigned char s_raw[];
     pdl_launch_dependents();
@@ -925,24 +889,10 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         const int b = static_cast<int>(max(start, rbase) - rbase);
         const int e = static_cast<int>(min(stop, rbase + V) - rbase);
         const int fk = static_cast<int>(div_floor(X.base_off + rbase, X.chunk));
-        bool plain = true;
-        if constexpr (kPen) {  // a penalised row takes the penalty path (target logits only)
-            if (!X.draft_rows) {
-                const int i = row_request(rq.cu, rq.n, row, threadIdx.x & 31);
-                const int q0 = sv_ldg(rq.cu + i);
-                const PenRow pr = pen_row(pt, draft_ids, i, q0, row - q0 - i, V);
-                if (pr.f != 0.0f) {
-                    bool greedy;
-                    const float c = request_invT(rq, i, greedy) * kLog2e;
-                    stats_segment_pen<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, c,
-                                         pr, X.part, s_lines, line_base,
-                                         s_raw + ring_off + (threadIdx.x >> 5) *
-                                                                (kPenRingBytes / kWarps));
-                    plain = false;
-                }
-            }
-        }
-        if (plain)
+        if constexpr (kPen)
+            stats_segment_mask<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, pt,
+                                  draft_ids, X.draft_rows != 0, X.part, s_lines, line_base);
+        else
             stats_segment<T>(X.logits, V, row, b, e, cta - fk, maxseg, X.base_off, rq, X.part,
                              s_lines, line_base, X.draft_rows != 0);
     }
@@ -957,6 +907,37 @@ sv_stats_kernel(int V, int maxseg, StatsArray<T> A, StatsArray<T> D, RequestTabl
         for (int k = nv * 16 / static_cast<int>(sizeof(T)) + threadIdx.x; k < nl; k += kThreads)
             sv_st(X.lines + line_base + k, s_lines[k]);
     }
+}
+
+// The nonzero pattern of every penalised request's counts row: bit v % 32 of word v / 32 of
+// mask[i * stride ..] is set when the count of token v is not 0, and the word after the last is
+// 0, so that a pair's two words can be read anywhere in the row. Requests without a penalty, or
+// whose counts row is outside the array, are skipped (pen_row gives them no penalty, so nothing
+// reads their bits). Each warp writes 32 words: word after word, a coalesced load of its 32
+// counts and a ballot. Grid: blocks_per_req CTAs per request, kWarps * 32 words each.
+__global__ void __launch_bounds__(kThreads)
+sv_pen_mask_kernel(PenTable pt, int n, int V, int blocks_per_req, uint32_t *__restrict__ mask)
+{
+    const int i = static_cast<int>(blockIdx.x) / blocks_per_req;
+    if (i >= n) return;
+    const int W = pt.mask_stride - 1;  // words of a row before the zero word
+    const int wb = (static_cast<int>(blockIdx.x) % blocks_per_req) * (kWarps * 32) +
+                   static_cast<int>(threadIdx.x >> 5) * 32;
+    if (wb > W) return;  // whole warps
+    const float f = sv_ldg(pt.f + i);
+    const int crow = pt.counts_row ? sv_ldg(pt.counts_row + i) : i;
+    if (f == 0.0f || crow < 0 || crow >= pt.counts_rows) return;
+    const int32_t *cnt = pt.counts + static_cast<size_t>(crow) * V;
+    const int lane = threadIdx.x & 31;
+    uint32_t mine = 0u;  // lane k: word wb + k
+#pragma unroll 8
+    for (int k = 0; k < 32; ++k) {
+        const int v = (wb + k) * 32 + lane;
+        const bool nz = v < V && sv_ldg(cnt + v) != 0;
+        const uint32_t bw = __ballot_sync(0xFFFFFFFFu, nz);
+        if (lane == k) mine = bw;
+    }
+    if (wb + lane <= W) sv_st(mask + static_cast<size_t>(i) * pt.mask_stride + wb + lane, mine);
 }
 
 // ---------------------------------------------------------------------------------------
@@ -3198,6 +3179,7 @@ struct spec_verify_ctx {
     float *sel_tau = nullptr;   // [max_rows] top-k / top-p threshold per row
     float *sel_S = nullptr;     // [max_rows] kept mass per row
     void *lines = nullptr;      // largest logit of every 64-element line (logits dtype), or null
+    uint32_t *penmask = nullptr;  // [max_num_reqs][ceil(V / 32) + 1] counts bits (frequency penalty)
     unsigned *flags = nullptr;  // [1] sticky error word
     // host-buffer staging
     void *io_logits = nullptr;
@@ -3261,6 +3243,7 @@ void free_all(spec_verify_ctx *ctx)
     cudaFree(ctx->sel_tau);
     cudaFree(ctx->sel_S);
     cudaFree(ctx->lines);
+    cudaFree(ctx->penmask);
     cudaFree(ctx->flags);
     cudaFree(ctx->io_logits);
     cudaFree(ctx->io_q);
@@ -3300,10 +3283,6 @@ cudaError_t setup_kernels(int device, int *stats_per_sm)
     if (es == cudaSuccess)
         es = cudaFuncSetAttribute(sv_select_kernel<T, true>,
                                   cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
-    if (es == cudaSuccess)  // line maxima of the largest chunk, then the staging ring
-        es = cudaFuncSetAttribute(sv_stats_kernel<T, true>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(kMaxChunk / kGroup * sizeof(T) + kPenRingBytes));
     if (es != cudaSuccess) return es;
     const void *kernels[] = {reinterpret_cast<const void *>(sv_shard_race_kernel<T>),
                              reinterpret_cast<const void *>(sv_verify_kernel<T, false, false>),
@@ -3377,6 +3356,8 @@ void dbg_add_ctx(DbgList &d, const spec_verify_ctx *ctx)
     d.add(ctx->sel_tau, rows * 4);
     d.add(ctx->sel_S, rows * 4);
     d.add(ctx->lines, (rows * V + 2 * kGroup) / kGroup * eb);
+    if (ctx->penmask)
+        d.add(ctx->penmask, static_cast<size_t>(ctx->max_num_reqs) * (static_cast<size_t>(ceil_div(ctx->V, 32)) + 1) * 4);
     d.add(ctx->flags, 2 * sizeof(unsigned));
 }
 #endif
@@ -3397,11 +3378,13 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
     const long long chunk1 = stats_chunk_for(ctx, total + total_d);
     const RequestTable rq{cu, b.temperature, b.is_greedy, b.top_k, num_reqs};
+    const int mask_stride = ceil_div(V, 32) + 1;
     const PenTable pen{b.frequency_penalty, b.output_bin_counts, b.counts_row, b.counts_rows, nd,
-                       kmax};
+                       kmax, ctx->penmask, mask_stride};
     const bool pen_on = b.frequency_penalty != nullptr;
     T *lines = static_cast<T *>(ctx->lines);
     if (pen_on && !lines) return SV_EINVAL;  // the race's line maxima of a penalised row
+    if (pen_on && !ctx->penmask) return SV_EINVAL;  // the statistics read the counts' bits
     const StatsArray<T> A = stats_array<T>(logits, total, chunk1, V, 0, ctx->statpart, lines);
     const StatsArray<T> D = stats_array<T>(dl, total_d, chunk1, V, 1, ctx->dpart, nullptr);
     const int base_off = A.base_off;
@@ -3476,13 +3459,17 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
         cudaEventRecord(slot->ev[0], stream);
     }
     const size_t smem1 = lines ? static_cast<size_t>(chunk1 / kGroup) * sizeof(T) : 0;
-    const size_t ring_off = (smem1 + 15) / 16 * 16;
+    if (pen_on && num_reqs > 0) {  // the counts' nonzero bits, read by the statistics
+        const int bpr = ceil_div(mask_stride, kWarps * 32);
+        sv_pen_mask_kernel<<<static_cast<unsigned>(num_reqs) * bpr, kThreads, 0, stream>>>(
+            pen, num_reqs, V, bpr, ctx->penmask);
+    }
     if (pen_on)
-        sv_stats_kernel<T, true><<<A.grid + D.grid, kThreads, ring_off + kPenRingBytes, stream>>>(
-            V, ctx->maxseg, A, D, rq, pen, b.draft_ids, static_cast<int>(ring_off));
+        sv_stats_kernel<T, true><<<A.grid + D.grid, kThreads, smem1, stream>>>(
+            V, ctx->maxseg, A, D, rq, pen, b.draft_ids);
     else
         sv_stats_kernel<T, false><<<A.grid + D.grid, kThreads, smem1, stream>>>(
-            V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids, 0);
+            V, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, b.draft_ids);
     if (slot) cudaEventRecord(slot->ev[1], stream);
     if (sel_on && !lines) return SV_EINVAL;  // the selection reads rows through their line maxima
     if (sel_on) {  // top-k / top-p: the kept set of every constrained row
@@ -3643,6 +3630,8 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     const size_t D = static_cast<size_t>(max_num_reqs) * static_cast<size_t>(max_spec_len);
     ok = ok && cudaMalloc(&ctx->sel_tau, R * sizeof(float)) == cudaSuccess &&
          cudaMalloc(&ctx->sel_S, R * sizeof(float)) == cudaSuccess;
+    const size_t mask_words = static_cast<size_t>(max_num_reqs) * (static_cast<size_t>(ceil_div(vocab_size, 32)) + 1);
+    ok = ok && cudaMalloc(&ctx->penmask, mask_words * sizeof(uint32_t)) == cudaSuccess;
     ok = ok && (!ctx->has_dl || D == 0 ||
                 cudaMalloc(&ctx->dpart, D * S * kWarps * sizeof(StatPart)) == cudaSuccess);
     ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
@@ -3758,7 +3747,7 @@ int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int 
         const StatsArray<T> D = stats_array<T>(nullptr, 0, chunk1, Vs, 1, nullptr, nullptr);
         const size_t smem1 = static_cast<size_t>(chunk1 / kGroup) * sizeof(T);
         sv_stats_kernel<T, false><<<A.grid, kThreads, smem1, stream>>>(
-            Vs, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, draft_ids, 0);
+            Vs, ctx->maxseg, A, D, rq, PenTable{nullptr, nullptr, nullptr, 0}, draft_ids);
         sv_shard_export_kernel<T><<<(R + kWarps - 1) / kWarps, kThreads, 0, stream>>>(
             lg, rq, draft_ids, draft_probs_shard, ctx->statpart, Vs, v0, ctx->maxseg, A.base_off,
             A.chunk, R, out);
