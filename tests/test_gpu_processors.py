@@ -220,3 +220,49 @@ def test_constraints_on_masked_and_huge_logits(dtype):
     b.logits = x if dtype == "f32" else (x.view(np.uint32) >> 16).astype(np.uint16)  # truncated
     _constrain(b, 111, [0, 1, 3, 40], [0.5, 0.95, 1.0])
     assert_parity(b, gpu_run(b), oracle.run(b))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V", [4096, 4099])
+def test_penalised_maxima_next_to_raw_ones(dtype, V):
+    """Penalised rows whose maximum is tied between a counted token (its value changed by the
+    penalty) and a raw one close by, in either order, at the row's first and last token, and
+    made by an earlier draft: the first occurrence of the processed maximum must come back as
+    the argmax (greedy requests emit it) and the statistics must match the oracle."""
+    Ks = [3, 2, 4, 1, 0, 2]
+    b = _batch(98, V, Ks, dtype, "noisy", greedy_frac=1.0)
+    n, R = b.num_reqs, b.num_rows
+    rng = np.random.default_rng(98)
+    x = np.minimum(rng.normal(0, 1.5, (R, V)), 4.0).astype(np.float32)
+    counts = np.zeros((n, V), np.int32)
+    f = np.full(n, -2.0, np.float32)           # a boost: y = l + 2 n
+    cu = b.cu_num_draft
+    rows = lambda i: range(int(cu[i]) + i, int(cu[i + 1]) + i + 1)  # noqa: E731
+    for r in rows(0):                          # counted token first, raw tie after it
+        x[r, 100], x[r, 105] = 6.0, 8.0
+    counts[0, 100] = 1
+    for r in rows(1):                          # raw token first, counted tie after it
+        x[r, 70], x[r, 80] = 8.0, 6.0
+    counts[1, 80] = 1
+    for r in rows(2):                          # the first token counted, a raw tie next to it
+        x[r, 0], x[r, 3] = 6.0, 8.0
+    counts[2, 0] = 1
+    for r in rows(3):                          # the last token counted: the top
+        x[r, V - 1] = 7.0
+    counts[3, V - 1] = 1
+    f[4] = 1.5                                 # a plain penalty on the top raw token
+    for r in rows(4):
+        x[r, 9] = 9.0
+    counts[4, 9] = 2
+    d = int(cu[5])                             # an earlier draft at position 1 lifts a token
+    b.draft_ids[d] = 2000
+    for r in rows(5):
+        x[r, 2000], x[r, 2001] = 6.0, 8.0
+    counts[5, 2000] = 0                        # only the draft counts it, from position 1 on
+    b.logits = (x.view(np.uint32) >> 16).astype(np.uint16) if dtype == "bf16" else x
+    b.output_bin_counts, b.counts_row, b.frequency_penalty = counts, None, f
+    got = gpu_run(b)
+    ref = oracle.run(b)
+    assert_parity(b, got, ref)
+    np.testing.assert_array_equal(got["row_argmax"], ref["row_argmax"])
+    assert got["error_word"] == 0
