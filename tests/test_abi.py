@@ -41,6 +41,9 @@ def test_argument_errors_need_no_device():
     assert L.spec_verify_init(None, 1, 1, 8, sv.SV_F32, 0, 0) == sv.SV_EINVAL
     assert L.spec_verify_init(ctypes.byref(ctx), 0, 1, 8, sv.SV_F32, 0, 0) == sv.SV_EINVAL
     assert L.spec_verify_init(ctypes.byref(ctx), 4, 1, 8, 7, 0, 0) == sv.SV_EDTYPE
+    # argmax candidates hold twice an index in an int: vocabularies from 2^30 on are refused
+    assert L.spec_verify_init(ctypes.byref(ctx), 1, 0, 1 << 30, sv.SV_F32, 0, 0) == sv.SV_ECAPACITY
+    assert ctx.value is None
     assert L.spec_verify_run(None, *([None] * 6), 0, 0, 1, 0, 0, None, None, None, None, None,
                              None, None) == sv.SV_EINVAL
     rc = L.spec_verify_init(ctypes.byref(ctx), 4, 3, 1024, sv.SV_F32, 1, 0)
