@@ -4,7 +4,7 @@ Token ids and accept lengths must match bit for bit. The only exception is a req
 outputs differ after a decision the oracle calls too close to call: an acceptance test with
 |u - p/q| < 1e-6 at a position both sides evaluated, or a residual race whose two best keys
 are closer than 1e-6 (the residual depends on the row's sum of exponentials S, which the two
-sides accumulate in different orders), or a top-p boundary within 1e-4 of the total mass at a
+sides accumulate in different orders), or a top-p boundary within 1e-6 of the total mass at a
 row both sides used (the kept mass is summed in binary32 on the GPU). Such a request is a
 counted tie and the rest of it is not compared. The row statistics must match: m and the
 argmax exactly, S (the kept mass under top-k / top-p) to 1e-5 relative, except at rows whose
@@ -15,7 +15,7 @@ from __future__ import annotations
 import numpy as np
 
 TIE_MARGIN = 1e-6
-SEL_MARGIN = 1e-4
+SEL_MARGIN = 1e-6
 S_RTOL = 1e-5
 RACE_NONE = 0
 
