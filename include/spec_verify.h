@@ -402,9 +402,10 @@ int spec_verify_set_profiling(spec_verify_ctx *ctx, int enable);
 int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls);
 
 /* Launch-shape knob: elements per CTA of the statistics kernel (0 keeps the current value; -1
- * restores the default, automatic: the flattened logits split evenly over a grid sized in whole
- * waves of CTAs). Values are rounded up to a multiple of 8 and kept at or above 2048. Results do
- * not depend on it (S, a sum, up to rounding). */
+ * restores the default, automatic: the flattened logits split evenly over the fewest whole waves
+ * of CTAs whose chunk is at most 2^19 elements, one wave when that fits). Values are rounded up
+ * to a multiple of 512 and kept between 2048 and 2^19. Results do not depend on it (S, a sum, up
+ * to rounding). */
 int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk);
 
 /* Number of kernel launches one call makes for a non-empty batch without top_k / top_p (one

@@ -49,7 +49,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMinChunk = 2048;     // smallest elements per statistics CTA (bounds the partials)
 constexpr int kChunkAlign = 512;    // statistics chunks: whole 16-byte spans of the line array
 constexpr int kMaxChunk = 1 << 19;  // largest: its line maxima fit in 32 KB of shared memory
-constexpr int kStatsWaves = 2;      // automatic statistics grid: this many full waves of CTAs
 constexpr int kFixedChunk = 32768;  // statistics chunk of the static-scratch entry point
 constexpr int kGroup = 64;          // tokens per race-clock group = elements per line
 constexpr float kLog2e = 0x1.715476p+0f;
@@ -3173,7 +3172,8 @@ struct spec_verify_ctx {
     float syn[SV_MAX_SYNTHETIC] = {};
     int max_rows = 0, maxseg = 0;
     int stats_chunk = 0;   // 0: automatic (even split over whole waves)
-    int stats_ctas = 1;    // one wave of the statistics kernel (SMs x CTAs per SM)
+    int stats_ctas = 1;      // one wave of the statistics kernel (SMs x CTAs per SM)
+    int stats_ctas_pen = 1;  // one wave of its frequency-penalty instantiation
     StatPart *statpart = nullptr;
     StatPart *dpart = nullptr;  // partials of the draft rows (draft-logits mode)
     float *sel_tau = nullptr;   // [max_rows] top-k / top-p threshold per row
@@ -3196,12 +3196,23 @@ struct spec_verify_ctx {
 
 namespace {
 
-long long stats_chunk_for(const spec_verify_ctx *ctx, long long all)
+long long stats_chunk_for(const spec_verify_ctx *ctx, long long all, bool pen)
 {
+    const long long wave = pen ? ctx->stats_ctas_pen : ctx->stats_ctas;
+    auto aligned = [](long long c) {
+        return std::max<long long>((c + kChunkAlign - 1) / kChunkAlign * kChunkAlign, kMinChunk);
+    };
     long long chunk = ctx->stats_chunk;
-    if (chunk <= 0) chunk = (all + kStatsWaves * ctx->stats_ctas - 1) / (kStatsWaves * ctx->stats_ctas);
-    return std::min<long long>(std::max<long long>((chunk + kChunkAlign - 1) / kChunkAlign * kChunkAlign,
-                                                   kMinChunk), kMaxChunk);
+    if (chunk <= 0) {
+        // automatic: an even split over the fewest whole waves of CTAs whose chunk fits, one wave
+        // when it can (measured faster than two on the bench workload: each CTA then runs one
+        // long stream, and no second wave starts behind the first)
+        for (long long waves = 1;; ++waves) {
+            chunk = aligned((all + waves * wave - 1) / (waves * wave));
+            if (chunk <= kMaxChunk) break;
+        }
+    }
+    return std::min<long long>(aligned(chunk), kMaxChunk);
 }
 
 struct DeviceGuard {
@@ -3274,7 +3285,7 @@ size_t verify_smem_limit(int device)
 // Allow the verify kernel the device's opt-in shared memory and report how many statistics
 // CTAs fit on one SM (for the whole-wave grid).
 template <typename T>
-cudaError_t setup_kernels(int device, int *stats_per_sm)
+cudaError_t setup_kernels(int device, int *stats_per_sm, int *stats_pen_per_sm)
 {
     const int limit = static_cast<int>(verify_smem_limit(device));
     // select: its fixed part and one row's line maxima; as much as a verify CTA may use
@@ -3294,13 +3305,17 @@ cudaError_t setup_kernels(int device, int *stats_per_sm)
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, limit);
     if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_pen_per_sm, sv_stats_kernel<T, true>,
+                                                      kThreads, 0);
+    if (e != cudaSuccess) return e;
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(stats_per_sm, sv_stats_kernel<T, false>,
                                                          kThreads, 0);
 }
 
-// Statistics chunk for an array of `total` elements: the context's, or an even split over
-// kStatsWaves waves of the CTAs (shared with any other array of the same launch).
-long long stats_chunk_for(const spec_verify_ctx *ctx, long long all);
+// Statistics chunk for an array of `total` elements: the context's, or an even split over the
+// fewest whole waves of CTAs that keeps a chunk within kMaxChunk (shared with any other array of
+// the same launch).
+long long stats_chunk_for(const spec_verify_ctx *ctx, long long all, bool pen);
 
 template <typename T>
 StatsArray<T> stats_array(const T *logits, long long total, long long chunk, int V, int draft_rows,
@@ -3376,7 +3391,7 @@ int launch_all(spec_verify_ctx *ctx, const spec_verify_batch &b, const spec_veri
     // statistics: the flattened [rows x V] logits (and [nd x V] draft logits) split evenly
     const long long total = static_cast<long long>(rows) * V;
     const long long total_d = dl ? static_cast<long long>(nd) * V : 0;
-    const long long chunk1 = stats_chunk_for(ctx, total + total_d);
+    const long long chunk1 = stats_chunk_for(ctx, total + total_d, b.frequency_penalty != nullptr);
     const RequestTable rq{cu, b.temperature, b.is_greedy, b.top_k, num_reqs};
     const int mask_stride = ceil_div(V, 32) + 1;
     const PenTable pen{b.frequency_penalty, b.output_bin_counts, b.counts_row, b.counts_rows, nd,
@@ -3635,9 +3650,10 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
     ok = ok && (!ctx->has_dl || D == 0 ||
                 cudaMalloc(&ctx->dpart, D * S * kWarps * sizeof(StatPart)) == cudaSuccess);
     ok = ok && cudaMemset(ctx->flags, 0, 2 * sizeof(unsigned)) == cudaSuccess;
-    int stats_per_sm = 0;
-    ok = ok && (logits_dtype == SV_BF16 ? setup_kernels<uint16_t>(device, &stats_per_sm)
-                                        : setup_kernels<float>(device, &stats_per_sm)) == cudaSuccess;
+    int stats_per_sm = 0, stats_pen_per_sm = 0;
+    ok = ok && (logits_dtype == SV_BF16 ? setup_kernels<uint16_t>(device, &stats_per_sm, &stats_pen_per_sm)
+                                        : setup_kernels<float>(device, &stats_per_sm, &stats_pen_per_sm)) ==
+                   cudaSuccess;
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_all(ctx);
@@ -3646,6 +3662,7 @@ int spec_verify_init(spec_verify_ctx **out, int max_num_reqs, int max_spec_len, 
         return SV_ECUDA;
     }
     ctx->stats_ctas = std::max(stats_per_sm, 1) * prop.multiProcessorCount;
+    ctx->stats_ctas_pen = std::max(stats_pen_per_sm, 1) * prop.multiProcessorCount;
     *out = ctx;
     return SV_OK;
 }
@@ -3722,7 +3739,7 @@ int spec_verify_shard_stats(spec_verify_ctx *ctx, const void *logits_shard, int 
     const int Vs = ctx->V, R = num_draft_tokens + num_reqs;
     const RequestTable rq{cu_num_draft, temperature, is_greedy, nullptr, num_reqs};
     const long long total = static_cast<long long>(R) * Vs;
-    const long long chunk1 = stats_chunk_for(ctx, total);
+    const long long chunk1 = stats_chunk_for(ctx, total, false);
 #ifdef SV_DEBUG_BOUNDS
     {
         const size_t n = static_cast<size_t>(num_reqs), Rz = static_cast<size_t>(R);
@@ -4109,7 +4126,8 @@ int noalloc_device(int dev, NoAllocDevice *out)
             return SV_ECUDA;
         }
         int a = 0;
-        if (setup_kernels<uint16_t>(dev, &a) != cudaSuccess || setup_kernels<float>(dev, &a) != cudaSuccess) {
+        int b = 0;
+        if (setup_kernels<uint16_t>(dev, &a, &b) != cudaSuccess || setup_kernels<float>(dev, &a, &b) != cudaSuccess) {
             cudaGetLastError();
             return SV_ECUDA;
         }
