@@ -548,10 +548,11 @@ def run_ours(args, world, rank, local):
     else:
         achieved = stats_bytes / (kavg["stats"] / 1e3) / 1e9
     plain = not extras and b.synthetic_rates is None and not sharded and not b.fp64_gumbel
-    # our kernels per step: statistics + verify (+ the top-k / top-p selection); sharded: each
-    # shard's statistics, export and race, and one finish
+    # our kernels per step: statistics + verify (+ the top-k / top-p selection, + the penalty's
+    # counts-mask pass); sharded: each shard's statistics, export and race, and one finish
     launches_per_step = (3 * len(sides) + 1 if sharded else
-                         sv.spec_verify_launches_per_run() + int(b.top_k is not None or b.top_p is not None))
+                         sv.spec_verify_launches_per_run() + int(b.top_k is not None or b.top_p is not None)
+                         + int(b.frequency_penalty is not None))
     traffic, traffic_src = (recorded_traffic("stats_kernel_workload3_draft_logits.md" if d_dl is not None
                                              else "stats_kernel_workload3.md")
                             if plain and args.workload == 3 else (None, "no ncu summary for this mode"))

@@ -408,8 +408,9 @@ int spec_verify_get_profile(spec_verify_ctx *ctx, double *ms, int64_t *calls);
  * to rounding). */
 int spec_verify_set_chunks(spec_verify_ctx *ctx, int stats_chunk);
 
-/* Number of kernel launches one call makes for a non-empty batch without top_k / top_p (one
- * more, the selection kernel, with them). */
+/* Number of kernel launches one call makes for a non-empty batch without top_k / top_p and
+ * without a frequency penalty (one more, the selection kernel, with top_k / top_p; one more, the
+ * counts-mask pass, with a penalty). */
 int spec_verify_launches_per_run(void);
 
 /*
